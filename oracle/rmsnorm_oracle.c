@@ -1,0 +1,361 @@
+/*
+ * rmsnorm_oracle.c -- CPU oracle for RMSNorm forward and backward (fp64).
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the CPU-baseline
+ * legs of the benchmark load this library. The CUDA library never links it,
+ * and it shares no code, header or table with the CUDA kernels.
+ *
+ * What it computes (plain definition, one row at a time, every step in
+ * double; inputs are decoded exactly from their storage type):
+ *
+ *   forward   h_j   = x_j                      plain
+ *             h_j   = R(x_j + r_j)             fused residual add (exact double
+ *                                              sum, one rounding to storage type)
+ *             ms    = (1/N) sum_j h_j^2
+ *             rstd  = 1 / sqrt(ms + eps)
+ *             y_j   = h_j * rstd * (offset + w_j)
+ *
+ *   backward  xhat_j = h_j * rstd
+ *             g_j    = dy_j * (offset + w_j)
+ *             c      = (1/N) sum_j g_j * xhat_j
+ *             dx_j   = rstd * (g_j - xhat_j * c)   [+ dres_j in the fused variant]
+ *             dW_j   = sum_rows dy_j * xhat_j
+ *
+ * Sources: "perf(cutedsl): add Blackwell fast path to RMSNorm" (Liger-Kernel
+ * PR #1388, Summary and section 2: llama-mode RMSNorm, offset as a runtime
+ * scalar, fused backward producing dX and dW) and "[Perf] Optimize RMSNorm
+ * backward with staged reduction and vec8 I/O" (ROCm/FlyDSL PR #855,
+ * Implementation: plain and fused-add backward, dx == dresidual, dweight
+ * written in the parameter dtype, round-to-nearest-even bf16 stores).
+ * The pages print no formula; the one above is the definition of RMSNorm
+ * with weight (offset + w) and its exact gradient:
+ *   d rstd / d h_k = -rstd^3 h_k / N, hence
+ *   dL/dh_k = rstd g_k - (rstd^3 h_k / N) sum_j g_j h_j = rstd (g_k - xhat_k c).
+ *
+ * R() is round-to-nearest-even to the storage type: bf16 is rounded from
+ * the double value in ONE step (no detour through binary32); fp32 by the C
+ * cast. f64 "storage" (dtype 2) means no rounding at all; the pins use it
+ * for finite differences.
+ *
+ * Parity pins live in tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F64 = 2 };
+
+/* ---------------------------------------------------------------- bf16 -- */
+
+/* bf16 is the upper half of an IEEE binary32, so decoding is exact. */
+double oracle_bf16_decode(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Round a double to bf16, nearest with ties to even, in a single step.
+ * bf16: 1 sign bit, 8 exponent bits (bias 127), 7 stored fraction bits.
+ * Returns 0 when the result is an ordinary finite value (normal, subnormal
+ * or zero), 1 when v is NaN or the rounded value overflows to infinity.
+ */
+int oracle_bf16_round(double v, uint16_t *out)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v);
+    if (isnan(v)) { *out = 0x7fc0u; return 1; }
+    if (isinf(v)) { *out = (uint16_t)(sign | 0x7f80u); return 1; }
+    if (a == 0.0) { *out = sign; return 0; }
+
+    const double min_normal = ldexp(1.0, -126);
+    if (a < min_normal) {
+        /* Subnormal range: the quantum is 2^-133. rint() rounds to nearest,
+         * ties to even, in the default rounding mode. A result of 128 is
+         * the smallest normal, whose encoding is also 128 (0x0080). */
+        double q = rint(ldexp(a, 133));
+        *out = (uint16_t)(sign | (uint16_t)q);
+        return 0;
+    }
+    int e;
+    double m = frexp(a, &e);          /* a = m * 2^e, 0.5 <= m < 1 */
+    double q = rint(ldexp(m, 8));     /* 8 significant bits: 128..256 */
+    if (q == 256.0) { q = 128.0; e += 1; }
+    /* value = q * 2^(e-8) with 128 <= q <= 255; biased exponent of the
+     * leading bit is (e - 1) + 127. */
+    int be = e - 1 + 127;
+    if (be >= 255) { *out = (uint16_t)(sign | 0x7f80u); return 1; }
+    uint16_t frac = (uint16_t)((int)q - 128);
+    *out = (uint16_t)(sign | (uint16_t)(be << 7) | frac);
+    return 0;
+}
+
+/* ------------------------------------------------------- storage access -- */
+
+static double load_elem(int dtype, const void *p, int64_t i)
+{
+    switch (dtype) {
+    case OR_BF16: return oracle_bf16_decode(((const uint16_t *)p)[i]);
+    case OR_F32:  return (double)((const float *)p)[i];
+    default:      return ((const double *)p)[i];
+    }
+}
+
+/* Stores R(v); returns 1 if the rounding overflowed or v was not finite. */
+static int store_elem(int dtype, void *p, int64_t i, double v)
+{
+    switch (dtype) {
+    case OR_BF16: {
+        uint16_t b;
+        int bad = oracle_bf16_round(v, &b);
+        ((uint16_t *)p)[i] = b;
+        return bad;
+    }
+    case OR_F32: {
+        float f = (float)v;
+        ((float *)p)[i] = f;
+        return !isfinite(f);
+    }
+    default:
+        ((double *)p)[i] = v;
+        return !isfinite(v);
+    }
+}
+
+/* R(v) as a double: the value a store of v would hold. */
+static double round_to(int dtype, double v)
+{
+    switch (dtype) {
+    case OR_BF16: {
+        uint16_t b;
+        oracle_bf16_round(v, &b);
+        return oracle_bf16_decode(b);
+    }
+    case OR_F32: return (double)(float)v;
+    default:     return v;
+    }
+}
+
+/* ------------------------------------------------------------- forward -- */
+
+typedef struct {
+    int dtype;
+    int64_t row0, row1, N;
+    const void *x, *residual, *w;
+    double eps, offset;
+    void *y;            /* storage type, may be NULL */
+    double *y64;        /* unrounded y, may be NULL */
+    void *h_out;        /* storage type (fused: residual_out), may be NULL */
+    double *rstd64;     /* may be NULL */
+    float *rstd32;      /* may be NULL */
+    int bad;
+} fwd_job;
+
+static void fwd_rows(fwd_job *jb)
+{
+    const int64_t N = jb->N;
+    double *h = (double *)malloc((size_t)N * sizeof(double));
+    for (int64_t i = jb->row0; i < jb->row1; ++i) {
+        const int64_t base = i * N;
+        /* h: the row that is normalised */
+        for (int64_t j = 0; j < N; ++j) {
+            double xv = load_elem(jb->dtype, jb->x, base + j);
+            if (jb->residual)
+                h[j] = round_to(jb->dtype, xv + load_elem(jb->dtype, jb->residual, base + j));
+            else
+                h[j] = xv;
+        }
+        double ss = 0.0;
+        for (int64_t j = 0; j < N; ++j) ss += h[j] * h[j];
+        const double ms = ss / (double)N;
+        const double rstd = 1.0 / sqrt(ms + jb->eps);
+        for (int64_t j = 0; j < N; ++j) {
+            const double wj = load_elem(jb->dtype, jb->w, j);
+            const double yj = h[j] * rstd * (jb->offset + wj);
+            if (jb->y64) jb->y64[base + j] = yj;
+            if (jb->y) jb->bad |= store_elem(jb->dtype, jb->y, base + j, yj);
+            if (jb->h_out) jb->bad |= store_elem(jb->dtype, jb->h_out, base + j, h[j]);
+        }
+        if (jb->rstd64) jb->rstd64[i] = rstd;
+        if (jb->rstd32) jb->rstd32[i] = (float)rstd;
+    }
+    free(h);
+}
+
+static void *fwd_thread(void *arg) { fwd_rows((fwd_job *)arg); return NULL; }
+
+/*
+ * Forward over an M x N row-major block. residual == NULL gives plain
+ * RMSNorm; otherwise h = R(x + residual) is normalised and, if h_out is
+ * given, stored there (the fused variant's residual_out). Rows are split
+ * into contiguous ranges over nthreads threads (rows are independent, so
+ * the thread count does not change any result).
+ * Returns the number of non-finite or overflowing stores (0 expected).
+ */
+int oracle_rmsnorm_fwd(int dtype, int64_t M, int64_t N,
+                       const void *x, const void *residual, const void *w,
+                       double eps, double offset,
+                       void *y, double *y64, void *h_out,
+                       double *rstd64, float *rstd32, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
+    fwd_job *jobs = (fwd_job *)calloc((size_t)nthreads, sizeof(fwd_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    for (int t = 0; t < nthreads; ++t) {
+        fwd_job *jb = &jobs[t];
+        jb->dtype = dtype; jb->N = N;
+        jb->row0 = M * t / nthreads; jb->row1 = M * (t + 1) / nthreads;
+        jb->x = x; jb->residual = residual; jb->w = w;
+        jb->eps = eps; jb->offset = offset;
+        jb->y = y; jb->y64 = y64; jb->h_out = h_out;
+        jb->rstd64 = rstd64; jb->rstd32 = rstd32;
+    }
+    if (nthreads == 1) {
+        fwd_rows(&jobs[0]);
+    } else {
+        for (int t = 0; t < nthreads; ++t) pthread_create(&tid[t], NULL, fwd_thread, &jobs[t]);
+        for (int t = 0; t < nthreads; ++t) pthread_join(tid[t], NULL);
+    }
+    int bad = 0;
+    for (int t = 0; t < nthreads; ++t) bad += jobs[t].bad;
+    free(jobs); free(tid);
+    return bad;
+}
+
+/* ------------------------------------------------------------ backward -- */
+
+typedef struct {
+    int dtype;
+    int64_t row0, row1, N;
+    const void *dy, *h, *w, *dres;
+    const float *rstd_in;
+    double eps, offset;
+    void *dx;
+    double *dx64, *dx_scale;
+    double *dw, *dw_abs;   /* this job's own partial sums, length N */
+    int bad;
+} bwd_job;
+
+static void bwd_rows(bwd_job *jb)
+{
+    const int64_t N = jb->N;
+    double *hv = (double *)malloc((size_t)N * sizeof(double));
+    double *wpo = (double *)malloc((size_t)N * sizeof(double));
+    for (int64_t j = 0; j < N; ++j) wpo[j] = jb->offset + load_elem(jb->dtype, jb->w, j);
+    for (int64_t i = jb->row0; i < jb->row1; ++i) {
+        const int64_t base = i * N;
+        for (int64_t j = 0; j < N; ++j) hv[j] = load_elem(jb->dtype, jb->h, base + j);
+        double rstd;
+        if (jb->rstd_in) {
+            rstd = (double)jb->rstd_in[i];
+        } else {
+            double ss = 0.0;
+            for (int64_t j = 0; j < N; ++j) ss += hv[j] * hv[j];
+            rstd = 1.0 / sqrt(ss / (double)N + jb->eps);
+        }
+        /* c = (1/N) sum_j g_j xhat_j */
+        double c = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            const double g = load_elem(jb->dtype, jb->dy, base + j) * wpo[j];
+            c += g * (hv[j] * rstd);
+        }
+        c /= (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            const double dyj = load_elem(jb->dtype, jb->dy, base + j);
+            const double xhat = hv[j] * rstd;
+            const double g = dyj * wpo[j];
+            double dxj = rstd * (g - xhat * c);
+            double scale = rstd * (fabs(g) + fabs(xhat * c));
+            if (jb->dres) {
+                const double d = load_elem(jb->dtype, jb->dres, base + j);
+                dxj += d;
+                scale += fabs(d);
+            }
+            if (jb->dx64) jb->dx64[base + j] = dxj;
+            if (jb->dx_scale) jb->dx_scale[base + j] = scale;
+            if (jb->dx) jb->bad |= store_elem(jb->dtype, jb->dx, base + j, dxj);
+            jb->dw[j] += dyj * xhat;
+            jb->dw_abs[j] += fabs(dyj * xhat);
+        }
+    }
+    free(hv);
+    free(wpo);
+}
+
+static void *bwd_thread(void *arg) { bwd_rows((bwd_job *)arg); return NULL; }
+
+/*
+ * Backward over an M x N block.
+ *   h        the normalised input (x for plain RMSNorm, residual_out of the
+ *            fused forward)
+ *   rstd_in  NULL: rstd is recomputed in double from h (the exact gradient);
+ *            otherwise the given fp32 values are used.
+ *   dres     NULL or the incoming residual-stream gradient (fused variant)
+ * Outputs (each may be NULL except dw64):
+ *   dx       R(dx) in the storage type
+ *   dx64     unrounded dx
+ *   dx_scale rstd (|g| + |xhat c|) [+ |dres|]: the magnitude of the terms
+ *            whose difference is dx, used to bound cancellation error
+ *   dw64     sum over rows of dy * xhat (length N)
+ *   dw_abs   sum over rows of |dy * xhat| (length N)
+ *   dw       R(dw64) in the storage type
+ * Rows are split into nthreads contiguous ranges; each range keeps its own
+ * dW partial and the partials are added in range order.
+ * Returns the number of non-finite or overflowing stores.
+ */
+int oracle_rmsnorm_bwd(int dtype, int64_t M, int64_t N,
+                       const void *dy, const void *h, const void *w,
+                       const float *rstd_in, const void *dres,
+                       double eps, double offset,
+                       void *dx, double *dx64, double *dx_scale,
+                       double *dw64, double *dw_abs, void *dw, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
+    bwd_job *jobs = (bwd_job *)calloc((size_t)nthreads, sizeof(bwd_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    for (int t = 0; t < nthreads; ++t) {
+        bwd_job *jb = &jobs[t];
+        jb->dtype = dtype; jb->N = N;
+        jb->row0 = M * t / nthreads; jb->row1 = M * (t + 1) / nthreads;
+        jb->dy = dy; jb->h = h; jb->w = w; jb->dres = dres; jb->rstd_in = rstd_in;
+        jb->eps = eps; jb->offset = offset;
+        jb->dx = dx; jb->dx64 = dx64; jb->dx_scale = dx_scale;
+        jb->dw = (double *)calloc((size_t)N, sizeof(double));
+        jb->dw_abs = (double *)calloc((size_t)N, sizeof(double));
+    }
+    if (nthreads == 1) {
+        bwd_rows(&jobs[0]);
+    } else {
+        for (int t = 0; t < nthreads; ++t) pthread_create(&tid[t], NULL, bwd_thread, &jobs[t]);
+        for (int t = 0; t < nthreads; ++t) pthread_join(tid[t], NULL);
+    }
+    int bad = 0;
+    for (int64_t j = 0; j < N; ++j) {
+        double s = 0.0, sa = 0.0;
+        for (int t = 0; t < nthreads; ++t) { s += jobs[t].dw[j]; sa += jobs[t].dw_abs[j]; }
+        dw64[j] = s;
+        if (dw_abs) dw_abs[j] = sa;
+        if (dw) bad |= store_elem(dtype, dw, j, s);
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        bad += jobs[t].bad;
+        free(jobs[t].dw);
+        free(jobs[t].dw_abs);
+    }
+    free(jobs); free(tid);
+    return bad;
+}
+
+/* Round an array of doubles to bf16 (for the tests of the rounding rule). */
+int oracle_bf16_round_array(const double *v, int64_t n, uint16_t *out)
+{
+    int bad = 0;
+    for (int64_t i = 0; i < n; ++i) bad += oracle_bf16_round(v[i], &out[i]);
+    return bad;
+}

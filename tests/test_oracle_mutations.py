@@ -1,0 +1,51 @@
+"""Mutation check of the oracle pins.
+
+Each case plants one plausible mistake in a copy of the oracle's C source,
+builds it on the CPU, and runs the pin suite against it; the suite must go
+red. This shows the pins constrain every term of the definition rather than
+re-deriving the oracle from itself.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "rmsnorm_oracle.c")
+
+MUTATIONS = {
+    "sum_instead_of_mean": ("const double ms = ss / (double)N;", "const double ms = ss;"),
+    "eps_outside_root": ("1.0 / sqrt(ms + jb->eps)", "1.0 / (sqrt(ms) + jb->eps)"),
+    "offset_dropped_fwd": ("h[j] * rstd * (jb->offset + wj)", "h[j] * rstd * wj"),
+    "w_index_reversed": ("load_elem(jb->dtype, jb->w, j);\n            const double yj",
+                         "load_elem(jb->dtype, jb->w, N - 1 - j);\n            const double yj"),
+    "bwd_sign_flip": ("rstd * (g - xhat * c)", "rstd * (g + xhat * c)"),
+    "bwd_c_not_mean": ("c /= (double)N;", "c /= 1.0;"),
+    "bwd_offset_dropped": ("wpo[j] = jb->offset + load_elem", "wpo[j] = 0.0 * jb->offset + load_elem"),
+    "dw_uses_g": ("jb->dw[j] += dyj * xhat;", "jb->dw[j] += g * xhat;"),
+    "dw_missing_rstd": ("jb->dw[j] += dyj * xhat;", "jb->dw[j] += dyj * hv[j];"),
+    "dres_dropped": ("dxj += d;", "dxj += 0.0 * d;"),
+    "fused_h_unrounded": ("h[j] = round_to(jb->dtype, xv + load_elem(jb->dtype, jb->residual, base + j));",
+                          "h[j] = xv + load_elem(jb->dtype, jb->residual, base + j);"),
+    "bf16_via_binary32": ("uint16_t sign = signbit(v) ? 0x8000u : 0u;",
+                          "v = (double)(float)v;\n    uint16_t sign = signbit(v) ? 0x8000u : 0u;"),
+    "bf16_ties_away": ("double q = rint(ldexp(m, 8));", "double q = round(ldexp(m, 8));"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=gnu99", "-fPIC", "-shared", "-ffp-contract=off",
+                           "-o", str(lib), str(mutated), "-lm", "-lpthread"])
+    env = dict(os.environ, RMSNORM_ORACLE_LIB_OVERRIDE=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch mutation {name}:\n{r.stdout[-2000:]}"

@@ -1,0 +1,313 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Every check here holds by mathematics: closed forms of special rows, exact
+invariances, the finite-difference gradient of the forward, hand-derived
+values, and the IEEE rounding rule for bf16 checked exhaustively and
+against an independent implementation. A plausible slip in the oracle (a
+sum instead of a mean, eps outside the square root, a dropped or sign-flipped
+term of the gradient, a transposed w index, rounding through binary32)
+fails at least one of these.
+
+The RMSNorm definitions follow the Liger-Kernel page "perf(cutedsl): add
+Blackwell fast path to RMSNorm" (llama mode, runtime offset) and the FlyDSL
+page "[Perf] Optimize RMSNorm backward with staged reduction and vec8 I/O"
+(fused-add backward: dx also serves as dresidual).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from row_wise_normalization_rmsnorm_gb300 import inputs
+
+
+def f64(shape, seed, scale=1.0, loc=0.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale + loc
+
+
+# ----------------------------------------------------------------- bf16 --
+
+def test_bf16_decode_round_identity_exhaustive():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    exp = (bits >> 7) & 0xFF
+    frac = bits & 0x7F
+    finite = ~((exp == 0xFF) & (frac != 0))          # drop NaNs
+    b = bits[finite]
+    assert np.array_equal(oracle.bf16_round(oracle.bf16_decode(b)), b)
+
+
+def test_bf16_round_ties_to_even_and_neighbours():
+    # every pair of adjacent positive finite bf16 values, normal and subnormal
+    lo = np.arange(0, 0x7F7F, dtype=np.uint16)
+    a = oracle.bf16_decode(lo)
+    b = oracle.bf16_decode(lo + 1)
+    mid = (a + b) / 2.0                               # exact in double
+    got = oracle.bf16_round(mid)
+    even = np.where((lo & 1) == 0, lo, lo + 1).astype(np.uint16)
+    assert np.array_equal(got, even)
+    below = np.nextafter(mid, -np.inf)
+    above = np.nextafter(mid, np.inf)
+    assert np.array_equal(oracle.bf16_round(below), lo)
+    assert np.array_equal(oracle.bf16_round(above), (lo + 1).astype(np.uint16))
+    # sign symmetry
+    assert np.array_equal(oracle.bf16_round(-mid), even | np.uint16(0x8000))
+
+
+def test_bf16_round_matches_torch_on_float32_values():
+    # For values that are exact binary32 numbers, one-step rounding from
+    # double equals torch's binary32 -> bf16 conversion (nearest, ties even).
+    v = np.random.default_rng(7).standard_normal(200_000).astype(np.float32)
+    v[:1000] *= np.float32(1e-30)
+    v[1000:2000] *= np.float32(1e30)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.bf16_round(v.astype(np.float64)), ref)
+
+
+def test_bf16_round_is_single_step():
+    # 1 + 2^-8 is the midpoint between bf16 1.0 and 1.0078125; a hair above it
+    # must round up. Going through binary32 first would land exactly on the
+    # midpoint and then round down to the even neighbour 1.0.
+    v = 1.0 + 2.0 ** -8 + 2.0 ** -30
+    assert float(np.float32(v)) == 1.0 + 2.0 ** -8
+    assert oracle.bf16_round(np.array([v]))[0] == 0x3F81
+    assert oracle.bf16_round(np.array([1.0 + 2.0 ** -8]))[0] == 0x3F80
+
+
+# ------------------------------------------------------------- forward --
+
+def test_fwd_hand_example():
+    # x = (3, 4): mean(x^2) = 12.5, rstd = 1/sqrt(12.5) = sqrt(2)/5.
+    x = np.array([[3.0, 4.0]])
+    w = np.array([1.0, 2.0])
+    r = oracle.fwd(x, w, dtype="f64", eps=0.0, offset=0.0)
+    s2 = math.sqrt(2.0)
+    assert r["rstd64"][0] == pytest.approx(s2 / 5, rel=1e-15)
+    assert r["y64"][0] == pytest.approx([3 * s2 / 5, 8 * s2 / 5], rel=1e-15)
+    # with eps = 0.5 inside the root: mean + eps = 13
+    r = oracle.fwd(x, w, dtype="f64", eps=0.5, offset=1.0)
+    assert r["rstd64"][0] == pytest.approx(1 / math.sqrt(13.0), rel=1e-15)
+    assert r["y64"][0] == pytest.approx([3 * 2 / math.sqrt(13), 4 * 3 / math.sqrt(13)], rel=1e-15)
+
+
+@pytest.mark.parametrize("a", [0.75, -3.5, 1e-3])
+@pytest.mark.parametrize("offset", [0.0, 1.0])
+def test_fwd_constant_row_eps0(a, offset):
+    N = 37
+    w = f64(N, 1, 0.1, 1.0)
+    x = np.full((2, N), a)
+    r = oracle.fwd(x, w, dtype="f64", eps=0.0, offset=offset)
+    np.testing.assert_allclose(r["y64"], np.sign(a) * (offset + w)[None, :].repeat(2, 0), rtol=1e-15)
+    np.testing.assert_allclose(r["rstd64"], 1 / abs(a), rtol=1e-15)
+
+
+def test_fwd_zero_row_eps_positive():
+    eps = 0.01
+    r = oracle.fwd(np.zeros((1, 16)), f64(16, 2), dtype="f64", eps=eps, offset=0.0)
+    assert r["rstd64"][0] == pytest.approx(10.0, rel=1e-15)   # eps^-1/2
+    assert np.all(r["y64"] == 0.0)
+
+
+@pytest.mark.parametrize("k", [-3, 5])
+def test_fwd_scale_invariance_eps0(k):
+    x = f64((4, 50), 3)
+    w = f64(50, 4, 0.1, 1.0)
+    r1 = oracle.fwd(x, w, dtype="f64", eps=0.0, offset=0.0)
+    r2 = oracle.fwd(x * 2.0 ** k, w, dtype="f64", eps=0.0, offset=0.0)
+    assert np.array_equal(r1["y64"], r2["y64"])
+    assert np.array_equal(r2["rstd64"], r1["rstd64"] * 2.0 ** -k)
+
+
+@pytest.mark.parametrize("eps", [0.0, 0.3])
+def test_fwd_norm_identity(eps):
+    # sum_j (y_j / (o + w_j))^2 = N ms / (ms + eps): the mean, with eps under the root
+    N = 64
+    x = f64((5, N), 5)
+    w = f64(N, 6, 0.1, 1.0)
+    r = oracle.fwd(x, w, dtype="f64", eps=eps, offset=0.5)
+    ms = np.mean(x * x, axis=1)
+    lhs = np.sum((r["y64"] / (0.5 + w)) ** 2, axis=1)
+    np.testing.assert_allclose(lhs, N * ms / (ms + eps), rtol=1e-13)
+
+
+def test_fwd_n1_special_case():
+    x = np.array([[0.5], [-2.0], [3.0]])
+    w = np.array([1.25])
+    eps = 0.2
+    r = oracle.fwd(x, w, dtype="f64", eps=eps, offset=1.0)
+    np.testing.assert_allclose(r["y64"][:, 0], x[:, 0] / np.sqrt(x[:, 0] ** 2 + eps) * 2.25, rtol=1e-15)
+
+
+def test_fwd_rows_independent_and_threads():
+    x = f64((33, 40), 8)
+    w = f64(40, 9, 0.1, 1.0)
+    full = oracle.fwd(x, w, dtype="f64", eps=1e-3, offset=0.0)
+    part = oracle.fwd(x[10:20], w, dtype="f64", eps=1e-3, offset=0.0)
+    thr = oracle.fwd(x, w, dtype="f64", eps=1e-3, offset=0.0, nthreads=4)
+    assert np.array_equal(full["y64"][10:20], part["y64"])
+    assert np.array_equal(full["y64"], thr["y64"])
+
+
+def test_fwd_storage_rounding_bf16_and_f32():
+    d = inputs.make_inputs(8, 96, "bf16", 11)
+    r = oracle.fwd(d["x"], d["w"], dtype="bf16", eps=1e-6, offset=0.0)
+    assert np.array_equal(r["y"], oracle.bf16_round(r["y64"]))
+    assert np.array_equal(r["rstd32"], r["rstd64"].astype(np.float32))
+    d = inputs.make_inputs(8, 96, "f32", 11)
+    r = oracle.fwd(d["x"], d["w"], dtype="f32", eps=1e-6, offset=0.0)
+    assert np.array_equal(r["y"], r["y64"].astype(np.float32))
+
+
+def test_fused_add_fwd_is_fwd_of_rounded_sum():
+    for dt in ("bf16", "f32"):
+        d = inputs.make_inputs(6, 72, dt, 12, residual=True)
+        r = oracle.fwd(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0, residual=d["residual"])
+        s = oracle.to_f64(d["x"], dt) + oracle.to_f64(d["residual"], dt)
+        h = oracle.bf16_round(s) if dt == "bf16" else s.astype(np.float32)
+        assert np.array_equal(r["h"], h)
+        p = oracle.fwd(h, d["w"], dtype=dt, eps=1e-6, offset=0.0)
+        assert np.array_equal(r["y"], p["y"]) and np.array_equal(r["rstd64"], p["rstd64"])
+
+
+# ------------------------------------------------------------ backward --
+
+def _bwd64(h, dy, w, eps, offset, dres=None):
+    return oracle.bwd(dy, h, w, dtype="f64", eps=eps, offset=offset, dres=dres)
+
+
+@pytest.mark.parametrize("offset", [0.0, 1.0])
+def test_bwd_orthogonality_eps0(offset):
+    # sum_j x_j dx_j = 0 when eps = 0, for any w and offset
+    x = f64((6, 45), 20)
+    dy = f64((6, 45), 21)
+    w = f64(45, 22, 0.3, 0.2)
+    r = _bwd64(x, dy, w, 0.0, offset)
+    dot = np.sum(x * r["dx64"], axis=1)
+    scale = np.sum(np.abs(x * r["dx64"]), axis=1)
+    assert np.all(np.abs(dot) <= 1e-13 * scale)
+
+
+def test_bwd_constant_row_eps0():
+    N = 30
+    x = np.full((3, N), -1.5)
+    dy = f64((3, N), 23)
+    w = f64(N, 24, 0.1, 1.0)
+    r = _bwd64(x, dy, w, 0.0, 0.0)
+    g = dy * w[None, :]
+    rstd = 1 / 1.5
+    np.testing.assert_allclose(r["dx64"], rstd * (g - g.mean(axis=1, keepdims=True)), rtol=1e-12, atol=1e-15)
+
+
+def test_bwd_zero_row_eps_positive():
+    dy = f64((1, 12), 25)
+    w = f64(12, 26, 0.1, 1.0)
+    r = _bwd64(np.zeros((1, 12)), dy, w, 0.04, 0.0)
+    np.testing.assert_allclose(r["dx64"][0], 5.0 * dy[0] * w, rtol=1e-15)
+    assert np.all(r["dw64"] == 0.0)
+
+
+@pytest.mark.parametrize("k", [-2, 3])
+def test_bwd_scaling_eps0(k):
+    x = f64((5, 33), 27)
+    dy = f64((5, 33), 28)
+    w = f64(33, 29, 0.1, 1.0)
+    r1 = _bwd64(x, dy, w, 0.0, 0.0)
+    r2 = _bwd64(x * 2.0 ** k, dy, w, 0.0, 0.0)
+    np.testing.assert_allclose(r2["dx64"], r1["dx64"] * 2.0 ** -k, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(r2["dw64"], r1["dw64"], rtol=1e-13, atol=1e-15)
+
+
+def test_bwd_n1_textbook_derivative():
+    # y = x (x^2+eps)^-1/2 (o+w): dy/dx = (o+w) eps / (x^2+eps)^(3/2)
+    x = np.array([[0.7], [-1.3], [2.0]])
+    dy = np.array([[1.0], [0.5], [-2.0]])
+    w = np.array([0.9])
+    eps = 0.3
+    r = _bwd64(x, dy, w, eps, 1.0)
+    want = dy[:, 0] * 1.9 * eps / (x[:, 0] ** 2 + eps) ** 1.5
+    np.testing.assert_allclose(r["dx64"][:, 0], want, rtol=1e-14)
+    np.testing.assert_allclose(r["dw64"][0], np.sum(dy[:, 0] * x[:, 0] / np.sqrt(x[:, 0] ** 2 + eps)), rtol=1e-14)
+
+
+def _loss(x, w, dy, eps, offset, residual=None, dres=None):
+    r = oracle.fwd(x, w, dtype="f64", eps=eps, offset=offset, residual=residual)
+    L = float(np.sum(r["y64"] * dy))
+    if dres is not None:
+        L += float(np.sum((x + residual) * dres))
+    return L
+
+
+@pytest.mark.parametrize("N", [1, 5, 8])
+@pytest.mark.parametrize("eps", [0.1, 1e-6])
+@pytest.mark.parametrize("offset", [0.0, 1.0])
+@pytest.mark.parametrize("fused", [False, True])
+def test_bwd_matches_finite_differences(N, eps, offset, fused):
+    """Central differences of L = sum y*dy (+ sum h*dres when fused) in x, w
+    and the residual agree with the oracle's dx and dW."""
+    M = 3
+    rng = np.random.default_rng(100 + N)
+    x = rng.standard_normal((M, N))
+    w = rng.standard_normal(N) * 0.1 + (0.0 if offset else 1.0)
+    dy = rng.standard_normal((M, N))
+    res = rng.standard_normal((M, N)) if fused else None
+    dres = rng.standard_normal((M, N)) if fused else None
+    h = x + res if fused else x
+    an = oracle.bwd(dy, h, w, dtype="f64", eps=eps, offset=offset, dres=dres)
+
+    def fd(fun, v, idx):
+        step = 1e-6 * max(1.0, abs(v[idx]))
+        vp = v.copy(); vp[idx] += step
+        vm = v.copy(); vm[idx] -= step
+        return (fun(vp) - fun(vm)) / (2 * step)
+
+    for idx in np.ndindex(M, N):
+        gx = fd(lambda v: _loss(v, w, dy, eps, offset, res, dres), x, idx)
+        tol = 1e-7 * max(abs(an["dx64"][idx]), an["dx_scale"][idx]) + 1e-9
+        assert abs(gx - an["dx64"][idx]) <= tol, (idx, gx, an["dx64"][idx])
+        if fused:
+            gr = fd(lambda v: _loss(x, w, dy, eps, offset, v, dres), res, idx)
+            assert abs(gr - an["dx64"][idx]) <= tol
+    for j in range(N):
+        gw = fd(lambda v: _loss(x, v, dy, eps, offset, res, dres), w, j)
+        tol = 1e-7 * max(abs(an["dw64"][j]), an["dw_abs"][j]) + 1e-9
+        assert abs(gw - an["dw64"][j]) <= tol, (j, gw, an["dw64"][j])
+
+
+def test_bwd_dw_order_independence_and_brute_force():
+    x = f64((40, 24), 30)
+    dy = f64((40, 24), 31)
+    w = f64(24, 32, 0.1, 1.0)
+    a = oracle.bwd(dy, x, w, dtype="f64", eps=1e-6, offset=0.0, nthreads=1)
+    b = oracle.bwd(dy, x, w, dtype="f64", eps=1e-6, offset=0.0, nthreads=5)
+    np.testing.assert_allclose(a["dw64"], b["dw64"], rtol=1e-12, atol=1e-14)
+    assert np.array_equal(a["dx64"], b["dx64"])
+    rstd = 1 / np.sqrt(np.mean(x * x, axis=1) + 1e-6)
+    brute = np.zeros(24)
+    for i in range(40):
+        for j in range(24):
+            brute[j] += dy[i, j] * x[i, j] * rstd[i]
+    np.testing.assert_allclose(a["dw64"], brute, rtol=1e-12, atol=1e-14)
+
+
+def test_bwd_given_rstd_and_dw_only_pass():
+    d = inputs.make_inputs(16, 64, "bf16", 33)
+    f = oracle.fwd(d["x"], d["w"], dtype="bf16", eps=1e-6, offset=0.0)
+    full = oracle.bwd(d["dy"], d["x"], d["w"], dtype="bf16", eps=1e-6, offset=0.0)
+    given = oracle.bwd(d["dy"], d["x"], d["w"], dtype="bf16", eps=1e-6, offset=0.0, rstd=f["rstd32"])
+    only = oracle.bwd(d["dy"], d["x"], d["w"], dtype="bf16", eps=1e-6, offset=0.0, want_dx=False)
+    assert np.array_equal(full["dw64"], only["dw64"])
+    # float32 rstd differs from the double one by <= 2^-24 relative; dx moves
+    # by a few times that relative to the size of its terms
+    assert np.all(np.abs(given["dx64"] - full["dx64"]) <= 1e-6 * full["dx_scale"])
+    assert np.array_equal(full["dx"], oracle.bf16_round(full["dx64"]))
+    assert np.array_equal(full["dw"], oracle.bf16_round(full["dw64"]))
+
+
+def test_fused_bwd_zero_dres_equals_plain_plus_nothing():
+    d = inputs.make_inputs(8, 48, "f32", 34, residual=True)
+    h = oracle.fwd(d["x"], d["w"], dtype="f32", eps=1e-6, offset=0.0, residual=d["residual"])["h"]
+    a = oracle.bwd(d["dy"], h, d["w"], dtype="f32", eps=1e-6, offset=0.0)
+    b = oracle.bwd(d["dy"], h, d["w"], dtype="f32", eps=1e-6, offset=0.0,
+                   dres=np.zeros_like(d["dy"]))
+    assert np.array_equal(a["dx64"], b["dx64"])
