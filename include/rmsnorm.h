@@ -1,0 +1,238 @@
+/*
+ * rmsnorm.h -- C ABI of librmsnorm_gb300.so: RMSNorm forward and backward
+ * over a row-major [M, N] activation matrix on one GB300 GPU (sm_103a).
+ *
+ * Operation (llama mode: every step in fp32, each output rounded once, to
+ * nearest-even, when it is stored):
+ *
+ *   forward   rstd_i = 1 / sqrt( (1/N) sum_j h_ij^2 + eps )
+ *             y_ij   = h_ij * rstd_i * (offset + w_j)
+ *             with h = x (plain) or h = R(x + residual) (fused residual add)
+ *   backward  xhat = h * rstd,  g = dy * (offset + w),
+ *             c_i  = (1/N) sum_j g_ij xhat_ij
+ *             dx   = rstd * (g - xhat * c)  [+ dresidual_out, fused variant]
+ *             dw_j = sum_i dy_ij xhat_ij
+ *
+ * Sources: Liger-Kernel PR #1388 "perf(cutedsl): add Blackwell fast path to
+ * RMSNorm" (Summary; section 1 for eps/offset as runtime fp32 scalars and a
+ * launch path without per-call marshalling; section 2 for the fused
+ * backward that produces dX and dW) and ROCm/FlyDSL PR #855 "[Perf]
+ * Optimize RMSNorm backward with staged reduction and vec8 I/O"
+ * (Implementation: a persistent main kernel writing one fp32 dweight
+ * partial per program, a finalizer that reduces the [num_programs, N]
+ * workspace and writes dweight in the parameter dtype, the fused-add
+ * specialisation with dx == dresidual; Runtime configuration and
+ * ownership: per-call workspace of num_programs * N * 4 bytes, launch on
+ * the caller's stream).
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers on the calling thread's current
+ *     CUDA device. The caller owns every buffer; the library keeps no
+ *     pointer after the call returns.
+ *   - Matrices are contiguous row-major [M, N] (row stride N elements).
+ *     w, dw are [N]; rstd is [M] fp32.
+ *   - x, residual, w, y, dy, dx, dw, residual_out, dresidual_out all share
+ *     the storage type `dt`. Pointers must be aligned to the element size;
+ *     16-byte alignment of every pointer (and N * sizeof(elem) % 16 == 0)
+ *     selects the vectorised kernels, anything else the generic kernels.
+ *   - Every call is asynchronous on `stream` (NULL = legacy default
+ *     stream). The library never synchronises and never copies between
+ *     host and device.
+ *   - eps >= 0 and offset are runtime values; they never change the kernel
+ *     chosen. M is runtime; the kernel depends on (dt, N, alignment) and the
+ *     backward's CTA count on M and the device's SM count.
+ *   - Errors are returned as status codes; nothing aborts or throws.
+ *     M == 0 is a successful call that launches no kernel (the backward
+ *     then sets dw to zero, the empty sum, with one cudaMemsetAsync).
+ *     INVALID_ARG: N < 1, N > RMSNORM_MAX_N, M < 0, M * N beyond 2^40, a
+ *     required pointer NULL or not element-aligned, eps < 0, eps or offset
+ *     not finite, an unknown dtype. WORKSPACE: a non-NULL workspace smaller
+ *     than rmsnorm_bwd_workspace_bytes() or not 16-byte aligned.
+ *     CUDA: a CUDA call failed; rmsnorm_last_cuda_error() returns its code.
+ *   - Aliasing: y may equal x; dx may equal dy; in the fused variants
+ *     residual_out may equal residual and dx may equal dresidual_out. No
+ *     other pair of buffers may overlap.
+ */
+#ifndef RMSNORM_GB300_H
+#define RMSNORM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *rmsnorm_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    RMSNORM_F32 = 0,  /* IEEE binary32 storage */
+    RMSNORM_BF16 = 1  /* bfloat16 storage, fp32 compute */
+} rmsnorm_dtype_t;
+
+typedef enum {
+    RMSNORM_SUCCESS = 0,
+    RMSNORM_ERR_INVALID_ARG = 1,
+    RMSNORM_ERR_UNSUPPORTED = 2,
+    RMSNORM_ERR_WORKSPACE = 3,
+    RMSNORM_ERR_CUDA = 4
+} rmsnorm_status_t;
+
+#define RMSNORM_MAX_N 65536
+
+/*
+ * Forward. Reads x [M,N] and w [N]; writes y [M,N] and rstd [M] (fp32).
+ * Liger-Kernel PR #1388, Summary and section 1 (vector forward with a
+ * CTA-level reduction; eps and offset runtime scalars).
+ */
+rmsnorm_status_t rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd,
+                             int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                             float eps, float offset, rmsnorm_stream_t stream);
+
+/*
+ * Backward. Reads dy, x [M,N], w [N] and the forward's rstd [M]; writes
+ * dx [M,N] and dw [N]. rstd is read, not recomputed, so eps is only
+ * validated (kept for symmetry with the forward). Two kernels run on
+ * `stream`: a persistent main kernel that writes dx and one fp32 dw
+ * partial row per CTA into the workspace, then a finalizer that sums the
+ * partial rows in a fixed order and writes dw in the storage type
+ * (FlyDSL PR #855, Implementation).
+ * workspace: NULL, or device memory of at least
+ * rmsnorm_bwd_workspace_bytes(M, N, dt) bytes, 16-byte aligned, not used
+ * by any other call in flight. Its contents on entry do not matter (every
+ * byte read is first written by this call). With NULL the library takes
+ * stream-ordered memory (cudaMallocAsync/cudaFreeAsync on `stream`).
+ */
+rmsnorm_status_t rmsnorm_bwd(const void *dy, const void *x, const void *w, const float *rstd,
+                             void *dx, void *dw, void *workspace, size_t workspace_bytes,
+                             int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                             float eps, float offset, rmsnorm_stream_t stream);
+
+/*
+ * Fused residual add + forward. h = R(x + residual) is rounded to the
+ * storage type, written to residual_out [M,N] and normalised into y
+ * (FlyDSL PR #855, Implementation: fused-add RMSNorm as a specialisation
+ * of the same kernels). residual_out may equal residual.
+ */
+rmsnorm_status_t rmsnorm_add_fwd(const void *x, const void *residual, const void *w,
+                                 void *y, void *residual_out, float *rstd,
+                                 int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                                 float eps, float offset, rmsnorm_stream_t stream);
+
+/*
+ * Fused residual add backward. h is the forward's residual_out. dx [M,N]
+ * receives rstd * (g - xhat * c) + dresidual_out, the gradient of both x
+ * and residual (one buffer serves as dx and dresidual, FlyDSL PR #855,
+ * Implementation). dresidual_out may be NULL (treated as zero) or equal dx.
+ * Workspace rules as in rmsnorm_bwd.
+ */
+rmsnorm_status_t rmsnorm_add_bwd(const void *dy, const void *dresidual_out, const void *h,
+                                 const void *w, const float *rstd, void *dx, void *dw,
+                                 void *workspace, size_t workspace_bytes,
+                                 int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                                 float eps, float offset, rmsnorm_stream_t stream);
+
+/*
+ * Bytes of workspace the backward needs for (M, N, dt) on the current
+ * device: (number of persistent CTAs) * N * 4, rounded up to 256 (FlyDSL
+ * PR #855, Runtime configuration and ownership). Returns 0 for M == 0 and
+ * for invalid arguments or when no CUDA device is usable.
+ */
+size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt);
+
+/* ------------------------------------------------------------------------
+ * Plans: which kernel runs. Exposed for tests and benchmarks (the analogue
+ * of the A/B toggles of Liger-Kernel PR #1388, "Behavior when the fast path
+ * does not apply", and of the tuned-kernel registry of
+ * ROCm/TransformerEngine PR #583, Description).
+ * --------------------------------------------------------------------- */
+
+typedef enum {
+    RMSNORM_PATH_VECTOR = 0,   /* 128-bit loads, row held in registers       */
+    RMSNORM_PATH_STAGED = 1,   /* row staged in shared memory by bulk copies */
+    RMSNORM_PATH_GENERIC = 2   /* any N and alignment, element loads         */
+} rmsnorm_path_t;
+
+typedef struct {
+    int32_t path;               /* rmsnorm_path_t                               */
+    int32_t plan_id;            /* index into the library's plan table          */
+    int32_t threads_per_row;
+    int32_t chunks_per_thread;  /* 16-byte chunks a thread holds per row        */
+    int32_t rows_per_cta;       /* rows a CTA works on concurrently             */
+    int32_t cta_threads;
+    int32_t packed;             /* 1: packed f32x2 arithmetic                   */
+    int32_t ctas;               /* grid size (backward: persistent CTAs = dw partial rows) */
+    int32_t ctas_per_sm;        /* backward: resident CTAs per SM used for `ctas` */
+    int32_t smem_bytes;         /* dynamic shared memory per CTA                */
+    int64_t workspace_bytes;    /* backward only                                */
+} rmsnorm_plan_t;
+
+#define RMSNORM_OP_FWD 0
+#define RMSNORM_OP_BWD 1
+
+/*
+ * Host-only plan query: no CUDA call, usable without a GPU. `aligned` says
+ * whether every pointer is 16-byte aligned; `num_sms` is the device's SM
+ * count and `ctas_per_sm` the resident backward CTAs per SM (<= 0: the
+ * plan's nominal value). force_plan < 0 picks the default plan; otherwise
+ * the plan with that id (UNSUPPORTED if it cannot serve N/dt/alignment).
+ * force_ctas > 0 sets the backward's CTA count (capped by the rows
+ * available).
+ */
+rmsnorm_status_t rmsnorm_plan_query(int op, int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                                    int aligned, int num_sms, int ctas_per_sm,
+                                    int force_plan, int force_ctas, rmsnorm_plan_t *out);
+
+/* Number of entries in the plan table. */
+int rmsnorm_plan_count(void);
+
+/* Plan id of table entry `index` (0 <= index < rmsnorm_plan_count()), or -1. */
+int rmsnorm_plan_id_at(int index);
+
+/*
+ * Forward with a forced plan (force_plan < 0: default). residual and
+ * residual_out NULL: plain forward; both non-NULL: fused add. Reports the
+ * plan that ran in *plan_used (may be NULL).
+ */
+rmsnorm_status_t rmsnorm_fwd_ex(const void *x, const void *residual, const void *w,
+                                void *y, void *residual_out, float *rstd,
+                                int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                                float eps, float offset, rmsnorm_stream_t stream,
+                                int force_plan, rmsnorm_plan_t *plan_used);
+
+/*
+ * Backward with a forced plan and CTA count (negative / zero: default),
+ * plain when `fused` is 0 (dresidual_out ignored), fused otherwise.
+ * force_packed: -1 default, 0 scalar fp32 arithmetic, 1 packed f32x2; both
+ * use the same even/odd accumulator pairing, so they agree bit for bit.
+ * event_after_main: if non-NULL, a cudaEvent_t recorded on `stream` between
+ * the main kernel and the finalizer (for timing the two separately).
+ */
+rmsnorm_status_t rmsnorm_bwd_ex(const void *dy, const void *dresidual_out, const void *x,
+                                const void *w, const float *rstd, void *dx, void *dw,
+                                void *workspace, size_t workspace_bytes,
+                                int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                                float eps, float offset, rmsnorm_stream_t stream,
+                                int fused, int force_plan, int force_ctas, int force_packed,
+                                void *event_after_main, rmsnorm_plan_t *plan_used);
+
+/* Static description of a status code. */
+const char *rmsnorm_status_string(rmsnorm_status_t status);
+
+/* cudaError_t of the last call on this thread that returned RMSNORM_ERR_CUDA. */
+int rmsnorm_last_cuda_error(void);
+
+/*
+ * Consistency check of the plan table, run once when the library loads and
+ * callable again: every (dtype, N-class) a table entry is registered for
+ * must select that entry, and its geometry must cover the class (the
+ * analogue of the key round-trip check of ROCm/TransformerEngine PR #583).
+ * Returns 0 when consistent, else the number of inconsistent entries.
+ */
+int rmsnorm_self_check(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_GB300_H */

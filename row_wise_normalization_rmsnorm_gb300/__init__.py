@@ -1,1 +1,33 @@
-"""GB300-native RMSNorm forward/backward (placeholder; binding added next)."""
+"""GB300-native RMSNorm forward and backward (sm_103a CUDA kernels behind a C ABI).
+
+The public functions take contiguous CUDA tensors (bf16 or fp32, rows of
+length N on the last dimension) and launch on the current stream:
+
+  rmsnorm_fwd(x, w)                       -> y, rstd
+  rmsnorm_add_fwd(x, residual, w)         -> y, residual_out, rstd
+  rmsnorm_bwd(dy, x, w, rstd)             -> dx, dw
+  rmsnorm_add_bwd(dy, dres, h, w, rstd)   -> dx (= dresidual), dw
+  rmsnorm_bwd_workspace_bytes(M, N, dt)
+
+The CUDA library is loaded on first use and must have been built
+(``python -m row_wise_normalization_rmsnorm_gb300.build``); there is no CPU
+fallback. ``inputs`` holds the seeded synthetic workloads.
+"""
+from ._binding import (  # noqa: F401
+    OP_BWD,
+    OP_FWD,
+    RMSNORM_BF16,
+    RMSNORM_F32,
+    LIB_PATH,
+    Plan,
+    RMSNormError,
+    lib,
+    plan_query,
+    rmsnorm_add_bwd,
+    rmsnorm_add_fwd,
+    rmsnorm_bwd,
+    rmsnorm_bwd_ex,
+    rmsnorm_bwd_workspace_bytes,
+    rmsnorm_fwd,
+    rmsnorm_fwd_ex,
+)

@@ -1,0 +1,270 @@
+"""ctypes binding of librmsnorm_gb300.so (declared in include/rmsnorm.h).
+
+Argument marshalling only: every step of RMSNorm runs in the library's CUDA
+kernels. PyTorch supplies device memory and the current stream. There is no
+CPU fallback: if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librmsnorm_gb300.so")
+
+RMSNORM_F32, RMSNORM_BF16 = 0, 1
+STATUS = {0: "SUCCESS", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_WORKSPACE", 4: "ERR_CUDA"}
+PATH_NAMES = {0: "vector", 1: "staged", 2: "generic"}
+OP_FWD, OP_BWD = 0, 1
+TORCH_DTYPE = {torch.float32: RMSNORM_F32, torch.bfloat16: RMSNORM_BF16}
+
+
+class RMSNormError(RuntimeError):
+    def __init__(self, status: int, what: str, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        msg = f"{what}: {STATUS.get(status, status)}"
+        if status == 4:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [
+        ("path", ctypes.c_int32),
+        ("plan_id", ctypes.c_int32),
+        ("threads_per_row", ctypes.c_int32),
+        ("chunks_per_thread", ctypes.c_int32),
+        ("rows_per_cta", ctypes.c_int32),
+        ("cta_threads", ctypes.c_int32),
+        ("packed", ctypes.c_int32),
+        ("ctas", ctypes.c_int32),
+        ("ctas_per_sm", ctypes.c_int32),
+        ("smem_bytes", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["path_name"] = PATH_NAMES.get(self.path, "?")
+        return d
+
+
+_lock = threading.Lock()
+_lib = None
+
+# name -> (restype, argtypes)
+_vp, _i64, _f, _i, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
+_PPlan = ctypes.POINTER(Plan)
+SIGNATURES = {
+    "rmsnorm_fwd": (_i, [_vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp]),
+    "rmsnorm_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i, _f, _f, _vp]),
+    "rmsnorm_add_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp]),
+    "rmsnorm_add_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i, _f, _f, _vp]),
+    "rmsnorm_bwd_workspace_bytes": (_sz, [_i64, _i64, _i]),
+    "rmsnorm_plan_query": (_i, [_i, _i64, _i64, _i, _i, _i, _i, _i, _i, _PPlan]),
+    "rmsnorm_plan_count": (_i, []),
+    "rmsnorm_plan_id_at": (_i, [_i]),
+    "rmsnorm_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp, _i, _PPlan]),
+    "rmsnorm_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i, _f, _f, _vp,
+                            _i, _i, _i, _i, _vp, _PPlan]),
+    "rmsnorm_status_string": (ctypes.c_char_p, [_i]),
+    "rmsnorm_last_cuda_error": (_i, []),
+    "rmsnorm_self_check": (_i, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library with every entry point's signature declared."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is not built; run `python -m row_wise_normalization_rmsnorm_gb300.build` "
+                    "(or __graft_entry__.build()). There is no CPU fallback.")
+            h = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(h, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = h
+    return _lib
+
+
+def _raise(status: int, what: str) -> None:
+    if status != 0:
+        raise RMSNormError(status, what, lib().rmsnorm_last_cuda_error() if status == 4 else 0)
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return TORCH_DTYPE[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}; use torch.float32 or torch.bfloat16") from None
+
+
+def _check(t: torch.Tensor, name: str, like: torch.Tensor | None = None, numel: int | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if like is not None and (t.dtype != like.dtype or t.device != like.device):
+        raise ValueError(f"{name} must match dtype/device of the input")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, has {t.numel()}")
+
+
+def _rows(x: torch.Tensor):
+    N = x.shape[-1]
+    M = x.numel() // N if N else 0
+    return M, N
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    _check(workspace, "workspace")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def rmsnorm_fwd(x, w, *, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=None, stream=None):
+    """y, rstd = RMSNorm(x) over the last dimension (llama mode)."""
+    M, N = _rows(x)
+    _check(x, "x")
+    _check(w, "w", like=x, numel=N)
+    y = torch.empty_like(x) if y is None else y
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
+    _check(y, "y", like=x, numel=x.numel())
+    _check(rstd, "rstd", numel=M)
+    st = lib().rmsnorm_fwd(x.data_ptr(), w.data_ptr(), y.data_ptr(), rstd.data_ptr(), M, N, _dtype_code(x),
+                           eps, offset, _stream_handle(stream, x.device))
+    _raise(st, "rmsnorm_fwd")
+    return y, rstd
+
+
+def rmsnorm_add_fwd(x, residual, w, *, eps: float = 1e-6, offset: float = 0.0, y=None, residual_out=None,
+                    rstd=None, stream=None):
+    """h = x + residual (rounded), y = RMSNorm(h); returns y, h, rstd."""
+    M, N = _rows(x)
+    _check(x, "x")
+    _check(residual, "residual", like=x, numel=x.numel())
+    _check(w, "w", like=x, numel=N)
+    y = torch.empty_like(x) if y is None else y
+    residual_out = torch.empty_like(x) if residual_out is None else residual_out
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
+    _check(y, "y", like=x, numel=x.numel())
+    _check(residual_out, "residual_out", like=x, numel=x.numel())
+    _check(rstd, "rstd", numel=M)
+    st = lib().rmsnorm_add_fwd(x.data_ptr(), residual.data_ptr(), w.data_ptr(), y.data_ptr(),
+                               residual_out.data_ptr(), rstd.data_ptr(), M, N, _dtype_code(x), eps, offset,
+                               _stream_handle(stream, x.device))
+    _raise(st, "rmsnorm_add_fwd")
+    return y, residual_out, rstd
+
+
+def rmsnorm_bwd(dy, x, w, rstd, *, eps: float = 1e-6, offset: float = 0.0, dx=None, dw=None, workspace=None,
+                stream=None):
+    """dx, dw of RMSNorm given the forward's rstd."""
+    M, N = _rows(x)
+    for t, n in ((dy, "dy"), (x, "x")):
+        _check(t, n, like=x, numel=x.numel())
+    _check(w, "w", like=x, numel=N)
+    _check(rstd, "rstd", numel=M)
+    dx = torch.empty_like(x) if dx is None else dx
+    dw = torch.empty_like(w) if dw is None else dw
+    _check(dx, "dx", like=x, numel=x.numel())
+    _check(dw, "dw", like=x, numel=N)
+    wp, wb = _ws(workspace)
+    st = lib().rmsnorm_bwd(dy.data_ptr(), x.data_ptr(), w.data_ptr(), rstd.data_ptr(), dx.data_ptr(),
+                           dw.data_ptr(), wp, wb, M, N, _dtype_code(x), eps, offset,
+                           _stream_handle(stream, x.device))
+    _raise(st, "rmsnorm_bwd")
+    return dx, dw
+
+
+def rmsnorm_add_bwd(dy, dresidual_out, h, w, rstd, *, eps: float = 1e-6, offset: float = 0.0, dx=None, dw=None,
+                    workspace=None, stream=None):
+    """dx (= dresidual) and dw of the fused residual-add RMSNorm; h is the forward's residual_out."""
+    M, N = _rows(h)
+    _check(dy, "dy", like=h, numel=h.numel())
+    _check(h, "h", like=h, numel=h.numel())
+    if dresidual_out is not None:
+        _check(dresidual_out, "dresidual_out", like=h, numel=h.numel())
+    _check(w, "w", like=h, numel=N)
+    _check(rstd, "rstd", numel=M)
+    dx = torch.empty_like(h) if dx is None else dx
+    dw = torch.empty_like(w) if dw is None else dw
+    _check(dx, "dx", like=h, numel=h.numel())
+    _check(dw, "dw", like=h, numel=N)
+    wp, wb = _ws(workspace)
+    st = lib().rmsnorm_add_bwd(dy.data_ptr(), _ptr(dresidual_out), h.data_ptr(), w.data_ptr(), rstd.data_ptr(),
+                               dx.data_ptr(), dw.data_ptr(), wp, wb, M, N, _dtype_code(h), eps, offset,
+                               _stream_handle(stream, h.device))
+    _raise(st, "rmsnorm_add_bwd")
+    return dx, dw
+
+
+def rmsnorm_bwd_workspace_bytes(M: int, N: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else TORCH_DTYPE[dtype]
+    return int(lib().rmsnorm_bwd_workspace_bytes(M, N, code))
+
+
+def plan_query(op: int, M: int, N: int, dtype: int, *, aligned: bool = True, num_sms: int = 152,
+               ctas_per_sm: int = 0, force_plan: int = -1, force_ctas: int = 0) -> dict:
+    """Host-only plan selection (no GPU needed)."""
+    p = Plan()
+    st = lib().rmsnorm_plan_query(op, M, N, dtype, int(aligned), num_sms, ctas_per_sm, force_plan, force_ctas,
+                                  ctypes.byref(p))
+    _raise(st, "rmsnorm_plan_query")
+    return p.as_dict()
+
+
+def rmsnorm_fwd_ex(x, w, *, residual=None, eps=1e-6, offset=0.0, y=None, residual_out=None, rstd=None,
+                   force_plan=-1, stream=None):
+    """Forward with a forced plan; returns (y, residual_out or None, rstd, plan dict)."""
+    M, N = _rows(x)
+    y = torch.empty_like(x) if y is None else y
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(x)
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
+    p = Plan()
+    st = lib().rmsnorm_fwd_ex(_ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(residual_out), _ptr(rstd), M, N,
+                              _dtype_code(x), eps, offset, _stream_handle(stream, x.device), force_plan,
+                              ctypes.byref(p))
+    _raise(st, "rmsnorm_fwd_ex")
+    return y, residual_out, rstd, p.as_dict()
+
+
+def rmsnorm_bwd_ex(dy, x, w, rstd, *, dresidual_out=None, fused=False, eps=1e-6, offset=0.0, dx=None, dw=None,
+                   workspace=None, force_plan=-1, force_ctas=0, force_packed=-1, event_after_main=None,
+                   stream=None):
+    """Backward with forced plan / CTA count / packed math; returns (dx, dw, plan dict)."""
+    M, N = _rows(x)
+    dx = torch.empty_like(x) if dx is None else dx
+    dw = torch.empty_like(w) if dw is None else dw
+    wp, wb = _ws(workspace)
+    ev = None if event_after_main is None else event_after_main.cuda_event
+    p = Plan()
+    st = lib().rmsnorm_bwd_ex(_ptr(dy), _ptr(dresidual_out), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw),
+                              wp, wb, M, N, _dtype_code(x), eps, offset, _stream_handle(stream, x.device),
+                              int(fused), force_plan, force_ctas, force_packed, ev, ctypes.byref(p))
+    _raise(st, "rmsnorm_bwd_ex")
+    return dx, dw, p.as_dict()

@@ -1,0 +1,479 @@
+// api.cu -- the C ABI of librmsnorm_gb300.so (declared in include/rmsnorm.h):
+// argument checks, plan selection from the specialisation table, the
+// backward's workspace, and the launches on the caller's stream.
+//
+// The host path does no per-call marshalling: plain pointers and scalars go
+// straight into a by-value kernel parameter block, the stream is the
+// caller's, and the only cached state is per-device SM counts and
+// occupancies (Liger-Kernel PR #1388, section 1: the direct-call launch;
+// ROCm/FlyDSL PR #855, "Hot-cache launch path" and "Runtime configuration
+// and ownership": raw caller stream, SM count cached per device, workspace
+// owned per call).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/rmsnorm.h"
+#include "plans.h"
+
+namespace rmsn {
+
+struct PlanDesc {
+    int id, op, path, tpr, v, teams, cmin, cmax;
+};
+
+static const PlanDesc kPlans[] = {
+#define RMSN_DESC(id, op, path, tpr, v, teams, cmin, cmax) {id, op, path, tpr, v, teams, cmin, cmax},
+    RMSNORM_PLAN_TABLE(RMSN_DESC)
+#undef RMSN_DESC
+};
+static const int kNumPlans = (int)(sizeof(kPlans) / sizeof(kPlans[0]));
+
+static const PlanDesc *find_plan(int id) {
+    for (int i = 0; i < kNumPlans; ++i)
+        if (kPlans[i].id == id) return &kPlans[i];
+    return nullptr;
+}
+
+static int elem_size(int dt) { return dt == RMSNORM_BF16 ? 2 : 4; }
+
+// Default plan for (op, chunks per row); nullptr when no vector plan covers C.
+static const PlanDesc *default_vector_plan(int op, int64_t C) {
+    for (int i = 0; i < kNumPlans; ++i) {
+        const PlanDesc &d = kPlans[i];
+        if (d.op == op && d.path == PATH_VECTOR && d.cmin > 0 && C >= d.cmin && C <= d.cmax) return &d;
+    }
+    return nullptr;
+}
+
+static const PlanDesc *generic_plan(int op) {
+    for (int i = 0; i < kNumPlans; ++i)
+        if (kPlans[i].op == op && kPlans[i].path == PATH_GENERIC) return &kPlans[i];
+    return nullptr;
+}
+
+static int cta_threads(const PlanDesc &d) { return d.path == PATH_GENERIC ? 256 : d.tpr * d.teams; }
+
+static int nominal_ctas_per_sm(const PlanDesc &d) {
+    const int t = cta_threads(d);
+    int c = 2048 / t;
+    return c < 1 ? 1 : c;
+}
+
+static int bwd_smem_bytes(const PlanDesc &d, int64_t N) {
+    if (d.path != PATH_VECTOR || d.teams <= 1) return 0;
+    return (int)((d.teams - 1) * N * 4);
+}
+
+// Pure selection: no CUDA calls.
+static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool aligned, int num_sms,
+                                    int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
+    if (!out) return RMSNORM_ERR_INVALID_ARG;
+    if (op != RMSNORM_OP_FWD && op != RMSNORM_OP_BWD) return RMSNORM_ERR_INVALID_ARG;
+    if (dt != RMSNORM_F32 && dt != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
+    if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
+    if (num_sms < 1) return RMSNORM_ERR_INVALID_ARG;
+    const int s = elem_size(dt);
+    const bool vec_ok = aligned && (N * s) % 16 == 0;
+    const int64_t C = vec_ok ? N * s / 16 : 0;
+
+    const PlanDesc *d = nullptr;
+    if (force_plan >= 0) {
+        d = find_plan(force_plan);
+        if (!d || d->op != op) return RMSNORM_ERR_UNSUPPORTED;
+        if (d->path == PATH_VECTOR && (!vec_ok || C > (int64_t)d->tpr * d->v)) return RMSNORM_ERR_UNSUPPORTED;
+        if (d->path == PATH_STAGED) return RMSNORM_ERR_UNSUPPORTED;
+    } else {
+        d = vec_ok ? default_vector_plan(op, C) : nullptr;
+        if (!d) d = generic_plan(op);
+    }
+    if (!d) return RMSNORM_ERR_UNSUPPORTED;
+
+    std::memset(out, 0, sizeof(*out));
+    out->path = d->path;
+    out->plan_id = d->id;
+    out->threads_per_row = d->path == PATH_GENERIC ? 256 : d->tpr;
+    out->chunks_per_thread = d->v;
+    out->rows_per_cta = d->path == PATH_GENERIC ? 1 : d->teams;
+    out->cta_threads = cta_threads(*d);
+    out->packed = 1;
+    if (op == RMSNORM_OP_FWD) {
+        out->ctas = (int32_t)((M + out->rows_per_cta - 1) / out->rows_per_cta);
+        out->ctas_per_sm = 0;
+        out->smem_bytes = 0;
+        out->workspace_bytes = 0;
+        if (d->path == PATH_GENERIC) out->packed = 0;
+        return RMSNORM_SUCCESS;
+    }
+    if (d->path == PATH_GENERIC) out->packed = 0;
+    const int cps = ctas_per_sm > 0 ? ctas_per_sm : nominal_ctas_per_sm(*d);
+    const int64_t max_useful = (M + out->rows_per_cta - 1) / out->rows_per_cta;
+    int64_t P = (int64_t)cps * num_sms;
+    if (force_ctas > 0) P = force_ctas;
+    if (P > max_useful) P = max_useful;
+    out->ctas = (int32_t)P;
+    out->ctas_per_sm = cps;
+    out->smem_bytes = bwd_smem_bytes(*d, N);
+    if (out->smem_bytes > 48 * 1024) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t bytes = P * N * 4;
+    out->workspace_bytes = (bytes + 255) / 256 * 256;
+    return RMSNORM_SUCCESS;
+}
+
+// ------------------------------------------------------ device queries --
+
+static thread_local int g_last_cuda_error = 0;
+
+static rmsnorm_status_t cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return RMSNORM_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+static std::atomic<int> g_sm_count[kMaxDevices];
+
+static cudaError_t device_sms(int *dev_out, int *sms_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int sms = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (sms <= 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_sm_count[dev].store(sms, std::memory_order_relaxed);
+    }
+    *dev_out = dev;
+    *sms_out = sms;
+    return cudaSuccess;
+}
+
+static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed) {
+    return dt == RMSNORM_BF16 ? bwd_main_kernel_ptr_bf16(plan_id, fused, packed)
+                              : bwd_main_kernel_ptr_f32(plan_id, fused, packed);
+}
+
+// Resident CTAs per SM for a backward plan: the minimum over its plain /
+// fused and packed / scalar variants, so the CTA count (and with it the
+// workspace size and dW's summation order) is the same for all of them.
+static std::mutex g_occ_mutex;
+static int g_occ_cache[kMaxDevices][2][64];
+
+static cudaError_t bwd_ctas_per_sm(int dev, int dt, const PlanDesc &d, int64_t N, int *out) {
+    const int slot = d.id;
+    if (slot < 0 || slot >= 64) return cudaErrorInvalidValue;
+    const int dti = dt == RMSNORM_BF16 ? 1 : 0;
+    // The dynamic shared memory of the team combine depends on N; occupancy
+    // is cached for the largest N the plan serves (the conservative value).
+    {
+        std::lock_guard<std::mutex> lk(g_occ_mutex);
+        if (g_occ_cache[dev][dti][slot] > 0) {
+            *out = g_occ_cache[dev][dti][slot];
+            return cudaSuccess;
+        }
+    }
+    const int threads = cta_threads(d);
+    const int E = 16 / elem_size(dt);
+    const int64_t nmax = d.path == PATH_VECTOR ? (int64_t)d.tpr * d.v * E : N;
+    const int smem = bwd_smem_bytes(d, nmax);
+    int best = 1 << 30;
+    for (int f = 0; f < 2; ++f) {
+        for (int pk = 0; pk < 2; ++pk) {
+            if (d.path == PATH_GENERIC && pk == 1) continue;
+            const void *k = bwd_kernel(d.id, dt, f != 0, pk != 0);
+            if (!k) return cudaErrorInvalidDeviceFunction;
+            int n = 0;
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem);
+            if (e != cudaSuccess) return e;
+            if (n < best) best = n;
+        }
+    }
+    if (best < 1) best = 1;
+    std::lock_guard<std::mutex> lk(g_occ_mutex);
+    g_occ_cache[dev][dti][slot] = best;
+    *out = best;
+    return cudaSuccess;
+}
+
+// ----------------------------------------------------- argument checks --
+
+static bool aligned_to(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+static bool finite_scalar(float v) { return std::isfinite(v); }
+
+static std::atomic<int> g_table_ok{-1};
+
+int self_check_impl() {
+    int bad = 0;
+    for (int op = 0; op < 2; ++op) {
+        int64_t expect = 1;
+        for (int i = 0; i < kNumPlans; ++i) {
+            const PlanDesc &d = kPlans[i];
+            if (d.op != op || d.path != PATH_VECTOR || d.cmin == 0) continue;
+            // ranges of default plans must tile [1, max] in table order
+            if (d.cmin != expect || d.cmax < d.cmin) ++bad;
+            expect = d.cmax + 1;
+            // the plan must hold every chunk of the largest row it serves
+            if ((int64_t)d.tpr * d.v < d.cmax) ++bad;
+            // both ends of its range must select it again
+            if (default_vector_plan(op, d.cmin) != &d || default_vector_plan(op, d.cmax) != &d) ++bad;
+        }
+        if (!generic_plan(op)) ++bad;
+    }
+    for (int i = 0; i < kNumPlans; ++i) {
+        const PlanDesc &d = kPlans[i];
+        if (find_plan(d.id) != &d) ++bad;  // ids unique
+        if (d.path == PATH_VECTOR) {
+            const bool pow2 = d.tpr > 0 && (d.tpr & (d.tpr - 1)) == 0;
+            if (!pow2 || d.tpr * d.teams > kMaxCtaThreads || d.tpr * d.teams < 32 || d.v < 1) ++bad;
+        }
+        if (d.id < 0 || d.id >= 64) ++bad;
+    }
+    return bad;
+}
+
+static bool table_ok() {
+    int s = g_table_ok.load(std::memory_order_relaxed);
+    if (s < 0) {
+        s = self_check_impl() == 0 ? 1 : 0;
+        g_table_ok.store(s, std::memory_order_relaxed);
+    }
+    return s == 1;
+}
+
+// Run the table check when the library is loaded.
+static const bool g_loaded_check = [] {
+    if (!table_ok()) std::fprintf(stderr, "librmsnorm_gb300: plan table self-check failed\n");
+    return true;
+}();
+
+// --------------------------------------------------------------- forward --
+
+static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void *w, void *y,
+                                 void *residual_out, float *rstd, int64_t M, int64_t N, int dt, float eps,
+                                 float offset, cudaStream_t stream, int force_plan, rmsnorm_plan_t *used) {
+    if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
+    if (dt != RMSNORM_F32 && dt != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
+    if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
+    if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
+    const bool fused = residual != nullptr || residual_out != nullptr;
+    if (fused && (!residual || !residual_out)) return RMSNORM_ERR_INVALID_ARG;
+    if (!x || !w || !y || !rstd) return RMSNORM_ERR_INVALID_ARG;
+    const uintptr_t s = (uintptr_t)elem_size(dt);
+    if (!aligned_to(x, s) || !aligned_to(w, s) || !aligned_to(y, s) || !aligned_to(rstd, 4))
+        return RMSNORM_ERR_INVALID_ARG;
+    if (fused && (!aligned_to(residual, s) || !aligned_to(residual_out, s))) return RMSNORM_ERR_INVALID_ARG;
+    if (M == 0) return RMSNORM_SUCCESS;
+
+    bool aligned = aligned_to(x, 16) && aligned_to(w, 16) && aligned_to(y, 16);
+    if (fused) aligned = aligned && aligned_to(residual, 16) && aligned_to(residual_out, 16);
+
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess) return cuda_fail(e);
+    rmsnorm_plan_t plan;
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, sms, 0, force_plan, 0, &plan);
+    if (st != RMSNORM_SUCCESS) return st;
+
+    FwdParams p;
+    p.x = x;
+    p.residual = residual;
+    p.w = w;
+    p.y = y;
+    p.residual_out = residual_out;
+    p.rstd = rstd;
+    p.M = M;
+    p.N = (int)N;
+    p.eps = eps;
+    p.offset = offset;
+    const int le = launch_fwd(plan.plan_id, dt == RMSNORM_BF16 ? 1 : 0, fused, p, plan.ctas, stream);
+    if (le != 0) return cuda_fail((cudaError_t)le);
+    if (used) *used = plan;
+    return RMSNORM_SUCCESS;
+}
+
+// -------------------------------------------------------------- backward --
+
+static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x, const void *w,
+                                 const float *rstd, void *dx, void *dw, void *workspace, size_t ws_bytes,
+                                 int64_t M, int64_t N, int dt, float eps, float offset, cudaStream_t stream,
+                                 bool fused, int force_plan, int force_ctas, int force_packed,
+                                 void *event_after_main, rmsnorm_plan_t *used) {
+    if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
+    if (dt != RMSNORM_F32 && dt != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
+    if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
+    if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
+    if (force_packed < -1 || force_packed > 1) return RMSNORM_ERR_INVALID_ARG;
+    if (!dy || !x || !w || !rstd || !dx || !dw) return RMSNORM_ERR_INVALID_ARG;
+    if (!fused) dres = nullptr;
+    const uintptr_t s = (uintptr_t)elem_size(dt);
+    if (!aligned_to(dy, s) || !aligned_to(x, s) || !aligned_to(w, s) || !aligned_to(dx, s) ||
+        !aligned_to(dw, s) || !aligned_to(rstd, 4) || (dres && !aligned_to(dres, s)))
+        return RMSNORM_ERR_INVALID_ARG;
+    if (workspace && !aligned_to(workspace, 16)) return RMSNORM_ERR_WORKSPACE;
+    if (M == 0) {
+        // dw is the empty sum
+        cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)N * s, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return RMSNORM_SUCCESS;
+    }
+    bool aligned = aligned_to(dy, 16) && aligned_to(x, 16) && aligned_to(w, 16) && aligned_to(dx, 16);
+    if (dres) aligned = aligned && aligned_to(dres, 16);
+
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess) return cuda_fail(e);
+    rmsnorm_plan_t plan;
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, sms, 1, force_plan, force_ctas, &plan);
+    if (st != RMSNORM_SUCCESS) return st;
+    const PlanDesc *d = find_plan(plan.plan_id);
+    int cps = 1;
+    e = bwd_ctas_per_sm(dev, dt, *d, N, &cps);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, sms, cps, force_plan, force_ctas, &plan);
+    if (st != RMSNORM_SUCCESS) return st;
+    bool packed = plan.packed != 0;
+    if (force_packed == 0) packed = false;
+    if (force_packed == 1 && plan.path == PATH_VECTOR) packed = true;
+    plan.packed = packed ? 1 : 0;
+
+    float *ws = static_cast<float *>(workspace);
+    bool owned = false;
+    if (ws) {
+        if (ws_bytes < (size_t)plan.workspace_bytes) return RMSNORM_ERR_WORKSPACE;
+    } else {
+        void *tmp = nullptr;
+        e = cudaMallocAsync(&tmp, (size_t)plan.workspace_bytes, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+        ws = static_cast<float *>(tmp);
+        owned = true;
+    }
+
+    BwdParams p;
+    p.dy = dy;
+    p.x = x;
+    p.w = w;
+    p.rstd = rstd;
+    p.dres = dres;
+    p.dx = dx;
+    p.ws = ws;
+    p.M = M;
+    p.N = (int)N;
+    p.offset = offset;
+    int le = dt == RMSNORM_BF16
+                 ? launch_bwd_main_bf16(plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream)
+                 : launch_bwd_main_f32(plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream);
+    if (le == 0 && event_after_main) le = (int)cudaEventRecord(static_cast<cudaEvent_t>(event_after_main), stream);
+    if (le == 0)
+        le = dt == RMSNORM_BF16 ? launch_dw_finalize_bf16(ws, plan.ctas, (int)N, dw, stream)
+                                : launch_dw_finalize_f32(ws, plan.ctas, (int)N, dw, stream);
+    if (owned) {
+        cudaError_t fe = cudaFreeAsync(ws, stream);
+        if (le == 0 && fe != cudaSuccess) le = (int)fe;
+    }
+    if (le != 0) return cuda_fail((cudaError_t)le);
+    if (used) *used = plan;
+    return RMSNORM_SUCCESS;
+}
+
+}  // namespace rmsn
+
+using namespace rmsn;
+
+extern "C" {
+
+rmsnorm_status_t rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd, int64_t M, int64_t N,
+                             rmsnorm_dtype_t dt, float eps, float offset, rmsnorm_stream_t stream) {
+    return fwd_impl(x, nullptr, w, y, nullptr, rstd, M, N, dt, eps, offset, (cudaStream_t)stream, -1, nullptr);
+}
+
+rmsnorm_status_t rmsnorm_add_fwd(const void *x, const void *residual, const void *w, void *y,
+                                 void *residual_out, float *rstd, int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                                 float eps, float offset, rmsnorm_stream_t stream) {
+    if (!residual || !residual_out) return RMSNORM_ERR_INVALID_ARG;
+    return fwd_impl(x, residual, w, y, residual_out, rstd, M, N, dt, eps, offset, (cudaStream_t)stream, -1,
+                    nullptr);
+}
+
+rmsnorm_status_t rmsnorm_fwd_ex(const void *x, const void *residual, const void *w, void *y,
+                                void *residual_out, float *rstd, int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                                float eps, float offset, rmsnorm_stream_t stream, int force_plan,
+                                rmsnorm_plan_t *plan_used) {
+    return fwd_impl(x, residual, w, y, residual_out, rstd, M, N, dt, eps, offset, (cudaStream_t)stream,
+                    force_plan, plan_used);
+}
+
+rmsnorm_status_t rmsnorm_bwd(const void *dy, const void *x, const void *w, const float *rstd, void *dx,
+                             void *dw, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                             rmsnorm_dtype_t dt, float eps, float offset, rmsnorm_stream_t stream) {
+    return bwd_impl(dy, nullptr, x, w, rstd, dx, dw, workspace, workspace_bytes, M, N, dt, eps, offset,
+                    (cudaStream_t)stream, false, -1, 0, -1, nullptr, nullptr);
+}
+
+rmsnorm_status_t rmsnorm_add_bwd(const void *dy, const void *dresidual_out, const void *h, const void *w,
+                                 const float *rstd, void *dx, void *dw, void *workspace, size_t workspace_bytes,
+                                 int64_t M, int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
+                                 rmsnorm_stream_t stream) {
+    return bwd_impl(dy, dresidual_out, h, w, rstd, dx, dw, workspace, workspace_bytes, M, N, dt, eps, offset,
+                    (cudaStream_t)stream, true, -1, 0, -1, nullptr, nullptr);
+}
+
+rmsnorm_status_t rmsnorm_bwd_ex(const void *dy, const void *dresidual_out, const void *x, const void *w,
+                                const float *rstd, void *dx, void *dw, void *workspace, size_t workspace_bytes,
+                                int64_t M, int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
+                                rmsnorm_stream_t stream, int fused, int force_plan, int force_ctas,
+                                int force_packed, void *event_after_main, rmsnorm_plan_t *plan_used) {
+    return bwd_impl(dy, dresidual_out, x, w, rstd, dx, dw, workspace, workspace_bytes, M, N, dt, eps, offset,
+                    (cudaStream_t)stream, fused != 0, force_plan, force_ctas, force_packed, event_after_main,
+                    plan_used);
+}
+
+size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt) {
+    if (M <= 0 || N < 1 || N > RMSNORM_MAX_N || (dt != RMSNORM_F32 && dt != RMSNORM_BF16)) return 0;
+    if (M > 0x7fffffffLL || !table_ok()) return 0;
+    int dev = 0, sms = 0;
+    if (device_sms(&dev, &sms) != cudaSuccess) return 0;
+    // The largest requirement over the aligned and generic plans, so one
+    // size serves any pointer alignment.
+    size_t best = 0;
+    for (int aligned = 0; aligned < 2; ++aligned) {
+        rmsnorm_plan_t plan;
+        if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, sms, 1, -1, 0, &plan) != RMSNORM_SUCCESS) return 0;
+        int cps = 1;
+        if (bwd_ctas_per_sm(dev, dt, *find_plan(plan.plan_id), N, &cps) != cudaSuccess) return 0;
+        if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, sms, cps, -1, 0, &plan) != RMSNORM_SUCCESS) return 0;
+        if ((size_t)plan.workspace_bytes > best) best = (size_t)plan.workspace_bytes;
+    }
+    return best;
+}
+
+rmsnorm_status_t rmsnorm_plan_query(int op, int64_t M, int64_t N, rmsnorm_dtype_t dt, int aligned, int num_sms,
+                                    int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
+    if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
+    return select_plan(op, M, N, dt, aligned != 0, num_sms, ctas_per_sm, force_plan, force_ctas, out);
+}
+
+int rmsnorm_plan_count(void) { return kNumPlans; }
+
+int rmsnorm_plan_id_at(int index) { return (index >= 0 && index < kNumPlans) ? kPlans[index].id : -1; }
+
+const char *rmsnorm_status_string(rmsnorm_status_t status) {
+    switch (status) {
+    case RMSNORM_SUCCESS: return "success";
+    case RMSNORM_ERR_INVALID_ARG: return "invalid argument";
+    case RMSNORM_ERR_UNSUPPORTED: return "unsupported plan or configuration";
+    case RMSNORM_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case RMSNORM_ERR_CUDA: return "CUDA error (see rmsnorm_last_cuda_error)";
+    default: return "unknown status";
+    }
+}
+
+int rmsnorm_last_cuda_error(void) { return g_last_cuda_error; }
+
+int rmsnorm_self_check(void) { return self_check_impl(); }
+
+}  // extern "C"

@@ -1,0 +1,318 @@
+// bwd_kernels.cuh -- RMSNorm backward kernels (plain and fused residual add).
+//
+// Two launches, no global atomics and no inter-CTA waits (the kernel
+// boundary is the only grid-wide barrier), after ROCm/FlyDSL PR #855
+// (Implementation, "Hybrid atomic / two-stage backward"):
+//
+//  1. Main kernel, persistent: P CTAs walk the rows in a grid-stride loop.
+//     A team of TPR threads owns a row; each thread holds V 16-byte chunks
+//     of x and dy in registers across both passes over the row, and its
+//     slice of (offset + w) for the whole run (loaded once per CTA):
+//       pass 1  dot = sum_j g_j xhat_j       (g = dy (offset + w), xhat = x rstd)
+//       pass 2  dx_j = rstd (g_j - xhat_j dot / N) [+ dres_j], stored directly
+//               acc_j += dy_j xhat_j           (fp32, in registers)
+//     At the end the CTA's teams are added in team order and the CTA writes
+//     one fp32 partial row ws[cta, 0..N).
+//  2. Finalizer: dw_j = R( sum_{p=0..P-1} ws[p, j] ) in a fixed order,
+//     written in the parameter dtype.
+//
+// Arithmetic is done on fp32 pairs (even, odd column). With PACKED the pair
+// ops are single f32x2 instructions (Liger-Kernel PR #1388, section 2:
+// packed math where the wide-row backward is issue-bound); without it they
+// are two fp32 intrinsics per pair. The association is the same, so the two
+// variants produce identical bits.
+#pragma once
+
+#include "common.cuh"
+#include "plans.h"
+
+namespace rmsn {
+
+template <typename T, int TPR, int V, int TEAMS, bool PACKED, bool FUSED>
+__global__ void __launch_bounds__(TPR *TEAMS)
+    rmsnorm_bwd_vector(const BwdParams p) {
+    using Pk = Pair<PACKED>;
+    constexpr int E = Elem<T>::E;
+    constexpr int NP = Elem<T>::NP;
+    constexpr int W = TPR > 32 ? TPR / 32 : 1;
+    __shared__ float red[2][TEAMS][W];       // double-buffered: one barrier per row
+    extern __shared__ float4 comb_smem[];    // (TEAMS - 1) * N floats
+
+    const int team = threadIdx.x / TPR;
+    const int t = threadIdx.x % TPR;
+    const int N = p.N;
+    const int C = N / E;
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x);
+    const uint4 *dy4 = reinterpret_cast<const uint4 *>(p.dy);
+    const uint4 *dr4 = reinterpret_cast<const uint4 *>(p.dres);
+    uint4 *dx4 = reinterpret_cast<uint4 *>(p.dx);
+    const bool has_dres = FUSED && p.dres != nullptr;
+
+    // (offset + w) for this thread's columns: loaded once per CTA.
+    const float2 o2 = make_float2(p.offset, p.offset);
+    float2 wp[V][NP], acc[V][NP];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * TPR + t;
+        float2 wv[NP];
+        unpack<T>(c < C ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + c) : make_uint4(0, 0, 0, 0), wv);
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            wp[v][k] = Pk::add(o2, wv[k]);
+            acc[v][k] = make_float2(0.f, 0.f);
+        }
+    }
+
+    // Every team of the CTA runs the same number of iterations (that of
+    // team 0, which has the lowest first row) so the CTA-wide barrier in the
+    // reduction is reached by all threads; rows past M are masked.
+    const int64_t G = (int64_t)gridDim.x * TEAMS;
+    const int64_t first = (int64_t)blockIdx.x * TEAMS;
+    const int64_t iters = (p.M - first + G - 1) / G;
+    for (int64_t i = 0; i < iters; ++i) {
+        const int64_t row = first + team + i * G;
+        const bool valid = row < p.M;
+        const int64_t rr = valid ? row : p.M - 1;
+        const int64_t base = rr * C;
+
+        uint4 xv[V], dv[V], rv[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * TPR + t;
+            const bool in = c < C;
+            xv[v] = in ? ld_stream(x4 + base + c) : make_uint4(0, 0, 0, 0);
+            dv[v] = in ? ld_stream(dy4 + base + c) : make_uint4(0, 0, 0, 0);
+            rv[v] = (has_dres && in) ? ld_stream(dr4 + base + c) : make_uint4(0, 0, 0, 0);
+        }
+        const float r = p.rstd[rr];
+        const float2 r2 = make_float2(r, r);
+
+        // pass 1: dot = sum g * xhat (even and odd columns in separate lanes)
+        float2 dot = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float2 xf[NP], df[NP];
+            unpack<T>(xv[v], xf);
+            unpack<T>(dv[v], df);
+#pragma unroll
+            for (int k = 0; k < NP; ++k) dot = Pk::fma(Pk::mul(df[k], wp[v][k]), Pk::mul(xf[k], r2), dot);
+        }
+        const float s = team_allreduce<TPR>(__fadd_rn(dot.x, dot.y), &red[i & 1][team][0], t);
+        const float cm = -__fdiv_rn(s, (float)N);
+        const float2 nc2 = make_float2(cm, cm);
+
+        // pass 2: dx from the registers, dW partial in registers
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * TPR + t;
+            float2 xf[NP], df[NP], out[NP];
+            unpack<T>(xv[v], xf);
+            unpack<T>(dv[v], df);
+#pragma unroll
+            for (int k = 0; k < NP; ++k) {
+                const float2 xh = Pk::mul(xf[k], r2);
+                const float2 g = Pk::mul(df[k], wp[v][k]);
+                out[k] = Pk::mul(Pk::fma(xh, nc2, g), r2);
+                if (valid) acc[v][k] = Pk::fma(df[k], xh, acc[v][k]);
+            }
+            if (has_dres) {
+                float2 rf[NP];
+                unpack<T>(rv[v], rf);
+#pragma unroll
+                for (int k = 0; k < NP; ++k) out[k] = Pk::add(out[k], rf[k]);
+            }
+            if (valid && c < C) st_chunk(dx4 + base + c, pack<T>(out));
+        }
+    }
+
+    // Combine the CTA's teams in team order, then write ws[blockIdx.x, :].
+    float *wsrow = p.ws + (int64_t)blockIdx.x * N;
+    if constexpr (TEAMS > 1) {
+        float *comb = reinterpret_cast<float *>(comb_smem);
+        if (team > 0) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const int c = v * TPR + t;
+                if (c < C) {
+                    float *d = comb + (int64_t)(team - 1) * N + c * E;
+#pragma unroll
+                    for (int k = 0; k < NP; ++k) {
+                        d[2 * k] = acc[v][k].x;
+                        d[2 * k + 1] = acc[v][k].y;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        if (team != 0) return;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * TPR + t;
+            if (c < C) {
+                for (int tm = 1; tm < TEAMS; ++tm) {
+                    const float *s2 = comb + (int64_t)(tm - 1) * N + c * E;
+#pragma unroll
+                    for (int k = 0; k < NP; ++k)
+                        acc[v][k] = Pk::add(acc[v][k], make_float2(s2[2 * k], s2[2 * k + 1]));
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * TPR + t;
+        if (c < C) {
+            float4 *d = reinterpret_cast<float4 *>(wsrow + c * E);
+#pragma unroll
+            for (int q = 0; q < NP / 2; ++q)
+                d[q] = make_float4(acc[v][2 * q].x, acc[v][2 * q].y, acc[v][2 * q + 1].x, acc[v][2 * q + 1].y);
+        }
+    }
+}
+
+// Generic main kernel: one 256-thread CTA per row at a time, element loads,
+// each row read twice (the second read is served by L1/L2). The CTA's dW
+// partial row lives in the workspace itself: the thread that owns column j
+// writes ws[cta, j] on its first row and updates it on later rows, so no
+// other thread touches it and no atomics are needed.
+template <typename T, bool FUSED>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
+    __shared__ float red[32];
+    const int N = p.N;
+    const T *w = reinterpret_cast<const T *>(p.w);
+    float *wsrow = p.ws + (int64_t)blockIdx.x * N;
+    const bool has_dres = FUSED && p.dres != nullptr;
+    bool first = true;
+    for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+        const T *x = reinterpret_cast<const T *>(p.x) + row * N;
+        const T *dy = reinterpret_cast<const T *>(p.dy) + row * N;
+        const T *dr = reinterpret_cast<const T *>(p.dres) + row * N;
+        T *dx = reinterpret_cast<T *>(p.dx) + row * N;
+        const float r = p.rstd[row];
+        float dot = 0.f;
+        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+            const float g = __fmul_rn(load_elem(dy, j), __fadd_rn(p.offset, load_w(w, j)));
+            dot = __fmaf_rn(g, __fmul_rn(load_elem(x, j), r), dot);
+        }
+        const float cm = -__fdiv_rn(cta_allreduce(dot, red), (float)N);
+        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+            const float dyj = load_elem(dy, j);
+            const float xh = __fmul_rn(load_elem(x, j), r);
+            const float g = __fmul_rn(dyj, __fadd_rn(p.offset, load_w(w, j)));
+            float d = __fmul_rn(__fmaf_rn(xh, cm, g), r);
+            if (has_dres) d = __fadd_rn(d, load_elem(dr, j));
+            store_elem(dx, j, d);
+            wsrow[j] = first ? __fmul_rn(dyj, xh) : __fmaf_rn(dyj, xh, wsrow[j]);
+        }
+        first = false;
+    }
+}
+
+// Finalizer: 32 columns per CTA, 8 groups of partial rows. Group q sums rows
+// [q P / 8, (q+1) P / 8) in order; the 8 group sums are then added in order.
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int parts, int N, T *dw) {
+    constexpr int RG = 8;
+    __shared__ float part[RG][32];
+    const int lane = threadIdx.x & 31;
+    const int rg = threadIdx.x >> 5;
+    const int col = blockIdx.x * 32 + lane;
+    const int p0 = (int)((int64_t)parts * rg / RG);
+    const int p1 = (int)((int64_t)parts * (rg + 1) / RG);
+    float s = 0.f;
+    if (col < N) {
+        const float *src = ws + col;
+#pragma unroll 8
+        for (int q = p0; q < p1; ++q) s = __fadd_rn(s, src[(int64_t)q * N]);
+    }
+    part[rg][lane] = s;
+    __syncthreads();
+    if (rg == 0 && col < N) {
+        float tot = part[0][lane];
+#pragma unroll
+        for (int g = 1; g < RG; ++g) tot = __fadd_rn(tot, part[g][lane]);
+        store_elem(dw, col, tot);
+    }
+}
+
+// ------------------------------------------------------------- dispatch --
+
+template <typename T, int TPR, int V, int TEAMS, bool PACKED>
+static int bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
+    if (fused)
+        rmsnorm_bwd_vector<T, TPR, V, TEAMS, PACKED, true><<<grid, TPR * TEAMS, smem, s>>>(p);
+    else
+        rmsnorm_bwd_vector<T, TPR, V, TEAMS, PACKED, false><<<grid, TPR * TEAMS, smem, s>>>(p);
+    return (int)cudaGetLastError();
+}
+
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS>
+static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int grid, int smem, cudaStream_t s) {
+    if constexpr (OP != OP_BWD) {
+        return (int)cudaErrorInvalidValue;
+    } else if constexpr (PATH == PATH_GENERIC) {
+        if (fused)
+            rmsnorm_bwd_generic<T, true><<<grid, 256, 0, s>>>(p);
+        else
+            rmsnorm_bwd_generic<T, false><<<grid, 256, 0, s>>>(p);
+        return (int)cudaGetLastError();
+    } else if constexpr (PATH == PATH_VECTOR) {
+        return packed ? bwd_launch_vec<T, TPR, V, TEAMS, true>(fused, p, grid, smem, s)
+                      : bwd_launch_vec<T, TPR, V, TEAMS, false>(fused, p, grid, smem, s);
+    } else {
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS>
+static const void *bwd_ptr_entry(bool fused, bool packed) {
+    if constexpr (OP != OP_BWD) {
+        return nullptr;
+    } else if constexpr (PATH == PATH_GENERIC) {
+        return fused ? (const void *)rmsnorm_bwd_generic<T, true> : (const void *)rmsnorm_bwd_generic<T, false>;
+    } else if constexpr (PATH == PATH_VECTOR) {
+        if (packed)
+            return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, true, true>
+                         : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, true, false>;
+        return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, false, true>
+                     : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, false, false>;
+    } else {
+        return nullptr;
+    }
+}
+
+template <typename T>
+static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem,
+                        void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (plan_id) {
+#define RMSN_BWD_CASE(id, op, path, tpr, v, teams, cmin, cmax) \
+    case id: return bwd_launch_entry<T, op, path, tpr, v, teams>(fused, packed, p, grid, smem, s);
+        RMSNORM_PLAN_TABLE(RMSN_BWD_CASE)
+#undef RMSN_BWD_CASE
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
+    switch (plan_id) {
+#define RMSN_BWD_PTR(id, op, path, tpr, v, teams, cmin, cmax) \
+    case id: return bwd_ptr_entry<T, op, path, tpr, v, teams>(fused, packed);
+        RMSNORM_PLAN_TABLE(RMSN_BWD_PTR)
+#undef RMSN_BWD_PTR
+    default:
+        return nullptr;
+    }
+}
+
+template <typename T>
+static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *stream) {
+    const int grid = (N + 31) / 32;
+    rmsnorm_dw_finalize<T><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(ws, parts, N,
+                                                                               static_cast<T *>(dw));
+    return (int)cudaGetLastError();
+}
+
+}  // namespace rmsn

@@ -1,0 +1,175 @@
+// common.cuh -- device helpers shared by the RMSNorm kernels: 16-byte
+// chunk access, bf16/fp32 pair conversion, packed f32x2 arithmetic and
+// team (sub-warp, warp or multi-warp) all-reduce.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+// Elements per 16-byte chunk and per register pair.
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int E = 4;   // elements per chunk
+    static constexpr int NP = 2;  // float2 pairs per chunk
+};
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int E = 8;
+    static constexpr int NP = 4;
+};
+
+// ----------------------------------------------------------- 16-byte I/O --
+// Row data is read once: ld.global.cs (streaming, evict-first). The weight
+// is shared by every row: the read-only path. Writes are plain stores.
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
+__device__ __forceinline__ uint4 ld_keep(const uint4 *p) { return __ldg(p); }
+__device__ __forceinline__ void st_chunk(uint4 *p, const uint4 &v) { *p = v; }
+
+// ------------------------------------------------- chunk <-> fp32 pairs --
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t u) {
+    // bf16 is the upper half of a binary32: widening is a shift / mask.
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf16x2(float2 v) {
+    __nv_bfloat162 b = __float22bfloat162_rn(v);  // round to nearest even
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+template <typename T> __device__ __forceinline__ void unpack(const uint4 &c, float2 (&p)[Elem<T>::NP]);
+template <> __device__ __forceinline__ void unpack<__nv_bfloat16>(const uint4 &c, float2 (&p)[4]) {
+    p[0] = bf16x2_to_f2(c.x);
+    p[1] = bf16x2_to_f2(c.y);
+    p[2] = bf16x2_to_f2(c.z);
+    p[3] = bf16x2_to_f2(c.w);
+}
+template <> __device__ __forceinline__ void unpack<float>(const uint4 &c, float2 (&p)[2]) {
+    p[0] = make_float2(__uint_as_float(c.x), __uint_as_float(c.y));
+    p[1] = make_float2(__uint_as_float(c.z), __uint_as_float(c.w));
+}
+
+template <typename T> __device__ __forceinline__ uint4 pack(const float2 (&p)[Elem<T>::NP]);
+template <> __device__ __forceinline__ uint4 pack<__nv_bfloat16>(const float2 (&p)[4]) {
+    return make_uint4(f2_to_bf16x2(p[0]), f2_to_bf16x2(p[1]), f2_to_bf16x2(p[2]), f2_to_bf16x2(p[3]));
+}
+template <> __device__ __forceinline__ uint4 pack<float>(const float2 (&p)[2]) {
+    return make_uint4(__float_as_uint(p[0].x), __float_as_uint(p[0].y), __float_as_uint(p[1].x),
+                      __float_as_uint(p[1].y));
+}
+
+// Scalar element access for the generic kernels.
+__device__ __forceinline__ float load_elem(const float *p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float load_elem(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ float load_w(const float *p, int64_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float load_w(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(__ldg(p + i));
+}
+__device__ __forceinline__ void store_elem(float *p, int64_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void store_elem(__nv_bfloat16 *p, int64_t i, float v) {
+    p[i] = __float2bfloat16_rn(v);
+}
+// Value a store of v would hold (round to the storage type).
+__device__ __forceinline__ float round_to(float v, const float *) { return v; }
+__device__ __forceinline__ float round_to(float v, const __nv_bfloat16 *) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// ------------------------------------------------------- pair arithmetic --
+// Two implementations with identical IEEE results lane by lane: packed
+// f32x2 instructions (one instruction for two fp32 lanes on data-centre
+// Blackwell, Liger-Kernel PR #1388 section 2) and per-lane fp32 intrinsics
+// that the compiler may not contract. The kernels use one even/odd pairing
+// for both, so the packed and scalar variants agree bit for bit.
+template <bool PACKED> struct Pair;
+
+template <> struct Pair<true> {
+    static __device__ __forceinline__ float2 fma(float2 a, float2 b, float2 c) {
+        float2 d;
+        asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+            "mov.b64 ra, {%2, %3};\n\t"
+            "mov.b64 rb, {%4, %5};\n\t"
+            "mov.b64 rc, {%6, %7};\n\t"
+            "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+            "mov.b64 {%0, %1}, rd;\n\t}"
+            : "=f"(d.x), "=f"(d.y)
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+        return d;
+    }
+    static __device__ __forceinline__ float2 mul(float2 a, float2 b) {
+        float2 d;
+        asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+            "mov.b64 ra, {%2, %3};\n\t"
+            "mov.b64 rb, {%4, %5};\n\t"
+            "mul.rn.f32x2 rd, ra, rb;\n\t"
+            "mov.b64 {%0, %1}, rd;\n\t}"
+            : "=f"(d.x), "=f"(d.y)
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+        return d;
+    }
+    static __device__ __forceinline__ float2 add(float2 a, float2 b) {
+        float2 d;
+        asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+            "mov.b64 ra, {%2, %3};\n\t"
+            "mov.b64 rb, {%4, %5};\n\t"
+            "add.rn.f32x2 rd, ra, rb;\n\t"
+            "mov.b64 {%0, %1}, rd;\n\t}"
+            : "=f"(d.x), "=f"(d.y)
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+        return d;
+    }
+};
+
+template <> struct Pair<false> {
+    static __device__ __forceinline__ float2 fma(float2 a, float2 b, float2 c) {
+        return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
+    }
+    static __device__ __forceinline__ float2 mul(float2 a, float2 b) {
+        return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
+    }
+    static __device__ __forceinline__ float2 add(float2 a, float2 b) {
+        return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
+    }
+};
+
+// --------------------------------------------------------- team reduce --
+// All-reduce of one float over a team of TPR consecutive threads
+// (TPR a power of two). Within a warp: xor butterfly; every lane ends with
+// the same bits because fp32 addition is commutative. Across the warps of
+// a team: lane 0 of each warp writes `red[warp]`, a CTA barrier, then every
+// thread adds red[0..W) in index order. The barrier is CTA-wide, so every
+// thread of the CTA must call this the same number of times.
+template <int TPR>
+__device__ __forceinline__ float team_allreduce(float v, float *red, int t) {
+    constexpr int WIDTH = TPR < 32 ? TPR : 32;
+#pragma unroll
+    for (int o = WIDTH / 2; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if constexpr (TPR > 32) {
+        constexpr int W = TPR / 32;
+        if ((t & 31) == 0) red[t >> 5] = v;
+        __syncthreads();
+        float s = red[0];
+#pragma unroll
+        for (int i = 1; i < W; ++i) s = __fadd_rn(s, red[i]);
+        v = s;
+    }
+    return v;
+}
+
+// CTA-wide sum for the generic kernels (blockDim.x a multiple of 32, at most
+// 1024). Same ordering rules as team_allreduce; `red` holds 32 floats.
+__device__ __forceinline__ float cta_allreduce(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int W = blockDim.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float s = red[0];
+    for (int i = 1; i < W; ++i) s = __fadd_rn(s, red[i]);
+    __syncthreads();  // red is reused by the next call
+    return s;
+}
+
+}  // namespace rmsn

@@ -1,0 +1,212 @@
+// fwd_kernels.cu -- RMSNorm forward kernels (plain and fused residual add).
+//
+// Vector kernel: a team of TPR threads owns one row; each thread loads V
+// 16-byte chunks of it (chunk c = v * TPR + t, so a warp's loads are
+// contiguous), keeps them in registers, reduces the sum of squares (warp
+// butterfly, then shared memory across the team's warps), and writes
+// y = x * rstd * (offset + w) from the same registers, rounded once.
+// This is the row-in-registers forward with vector loads and a CTA-level
+// reduction of Liger-Kernel PR #1388 (Summary; "_launch_fwd_vector"), with
+// the warps per row chosen by N as in the tuned per-hidden-size kernels of
+// ROCm/TransformerEngine PR #583 (Description).
+//
+// Generic kernel: one 256-thread CTA per row, element loads, the row read
+// twice (the second read hits L1/L2). Serves any N and any element-aligned
+// pointers (Liger-Kernel PR #1388, "Behavior when the fast path does not
+// apply": irregular or unaligned shapes take scalar paths).
+#include "common.cuh"
+#include "plans.h"
+
+namespace rmsn {
+
+template <typename T, int TPR, int V, int TEAMS, bool FUSED>
+__global__ void __launch_bounds__(TPR *TEAMS)
+    rmsnorm_fwd_vector(const FwdParams p) {
+    using Pk = Pair<true>;
+    constexpr int NP = Elem<T>::NP;
+    constexpr int W = TPR > 32 ? TPR / 32 : 1;
+    __shared__ float red[TEAMS][W];
+
+    const int team = threadIdx.x / TPR;
+    const int t = threadIdx.x % TPR;
+    const int64_t row = (int64_t)blockIdx.x * TEAMS + team;
+    const bool valid = row < p.M;
+    const int64_t rr = valid ? row : p.M - 1;  // keep every thread in the reductions
+    const int C = p.N / Elem<T>::E;
+    const int64_t base = rr * C;
+
+    uint4 xv[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * TPR + t;
+        xv[v] = c < C ? ld_stream(reinterpret_cast<const uint4 *>(p.x) + base + c) : make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (FUSED) {
+        // h = R(x + residual). For bf16 inputs the fp32 sum is exact unless
+        // the exponents differ by more than 15, and then both it and the
+        // exact sum round to the larger operand: one rounding to bf16 gives
+        // the correctly rounded sum. For fp32 the add is the rounding.
+        uint4 rv[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * TPR + t;
+            rv[v] = c < C ? ld_stream(reinterpret_cast<const uint4 *>(p.residual) + base + c)
+                          : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float2 a[NP], b[NP];
+            unpack<T>(xv[v], a);
+            unpack<T>(rv[v], b);
+#pragma unroll
+            for (int k = 0; k < NP; ++k) a[k] = Pk::add(a[k], b[k]);
+            xv[v] = pack<T>(a);
+            const int c = v * TPR + t;
+            if (valid && c < C) st_chunk(reinterpret_cast<uint4 *>(p.residual_out) + base + c, xv[v]);
+        }
+    }
+
+    float2 ss = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        float2 a[NP];
+        unpack<T>(xv[v], a);
+#pragma unroll
+        for (int k = 0; k < NP; ++k) ss = Pk::fma(a[k], a[k], ss);
+    }
+    const float s = team_allreduce<TPR>(__fadd_rn(ss.x, ss.y), &red[team][0], t);
+    const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(s, (float)p.N), p.eps));
+    if (valid && t == 0) p.rstd[row] = rstd;
+    if (!valid) return;
+
+    const float2 r2 = make_float2(rstd, rstd);
+    const float2 o2 = make_float2(p.offset, p.offset);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * TPR + t;
+        if (c < C) {
+            float2 a[NP], wv[NP];
+            unpack<T>(xv[v], a);
+            unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.w) + c), wv);
+#pragma unroll
+            for (int k = 0; k < NP; ++k) a[k] = Pk::mul(Pk::mul(a[k], r2), Pk::add(o2, wv[k]));
+            st_chunk(reinterpret_cast<uint4 *>(p.y) + base + c, pack<T>(a));
+        }
+    }
+}
+
+template <typename T, bool FUSED>
+__global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
+    __shared__ float red[32];
+    const int64_t row = blockIdx.x;
+    const int N = p.N;
+    const T *x = reinterpret_cast<const T *>(p.x) + row * N;
+    const T *res = reinterpret_cast<const T *>(p.residual) + row * N;
+    T *hout = reinterpret_cast<T *>(p.residual_out) + row * N;
+    const T *w = reinterpret_cast<const T *>(p.w);
+    T *y = reinterpret_cast<T *>(p.y) + row * N;
+
+    float ss = 0.f;
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        float h = load_elem(x, j);
+        if constexpr (FUSED) {
+            h = round_to(__fadd_rn(h, load_elem(res, j)), x);
+            store_elem(hout, j, h);
+        }
+        ss = __fmaf_rn(h, h, ss);
+    }
+    const float s = cta_allreduce(ss, red);
+    const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(s, (float)N), p.eps));
+    if (threadIdx.x == 0) p.rstd[row] = rstd;
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        // The same thread wrote hout[j] above, so it reads its own value.
+        const float h = FUSED ? load_elem(static_cast<const T *>(hout), j) : load_elem(x, j);
+        store_elem(y, j, __fmul_rn(__fmul_rn(h, rstd), __fadd_rn(p.offset, load_w(w, j))));
+    }
+}
+
+// ------------------------------------------------------------- dispatch --
+
+template <typename T, int TPR, int V, int TEAMS>
+static int launch_vec(bool fused, const FwdParams &p, int grid, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fused)
+        rmsnorm_fwd_vector<T, TPR, V, TEAMS, true><<<grid, TPR * TEAMS, 0, s>>>(p);
+    else
+        rmsnorm_fwd_vector<T, TPR, V, TEAMS, false><<<grid, TPR * TEAMS, 0, s>>>(p);
+    return (int)cudaGetLastError();
+}
+
+template <typename T, int TPR, int V, int TEAMS>
+static const void *ptr_vec(bool fused) {
+    return fused ? (const void *)rmsnorm_fwd_vector<T, TPR, V, TEAMS, true>
+                 : (const void *)rmsnorm_fwd_vector<T, TPR, V, TEAMS, false>;
+}
+
+template <typename T>
+static int launch_gen(bool fused, const FwdParams &p, int grid, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fused)
+        rmsnorm_fwd_generic<T, true><<<grid, 256, 0, s>>>(p);
+    else
+        rmsnorm_fwd_generic<T, false><<<grid, 256, 0, s>>>(p);
+    return (int)cudaGetLastError();
+}
+
+template <typename T>
+static const void *ptr_gen(bool fused) {
+    return fused ? (const void *)rmsnorm_fwd_generic<T, true> : (const void *)rmsnorm_fwd_generic<T, false>;
+}
+
+// One switch case per table entry; `if constexpr` keeps kernels of other
+// ops and paths from being instantiated here.
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS>
+static int launch_entry(bool fused, const FwdParams &p, int grid, void *stream) {
+    if constexpr (OP != OP_FWD) return (int)cudaErrorInvalidValue;
+    else if constexpr (PATH == PATH_GENERIC) return launch_gen<T>(fused, p, grid, stream);
+    else if constexpr (PATH == PATH_VECTOR) return launch_vec<T, TPR, V, TEAMS>(fused, p, grid, stream);
+    else return (int)cudaErrorInvalidValue;
+}
+
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS>
+static const void *ptr_entry(bool fused) {
+    if constexpr (OP != OP_FWD) return nullptr;
+    else if constexpr (PATH == PATH_GENERIC) return ptr_gen<T>(fused);
+    else if constexpr (PATH == PATH_VECTOR) return ptr_vec<T, TPR, V, TEAMS>(fused);
+    else return nullptr;
+}
+
+template <typename T>
+static int launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
+    switch (plan_id) {
+#define RMSN_FWD_CASE(id, op, path, tpr, v, teams, cmin, cmax) \
+    case id: return launch_entry<T, op, path, tpr, v, teams>(fused, p, grid, stream);
+        RMSNORM_PLAN_TABLE(RMSN_FWD_CASE)
+#undef RMSN_FWD_CASE
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+static const void *ptr_t(int plan_id, bool fused) {
+    switch (plan_id) {
+#define RMSN_FWD_PTR(id, op, path, tpr, v, teams, cmin, cmax) \
+    case id: return ptr_entry<T, op, path, tpr, v, teams>(fused);
+        RMSNORM_PLAN_TABLE(RMSN_FWD_PTR)
+#undef RMSN_FWD_PTR
+    default:
+        return nullptr;
+    }
+}
+
+int launch_fwd(int plan_id, int dtype, bool fused, const FwdParams &p, int grid, void *stream) {
+    return dtype == 1 ? launch_t<__nv_bfloat16>(plan_id, fused, p, grid, stream)
+                      : launch_t<float>(plan_id, fused, p, grid, stream);
+}
+
+const void *fwd_kernel_ptr(int plan_id, int dtype, bool fused) {
+    return dtype == 1 ? ptr_t<__nv_bfloat16>(plan_id, fused) : ptr_t<float>(plan_id, fused);
+}
+
+}  // namespace rmsn

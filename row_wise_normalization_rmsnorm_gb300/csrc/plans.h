@@ -1,0 +1,107 @@
+// plans.h -- the specialisation table shared by the host selector and the
+// kernel instantiations, and the parameter blocks the kernels receive.
+//
+// A plan fixes the geometry of one kernel: how many threads share a row
+// (a "team"), how many 16-byte chunks of the row each thread holds, and how
+// many teams a CTA runs side by side. Plans are keyed by the row length in
+// 16-byte chunks, C = N * sizeof(elem) / 16, so one table serves bf16 and
+// fp32 (a bf16 row of 8192 and an fp32 row of 4096 are both 1024 chunks).
+// The geometry depends only on (dtype, N, alignment), never on M: a row's
+// in-CTA reduction order, and with it y, rstd and dx, is the same whatever
+// the batch size (ROCm/FlyDSL PR #855, "Runtime configuration and
+// ownership": M is a runtime argument of one compiled kernel).
+#pragma once
+
+#include <stdint.h>
+
+namespace rmsn {
+
+enum PlanOp { OP_FWD = 0, OP_BWD = 1 };
+enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2 };
+
+// X(id, op, path, threads_per_row, chunks_per_thread, teams_per_cta, cmin, cmax)
+// [cmin, cmax] is the range of C for which the plan is the default; 0, 0
+// marks an alternative that runs only when forced (tuning and A/B tests).
+// Generic plans hold no chunks (they use a 256-thread CTA per row).
+#define RMSNORM_PLAN_TABLE(X)                                   \
+    /* forward, row in registers */                             \
+    X( 0, OP_FWD, PATH_VECTOR,    8, 1, 32,    1,    8)         \
+    X( 1, OP_FWD, PATH_VECTOR,   16, 1, 16,    9,   16)         \
+    X( 2, OP_FWD, PATH_VECTOR,   32, 1,  8,   17,   32)         \
+    X( 3, OP_FWD, PATH_VECTOR,   32, 2,  8,   33,   64)         \
+    X( 4, OP_FWD, PATH_VECTOR,   32, 4,  8,   65,  128)         \
+    X( 5, OP_FWD, PATH_VECTOR,   64, 4,  4,  129,  256)         \
+    X( 6, OP_FWD, PATH_VECTOR,  128, 4,  2,  257,  512)         \
+    X( 7, OP_FWD, PATH_VECTOR,  256, 4,  1,  513, 1024)         \
+    X( 8, OP_FWD, PATH_VECTOR,  512, 4,  1, 1025, 2048)         \
+    X( 9, OP_FWD, PATH_VECTOR, 1024, 4,  1, 2049, 4096)         \
+    X(10, OP_FWD, PATH_VECTOR,  128, 8,  2,    0,    0)         \
+    X(11, OP_FWD, PATH_VECTOR,  512, 2,  1,    0,    0)         \
+    X(12, OP_FWD, PATH_VECTOR, 1024, 1,  1,    0,    0)         \
+    X(13, OP_FWD, PATH_VECTOR,  256, 2,  2,    0,    0)         \
+    X(14, OP_FWD, PATH_VECTOR,   64, 8,  4,    0,    0)         \
+    X(15, OP_FWD, PATH_VECTOR,   16, 2, 16,    0,    0)         \
+    /* forward, any N and alignment */                          \
+    X(16, OP_FWD, PATH_GENERIC, 256, 0,  1,    0,    0)         \
+    /* backward main kernel, persistent, row in registers */    \
+    X(20, OP_BWD, PATH_VECTOR,    8, 1, 32,    1,    8)         \
+    X(21, OP_BWD, PATH_VECTOR,   16, 1, 16,    9,   16)         \
+    X(22, OP_BWD, PATH_VECTOR,   32, 1,  8,   17,   32)         \
+    X(23, OP_BWD, PATH_VECTOR,   32, 2,  8,   33,   64)         \
+    X(24, OP_BWD, PATH_VECTOR,   64, 2,  4,   65,  128)         \
+    X(25, OP_BWD, PATH_VECTOR,  128, 2,  2,  129,  256)         \
+    X(26, OP_BWD, PATH_VECTOR,  256, 2,  2,  257,  512)         \
+    X(27, OP_BWD, PATH_VECTOR,  512, 2,  1,  513, 1024)         \
+    X(28, OP_BWD, PATH_VECTOR, 1024, 2,  1, 1025, 2048)         \
+    X(29, OP_BWD, PATH_VECTOR,  256, 4,  1,    0,    0)         \
+    X(30, OP_BWD, PATH_VECTOR,  128, 4,  2,    0,    0)         \
+    X(31, OP_BWD, PATH_VECTOR, 1024, 1,  1,    0,    0)         \
+    X(32, OP_BWD, PATH_VECTOR,  256, 1,  2,    0,    0)         \
+    X(33, OP_BWD, PATH_VECTOR,   16, 2, 16,    0,    0)         \
+    /* backward main kernel, any N and alignment */             \
+    X(36, OP_BWD, PATH_GENERIC, 256, 0,  1,    0,    0)
+
+// Largest CTA any plan uses.
+constexpr int kMaxCtaThreads = 1024;
+
+struct FwdParams {
+    const void *x;
+    const void *residual;    // NULL: plain forward
+    const void *w;
+    void *y;
+    void *residual_out;      // fused only
+    float *rstd;
+    int64_t M;
+    int N;
+    float eps;
+    float offset;
+};
+
+struct BwdParams {
+    const void *dy;
+    const void *x;           // h for the fused variant
+    const void *w;
+    const float *rstd;
+    const void *dres;        // fused only, may be NULL
+    void *dx;
+    float *ws;               // [ctas, N] fp32 partial rows of dw
+    int64_t M;
+    int N;
+    float offset;
+};
+
+// Launchers, defined in the translation units that instantiate the
+// kernels. dtype: 0 fp32, 1 bf16. They return the launch's cudaError_t.
+int launch_fwd(int plan_id, int dtype, bool fused, const FwdParams &p, int grid, void *stream);
+const void *fwd_kernel_ptr(int plan_id, int dtype, bool fused);
+
+int launch_bwd_main_bf16(int plan_id, bool fused, bool packed, const BwdParams &p, int grid,
+                         int smem, void *stream);
+int launch_bwd_main_f32(int plan_id, bool fused, bool packed, const BwdParams &p, int grid,
+                        int smem, void *stream);
+const void *bwd_main_kernel_ptr_bf16(int plan_id, bool fused, bool packed);
+const void *bwd_main_kernel_ptr_f32(int plan_id, bool fused, bool packed);
+int launch_dw_finalize_bf16(const float *ws, int parts, int N, void *dw, void *stream);
+int launch_dw_finalize_f32(const float *ws, int parts, int N, void *dw, void *stream);
+
+}  // namespace rmsn

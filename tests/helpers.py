@@ -1,0 +1,113 @@
+"""Shared helpers for the GPU parity tests: device upload (optionally at a
+non-16-byte-aligned offset), readback, and the tolerance checks.
+
+Tolerances (the RMSNorm definition and bounds are restated in the oracle):
+  y    bf16: within 1 ulp of the correctly rounded oracle value (distance of
+       the ordered bit patterns); fp32: |d| <= 1e-5 |ref| + 1e-6.
+  dx   as y, or -- where the result comes from cancelling terms -- within
+       8 * 2^-24 * rstd (|g| + |xhat c|) [+ |dres|], the fp32 rounding bound
+       of the difference of the two terms (counted and reported).
+  dw   bf16: |d| <= 4e-3 |ref| + 2^-20 S; fp32: |d| <= 1e-4 |ref| + 2^-20 S,
+       with ref the unrounded double sum and S = sum_i |dy xhat| (the scale
+       of the fp32 summation error).
+  rstd relative 2e-6.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+FLOOR_ULPS = 8.0 * 2.0 ** -24
+
+
+def to_dev(a: np.ndarray, dtype: str, device="cuda", offset: int = 0) -> torch.Tensor:
+    """Upload storage-typed numpy data. offset > 0 places the tensor `offset`
+    elements past a 256-byte-aligned allocation (a contiguous tensor whose
+    base is not 16-byte aligned)."""
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    if offset == 0:
+        return t.to(device)
+    buf = torch.empty(t.numel() + offset + 16, dtype=t.dtype, device=device)
+    view = buf[offset:offset + t.numel()].view(t.shape)
+    view.copy_(t.to(device))
+    return view
+
+
+def empty_dev(shape, dtype: str, device="cuda", offset: int = 0, fill=float("nan")) -> torch.Tensor:
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    n = int(np.prod(shape))
+    buf = torch.full((n + offset + 16,), fill, dtype=td, device=device)
+    return buf[offset:offset + n].view(shape)
+
+
+def to_host(t: torch.Tensor, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.contiguous().cpu().numpy()
+
+
+def decode(a: np.ndarray, dtype: str) -> np.ndarray:
+    return oracle.to_f64(a, dtype)
+
+
+def bf16_ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """|ordered(a) - ordered(b)| for bf16 bit patterns (signed-magnitude
+    mapped to a monotone integer line, so +0 and -0 are 0 apart)."""
+    def ordered(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x)
+    return np.abs(ordered(a) - ordered(b))
+
+
+def check_y(got: np.ndarray, ref: dict, dtype: str, key="y", key64="y64"):
+    if dtype == "bf16":
+        d = bf16_ulp_distance(got, ref[key])
+        assert d.max() <= 1, f"{key}: max {d.max()} ulp"
+        return {"max_ulp": int(d.max())}
+    r = ref[key64]
+    err = np.abs(got.astype(np.float64) - r)
+    bad = err > 1e-5 * np.abs(r) + 1e-6
+    assert not bad.any(), f"{key}: {bad.sum()} elements off, worst {err.max()}"
+    return {"max_abs": float(err.max())}
+
+
+def check_rstd(got: np.ndarray, ref64: np.ndarray):
+    rel = np.abs(got.astype(np.float64) - ref64) / ref64
+    assert rel.max() <= 2e-6, f"rstd rel err {rel.max()}"
+    return float(rel.max())
+
+
+def check_dx(got: np.ndarray, ref: dict, dtype: str, floor_mult: float = 1.0):
+    """Returns the number of elements that needed the cancellation floor."""
+    v = decode(got, dtype)
+    floor = floor_mult * FLOOR_ULPS * ref["dx_scale"]
+    near = np.abs(v - ref["dx64"]) <= floor
+    if dtype == "bf16":
+        ok = (bf16_ulp_distance(got, ref["dx"]) <= 1)
+    else:
+        r = ref["dx64"]
+        ok = np.abs(v - r) <= 1e-5 * np.abs(r) + 1e-6
+    needed = int((~ok & near).sum())
+    ok = ok | near
+    assert ok.all(), f"dx: {(~ok).sum()} elements off; worst index {np.argmax(np.abs(v - ref['dx64']) / (ref['dx_scale'] + 1e-30))}"
+    return needed
+
+
+def check_dw(got: np.ndarray, ref: dict, dtype: str):
+    v = decode(got, dtype)
+    rel = 4e-3 if dtype == "bf16" else 1e-4
+    err = np.abs(v - ref["dw64"])
+    tol = rel * np.abs(ref["dw64"]) + 2.0 ** -20 * ref["dw_abs"]
+    assert (err <= tol).all(), f"dw: {(err > tol).sum()} columns off, worst ratio {(err / tol).max()}"
+    return float((err / np.maximum(tol, 1e-300)).max())
+
+
+def cuda_bits_equal(a: torch.Tensor, b: torch.Tensor) -> bool:
+    if a.dtype == torch.bfloat16:
+        return torch.equal(a.view(torch.int16), b.view(torch.int16))
+    return torch.equal(a.view(torch.int32), b.view(torch.int32))

@@ -1,0 +1,137 @@
+"""Host-side tests of the C ABI that need no GPU: the library loads, exports
+every entry point the header declares, its plan table passes the self-check,
+plan selection follows the table, and argument errors are reported as
+status codes before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from row_wise_normalization_rmsnorm_gb300 import build as rn_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
+
+
+@pytest.fixture(scope="module")
+def rn():
+    rn_build.build()
+    import row_wise_normalization_rmsnorm_gb300 as pkg
+    return pkg
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rmsnorm_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_add_fwd", "rmsnorm_add_bwd",
+                     "rmsnorm_bwd_workspace_bytes"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(rn):
+    h = ctypes.CDLL(rn.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(h, n)]
+    assert not missing, missing
+    # and the binding declares a signature for each
+    from row_wise_normalization_rmsnorm_gb300._binding import SIGNATURES
+    assert set(declared_functions()) <= set(SIGNATURES)
+
+
+def test_plan_table_self_check(rn):
+    assert rn.lib().rmsnorm_self_check() == 0
+    ids = [rn.lib().rmsnorm_plan_id_at(i) for i in range(rn.lib().rmsnorm_plan_count())]
+    assert len(ids) == len(set(ids))
+    assert rn.lib().rmsnorm_plan_id_at(len(ids)) == -1
+
+
+@pytest.mark.parametrize("dt,N,tpr,v", [
+    (1, 128, 16, 1), (1, 2048, 64, 4), (1, 4096, 128, 4), (1, 7168, 256, 4), (1, 8192, 256, 4),
+    (1, 16384, 512, 4), (0, 256, 32, 2), (0, 2048, 128, 4), (0, 6144, 512, 4), (0, 16384, 1024, 4),
+])
+def test_fwd_default_plans(rn, dt, N, tpr, v):
+    p = rn.plan_query(rn.OP_FWD, 4096, N, dt)
+    assert p["path_name"] == "vector"
+    assert (p["threads_per_row"], p["chunks_per_thread"]) == (tpr, v)
+    # the row fits the plan's registers
+    per_chunk = 8 if dt == 1 else 4
+    assert tpr * v * per_chunk >= N
+
+
+@pytest.mark.parametrize("dt,N", [(1, 4097), (1, 8191), (1, 8193), (0, 4097), (1, 65536), (0, 32768), (1, 1), (0, 3)])
+def test_fwd_generic_when_vector_cannot_serve(rn, dt, N):
+    p = rn.plan_query(rn.OP_FWD, 100, N, dt)
+    assert p["path_name"] == "generic"
+
+
+def test_misaligned_pointers_take_generic(rn):
+    assert rn.plan_query(rn.OP_FWD, 4096, 7168, 1, aligned=False)["path_name"] == "generic"
+    assert rn.plan_query(rn.OP_BWD, 4096, 2048, 0, aligned=False)["path_name"] == "generic"
+
+
+def test_plan_independent_of_m(rn):
+    for N in (128, 2048, 8192):
+        ids = {rn.plan_query(op, M, N, 1)["plan_id"] for op in (0,) for M in (1, 7, 4096, 524288)}
+        assert len(ids) == 1
+        ids = {rn.plan_query(1, M, N, 1)["plan_id"] for M in (1, 7, 4096, 524288)}
+        assert len(ids) == 1
+
+
+def test_bwd_cta_count_and_workspace(rn):
+    p = rn.plan_query(rn.OP_BWD, 16384, 8192, 1, num_sms=152, ctas_per_sm=2)
+    assert p["ctas"] == 304 and p["ctas_per_sm"] == 2
+    assert p["workspace_bytes"] == 304 * 8192 * 4
+    # capped by the rows available (rows_per_cta rows per CTA)
+    q = rn.plan_query(rn.OP_BWD, 10, 2048, 1, num_sms=152, ctas_per_sm=2)
+    assert q["ctas"] == -(-10 // q["rows_per_cta"])
+    # forced CTA count
+    r = rn.plan_query(rn.OP_BWD, 16384, 8192, 1, num_sms=152, ctas_per_sm=2, force_ctas=77)
+    assert r["ctas"] == 77 and r["workspace_bytes"] == (77 * 8192 * 4 + 255) // 256 * 256
+
+
+def test_forced_plan_rules(rn):
+    # a forward plan id is not a backward plan
+    with pytest.raises(rn.RMSNormError):
+        rn.plan_query(rn.OP_BWD, 10, 8192, 1, force_plan=7)
+    # a vector plan too small for the row is refused
+    with pytest.raises(rn.RMSNormError):
+        rn.plan_query(rn.OP_FWD, 10, 8192, 1, force_plan=0)
+    # the generic plan serves anything
+    assert rn.plan_query(rn.OP_FWD, 10, 8192, 1, force_plan=16)["path_name"] == "generic"
+    assert rn.plan_query(rn.OP_BWD, 10, 5, 0, force_plan=36)["path_name"] == "generic"
+
+
+def test_invalid_arguments_without_gpu(rn):
+    L = rn.lib()
+    x = ctypes.c_void_p(256)
+    r = ctypes.c_void_p(512)
+    # N out of range, null pointers, negative eps, non-finite scalars: all
+    # rejected before any CUDA call
+    assert L.rmsnorm_fwd(x, x, x, r, 4, 0, 1, 1e-6, 0.0, None) == 1
+    assert L.rmsnorm_fwd(x, x, x, r, 4, 65537, 1, 1e-6, 0.0, None) == 1
+    assert L.rmsnorm_fwd(None, x, x, r, 4, 8, 1, 1e-6, 0.0, None) == 1
+    assert L.rmsnorm_fwd(x, x, x, r, 4, 8, 1, -1.0, 0.0, None) == 1
+    assert L.rmsnorm_fwd(x, x, x, r, 4, 8, 1, float("nan"), 0.0, None) == 1
+    assert L.rmsnorm_fwd(x, x, x, r, 4, 8, 1, 1e-6, float("inf"), None) == 1
+    assert L.rmsnorm_fwd(x, x, x, r, 4, 8, 7, 1e-6, 0.0, None) == 1           # unknown dtype
+    assert L.rmsnorm_fwd(x, x, x, r, -1, 8, 1, 1e-6, 0.0, None) == 1          # negative M
+    assert L.rmsnorm_fwd(ctypes.c_void_p(257), x, x, r, 4, 8, 1, 1e-6, 0.0, None) == 1  # odd bf16 address
+    assert L.rmsnorm_add_fwd(x, None, x, x, x, r, 4, 8, 1, 1e-6, 0.0, None) == 1
+    assert L.rmsnorm_bwd(x, x, x, r, x, None, None, 0, 4, 8, 1, 1e-6, 0.0, None) == 1
+    assert L.rmsnorm_bwd(x, x, x, r, x, x, ctypes.c_void_p(264), 1 << 20, 4, 8, 1, 1e-6, 0.0, None) == 3
+    # M == 0 forward is a no-op that needs no device
+    assert L.rmsnorm_fwd(x, x, x, r, 0, 8, 1, 1e-6, 0.0, None) == 0
+    assert L.rmsnorm_status_string(3) == b"workspace too small or misaligned"
+
+
+def test_workspace_query_without_device_is_zero(rn):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host has a GPU")
+    assert rn.rmsnorm_bwd_workspace_bytes(4096, 2048, 1) == 0
+    assert rn.rmsnorm_bwd_workspace_bytes(0, 2048, 1) == 0
