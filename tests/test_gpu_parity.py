@@ -1,0 +1,179 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle,
+element by element, on seeded inputs.
+
+The backward is fed the oracle forward's own float32 rstd (an input of the
+backward), so every oracle input is generator- or oracle-made; the
+end-to-end test then runs forward and backward on the GPU against the exact
+gradient. Shapes span several tiles, ragged row counts and every kernel
+family: register-resident vector plans, sub-warp teams, multi-warp teams,
+and the generic path for N not a multiple of the 16-byte chunk.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import check_dw, check_dx, check_rstd, check_y, empty_dev, to_dev, to_host
+from row_wise_normalization_rmsnorm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rn():
+    from row_wise_normalization_rmsnorm_gb300 import build
+    build.build()
+    import row_wise_normalization_rmsnorm_gb300 as pkg
+    return pkg
+
+
+def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_path=None):
+    M, N = d["x"].shape
+    x = to_dev(d["x"], dt, offset=offset_elems)
+    w = to_dev(d["w"], dt, offset=offset_elems)
+    dy = to_dev(d["dy"], dt, offset=offset_elems)
+    y = empty_dev((M, N), dt, offset=offset_elems)
+    rstd = torch.full((M,), float("nan"), device="cuda")
+    res = to_dev(d["residual"], dt, offset=offset_elems) if fused else None
+    hout = empty_dev((M, N), dt, offset=offset_elems) if fused else None
+    _, _, _, fplan = rn.rmsnorm_fwd_ex(x, w, residual=res, residual_out=hout, y=y, rstd=rstd, eps=eps,
+                                       offset=offset)
+    f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=eps, offset=offset, residual=d.get("residual") if fused else None)
+    torch.cuda.synchronize()
+    check_y(to_host(y, dt), f, dt)
+    check_rstd(rstd.cpu().numpy(), f["rstd64"])
+    if fused:
+        assert np.array_equal(to_host(hout, dt), f["h"]), "residual_out differs from R(x + residual)"
+    h_np = f["h"] if fused else d["x"]
+
+    # backward, fed the oracle's fp32 rstd
+    r32 = torch.from_numpy(f["rstd32"]).cuda()
+    hdev = to_dev(h_np, dt, offset=offset_elems)
+    dx = empty_dev((M, N), dt, offset=offset_elems)
+    dw = empty_dev((N,), dt, offset=offset_elems)
+    dres_np = d.get("dres") if fused else None
+    dres = to_dev(dres_np, dt, offset=offset_elems) if dres_np is not None else None
+    _, _, bplan = rn.rmsnorm_bwd_ex(dy, hdev, w, r32, dresidual_out=dres, fused=fused, dx=dx, dw=dw, eps=eps,
+                                    offset=offset)
+    b = oracle.bwd(d["dy"], h_np, d["w"], dtype=dt, eps=eps, offset=offset, rstd=f["rstd32"], dres=dres_np)
+    torch.cuda.synchronize()
+    needed = check_dx(to_host(dx, dt), b, dt)
+    check_dw(to_host(dw, dt), b, dt)
+    if expect_path is not None:
+        assert fplan["path_name"] == expect_path and bplan["path_name"] == expect_path, (fplan, bplan)
+    # the floor is for cancellation only: it should be needed rarely
+    assert needed <= max(2, M * N // 20000), needed
+    return fplan, bplan
+
+
+def test_config_small_f32_64x256(rn):
+    d, p = inputs.workload_inputs("small_f32")
+    fp, bp = _fwd_bwd_check(rn, d, "f32", p["eps"], p["offset"])
+    assert fp["path_name"] == "vector" and bp["path_name"] == "vector"
+
+
+def test_config_llama_bf16_4096x2048(rn):
+    d, p = inputs.workload_inputs("llama_bf16_4096x2048")
+    fp, bp = _fwd_bwd_check(rn, d, "bf16", p["eps"], p["offset"])
+    assert fp["path_name"] == "vector" and bp["path_name"] == "vector"
+
+
+@pytest.mark.parametrize("name", ["add_bf16_1024x8192", "add_gemma_bf16_1024x8192",
+                                  "add_bf16_4096x4096", "add_gemma_bf16_4096x4096"])
+def test_config_fused_add(rn, name):
+    d, p = inputs.workload_inputs(name)
+    _fwd_bwd_check(rn, d, "bf16", p["eps"], p["offset"], fused=True, expect_path="vector")
+
+
+def test_fused_add_without_dres(rn):
+    d = inputs.make_inputs(300, 4096, "bf16", 41, residual=True)
+    _fwd_bwd_check(rn, d, "bf16", 1e-6, 0.0, fused=True)
+
+
+RAGGED = [
+    # (dtype, M, N)  sub-warp, warp and multi-warp teams, ragged M, generic N
+    ("bf16", 333, 8), ("bf16", 333, 64), ("bf16", 513, 128), ("bf16", 77, 256), ("bf16", 129, 1000),
+    ("bf16", 300, 4096), ("bf16", 301, 5000), ("bf16", 130, 7168), ("bf16", 257, 8192),
+    ("bf16", 97, 12288), ("bf16", 65, 16384), ("bf16", 33, 32768),
+    ("bf16", 211, 4097), ("bf16", 101, 8191), ("bf16", 101, 8193), ("bf16", 9, 65536),
+    ("bf16", 1, 2048), ("bf16", 3, 2048), ("bf16", 5, 1), ("bf16", 40, 3),
+    ("f32", 333, 4), ("f32", 333, 32), ("f32", 513, 128), ("f32", 77, 256), ("f32", 301, 2048),
+    ("f32", 130, 5000), ("f32", 257, 6144), ("f32", 97, 8192), ("f32", 65, 16384),
+    ("f32", 211, 4097), ("f32", 101, 8191), ("f32", 1, 1), ("f32", 7, 3), ("f32", 9, 65536),
+]
+
+
+@pytest.mark.parametrize("dt,M,N", RAGGED)
+def test_ragged_shapes(rn, dt, M, N):
+    d = inputs.make_inputs(M, N, dt, 50 + N % 97)
+    _fwd_bwd_check(rn, d, dt, 1e-6, 0.0)
+
+
+@pytest.mark.parametrize("dt,M,N", [("bf16", 257, 8192), ("f32", 130, 5000), ("bf16", 77, 100)])
+def test_fused_ragged_gemma(rn, dt, M, N):
+    d = inputs.make_inputs(M, N, dt, 60, w_mode="gemma", residual=True, dres=True)
+    _fwd_bwd_check(rn, d, dt, 1e-5, 1.0, fused=True)
+
+
+@pytest.mark.parametrize("dt,M,N", [("bf16", 4096, 7168), ("f32", 4096, 2048)])
+def test_misaligned_storage_offset(rn, dt, M, N):
+    """All of x, w, y, dy, dx at +1 element from a 256-byte-aligned allocation."""
+    d = inputs.make_inputs(M, N, dt, inputs.SWEEP_SEED)
+    _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, offset_elems=1, expect_path="generic")
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-2, 10.0])
+def test_eps_values(rn, eps):
+    d = inputs.make_inputs(200, 2048, "bf16", 71)
+    _fwd_bwd_check(rn, d, "bf16", eps, 0.0)
+
+
+def test_end_to_end_against_exact_gradient(rn):
+    """GPU forward, then GPU backward on the GPU's rstd, against the oracle's
+    exact gradient (rstd recomputed in double). The forward's rstd error
+    (<= 2e-6 relative) enters dx three times over, hence 4x the floor."""
+    for dt, M, N in (("bf16", 1024, 8192), ("f32", 512, 6144)):
+        d = inputs.make_inputs(M, N, dt, 80, outlier_frac=0.01)
+        x, w, dy = (to_dev(d[k], dt) for k in ("x", "w", "dy"))
+        y, rstd = rn.rmsnorm_fwd(x, w, eps=1e-6)
+        dx, dw = rn.rmsnorm_bwd(dy, x, w, rstd, eps=1e-6)
+        b = oracle.bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0)
+        torch.cuda.synchronize()
+        check_dx(to_host(dx, dt), b, dt, floor_mult=4.0)
+        check_dw(to_host(dw, dt), b, dt)
+
+
+def _rstd32_all_rows(x, w, dt, eps, chunk=2048):
+    out = np.empty(x.shape[0], dtype=np.float32)
+    for r0 in range(0, x.shape[0], chunk):
+        out[r0:r0 + chunk] = oracle.fwd(x[r0:r0 + chunk], w, dtype=dt, eps=eps, offset=0.0, nthreads=8)["rstd32"]
+    return out
+
+
+def sampled_rows(M, k=48, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(M, size=min(k, M), replace=False).tolist()) | {0, M - 1}
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", ["wide_bf16_16384x8192", "wide_f32_16384x6144"])
+def test_full_size_wide_rows(rn, name):
+    """The bench's workload sizes: sampled rows of y, rstd and dx against the
+    oracle, dW over every row (the oracle's dW-only pass)."""
+    d, p = inputs.workload_inputs(name)
+    dt, eps = p["dtype"], p["eps"]
+    M, N = d["x"].shape
+    x, w, dy = (to_dev(d[k], dt) for k in ("x", "w", "dy"))
+    y, rstd = rn.rmsnorm_fwd(x, w, eps=eps)
+    r32 = _rstd32_all_rows(d["x"], d["w"], dt, eps)
+    dx, dw = rn.rmsnorm_bwd(dy, x, w, torch.from_numpy(r32).cuda(), eps=eps)
+    torch.cuda.synchronize()
+    rows = sampled_rows(M)
+    rows_t = torch.from_numpy(rows).cuda()
+    f = oracle.fwd(d["x"][rows], d["w"], dtype=dt, eps=eps, offset=0.0)
+    check_y(to_host(y[rows_t], dt), f, dt)
+    check_rstd(rstd.cpu().numpy()[rows], f["rstd64"])
+    b = oracle.bwd(d["dy"][rows], d["x"][rows], d["w"], dtype=dt, eps=eps, offset=0.0, rstd=r32[rows])
+    check_dx(to_host(dx[rows_t], dt), b, dt)
+    full = oracle.bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=eps, offset=0.0, rstd=r32, want_dx=False, nthreads=8)
+    check_dw(to_host(dw, dt), full, dt)

@@ -1,0 +1,243 @@
+"""GPU launch-variant tests: where two launches use the same association of
+every sum, their results must be identical bit for bit (packed vs scalar
+arithmetic, CUDA-graph replay vs direct launch, default vs side stream,
+concurrent streams with their own workspaces, poisoned vs clean workspace,
+different batch sizes and batch splits, fused add vs plain on the rounded
+sum). Also: in-place aliasing, guard regions, M == 0 and status codes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import check_dw, check_dx, cuda_bits_equal, empty_dev, to_dev, to_host
+from row_wise_normalization_rmsnorm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rn():
+    from row_wise_normalization_rmsnorm_gb300 import build
+    build.build()
+    import row_wise_normalization_rmsnorm_gb300 as pkg
+    return pkg
+
+
+def dev_inputs(M, N, dt, seed, **kw):
+    d = inputs.make_inputs(M, N, dt, seed, **kw)
+    return d, {k: to_dev(v, dt) for k, v in d.items()}
+
+
+@pytest.mark.parametrize("dt,M,N", [("bf16", 2048, 8192), ("f32", 1024, 6144), ("bf16", 999, 128),
+                                    ("bf16", 500, 2048), ("f32", 300, 16)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_packed_matches_scalar_bitwise(rn, dt, M, N, fused):
+    _, t = dev_inputs(M, N, dt, 90, residual=fused, dres=fused)
+    _, rstd = rn.rmsnorm_fwd(t["x"], t["w"])
+    kw = dict(dresidual_out=t.get("dres"), fused=fused)
+    dx1, dw1, p1 = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], rstd, force_packed=1, **kw)
+    dx0, dw0, p0 = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], rstd, force_packed=0, **kw)
+    assert p1["packed"] == 1 and p0["packed"] == 0 and p1["plan_id"] == p0["plan_id"]
+    assert p1["ctas"] == p0["ctas"]
+    assert cuda_bits_equal(dx1, dx0) and cuda_bits_equal(dw1, dw0)
+
+
+def test_graph_replay_matches_direct(rn):
+    _, t = dev_inputs(1000, 4096, "bf16", 91)
+    ws = torch.empty(rn.rmsnorm_bwd_workspace_bytes(1000, 4096, torch.bfloat16), dtype=torch.uint8, device="cuda")
+    y0, r0 = rn.rmsnorm_fwd(t["x"], t["w"])
+    dx0, dw0 = rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], r0, workspace=ws)
+    y, r, dx, dw = (torch.empty_like(a) for a in (y0, r0, dx0, dw0))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            rn.rmsnorm_fwd(t["x"], t["w"], y=y, rstd=r)
+            rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], r, dx=dx, dw=dw, workspace=ws)
+    for a in (y, r, dx, dw):
+        a.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert cuda_bits_equal(y, y0) and cuda_bits_equal(r, r0)
+    assert cuda_bits_equal(dx, dx0) and cuda_bits_equal(dw, dw0)
+
+
+def test_side_streams_concurrent_match_serial(rn):
+    M, N, dt = 4096, 2048, "bf16"
+    _, a = dev_inputs(M, N, dt, 92)
+    _, b = dev_inputs(M, N, dt, 93)
+    ya, ra = rn.rmsnorm_fwd(a["x"], a["w"])
+    yb, rb = rn.rmsnorm_fwd(b["x"], b["w"])
+    dxa, dwa = rn.rmsnorm_bwd(a["dy"], a["x"], a["w"], ra)
+    dxb, dwb = rn.rmsnorm_bwd(b["dy"], b["x"], b["w"], rb)
+    nb = rn.rmsnorm_bwd_workspace_bytes(M, N, torch.bfloat16)
+    wsa = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    wsb = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    out = {}
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            out["ya"] = rn.rmsnorm_fwd(a["x"], a["w"])
+            out["ga"] = rn.rmsnorm_bwd(a["dy"], a["x"], a["w"], ra, workspace=wsa)
+        with torch.cuda.stream(s2):
+            out["yb"] = rn.rmsnorm_fwd(b["x"], b["w"])
+            out["gb"] = rn.rmsnorm_bwd(b["dy"], b["x"], b["w"], rb, workspace=wsb)
+    torch.cuda.synchronize()
+    assert cuda_bits_equal(out["ya"][0], ya) and cuda_bits_equal(out["yb"][0], yb)
+    assert cuda_bits_equal(out["ga"][0], dxa) and cuda_bits_equal(out["ga"][1], dwa)
+    assert cuda_bits_equal(out["gb"][0], dxb) and cuda_bits_equal(out["gb"][1], dwb)
+
+
+@pytest.mark.parametrize("dt,N", [("bf16", 8192), ("f32", 4097), ("bf16", 128)])
+def test_workspace_poisoned_clean_and_null(rn, dt, N):
+    M = 1500
+    _, t = dev_inputs(M, N, dt, 94)
+    _, rstd = rn.rmsnorm_fwd(t["x"], t["w"])
+    nb = rn.rmsnorm_bwd_workspace_bytes(M, N, t["x"].dtype)
+    assert nb > 0
+    nan_ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda")   # every fp32 word a NaN
+    zero_ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    dx1, dw1 = rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], rstd, workspace=nan_ws)
+    dx2, dw2 = rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], rstd, workspace=zero_ws)
+    dx3, dw3 = rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], rstd)
+    torch.cuda.synchronize()
+    assert not torch.isnan(dw1.float()).any()
+    assert cuda_bits_equal(dw1, dw2) and cuda_bits_equal(dw1, dw3)
+    assert cuda_bits_equal(dx1, dx2) and cuda_bits_equal(dx1, dx3)
+
+
+@pytest.mark.parametrize("dt,N", [("bf16", 8192), ("bf16", 128), ("f32", 5000), ("bf16", 4097)])
+def test_rows_independent_of_batch_and_split(rn, dt, N):
+    M = 1234
+    _, t = dev_inputs(M, N, dt, 95)
+    y, r = rn.rmsnorm_fwd(t["x"], t["w"])
+    dx, _ = rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], r)
+    cut = 517
+    parts = []
+    for lo, hi in ((0, cut), (cut, M)):
+        yp, rp = rn.rmsnorm_fwd(t["x"][lo:hi], t["w"])
+        dxp, _ = rn.rmsnorm_bwd(t["dy"][lo:hi], t["x"][lo:hi], t["w"], rp)
+        parts.append((yp, rp, dxp))
+    torch.cuda.synchronize()
+    assert cuda_bits_equal(torch.cat([p[0] for p in parts]), y)
+    assert cuda_bits_equal(torch.cat([p[1] for p in parts]), r)
+    assert cuda_bits_equal(torch.cat([p[2] for p in parts]), dx)
+
+
+@pytest.mark.parametrize("dt,N", [("bf16", 4096), ("f32", 2048), ("bf16", 5003)])
+def test_fused_forward_equals_plain_on_rounded_sum(rn, dt, N):
+    M = 700
+    _, t = dev_inputs(M, N, dt, 96, residual=True)
+    ya, h, ra = rn.rmsnorm_add_fwd(t["x"], t["residual"], t["w"])
+    yp, rp = rn.rmsnorm_fwd(h.clone(), t["w"])
+    torch.cuda.synchronize()
+    assert cuda_bits_equal(ya, yp) and cuda_bits_equal(ra, rp)
+
+
+def test_fused_backward_null_dres_equals_zero_buffer(rn):
+    _, t = dev_inputs(800, 8192, "bf16", 97, residual=True)
+    _, h, r = rn.rmsnorm_add_fwd(t["x"], t["residual"], t["w"])
+    dx1, dw1 = rn.rmsnorm_add_bwd(t["dy"], None, h, t["w"], r)
+    dx2, dw2 = rn.rmsnorm_add_bwd(t["dy"], torch.zeros_like(h), h, t["w"], r)
+    dx3, dw3 = rn.rmsnorm_bwd(t["dy"], h, t["w"], r)
+    torch.cuda.synchronize()
+    assert cuda_bits_equal(dx1, dx2) and cuda_bits_equal(dw1, dw2)
+    assert cuda_bits_equal(dx1, dx3) and cuda_bits_equal(dw1, dw3)
+
+
+@pytest.mark.parametrize("dt,N", [("bf16", 8192), ("f32", 257), ("bf16", 64)])
+def test_in_place_aliasing(rn, dt, N):
+    M = 640
+    _, t = dev_inputs(M, N, dt, 98, residual=True, dres=True)
+    y, r = rn.rmsnorm_fwd(t["x"], t["w"])
+    dx, dw = rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], r)
+    xa = t["x"].clone()
+    rn.rmsnorm_fwd(xa, t["w"], y=xa, rstd=torch.empty_like(r))          # y == x
+    dya = t["dy"].clone()
+    rn.rmsnorm_bwd(dya, t["x"], t["w"], r, dx=dya)                      # dx == dy
+    ya, h, ra = rn.rmsnorm_add_fwd(t["x"], t["residual"], t["w"])
+    res = t["residual"].clone()
+    rn.rmsnorm_add_fwd(t["x"], res, t["w"], residual_out=res)           # residual_out == residual
+    dxa, dwa = rn.rmsnorm_add_bwd(t["dy"], t["dres"], h, t["w"], ra)
+    dr = t["dres"].clone()
+    rn.rmsnorm_add_bwd(t["dy"], dr, h, t["w"], ra, dx=dr)               # dx == dresidual_out
+    torch.cuda.synchronize()
+    assert cuda_bits_equal(xa, y) and cuda_bits_equal(dya, dx)
+    assert cuda_bits_equal(res, h) and cuda_bits_equal(dr, dxa)
+
+
+@pytest.mark.parametrize("dt,N", [("bf16", 2048), ("bf16", 4097), ("f32", 130)])
+def test_guard_regions_untouched(rn, dt, N):
+    M, G = 301, 4096
+    d, t = dev_inputs(M, N, dt, 99)
+    td = t["x"].dtype
+
+    def guarded(n):
+        buf = torch.full((G + n + G,), float("nan"), dtype=td, device="cuda")
+        return buf, buf[G:G + n]
+
+    ybuf, y = guarded(M * N)
+    rbuf = torch.full((G + M + G,), float("nan"), device="cuda")
+    r = rbuf[G:G + M]
+    dxbuf, dx = guarded(M * N)
+    dwbuf, dw = guarded(N)
+    rn.rmsnorm_fwd(t["x"], t["w"], y=y.view(M, N), rstd=r)
+    rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], r, dx=dx.view(M, N), dw=dw)
+    torch.cuda.synchronize()
+    for buf, n in ((ybuf, M * N), (rbuf, M), (dxbuf, M * N), (dwbuf, N)):
+        assert torch.isnan(buf[:G].float()).all() and torch.isnan(buf[G + n:].float()).all()
+        assert not torch.isnan(buf[G:G + n].float()).any()
+
+
+def test_zero_rows(rn):
+    x = torch.empty((0, 1024), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(1024, dtype=torch.bfloat16, device="cuda")
+    y, r = rn.rmsnorm_fwd(x, w)
+    assert y.shape == (0, 1024) and r.shape == (0,)
+    dw = torch.full((1024,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rn.rmsnorm_bwd(x, x, w, r, dw=dw)
+    torch.cuda.synchronize()
+    assert (dw.float() == 0).all()          # the empty sum
+
+
+def test_status_codes_on_device(rn):
+    _, t = dev_inputs(64, 2048, "bf16", 100)
+    _, r = rn.rmsnorm_fwd(t["x"], t["w"])
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], r, workspace=small)
+    assert e.value.status == 3
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.rmsnorm_fwd_ex(t["x"], t["w"], force_plan=0)                 # plan too narrow for N
+    assert e.value.status == 2
+
+
+@pytest.mark.parametrize("plan", [7, 10, 11, 12, 16])
+def test_forced_forward_plans_match_oracle(rn, plan):
+    M, N, dt = 777, 8192, "bf16"
+    d, t = dev_inputs(M, N, dt, 101)
+    y, _, r, p = rn.rmsnorm_fwd_ex(t["x"], t["w"], force_plan=plan)
+    assert p["plan_id"] == plan
+    f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0)
+    torch.cuda.synchronize()
+    from helpers import check_rstd, check_y
+    check_y(to_host(y, dt), f, dt)
+    check_rstd(r.cpu().numpy(), f["rstd64"])
+
+
+@pytest.mark.parametrize("plan", [27, 29, 31, 36])
+def test_forced_backward_plans_match_oracle(rn, plan):
+    M, N, dt = 777, 8192, "bf16"
+    d, t = dev_inputs(M, N, dt, 102)
+    f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0)
+    r = torch.from_numpy(f["rstd32"]).cuda()
+    dx, dw, p = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], r, force_plan=plan, force_ctas=100)
+    assert p["plan_id"] == plan and p["ctas"] == 100
+    b = oracle.bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0, rstd=f["rstd32"])
+    torch.cuda.synchronize()
+    check_dx(to_host(dx, dt), b, dt)
+    check_dw(to_host(dw, dt), b, dt)
