@@ -1,0 +1,416 @@
+"""RMSNorm forward + backward benchmark on GB300.
+
+One step = rmsnorm_fwd then rmsnorm_bwd (main kernel + dW finalizer) over a
+bf16 16384 x 8192 activation matrix (llama mode, eps 1e-6, offset 0, 1%
+outlier columns), inputs resident in HBM. The metric is achieved HBM
+bandwidth: algorithmic bytes (every tensor read and written, including the
+backward's fp32 workspace, written then read) per step / step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0. Under torchrun each rank runs the same
+workload on its own GPU (independent batches, no collective on the data
+path): weak scaling, value = bytes of all ranks / max time over ranks.
+`--impl reference` times the CPU oracle (fp64 C, all host cores) on a
+bounded row sample of the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "wide_bf16_16384x8192"
+METRIC = "RMSNorm fwd/bwd achieved HBM GB/s (% of GB300 peak) and us/call, bf16 16384x8192"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- helpers --
+
+def bytes_fwd(M, N, s):
+    return 2 * M * N * s + N * s + 4 * M
+
+
+def bytes_bwd_main(M, N, s, P):
+    return 3 * M * N * s + N * s + 4 * M + 4 * P * N
+
+
+def bytes_bwd_finalize(N, s, P):
+    return 4 * P * N + N * s
+
+
+def bytes_bwd(M, N, s, P):
+    return 3 * M * N * s + 2 * N * s + 4 * M + 8 * P * N
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "row_wise_normalization_rmsnorm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    k = d.get("kernels", {}).get(kernel_key)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, enabled=True):
+        self.index, self.proc, self.enabled = index, None, enabled
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        if not self.enabled:
+            return self
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        except OSError:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU legs --
+
+def oracle_sample(arrays, p, rows, nthreads):
+    import oracle
+    x = arrays["x"][:rows]
+    dy = arrays["dy"][:rows]
+    t0 = time.perf_counter()
+    f = oracle.fwd(x, arrays["w"], dtype=p["dtype"], eps=p["eps"], offset=p["offset"], nthreads=nthreads)
+    oracle.bwd(dy, x, arrays["w"], dtype=p["dtype"], eps=p["eps"], offset=p["offset"], rstd=f["rstd32"],
+               nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(arrays, p, target_s=8.0):
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    M, N = arrays["x"].shape
+    s = 2 if p["dtype"] == "bf16" else 4
+    t = oracle_sample(arrays, p, 64, cores)
+    rows = int(min(M, max(64, 64 * target_s / max(t, 1e-3))))
+    rows = max(cores, rows // cores * cores)
+    t = oracle_sample(arrays, p, rows, cores)
+    by = bytes_fwd(rows, N, s) + bytes_bwd(rows, N, s, 0)
+    return {"value": by / t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} of {M} rows of the workload, fwd + bwd, fp64 C oracle, "
+                      f"row-parallel on {cores} threads, {t:.2f} s wall"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from row_wise_normalization_rmsnorm_gb300 import inputs
+    import oracle
+    oracle.build()
+    arrays, p = inputs.workload_inputs(WORKLOAD)
+    M, N = arrays["x"].shape
+    s = 2
+    cores = os.cpu_count() or 1
+    t1 = oracle_sample(arrays, p, cores, cores)
+    # rows per step so that warmup + steps end within about a minute
+    per_row = t1 / cores
+    rows = int(max(1, min(512, 60.0 / max(1, args.steps + args.warmup) / max(per_row, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_sample(arrays, p, rows, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(arrays, p, rows, cores)
+    dt = time.perf_counter() - t0
+    by = (bytes_fwd(rows, N, s) + bytes_bwd(rows, N, s, 0)) * args.steps
+    val = by / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"rmsnorm fwd+bwd bf16 M={M} N={N} (row sample of {rows} rows per step)",
+                   "M": M, "N": N, "rows_per_step": rows, "eps": p["eps"], "offset": p["offset"]},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} rows per step of the {M}x{N} workload, fwd+bwd, fp64 C oracle"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------- GPU arm --
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from row_wise_normalization_rmsnorm_gb300 import build as rn_build
+    rn_build.build()
+    import row_wise_normalization_rmsnorm_gb300 as rn
+    from row_wise_normalization_rmsnorm_gb300 import inputs
+
+    arrays, p = inputs.workload_inputs(WORKLOAD)
+    M, N, eps = p["M"], p["N"], p["eps"]
+    s = 2
+
+    def up(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x, dy, w = up(arrays["x"]), up(arrays["dy"]), up(arrays["w"])
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(w)
+    rstd = torch.empty(M, dtype=torch.float32, device=dev)
+    ws_bytes = rn.rmsnorm_bwd_workspace_bytes(M, N, torch.bfloat16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    _, _, _, fplan = rn.rmsnorm_fwd_ex(x, w, y=y, rstd=rstd, eps=eps)
+    _, _, bplan = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dx=dx, dw=dw, workspace=ws, eps=eps)
+    P = bplan["ctas"]
+
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    # torch creates an event on its first record(); the library records the
+    # mid-backward event itself, so materialise every handle up front
+    for e in ev:
+        for q in e:
+            q.record(stream)
+    torch.cuda.synchronize()
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        rn.rmsnorm_fwd(x, w, y=y, rstd=rstd, eps=eps)
+        if e is not None:
+            e[1].record(stream)
+        rn.rmsnorm_bwd_ex(dy, x, w, rstd, dx=dx, dw=dw, workspace=ws, eps=eps,
+                          event_after_main=None if e is None else e[2])
+        if e is not None:
+            e[3].record(stream)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local, enabled=not args.no_clocks) as clk:
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        start.record(stream)
+        for i in range(K):
+            step(ev[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    t_fwd = [e[0].elapsed_time(e[1]) for e in ev]
+    t_main = [e[1].elapsed_time(e[2]) for e in ev]
+    t_fin = [e[2].elapsed_time(e[3]) for e in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    step_bytes = bytes_fwd(M, N, s) + bytes_bwd(M, N, s, P)
+    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+    peak, peak_kind = peaks()
+    comp = {}
+    for name, ts, by in (("fwd", t_fwd, bytes_fwd(M, N, s)),
+                         ("bwd_main", t_main, bytes_bwd_main(M, N, s, P)),
+                         ("bwd_finalize", t_fin, bytes_bwd_finalize(N, s, P))):
+        avg = sum(ts) / len(ts)
+        comp[name] = {"us": avg * 1e3, "median_us": statistics.median(ts) * 1e3, "bytes": by,
+                      "gbs": by / (avg * 1e-3) / 1e9, "frac_of_peak": by / (avg * 1e-3) / 1e9 / peak}
+    comp["bwd"] = {"us": comp["bwd_main"]["us"] + comp["bwd_finalize"]["us"], "bytes": bytes_bwd(M, N, s, P)}
+    comp["bwd"]["gbs"] = comp["bwd"]["bytes"] / (comp["bwd"]["us"] * 1e-6) / 1e9
+    comp["bwd"]["frac_of_peak"] = comp["bwd"]["gbs"] / peak
+    dom = max(("fwd", "bwd_main", "bwd_finalize"), key=lambda k: comp[k]["us"])
+    kname = {"fwd": "rmsnorm_fwd_vector", "bwd_main": "rmsnorm_bwd_vector",
+             "bwd_finalize": "rmsnorm_dw_finalize"}[dom]
+    roof = {"kernel": kname, "bound": "hbm", "achieved": comp[dom]["gbs"], "peak": peak, "unit": "GB/s",
+            "frac": comp[dom]["gbs"] / peak, "traffic": ncu_traffic(dom), "peak_source": peak_kind,
+            "bytes_per_launch": comp[dom]["bytes"]}
+
+    # end to end: pinned host buffers, copies inside the timed region
+    h_x = torch.empty_like(x, device="cpu").pin_memory()
+    h_dy = torch.empty_like(dy, device="cpu").pin_memory()
+    h_w = torch.empty_like(w, device="cpu").pin_memory()
+    h_x.copy_(x.cpu())
+    h_dy.copy_(dy.cpu())
+    h_w.copy_(w.cpu())
+    o_y = torch.empty_like(y, device="cpu").pin_memory()
+    o_dx = torch.empty_like(dx, device="cpu").pin_memory()
+    o_dw = torch.empty_like(dw, device="cpu").pin_memory()
+    o_r = torch.empty_like(rstd, device="cpu").pin_memory()
+    d_x, d_dy, d_w = torch.empty_like(x), torch.empty_like(dy), torch.empty_like(w)
+
+    def e2e_step():
+        d_x.copy_(h_x, non_blocking=True)
+        d_dy.copy_(h_dy, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        rn.rmsnorm_fwd(d_x, d_w, y=y, rstd=rstd, eps=eps)
+        rn.rmsnorm_bwd(d_dy, d_x, d_w, rstd, dx=dx, dw=dw, workspace=ws, eps=eps)
+        o_y.copy_(y, non_blocking=True)
+        o_r.copy_(rstd, non_blocking=True)
+        o_dx.copy_(dx, non_blocking=True)
+        o_dw.copy_(dw, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = (h_x.numel() + h_dy.numel() + h_w.numel()) * s
+    d2h = (o_y.numel() + o_dx.numel() + o_dw.numel()) * s + o_r.numel() * 4
+    e2e = {"value": step_bytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"rmsnorm fwd+bwd bf16 M={M} N={N}, llama mode eps=1e-6 offset=0, "
+                               f"1% outlier columns x20", "M": M, "N": N, "per_rank_rows": M,
+                   "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": "inputs larger than L2 (268 MB per tensor, 126 MB L2); no flush",
+                   "fwd_plan": fplan["plan_id"], "bwd_plan": bplan["plan_id"], "bwd_ctas": P,
+                   "workspace_bytes": ws_bytes},
+        "frac_of_peak": value / world / peak,
+        "components": comp,
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(arrays, p)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

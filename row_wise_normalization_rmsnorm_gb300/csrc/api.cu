@@ -260,6 +260,8 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (dt != RMSNORM_F32 && dt != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
+    // An empty batch reads and writes nothing; its (empty) tensors may be NULL.
+    if (M == 0) return RMSNORM_SUCCESS;
     const bool fused = residual != nullptr || residual_out != nullptr;
     if (fused && (!residual || !residual_out)) return RMSNORM_ERR_INVALID_ARG;
     if (!x || !w || !y || !rstd) return RMSNORM_ERR_INVALID_ARG;
@@ -267,7 +269,6 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (!aligned_to(x, s) || !aligned_to(w, s) || !aligned_to(y, s) || !aligned_to(rstd, 4))
         return RMSNORM_ERR_INVALID_ARG;
     if (fused && (!aligned_to(residual, s) || !aligned_to(residual_out, s))) return RMSNORM_ERR_INVALID_ARG;
-    if (M == 0) return RMSNORM_SUCCESS;
 
     bool aligned = aligned_to(x, 16) && aligned_to(w, 16) && aligned_to(y, 16);
     if (fused) aligned = aligned && aligned_to(residual, 16) && aligned_to(residual_out, 16);
@@ -308,19 +309,20 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
     if (force_packed < -1 || force_packed > 1) return RMSNORM_ERR_INVALID_ARG;
-    if (!dy || !x || !w || !rstd || !dx || !dw) return RMSNORM_ERR_INVALID_ARG;
     if (!fused) dres = nullptr;
     const uintptr_t s = (uintptr_t)elem_size(dt);
-    if (!aligned_to(dy, s) || !aligned_to(x, s) || !aligned_to(w, s) || !aligned_to(dx, s) ||
-        !aligned_to(dw, s) || !aligned_to(rstd, 4) || (dres && !aligned_to(dres, s)))
-        return RMSNORM_ERR_INVALID_ARG;
-    if (workspace && !aligned_to(workspace, 16)) return RMSNORM_ERR_WORKSPACE;
     if (M == 0) {
-        // dw is the empty sum
+        // dw is the empty sum; the empty [0, N] tensors may be NULL
+        if (!dw || !aligned_to(dw, s)) return RMSNORM_ERR_INVALID_ARG;
         cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)N * s, stream);
         if (e != cudaSuccess) return cuda_fail(e);
         return RMSNORM_SUCCESS;
     }
+    if (!dy || !x || !w || !rstd || !dx || !dw) return RMSNORM_ERR_INVALID_ARG;
+    if (!aligned_to(dy, s) || !aligned_to(x, s) || !aligned_to(w, s) || !aligned_to(dx, s) ||
+        !aligned_to(dw, s) || !aligned_to(rstd, 4) || (dres && !aligned_to(dres, s)))
+        return RMSNORM_ERR_INVALID_ARG;
+    if (workspace && !aligned_to(workspace, 16)) return RMSNORM_ERR_WORKSPACE;
     bool aligned = aligned_to(dy, 16) && aligned_to(x, 16) && aligned_to(w, 16) && aligned_to(dx, 16);
     if (dres) aligned = aligned && aligned_to(dres, 16);
 
