@@ -133,6 +133,32 @@ rmsnorm_status_t rmsnorm_add_bwd(const void *dy, const void *dresidual_out, cons
                                  float eps, float offset, rmsnorm_stream_t stream);
 
 /*
+ * Backward without any allocation, for callers that cannot allocate device
+ * memory when they call (an engine that reserves all device memory at
+ * start-up, a plug-in host that passes its ops no workspace, code running
+ * while a global-mode stream capture forbids cudaMalloc). The pages have no
+ * counterpart to this entry point.
+ * Same arguments and results as rmsnorm_bwd, but the dW partial rows live
+ * in a fixed array inside the library, RMSNORM_NOALLOC_SCRATCH_BYTES per
+ * GPU, held from the time the library's kernels load on that GPU until the
+ * process exits. Returns RMSNORM_ERR_WORKSPACE, launching nothing, when the
+ * workspace this call needs (at most rmsnorm_bwd_workspace_bytes(M, N, dt))
+ * exceeds that size.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call on a device uses the same array and leaves its partial rows
+ * there; nothing needs clearing, because each call writes every partial it
+ * reads. Calls that can overlap on the GPU (other streams, other threads)
+ * race on the array: serialise them.
+ */
+rmsnorm_status_t rmsnorm_bwd_noalloc(const void *dy, const void *x, const void *w,
+                                     const float *rstd, void *dx, void *dw,
+                                     int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                                     float eps, float offset, rmsnorm_stream_t stream);
+
+#define RMSNORM_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+
+/*
  * Bytes of workspace the backward needs for (M, N, dt) on the current
  * device: (number of persistent CTAs) * N * 4, rounded up to 256 (FlyDSL
  * PR #855, Runtime configuration and ownership). Returns 0 for M == 0 and

@@ -65,6 +65,7 @@ SIGNATURES = {
     "rmsnorm_add_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp]),
     "rmsnorm_add_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i, _f, _f, _vp]),
     "rmsnorm_bwd_workspace_bytes": (_sz, [_i64, _i64, _i]),
+    "rmsnorm_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp]),
     "rmsnorm_plan_query": (_i, [_i, _i64, _i64, _i, _i, _i, _i, _i, _i, _PPlan]),
     "rmsnorm_plan_count": (_i, []),
     "rmsnorm_plan_id_at": (_i, [_i]),

@@ -24,7 +24,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librmsnorm_gb300.so")
 HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
 
-SOURCES = ["api.cu", "fwd_kernels.cu", "bwd_bf16.cu", "bwd_f32.cu"]
+SOURCES = ["api.cu", "fwd_kernels.cu", "bwd_bf16.cu", "bwd_f32.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "plans.h", "bwd_kernels.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -133,6 +133,8 @@ static rmsnorm_status_t cuda_fail(cudaError_t e) {
     return RMSNORM_ERR_CUDA;
 }
 
+void set_last_cuda_error(int e) { g_last_cuda_error = e; }
+
 constexpr int kMaxDevices = 64;
 static std::atomic<int> g_sm_count[kMaxDevices];
 

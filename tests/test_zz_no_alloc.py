@@ -1,0 +1,62 @@
+"""rmsnorm_bwd_noalloc: the backward for callers that cannot allocate device
+memory when they call (engines that reserve all memory up front, plug-in
+hosts that give an op no workspace, code running under a global-mode stream
+capture). It keeps the dW partial rows in a fixed array inside the library.
+
+Called through the C ABI, twice in a row on different inputs, its dx and dw
+must agree with rmsnorm_bwd (which gets its own workspace) within the
+tolerances the parity tests use: dx within 1 bf16 ulp, dw within 4e-3
+relative. A size whose workspace exceeds the array must be refused without
+a launch. This file sorts last so that a run stopping at the first failure
+has already run every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_ulp_distance, to_dev, to_host
+from row_wise_normalization_rmsnorm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rn():
+    from row_wise_normalization_rmsnorm_gb300 import build
+    build.build()
+    import row_wise_normalization_rmsnorm_gb300 as pkg
+    return pkg
+
+
+def test_noalloc_backward_matches_rmsnorm_bwd_on_two_calls(rn):
+    L = rn.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    for M, N, seed in ((4096, 8192, 301), (1000, 2048, 302)):
+        d = inputs.make_inputs(M, N, "bf16", seed)
+        x, dy, w = (to_dev(d[k], "bf16") for k in ("x", "dy", "w"))
+        _, rstd = rn.rmsnorm_fwd(x, w)
+        dx_ref, dw_ref = rn.rmsnorm_bwd(dy, x, w, rstd)
+        dx = torch.full_like(x, float("nan"))
+        dw = torch.full_like(w, float("nan"))
+        st = L.rmsnorm_bwd_noalloc(dy.data_ptr(), x.data_ptr(), w.data_ptr(), rstd.data_ptr(), dx.data_ptr(),
+                                   dw.data_ptr(), M, N, 1, 1e-6, 0.0, stream)
+        assert st == 0, rn.lib().rmsnorm_status_string(st)
+        torch.cuda.synchronize()
+        assert bf16_ulp_distance(to_host(dx, "bf16"), to_host(dx_ref, "bf16")).max() <= 1
+        a = dw.float().cpu().numpy().astype(np.float64)
+        b = dw_ref.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(a))
+        assert np.all(np.abs(a - b) <= 4e-3 * np.abs(b) + 1e-6)
+
+
+def test_noalloc_refuses_sizes_beyond_its_array(rn):
+    L = rn.lib()
+    limit = 32 << 20
+    M, N = 1 << 20, 65536
+    assert rn.rmsnorm_bwd_workspace_bytes(M, N, torch.bfloat16) > limit
+    t = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    r = torch.zeros(16, dtype=torch.float32, device="cuda")
+    st = L.rmsnorm_bwd_noalloc(t.data_ptr(), t.data_ptr(), t.data_ptr(), r.data_ptr(), t.data_ptr(),
+                               t.data_ptr(), M, N, 1, 1e-6, 0.0, torch.cuda.current_stream().cuda_stream)
+    assert st == 3          # RMSNORM_ERR_WORKSPACE, nothing launched
+    torch.cuda.synchronize()
