@@ -67,7 +67,7 @@ def _load():
                                                vp, vp, vp, vp, vp, i32]
             lib.oracle_rmsnorm_bwd.restype = i32
             lib.oracle_rmsnorm_bwd.argtypes = [i32, i64, i64, vp, vp, vp, vp, vp, dbl, dbl,
-                                               vp, vp, vp, vp, vp, vp, i32]
+                                               vp, vp, vp, vp, vp, vp, vp, i32]
             lib.oracle_bf16_round_array.restype = i32
             lib.oracle_bf16_round_array.argtypes = [vp, i64, vp]
             lib.oracle_bf16_decode.restype = dbl
@@ -151,8 +151,9 @@ def bwd(dy, h, w, *, dtype, eps, offset, rstd=None, dres=None, want_dx=True, nth
     produced (no M x N outputs).
 
     Returns a dict with ``dx`` (storage type), ``dx64``, ``dx_scale``
-    (rstd (|g| + |xhat c|) [+ |dres|]), ``dw64``, ``dw_abs`` (sum |dy xhat|)
-    and ``dw`` (storage type).
+    (rstd (|g| + |xhat c|) [+ |dres|]), ``dx_cscale`` (rstd |xhat| (1/N)
+    sum |g xhat|, the sensitivity of dx to rounding in the sum behind c),
+    ``dw64``, ``dw_abs`` (sum |dy xhat|) and ``dw`` (storage type).
     """
     dy = _as_storage(dy, dtype)
     M, N = dy.shape
@@ -167,13 +168,14 @@ def bwd(dy, h, w, *, dtype, eps, offset, rstd=None, dres=None, want_dx=True, nth
     dx = np.empty((M, N), dtype=st) if want_dx else None
     dx64 = np.empty((M, N), dtype=np.float64) if want_dx else None
     dxs = np.empty((M, N), dtype=np.float64) if want_dx else None
+    dxc = np.empty((M, N), dtype=np.float64) if want_dx else None
     dw64 = np.empty((N,), dtype=np.float64)
     dwa = np.empty((N,), dtype=np.float64)
     dw = np.empty((N,), dtype=st)
     bad = _load().oracle_rmsnorm_bwd(_DTYPE_CODE[dtype], M, N, _ptr(dy), _ptr(h), _ptr(w),
                                      _ptr(rstd), _ptr(dres), float(eps), float(offset),
-                                     _ptr(dx), _ptr(dx64), _ptr(dxs), _ptr(dw64), _ptr(dwa),
+                                     _ptr(dx), _ptr(dx64), _ptr(dxs), _ptr(dxc), _ptr(dw64), _ptr(dwa),
                                      _ptr(dw), int(nthreads))
     if bad:
         raise FloatingPointError(f"oracle bwd: {bad} non-finite or overflowing stores")
-    return {"dx": dx, "dx64": dx64, "dx_scale": dxs, "dw64": dw64, "dw_abs": dwa, "dw": dw}
+    return {"dx": dx, "dx64": dx64, "dx_scale": dxs, "dx_cscale": dxc, "dw64": dw64, "dw_abs": dwa, "dw": dw}

@@ -236,7 +236,7 @@ typedef struct {
     const float *rstd_in;
     double eps, offset;
     void *dx;
-    double *dx64, *dx_scale;
+    double *dx64, *dx_scale, *dx_cscale;
     double *dw, *dw_abs;   /* this job's own partial sums, length N */
     int bad;
 } bwd_job;
@@ -258,13 +258,15 @@ static void bwd_rows(bwd_job *jb)
             for (int64_t j = 0; j < N; ++j) ss += hv[j] * hv[j];
             rstd = 1.0 / sqrt(ss / (double)N + jb->eps);
         }
-        /* c = (1/N) sum_j g_j xhat_j */
-        double c = 0.0;
+        /* c = (1/N) sum_j g_j xhat_j; cabs = (1/N) sum_j |g_j xhat_j| */
+        double c = 0.0, cabs = 0.0;
         for (int64_t j = 0; j < N; ++j) {
             const double g = load_elem(jb->dtype, jb->dy, base + j) * wpo[j];
             c += g * (hv[j] * rstd);
+            cabs += fabs(g * (hv[j] * rstd));
         }
         c /= (double)N;
+        cabs /= (double)N;
         for (int64_t j = 0; j < N; ++j) {
             const double dyj = load_elem(jb->dtype, jb->dy, base + j);
             const double xhat = hv[j] * rstd;
@@ -278,6 +280,7 @@ static void bwd_rows(bwd_job *jb)
             }
             if (jb->dx64) jb->dx64[base + j] = dxj;
             if (jb->dx_scale) jb->dx_scale[base + j] = scale;
+            if (jb->dx_cscale) jb->dx_cscale[base + j] = rstd * fabs(xhat) * cabs;
             if (jb->dx) jb->bad |= store_elem(jb->dtype, jb->dx, base + j, dxj);
             jb->dw[j] += dyj * xhat;
             jb->dw_abs[j] += fabs(dyj * xhat);
@@ -301,6 +304,10 @@ static void *bwd_thread(void *arg) { bwd_rows((bwd_job *)arg); return NULL; }
  *   dx64     unrounded dx
  *   dx_scale rstd (|g| + |xhat c|) [+ |dres|]: the magnitude of the terms
  *            whose difference is dx, used to bound cancellation error
+ *   dx_cscale rstd |xhat| (1/N) sum_j |g_j xhat_j|: how far dx moves per
+ *            unit relative error of the terms summed into c (a sum of
+ *            g xhat can cancel, so its rounding error scales with the sum
+ *            of magnitudes, not with |c|)
  *   dw64     sum over rows of dy * xhat (length N)
  *   dw_abs   sum over rows of |dy * xhat| (length N)
  *   dw       R(dw64) in the storage type
@@ -312,7 +319,7 @@ int oracle_rmsnorm_bwd(int dtype, int64_t M, int64_t N,
                        const void *dy, const void *h, const void *w,
                        const float *rstd_in, const void *dres,
                        double eps, double offset,
-                       void *dx, double *dx64, double *dx_scale,
+                       void *dx, double *dx64, double *dx_scale, double *dx_cscale,
                        double *dw64, double *dw_abs, void *dw, int nthreads)
 {
     if (nthreads < 1) nthreads = 1;
@@ -325,7 +332,7 @@ int oracle_rmsnorm_bwd(int dtype, int64_t M, int64_t N,
         jb->row0 = M * t / nthreads; jb->row1 = M * (t + 1) / nthreads;
         jb->dy = dy; jb->h = h; jb->w = w; jb->dres = dres; jb->rstd_in = rstd_in;
         jb->eps = eps; jb->offset = offset;
-        jb->dx = dx; jb->dx64 = dx64; jb->dx_scale = dx_scale;
+        jb->dx = dx; jb->dx64 = dx64; jb->dx_scale = dx_scale; jb->dx_cscale = dx_cscale;
         jb->dw = (double *)calloc((size_t)N, sizeof(double));
         jb->dw_abs = (double *)calloc((size_t)N, sizeof(double));
     }

@@ -23,11 +23,11 @@
 namespace rmsn {
 
 struct PlanDesc {
-    int id, op, path, tpr, v, teams, cmin, cmax;
+    int id, op, path, tpr, v, teams, depth, cmin, cmax;
 };
 
 static const PlanDesc kPlans[] = {
-#define RMSN_DESC(id, op, path, tpr, v, teams, cmin, cmax) {id, op, path, tpr, v, teams, cmin, cmax},
+#define RMSN_DESC(id, op, path, tpr, v, teams, depth, cmin, cmax) {id, op, path, tpr, v, teams, depth, cmin, cmax},
     RMSNORM_PLAN_TABLE(RMSN_DESC)
 #undef RMSN_DESC
 };

@@ -28,23 +28,49 @@
 
 namespace rmsn {
 
-template <typename T, int TPR, int V, int TEAMS, bool PACKED, bool FUSED>
+// x, dy (and dres) chunks of one row, and its rstd, into registers. Rows
+// past M are clamped to the last row (their results are masked later), so
+// every thread of the CTA keeps taking part in the reductions.
+template <typename T, int TPR, int V>
+__device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, int C, int t, bool has_dres,
+                                             uint4 (&x)[V], uint4 (&d)[V], uint4 (&r)[V], float &rs) {
+    const int64_t rr = row < p.M ? row : p.M - 1;
+    const int64_t base = rr * C;
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x) + base;
+    const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dy) + base;
+    const uint4 *r4 = reinterpret_cast<const uint4 *>(p.dres) + base;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * TPR + t;
+        const bool in = c < C;
+        x[v] = in ? ld_stream(x4 + c) : make_uint4(0, 0, 0, 0);
+        d[v] = in ? ld_stream(d4 + c) : make_uint4(0, 0, 0, 0);
+        r[v] = (has_dres && in) ? ld_stream(r4 + c) : make_uint4(0, 0, 0, 0);
+    }
+    rs = p.rstd[rr];
+}
+
+// Persistent main kernel. Rows are software-pipelined through a register
+// ring of D + 1 slots: while row k is reduced and written, the loads of rows
+// k+1 .. k+D are already in flight, so the SM keeps memory requests
+// outstanding across the reduction barrier and the stores. Each row's x and
+// dy stay in registers across both passes.
+template <typename T, int TPR, int V, int TEAMS, int D, bool PACKED, bool FUSED>
 __global__ void __launch_bounds__(TPR *TEAMS)
     rmsnorm_bwd_vector(const BwdParams p) {
     using Pk = Pair<PACKED>;
     constexpr int E = Elem<T>::E;
     constexpr int NP = Elem<T>::NP;
     constexpr int W = TPR > 32 ? TPR / 32 : 1;
-    __shared__ float red[2][TEAMS][W];       // double-buffered: one barrier per row
-    extern __shared__ float4 comb_smem[];    // (TEAMS - 1) * N floats
+    constexpr int B = D + 1;              // ring slots
+    constexpr int BR = FUSED ? B : 1;     // dres slots
+    __shared__ float red[2][TEAMS][W];    // double-buffered: one barrier per row
+    extern __shared__ float4 comb_smem[]; // (TEAMS - 1) * N floats
 
     const int team = threadIdx.x / TPR;
     const int t = threadIdx.x % TPR;
     const int N = p.N;
     const int C = N / E;
-    const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x);
-    const uint4 *dy4 = reinterpret_cast<const uint4 *>(p.dy);
-    const uint4 *dr4 = reinterpret_cast<const uint4 *>(p.dres);
     uint4 *dx4 = reinterpret_cast<uint4 *>(p.dx);
     const bool has_dres = FUSED && p.dres != nullptr;
 
@@ -67,27 +93,18 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     // team 0, which has the lowest first row) so the CTA-wide barrier in the
     // reduction is reached by all threads; rows past M are masked.
     const int64_t G = (int64_t)gridDim.x * TEAMS;
-    const int64_t first = (int64_t)blockIdx.x * TEAMS;
-    const int64_t iters = (p.M - first + G - 1) / G;
-    for (int64_t i = 0; i < iters; ++i) {
-        const int64_t row = first + team + i * G;
+    const int64_t first = (int64_t)blockIdx.x * TEAMS + team;
+    const int64_t iters = (p.M - (int64_t)blockIdx.x * TEAMS + G - 1) / G;
+
+    uint4 xb[B][V], db[B][V], rb[BR][V];
+    float rs[B];
+
+    auto process = [&](uint4 (&xv)[V], uint4 (&dv)[V], uint4 (&rv)[V], float r, int64_t k) {
+        const int64_t row = first + k * G;
         const bool valid = row < p.M;
-        const int64_t rr = valid ? row : p.M - 1;
-        const int64_t base = rr * C;
-
-        uint4 xv[V], dv[V], rv[V];
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-            const int c = v * TPR + t;
-            const bool in = c < C;
-            xv[v] = in ? ld_stream(x4 + base + c) : make_uint4(0, 0, 0, 0);
-            dv[v] = in ? ld_stream(dy4 + base + c) : make_uint4(0, 0, 0, 0);
-            rv[v] = (has_dres && in) ? ld_stream(dr4 + base + c) : make_uint4(0, 0, 0, 0);
-        }
-        const float r = p.rstd[rr];
         const float2 r2 = make_float2(r, r);
-
-        // pass 1: dot = sum g * xhat (even and odd columns in separate lanes)
+        // pass 1: sum of g * x (g = dy (offset + w)); even and odd columns
+        // accumulate in separate lanes and are folded before the reduction
         float2 dot = make_float2(0.f, 0.f);
 #pragma unroll
         for (int v = 0; v < V; ++v) {
@@ -95,13 +112,14 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             unpack<T>(xv[v], xf);
             unpack<T>(dv[v], df);
 #pragma unroll
-            for (int k = 0; k < NP; ++k) dot = Pk::fma(Pk::mul(df[k], wp[v][k]), Pk::mul(xf[k], r2), dot);
+            for (int q = 0; q < NP; ++q) dot = Pk::fma(Pk::mul(df[q], wp[v][q]), xf[q], dot);
         }
-        const float s = team_allreduce<TPR>(__fadd_rn(dot.x, dot.y), &red[i & 1][team][0], t);
-        const float cm = -__fdiv_rn(s, (float)N);
+        const float s = team_allreduce<TPR>(__fadd_rn(dot.x, dot.y), &red[k & 1][team][0], t);
+        // c = (1/N) sum g xhat = rstd * (sum g x) / N
+        const float cm = -__fdiv_rn(__fmul_rn(s, r), (float)N);
         const float2 nc2 = make_float2(cm, cm);
-
-        // pass 2: dx from the registers, dW partial in registers
+        // pass 2: dx = rstd (g - xhat c) [+ dres], stored directly; dW partial
+        const int64_t base = (valid ? row : p.M - 1) * C;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = v * TPR + t;
@@ -109,19 +127,39 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             unpack<T>(xv[v], xf);
             unpack<T>(dv[v], df);
 #pragma unroll
-            for (int k = 0; k < NP; ++k) {
-                const float2 xh = Pk::mul(xf[k], r2);
-                const float2 g = Pk::mul(df[k], wp[v][k]);
-                out[k] = Pk::mul(Pk::fma(xh, nc2, g), r2);
-                if (valid) acc[v][k] = Pk::fma(df[k], xh, acc[v][k]);
+            for (int q = 0; q < NP; ++q) {
+                const float2 xh = Pk::mul(xf[q], r2);
+                const float2 g = Pk::mul(df[q], wp[v][q]);
+                out[q] = Pk::mul(Pk::fma(xh, nc2, g), r2);
+                if (valid) acc[v][q] = Pk::fma(df[q], xh, acc[v][q]);
             }
             if (has_dres) {
                 float2 rf[NP];
                 unpack<T>(rv[v], rf);
 #pragma unroll
-                for (int k = 0; k < NP; ++k) out[k] = Pk::add(out[k], rf[k]);
+                for (int q = 0; q < NP; ++q) out[q] = Pk::add(out[q], rf[q]);
             }
             if (valid && c < C) st_chunk(dx4 + base + c, pack<T>(out));
+        }
+    };
+
+    // prologue: rows 0 .. D-1 into slots 0 .. D-1
+#pragma unroll
+    for (int s = 0; s < D; ++s)
+        if (s < iters) bwd_load_row<T, TPR, V>(p, first + s * G, C, t, has_dres, xb[s], db[s], rb[FUSED ? s : 0], rs[s]);
+
+    for (int64_t k0 = 0; k0 < iters; k0 += B) {
+#pragma unroll
+        for (int s = 0; s < B; ++s) {
+            const int64_t k = k0 + s;
+            if (k < iters) {
+                // slot (s + D) % B held row k - 1, already done: refill it with row k + D
+                        const int sn = (s + D) % B;
+                if (k + D < iters)
+                    bwd_load_row<T, TPR, V>(p, first + (k + D) * G, C, t, has_dres, xb[sn], db[sn],
+                                            rb[FUSED ? sn : 0], rs[sn]);
+                process(xb[s], db[s], rb[FUSED ? s : 0], rs[s], k);
+            }
         }
     }
 
@@ -136,9 +174,9 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                 if (c < C) {
                     float *d = comb + (int64_t)(team - 1) * N + c * E;
 #pragma unroll
-                    for (int k = 0; k < NP; ++k) {
-                        d[2 * k] = acc[v][k].x;
-                        d[2 * k + 1] = acc[v][k].y;
+                    for (int q = 0; q < NP; ++q) {
+                        d[2 * q] = acc[v][q].x;
+                        d[2 * q + 1] = acc[v][q].y;
                     }
                 }
             }
@@ -152,8 +190,8 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                 for (int tm = 1; tm < TEAMS; ++tm) {
                     const float *s2 = comb + (int64_t)(tm - 1) * N + c * E;
 #pragma unroll
-                    for (int k = 0; k < NP; ++k)
-                        acc[v][k] = Pk::add(acc[v][k], make_float2(s2[2 * k], s2[2 * k + 1]));
+                    for (int q = 0; q < NP; ++q)
+                        acc[v][q] = Pk::add(acc[v][q], make_float2(s2[2 * q], s2[2 * q + 1]));
                 }
             }
         }
@@ -237,16 +275,16 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int 
 
 // ------------------------------------------------------------- dispatch --
 
-template <typename T, int TPR, int V, int TEAMS, bool PACKED>
+template <typename T, int TPR, int V, int TEAMS, int D, bool PACKED>
 static int bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     if (fused)
-        rmsnorm_bwd_vector<T, TPR, V, TEAMS, PACKED, true><<<grid, TPR * TEAMS, smem, s>>>(p);
+        rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, PACKED, true><<<grid, TPR * TEAMS, smem, s>>>(p);
     else
-        rmsnorm_bwd_vector<T, TPR, V, TEAMS, PACKED, false><<<grid, TPR * TEAMS, smem, s>>>(p);
+        rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, PACKED, false><<<grid, TPR * TEAMS, smem, s>>>(p);
     return (int)cudaGetLastError();
 }
 
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS>
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D>
 static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     if constexpr (OP != OP_BWD) {
         return (int)cudaErrorInvalidValue;
@@ -257,14 +295,14 @@ static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int gri
             rmsnorm_bwd_generic<T, false><<<grid, 256, 0, s>>>(p);
         return (int)cudaGetLastError();
     } else if constexpr (PATH == PATH_VECTOR) {
-        return packed ? bwd_launch_vec<T, TPR, V, TEAMS, true>(fused, p, grid, smem, s)
-                      : bwd_launch_vec<T, TPR, V, TEAMS, false>(fused, p, grid, smem, s);
+        return packed ? bwd_launch_vec<T, TPR, V, TEAMS, D, true>(fused, p, grid, smem, s)
+                      : bwd_launch_vec<T, TPR, V, TEAMS, D, false>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
 }
 
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS>
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D>
 static const void *bwd_ptr_entry(bool fused, bool packed) {
     if constexpr (OP != OP_BWD) {
         return nullptr;
@@ -272,10 +310,10 @@ static const void *bwd_ptr_entry(bool fused, bool packed) {
         return fused ? (const void *)rmsnorm_bwd_generic<T, true> : (const void *)rmsnorm_bwd_generic<T, false>;
     } else if constexpr (PATH == PATH_VECTOR) {
         if (packed)
-            return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, true, true>
-                         : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, true, false>;
-        return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, false, true>
-                     : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, false, false>;
+            return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, true, true>
+                         : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, true, false>;
+        return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, false, true>
+                     : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, false, false>;
     } else {
         return nullptr;
     }
@@ -286,8 +324,8 @@ static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p
                         void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (plan_id) {
-#define RMSN_BWD_CASE(id, op, path, tpr, v, teams, cmin, cmax) \
-    case id: return bwd_launch_entry<T, op, path, tpr, v, teams>(fused, packed, p, grid, smem, s);
+#define RMSN_BWD_CASE(id, op, path, tpr, v, teams, depth, cmin, cmax) \
+    case id: return bwd_launch_entry<T, op, path, tpr, v, teams, depth>(fused, packed, p, grid, smem, s);
         RMSNORM_PLAN_TABLE(RMSN_BWD_CASE)
 #undef RMSN_BWD_CASE
     default:
@@ -298,8 +336,8 @@ static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p
 template <typename T>
 static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
     switch (plan_id) {
-#define RMSN_BWD_PTR(id, op, path, tpr, v, teams, cmin, cmax) \
-    case id: return bwd_ptr_entry<T, op, path, tpr, v, teams>(fused, packed);
+#define RMSN_BWD_PTR(id, op, path, tpr, v, teams, depth, cmin, cmax) \
+    case id: return bwd_ptr_entry<T, op, path, tpr, v, teams, depth>(fused, packed);
         RMSNORM_PLAN_TABLE(RMSN_BWD_PTR)
 #undef RMSN_BWD_PTR
     default:

@@ -6,7 +6,11 @@ Tolerances (the RMSNorm definition and bounds are restated in the oracle):
        the ordered bit patterns); fp32: |d| <= 1e-5 |ref| + 1e-6.
   dx   as y, or -- where the result comes from cancelling terms -- within
        8 * 2^-24 * rstd (|g| + |xhat c|) [+ |dres|], the fp32 rounding bound
-       of the difference of the two terms (counted and reported).
+       of the difference of the two terms, plus (N/256 + 48) * 2^-24 *
+       rstd |xhat| (1/N) sum |g xhat|, the worst-case fp32 error of the sum
+       behind c (at most N/256 terms added in sequence per thread, then a
+       tree and at most 32 warp partials), which can itself cancel
+       (counted and reported).
   dw   bf16: |d| <= 4e-3 |ref| + 2^-20 S; fp32: |d| <= 1e-4 |ref| + 2^-20 S,
        with ref the unrounded double sum and S = sum_i |dy xhat| (the scale
        of the fp32 summation error).
@@ -82,10 +86,15 @@ def check_rstd(got: np.ndarray, ref64: np.ndarray):
     return float(rel.max())
 
 
+def reduction_ulps(N: int) -> float:
+    return (N / 256.0 + 48.0) * 2.0 ** -24
+
+
 def check_dx(got: np.ndarray, ref: dict, dtype: str, floor_mult: float = 1.0):
     """Returns the number of elements that needed the cancellation floor."""
     v = decode(got, dtype)
-    floor = floor_mult * FLOOR_ULPS * ref["dx_scale"]
+    N = got.shape[-1]
+    floor = floor_mult * (FLOOR_ULPS * ref["dx_scale"] + reduction_ulps(N) * ref["dx_cscale"])
     near = np.abs(v - ref["dx64"]) <= floor
     if dtype == "bf16":
         ok = (bf16_ulp_distance(got, ref["dx"]) <= 1)
@@ -94,7 +103,11 @@ def check_dx(got: np.ndarray, ref: dict, dtype: str, floor_mult: float = 1.0):
         ok = np.abs(v - r) <= 1e-5 * np.abs(r) + 1e-6
     needed = int((~ok & near).sum())
     ok = ok | near
-    assert ok.all(), f"dx: {(~ok).sum()} elements off; worst index {np.argmax(np.abs(v - ref['dx64']) / (ref['dx_scale'] + 1e-30))}"
+    if not ok.all():
+        i = np.flatnonzero(~ok)[0]
+        raise AssertionError(f"dx: {(~ok).sum()} elements off; first at flat index {i}: got {v.flat[i]!r} "
+                             f"ref {ref['dx64'].flat[i]!r} scale {ref['dx_scale'].flat[i]!r} "
+                             f"cscale {ref['dx_cscale'].flat[i]!r}")
     return needed
 
 
