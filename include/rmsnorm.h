@@ -44,7 +44,7 @@
  *   - Errors are returned as status codes; nothing aborts or throws.
  *     M == 0 is a successful call that launches no kernel (the backward
  *     then sets dw to zero, the empty sum, with one cudaMemsetAsync).
- *     INVALID_ARG: N < 1, N > RMSNORM_MAX_N, M < 0, M * N beyond 2^40, a
+ *     INVALID_ARG: N < 1, N > RMSNORM_MAX_N, M < 0, M > 2^31 - 1, a
  *     required pointer NULL or not element-aligned, eps < 0, eps or offset
  *     not finite, an unknown dtype. WORKSPACE: a non-NULL workspace smaller
  *     than rmsnorm_bwd_workspace_bytes() or not 16-byte aligned.
