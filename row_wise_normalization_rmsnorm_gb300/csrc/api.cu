@@ -373,8 +373,8 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
                  : launch_bwd_main_f32(plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream);
     if (le == 0 && event_after_main) le = (int)cudaEventRecord(static_cast<cudaEvent_t>(event_after_main), stream);
     if (le == 0)
-        le = dt == RMSNORM_BF16 ? launch_dw_finalize_bf16(ws, plan.ctas, (int)N, dw, stream)
-                                : launch_dw_finalize_f32(ws, plan.ctas, (int)N, dw, stream);
+        le = dt == RMSNORM_BF16 ? launch_dw_finalize_bf16(ws, plan.ctas, (int)N, dw, stream, event_after_main != nullptr)
+                                : launch_dw_finalize_f32(ws, plan.ctas, (int)N, dw, stream, event_after_main != nullptr);
     if (owned) {
         cudaError_t fe = cudaFreeAsync(ws, stream);
         if (le == 0 && fe != cudaSuccess) le = (int)fe;

@@ -163,6 +163,10 @@ __global__ void __launch_bounds__(TPR *TEAMS)
         }
     }
 
+    // The finalizer may start launching now; it waits for this grid to
+    // finish (griddepcontrol.wait) before it reads the workspace.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // Combine the CTA's teams in team order, then write ws[blockIdx.x, :].
     float *wsrow = p.ws + (int64_t)blockIdx.x * N;
     if constexpr (TEAMS > 1) {
@@ -246,12 +250,61 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
     }
 }
 
-// Finalizer: 32 columns per CTA, 8 groups of partial rows. Group q sums rows
-// [q P / 8, (q+1) P / 8) in order; the 8 group sums are then added in order.
+// Finalizer. When launched as a programmatic dependent of the main kernel
+// it starts early and waits here until the main grid has completed and its
+// workspace writes are visible; otherwise the wait returns at once.
+__device__ __forceinline__ void wait_for_main_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Vector finalizer (N % 4 == 0): a CTA owns 32 columns as 8 float4 lanes and
+// splits the P partial rows into 32 groups; group q sums rows
+// [q P / 32, (q+1) P / 32) in order, then each column adds the 32 group sums
+// in order. A few float4 loads per thread keep the L2 round trips short.
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_dw_finalize4(const float *ws, int parts, int N, T *dw) {
+    constexpr int RG = 32;
+    __shared__ float part[RG][33];
+    wait_for_main_grid();
+    const int lane = threadIdx.x & 7;     // float4 column within the CTA's 32 columns
+    const int rg = threadIdx.x >> 3;      // row group
+    const int col = blockIdx.x * 32 + lane * 4;
+    const int p0 = (int)((int64_t)parts * rg / RG);
+    const int p1 = (int)((int64_t)parts * (rg + 1) / RG);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col < N) {
+        const float4 *src = reinterpret_cast<const float4 *>(ws + col);
+        const int64_t stride = N / 4;
+#pragma unroll 4
+        for (int q = p0; q < p1; ++q) {
+            const float4 v = src[(int64_t)q * stride];
+            s.x = __fadd_rn(s.x, v.x);
+            s.y = __fadd_rn(s.y, v.y);
+            s.z = __fadd_rn(s.z, v.z);
+            s.w = __fadd_rn(s.w, v.w);
+        }
+    }
+    part[rg][lane * 4 + 0] = s.x;
+    part[rg][lane * 4 + 1] = s.y;
+    part[rg][lane * 4 + 2] = s.z;
+    part[rg][lane * 4 + 3] = s.w;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int c = blockIdx.x * 32 + threadIdx.x;
+        if (c < N) {
+            float tot = part[0][threadIdx.x];
+#pragma unroll
+            for (int g = 1; g < RG; ++g) tot = __fadd_rn(tot, part[g][threadIdx.x]);
+            store_elem(dw, c, tot);
+        }
+    }
+}
+
+// Scalar finalizer for any N: 32 columns per CTA, 8 groups of partial rows,
+// same fixed order rules.
 template <typename T>
 __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int parts, int N, T *dw) {
     constexpr int RG = 8;
     __shared__ float part[RG][32];
+    wait_for_main_grid();
     const int lane = threadIdx.x & 31;
     const int rg = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
@@ -345,12 +398,25 @@ static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
     }
 }
 
+// The finalizer is launched as a programmatic dependent of the main kernel
+// (its launch overlaps the main kernel's tail) unless `serial` asks for a
+// plain launch (when the caller records an event between the two).
 template <typename T>
-static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *stream) {
-    const int grid = (N + 31) / 32;
-    rmsnorm_dw_finalize<T><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(ws, parts, N,
-                                                                               static_cast<T *>(dw));
-    return (int)cudaGetLastError();
+static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *stream, bool serial) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + 31) / 32));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = serial ? 0 : 1;
+    T *out = static_cast<T *>(dw);
+    cudaError_t e = (N % 4 == 0) ? cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize4<T>, ws, parts, N, out)
+                                 : cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize<T>, ws, parts, N, out);
+    return (int)e;
 }
 
 }  // namespace rmsn

@@ -113,7 +113,7 @@ int launch_bwd_main_f32(int plan_id, bool fused, bool packed, const BwdParams &p
                         int smem, void *stream);
 const void *bwd_main_kernel_ptr_bf16(int plan_id, bool fused, bool packed);
 const void *bwd_main_kernel_ptr_f32(int plan_id, bool fused, bool packed);
-int launch_dw_finalize_bf16(const float *ws, int parts, int N, void *dw, void *stream);
-int launch_dw_finalize_f32(const float *ws, int parts, int N, void *dw, void *stream);
+int launch_dw_finalize_bf16(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
+int launch_dw_finalize_f32(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
 
 }  // namespace rmsn
