@@ -46,6 +46,11 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time fwd and bwd over the shape sweep, fused-add and misaligned cases; "
+                         "one JSON line per point (not the headline line)")
+    ap.add_argument("--sweep-iters", type=int, default=20)
+    ap.add_argument("--sweep-filter", default="", help="only points whose label contains this text")
     return ap.parse_args()
 
 
@@ -231,12 +236,114 @@ def run_reference(args):
 
 # ----------------------------------------------------------- GPU arm --
 
+def sweep_points():
+    """(label, dtype, M, N, fused, misaligned) of the shape sweep (N x M grid,
+    N = 128 as per-head rows), the fused-add shapes and one misaligned case
+    per dtype."""
+    from row_wise_normalization_rmsnorm_gb300 import inputs
+    pts = []
+    for dt in ("bf16", "f32"):
+        for M, N in inputs.sweep_points(dt):
+            pts.append((f"{dt} {M}x{N}", dt, M, N, False, False))
+    for M, N in ((4096, 4096), (1024, 8192)):
+        pts.append((f"add bf16 {M}x{N}", "bf16", M, N, True, False))
+    pts.append(("misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
+    pts.append(("misaligned f32 4096x2048", "f32", 4096, 2048, False, True))
+    pts.append(("wide f32 16384x6144", "f32", 16384, 6144, False, False))
+    pts.append(("small f32 64x256", "f32", 64, 256, False, False))
+    return pts
+
+
+def run_sweep(args):
+    """Per-call device time of fwd and bwd at every sweep point. Inputs are
+    N(0,1) draws made on the device (timing only; parity uses the seeded
+    host recipe). Before every timed call a buffer twice the L2 size is
+    written, outside the event bracket, so no call starts with its data in
+    L2."""
+    import torch
+    from row_wise_normalization_rmsnorm_gb300 import build as rn_build
+    rn_build.build()
+    import row_wise_normalization_rmsnorm_gb300 as rn
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1005)
+    for label, dt, M, N, fused, mis in sweep_points():
+        if args.sweep_filter and args.sweep_filter not in label:
+            continue
+        td = torch.bfloat16 if dt == "bf16" else torch.float32
+        s = 2 if dt == "bf16" else 4
+        off = 1 if mis else 0
+
+        def mk(n):
+            buf = torch.randn(n + off, generator=g, device=dev, dtype=torch.float32).to(td)
+            return buf[off:off + n]
+
+        x = mk(M * N).view(M, N)
+        dy = mk(M * N).view(M, N)
+        w = (1 + 0.1 * mk(N).float()).to(td)
+        if mis:
+            wb = torch.empty(N + 1, dtype=td, device=dev)
+            wb[1:].copy_(w)
+            w = wb[1:]
+        y = mk(M * N).view(M, N)
+        dx = mk(M * N).view(M, N)
+        dw = torch.empty_like(w)
+        rstd = torch.empty(M, dtype=torch.float32, device=dev)
+        res = mk(M * N).view(M, N) if fused else None
+        hout = torch.empty_like(x) if fused else None
+        dres = mk(M * N).view(M, N) if fused else None
+        nb = rn.rmsnorm_bwd_workspace_bytes(M, N, td)
+        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+        if fused:
+            fwd = lambda: rn.rmsnorm_add_fwd(x, res, w, y=y, residual_out=hout, rstd=rstd)  # noqa: E731
+            bwd = lambda: rn.rmsnorm_add_bwd(dy, dres, hout, w, rstd, dx=dx, dw=dw, workspace=ws)  # noqa: E731
+        else:
+            fwd = lambda: rn.rmsnorm_fwd(x, w, y=y, rstd=rstd)  # noqa: E731
+            bwd = lambda: rn.rmsnorm_bwd(dy, x, w, rstd, dx=dx, dw=dw, workspace=ws)  # noqa: E731
+        _, _, _, fplan = rn.rmsnorm_fwd_ex(x, w, residual=res, residual_out=hout, y=y, rstd=rstd)
+        _, _, bplan = rn.rmsnorm_bwd_ex(dy, hout if fused else x, w, rstd, dresidual_out=dres, fused=fused,
+                                        dx=dx, dw=dw, workspace=ws)
+        P = bplan["ctas"]
+        k = 1 if fused else 0
+        by = {"fwd": (2 + 2 * k) * M * N * s + N * s + 4 * M,
+              "bwd": (3 + k) * M * N * s + 2 * N * s + 4 * M + 8 * P * N}
+        for op, fn, plan in (("fwd", fwd, fplan), ("bwd", bwd, bplan)):
+            for _ in range(3):
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.sweep_iters)]
+            for a, b in ev:
+                flush.fill_(1.0)
+                a.record()
+                fn()
+                b.record()
+            torch.cuda.synchronize()
+            ts = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+            us = ts[len(ts) // 2]
+            gbs = by[op] / us / 1e3
+            print(json.dumps({"sweep": label, "op": op, "dtype": dt, "M": M, "N": N, "fused": fused,
+                              "misaligned": mis, "us": round(us, 2), "gbs": round(gbs, 1),
+                              "frac_of_peak": round(gbs / peak, 4), "peak": peak, "peak_source": peak_kind,
+                              "plan": plan["plan_id"], "path": plan["path_name"],
+                              "ctas": plan["ctas"], "bytes": by[op]}), flush=True)
+        del x, dy, w, y, dx, dw, res, hout, dres, ws
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     args = parse()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
 
     import torch
     import torch.distributed as dist

@@ -187,9 +187,11 @@ typedef struct {
     int32_t rows_per_cta;       /* rows a CTA works on concurrently             */
     int32_t cta_threads;
     int32_t packed;             /* 1: packed f32x2 arithmetic                   */
-    int32_t ctas;               /* grid size (backward: persistent CTAs = dw partial rows) */
+    int32_t ctas;               /* grid size in CTAs                            */
     int32_t ctas_per_sm;        /* backward: resident CTAs per SM used for `ctas` */
     int32_t smem_bytes;         /* dynamic shared memory per CTA                */
+    int32_t cluster_size;       /* CTAs of a thread-block cluster sharing a row (1: none) */
+    int32_t ws_rows;            /* backward: dW partial rows (CTAs, or clusters) */
     int64_t workspace_bytes;    /* backward only                                */
 } rmsnorm_plan_t;
 

@@ -44,6 +44,8 @@ class Plan(ctypes.Structure):
         ("ctas", ctypes.c_int32),
         ("ctas_per_sm", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
+        ("cluster_size", ctypes.c_int32),
+        ("ws_rows", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
     ]
 

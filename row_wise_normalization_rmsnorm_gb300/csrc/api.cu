@@ -23,11 +23,11 @@
 namespace rmsn {
 
 struct PlanDesc {
-    int id, op, path, tpr, v, teams, depth, cmin, cmax;
+    int id, op, path, tpr, v, teams, depth, cs, cmin, cmax;
 };
 
 static const PlanDesc kPlans[] = {
-#define RMSN_DESC(id, op, path, tpr, v, teams, depth, cmin, cmax) {id, op, path, tpr, v, teams, depth, cmin, cmax},
+#define RMSN_DESC(id, op, path, tpr, v, teams, depth, cs, cmin, cmax) {id, op, path, tpr, v, teams, depth, cs, cmin, cmax},
     RMSNORM_PLAN_TABLE(RMSN_DESC)
 #undef RMSN_DESC
 };
@@ -69,14 +69,19 @@ static int bwd_smem_bytes(const PlanDesc &d, int64_t N) {
     return (int)((d.teams - 1) * N * 4);
 }
 
-// Pure selection: no CUDA calls.
-static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool aligned, int num_sms,
+// Chunks one plan can hold per row.
+static int64_t plan_capacity(const PlanDesc &d) { return (int64_t)d.tpr * d.v * d.cs; }
+
+// Pure selection: no CUDA calls. max_parts is the largest useful number of
+// backward dW partial rows: resident CTAs (or, for cluster plans, resident
+// clusters) on the device; ctas_per_sm is reported only.
+static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool aligned, int64_t max_parts,
                                     int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
     if (!out) return RMSNORM_ERR_INVALID_ARG;
     if (op != RMSNORM_OP_FWD && op != RMSNORM_OP_BWD) return RMSNORM_ERR_INVALID_ARG;
     if (dt != RMSNORM_F32 && dt != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
-    if (num_sms < 1) return RMSNORM_ERR_INVALID_ARG;
+    if (max_parts < 1) return RMSNORM_ERR_INVALID_ARG;
     const int s = elem_size(dt);
     const bool vec_ok = aligned && (N * s) % 16 == 0;
     const int64_t C = vec_ok ? N * s / 16 : 0;
@@ -85,7 +90,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     if (force_plan >= 0) {
         d = find_plan(force_plan);
         if (!d || d->op != op) return RMSNORM_ERR_UNSUPPORTED;
-        if (d->path == PATH_VECTOR && (!vec_ok || C > (int64_t)d->tpr * d->v)) return RMSNORM_ERR_UNSUPPORTED;
+        if (d->path == PATH_VECTOR && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
         if (d->path == PATH_STAGED) return RMSNORM_ERR_UNSUPPORTED;
     } else {
         d = vec_ok ? default_vector_plan(op, C) : nullptr;
@@ -100,23 +105,19 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     out->chunks_per_thread = d->v;
     out->rows_per_cta = d->path == PATH_GENERIC ? 1 : d->teams;
     out->cta_threads = cta_threads(*d);
-    out->packed = 1;
+    out->packed = d->path == PATH_GENERIC ? 0 : 1;
+    out->cluster_size = d->cs;
+    const int64_t units = (M + out->rows_per_cta - 1) / out->rows_per_cta;  // CTAs (or clusters) with rows
     if (op == RMSNORM_OP_FWD) {
-        out->ctas = (int32_t)((M + out->rows_per_cta - 1) / out->rows_per_cta);
-        out->ctas_per_sm = 0;
-        out->smem_bytes = 0;
-        out->workspace_bytes = 0;
-        if (d->path == PATH_GENERIC) out->packed = 0;
+        out->ctas = (int32_t)(units * d->cs);
         return RMSNORM_SUCCESS;
     }
-    if (d->path == PATH_GENERIC) out->packed = 0;
-    const int cps = ctas_per_sm > 0 ? ctas_per_sm : nominal_ctas_per_sm(*d);
-    const int64_t max_useful = (M + out->rows_per_cta - 1) / out->rows_per_cta;
-    int64_t P = (int64_t)cps * num_sms;
+    int64_t P = max_parts;
     if (force_ctas > 0) P = force_ctas;
-    if (P > max_useful) P = max_useful;
-    out->ctas = (int32_t)P;
-    out->ctas_per_sm = cps;
+    if (P > units) P = units;
+    out->ws_rows = (int32_t)P;
+    out->ctas = (int32_t)(P * d->cs);
+    out->ctas_per_sm = ctas_per_sm;
     out->smem_bytes = bwd_smem_bytes(*d, N);
     if (out->smem_bytes > 48 * 1024) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t bytes = P * N * 4;
@@ -159,28 +160,33 @@ static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed) {
                               : bwd_main_kernel_ptr_f32(plan_id, fused, packed);
 }
 
-// Resident CTAs per SM for a backward plan: the minimum over its plain /
-// fused and packed / scalar variants, so the CTA count (and with it the
-// workspace size and dW's summation order) is the same for all of them.
+// Largest number of backward dW partial rows worth launching for a plan:
+// resident CTAs on the device (resident clusters for a cluster plan), the
+// minimum over its plain / fused and packed / scalar variants, so the count
+// (and with it the workspace size and dW's summation order) is the same for
+// all of them. Cached per device, dtype and plan.
 static std::mutex g_occ_mutex;
-static int g_occ_cache[kMaxDevices][2][64];
+static int g_parts_cache[kMaxDevices][2][64];
+static int g_cps_cache[kMaxDevices][2][64];
 
-static cudaError_t bwd_ctas_per_sm(int dev, int dt, const PlanDesc &d, int64_t N, int *out) {
+static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, int64_t N, int *parts_out,
+                                 int *cps_out) {
     const int slot = d.id;
     if (slot < 0 || slot >= 64) return cudaErrorInvalidValue;
     const int dti = dt == RMSNORM_BF16 ? 1 : 0;
-    // The dynamic shared memory of the team combine depends on N; occupancy
-    // is cached for the largest N the plan serves (the conservative value).
     {
         std::lock_guard<std::mutex> lk(g_occ_mutex);
-        if (g_occ_cache[dev][dti][slot] > 0) {
-            *out = g_occ_cache[dev][dti][slot];
+        if (g_parts_cache[dev][dti][slot] > 0) {
+            *parts_out = g_parts_cache[dev][dti][slot];
+            *cps_out = g_cps_cache[dev][dti][slot];
             return cudaSuccess;
         }
     }
     const int threads = cta_threads(d);
     const int E = 16 / elem_size(dt);
-    const int64_t nmax = d.path == PATH_VECTOR ? (int64_t)d.tpr * d.v * E : N;
+    // The dynamic shared memory of the team combine depends on N; occupancy
+    // is taken for the largest N the plan serves (the conservative value).
+    const int64_t nmax = d.path == PATH_VECTOR ? plan_capacity(d) * E : N;
     const int smem = bwd_smem_bytes(d, nmax);
     int best = 1 << 30;
     for (int f = 0; f < 2; ++f) {
@@ -189,15 +195,35 @@ static cudaError_t bwd_ctas_per_sm(int dev, int dt, const PlanDesc &d, int64_t N
             const void *k = bwd_kernel(d.id, dt, f != 0, pk != 0);
             if (!k) return cudaErrorInvalidDeviceFunction;
             int n = 0;
-            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem);
+            cudaError_t e;
+            if (d.cs > 1) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3((unsigned)(d.cs * sms));
+                cfg.blockDim = dim3((unsigned)threads);
+                cfg.dynamicSmemBytes = (size_t)smem;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = (unsigned)d.cs;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+            } else {
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem);
+                n *= sms;
+            }
             if (e != cudaSuccess) return e;
             if (n < best) best = n;
         }
     }
     if (best < 1) best = 1;
+    const int cps = (int)(((int64_t)best * d.cs + sms - 1) / sms);
     std::lock_guard<std::mutex> lk(g_occ_mutex);
-    g_occ_cache[dev][dti][slot] = best;
-    *out = best;
+    g_parts_cache[dev][dti][slot] = best;
+    g_cps_cache[dev][dti][slot] = cps;
+    *parts_out = best;
+    *cps_out = cps;
     return cudaSuccess;
 }
 
@@ -220,7 +246,7 @@ int self_check_impl() {
             if (d.cmin != expect || d.cmax < d.cmin) ++bad;
             expect = d.cmax + 1;
             // the plan must hold every chunk of the largest row it serves
-            if ((int64_t)d.tpr * d.v < d.cmax) ++bad;
+            if (plan_capacity(d) < d.cmax) ++bad;
             // both ends of its range must select it again
             if (default_vector_plan(op, d.cmin) != &d || default_vector_plan(op, d.cmax) != &d) ++bad;
         }
@@ -232,6 +258,8 @@ int self_check_impl() {
         if (d.path == PATH_VECTOR) {
             const bool pow2 = d.tpr > 0 && (d.tpr & (d.tpr - 1)) == 0;
             if (!pow2 || d.tpr * d.teams > kMaxCtaThreads || d.tpr * d.teams < 32 || d.v < 1) ++bad;
+            // a cluster row has one team per CTA, of whole warps, and at most 8 CTAs
+            if (d.cs < 1 || d.cs > 8 || (d.cs > 1 && (d.teams != 1 || d.tpr < 32))) ++bad;
         }
         if (d.id < 0 || d.id >= 64) ++bad;
     }
@@ -275,11 +303,8 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     bool aligned = aligned_to(x, 16) && aligned_to(w, 16) && aligned_to(y, 16);
     if (fused) aligned = aligned && aligned_to(residual, 16) && aligned_to(residual_out, 16);
 
-    int dev = 0, sms = 0;
-    cudaError_t e = device_sms(&dev, &sms);
-    if (e != cudaSuccess) return cuda_fail(e);
     rmsnorm_plan_t plan;
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, sms, 0, force_plan, 0, &plan);
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, 1, 0, force_plan, 0, &plan);
     if (st != RMSNORM_SUCCESS) return st;
 
     FwdParams p;
@@ -332,13 +357,13 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     cudaError_t e = device_sms(&dev, &sms);
     if (e != cudaSuccess) return cuda_fail(e);
     rmsnorm_plan_t plan;
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, sms, 1, force_plan, force_ctas, &plan);
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, 1, 0, force_plan, force_ctas, &plan);
     if (st != RMSNORM_SUCCESS) return st;
     const PlanDesc *d = find_plan(plan.plan_id);
-    int cps = 1;
-    e = bwd_ctas_per_sm(dev, dt, *d, N, &cps);
+    int parts = 1, cps = 1;
+    e = bwd_max_parts(dev, sms, dt, *d, N, &parts, &cps);
     if (e != cudaSuccess) return cuda_fail(e);
-    st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, sms, cps, force_plan, force_ctas, &plan);
+    st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, parts, cps, force_plan, force_ctas, &plan);
     if (st != RMSNORM_SUCCESS) return st;
     bool packed = plan.packed != 0;
     if (force_packed == 0) packed = false;
@@ -373,8 +398,9 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
                  : launch_bwd_main_f32(plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream);
     if (le == 0 && event_after_main) le = (int)cudaEventRecord(static_cast<cudaEvent_t>(event_after_main), stream);
     if (le == 0)
-        le = dt == RMSNORM_BF16 ? launch_dw_finalize_bf16(ws, plan.ctas, (int)N, dw, stream, event_after_main != nullptr)
-                                : launch_dw_finalize_f32(ws, plan.ctas, (int)N, dw, stream, event_after_main != nullptr);
+        le = dt == RMSNORM_BF16
+                 ? launch_dw_finalize_bf16(ws, plan.ws_rows, (int)N, dw, stream, event_after_main != nullptr)
+                 : launch_dw_finalize_f32(ws, plan.ws_rows, (int)N, dw, stream, event_after_main != nullptr);
     if (owned) {
         cudaError_t fe = cudaFreeAsync(ws, stream);
         if (le == 0 && fe != cudaSuccess) le = (int)fe;
@@ -446,10 +472,11 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt) {
     size_t best = 0;
     for (int aligned = 0; aligned < 2; ++aligned) {
         rmsnorm_plan_t plan;
-        if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, sms, 1, -1, 0, &plan) != RMSNORM_SUCCESS) return 0;
-        int cps = 1;
-        if (bwd_ctas_per_sm(dev, dt, *find_plan(plan.plan_id), N, &cps) != cudaSuccess) return 0;
-        if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, sms, cps, -1, 0, &plan) != RMSNORM_SUCCESS) return 0;
+        if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, 1, 0, -1, 0, &plan) != RMSNORM_SUCCESS) return 0;
+        int parts = 1, cps = 1;
+        if (bwd_max_parts(dev, sms, dt, *find_plan(plan.plan_id), N, &parts, &cps) != cudaSuccess) return 0;
+        if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, parts, cps, -1, 0, &plan) != RMSNORM_SUCCESS)
+            return 0;
         if ((size_t)plan.workspace_bytes > best) best = (size_t)plan.workspace_bytes;
     }
     return best;
@@ -458,7 +485,29 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt) {
 rmsnorm_status_t rmsnorm_plan_query(int op, int64_t M, int64_t N, rmsnorm_dtype_t dt, int aligned, int num_sms,
                                     int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
     if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
-    return select_plan(op, M, N, dt, aligned != 0, num_sms, ctas_per_sm, force_plan, force_ctas, out);
+    if (num_sms < 1) return RMSNORM_ERR_INVALID_ARG;
+    // Without a device the resident-CTA count is the caller's (or the plan's
+    // nominal 2048 threads per SM); a cluster plan packs cluster-size CTAs.
+    int cps = ctas_per_sm;
+    int cs = 1;
+    if (force_plan >= 0) {
+        const PlanDesc *fd = find_plan(force_plan);
+        if (fd) {
+            if (cps <= 0) cps = nominal_ctas_per_sm(*fd);
+            cs = fd->cs;
+        }
+    } else {
+        rmsnorm_plan_t probe;
+        rmsnorm_status_t st = select_plan(op, M, N, dt, aligned != 0, 1, 0, -1, 0, &probe);
+        if (st != RMSNORM_SUCCESS) return st;
+        const PlanDesc *pd = find_plan(probe.plan_id);
+        if (cps <= 0) cps = nominal_ctas_per_sm(*pd);
+        cs = pd->cs;
+    }
+    if (cps <= 0) cps = 1;
+    int64_t parts = (int64_t)cps * num_sms / cs;
+    if (parts < 1) parts = 1;
+    return select_plan(op, M, N, dt, aligned != 0, parts, cps, force_plan, force_ctas, out);
 }
 
 int rmsnorm_plan_count(void) { return kNumPlans; }

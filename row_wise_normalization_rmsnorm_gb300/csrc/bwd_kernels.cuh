@@ -32,8 +32,9 @@ namespace rmsn {
 // past M are clamped to the last row (their results are masked later), so
 // every thread of the CTA keeps taking part in the reductions.
 template <typename T, int TPR, int V>
-__device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, int C, int t, bool has_dres,
-                                             uint4 (&x)[V], uint4 (&d)[V], uint4 (&r)[V], float &rs) {
+__device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, int C, int cbase, int t,
+                                             bool has_dres, uint4 (&x)[V], uint4 (&d)[V], uint4 (&r)[V],
+                                             float &rs) {
     const int64_t rr = row < p.M ? row : p.M - 1;
     const int64_t base = rr * C;
     const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x) + base;
@@ -41,7 +42,7 @@ __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, in
     const uint4 *r4 = reinterpret_cast<const uint4 *>(p.dres) + base;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        const int c = v * TPR + t;
+        const int c = cbase + v * TPR + t;
         const bool in = c < C;
         x[v] = in ? ld_stream(x4 + c) : make_uint4(0, 0, 0, 0);
         d[v] = in ? ld_stream(d4 + c) : make_uint4(0, 0, 0, 0);
@@ -55,16 +56,20 @@ __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, in
 // k+1 .. k+D are already in flight, so the SM keeps memory requests
 // outstanding across the reduction barrier and the stores. Each row's x and
 // dy stay in registers across both passes.
-template <typename T, int TPR, int V, int TEAMS, int D, bool PACKED, bool FUSED>
+// CS > 1: the CTAs of a cluster share each row (CTA rank r holds chunks
+// [r TPR V, (r+1) TPR V)); the row sum meets in distributed shared memory
+// and the cluster, not the CTA, owns one dW partial row.
+template <typename T, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool FUSED>
 __global__ void __launch_bounds__(TPR *TEAMS)
     rmsnorm_bwd_vector(const BwdParams p) {
+    static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
     using Pk = Pair<PACKED>;
     constexpr int E = Elem<T>::E;
     constexpr int NP = Elem<T>::NP;
     constexpr int W = TPR > 32 ? TPR / 32 : 1;
     constexpr int B = D + 1;              // ring slots
     constexpr int BR = FUSED ? B : 1;     // dres slots
-    __shared__ float red[2][TEAMS][W];    // double-buffered: one barrier per row
+    __shared__ float red[2][TEAMS][W * CS];  // double-buffered: one barrier per row
     extern __shared__ float4 comb_smem[]; // (TEAMS - 1) * N floats
 
     const int team = threadIdx.x / TPR;
@@ -73,13 +78,16 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     const int C = N / E;
     uint4 *dx4 = reinterpret_cast<uint4 *>(p.dx);
     const bool has_dres = FUSED && p.dres != nullptr;
+    uint32_t rank = 0;
+    if constexpr (CS > 1) rank = cluster_ctarank();
+    const int cbase = (int)rank * TPR * V;  // first chunk of this CTA's slice
 
     // (offset + w) for this thread's columns: loaded once per CTA.
     const float2 o2 = make_float2(p.offset, p.offset);
     float2 wp[V][NP], acc[V][NP];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        const int c = v * TPR + t;
+        const int c = cbase + v * TPR + t;
         float2 wv[NP];
         unpack<T>(c < C ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + c) : make_uint4(0, 0, 0, 0), wv);
 #pragma unroll
@@ -92,9 +100,12 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     // Every team of the CTA runs the same number of iterations (that of
     // team 0, which has the lowest first row) so the CTA-wide barrier in the
     // reduction is reached by all threads; rows past M are masked.
-    const int64_t G = (int64_t)gridDim.x * TEAMS;
-    const int64_t first = (int64_t)blockIdx.x * TEAMS + team;
-    const int64_t iters = (p.M - (int64_t)blockIdx.x * TEAMS + G - 1) / G;
+    // With clusters the unit is the cluster: cluster q takes rows q, q + Q, ...
+    const int64_t unit = CS > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
+    const int64_t units = CS > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
+    const int64_t G = units * TEAMS;
+    const int64_t first = unit * TEAMS + team;
+    const int64_t iters = (p.M - unit * TEAMS + G - 1) / G;
 
     uint4 xb[B][V], db[B][V], rb[BR][V];
     float rs[B];
@@ -114,7 +125,11 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 #pragma unroll
             for (int q = 0; q < NP; ++q) dot = Pk::fma(Pk::mul(df[q], wp[v][q]), xf[q], dot);
         }
-        const float s = team_allreduce<TPR>(__fadd_rn(dot.x, dot.y), &red[k & 1][team][0], t);
+        float s;
+        if constexpr (CS > 1)
+            s = cluster_allreduce<TPR, CS>(__fadd_rn(dot.x, dot.y), &red[k & 1][0][0], t, rank);
+        else
+            s = team_allreduce<TPR>(__fadd_rn(dot.x, dot.y), &red[k & 1][team][0], t);
         // c = (1/N) sum g xhat = rstd * (sum g x) / N
         const float cm = -__fdiv_rn(__fmul_rn(s, r), (float)N);
         const float2 nc2 = make_float2(cm, cm);
@@ -122,7 +137,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
         const int64_t base = (valid ? row : p.M - 1) * C;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
-            const int c = v * TPR + t;
+            const int c = cbase + v * TPR + t;
             float2 xf[NP], df[NP], out[NP];
             unpack<T>(xv[v], xf);
             unpack<T>(dv[v], df);
@@ -146,7 +161,11 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     // prologue: rows 0 .. D-1 into slots 0 .. D-1
 #pragma unroll
     for (int s = 0; s < D; ++s)
-        if (s < iters) bwd_load_row<T, TPR, V>(p, first + s * G, C, t, has_dres, xb[s], db[s], rb[FUSED ? s : 0], rs[s]);
+        if (s < iters)
+            bwd_load_row<T, TPR, V>(p, first + s * G, C, cbase, t, has_dres, xb[s], db[s], rb[FUSED ? s : 0],
+                                    rs[s]);
+    // every CTA of the cluster runs before any distributed-shared store
+    if constexpr (CS > 1) cluster_sync();
 
     for (int64_t k0 = 0; k0 < iters; k0 += B) {
 #pragma unroll
@@ -156,7 +175,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                 // slot (s + D) % B held row k - 1, already done: refill it with row k + D
                         const int sn = (s + D) % B;
                 if (k + D < iters)
-                    bwd_load_row<T, TPR, V>(p, first + (k + D) * G, C, t, has_dres, xb[sn], db[sn],
+                    bwd_load_row<T, TPR, V>(p, first + (k + D) * G, C, cbase, t, has_dres, xb[sn], db[sn],
                                             rb[FUSED ? sn : 0], rs[sn]);
                 process(xb[s], db[s], rb[FUSED ? s : 0], rs[s], k);
             }
@@ -167,8 +186,9 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     // finish (griddepcontrol.wait) before it reads the workspace.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // Combine the CTA's teams in team order, then write ws[blockIdx.x, :].
-    float *wsrow = p.ws + (int64_t)blockIdx.x * N;
+    // Combine the CTA's teams in team order, then write the unit's partial
+    // row ws[unit, :] (a cluster's CTAs each write their slice of it).
+    float *wsrow = p.ws + unit * N;
     if constexpr (TEAMS > 1) {
         float *comb = reinterpret_cast<float *>(comb_smem);
         if (team > 0) {
@@ -202,7 +222,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     }
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        const int c = v * TPR + t;
+        const int c = cbase + v * TPR + t;
         if (c < C) {
             float4 *d = reinterpret_cast<float4 *>(wsrow + c * E);
 #pragma unroll
@@ -328,16 +348,33 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int 
 
 // ------------------------------------------------------------- dispatch --
 
-template <typename T, int TPR, int V, int TEAMS, int D, bool PACKED>
+template <typename T, int TPR, int V, int TEAMS, int D, int CS, bool PACKED>
 static int bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    if (fused)
-        rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, PACKED, true><<<grid, TPR * TEAMS, smem, s>>>(p);
-    else
-        rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, PACKED, false><<<grid, TPR * TEAMS, smem, s>>>(p);
-    return (int)cudaGetLastError();
+    if constexpr (CS == 1) {
+        if (fused)
+            rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, 1, PACKED, true><<<grid, TPR * TEAMS, smem, s>>>(p);
+        else
+            rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, 1, PACKED, false><<<grid, TPR * TEAMS, smem, s>>>(p);
+        return (int)cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(TPR * TEAMS);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, PACKED, true>, p)
+                     : (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, PACKED, false>, p);
+    }
 }
 
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D>
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
 static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     if constexpr (OP != OP_BWD) {
         return (int)cudaErrorInvalidValue;
@@ -348,14 +385,14 @@ static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int gri
             rmsnorm_bwd_generic<T, false><<<grid, 256, 0, s>>>(p);
         return (int)cudaGetLastError();
     } else if constexpr (PATH == PATH_VECTOR) {
-        return packed ? bwd_launch_vec<T, TPR, V, TEAMS, D, true>(fused, p, grid, smem, s)
-                      : bwd_launch_vec<T, TPR, V, TEAMS, D, false>(fused, p, grid, smem, s);
+        return packed ? bwd_launch_vec<T, TPR, V, TEAMS, D, CS, true>(fused, p, grid, smem, s)
+                      : bwd_launch_vec<T, TPR, V, TEAMS, D, CS, false>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
 }
 
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D>
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
 static const void *bwd_ptr_entry(bool fused, bool packed) {
     if constexpr (OP != OP_BWD) {
         return nullptr;
@@ -363,10 +400,10 @@ static const void *bwd_ptr_entry(bool fused, bool packed) {
         return fused ? (const void *)rmsnorm_bwd_generic<T, true> : (const void *)rmsnorm_bwd_generic<T, false>;
     } else if constexpr (PATH == PATH_VECTOR) {
         if (packed)
-            return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, true, true>
-                         : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, true, false>;
-        return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, false, true>
-                     : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, false, false>;
+            return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true, true>
+                         : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true, false>;
+        return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false, true>
+                     : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false, false>;
     } else {
         return nullptr;
     }
@@ -377,8 +414,8 @@ static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p
                         void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (plan_id) {
-#define RMSN_BWD_CASE(id, op, path, tpr, v, teams, depth, cmin, cmax) \
-    case id: return bwd_launch_entry<T, op, path, tpr, v, teams, depth>(fused, packed, p, grid, smem, s);
+#define RMSN_BWD_CASE(id, op, path, tpr, v, teams, depth, cs, cmin, cmax) \
+    case id: return bwd_launch_entry<T, op, path, tpr, v, teams, depth, cs>(fused, packed, p, grid, smem, s);
         RMSNORM_PLAN_TABLE(RMSN_BWD_CASE)
 #undef RMSN_BWD_CASE
     default:
@@ -389,8 +426,8 @@ static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p
 template <typename T>
 static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
     switch (plan_id) {
-#define RMSN_BWD_PTR(id, op, path, tpr, v, teams, depth, cmin, cmax) \
-    case id: return bwd_ptr_entry<T, op, path, tpr, v, teams, depth>(fused, packed);
+#define RMSN_BWD_PTR(id, op, path, tpr, v, teams, depth, cs, cmin, cmax) \
+    case id: return bwd_ptr_entry<T, op, path, tpr, v, teams, depth, cs>(fused, packed);
         RMSNORM_PLAN_TABLE(RMSN_BWD_PTR)
 #undef RMSN_BWD_PTR
     default:

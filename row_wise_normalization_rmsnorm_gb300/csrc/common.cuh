@@ -172,4 +172,61 @@ __device__ __forceinline__ float cta_allreduce(float v, float *red) {
     return s;
 }
 
+// ------------------------------------------------------------- clusters --
+// A row can be shared by the CTAs of a thread-block cluster: each CTA keeps
+// its slice in registers and the per-warp partial sums are exchanged
+// through distributed shared memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// Barrier over every thread of every CTA in the cluster. Writes made to
+// (distributed) shared memory before it are visible to all after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Store v at the address of `local` (a shared variable of this CTA) in the
+// shared memory of cluster CTA `cta`.
+__device__ __forceinline__ void st_cluster(float *local, uint32_t cta, float v) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(cta));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
+}
+
+// All-reduce of one float over a row shared by the CS CTAs of a cluster
+// (one team of TPR >= 32 threads per CTA). Lane 0 of each warp writes its
+// warp sum into slot [rank * W + warp] of every CTA; after one cluster
+// barrier every thread adds the CS * W slots in index order, so every
+// thread of the cluster obtains the same bits. `red` holds CS * W floats;
+// callers alternate two buffers between rows.
+template <int TPR, int CS>
+__device__ __forceinline__ float cluster_allreduce(float v, float *red, int t, uint32_t rank) {
+    static_assert(TPR >= 32, "cluster rows need whole warps");
+    constexpr int W = TPR / 32;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((t & 31) == 0) {
+#pragma unroll
+        for (int c = 0; c < CS; ++c) st_cluster(&red[rank * W + (t >> 5)], (uint32_t)c, v);
+    }
+    cluster_sync();
+    float s = red[0];
+#pragma unroll
+    for (int i = 1; i < CS * W; ++i) s = __fadd_rn(s, red[i]);
+    return s;
+}
+
 }  // namespace rmsn

@@ -19,17 +19,29 @@
 
 namespace rmsn {
 
-template <typename T, int TPR, int V, int TEAMS, bool FUSED>
+// CS > 1: the CTAs of a cluster share one row; CTA rank r holds chunks
+// [r TPR V, (r+1) TPR V) and the sum of squares meets in distributed shared
+// memory (wide rows whose chunks exceed one CTA's registers).
+template <typename T, int TPR, int V, int TEAMS, int CS, bool FUSED>
 __global__ void __launch_bounds__(TPR *TEAMS)
     rmsnorm_fwd_vector(const FwdParams p) {
+    static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
     using Pk = Pair<true>;
     constexpr int NP = Elem<T>::NP;
     constexpr int W = TPR > 32 ? TPR / 32 : 1;
-    __shared__ float red[TEAMS][W];
+    __shared__ float red[TEAMS][W * CS];
 
     const int team = threadIdx.x / TPR;
     const int t = threadIdx.x % TPR;
-    const int64_t row = (int64_t)blockIdx.x * TEAMS + team;
+    uint32_t rank = 0;
+    int64_t row;
+    if constexpr (CS > 1) {
+        rank = cluster_ctarank();
+        row = cluster_id_x();
+    } else {
+        row = (int64_t)blockIdx.x * TEAMS + team;
+    }
+    const int cbase = (int)rank * TPR * V;  // first chunk of this CTA's slice
     const bool valid = row < p.M;
     const int64_t rr = valid ? row : p.M - 1;  // keep every thread in the reductions
     const int C = p.N / Elem<T>::E;
@@ -38,7 +50,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     uint4 xv[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        const int c = v * TPR + t;
+        const int c = cbase + v * TPR + t;
         xv[v] = c < C ? ld_stream(reinterpret_cast<const uint4 *>(p.x) + base + c) : make_uint4(0, 0, 0, 0);
     }
     if constexpr (FUSED) {
@@ -49,7 +61,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
         uint4 rv[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) {
-            const int c = v * TPR + t;
+            const int c = cbase + v * TPR + t;
             rv[v] = c < C ? ld_stream(reinterpret_cast<const uint4 *>(p.residual) + base + c)
                           : make_uint4(0, 0, 0, 0);
         }
@@ -61,7 +73,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 #pragma unroll
             for (int k = 0; k < NP; ++k) a[k] = Pk::add(a[k], b[k]);
             xv[v] = pack<T>(a);
-            const int c = v * TPR + t;
+            const int c = cbase + v * TPR + t;
             if (valid && c < C) st_chunk(reinterpret_cast<uint4 *>(p.residual_out) + base + c, xv[v]);
         }
     }
@@ -74,16 +86,22 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 #pragma unroll
         for (int k = 0; k < NP; ++k) ss = Pk::fma(a[k], a[k], ss);
     }
-    const float s = team_allreduce<TPR>(__fadd_rn(ss.x, ss.y), &red[team][0], t);
+    float s;
+    if constexpr (CS > 1) {
+        cluster_sync();  // every CTA of the cluster runs before any distributed-shared store
+        s = cluster_allreduce<TPR, CS>(__fadd_rn(ss.x, ss.y), &red[0][0], t, rank);
+    } else {
+        s = team_allreduce<TPR>(__fadd_rn(ss.x, ss.y), &red[team][0], t);
+    }
     const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(s, (float)p.N), p.eps));
-    if (valid && t == 0) p.rstd[row] = rstd;
+    if (valid && t == 0 && rank == 0) p.rstd[row] = rstd;
     if (!valid) return;
 
     const float2 r2 = make_float2(rstd, rstd);
     const float2 o2 = make_float2(p.offset, p.offset);
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        const int c = v * TPR + t;
+        const int c = cbase + v * TPR + t;
         if (c < C) {
             float2 a[NP], wv[NP];
             unpack<T>(xv[v], a);
@@ -127,20 +145,36 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
 
 // ------------------------------------------------------------- dispatch --
 
-template <typename T, int TPR, int V, int TEAMS>
+template <typename T, int TPR, int V, int TEAMS, int CS>
 static int launch_vec(bool fused, const FwdParams &p, int grid, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (fused)
-        rmsnorm_fwd_vector<T, TPR, V, TEAMS, true><<<grid, TPR * TEAMS, 0, s>>>(p);
-    else
-        rmsnorm_fwd_vector<T, TPR, V, TEAMS, false><<<grid, TPR * TEAMS, 0, s>>>(p);
-    return (int)cudaGetLastError();
+    if constexpr (CS == 1) {
+        if (fused)
+            rmsnorm_fwd_vector<T, TPR, V, TEAMS, 1, true><<<grid, TPR * TEAMS, 0, s>>>(p);
+        else
+            rmsnorm_fwd_vector<T, TPR, V, TEAMS, 1, false><<<grid, TPR * TEAMS, 0, s>>>(p);
+        return (int)cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(TPR * TEAMS);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TPR, V, TEAMS, CS, true>, p)
+                     : (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TPR, V, TEAMS, CS, false>, p);
+    }
 }
 
-template <typename T, int TPR, int V, int TEAMS>
+template <typename T, int TPR, int V, int TEAMS, int CS>
 static const void *ptr_vec(bool fused) {
-    return fused ? (const void *)rmsnorm_fwd_vector<T, TPR, V, TEAMS, true>
-                 : (const void *)rmsnorm_fwd_vector<T, TPR, V, TEAMS, false>;
+    return fused ? (const void *)rmsnorm_fwd_vector<T, TPR, V, TEAMS, CS, true>
+                 : (const void *)rmsnorm_fwd_vector<T, TPR, V, TEAMS, CS, false>;
 }
 
 template <typename T>
@@ -160,27 +194,27 @@ static const void *ptr_gen(bool fused) {
 
 // One switch case per table entry; `if constexpr` keeps kernels of other
 // ops and paths from being instantiated here.
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS>
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int CS>
 static int launch_entry(bool fused, const FwdParams &p, int grid, void *stream) {
     if constexpr (OP != OP_FWD) return (int)cudaErrorInvalidValue;
     else if constexpr (PATH == PATH_GENERIC) return launch_gen<T>(fused, p, grid, stream);
-    else if constexpr (PATH == PATH_VECTOR) return launch_vec<T, TPR, V, TEAMS>(fused, p, grid, stream);
+    else if constexpr (PATH == PATH_VECTOR) return launch_vec<T, TPR, V, TEAMS, CS>(fused, p, grid, stream);
     else return (int)cudaErrorInvalidValue;
 }
 
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS>
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int CS>
 static const void *ptr_entry(bool fused) {
     if constexpr (OP != OP_FWD) return nullptr;
     else if constexpr (PATH == PATH_GENERIC) return ptr_gen<T>(fused);
-    else if constexpr (PATH == PATH_VECTOR) return ptr_vec<T, TPR, V, TEAMS>(fused);
+    else if constexpr (PATH == PATH_VECTOR) return ptr_vec<T, TPR, V, TEAMS, CS>(fused);
     else return nullptr;
 }
 
 template <typename T>
 static int launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
     switch (plan_id) {
-#define RMSN_FWD_CASE(id, op, path, tpr, v, teams, depth, cmin, cmax) \
-    case id: return launch_entry<T, op, path, tpr, v, teams>(fused, p, grid, stream);
+#define RMSN_FWD_CASE(id, op, path, tpr, v, teams, depth, cs, cmin, cmax) \
+    case id: return launch_entry<T, op, path, tpr, v, teams, cs>(fused, p, grid, stream);
         RMSNORM_PLAN_TABLE(RMSN_FWD_CASE)
 #undef RMSN_FWD_CASE
     default:
@@ -191,8 +225,8 @@ static int launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void 
 template <typename T>
 static const void *ptr_t(int plan_id, bool fused) {
     switch (plan_id) {
-#define RMSN_FWD_PTR(id, op, path, tpr, v, teams, depth, cmin, cmax) \
-    case id: return ptr_entry<T, op, path, tpr, v, teams>(fused);
+#define RMSN_FWD_PTR(id, op, path, tpr, v, teams, depth, cs, cmin, cmax) \
+    case id: return ptr_entry<T, op, path, tpr, v, teams, cs>(fused);
         RMSNORM_PLAN_TABLE(RMSN_FWD_PTR)
 #undef RMSN_FWD_PTR
     default:

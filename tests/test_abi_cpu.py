@@ -50,20 +50,30 @@ def test_plan_table_self_check(rn):
     assert rn.lib().rmsnorm_plan_id_at(len(ids)) == -1
 
 
-@pytest.mark.parametrize("dt,N,tpr,v", [
-    (1, 128, 16, 1), (1, 2048, 64, 4), (1, 4096, 128, 4), (1, 7168, 256, 4), (1, 8192, 256, 4),
-    (1, 16384, 512, 4), (0, 256, 32, 2), (0, 2048, 128, 4), (0, 6144, 512, 4), (0, 16384, 1024, 4),
+@pytest.mark.parametrize("dt,N,tpr,v,cs", [
+    (1, 128, 16, 1, 1), (1, 2048, 64, 4, 1), (1, 4096, 128, 4, 1), (1, 7168, 256, 4, 1), (1, 8192, 256, 4, 1),
+    (1, 16384, 512, 4, 1), (0, 256, 32, 2, 1), (0, 2048, 128, 4, 1), (0, 6144, 512, 4, 1),
+    (0, 16384, 512, 4, 2), (1, 65536, 512, 4, 4), (0, 65536, 512, 4, 8),
 ])
-def test_fwd_default_plans(rn, dt, N, tpr, v):
+def test_fwd_default_plans(rn, dt, N, tpr, v, cs):
     p = rn.plan_query(rn.OP_FWD, 4096, N, dt)
     assert p["path_name"] == "vector"
-    assert (p["threads_per_row"], p["chunks_per_thread"]) == (tpr, v)
-    # the row fits the plan's registers
+    assert (p["threads_per_row"], p["chunks_per_thread"], p["cluster_size"]) == (tpr, v, cs)
+    # the row fits the registers of the plan's CTA (or cluster of CTAs)
     per_chunk = 8 if dt == 1 else 4
-    assert tpr * v * per_chunk >= N
+    assert tpr * v * cs * per_chunk >= N
+    assert p["ctas"] == 4096 // p["rows_per_cta"] * cs
 
 
-@pytest.mark.parametrize("dt,N", [(1, 4097), (1, 8191), (1, 8193), (0, 4097), (1, 65536), (0, 32768), (1, 1), (0, 3)])
+@pytest.mark.parametrize("dt,N,cs", [(1, 16384, 2), (0, 8192, 2), (0, 16384, 4), (1, 32768, 4), (1, 65536, 8)])
+def test_bwd_wide_rows_use_clusters(rn, dt, N, cs):
+    p = rn.plan_query(rn.OP_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)
+    assert p["path_name"] == "vector" and p["cluster_size"] == cs
+    assert p["ws_rows"] == 152 // cs and p["ctas"] == p["ws_rows"] * cs
+    assert p["workspace_bytes"] == (p["ws_rows"] * N * 4 + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("dt,N", [(1, 4097), (1, 8191), (1, 8193), (0, 4097), (1, 65535), (0, 32767), (1, 1), (0, 3)])
 def test_fwd_generic_when_vector_cannot_serve(rn, dt, N):
     p = rn.plan_query(rn.OP_FWD, 100, N, dt)
     assert p["path_name"] == "generic"
@@ -84,7 +94,7 @@ def test_plan_independent_of_m(rn):
 
 def test_bwd_cta_count_and_workspace(rn):
     p = rn.plan_query(rn.OP_BWD, 16384, 8192, 1, num_sms=152, ctas_per_sm=2)
-    assert p["ctas"] == 304 and p["ctas_per_sm"] == 2
+    assert p["ctas"] == 304 and p["ctas_per_sm"] == 2 and p["ws_rows"] == 304
     assert p["workspace_bytes"] == 304 * 8192 * 4
     # capped by the rows available (rows_per_cta rows per CTA)
     q = rn.plan_query(rn.OP_BWD, 10, 2048, 1, num_sms=152, ctas_per_sm=2)

@@ -30,7 +30,8 @@ def dev_inputs(M, N, dt, seed, **kw):
 
 
 @pytest.mark.parametrize("dt,M,N", [("bf16", 2048, 8192), ("f32", 1024, 6144), ("bf16", 999, 128),
-                                    ("bf16", 500, 2048), ("f32", 300, 16)])
+                                    ("bf16", 500, 2048), ("f32", 300, 16), ("bf16", 300, 16384),
+                                    ("f32", 200, 16384)])
 @pytest.mark.parametrize("fused", [False, True])
 def test_packed_matches_scalar_bitwise(rn, dt, M, N, fused):
     _, t = dev_inputs(M, N, dt, 90, residual=fused, dres=fused)
@@ -110,7 +111,8 @@ def test_workspace_poisoned_clean_and_null(rn, dt, N):
     assert cuda_bits_equal(dx1, dx2) and cuda_bits_equal(dx1, dx3)
 
 
-@pytest.mark.parametrize("dt,N", [("bf16", 8192), ("bf16", 128), ("f32", 5000), ("bf16", 4097)])
+@pytest.mark.parametrize("dt,N", [("bf16", 8192), ("bf16", 128), ("f32", 5000), ("bf16", 4097),
+                                  ("bf16", 16384), ("f32", 32768)])
 def test_rows_independent_of_batch_and_split(rn, dt, N):
     M = 1234
     _, t = dev_inputs(M, N, dt, 95)
@@ -216,7 +218,7 @@ def test_status_codes_on_device(rn):
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("plan", [7, 10, 11, 12, 16])
+@pytest.mark.parametrize("plan", [7, 9, 10, 11, 12, 16, 17])
 def test_forced_forward_plans_match_oracle(rn, plan):
     M, N, dt = 777, 8192, "bf16"
     d, t = dev_inputs(M, N, dt, 101)
@@ -229,14 +231,14 @@ def test_forced_forward_plans_match_oracle(rn, plan):
     check_rstd(r.cpu().numpy(), f["rstd64"])
 
 
-@pytest.mark.parametrize("plan", [27, 29, 31, 36])
+@pytest.mark.parametrize("plan", [27, 34, 35, 36, 44, 45, 48, 49])
 def test_forced_backward_plans_match_oracle(rn, plan):
     M, N, dt = 777, 8192, "bf16"
     d, t = dev_inputs(M, N, dt, 102)
     f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0)
     r = torch.from_numpy(f["rstd32"]).cuda()
     dx, dw, p = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], r, force_plan=plan, force_ctas=100)
-    assert p["plan_id"] == plan and p["ctas"] == 100
+    assert p["plan_id"] == plan and p["ws_rows"] == 100 and p["ctas"] == 100 * p["cluster_size"]
     b = oracle.bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0, rstd=f["rstd32"])
     torch.cuda.synchronize()
     check_dx(to_host(dx, dt), b, dt)

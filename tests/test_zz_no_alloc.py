@@ -50,13 +50,25 @@ def test_noalloc_backward_matches_rmsnorm_bwd_on_two_calls(rn):
 
 
 def test_noalloc_refuses_sizes_beyond_its_array(rn):
+    """A call whose partial rows do not fit is refused before any launch.
+    Every buffer passed is real and large enough for the call, so nothing
+    could go out of bounds even if it were not refused. Bases one element
+    past an aligned allocation select the generic backward, which keeps at
+    least one partial row per SM: >= 152 rows x 65536 x 4 B > 32 MiB."""
     L = rn.lib()
     limit = 32 << 20
-    M, N = 1 << 20, 65536
-    assert rn.rmsnorm_bwd_workspace_bytes(M, N, torch.bfloat16) > limit
-    t = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
-    r = torch.zeros(16, dtype=torch.float32, device="cuda")
-    st = L.rmsnorm_bwd_noalloc(t.data_ptr(), t.data_ptr(), t.data_ptr(), r.data_ptr(), t.data_ptr(),
-                               t.data_ptr(), M, N, 1, 1e-6, 0.0, torch.cuda.current_stream().cuda_stream)
+    M, N = 2048, 65536
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = rn.plan_query(rn.OP_BWD, M, N, rn.RMSNORM_BF16, aligned=False, num_sms=sms, ctas_per_sm=1)
+    assert plan["path_name"] == "generic" and plan["workspace_bytes"] > limit
+
+    def buf(n, dtype=torch.bfloat16):
+        return torch.zeros(n + 1, dtype=dtype, device="cuda")[1:]
+
+    x, dy, dx = buf(M * N), buf(M * N), buf(M * N)
+    w, dw = buf(N), buf(N)
+    r = torch.ones(M, dtype=torch.float32, device="cuda")
+    st = L.rmsnorm_bwd_noalloc(dy.data_ptr(), x.data_ptr(), w.data_ptr(), r.data_ptr(), dx.data_ptr(),
+                               dw.data_ptr(), M, N, 1, 1e-6, 0.0, torch.cuda.current_stream().cuda_stream)
     assert st == 3          # RMSNORM_ERR_WORKSPACE, nothing launched
     torch.cuda.synchronize()
