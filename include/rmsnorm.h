@@ -244,6 +244,15 @@ rmsnorm_status_t rmsnorm_bwd_ex(const void *dy, const void *dresidual_out, const
                                 int fused, int force_plan, int force_ctas, int force_packed,
                                 void *event_after_main, rmsnorm_plan_t *plan_used);
 
+/*
+ * Device status word of the current device, for diagnostics: 0 normally; 1
+ * if a backward kernel that shares rows across a thread-block cluster gave
+ * up waiting for a peer's partial sum (its bounded wait expired; that call's
+ * outputs are incomplete). Synchronises the device; clear != 0 resets the
+ * word. Returns -1 if the device cannot be queried.
+ */
+int rmsnorm_device_status(int clear);
+
 /* Static description of a status code. */
 const char *rmsnorm_status_string(rmsnorm_status_t status);
 

@@ -77,6 +77,7 @@ SIGNATURES = {
     "rmsnorm_status_string": (ctypes.c_char_p, [_i]),
     "rmsnorm_last_cuda_error": (_i, []),
     "rmsnorm_self_check": (_i, []),
+    "rmsnorm_device_status": (_i, [_i]),
 }
 
 

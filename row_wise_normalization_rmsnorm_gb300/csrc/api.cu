@@ -136,6 +136,25 @@ static rmsnorm_status_t cuda_fail(cudaError_t e) {
 
 void set_last_cuda_error(int e) { g_last_cuda_error = e; }
 
+// Device status word: a kernel whose bounded wait gave up writes a non-zero
+// code here (rmsnorm_device_status reads it). One per device; its address
+// is looked up once per device.
+static __device__ int g_rmsnorm_device_status;
+static std::mutex g_status_mutex;
+static int *g_status_ptr[64];
+
+static cudaError_t status_word(int dev, int **out) {
+    std::lock_guard<std::mutex> lk(g_status_mutex);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_rmsnorm_device_status);
+        if (e != cudaSuccess) return e;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    *out = g_status_ptr[dev];
+    return cudaSuccess;
+}
+
 constexpr int kMaxDevices = 64;
 static std::atomic<int> g_sm_count[kMaxDevices];
 
@@ -382,7 +401,15 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
         owned = true;
     }
 
+    int *status = nullptr;
+    e = status_word(dev, &status);
+    if (e != cudaSuccess) {
+        if (owned) cudaFreeAsync(ws, stream);
+        return cuda_fail(e);
+    }
+
     BwdParams p;
+    p.status = status;
     p.dy = dy;
     p.x = x;
     p.w = w;
@@ -528,5 +555,19 @@ const char *rmsnorm_status_string(rmsnorm_status_t status) {
 int rmsnorm_last_cuda_error(void) { return g_last_cuda_error; }
 
 int rmsnorm_self_check(void) { return self_check_impl(); }
+
+int rmsnorm_device_status(int clear) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    int *w = nullptr;
+    if (status_word(dev, &w) != cudaSuccess) return -1;
+    int v = 0;
+    if (cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+    if (clear && v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return -1;
+    }
+    return v;
+}
 
 }  // extern "C"

@@ -69,8 +69,9 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     constexpr int W = TPR > 32 ? TPR / 32 : 1;
     constexpr int B = D + 1;              // ring slots
     constexpr int BR = FUSED ? B : 1;     // dres slots
-    __shared__ float red[2][TEAMS][W * CS];  // double-buffered: one barrier per row
-    extern __shared__ float4 comb_smem[]; // (TEAMS - 1) * N floats
+    __shared__ float red[2][TEAMS][W * CS];    // double-buffered: one barrier per row
+    __shared__ __align__(8) uint64_t rbar[2];  // cluster rows: arrival of the peers' partials
+    extern __shared__ float4 comb_smem[];      // (TEAMS - 1) * N floats
 
     const int team = threadIdx.x / TPR;
     const int t = threadIdx.x % TPR;
@@ -110,6 +111,9 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     uint4 xb[B][V], db[B][V], rb[BR][V];
     float rs[B];
 
+    constexpr uint32_t kSlotBytes = CS * W * 4;  // one row's partials from the whole cluster
+    bool failed = false;
+
     auto process = [&](uint4 (&xv)[V], uint4 (&dv)[V], uint4 (&rv)[V], float r, int64_t k) {
         const int64_t row = first + k * G;
         const bool valid = row < p.M;
@@ -125,11 +129,42 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 #pragma unroll
             for (int q = 0; q < NP; ++q) dot = Pk::fma(Pk::mul(df[q], wp[v][q]), xf[q], dot);
         }
+        const float part = __fadd_rn(dot.x, dot.y);
         float s;
-        if constexpr (CS > 1)
-            s = cluster_allreduce<TPR, CS>(__fadd_rn(dot.x, dot.y), &red[k & 1][0][0], t, rank);
-        else
-            s = team_allreduce<TPR>(__fadd_rn(dot.x, dot.y), &red[k & 1][team][0], t);
+        if constexpr (CS > 1) {
+            // Row k uses slot buffer b = k & 1, whose barrier phase for it
+            // has parity (k >> 1) & 1. Each warp sends its sum to every
+            // CTA of the cluster; a CTA reuses buffer b (row k + 2) only
+            // after every peer has sent its row k + 1 partial, which each
+            // peer does after reading its own buffer b for row k.
+            const int b = (int)(k & 1);
+            float wsum = part;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(0xffffffffu, wsum, o));
+            if ((t & 31) == 0) {
+#pragma unroll
+                for (int c = 0; c < CS; ++c)
+                    st_async_cluster(&red[b][0][rank * W + (t >> 5)], &rbar[b], (uint32_t)c, wsum);
+            }
+            // while the partials travel: the dW partial, which does not
+            // need the row sum
+            if (valid) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    float2 xf[NP], df[NP];
+                    unpack<T>(xv[v], xf);
+                    unpack<T>(dv[v], df);
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) acc[v][q] = Pk::fma(df[q], Pk::mul(xf[q], r2), acc[v][q]);
+                }
+            }
+            if (!mbar_wait(&rbar[b], (uint32_t)((k >> 1) & 1), kWaitLimit)) failed = true;
+            s = sum_slots<CS * W>(&red[b][0][0], t & 31);
+            // re-arm this buffer for row k + 2 (its phase for row k is done)
+            if (t == 0) mbar_arrive_expect_tx(&rbar[b], kSlotBytes);
+        } else {
+            s = team_allreduce<TPR>(part, &red[k & 1][team][0], t);
+        }
         // c = (1/N) sum g xhat = rstd * (sum g x) / N
         const float cm = -__fdiv_rn(__fmul_rn(s, r), (float)N);
         const float2 nc2 = make_float2(cm, cm);
@@ -146,7 +181,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                 const float2 xh = Pk::mul(xf[q], r2);
                 const float2 g = Pk::mul(df[q], wp[v][q]);
                 out[q] = Pk::mul(Pk::fma(xh, nc2, g), r2);
-                if (valid) acc[v][q] = Pk::fma(df[q], xh, acc[v][q]);
+                if (CS == 1 && valid) acc[v][q] = Pk::fma(df[q], xh, acc[v][q]);
             }
             if (has_dres) {
                 float2 rf[NP];
@@ -158,13 +193,24 @@ __global__ void __launch_bounds__(TPR *TEAMS)
         }
     };
 
+    if constexpr (CS > 1) {
+        if (t == 0) {
+            mbar_init(&rbar[0], 1);
+            mbar_init(&rbar[1], 1);
+            mbar_arrive_expect_tx(&rbar[0], kSlotBytes);  // rows 0 and 1
+            mbar_arrive_expect_tx(&rbar[1], kSlotBytes);
+            mbar_init_fence();
+        }
+    }
+
     // prologue: rows 0 .. D-1 into slots 0 .. D-1
 #pragma unroll
     for (int s = 0; s < D; ++s)
         if (s < iters)
             bwd_load_row<T, TPR, V>(p, first + s * G, C, cbase, t, has_dres, xb[s], db[s], rb[FUSED ? s : 0],
                                     rs[s]);
-    // every CTA of the cluster runs before any distributed-shared store
+    // every CTA of the cluster runs, with its barriers initialised, before
+    // any peer stores into its shared memory
     if constexpr (CS > 1) cluster_sync();
 
     for (int64_t k0 = 0; k0 < iters; k0 += B) {
@@ -173,13 +219,21 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             const int64_t k = k0 + s;
             if (k < iters) {
                 // slot (s + D) % B held row k - 1, already done: refill it with row k + D
-                        const int sn = (s + D) % B;
+                const int sn = (s + D) % B;
                 if (k + D < iters)
                     bwd_load_row<T, TPR, V>(p, first + (k + D) * G, C, cbase, t, has_dres, xb[sn], db[sn],
                                             rb[FUSED ? sn : 0], rs[sn]);
                 process(xb[s], db[s], rb[FUSED ? s : 0], rs[s], k);
+                if (CS > 1 && failed) break;
             }
         }
+        if (CS > 1 && failed) break;
+    }
+    if (CS > 1 && failed) {
+        // A peer's partial never arrived: record it and stop (no dW for
+        // this call). The host reads the word with rmsnorm_device_status().
+        if (t == 0 && p.status) *p.status = kStatusClusterWaitTimeout;
+        return;
     }
 
     // The finalizer may start launching now; it waits for this grid to

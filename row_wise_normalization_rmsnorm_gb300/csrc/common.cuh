@@ -135,12 +135,34 @@ template <> struct Pair<false> {
 };
 
 // --------------------------------------------------------- team reduce --
+// Sum of the S slots red[0..S) (S a power of two), computed by every warp:
+// lane i starts from red[i mod S] (S <= 32) or from red[i] + red[i+32] + ...
+// (S > 32), then a butterfly over min(S, 32) lanes. Every lane of every warp
+// ends with the same bits (same values, same association).
+template <int S>
+__device__ __forceinline__ float sum_slots(const float *red, int lane) {
+    static_assert((S & (S - 1)) == 0, "slot count must be a power of two");
+    float s;
+    if constexpr (S <= 32) {
+        s = red[lane & (S - 1)];
+    } else {
+        s = red[lane];
+#pragma unroll
+        for (int j = 1; j < S / 32; ++j) s = __fadd_rn(s, red[lane + 32 * j]);
+    }
+    constexpr int WIDTH = S < 32 ? S : 32;
+#pragma unroll
+    for (int o = WIDTH / 2; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+    return s;
+}
+
 // All-reduce of one float over a team of TPR consecutive threads
 // (TPR a power of two). Within a warp: xor butterfly; every lane ends with
 // the same bits because fp32 addition is commutative. Across the warps of
 // a team: lane 0 of each warp writes `red[warp]`, a CTA barrier, then every
-// thread adds red[0..W) in index order. The barrier is CTA-wide, so every
-// thread of the CTA must call this the same number of times.
+// warp combines the W slots with a second butterfly (sum_slots). The
+// barrier is CTA-wide, so every thread of the CTA must call this the same
+// number of times.
 template <int TPR>
 __device__ __forceinline__ float team_allreduce(float v, float *red, int t) {
     constexpr int WIDTH = TPR < 32 ? TPR : 32;
@@ -150,10 +172,7 @@ __device__ __forceinline__ float team_allreduce(float v, float *red, int t) {
         constexpr int W = TPR / 32;
         if ((t & 31) == 0) red[t >> 5] = v;
         __syncthreads();
-        float s = red[0];
-#pragma unroll
-        for (int i = 1; i < W; ++i) s = __fadd_rn(s, red[i]);
-        v = s;
+        v = sum_slots<W>(red, t & 31);
     }
     return v;
 }
@@ -206,14 +225,66 @@ __device__ __forceinline__ void st_cluster(float *local, uint32_t cta, float v) 
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
 }
 
+// ------------------------------------------------------------ mbarriers --
+// Used by the backward's cluster rows: partial sums travel to the peers'
+// shared memory with st.async, whose completion is counted in bytes on an
+// mbarrier of the receiving CTA. The asynchronous store carries its own
+// release, so, unlike a cluster barrier, the sender never has to wait for
+// its earlier global stores (the previous row's dx) to become visible.
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// One arrival that also announces `bytes` of incoming asynchronous data.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+// True once the phase with the given parity has completed; acquire at
+// cluster scope, so data delivered by the peers' st.async is visible.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Bounded wait: gives up after `limit` polls (each poll may suspend the
+// thread for a short, hardware-chosen time) and reports false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// Store v at the address of `local_slot` in cluster CTA `cta` and count 4
+// bytes on that CTA's barrier at the address of `local_bar`.
+__device__ __forceinline__ void st_async_cluster(float *local_slot, uint64_t *local_bar, uint32_t cta, float v) {
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local_slot)), "r"(cta));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(local_bar)), "r"(cta));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
+                 "r"(__float_as_uint(v)), "r"(rb)
+                 : "memory");
+}
+
 // All-reduce of one float over a row shared by the CS CTAs of a cluster
-// (one team of TPR >= 32 threads per CTA). Lane 0 of each warp writes its
-// warp sum into slot [rank * W + warp] of every CTA; after one cluster
-// barrier every thread adds the CS * W slots in index order, so every
-// thread of the cluster obtains the same bits. `red` holds CS * W floats;
-// callers alternate two buffers between rows.
+// (one team of TPR >= 32 threads per CTA), in two halves so that work that
+// does not need the result can run while the cluster barrier completes:
+//  begin: warp butterfly; lane 0 of each warp stores its warp sum into slot
+//         [rank * W + warp] of every CTA of the cluster; barrier arrive.
+//  end:   barrier wait; every warp combines the CS * W slots (sum_slots),
+//         so every thread of the cluster obtains the same bits.
+// `red` holds CS * W floats; callers alternate buffers between rows.
 template <int TPR, int CS>
-__device__ __forceinline__ float cluster_allreduce(float v, float *red, int t, uint32_t rank) {
+__device__ __forceinline__ void cluster_allreduce_begin(float v, float *red, int t, uint32_t rank) {
     static_assert(TPR >= 32, "cluster rows need whole warps");
     constexpr int W = TPR / 32;
 #pragma unroll
@@ -222,11 +293,19 @@ __device__ __forceinline__ float cluster_allreduce(float v, float *red, int t, u
 #pragma unroll
         for (int c = 0; c < CS; ++c) st_cluster(&red[rank * W + (t >> 5)], (uint32_t)c, v);
     }
-    cluster_sync();
-    float s = red[0];
-#pragma unroll
-    for (int i = 1; i < CS * W; ++i) s = __fadd_rn(s, red[i]);
-    return s;
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+template <int TPR, int CS>
+__device__ __forceinline__ float cluster_allreduce_end(const float *red, int t) {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    return sum_slots<CS *(TPR / 32)>(red, t & 31);
+}
+
+template <int TPR, int CS>
+__device__ __forceinline__ float cluster_allreduce(float v, float *red, int t, uint32_t rank) {
+    cluster_allreduce_begin<TPR, CS>(v, red, t, rank);
+    return cluster_allreduce_end<TPR, CS>(red, t);
 }
 
 }  // namespace rmsn

@@ -101,10 +101,16 @@ struct BwdParams {
     const void *dres;        // fused only, may be NULL
     void *dx;
     float *ws;               // [ctas, N] fp32 partial rows of dw
+    int *status;             // device word: set non-zero if a bounded wait gave up
     int64_t M;
     int N;
     float offset;
 };
+
+// Codes written to BwdParams::status.
+constexpr int kStatusClusterWaitTimeout = 1;
+// Polls of an mbarrier before a wait gives up (at most seconds).
+constexpr uint32_t kWaitLimit = 1u << 22;
 
 // Launchers, defined in the translation units that instantiate the
 // kernels. dtype: 0 fp32, 1 bf16. They return the launch's cudaError_t.

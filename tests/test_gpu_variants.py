@@ -243,3 +243,15 @@ def test_forced_backward_plans_match_oracle(rn, plan):
     torch.cuda.synchronize()
     check_dx(to_host(dx, dt), b, dt)
     check_dw(to_host(dw, dt), b, dt)
+
+
+def test_device_status_clean_after_cluster_rows(rn):
+    """Backward kernels that share rows across a cluster wait, with a bound,
+    for their peers' partial sums; none of the runs in this module may have
+    given up."""
+    for dt, N in (("bf16", 16384), ("f32", 16384), ("bf16", 65536)):
+        _, t = dev_inputs(257, N, dt, 103)
+        _, r = rn.rmsnorm_fwd(t["x"], t["w"])
+        rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], r)
+    torch.cuda.synchronize()
+    assert rn.lib().rmsnorm_device_status(0) == 0
