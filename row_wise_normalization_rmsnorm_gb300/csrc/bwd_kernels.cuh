@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     constexpr int W = TPR > 32 ? TPR / 32 : 1;
     constexpr int B = D + 1;              // ring slots
     constexpr int BR = FUSED ? B : 1;     // dres slots
-    __shared__ float red[2][TEAMS][W * CS];    // double-buffered: one barrier per row
-    __shared__ __align__(8) uint64_t rbar[2];  // cluster rows: arrival of the peers' partials
+    __shared__ float red[2][TEAMS][W * CS];           // row partials, double-buffered
+    __shared__ __align__(8) uint64_t rbar[2][1];      // cluster rows: arrival of the peers' partials
     extern __shared__ float4 comb_smem[];      // (TEAMS - 1) * N floats
 
     const int team = threadIdx.x / TPR;
@@ -132,11 +132,13 @@ __global__ void __launch_bounds__(TPR *TEAMS)
         const float part = __fadd_rn(dot.x, dot.y);
         float s;
         if constexpr (CS > 1) {
-            // Row k uses slot buffer b = k & 1, whose barrier phase for it
-            // has parity (k >> 1) & 1. Each warp sends its sum to every
-            // CTA of the cluster; a CTA reuses buffer b (row k + 2) only
-            // after every peer has sent its row k + 1 partial, which each
-            // peer does after reading its own buffer b for row k.
+            // Split-phase row sum across the cluster. Row k uses slot buffer
+            // b = k & 1, whose barrier phase for it has parity (k >> 1) & 1.
+            // Each warp sends its sum to its slot in every CTA of the
+            // cluster with st.async, counted in bytes on the receiver's
+            // barrier. A CTA reuses buffer b (row k + 2) only after every
+            // warp of the row has sent its row k + 1 partial, which each
+            // warp does after reading buffer b for row k.
             const int b = (int)(k & 1);
             float wsum = part;
 #pragma unroll
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             if ((t & 31) == 0) {
 #pragma unroll
                 for (int c = 0; c < CS; ++c)
-                    st_async_cluster(&red[b][0][rank * W + (t >> 5)], &rbar[b], (uint32_t)c, wsum);
+                    st_async_cluster(&red[b][0][rank * W + (t >> 5)], &rbar[b][0], (uint32_t)c, wsum);
             }
             // while the partials travel: the dW partial, which does not
             // need the row sum
@@ -158,10 +160,10 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                     for (int q = 0; q < NP; ++q) acc[v][q] = Pk::fma(df[q], Pk::mul(xf[q], r2), acc[v][q]);
                 }
             }
-            if (!mbar_wait(&rbar[b], (uint32_t)((k >> 1) & 1), kWaitLimit)) failed = true;
+            if (!mbar_wait(&rbar[b][0], (uint32_t)((k >> 1) & 1), kWaitLimit)) failed = true;
             s = sum_slots<CS * W>(&red[b][0][0], t & 31);
             // re-arm this buffer for row k + 2 (its phase for row k is done)
-            if (t == 0) mbar_arrive_expect_tx(&rbar[b], kSlotBytes);
+            if (t == 0) mbar_arrive_expect_tx(&rbar[b][0], kSlotBytes);
         } else {
             s = team_allreduce<TPR>(part, &red[k & 1][team][0], t);
         }
@@ -195,10 +197,11 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 
     if constexpr (CS > 1) {
         if (t == 0) {
-            mbar_init(&rbar[0], 1);
-            mbar_init(&rbar[1], 1);
-            mbar_arrive_expect_tx(&rbar[0], kSlotBytes);  // rows 0 and 1
-            mbar_arrive_expect_tx(&rbar[1], kSlotBytes);
+            // one arrival (the re-arm) plus the row's bytes
+            mbar_init(&rbar[0][0], 1);
+            mbar_init(&rbar[1][0], 1);
+            mbar_arrive_expect_tx(&rbar[0][0], kSlotBytes);  // rows 0 and 1
+            mbar_arrive_expect_tx(&rbar[1][0], kSlotBytes);
             mbar_init_fence();
         }
     }
@@ -224,16 +227,16 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                     bwd_load_row<T, TPR, V>(p, first + (k + D) * G, C, cbase, t, has_dres, xb[sn], db[sn],
                                             rb[FUSED ? sn : 0], rs[sn]);
                 process(xb[s], db[s], rb[FUSED ? s : 0], rs[s], k);
-                if (CS > 1 && failed) break;
+                if (failed) break;
             }
         }
-        if (CS > 1 && failed) break;
+        if (failed) break;
     }
-    if (CS > 1 && failed) {
-        // A peer's partial never arrived: record it and stop (no dW for
-        // this call). The host reads the word with rmsnorm_device_status().
-        if (t == 0 && p.status) *p.status = kStatusClusterWaitTimeout;
-        return;
+    if (failed) {
+        // A peer's partial never arrived: record it and stop taking rows
+        // (this call's outputs are incomplete). The host reads the word
+        // with rmsnorm_device_status().
+        if (p.status) *p.status = kStatusClusterWaitTimeout;
     }
 
     // The finalizer may start launching now; it waits for this grid to

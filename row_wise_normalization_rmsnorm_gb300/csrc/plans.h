@@ -74,6 +74,12 @@ enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2 };
     X(44, OP_BWD, PATH_VECTOR ,  512, 3,  1, 2, 1,    0,    0) \
     X(48, OP_BWD, PATH_VECTOR ,  512, 3,  1, 1, 2,    0,    0) \
     X(49, OP_BWD, PATH_VECTOR ,  512, 2,  1, 2, 2,    0,    0) \
+    X(50, OP_BWD, PATH_VECTOR ,  256, 2,  1, 1, 2,    0,    0) \
+    X(51, OP_BWD, PATH_VECTOR ,  512, 1,  1, 1, 2,    0,    0) \
+    X(52, OP_BWD, PATH_VECTOR ,  128, 2,  1, 1, 2,    0,    0) \
+    X(53, OP_BWD, PATH_VECTOR ,  256, 1,  1, 1, 2,    0,    0) \
+    X(54, OP_BWD, PATH_VECTOR ,  256, 2,  1, 1, 4,    0,    0) \
+    X(55, OP_BWD, PATH_VECTOR ,  128, 2,  1, 1, 4,    0,    0) \
     /* backward main kernel, any N and alignment */ \
     X(36, OP_BWD, PATH_GENERIC,  256, 0,  1, 0, 1,    0,    0)
 
