@@ -257,9 +257,10 @@ def sweep_points():
 def run_sweep(args):
     """Per-call device time of fwd and bwd at every sweep point. Inputs are
     N(0,1) draws made on the device (timing only; parity uses the seeded
-    host recipe). Before every timed call a buffer twice the L2 size is
-    written, outside the event bracket, so no call starts with its data in
-    L2."""
+    host recipe). Before every timed call a buffer twice the L2 size is read
+    (a sum), outside the event bracket, so no call starts with its data in
+    L2 and the lines left in L2 are clean: a write-based flush would leave
+    dirty lines whose write-back the timed call would pay for."""
     import torch
     from row_wise_normalization_rmsnorm_gb300 import build as rn_build
     rn_build.build()
@@ -269,7 +270,8 @@ def run_sweep(args):
     torch.cuda.set_device(dev)
     peak, peak_kind = peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    flush = torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     g = torch.Generator(device=dev)
     g.manual_seed(1005)
     for label, dt, M, N, fused, mis in sweep_points():
@@ -318,7 +320,7 @@ def run_sweep(args):
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(args.sweep_iters)]
             for a, b in ev:
-                flush.fill_(1.0)
+                torch.sum(flush, 0, out=sink)
                 a.record()
                 fn()
                 b.record()
