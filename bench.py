@@ -32,6 +32,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = "wide_bf16_16384x8192"
+WORKLOAD_DESC = ("rmsnorm fwd+bwd bf16 M=16384 N=8192, llama mode eps=1e-6 offset=0, "
+                 "1% outlier columns x20")
 METRIC = "RMSNorm fwd/bwd achieved HBM GB/s (% of GB300 peak) and us/call, bf16 16384x8192"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 1024 * 1024
@@ -70,6 +72,22 @@ def bytes_bwd_finalize(N, s, P):
 
 def bytes_bwd(M, N, s, P):
     return 3 * M * N * s + 2 * N * s + 4 * M + 8 * P * N
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """Largest value of x over all ranks (x itself with one rank)."""
+    import torch
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank moves bytes_per_rank_step per step and
+    the step time is the slowest rank's."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
 
 
 def peaks():
@@ -223,8 +241,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"rmsnorm fwd+bwd bf16 M={M} N={N} (row sample of {rows} rows per step)",
-                   "M": M, "N": N, "rows_per_step": rows, "eps": p["eps"], "offset": p["offset"]},
+        "config": {"workload": WORKLOAD_DESC, "M": M, "N": N, "rows_per_step": rows,
+                   "eps": p["eps"], "offset": p["offset"]},
         "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{rows} rows per step of the {M}x{N} workload, fwd+bwd, fp64 C oracle"},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -418,16 +436,12 @@ def main():
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(start.elapsed_time(end), dist if world > 1 else None, dev)
     t_fwd = [e[0].elapsed_time(e[1]) for e in ev]
     t_bwd = [e[1].elapsed_time(e[2]) for e in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / K
     step_bytes = bytes_fwd(M, N, s) + bytes_bwd(M, N, s, P)
-    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, world, ms_per_step)
 
     # Diagnostic split of the backward into its two kernels, outside the
     # timed region: an event between them serialises the finalizer's launch.
@@ -496,22 +510,17 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dist if world > 1 else None, dev)
     h2d = (h_x.numel() + h_dy.numel() + h_w.numel()) * s
     d2h = (o_y.numel() + o_dx.numel() + o_dw.numel()) * s + o_r.numel() * 4
-    e2e = {"value": step_bytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+    e2e = {"value": whole_job_gbs(step_bytes, world, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"rmsnorm fwd+bwd bf16 M={M} N={N}, llama mode eps=1e-6 offset=0, "
-                               f"1% outlier columns x20", "M": M, "N": N, "per_rank_rows": M,
+        "config": {"workload": WORKLOAD_DESC, "M": M, "N": N, "per_rank_rows": M,
                    "parallelism": f"replicas x{world} (independent batches)",
                    "l2": "inputs larger than L2 (268 MB per tensor, 126 MB L2); no flush",
                    "fwd_plan": fplan["plan_id"], "bwd_plan": bplan["plan_id"], "bwd_ctas": P,
