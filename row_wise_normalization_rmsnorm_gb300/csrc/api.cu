@@ -23,11 +23,11 @@
 namespace rmsn {
 
 struct PlanDesc {
-    int id, op, path, tpr, v, teams, depth, cs, cmin, cmax;
+    int id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax;
 };
 
 static const PlanDesc kPlans[] = {
-#define RMSN_DESC(id, op, path, tpr, v, teams, depth, cs, cmin, cmax) {id, op, path, tpr, v, teams, depth, cs, cmin, cmax},
+#define RMSN_DESC(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) {id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax},
     RMSNORM_PLAN_TABLE(RMSN_DESC)
 #undef RMSN_DESC
 };
@@ -41,11 +41,16 @@ static const PlanDesc *find_plan(int id) {
 
 static int elem_size(int dt) { return dt == RMSNORM_BF16 ? 2 : 4; }
 
-// Default plan for (op, chunks per row); nullptr when no vector plan covers C.
-static const PlanDesc *default_vector_plan(int op, int64_t C) {
+static int dtype_bit(int dt) { return dt == RMSNORM_BF16 ? DT_BF16 : DT_F32; }
+
+// Default plan for (op, dtype, chunks per row); nullptr when no vector plan
+// covers C.
+static const PlanDesc *default_vector_plan(int op, int dt, int64_t C) {
     for (int i = 0; i < kNumPlans; ++i) {
         const PlanDesc &d = kPlans[i];
-        if (d.op == op && d.path == PATH_VECTOR && d.cmin > 0 && C >= d.cmin && C <= d.cmax) return &d;
+        if (d.op == op && d.path == PATH_VECTOR && d.cmin > 0 && (d.dtm & dtype_bit(dt)) && C >= d.cmin &&
+            C <= d.cmax)
+            return &d;
     }
     return nullptr;
 }
@@ -93,7 +98,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
         if (d->path == PATH_VECTOR && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
         if (d->path == PATH_STAGED) return RMSNORM_ERR_UNSUPPORTED;
     } else {
-        d = vec_ok ? default_vector_plan(op, C) : nullptr;
+        d = vec_ok ? default_vector_plan(op, dt, C) : nullptr;
         if (!d) d = generic_plan(op);
     }
     if (!d) return RMSNORM_ERR_UNSUPPORTED;
@@ -181,23 +186,24 @@ static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed) {
 
 // Largest number of backward dW partial rows worth launching for a plan:
 // resident CTAs on the device (resident clusters for a cluster plan), the
-// minimum over its plain / fused and packed / scalar variants, so the count
-// (and with it the workspace size and dW's summation order) is the same for
-// all of them. Cached per device, dtype and plan.
+// minimum over its packed and scalar variants for the given fusion mode, so
+// those two variants use the same count (and dW the same summation order).
+// Cached per device, dtype, plan and mode.
 static std::mutex g_occ_mutex;
-static int g_parts_cache[kMaxDevices][2][64];
-static int g_cps_cache[kMaxDevices][2][64];
+static int g_parts_cache[kMaxDevices][2][2][64];
+static int g_cps_cache[kMaxDevices][2][2][64];
 
-static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, int64_t N, int *parts_out,
-                                 int *cps_out) {
+static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, int64_t N, bool fused,
+                                 int *parts_out, int *cps_out) {
     const int slot = d.id;
     if (slot < 0 || slot >= 64) return cudaErrorInvalidValue;
     const int dti = dt == RMSNORM_BF16 ? 1 : 0;
+    const int fi = fused ? 1 : 0;
     {
         std::lock_guard<std::mutex> lk(g_occ_mutex);
-        if (g_parts_cache[dev][dti][slot] > 0) {
-            *parts_out = g_parts_cache[dev][dti][slot];
-            *cps_out = g_cps_cache[dev][dti][slot];
+        if (g_parts_cache[dev][dti][fi][slot] > 0) {
+            *parts_out = g_parts_cache[dev][dti][fi][slot];
+            *cps_out = g_cps_cache[dev][dti][fi][slot];
             return cudaSuccess;
         }
     }
@@ -208,39 +214,37 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
     const int64_t nmax = d.path == PATH_VECTOR ? plan_capacity(d) * E : N;
     const int smem = bwd_smem_bytes(d, nmax);
     int best = 1 << 30;
-    for (int f = 0; f < 2; ++f) {
-        for (int pk = 0; pk < 2; ++pk) {
-            if (d.path == PATH_GENERIC && pk == 1) continue;
-            const void *k = bwd_kernel(d.id, dt, f != 0, pk != 0);
-            if (!k) return cudaErrorInvalidDeviceFunction;
-            int n = 0;
-            cudaError_t e;
-            if (d.cs > 1) {
-                cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3((unsigned)(d.cs * sms));
-                cfg.blockDim = dim3((unsigned)threads);
-                cfg.dynamicSmemBytes = (size_t)smem;
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = (unsigned)d.cs;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
-                e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
-            } else {
-                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem);
-                n *= sms;
-            }
-            if (e != cudaSuccess) return e;
-            if (n < best) best = n;
+    for (int pk = 0; pk < 2; ++pk) {
+        if (d.path == PATH_GENERIC && pk == 1) continue;
+        const void *k = bwd_kernel(d.id, dt, fused, pk != 0);
+        if (!k) return cudaErrorInvalidDeviceFunction;
+        int n = 0;
+        cudaError_t e;
+        if (d.cs > 1) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(d.cs * sms));
+            cfg.blockDim = dim3((unsigned)threads);
+            cfg.dynamicSmemBytes = (size_t)smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)d.cs;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+        } else {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem);
+            n *= sms;
         }
+        if (e != cudaSuccess) return e;
+        if (n < best) best = n;
     }
     if (best < 1) best = 1;
     const int cps = (int)(((int64_t)best * d.cs + sms - 1) / sms);
     std::lock_guard<std::mutex> lk(g_occ_mutex);
-    g_parts_cache[dev][dti][slot] = best;
-    g_cps_cache[dev][dti][slot] = cps;
+    g_parts_cache[dev][dti][fi][slot] = best;
+    g_cps_cache[dev][dti][fi][slot] = cps;
     *parts_out = best;
     *cps_out = cps;
     return cudaSuccess;
@@ -257,17 +261,19 @@ static std::atomic<int> g_table_ok{-1};
 int self_check_impl() {
     int bad = 0;
     for (int op = 0; op < 2; ++op) {
-        int64_t expect = 1;
-        for (int i = 0; i < kNumPlans; ++i) {
-            const PlanDesc &d = kPlans[i];
-            if (d.op != op || d.path != PATH_VECTOR || d.cmin == 0) continue;
-            // ranges of default plans must tile [1, max] in table order
-            if (d.cmin != expect || d.cmax < d.cmin) ++bad;
-            expect = d.cmax + 1;
-            // the plan must hold every chunk of the largest row it serves
-            if (plan_capacity(d) < d.cmax) ++bad;
-            // both ends of its range must select it again
-            if (default_vector_plan(op, d.cmin) != &d || default_vector_plan(op, d.cmax) != &d) ++bad;
+        for (int dt = 0; dt < 2; ++dt) {
+            int64_t expect = 1;
+            for (int i = 0; i < kNumPlans; ++i) {
+                const PlanDesc &d = kPlans[i];
+                if (d.op != op || d.path != PATH_VECTOR || d.cmin == 0 || !(d.dtm & dtype_bit(dt))) continue;
+                // ranges of a dtype's default plans must tile [1, max] in table order
+                if (d.cmin != expect || d.cmax < d.cmin) ++bad;
+                expect = d.cmax + 1;
+                // the plan must hold every chunk of the largest row it serves
+                if (plan_capacity(d) < d.cmax) ++bad;
+                // both ends of its range must select it again
+                if (default_vector_plan(op, dt, d.cmin) != &d || default_vector_plan(op, dt, d.cmax) != &d) ++bad;
+            }
         }
         if (!generic_plan(op)) ++bad;
     }
@@ -280,6 +286,7 @@ int self_check_impl() {
             // a cluster row has one team per CTA, of whole warps, and at most 8 CTAs
             if (d.cs < 1 || d.cs > 8 || (d.cs > 1 && (d.teams != 1 || d.tpr < 32))) ++bad;
         }
+        if (d.dtm < 1 || d.dtm > 3) ++bad;
         if (d.id < 0 || d.id >= 64) ++bad;
     }
     return bad;
@@ -380,7 +387,7 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     if (st != RMSNORM_SUCCESS) return st;
     const PlanDesc *d = find_plan(plan.plan_id);
     int parts = 1, cps = 1;
-    e = bwd_max_parts(dev, sms, dt, *d, N, &parts, &cps);
+    e = bwd_max_parts(dev, sms, dt, *d, N, fused, &parts, &cps);
     if (e != cudaSuccess) return cuda_fail(e);
     st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, parts, cps, force_plan, force_ctas, &plan);
     if (st != RMSNORM_SUCCESS) return st;
@@ -494,17 +501,23 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt) {
     if (M > 0x7fffffffLL || !table_ok()) return 0;
     int dev = 0, sms = 0;
     if (device_sms(&dev, &sms) != cudaSuccess) return 0;
-    // The largest requirement over the aligned and generic plans, so one
-    // size serves any pointer alignment.
     size_t best = 0;
+    // The largest requirement over the aligned and generic plans and the
+    // plain and fused variants, so one size serves every call.
     for (int aligned = 0; aligned < 2; ++aligned) {
-        rmsnorm_plan_t plan;
-        if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, 1, 0, -1, 0, &plan) != RMSNORM_SUCCESS) return 0;
-        int parts = 1, cps = 1;
-        if (bwd_max_parts(dev, sms, dt, *find_plan(plan.plan_id), N, &parts, &cps) != cudaSuccess) return 0;
-        if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, parts, cps, -1, 0, &plan) != RMSNORM_SUCCESS)
-            return 0;
-        if ((size_t)plan.workspace_bytes > best) best = (size_t)plan.workspace_bytes;
+        for (int fused = 0; fused < 2; ++fused) {
+            rmsnorm_plan_t plan;
+            if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, 1, 0, -1, 0, &plan) != RMSNORM_SUCCESS)
+                return 0;
+            int parts = 1, cps = 1;
+            if (bwd_max_parts(dev, sms, dt, *find_plan(plan.plan_id), N, fused != 0, &parts, &cps) !=
+                cudaSuccess)
+                return 0;
+            if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, parts, cps, -1, 0, &plan) !=
+                RMSNORM_SUCCESS)
+                return 0;
+            if ((size_t)plan.workspace_bytes > best) best = (size_t)plan.workspace_bytes;
+        }
     }
     return best;
 }

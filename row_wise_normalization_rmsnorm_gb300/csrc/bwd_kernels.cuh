@@ -471,7 +471,7 @@ static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p
                         void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (plan_id) {
-#define RMSN_BWD_CASE(id, op, path, tpr, v, teams, depth, cs, cmin, cmax) \
+#define RMSN_BWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
     case id: return bwd_launch_entry<T, op, path, tpr, v, teams, depth, cs>(fused, packed, p, grid, smem, s);
         RMSNORM_PLAN_TABLE(RMSN_BWD_CASE)
 #undef RMSN_BWD_CASE
@@ -483,7 +483,7 @@ static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p
 template <typename T>
 static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
     switch (plan_id) {
-#define RMSN_BWD_PTR(id, op, path, tpr, v, teams, depth, cs, cmin, cmax) \
+#define RMSN_BWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
     case id: return bwd_ptr_entry<T, op, path, tpr, v, teams, depth, cs>(fused, packed);
         RMSNORM_PLAN_TABLE(RMSN_BWD_PTR)
 #undef RMSN_BWD_PTR

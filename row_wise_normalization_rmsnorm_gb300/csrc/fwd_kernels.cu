@@ -213,7 +213,7 @@ static const void *ptr_entry(bool fused) {
 template <typename T>
 static int launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
     switch (plan_id) {
-#define RMSN_FWD_CASE(id, op, path, tpr, v, teams, depth, cs, cmin, cmax) \
+#define RMSN_FWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
     case id: return launch_entry<T, op, path, tpr, v, teams, cs>(fused, p, grid, stream);
         RMSNORM_PLAN_TABLE(RMSN_FWD_CASE)
 #undef RMSN_FWD_CASE
@@ -225,7 +225,7 @@ static int launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void 
 template <typename T>
 static const void *ptr_t(int plan_id, bool fused) {
     switch (plan_id) {
-#define RMSN_FWD_PTR(id, op, path, tpr, v, teams, depth, cs, cmin, cmax) \
+#define RMSN_FWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
     case id: return ptr_entry<T, op, path, tpr, v, teams, cs>(fused);
         RMSNORM_PLAN_TABLE(RMSN_FWD_PTR)
 #undef RMSN_FWD_PTR

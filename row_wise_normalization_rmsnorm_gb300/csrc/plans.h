@@ -18,10 +18,13 @@ namespace rmsn {
 
 enum PlanOp { OP_FWD = 0, OP_BWD = 1 };
 enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2 };
+// Storage types a default plan applies to (bit 0: fp32, bit 1: bf16).
+enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_ANY = 3 };
 
-// X(id, op, path, threads_per_row, chunks_per_thread, teams_per_cta, depth, cluster, cmin, cmax)
-// [cmin, cmax] is the range of C for which the plan is the default; 0, 0
-// marks an alternative that runs only when forced (tuning and A/B tests).
+// X(id, op, path, threads_per_row, chunks_per_thread, teams_per_cta, depth, cluster, dtypes, cmin, cmax)
+// [cmin, cmax] is the range of C for which the plan is the default for the
+// storage types in `dtypes`; 0, 0 marks an alternative that runs only when
+// forced (tuning and A/B tests).
 // depth (backward only): rows whose x/dy loads are in flight while the
 // current row is computed (a register ring of depth + 1 rows).
 // cluster: CTAs of a thread-block cluster that share one row; each holds
@@ -30,58 +33,58 @@ enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2 };
 // Generic plans hold no chunks (they use a 256-thread CTA per row).
 #define RMSNORM_PLAN_TABLE(X) \
     /* forward, row in registers */ \
-    X( 0, OP_FWD, PATH_VECTOR ,    8, 1, 32, 0, 1,    1,    8) \
-    X( 1, OP_FWD, PATH_VECTOR ,   16, 1, 16, 0, 1,    9,   16) \
-    X( 2, OP_FWD, PATH_VECTOR ,   32, 1,  8, 0, 1,   17,   32) \
-    X( 3, OP_FWD, PATH_VECTOR ,   32, 2,  8, 0, 1,   33,   64) \
-    X( 4, OP_FWD, PATH_VECTOR ,   32, 4,  8, 0, 1,   65,  128) \
-    X( 5, OP_FWD, PATH_VECTOR ,   64, 4,  4, 0, 1,  129,  256) \
-    X( 6, OP_FWD, PATH_VECTOR ,  128, 4,  2, 0, 1,  257,  512) \
-    X( 7, OP_FWD, PATH_VECTOR ,  256, 4,  1, 0, 1,  513, 1024) \
-    X( 8, OP_FWD, PATH_VECTOR ,  512, 4,  1, 0, 1, 1025, 2048) \
-    X(17, OP_FWD, PATH_VECTOR ,  512, 4,  1, 0, 2, 2049, 4096) \
-    X(18, OP_FWD, PATH_VECTOR ,  512, 4,  1, 0, 4, 4097, 8192) \
-    X(19, OP_FWD, PATH_VECTOR ,  512, 4,  1, 0, 8, 8193, 16384) \
-    X( 9, OP_FWD, PATH_VECTOR , 1024, 4,  1, 0, 1,    0,    0) \
-    X(10, OP_FWD, PATH_VECTOR ,  128, 8,  2, 0, 1,    0,    0) \
-    X(11, OP_FWD, PATH_VECTOR ,  512, 2,  1, 0, 1,    0,    0) \
-    X(12, OP_FWD, PATH_VECTOR , 1024, 1,  1, 0, 1,    0,    0) \
-    X(13, OP_FWD, PATH_VECTOR ,  256, 2,  2, 0, 1,    0,    0) \
-    X(14, OP_FWD, PATH_VECTOR ,   64, 8,  4, 0, 1,    0,    0) \
-    X(15, OP_FWD, PATH_VECTOR ,   16, 2, 16, 0, 1,    0,    0) \
+    X( 0, OP_FWD, PATH_VECTOR ,    8, 1, 32, 0, 1, DT_ANY,     1,     8) \
+    X( 1, OP_FWD, PATH_VECTOR ,   16, 1, 16, 0, 1, DT_ANY,     9,    16) \
+    X( 2, OP_FWD, PATH_VECTOR ,   32, 1,  8, 0, 1, DT_ANY,    17,    32) \
+    X( 3, OP_FWD, PATH_VECTOR ,   32, 2,  8, 0, 1, DT_ANY,    33,    64) \
+    X( 4, OP_FWD, PATH_VECTOR ,   32, 4,  8, 0, 1, DT_ANY,    65,   128) \
+    X( 5, OP_FWD, PATH_VECTOR ,   64, 4,  4, 0, 1, DT_ANY,   129,   256) \
+    X( 6, OP_FWD, PATH_VECTOR ,  128, 4,  2, 0, 1, DT_ANY,   257,   512) \
+    X( 7, OP_FWD, PATH_VECTOR ,  256, 4,  1, 0, 1, DT_ANY,   513,  1024) \
+    X( 8, OP_FWD, PATH_VECTOR ,  512, 4,  1, 0, 1, DT_ANY,  1025,  2048) \
+    X(17, OP_FWD, PATH_VECTOR ,  512, 4,  1, 0, 2, DT_ANY,  2049,  4096) \
+    X(18, OP_FWD, PATH_VECTOR ,  512, 4,  1, 0, 4, DT_ANY,  4097,  8192) \
+    X(19, OP_FWD, PATH_VECTOR ,  512, 4,  1, 0, 8, DT_ANY,  8193, 16384) \
+    X( 9, OP_FWD, PATH_VECTOR , 1024, 4,  1, 0, 1, DT_ANY,     0,     0) \
+    X(10, OP_FWD, PATH_VECTOR ,  128, 8,  2, 0, 1, DT_ANY,     0,     0) \
+    X(11, OP_FWD, PATH_VECTOR ,  512, 2,  1, 0, 1, DT_ANY,     0,     0) \
+    X(12, OP_FWD, PATH_VECTOR , 1024, 1,  1, 0, 1, DT_ANY,     0,     0) \
+    X(13, OP_FWD, PATH_VECTOR ,  256, 2,  2, 0, 1, DT_ANY,     0,     0) \
+    X(14, OP_FWD, PATH_VECTOR ,   64, 8,  4, 0, 1, DT_ANY,     0,     0) \
+    X(15, OP_FWD, PATH_VECTOR ,   16, 2, 16, 0, 1, DT_ANY,     0,     0) \
     /* forward, any N and alignment */ \
-    X(16, OP_FWD, PATH_GENERIC,  256, 0,  1, 0, 1,    0,    0) \
+    X(16, OP_FWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0) \
     /* backward main kernel, persistent, row in registers */ \
-    X(20, OP_BWD, PATH_VECTOR ,    8, 1, 32, 1, 1,    1,    8) \
-    X(21, OP_BWD, PATH_VECTOR ,   16, 1, 16, 1, 1,    9,   16) \
-    X(22, OP_BWD, PATH_VECTOR ,   32, 1,  8, 1, 1,   17,   32) \
-    X(23, OP_BWD, PATH_VECTOR ,   32, 2,  8, 1, 1,   33,   64) \
-    X(24, OP_BWD, PATH_VECTOR ,   64, 2,  4, 1, 1,   65,  128) \
-    X(25, OP_BWD, PATH_VECTOR ,  128, 2,  2, 1, 1,  129,  256) \
-    X(26, OP_BWD, PATH_VECTOR ,  256, 2,  2, 1, 1,  257,  512) \
-    X(27, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 1,  513, 1024) \
-    X(42, OP_BWD, PATH_VECTOR ,  512, 3,  1, 1, 1, 1025, 1536) \
-    X(45, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 2, 1537, 2048) \
-    X(46, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 4, 2049, 4096) \
-    X(47, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 8, 4097, 8192) \
-    X(32, OP_BWD, PATH_VECTOR ,  256, 1,  2, 2, 1,    0,    0) \
-    X(33, OP_BWD, PATH_VECTOR ,   16, 2, 16, 1, 1,    0,    0) \
-    X(34, OP_BWD, PATH_VECTOR ,  512, 2,  1, 2, 1,    0,    0) \
-    X(35, OP_BWD, PATH_VECTOR ,  512, 2,  1, 0, 1,    0,    0) \
-    X(38, OP_BWD, PATH_VECTOR ,  256, 2,  2, 2, 1,    0,    0) \
-    X(40, OP_BWD, PATH_VECTOR ,  128, 2,  2, 2, 1,    0,    0) \
-    X(41, OP_BWD, PATH_VECTOR ,  128, 2,  4, 1, 1,    0,    0) \
-    X(44, OP_BWD, PATH_VECTOR ,  512, 3,  1, 2, 1,    0,    0) \
-    X(48, OP_BWD, PATH_VECTOR ,  512, 3,  1, 1, 2,    0,    0) \
-    X(49, OP_BWD, PATH_VECTOR ,  512, 2,  1, 2, 2,    0,    0) \
-    X(50, OP_BWD, PATH_VECTOR ,  256, 2,  1, 1, 2,    0,    0) \
-    X(51, OP_BWD, PATH_VECTOR ,  512, 1,  1, 1, 2,    0,    0) \
-    X(52, OP_BWD, PATH_VECTOR ,  128, 2,  1, 1, 2,    0,    0) \
-    X(53, OP_BWD, PATH_VECTOR ,  256, 1,  1, 1, 2,    0,    0) \
-    X(54, OP_BWD, PATH_VECTOR ,  256, 2,  1, 1, 4,    0,    0) \
-    X(55, OP_BWD, PATH_VECTOR ,  128, 2,  1, 1, 4,    0,    0) \
+    X(20, OP_BWD, PATH_VECTOR ,    8, 1, 32, 1, 1, DT_ANY,     1,     8) \
+    X(21, OP_BWD, PATH_VECTOR ,   16, 1, 16, 1, 1, DT_ANY,     9,    16) \
+    X(22, OP_BWD, PATH_VECTOR ,   32, 1,  8, 1, 1, DT_ANY,    17,    32) \
+    X(23, OP_BWD, PATH_VECTOR ,   32, 2,  8, 1, 1, DT_ANY,    33,    64) \
+    X(24, OP_BWD, PATH_VECTOR ,   64, 2,  4, 1, 1, DT_ANY,    65,   128) \
+    X(25, OP_BWD, PATH_VECTOR ,  128, 2,  2, 1, 1, DT_ANY,   129,   256) \
+    X(26, OP_BWD, PATH_VECTOR ,  256, 2,  2, 1, 1, DT_BF16,   257,   512) \
+    X(38, OP_BWD, PATH_VECTOR ,  256, 2,  2, 2, 1, DT_F32,   257,   512) \
+    X(27, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 1, DT_BF16,   513,  1024) \
+    X(34, OP_BWD, PATH_VECTOR ,  512, 2,  1, 2, 1, DT_F32,   513,  1024) \
+    X(42, OP_BWD, PATH_VECTOR ,  512, 3,  1, 1, 1, DT_ANY,  1025,  1536) \
+    X(45, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 2, DT_ANY,  1537,  2048) \
+    X(46, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 4, DT_ANY,  2049,  4096) \
+    X(47, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 8, DT_ANY,  4097,  8192) \
+    X(32, OP_BWD, PATH_VECTOR ,  256, 1,  2, 2, 1, DT_ANY,     0,     0) \
+    X(33, OP_BWD, PATH_VECTOR ,   16, 2, 16, 1, 1, DT_ANY,     0,     0) \
+    X(35, OP_BWD, PATH_VECTOR ,  512, 2,  1, 0, 1, DT_ANY,     0,     0) \
+    X(40, OP_BWD, PATH_VECTOR ,  128, 2,  2, 2, 1, DT_ANY,     0,     0) \
+    X(41, OP_BWD, PATH_VECTOR ,  128, 2,  4, 1, 1, DT_ANY,     0,     0) \
+    X(44, OP_BWD, PATH_VECTOR ,  512, 3,  1, 2, 1, DT_ANY,     0,     0) \
+    X(48, OP_BWD, PATH_VECTOR ,  512, 3,  1, 1, 2, DT_ANY,     0,     0) \
+    X(49, OP_BWD, PATH_VECTOR ,  512, 2,  1, 2, 2, DT_ANY,     0,     0) \
+    X(50, OP_BWD, PATH_VECTOR ,  256, 2,  1, 1, 2, DT_ANY,     0,     0) \
+    X(51, OP_BWD, PATH_VECTOR ,  512, 1,  1, 1, 2, DT_ANY,     0,     0) \
+    X(52, OP_BWD, PATH_VECTOR ,  128, 2,  1, 1, 2, DT_ANY,     0,     0) \
+    X(53, OP_BWD, PATH_VECTOR ,  256, 1,  1, 1, 2, DT_ANY,     0,     0) \
+    X(54, OP_BWD, PATH_VECTOR ,  256, 2,  1, 1, 4, DT_ANY,     0,     0) \
+    X(55, OP_BWD, PATH_VECTOR ,  128, 2,  1, 1, 4, DT_ANY,     0,     0) \
     /* backward main kernel, any N and alignment */ \
-    X(36, OP_BWD, PATH_GENERIC,  256, 0,  1, 0, 1,    0,    0)
+    X(36, OP_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0)
 
 // Largest CTA any plan uses.
 constexpr int kMaxCtaThreads = 1024;

@@ -79,6 +79,15 @@ def test_fwd_generic_when_vector_cannot_serve(rn, dt, N):
     assert p["path_name"] == "generic"
 
 
+def test_dtype_specific_backward_defaults(rn):
+    # fp32 rows of 2052..4096 elements keep two rows of loads in flight;
+    # bf16 rows of the same byte width keep one
+    f = rn.plan_query(rn.OP_BWD, 16384, 4096, 0, num_sms=152, ctas_per_sm=1)
+    b = rn.plan_query(rn.OP_BWD, 16384, 8192, 1, num_sms=152, ctas_per_sm=1)
+    assert f["plan_id"] != b["plan_id"]
+    assert (f["threads_per_row"], f["chunks_per_thread"]) == (b["threads_per_row"], b["chunks_per_thread"])
+
+
 def test_misaligned_pointers_take_generic(rn):
     assert rn.plan_query(rn.OP_FWD, 4096, 7168, 1, aligned=False)["path_name"] == "generic"
     assert rn.plan_query(rn.OP_BWD, 4096, 2048, 0, aligned=False)["path_name"] == "generic"
