@@ -115,6 +115,7 @@ def to_f64(a, dtype) -> np.ndarray:
 
 def fwd(x, w, *, dtype, eps, offset, residual=None, nthreads=1):
     """RMSNorm forward (optionally with the fused residual add) on an M x N block.
+    ``w`` None is non-affine RMSNorm (weight factor 1, offset unused).
 
     Returns a dict with
       ``y``       R(y) in the storage type, shape (M, N)
@@ -125,7 +126,7 @@ def fwd(x, w, *, dtype, eps, offset, residual=None, nthreads=1):
     """
     x = _as_storage(x, dtype)
     M, N = x.shape
-    w = _as_storage(w, dtype, (N,))
+    w = _as_storage(w, dtype, (N,))   # None: non-affine (weight factor 1)
     residual = _as_storage(residual, dtype, (M, N))
     st = _NP_STORAGE[dtype]
     y = np.empty((M, N), dtype=st)
@@ -145,6 +146,8 @@ def bwd(dy, h, w, *, dtype, eps, offset, rstd=None, dres=None, want_dx=True, nth
     """RMSNorm backward on an M x N block.
 
     ``h`` is the normalised input (x, or residual_out of the fused forward).
+    ``w`` None is non-affine RMSNorm (weight factor 1; the dW outputs are
+    then the sums of dy xhat, which a non-affine layer does not use).
     ``rstd`` None recomputes rstd in double from h; otherwise the given
     float32 values are used. ``dres`` is the fused variant's incoming
     residual-stream gradient. With ``want_dx=False`` only the dW sums are
@@ -158,7 +161,7 @@ def bwd(dy, h, w, *, dtype, eps, offset, rstd=None, dres=None, want_dx=True, nth
     dy = _as_storage(dy, dtype)
     M, N = dy.shape
     h = _as_storage(h, dtype, (M, N))
-    w = _as_storage(w, dtype, (N,))
+    w = _as_storage(w, dtype, (N,))   # None: non-affine (g = dy; dW is not a result)
     dres = _as_storage(dres, dtype, (M, N))
     if rstd is not None:
         rstd = np.ascontiguousarray(rstd, dtype=np.float32)

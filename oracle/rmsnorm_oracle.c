@@ -32,6 +32,10 @@
  *   d rstd / d h_k = -rstd^3 h_k / N, hence
  *   dL/dh_k = rstd g_k - (rstd^3 h_k / N) sum_j g_j h_j = rstd (g_k - xhat_k c).
  *
+ * Non-affine RMSNorm (w == NULL): the weight factor (offset + w_j) is
+ * replaced by 1, so y_j = h_j * rstd, g_j = dy_j, and there is no dW (the
+ * Liger-Kernel page's "non-affine" case, Validation).
+ *
  * R() is round-to-nearest-even to the storage type: bf16 is rounded from
  * the double value in ONE step (no detour through binary32); fp32 by the C
  * cast. f64 "storage" (dtype 2) means no rounding at all; the pins use it
@@ -174,8 +178,8 @@ static void fwd_rows(fwd_job *jb)
         const double ms = ss / (double)N;
         const double rstd = 1.0 / sqrt(ms + jb->eps);
         for (int64_t j = 0; j < N; ++j) {
-            const double wj = load_elem(jb->dtype, jb->w, j);
-            const double yj = h[j] * rstd * (jb->offset + wj);
+            const double factor = jb->w ? jb->offset + load_elem(jb->dtype, jb->w, j) : 1.0;
+            const double yj = h[j] * rstd * factor;
             if (jb->y64) jb->y64[base + j] = yj;
             if (jb->y) jb->bad |= store_elem(jb->dtype, jb->y, base + j, yj);
             if (jb->h_out) jb->bad |= store_elem(jb->dtype, jb->h_out, base + j, h[j]);
@@ -246,7 +250,7 @@ static void bwd_rows(bwd_job *jb)
     const int64_t N = jb->N;
     double *hv = (double *)malloc((size_t)N * sizeof(double));
     double *wpo = (double *)malloc((size_t)N * sizeof(double));
-    for (int64_t j = 0; j < N; ++j) wpo[j] = jb->offset + load_elem(jb->dtype, jb->w, j);
+    for (int64_t j = 0; j < N; ++j) wpo[j] = jb->w ? jb->offset + load_elem(jb->dtype, jb->w, j) : 1.0;
     for (int64_t i = jb->row0; i < jb->row1; ++i) {
         const int64_t base = i * N;
         for (int64_t j = 0; j < N; ++j) hv[j] = load_elem(jb->dtype, jb->h, base + j);

@@ -17,12 +17,13 @@ SRC = os.path.join(ROOT, "oracle", "rmsnorm_oracle.c")
 MUTATIONS = {
     "sum_instead_of_mean": ("const double ms = ss / (double)N;", "const double ms = ss;"),
     "eps_outside_root": ("1.0 / sqrt(ms + jb->eps)", "1.0 / (sqrt(ms) + jb->eps)"),
-    "offset_dropped_fwd": ("h[j] * rstd * (jb->offset + wj)", "h[j] * rstd * wj"),
-    "w_index_reversed": ("load_elem(jb->dtype, jb->w, j);\n            const double yj",
-                         "load_elem(jb->dtype, jb->w, N - 1 - j);\n            const double yj"),
+    "offset_dropped_fwd": ("const double factor = jb->w ? jb->offset + load_elem",
+                           "const double factor = jb->w ? load_elem"),
+    "w_index_reversed": ("load_elem(jb->dtype, jb->w, j) : 1.0;\n            const double yj",
+                         "load_elem(jb->dtype, jb->w, N - 1 - j) : 1.0;\n            const double yj"),
     "bwd_sign_flip": ("rstd * (g - xhat * c)", "rstd * (g + xhat * c)"),
     "bwd_c_not_mean": ("c /= (double)N;", "c /= 1.0;"),
-    "bwd_offset_dropped": ("wpo[j] = jb->offset + load_elem", "wpo[j] = 0.0 * jb->offset + load_elem"),
+    "bwd_offset_dropped": ("wpo[j] = jb->w ? jb->offset + load_elem", "wpo[j] = jb->w ? 0.0 * jb->offset + load_elem"),
     "dw_uses_g": ("jb->dw[j] += dyj * xhat;", "jb->dw[j] += g * xhat;"),
     "dw_missing_rstd": ("jb->dw[j] += dyj * xhat;", "jb->dw[j] += dyj * hv[j];"),
     "dres_dropped": ("dxj += d;", "dxj += 0.0 * d;"),
@@ -31,6 +32,8 @@ MUTATIONS = {
     "bf16_via_binary32": ("uint16_t sign = signbit(v) ? 0x8000u : 0u;",
                           "v = (double)(float)v;\n    uint16_t sign = signbit(v) ? 0x8000u : 0u;"),
     "bf16_ties_away": ("double q = rint(ldexp(m, 8));", "double q = round(ldexp(m, 8));"),
+    "non_affine_keeps_offset": ("load_elem(jb->dtype, jb->w, j) : 1.0;\n            const double yj",
+                                "load_elem(jb->dtype, jb->w, j) : jb->offset + 1.0;\n            const double yj"),
 }
 
 

@@ -311,3 +311,44 @@ def test_fused_bwd_zero_dres_equals_plain_plus_nothing():
     b = oracle.bwd(d["dy"], h, d["w"], dtype="f32", eps=1e-6, offset=0.0,
                    dres=np.zeros_like(d["dy"]))
     assert np.array_equal(a["dx64"], b["dx64"])
+
+
+# ------------------------------------------------------------ non-affine --
+
+def test_non_affine_is_affine_with_unit_weight():
+    # without a weight the factor is exactly 1 (offset unused)
+    x = f64((5, 30), 40)
+    dy = f64((5, 30), 41)
+    a = oracle.fwd(x, None, dtype="f64", eps=1e-3, offset=7.0)
+    b = oracle.fwd(x, np.ones(30), dtype="f64", eps=1e-3, offset=0.0)
+    assert np.array_equal(a["y64"], b["y64"]) and np.array_equal(a["rstd64"], b["rstd64"])
+    ga = oracle.bwd(dy, x, None, dtype="f64", eps=1e-3, offset=7.0)
+    gb = oracle.bwd(dy, x, np.ones(30), dtype="f64", eps=1e-3, offset=0.0)
+    assert np.array_equal(ga["dx64"], gb["dx64"])
+
+
+def test_non_affine_hand_example_and_unit_rms():
+    # x = (3, 4): y = x / sqrt(12.5); the output row has mean square 1 at eps 0
+    r = oracle.fwd(np.array([[3.0, 4.0]]), None, dtype="f64", eps=0.0, offset=0.0)
+    assert r["y64"][0] == pytest.approx([3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rel=1e-15)
+    y = oracle.fwd(f64((4, 64), 42), None, dtype="f64", eps=0.0, offset=0.0)["y64"]
+    np.testing.assert_allclose(np.mean(y * y, axis=1), 1.0, rtol=1e-14)
+
+
+@pytest.mark.parametrize("eps", [0.1, 1e-6])
+def test_non_affine_bwd_matches_finite_differences(eps):
+    M, N = 3, 6
+    rng = np.random.default_rng(43)
+    x = rng.standard_normal((M, N))
+    dy = rng.standard_normal((M, N))
+    an = oracle.bwd(dy, x, None, dtype="f64", eps=eps, offset=0.0)
+
+    def loss(v):
+        return float(np.sum(oracle.fwd(v, None, dtype="f64", eps=eps, offset=0.0)["y64"] * dy))
+
+    for idx in np.ndindex(M, N):
+        step = 1e-6 * max(1.0, abs(x[idx]))
+        xp = x.copy(); xp[idx] += step
+        xm = x.copy(); xm[idx] -= step
+        fd = (loss(xp) - loss(xm)) / (2 * step)
+        assert abs(fd - an["dx64"][idx]) <= 1e-7 * max(abs(an["dx64"][idx]), an["dx_scale"][idx]) + 1e-9
