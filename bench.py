@@ -265,6 +265,8 @@ def sweep_points():
             pts.append((f"{dt} {M}x{N}", dt, M, N, False, False))
     for M, N in ((4096, 4096), (1024, 8192)):
         pts.append((f"add bf16 {M}x{N}", "bf16", M, N, True, False))
+    pts.append(("nonaffine bf16 16384x8192", "bf16", 16384, 8192, False, False))
+    pts.append(("nonaffine f32 16384x6144", "f32", 16384, 6144, False, False))
     pts.append(("misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
     pts.append(("misaligned f32 4096x2048", "f32", 4096, 2048, False, True))
     pts.append(("wide f32 16384x6144", "f32", 16384, 6144, False, False))
@@ -303,6 +305,7 @@ def run_sweep(args):
             buf = torch.randn(n + off, generator=g, device=dev, dtype=torch.float32).to(td)
             return buf[off:off + n]
 
+        affine = not label.startswith("nonaffine")
         x = mk(M * N).view(M, N)
         dy = mk(M * N).view(M, N)
         w = (1 + 0.1 * mk(N).float()).to(td)
@@ -313,6 +316,8 @@ def run_sweep(args):
         y = mk(M * N).view(M, N)
         dx = mk(M * N).view(M, N)
         dw = torch.empty_like(w)
+        if not affine:
+            w, dw = None, None
         rstd = torch.empty(M, dtype=torch.float32, device=dev)
         res = mk(M * N).view(M, N) if fused else None
         hout = torch.empty_like(x) if fused else None
@@ -330,8 +335,9 @@ def run_sweep(args):
                                         dx=dx, dw=dw, workspace=ws)
         P = bplan["ctas"]
         k = 1 if fused else 0
-        by = {"fwd": (2 + 2 * k) * M * N * s + N * s + 4 * M,
-              "bwd": (3 + k) * M * N * s + 2 * N * s + 4 * M + 8 * P * N}
+        wb = 1 if affine else 0   # the weight, dW and the workspace exist only with a weight
+        by = {"fwd": (2 + 2 * k) * M * N * s + wb * N * s + 4 * M,
+              "bwd": (3 + k) * M * N * s + wb * (2 * N * s + 8 * P * N) + 4 * M}
         for op, fn, plan in (("fwd", fwd, fplan), ("bwd", bwd, bplan)):
             for _ in range(3):
                 fn()

@@ -84,6 +84,9 @@ typedef enum {
  * Forward. Reads x [M,N] and w [N]; writes y [M,N] and rstd [M] (fp32).
  * Liger-Kernel PR #1388, Summary and section 1 (vector forward with a
  * CTA-level reduction; eps and offset runtime scalars).
+ * w == NULL: non-affine RMSNorm, y = x * rstd (the weight factor is 1 and
+ * offset is unused; Liger-Kernel PR #1388, Validation: affine and
+ * non-affine launches).
  */
 rmsnorm_status_t rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd,
                              int64_t M, int64_t N, rmsnorm_dtype_t dt,
@@ -102,6 +105,8 @@ rmsnorm_status_t rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd,
  * by any other call in flight. Its contents on entry do not matter (every
  * byte read is first written by this call). With NULL the library takes
  * stream-ordered memory (cudaMallocAsync/cudaFreeAsync on `stream`).
+ * w == NULL: non-affine backward (g = dy); dw must then be NULL too (there
+ * is no weight gradient), no workspace is used and only the main kernel runs.
  */
 rmsnorm_status_t rmsnorm_bwd(const void *dy, const void *x, const void *w, const float *rstd,
                              void *dx, void *dw, void *workspace, size_t workspace_bytes,
@@ -112,7 +117,8 @@ rmsnorm_status_t rmsnorm_bwd(const void *dy, const void *x, const void *w, const
  * Fused residual add + forward. h = R(x + residual) is rounded to the
  * storage type, written to residual_out [M,N] and normalised into y
  * (FlyDSL PR #855, Implementation: fused-add RMSNorm as a specialisation
- * of the same kernels). residual_out may equal residual.
+ * of the same kernels). residual_out may equal residual. w may be NULL
+ * (non-affine), as in rmsnorm_fwd.
  */
 rmsnorm_status_t rmsnorm_add_fwd(const void *x, const void *residual, const void *w,
                                  void *y, void *residual_out, float *rstd,
@@ -124,7 +130,7 @@ rmsnorm_status_t rmsnorm_add_fwd(const void *x, const void *residual, const void
  * receives rstd * (g - xhat * c) + dresidual_out, the gradient of both x
  * and residual (one buffer serves as dx and dresidual, FlyDSL PR #855,
  * Implementation). dresidual_out may be NULL (treated as zero) or equal dx.
- * Workspace rules as in rmsnorm_bwd.
+ * Workspace and non-affine (w, dw NULL) rules as in rmsnorm_bwd.
  */
 rmsnorm_status_t rmsnorm_add_bwd(const void *dy, const void *dresidual_out, const void *h,
                                  const void *w, const float *rstd, void *dx, void *dw,

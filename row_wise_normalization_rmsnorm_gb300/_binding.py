@@ -150,15 +150,17 @@ def _ws(workspace):
 
 
 def rmsnorm_fwd(x, w, *, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=None, stream=None):
-    """y, rstd = RMSNorm(x) over the last dimension (llama mode)."""
+    """y, rstd = RMSNorm(x) over the last dimension (llama mode); w None is
+    non-affine RMSNorm (y = x * rstd)."""
     M, N = _rows(x)
     _check(x, "x")
-    _check(w, "w", like=x, numel=N)
+    if w is not None:
+        _check(w, "w", like=x, numel=N)
     y = torch.empty_like(x) if y is None else y
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
     _check(y, "y", like=x, numel=x.numel())
     _check(rstd, "rstd", numel=M)
-    st = lib().rmsnorm_fwd(x.data_ptr(), w.data_ptr(), y.data_ptr(), rstd.data_ptr(), M, N, _dtype_code(x),
+    st = lib().rmsnorm_fwd(x.data_ptr(), _ptr(w), y.data_ptr(), rstd.data_ptr(), M, N, _dtype_code(x),
                            eps, offset, _stream_handle(stream, x.device))
     _raise(st, "rmsnorm_fwd")
     return y, rstd
@@ -170,14 +172,15 @@ def rmsnorm_add_fwd(x, residual, w, *, eps: float = 1e-6, offset: float = 0.0, y
     M, N = _rows(x)
     _check(x, "x")
     _check(residual, "residual", like=x, numel=x.numel())
-    _check(w, "w", like=x, numel=N)
+    if w is not None:
+        _check(w, "w", like=x, numel=N)
     y = torch.empty_like(x) if y is None else y
     residual_out = torch.empty_like(x) if residual_out is None else residual_out
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
     _check(y, "y", like=x, numel=x.numel())
     _check(residual_out, "residual_out", like=x, numel=x.numel())
     _check(rstd, "rstd", numel=M)
-    st = lib().rmsnorm_add_fwd(x.data_ptr(), residual.data_ptr(), w.data_ptr(), y.data_ptr(),
+    st = lib().rmsnorm_add_fwd(x.data_ptr(), residual.data_ptr(), _ptr(w), y.data_ptr(),
                                residual_out.data_ptr(), rstd.data_ptr(), M, N, _dtype_code(x), eps, offset,
                                _stream_handle(stream, x.device))
     _raise(st, "rmsnorm_add_fwd")
@@ -186,19 +189,22 @@ def rmsnorm_add_fwd(x, residual, w, *, eps: float = 1e-6, offset: float = 0.0, y
 
 def rmsnorm_bwd(dy, x, w, rstd, *, eps: float = 1e-6, offset: float = 0.0, dx=None, dw=None, workspace=None,
                 stream=None):
-    """dx, dw of RMSNorm given the forward's rstd."""
+    """dx, dw of RMSNorm given the forward's rstd; w None is non-affine (dw None)."""
     M, N = _rows(x)
     for t, n in ((dy, "dy"), (x, "x")):
         _check(t, n, like=x, numel=x.numel())
-    _check(w, "w", like=x, numel=N)
     _check(rstd, "rstd", numel=M)
     dx = torch.empty_like(x) if dx is None else dx
-    dw = torch.empty_like(w) if dw is None else dw
     _check(dx, "dx", like=x, numel=x.numel())
-    _check(dw, "dw", like=x, numel=N)
+    if w is not None:
+        _check(w, "w", like=x, numel=N)
+        dw = torch.empty_like(w) if dw is None else dw
+        _check(dw, "dw", like=x, numel=N)
+    else:
+        dw = None
     wp, wb = _ws(workspace)
-    st = lib().rmsnorm_bwd(dy.data_ptr(), x.data_ptr(), w.data_ptr(), rstd.data_ptr(), dx.data_ptr(),
-                           dw.data_ptr(), wp, wb, M, N, _dtype_code(x), eps, offset,
+    st = lib().rmsnorm_bwd(dy.data_ptr(), x.data_ptr(), _ptr(w), rstd.data_ptr(), dx.data_ptr(),
+                           _ptr(dw), wp, wb, M, N, _dtype_code(x), eps, offset,
                            _stream_handle(stream, x.device))
     _raise(st, "rmsnorm_bwd")
     return dx, dw
@@ -212,15 +218,18 @@ def rmsnorm_add_bwd(dy, dresidual_out, h, w, rstd, *, eps: float = 1e-6, offset:
     _check(h, "h", like=h, numel=h.numel())
     if dresidual_out is not None:
         _check(dresidual_out, "dresidual_out", like=h, numel=h.numel())
-    _check(w, "w", like=h, numel=N)
     _check(rstd, "rstd", numel=M)
     dx = torch.empty_like(h) if dx is None else dx
-    dw = torch.empty_like(w) if dw is None else dw
     _check(dx, "dx", like=h, numel=h.numel())
-    _check(dw, "dw", like=h, numel=N)
+    if w is not None:
+        _check(w, "w", like=h, numel=N)
+        dw = torch.empty_like(w) if dw is None else dw
+        _check(dw, "dw", like=h, numel=N)
+    else:
+        dw = None
     wp, wb = _ws(workspace)
-    st = lib().rmsnorm_add_bwd(dy.data_ptr(), _ptr(dresidual_out), h.data_ptr(), w.data_ptr(), rstd.data_ptr(),
-                               dx.data_ptr(), dw.data_ptr(), wp, wb, M, N, _dtype_code(h), eps, offset,
+    st = lib().rmsnorm_add_bwd(dy.data_ptr(), _ptr(dresidual_out), h.data_ptr(), _ptr(w), rstd.data_ptr(),
+                               dx.data_ptr(), _ptr(dw), wp, wb, M, N, _dtype_code(h), eps, offset,
                                _stream_handle(stream, h.device))
     _raise(st, "rmsnorm_add_bwd")
     return dx, dw
@@ -263,7 +272,8 @@ def rmsnorm_bwd_ex(dy, x, w, rstd, *, dresidual_out=None, fused=False, eps=1e-6,
     """Backward with forced plan / CTA count / packed math; returns (dx, dw, plan dict)."""
     M, N = _rows(x)
     dx = torch.empty_like(x) if dx is None else dx
-    dw = torch.empty_like(w) if dw is None else dw
+    if w is not None and dw is None:
+        dw = torch.empty_like(w)
     wp, wb = _ws(workspace)
     ev = None if event_after_main is None else event_after_main.cuda_event
     p = Plan()

@@ -320,13 +320,13 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (M == 0) return RMSNORM_SUCCESS;
     const bool fused = residual != nullptr || residual_out != nullptr;
     if (fused && (!residual || !residual_out)) return RMSNORM_ERR_INVALID_ARG;
-    if (!x || !w || !y || !rstd) return RMSNORM_ERR_INVALID_ARG;
+    if (!x || !y || !rstd) return RMSNORM_ERR_INVALID_ARG;  // w NULL: non-affine
     const uintptr_t s = (uintptr_t)elem_size(dt);
-    if (!aligned_to(x, s) || !aligned_to(w, s) || !aligned_to(y, s) || !aligned_to(rstd, 4))
+    if (!aligned_to(x, s) || (w && !aligned_to(w, s)) || !aligned_to(y, s) || !aligned_to(rstd, 4))
         return RMSNORM_ERR_INVALID_ARG;
     if (fused && (!aligned_to(residual, s) || !aligned_to(residual_out, s))) return RMSNORM_ERR_INVALID_ARG;
 
-    bool aligned = aligned_to(x, 16) && aligned_to(w, 16) && aligned_to(y, 16);
+    bool aligned = aligned_to(x, 16) && (!w || aligned_to(w, 16)) && aligned_to(y, 16);
     if (fused) aligned = aligned && aligned_to(residual, 16) && aligned_to(residual_out, 16);
 
     rmsnorm_plan_t plan;
@@ -364,19 +364,23 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     if (force_packed < -1 || force_packed > 1) return RMSNORM_ERR_INVALID_ARG;
     if (!fused) dres = nullptr;
     const uintptr_t s = (uintptr_t)elem_size(dt);
+    // Non-affine (w NULL): there is no dW, so dw must be NULL as well.
+    if ((w == nullptr) != (dw == nullptr)) return RMSNORM_ERR_INVALID_ARG;
+    const bool affine = w != nullptr;
     if (M == 0) {
         // dw is the empty sum; the empty [0, N] tensors may be NULL
-        if (!dw || !aligned_to(dw, s)) return RMSNORM_ERR_INVALID_ARG;
+        if (!affine) return RMSNORM_SUCCESS;
+        if (!aligned_to(dw, s)) return RMSNORM_ERR_INVALID_ARG;
         cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)N * s, stream);
         if (e != cudaSuccess) return cuda_fail(e);
         return RMSNORM_SUCCESS;
     }
-    if (!dy || !x || !w || !rstd || !dx || !dw) return RMSNORM_ERR_INVALID_ARG;
-    if (!aligned_to(dy, s) || !aligned_to(x, s) || !aligned_to(w, s) || !aligned_to(dx, s) ||
-        !aligned_to(dw, s) || !aligned_to(rstd, 4) || (dres && !aligned_to(dres, s)))
+    if (!dy || !x || !rstd || !dx) return RMSNORM_ERR_INVALID_ARG;
+    if (!aligned_to(dy, s) || !aligned_to(x, s) || (affine && (!aligned_to(w, s) || !aligned_to(dw, s))) ||
+        !aligned_to(dx, s) || !aligned_to(rstd, 4) || (dres && !aligned_to(dres, s)))
         return RMSNORM_ERR_INVALID_ARG;
     if (workspace && !aligned_to(workspace, 16)) return RMSNORM_ERR_WORKSPACE;
-    bool aligned = aligned_to(dy, 16) && aligned_to(x, 16) && aligned_to(w, 16) && aligned_to(dx, 16);
+    bool aligned = aligned_to(dy, 16) && aligned_to(x, 16) && (!affine || aligned_to(w, 16)) && aligned_to(dx, 16);
     if (dres) aligned = aligned && aligned_to(dres, 16);
 
     int dev = 0, sms = 0;
@@ -398,7 +402,9 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
 
     float *ws = static_cast<float *>(workspace);
     bool owned = false;
-    if (ws) {
+    if (!affine) {
+        ws = nullptr;  // non-affine: no dW partials, no workspace
+    } else if (ws) {
         if (ws_bytes < (size_t)plan.workspace_bytes) return RMSNORM_ERR_WORKSPACE;
     } else {
         void *tmp = nullptr;
@@ -431,7 +437,7 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
                  ? launch_bwd_main_bf16(plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream)
                  : launch_bwd_main_f32(plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream);
     if (le == 0 && event_after_main) le = (int)cudaEventRecord(static_cast<cudaEvent_t>(event_after_main), stream);
-    if (le == 0)
+    if (le == 0 && affine)
         le = dt == RMSNORM_BF16
                  ? launch_dw_finalize_bf16(ws, plan.ws_rows, (int)N, dw, stream, event_after_main != nullptr)
                  : launch_dw_finalize_f32(ws, plan.ws_rows, (int)N, dw, stream, event_after_main != nullptr);

@@ -83,17 +83,20 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     if constexpr (CS > 1) rank = cluster_ctarank();
     const int cbase = (int)rank * TPR * V;  // first chunk of this CTA's slice
 
-    // (offset + w) for this thread's columns: loaded once per CTA.
+    // (offset + w) for this thread's columns: loaded once per CTA. Without
+    // a weight (non-affine) the factor is 1 and there is no dW.
+    const bool has_w = p.w != nullptr;
     const float2 o2 = make_float2(p.offset, p.offset);
     float2 wp[V][NP], acc[V][NP];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
         float2 wv[NP];
-        unpack<T>(c < C ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + c) : make_uint4(0, 0, 0, 0), wv);
+        unpack<T>((has_w && c < C) ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + c) : make_uint4(0, 0, 0, 0),
+                  wv);
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
-            wp[v][k] = Pk::add(o2, wv[k]);
+            wp[v][k] = has_w ? Pk::add(o2, wv[k]) : make_float2(1.f, 1.f);
             acc[v][k] = make_float2(0.f, 0.f);
         }
     }
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             }
             // while the partials travel: the dW partial, which does not
             // need the row sum
-            if (valid) {
+            if (valid && has_w) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     float2 xf[NP], df[NP];
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                 const float2 xh = Pk::mul(xf[q], r2);
                 const float2 g = Pk::mul(df[q], wp[v][q]);
                 out[q] = Pk::mul(Pk::fma(xh, nc2, g), r2);
-                if (CS == 1 && valid) acc[v][q] = Pk::fma(df[q], xh, acc[v][q]);
+                if (CS == 1 && valid && has_w) acc[v][q] = Pk::fma(df[q], xh, acc[v][q]);
             }
             if (has_dres) {
                 float2 rf[NP];
@@ -242,6 +245,8 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     // The finalizer may start launching now; it waits for this grid to
     // finish (griddepcontrol.wait) before it reads the workspace.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (!has_w) return;  // non-affine: no dW partials
 
     // Combine the CTA's teams in team order, then write the unit's partial
     // row ws[unit, :] (a cluster's CTAs each write their slice of it).
@@ -310,18 +315,19 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
         const float r = p.rstd[row];
         float dot = 0.f;
         for (int j = threadIdx.x; j < N; j += blockDim.x) {
-            const float g = __fmul_rn(load_elem(dy, j), __fadd_rn(p.offset, load_w(w, j)));
+            const float dyj = load_elem(dy, j);
+            const float g = w ? __fmul_rn(dyj, __fadd_rn(p.offset, load_w(w, j))) : dyj;
             dot = __fmaf_rn(g, __fmul_rn(load_elem(x, j), r), dot);
         }
         const float cm = -__fdiv_rn(cta_allreduce(dot, red), (float)N);
         for (int j = threadIdx.x; j < N; j += blockDim.x) {
             const float dyj = load_elem(dy, j);
             const float xh = __fmul_rn(load_elem(x, j), r);
-            const float g = __fmul_rn(dyj, __fadd_rn(p.offset, load_w(w, j)));
+            const float g = w ? __fmul_rn(dyj, __fadd_rn(p.offset, load_w(w, j))) : dyj;
             float d = __fmul_rn(__fmaf_rn(xh, cm, g), r);
             if (has_dres) d = __fadd_rn(d, load_elem(dr, j));
             store_elem(dx, j, d);
-            wsrow[j] = first ? __fmul_rn(dyj, xh) : __fmaf_rn(dyj, xh, wsrow[j]);
+            if (w) wsrow[j] = first ? __fmul_rn(dyj, xh) : __fmaf_rn(dyj, xh, wsrow[j]);
         }
         first = false;
     }

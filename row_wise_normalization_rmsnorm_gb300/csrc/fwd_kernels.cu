@@ -99,15 +99,22 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 
     const float2 r2 = make_float2(rstd, rstd);
     const float2 o2 = make_float2(p.offset, p.offset);
+    const bool has_w = p.w != nullptr;  // no weight: non-affine, factor 1
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
         if (c < C) {
-            float2 a[NP], wv[NP];
+            float2 a[NP];
             unpack<T>(xv[v], a);
-            unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.w) + c), wv);
+            if (has_w) {
+                float2 wv[NP];
+                unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.w) + c), wv);
 #pragma unroll
-            for (int k = 0; k < NP; ++k) a[k] = Pk::mul(Pk::mul(a[k], r2), Pk::add(o2, wv[k]));
+                for (int k = 0; k < NP; ++k) a[k] = Pk::mul(Pk::mul(a[k], r2), Pk::add(o2, wv[k]));
+            } else {
+#pragma unroll
+                for (int k = 0; k < NP; ++k) a[k] = Pk::mul(a[k], r2);
+            }
             st_chunk(reinterpret_cast<uint4 *>(p.y) + base + c, pack<T>(a));
         }
     }
@@ -139,7 +146,8 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     for (int j = threadIdx.x; j < N; j += blockDim.x) {
         // The same thread wrote hout[j] above, so it reads its own value.
         const float h = FUSED ? load_elem(static_cast<const T *>(hout), j) : load_elem(x, j);
-        store_elem(y, j, __fmul_rn(__fmul_rn(h, rstd), __fadd_rn(p.offset, load_w(w, j))));
+        const float hr = __fmul_rn(h, rstd);
+        store_elem(y, j, w ? __fmul_rn(hr, __fadd_rn(p.offset, load_w(w, j))) : hr);
     }
 }
 

@@ -180,3 +180,34 @@ def test_full_size_wide_rows(rn, name):
     check_dx(to_host(dx[rows_t], dt), b, dt)
     full = oracle.bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=eps, offset=0.0, rstd=r32, want_dx=False, nthreads=8)
     check_dw(to_host(dw, dt), full, dt)
+
+
+# ------------------------------------------------------------ non-affine --
+
+@pytest.mark.parametrize("dt,M,N", [("bf16", 4096, 2048), ("f32", 300, 6144), ("bf16", 257, 16384),
+                                    ("f32", 65, 16384), ("bf16", 211, 4097), ("bf16", 333, 128)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_non_affine_matches_oracle(rn, dt, M, N, fused):
+    """w absent: y = h rstd, dx = rstd (dy - xhat c), no dW."""
+    d = inputs.make_inputs(M, N, dt, 110 + N % 7, residual=fused, dres=fused)
+    x, dy = to_dev(d["x"], dt), to_dev(d["dy"], dt)
+    if fused:
+        y, h, rstd = rn.rmsnorm_add_fwd(x, to_dev(d["residual"], dt), None)
+    else:
+        y, rstd = rn.rmsnorm_fwd(x, None)
+        h = x
+    f = oracle.fwd(d["x"], None, dtype=dt, eps=1e-6, offset=0.0, residual=d.get("residual") if fused else None)
+    torch.cuda.synchronize()
+    check_y(to_host(y, dt), f, dt)
+    check_rstd(rstd.cpu().numpy(), f["rstd64"])
+    h_np = f["h"] if fused else d["x"]
+    r32 = torch.from_numpy(f["rstd32"]).cuda()
+    if fused:
+        dx, dw = rn.rmsnorm_add_bwd(dy, to_dev(d["dres"], dt), to_dev(h_np, dt), None, r32)
+    else:
+        dx, dw = rn.rmsnorm_bwd(dy, h, None, r32)
+    assert dw is None
+    b = oracle.bwd(d["dy"], h_np, None, dtype=dt, eps=1e-6, offset=0.0, rstd=f["rstd32"],
+                   dres=d.get("dres") if fused else None)
+    torch.cuda.synchronize()
+    check_dx(to_host(dx, dt), b, dt)

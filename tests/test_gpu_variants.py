@@ -255,3 +255,30 @@ def test_device_status_clean_after_cluster_rows(rn):
         rn.rmsnorm_bwd(t["dy"], t["x"], t["w"], r)
     torch.cuda.synchronize()
     assert rn.lib().rmsnorm_device_status(0) == 0
+
+
+@pytest.mark.parametrize("dt,N", [("bf16", 8192), ("f32", 16384), ("bf16", 4097), ("bf16", 128)])
+def test_non_affine_equals_unit_weight_bitwise(rn, dt, N):
+    """Without a weight the factor is exactly 1: y, rstd and dx equal those of
+    a weight of ones with offset 0, bit for bit."""
+    _, t = dev_inputs(500, N, dt, 104)
+    ones = torch.ones_like(t["w"])
+    y0, r0 = rn.rmsnorm_fwd(t["x"], ones, offset=0.0)
+    y1, r1 = rn.rmsnorm_fwd(t["x"], None, offset=3.0)
+    dx0, _ = rn.rmsnorm_bwd(t["dy"], t["x"], ones, r0, offset=0.0)
+    dx1, dw1 = rn.rmsnorm_bwd(t["dy"], t["x"], None, r0, offset=3.0)
+    torch.cuda.synchronize()
+    assert dw1 is None
+    assert cuda_bits_equal(y0, y1) and cuda_bits_equal(r0, r1) and cuda_bits_equal(dx0, dx1)
+
+
+def test_non_affine_argument_rules(rn):
+    _, t = dev_inputs(16, 256, "bf16", 105)
+    _, r = rn.rmsnorm_fwd(t["x"], None)
+    L = rn.lib()
+    s = torch.cuda.current_stream().cuda_stream
+    # a weight without dw, or dw without a weight, is refused
+    assert L.rmsnorm_bwd(t["dy"].data_ptr(), t["x"].data_ptr(), t["w"].data_ptr(), r.data_ptr(),
+                         t["dy"].data_ptr(), None, None, 0, 16, 256, 1, 1e-6, 0.0, s) == 1
+    assert L.rmsnorm_bwd(t["dy"].data_ptr(), t["x"].data_ptr(), None, r.data_ptr(),
+                         t["dy"].data_ptr(), t["w"].data_ptr(), None, 0, 16, 256, 1, 1e-6, 0.0, s) == 1
