@@ -15,8 +15,9 @@ to RMSNorm" (Summary, section 2) and the FlyDSL page "[Perf] Optimize
 RMSNorm backward with staged reduction and vec8 I/O" (Implementation).
 
 Storage types: ``"bf16"`` arrays are numpy ``uint16`` bit patterns,
-``"f32"`` arrays are ``float32``, ``"f64"`` arrays are ``float64`` (no
-rounding; used by the finite-difference pins).
+``"f16"`` arrays are ``float16``, ``"f32"`` arrays are ``float32``,
+``"f64"`` arrays are ``float64`` (no rounding; used by the finite-difference
+pins).
 
 Every function here is pinned by ``tests/test_oracle_pins.py``.
 """
@@ -33,8 +34,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "rmsnorm_oracle.c")
 _LIB = os.path.join(_HERE, "librmsnorm_oracle.so")
 
-_DTYPE_CODE = {"f32": 0, "bf16": 1, "f64": 2}
-_NP_STORAGE = {"f32": np.float32, "bf16": np.uint16, "f64": np.float64}
+_DTYPE_CODE = {"f32": 0, "bf16": 1, "f64": 2, "f16": 3}
+_NP_STORAGE = {"f32": np.float32, "bf16": np.uint16, "f64": np.float64, "f16": np.float16}
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +73,8 @@ def _load():
             lib.oracle_bf16_round_array.argtypes = [vp, i64, vp]
             lib.oracle_bf16_decode.restype = dbl
             lib.oracle_bf16_decode.argtypes = [ctypes.c_uint16]
+            lib.oracle_f16_round_array.restype = i32
+            lib.oracle_f16_round_array.argtypes = [vp, i64, vp]
             _lib = lib
     return _lib
 
@@ -104,6 +107,14 @@ def bf16_decode(b) -> np.ndarray:
     """Exact value of bf16 bit patterns as float64 (bf16 is the top half of binary32)."""
     b = np.ascontiguousarray(b, dtype=np.uint16)
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def f16_round(v) -> np.ndarray:
+    """Round float64 values to binary16 (ties to even) in one step; returns float16."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_f16_round_array(_ptr(v), v.size, _ptr(out))
+    return out.view(np.float16)
 
 
 def to_f64(a, dtype) -> np.ndarray:

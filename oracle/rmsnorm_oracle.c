@@ -36,9 +36,9 @@
  * replaced by 1, so y_j = h_j * rstd, g_j = dy_j, and there is no dW (the
  * Liger-Kernel page's "non-affine" case, Validation).
  *
- * R() is round-to-nearest-even to the storage type: bf16 is rounded from
- * the double value in ONE step (no detour through binary32); fp32 by the C
- * cast. f64 "storage" (dtype 2) means no rounding at all; the pins use it
+ * R() is round-to-nearest-even to the storage type: bf16 and fp16 are
+ * rounded from the double value in ONE step (no detour through binary32);
+ * fp32 by the C cast. f64 "storage" (dtype 2) means no rounding at all; the pins use it
  * for finite differences.
  *
  * Parity pins live in tests/test_oracle_pins.py.
@@ -49,7 +49,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { OR_F32 = 0, OR_BF16 = 1, OR_F64 = 2 };
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F64 = 2, OR_F16 = 3 };
 
 /* ---------------------------------------------------------------- bf16 -- */
 
@@ -98,6 +98,53 @@ int oracle_bf16_round(double v, uint16_t *out)
     return 0;
 }
 
+/* ---------------------------------------------------------------- fp16 -- */
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_f16_decode(uint16_t b)
+{
+    const int sign = (b >> 15) & 1;
+    const int e = (b >> 10) & 0x1f;
+    const int f = b & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);                  /* subnormal: f * 2^-24 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f + 1024), e - 25);      /* (1024 + f) * 2^(e-15-10) */
+    return sign ? -v : v;
+}
+
+/*
+ * Round a double to binary16, nearest with ties to even, in a single step.
+ * Returns 0 for an ordinary finite result (normal, subnormal or zero), 1
+ * when v is NaN or the rounded value overflows to infinity.
+ */
+int oracle_f16_round(double v, uint16_t *out)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v);
+    if (isnan(v)) { *out = 0x7e00u; return 1; }
+    if (isinf(v)) { *out = (uint16_t)(sign | 0x7c00u); return 1; }
+    if (a == 0.0) { *out = sign; return 0; }
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range, quantum 2^-24; 1024 is the smallest normal,
+         * whose encoding is also 1024 (0x0400) */
+        double q = rint(ldexp(a, 24));
+        *out = (uint16_t)(sign | (uint16_t)q);
+        return 0;
+    }
+    int e;
+    double m = frexp(a, &e);          /* a = m * 2^e, 0.5 <= m < 1 */
+    double q = rint(ldexp(m, 11));    /* 11 significant bits: 1024..2048 */
+    if (q == 2048.0) { q = 1024.0; e += 1; }
+    int be = e - 1 + 15;
+    if (be >= 31) { *out = (uint16_t)(sign | 0x7c00u); return 1; }
+    *out = (uint16_t)(sign | (uint16_t)(be << 10) | (uint16_t)((int)q - 1024));
+    return 0;
+}
+
 /* ------------------------------------------------------- storage access -- */
 
 static double load_elem(int dtype, const void *p, int64_t i)
@@ -105,6 +152,7 @@ static double load_elem(int dtype, const void *p, int64_t i)
     switch (dtype) {
     case OR_BF16: return oracle_bf16_decode(((const uint16_t *)p)[i]);
     case OR_F32:  return (double)((const float *)p)[i];
+    case OR_F16:  return oracle_f16_decode(((const uint16_t *)p)[i]);
     default:      return ((const double *)p)[i];
     }
 }
@@ -124,6 +172,12 @@ static int store_elem(int dtype, void *p, int64_t i, double v)
         ((float *)p)[i] = f;
         return !isfinite(f);
     }
+    case OR_F16: {
+        uint16_t b;
+        int bad = oracle_f16_round(v, &b);
+        ((uint16_t *)p)[i] = b;
+        return bad;
+    }
     default:
         ((double *)p)[i] = v;
         return !isfinite(v);
@@ -140,6 +194,11 @@ static double round_to(int dtype, double v)
         return oracle_bf16_decode(b);
     }
     case OR_F32: return (double)(float)v;
+    case OR_F16: {
+        uint16_t b;
+        oracle_f16_round(v, &b);
+        return oracle_f16_decode(b);
+    }
     default:     return v;
     }
 }
@@ -368,5 +427,13 @@ int oracle_bf16_round_array(const double *v, int64_t n, uint16_t *out)
 {
     int bad = 0;
     for (int64_t i = 0; i < n; ++i) bad += oracle_bf16_round(v[i], &out[i]);
+    return bad;
+}
+
+/* Round an array of doubles to binary16 (for the tests of the rounding rule). */
+int oracle_f16_round_array(const double *v, int64_t n, uint16_t *out)
+{
+    int bad = 0;
+    for (int64_t i = 0; i < n; ++i) bad += oracle_f16_round(v[i], &out[i]);
     return bad;
 }

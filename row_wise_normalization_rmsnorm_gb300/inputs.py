@@ -15,8 +15,9 @@ Recipe (numpy PCG64, ``default_rng([seed, stream])``):
   stream 5  outlier columns: ceil(frac * N) columns chosen by a seeded
             permutation, whose x values are multiplied by 20
 Draws are float32; bf16 values are the float32 draws rounded to nearest
-(ties to even) on their bit patterns. bf16 arrays are numpy uint16 bit
-patterns, fp32 arrays are float32.
+(ties to even) on their bit patterns, fp16 values numpy's float32 -> float16
+conversion (nearest, ties to even). bf16 arrays are numpy uint16 bit
+patterns, fp16 arrays float16, fp32 arrays float32.
 
 The shapes, scales and outlier structure follow the workloads of the
 RMSNorm pages (llama/gemma weights, bf16 activations, 1% outlier channels
@@ -56,6 +57,8 @@ def _normal(seed, stream, shape, scale=1.0):
 def to_storage(a_f32: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return f32_to_bf16_bits(a_f32)
+    if dtype == "f16":
+        return np.ascontiguousarray(a_f32).astype(np.float16)   # nearest, ties to even
     if dtype == "f32":
         return np.ascontiguousarray(a_f32, dtype=np.float32)
     raise ValueError(f"unsupported storage dtype {dtype!r}")

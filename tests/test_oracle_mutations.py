@@ -29,9 +29,13 @@ MUTATIONS = {
     "dres_dropped": ("dxj += d;", "dxj += 0.0 * d;"),
     "fused_h_unrounded": ("h[j] = round_to(jb->dtype, xv + load_elem(jb->dtype, jb->residual, base + j));",
                           "h[j] = xv + load_elem(jb->dtype, jb->residual, base + j);"),
-    "bf16_via_binary32": ("uint16_t sign = signbit(v) ? 0x8000u : 0u;",
-                          "v = (double)(float)v;\n    uint16_t sign = signbit(v) ? 0x8000u : 0u;"),
+    "bf16_via_binary32": ("int oracle_bf16_round(double v, uint16_t *out)\n{\n",
+                          "int oracle_bf16_round(double v, uint16_t *out)\n{\n    v = (double)(float)v;\n"),
+    "f16_via_binary32": ("int oracle_f16_round(double v, uint16_t *out)\n{\n",
+                         "int oracle_f16_round(double v, uint16_t *out)\n{\n    v = (double)(float)v;\n"),
     "bf16_ties_away": ("double q = rint(ldexp(m, 8));", "double q = round(ldexp(m, 8));"),
+    "f16_ties_away": ("double q = rint(ldexp(m, 11));", "double q = round(ldexp(m, 11));"),
+    "f16_subnormal_quantum": ("double q = rint(ldexp(a, 24));", "double q = rint(ldexp(a, 23));"),
     "non_affine_keeps_offset": ("load_elem(jb->dtype, jb->w, j) : 1.0;\n            const double yj",
                                 "load_elem(jb->dtype, jb->w, j) : jb->offset + 1.0;\n            const double yj"),
 }

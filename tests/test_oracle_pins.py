@@ -352,3 +352,43 @@ def test_non_affine_bwd_matches_finite_differences(eps):
         xm = x.copy(); xm[idx] -= step
         fd = (loss(xp) - loss(xm)) / (2 * step)
         assert abs(fd - an["dx64"][idx]) <= 1e-7 * max(abs(an["dx64"][idx]), an["dx_scale"][idx]) + 1e-9
+
+
+# ------------------------------------------------------------------ fp16 --
+
+def test_f16_decode_round_identity_exhaustive():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    exp = (bits >> 10) & 0x1F
+    frac = bits & 0x3FF
+    b = bits[~((exp == 0x1F) & (frac != 0))]           # drop NaNs
+    v = b.view(np.float16).astype(np.float64)          # numpy's exact decode
+    assert np.array_equal(oracle.f16_round(v).view(np.uint16), b)
+
+
+def test_f16_round_ties_to_even_and_neighbours():
+    lo = np.arange(0, 0x7BFF, dtype=np.uint16)          # adjacent finite pairs
+    a = lo.view(np.float16).astype(np.float64)
+    b = (lo + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    mid = (a + b) / 2.0
+    even = np.where((lo & 1) == 0, lo, lo + 1).astype(np.uint16)
+    assert np.array_equal(oracle.f16_round(mid).view(np.uint16), even)
+    assert np.array_equal(oracle.f16_round(np.nextafter(mid, -np.inf)).view(np.uint16), lo)
+    assert np.array_equal(oracle.f16_round(np.nextafter(mid, np.inf)).view(np.uint16), (lo + 1).astype(np.uint16))
+
+
+def test_f16_round_matches_numpy_double_to_half():
+    # numpy converts float64 to float16 directly, nearest with ties to even
+    v = np.random.default_rng(8).standard_normal(300_000)
+    v[:20_000] *= 1e-5                                   # subnormal range
+    v[20_000:30_000] *= 3e4                              # near the top of the range
+    v = v[np.abs(v) < 65504.0]
+    assert np.array_equal(oracle.f16_round(v), v.astype(np.float16))
+
+
+def test_f16_storage_forward_rounds_once():
+    d = inputs.make_inputs(8, 96, "f16", 13)
+    r = oracle.fwd(d["x"], d["w"], dtype="f16", eps=1e-6, offset=0.0)
+    assert np.array_equal(r["y"], oracle.f16_round(r["y64"]))
+    r2 = oracle.fwd(oracle.to_f64(d["x"], "f16"), oracle.to_f64(d["w"], "f16"), dtype="f64", eps=1e-6,
+                    offset=0.0)
+    assert np.array_equal(r["y64"], r2["y64"])
