@@ -265,6 +265,8 @@ def sweep_points():
             pts.append((f"{dt} {M}x{N}", dt, M, N, False, False))
     for M, N in ((4096, 4096), (1024, 8192)):
         pts.append((f"add bf16 {M}x{N}", "bf16", M, N, True, False))
+    for M, N in ((16384, 8192), (4096, 8192), (16384, 16384)):
+        pts.append((f"f16 {M}x{N}", "f16", M, N, False, False))
     pts.append(("nonaffine bf16 16384x8192", "bf16", 16384, 8192, False, False))
     pts.append(("nonaffine f32 16384x6144", "f32", 16384, 6144, False, False))
     pts.append(("misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
@@ -297,8 +299,8 @@ def run_sweep(args):
     for label, dt, M, N, fused, mis in sweep_points():
         if args.sweep_filter and args.sweep_filter not in label:
             continue
-        td = torch.bfloat16 if dt == "bf16" else torch.float32
-        s = 2 if dt == "bf16" else 4
+        td = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dt]
+        s = 4 if dt == "f32" else 2
         off = 1 if mis else 0
 
         def mk(n):

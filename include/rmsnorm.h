@@ -67,7 +67,8 @@ typedef struct CUstream_st *rmsnorm_stream_t; /* same type as cudaStream_t */
 
 typedef enum {
     RMSNORM_F32 = 0,  /* IEEE binary32 storage */
-    RMSNORM_BF16 = 1  /* bfloat16 storage, fp32 compute */
+    RMSNORM_BF16 = 1, /* bfloat16 storage, fp32 compute */
+    RMSNORM_F16 = 2   /* IEEE binary16 storage, fp32 compute */
 } rmsnorm_dtype_t;
 
 typedef enum {

@@ -1,6 +1,6 @@
 """GB300-native RMSNorm forward and backward (sm_103a CUDA kernels behind a C ABI).
 
-The public functions take contiguous CUDA tensors (bf16 or fp32, rows of
+The public functions take contiguous CUDA tensors (bf16, fp16 or fp32, rows of
 length N on the last dimension) and launch on the current stream:
 
   rmsnorm_fwd(x, w)                       -> y, rstd
@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     OP_BWD,
     OP_FWD,
     RMSNORM_BF16,
+    RMSNORM_F16,
     RMSNORM_F32,
     LIB_PATH,
     Plan,

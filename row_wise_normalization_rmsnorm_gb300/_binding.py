@@ -15,11 +15,11 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "librmsnorm_gb300.so")
 
-RMSNORM_F32, RMSNORM_BF16 = 0, 1
+RMSNORM_F32, RMSNORM_BF16, RMSNORM_F16 = 0, 1, 2
 STATUS = {0: "SUCCESS", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_WORKSPACE", 4: "ERR_CUDA"}
 PATH_NAMES = {0: "vector", 1: "staged", 2: "generic"}
 OP_FWD, OP_BWD = 0, 1
-TORCH_DTYPE = {torch.float32: RMSNORM_F32, torch.bfloat16: RMSNORM_BF16}
+TORCH_DTYPE = {torch.float32: RMSNORM_F32, torch.bfloat16: RMSNORM_BF16, torch.float16: RMSNORM_F16}
 
 
 class RMSNormError(RuntimeError):
@@ -116,7 +116,7 @@ def _dtype_code(t: torch.Tensor) -> int:
     try:
         return TORCH_DTYPE[t.dtype]
     except KeyError:
-        raise TypeError(f"unsupported dtype {t.dtype}; use torch.float32 or torch.bfloat16") from None
+        raise TypeError(f"unsupported dtype {t.dtype}; use torch.float32, torch.bfloat16 or torch.float16") from None
 
 
 def _check(t: torch.Tensor, name: str, like: torch.Tensor | None = None, numel: int | None = None):

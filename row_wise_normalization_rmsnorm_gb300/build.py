@@ -24,8 +24,9 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librmsnorm_gb300.so")
 HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
 
-SOURCES = ["api.cu", "fwd_kernels.cu", "bwd_bf16.cu", "bwd_f32.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "plans.h", "bwd_kernels.cuh"]
+SOURCES = ["api.cu", "fwd_bf16.cu", "fwd_f32.cu", "fwd_f16.cu", "bwd_bf16.cu", "bwd_f32.cu", "bwd_f16.cu",
+           "noalloc.cu"]
+HEADERS = ["common.cuh", "plans.h", "fwd_kernels.cuh", "bwd_kernels.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -39,9 +39,10 @@ static const PlanDesc *find_plan(int id) {
     return nullptr;
 }
 
-static int elem_size(int dt) { return dt == RMSNORM_BF16 ? 2 : 4; }
+static bool valid_dtype(int dt) { return dt == RMSNORM_F32 || dt == RMSNORM_BF16 || dt == RMSNORM_F16; }
+static int elem_size(int dt) { return dt == RMSNORM_F32 ? 4 : 2; }
 
-static int dtype_bit(int dt) { return dt == RMSNORM_BF16 ? DT_BF16 : DT_F32; }
+static int dtype_bit(int dt) { return dt == RMSNORM_BF16 ? DT_BF16 : (dt == RMSNORM_F16 ? DT_F16 : DT_F32); }
 
 // Default plan for (op, dtype, chunks per row); nullptr when no vector plan
 // covers C.
@@ -84,7 +85,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
                                     int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
     if (!out) return RMSNORM_ERR_INVALID_ARG;
     if (op != RMSNORM_OP_FWD && op != RMSNORM_OP_BWD) return RMSNORM_ERR_INVALID_ARG;
-    if (dt != RMSNORM_F32 && dt != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
+    if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (max_parts < 1) return RMSNORM_ERR_INVALID_ARG;
     const int s = elem_size(dt);
@@ -180,8 +181,36 @@ static cudaError_t device_sms(int *dev_out, int *sms_out) {
 }
 
 static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed) {
-    return dt == RMSNORM_BF16 ? bwd_main_kernel_ptr_bf16(plan_id, fused, packed)
-                              : bwd_main_kernel_ptr_f32(plan_id, fused, packed);
+    switch (dt) {
+    case RMSNORM_BF16: return bwd_main_kernel_ptr_bf16(plan_id, fused, packed);
+    case RMSNORM_F16: return bwd_main_kernel_ptr_f16(plan_id, fused, packed);
+    default: return bwd_main_kernel_ptr_f32(plan_id, fused, packed);
+    }
+}
+
+static int launch_fwd_dt(int dt, int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
+    switch (dt) {
+    case RMSNORM_BF16: return launch_fwd_bf16(plan_id, fused, p, grid, stream);
+    case RMSNORM_F16: return launch_fwd_f16(plan_id, fused, p, grid, stream);
+    default: return launch_fwd_f32(plan_id, fused, p, grid, stream);
+    }
+}
+
+static int launch_bwd_dt(int dt, int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem,
+                         void *stream) {
+    switch (dt) {
+    case RMSNORM_BF16: return launch_bwd_main_bf16(plan_id, fused, packed, p, grid, smem, stream);
+    case RMSNORM_F16: return launch_bwd_main_f16(plan_id, fused, packed, p, grid, smem, stream);
+    default: return launch_bwd_main_f32(plan_id, fused, packed, p, grid, smem, stream);
+    }
+}
+
+static int launch_finalize_dt(int dt, const float *ws, int parts, int N, void *dw, void *stream, bool serial) {
+    switch (dt) {
+    case RMSNORM_BF16: return launch_dw_finalize_bf16(ws, parts, N, dw, stream, serial);
+    case RMSNORM_F16: return launch_dw_finalize_f16(ws, parts, N, dw, stream, serial);
+    default: return launch_dw_finalize_f32(ws, parts, N, dw, stream, serial);
+    }
 }
 
 // Largest number of backward dW partial rows worth launching for a plan:
@@ -190,14 +219,14 @@ static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed) {
 // those two variants use the same count (and dW the same summation order).
 // Cached per device, dtype, plan and mode.
 static std::mutex g_occ_mutex;
-static int g_parts_cache[kMaxDevices][2][2][64];
-static int g_cps_cache[kMaxDevices][2][2][64];
+static int g_parts_cache[kMaxDevices][3][2][64];
+static int g_cps_cache[kMaxDevices][3][2][64];
 
 static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, int64_t N, bool fused,
                                  int *parts_out, int *cps_out) {
     const int slot = d.id;
     if (slot < 0 || slot >= 64) return cudaErrorInvalidValue;
-    const int dti = dt == RMSNORM_BF16 ? 1 : 0;
+    const int dti = dt;  // 0 fp32, 1 bf16, 2 fp16
     const int fi = fused ? 1 : 0;
     {
         std::lock_guard<std::mutex> lk(g_occ_mutex);
@@ -261,7 +290,7 @@ static std::atomic<int> g_table_ok{-1};
 int self_check_impl() {
     int bad = 0;
     for (int op = 0; op < 2; ++op) {
-        for (int dt = 0; dt < 2; ++dt) {
+        for (int dt = 0; dt < 3; ++dt) {
             int64_t expect = 1;
             for (int i = 0; i < kNumPlans; ++i) {
                 const PlanDesc &d = kPlans[i];
@@ -286,7 +315,7 @@ int self_check_impl() {
             // a cluster row has one team per CTA, of whole warps, and at most 8 CTAs
             if (d.cs < 1 || d.cs > 8 || (d.cs > 1 && (d.teams != 1 || d.tpr < 32))) ++bad;
         }
-        if (d.dtm < 1 || d.dtm > 3) ++bad;
+        if (d.dtm < 1 || d.dtm > DT_ANY) ++bad;
         if (d.id < 0 || d.id >= 64) ++bad;
     }
     return bad;
@@ -313,7 +342,7 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
                                  void *residual_out, float *rstd, int64_t M, int64_t N, int dt, float eps,
                                  float offset, cudaStream_t stream, int force_plan, rmsnorm_plan_t *used) {
     if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
-    if (dt != RMSNORM_F32 && dt != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
+    if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
     // An empty batch reads and writes nothing; its (empty) tensors may be NULL.
@@ -344,7 +373,7 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     p.N = (int)N;
     p.eps = eps;
     p.offset = offset;
-    const int le = launch_fwd(plan.plan_id, dt == RMSNORM_BF16 ? 1 : 0, fused, p, plan.ctas, stream);
+    const int le = launch_fwd_dt(dt, plan.plan_id, fused, p, plan.ctas, stream);
     if (le != 0) return cuda_fail((cudaError_t)le);
     if (used) *used = plan;
     return RMSNORM_SUCCESS;
@@ -358,7 +387,7 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
                                  bool fused, int force_plan, int force_ctas, int force_packed,
                                  void *event_after_main, rmsnorm_plan_t *used) {
     if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
-    if (dt != RMSNORM_F32 && dt != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
+    if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
     if (force_packed < -1 || force_packed > 1) return RMSNORM_ERR_INVALID_ARG;
@@ -433,14 +462,10 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     p.M = M;
     p.N = (int)N;
     p.offset = offset;
-    int le = dt == RMSNORM_BF16
-                 ? launch_bwd_main_bf16(plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream)
-                 : launch_bwd_main_f32(plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream);
+    int le = launch_bwd_dt(dt, plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream);
     if (le == 0 && event_after_main) le = (int)cudaEventRecord(static_cast<cudaEvent_t>(event_after_main), stream);
     if (le == 0 && affine)
-        le = dt == RMSNORM_BF16
-                 ? launch_dw_finalize_bf16(ws, plan.ws_rows, (int)N, dw, stream, event_after_main != nullptr)
-                 : launch_dw_finalize_f32(ws, plan.ws_rows, (int)N, dw, stream, event_after_main != nullptr);
+        le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)N, dw, stream, event_after_main != nullptr);
     if (owned) {
         cudaError_t fe = cudaFreeAsync(ws, stream);
         if (le == 0 && fe != cudaSuccess) le = (int)fe;
@@ -503,7 +528,7 @@ rmsnorm_status_t rmsnorm_bwd_ex(const void *dy, const void *dresidual_out, const
 }
 
 size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt) {
-    if (M <= 0 || N < 1 || N > RMSNORM_MAX_N || (dt != RMSNORM_F32 && dt != RMSNORM_BF16)) return 0;
+    if (M <= 0 || N < 1 || N > RMSNORM_MAX_N || !valid_dtype(dt)) return 0;
     if (M > 0x7fffffffLL || !table_ok()) return 0;
     int dev = 0, sms = 0;
     if (device_sms(&dev, &sms) != cudaSuccess) return 0;

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -16,6 +17,10 @@ template <> struct Elem<float> {
     static constexpr int NP = 2;  // float2 pairs per chunk
 };
 template <> struct Elem<__nv_bfloat16> {
+    static constexpr int E = 8;
+    static constexpr int NP = 4;
+};
+template <> struct Elem<__half> {
     static constexpr int E = 8;
     static constexpr int NP = 4;
 };
@@ -37,7 +42,22 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(float2 v) {
     return *reinterpret_cast<uint32_t *>(&b);
 }
 
+__device__ __forceinline__ float2 f16x2_to_f2(uint32_t u) {
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    return __half22float2(h);  // exact widening
+}
+__device__ __forceinline__ uint32_t f2_to_f16x2(float2 v) {
+    __half2 h = __float22half2_rn(v);  // round to nearest even
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
 template <typename T> __device__ __forceinline__ void unpack(const uint4 &c, float2 (&p)[Elem<T>::NP]);
+template <> __device__ __forceinline__ void unpack<__half>(const uint4 &c, float2 (&p)[4]) {
+    p[0] = f16x2_to_f2(c.x);
+    p[1] = f16x2_to_f2(c.y);
+    p[2] = f16x2_to_f2(c.z);
+    p[3] = f16x2_to_f2(c.w);
+}
 template <> __device__ __forceinline__ void unpack<__nv_bfloat16>(const uint4 &c, float2 (&p)[4]) {
     p[0] = bf16x2_to_f2(c.x);
     p[1] = bf16x2_to_f2(c.y);
@@ -50,6 +70,9 @@ template <> __device__ __forceinline__ void unpack<float>(const uint4 &c, float2
 }
 
 template <typename T> __device__ __forceinline__ uint4 pack(const float2 (&p)[Elem<T>::NP]);
+template <> __device__ __forceinline__ uint4 pack<__half>(const float2 (&p)[4]) {
+    return make_uint4(f2_to_f16x2(p[0]), f2_to_f16x2(p[1]), f2_to_f16x2(p[2]), f2_to_f16x2(p[3]));
+}
 template <> __device__ __forceinline__ uint4 pack<__nv_bfloat16>(const float2 (&p)[4]) {
     return make_uint4(f2_to_bf16x2(p[0]), f2_to_bf16x2(p[1]), f2_to_bf16x2(p[2]), f2_to_bf16x2(p[3]));
 }
@@ -63,16 +86,20 @@ __device__ __forceinline__ float load_elem(const float *p, int64_t i) { return p
 __device__ __forceinline__ float load_elem(const __nv_bfloat16 *p, int64_t i) {
     return __bfloat162float(p[i]);
 }
+__device__ __forceinline__ float load_elem(const __half *p, int64_t i) { return __half2float(p[i]); }
 __device__ __forceinline__ float load_w(const float *p, int64_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float load_w(const __half *p, int64_t i) { return __half2float(__ldg(p + i)); }
 __device__ __forceinline__ float load_w(const __nv_bfloat16 *p, int64_t i) {
     return __bfloat162float(__ldg(p + i));
 }
 __device__ __forceinline__ void store_elem(float *p, int64_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void store_elem(__half *p, int64_t i, float v) { p[i] = __float2half_rn(v); }
 __device__ __forceinline__ void store_elem(__nv_bfloat16 *p, int64_t i, float v) {
     p[i] = __float2bfloat16_rn(v);
 }
 // Value a store of v would hold (round to the storage type).
 __device__ __forceinline__ float round_to(float v, const float *) { return v; }
+__device__ __forceinline__ float round_to(float v, const __half *) { return __half2float(__float2half_rn(v)); }
 __device__ __forceinline__ float round_to(float v, const __nv_bfloat16 *) {
     return __bfloat162float(__float2bfloat16_rn(v));
 }

@@ -1,4 +1,4 @@
-// fwd_kernels.cu -- RMSNorm forward kernels (plain and fused residual add).
+// fwd_kernels.cuh -- RMSNorm forward kernels (plain and fused residual add).
 //
 // Vector kernel: a team of TPR threads owns one row; each thread loads V
 // 16-byte chunks of it (chunk c = v * TPR + t, so a warp's loads are
@@ -14,6 +14,8 @@
 // twice (the second read hits L1/L2). Serves any N and any element-aligned
 // pointers (Liger-Kernel PR #1388, "Behavior when the fast path does not
 // apply": irregular or unaligned shapes take scalar paths).
+#pragma once
+
 #include "common.cuh"
 #include "plans.h"
 
@@ -240,15 +242,6 @@ static const void *ptr_t(int plan_id, bool fused) {
     default:
         return nullptr;
     }
-}
-
-int launch_fwd(int plan_id, int dtype, bool fused, const FwdParams &p, int grid, void *stream) {
-    return dtype == 1 ? launch_t<__nv_bfloat16>(plan_id, fused, p, grid, stream)
-                      : launch_t<float>(plan_id, fused, p, grid, stream);
-}
-
-const void *fwd_kernel_ptr(int plan_id, int dtype, bool fused) {
-    return dtype == 1 ? ptr_t<__nv_bfloat16>(plan_id, fused) : ptr_t<float>(plan_id, fused);
 }
 
 }  // namespace rmsn

@@ -18,8 +18,9 @@ namespace rmsn {
 
 enum PlanOp { OP_FWD = 0, OP_BWD = 1 };
 enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2 };
-// Storage types a default plan applies to (bit 0: fp32, bit 1: bf16).
-enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_ANY = 3 };
+// Storage types a default plan applies to (bit 0: fp32, bit 1: bf16,
+// bit 2: fp16; DT_16 = both 2-byte types).
+enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
 
 // X(id, op, path, threads_per_row, chunks_per_thread, teams_per_cta, depth, cluster, dtypes, cmin, cmax)
 // [cmin, cmax] is the range of C for which the plan is the default for the
@@ -61,9 +62,9 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_ANY = 3 };
     X(23, OP_BWD, PATH_VECTOR ,   32, 2,  8, 1, 1, DT_ANY,    33,    64) \
     X(24, OP_BWD, PATH_VECTOR ,   64, 2,  4, 1, 1, DT_ANY,    65,   128) \
     X(25, OP_BWD, PATH_VECTOR ,  128, 2,  2, 1, 1, DT_ANY,   129,   256) \
-    X(26, OP_BWD, PATH_VECTOR ,  256, 2,  2, 1, 1, DT_BF16,   257,   512) \
+    X(26, OP_BWD, PATH_VECTOR ,  256, 2,  2, 1, 1, DT_16,     257,   512) \
     X(38, OP_BWD, PATH_VECTOR ,  256, 2,  2, 2, 1, DT_F32,   257,   512) \
-    X(27, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 1, DT_BF16,   513,  1024) \
+    X(27, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 1, DT_16,     513,  1024) \
     X(34, OP_BWD, PATH_VECTOR ,  512, 2,  1, 2, 1, DT_F32,   513,  1024) \
     X(42, OP_BWD, PATH_VECTOR ,  512, 3,  1, 1, 1, DT_ANY,  1025,  1536) \
     X(45, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 2, DT_ANY,  1537,  2048) \
@@ -121,18 +122,26 @@ constexpr int kStatusClusterWaitTimeout = 1;
 // Polls of an mbarrier before a wait gives up (at most seconds).
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-// Launchers, defined in the translation units that instantiate the
-// kernels. dtype: 0 fp32, 1 bf16. They return the launch's cudaError_t.
-int launch_fwd(int plan_id, int dtype, bool fused, const FwdParams &p, int grid, void *stream);
-const void *fwd_kernel_ptr(int plan_id, int dtype, bool fused);
+// Launchers, defined in the per-dtype translation units that instantiate
+// the kernels. They return the launch's cudaError_t.
+int launch_fwd_f32(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);
+int launch_fwd_bf16(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);
+int launch_fwd_f16(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);
+const void *fwd_kernel_ptr_f32(int plan_id, bool fused);
+const void *fwd_kernel_ptr_bf16(int plan_id, bool fused);
+const void *fwd_kernel_ptr_f16(int plan_id, bool fused);
 
 int launch_bwd_main_bf16(int plan_id, bool fused, bool packed, const BwdParams &p, int grid,
                          int smem, void *stream);
 int launch_bwd_main_f32(int plan_id, bool fused, bool packed, const BwdParams &p, int grid,
                         int smem, void *stream);
+int launch_bwd_main_f16(int plan_id, bool fused, bool packed, const BwdParams &p, int grid,
+                        int smem, void *stream);
 const void *bwd_main_kernel_ptr_bf16(int plan_id, bool fused, bool packed);
 const void *bwd_main_kernel_ptr_f32(int plan_id, bool fused, bool packed);
+const void *bwd_main_kernel_ptr_f16(int plan_id, bool fused, bool packed);
 int launch_dw_finalize_bf16(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
 int launch_dw_finalize_f32(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
+int launch_dw_finalize_f16(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
 
 }  // namespace rmsn

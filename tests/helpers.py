@@ -2,8 +2,8 @@
 non-16-byte-aligned offset), readback, and the tolerance checks.
 
 Tolerances (the RMSNorm definition and bounds are restated in the oracle):
-  y    bf16: within 1 ulp of the correctly rounded oracle value (distance of
-       the ordered bit patterns); fp32: |d| <= 1e-5 |ref| + 1e-6.
+  y    bf16 / fp16: within 1 ulp of the correctly rounded oracle value
+       (distance of the ordered bit patterns); fp32: |d| <= 1e-5 |ref| + 1e-6.
   dx   as y, or -- where the result comes from cancelling terms -- within
        8 * 2^-24 * rstd (|g| + |xhat c|) [+ |dres|], the fp32 rounding bound
        of the difference of the two terms, plus (N/256 + 48) * 2^-24 *
@@ -11,7 +11,8 @@ Tolerances (the RMSNorm definition and bounds are restated in the oracle):
        behind c (at most N/256 terms added in sequence per thread, then a
        tree and at most 32 warp partials), which can itself cancel
        (counted and reported).
-  dw   bf16: |d| <= 4e-3 |ref| + 2^-20 S; fp32: |d| <= 1e-4 |ref| + 2^-20 S,
+  dw   bf16: |d| <= 4e-3 |ref| + 2^-20 S; fp16: 1e-3 |ref| + 2^-20 S (its
+       output rounding is 2^-11); fp32: |d| <= 1e-4 |ref| + 2^-20 S,
        with ref the unrounded double sum and S = sum_i |dy xhat| (the scale
        of the fp32 summation error).
   rstd relative 2e-6.
@@ -26,12 +27,17 @@ import oracle
 FLOOR_ULPS = 8.0 * 2.0 ** -24
 
 
+TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+
 def to_dev(a: np.ndarray, dtype: str, device="cuda", offset: int = 0) -> torch.Tensor:
     """Upload storage-typed numpy data. offset > 0 places the tensor `offset`
     elements past a 256-byte-aligned allocation (a contiguous tensor whose
     base is not 16-byte aligned)."""
     if dtype == "bf16":
         t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    elif dtype == "f16":
+        t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float16))
     else:
         t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
     if offset == 0:
@@ -43,7 +49,7 @@ def to_dev(a: np.ndarray, dtype: str, device="cuda", offset: int = 0) -> torch.T
 
 
 def empty_dev(shape, dtype: str, device="cuda", offset: int = 0, fill=float("nan")) -> torch.Tensor:
-    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    td = TORCH_DT[dtype]
     n = int(np.prod(shape))
     buf = torch.full((n + offset + 16,), fill, dtype=td, device=device)
     return buf[offset:offset + n].view(shape)
@@ -52,25 +58,29 @@ def empty_dev(shape, dtype: str, device="cuda", offset: int = 0, fill=float("nan
 def to_host(t: torch.Tensor, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    return t.contiguous().cpu().numpy()
+    return t.contiguous().cpu().numpy()   # float16 or float32
 
 
 def decode(a: np.ndarray, dtype: str) -> np.ndarray:
     return oracle.to_f64(a, dtype)
 
 
-def bf16_ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
-    """|ordered(a) - ordered(b)| for bf16 bit patterns (signed-magnitude
-    mapped to a monotone integer line, so +0 and -0 are 0 apart)."""
+def ulp16_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """|ordered(a) - ordered(b)| for 16-bit sign-magnitude bit patterns (bf16
+    or fp16, as uint16 or float16 arrays), mapped to a monotone integer line
+    so +0 and -0 are 0 apart; 1 means adjacent representable values."""
     def ordered(x):
-        x = x.astype(np.int32)
+        x = np.ascontiguousarray(x).view(np.uint16).astype(np.int32)
         return np.where(x & 0x8000, -(x & 0x7FFF), x)
     return np.abs(ordered(a) - ordered(b))
 
 
+bf16_ulp_distance = ulp16_distance
+
+
 def check_y(got: np.ndarray, ref: dict, dtype: str, key="y", key64="y64"):
-    if dtype == "bf16":
-        d = bf16_ulp_distance(got, ref[key])
+    if dtype in ("bf16", "f16"):
+        d = ulp16_distance(got, ref[key])
         assert d.max() <= 1, f"{key}: max {d.max()} ulp"
         return {"max_ulp": int(d.max())}
     r = ref[key64]
@@ -96,8 +106,8 @@ def check_dx(got: np.ndarray, ref: dict, dtype: str, floor_mult: float = 1.0):
     N = got.shape[-1]
     floor = floor_mult * (FLOOR_ULPS * ref["dx_scale"] + reduction_ulps(N) * ref["dx_cscale"])
     near = np.abs(v - ref["dx64"]) <= floor
-    if dtype == "bf16":
-        ok = (bf16_ulp_distance(got, ref["dx"]) <= 1)
+    if dtype in ("bf16", "f16"):
+        ok = (ulp16_distance(got, ref["dx"]) <= 1)
     else:
         r = ref["dx64"]
         ok = np.abs(v - r) <= 1e-5 * np.abs(r) + 1e-6
@@ -113,7 +123,7 @@ def check_dx(got: np.ndarray, ref: dict, dtype: str, floor_mult: float = 1.0):
 
 def check_dw(got: np.ndarray, ref: dict, dtype: str):
     v = decode(got, dtype)
-    rel = 4e-3 if dtype == "bf16" else 1e-4
+    rel = {"bf16": 4e-3, "f16": 1e-3, "f32": 1e-4}[dtype]
     err = np.abs(v - ref["dw64"])
     tol = rel * np.abs(ref["dw64"]) + 2.0 ** -20 * ref["dw_abs"]
     assert (err <= tol).all(), f"dw: {(err > tol).sum()} columns off, worst ratio {(err / tol).max()}"

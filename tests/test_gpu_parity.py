@@ -211,3 +211,40 @@ def test_non_affine_matches_oracle(rn, dt, M, N, fused):
                    dres=d.get("dres") if fused else None)
     torch.cuda.synchronize()
     check_dx(to_host(dx, dt), b, dt)
+
+
+
+# ------------------------------------------------------------------ fp16 --
+
+F16_SHAPES = [(333, 128), (4096, 2048), (300, 4096), (301, 5000), (257, 8192), (65, 16384), (33, 32768),
+              (211, 4097), (9, 65536), (40, 3)]
+
+
+@pytest.mark.parametrize("M,N", F16_SHAPES)
+def test_f16_shapes(rn, M, N):
+    d = inputs.make_inputs(M, N, "f16", 120 + N % 11)
+    _fwd_bwd_check(rn, d, "f16", 1e-6, 0.0)
+
+
+@pytest.mark.parametrize("M,N", [(4096, 4096), (1024, 8192)])
+def test_f16_fused_add_gemma(rn, M, N):
+    d = inputs.make_inputs(M, N, "f16", 121, w_mode="gemma", residual=True, dres=True)
+    _fwd_bwd_check(rn, d, "f16", 1e-6, 1.0, fused=True)
+
+
+def test_f16_misaligned(rn):
+    d = inputs.make_inputs(1024, 7168, "f16", inputs.SWEEP_SEED)
+    _fwd_bwd_check(rn, d, "f16", 1e-6, 0.0, offset_elems=1, expect_path="generic")
+
+
+def test_f16_non_affine(rn):
+    d = inputs.make_inputs(2048, 8192, "f16", 122)
+    x, dy = to_dev(d["x"], "f16"), to_dev(d["dy"], "f16")
+    y, rstd = rn.rmsnorm_fwd(x, None)
+    f = oracle.fwd(d["x"], None, dtype="f16", eps=1e-6, offset=0.0)
+    dx, dw = rn.rmsnorm_bwd(dy, x, None, torch.from_numpy(f["rstd32"]).cuda())
+    b = oracle.bwd(d["dy"], d["x"], None, dtype="f16", eps=1e-6, offset=0.0, rstd=f["rstd32"])
+    torch.cuda.synchronize()
+    assert dw is None
+    check_y(to_host(y, "f16"), f, "f16")
+    check_dx(to_host(dx, "f16"), b, "f16")

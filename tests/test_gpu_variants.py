@@ -31,7 +31,7 @@ def dev_inputs(M, N, dt, seed, **kw):
 
 @pytest.mark.parametrize("dt,M,N", [("bf16", 2048, 8192), ("f32", 1024, 6144), ("bf16", 999, 128),
                                     ("bf16", 500, 2048), ("f32", 300, 16), ("bf16", 300, 16384),
-                                    ("f32", 200, 16384)])
+                                    ("f32", 200, 16384), ("f16", 1000, 8192), ("f16", 300, 16384)])
 @pytest.mark.parametrize("fused", [False, True])
 def test_packed_matches_scalar_bitwise(rn, dt, M, N, fused):
     _, t = dev_inputs(M, N, dt, 90, residual=fused, dres=fused)
