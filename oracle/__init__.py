@@ -64,10 +64,10 @@ def _load():
             lib = ctypes.CDLL(override if override else build())
             i64, dbl, vp, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
             lib.oracle_rmsnorm_fwd.restype = i32
-            lib.oracle_rmsnorm_fwd.argtypes = [i32, i64, i64, vp, vp, vp, dbl, dbl,
+            lib.oracle_rmsnorm_fwd.argtypes = [i32, i32, i64, i64, vp, vp, vp, dbl, dbl,
                                                vp, vp, vp, vp, vp, i32]
             lib.oracle_rmsnorm_bwd.restype = i32
-            lib.oracle_rmsnorm_bwd.argtypes = [i32, i64, i64, vp, vp, vp, vp, vp, dbl, dbl,
+            lib.oracle_rmsnorm_bwd.argtypes = [i32, i32, i64, i64, vp, vp, vp, vp, vp, dbl, dbl,
                                                vp, vp, vp, vp, vp, vp, vp, i32]
             lib.oracle_bf16_round_array.restype = i32
             lib.oracle_bf16_round_array.argtypes = [vp, i64, vp]
@@ -124,9 +124,10 @@ def to_f64(a, dtype) -> np.ndarray:
     return np.asarray(a, dtype=np.float64)
 
 
-def fwd(x, w, *, dtype, eps, offset, residual=None, nthreads=1):
+def fwd(x, w, *, dtype, eps, offset, residual=None, nthreads=1, wdtype=None):
     """RMSNorm forward (optionally with the fused residual add) on an M x N block.
-    ``w`` None is non-affine RMSNorm (weight factor 1, offset unused).
+    ``w`` None is non-affine RMSNorm (weight factor 1, offset unused);
+    ``wdtype`` is the weight's storage type (default: ``dtype``).
 
     Returns a dict with
       ``y``       R(y) in the storage type, shape (M, N)
@@ -135,9 +136,10 @@ def fwd(x, w, *, dtype, eps, offset, residual=None, nthreads=1):
       ``rstd64``  rstd in double, shape (M,)
       ``rstd32``  rstd rounded to float32
     """
+    wdtype = wdtype or dtype
     x = _as_storage(x, dtype)
     M, N = x.shape
-    w = _as_storage(w, dtype, (N,))   # None: non-affine (weight factor 1)
+    w = _as_storage(w, wdtype, (N,))   # None: non-affine (weight factor 1)
     residual = _as_storage(residual, dtype, (M, N))
     st = _NP_STORAGE[dtype]
     y = np.empty((M, N), dtype=st)
@@ -145,7 +147,7 @@ def fwd(x, w, *, dtype, eps, offset, residual=None, nthreads=1):
     h = np.empty((M, N), dtype=st) if residual is not None else None
     r64 = np.empty((M,), dtype=np.float64)
     r32 = np.empty((M,), dtype=np.float32)
-    bad = _load().oracle_rmsnorm_fwd(_DTYPE_CODE[dtype], M, N, _ptr(x), _ptr(residual), _ptr(w),
+    bad = _load().oracle_rmsnorm_fwd(_DTYPE_CODE[dtype], _DTYPE_CODE[wdtype], M, N, _ptr(x), _ptr(residual), _ptr(w),
                                      float(eps), float(offset), _ptr(y), _ptr(y64), _ptr(h),
                                      _ptr(r64), _ptr(r32), int(nthreads))
     if bad:
@@ -153,7 +155,7 @@ def fwd(x, w, *, dtype, eps, offset, residual=None, nthreads=1):
     return {"y": y, "y64": y64, "h": h, "rstd64": r64, "rstd32": r32}
 
 
-def bwd(dy, h, w, *, dtype, eps, offset, rstd=None, dres=None, want_dx=True, nthreads=1):
+def bwd(dy, h, w, *, dtype, eps, offset, rstd=None, dres=None, want_dx=True, nthreads=1, wdtype=None):
     """RMSNorm backward on an M x N block.
 
     ``h`` is the normalised input (x, or residual_out of the fused forward).
@@ -167,12 +169,14 @@ def bwd(dy, h, w, *, dtype, eps, offset, rstd=None, dres=None, want_dx=True, nth
     Returns a dict with ``dx`` (storage type), ``dx64``, ``dx_scale``
     (rstd (|g| + |xhat c|) [+ |dres|]), ``dx_cscale`` (rstd |xhat| (1/N)
     sum |g xhat|, the sensitivity of dx to rounding in the sum behind c),
-    ``dw64``, ``dw_abs`` (sum |dy xhat|) and ``dw`` (storage type).
+    ``dw64``, ``dw_abs`` (sum |dy xhat|) and ``dw`` (the weight's storage
+    type, ``wdtype``, default ``dtype``).
     """
+    wdtype = wdtype or dtype
     dy = _as_storage(dy, dtype)
     M, N = dy.shape
     h = _as_storage(h, dtype, (M, N))
-    w = _as_storage(w, dtype, (N,))   # None: non-affine (g = dy; dW is not a result)
+    w = _as_storage(w, wdtype, (N,))   # None: non-affine (g = dy; dW is not a result)
     dres = _as_storage(dres, dtype, (M, N))
     if rstd is not None:
         rstd = np.ascontiguousarray(rstd, dtype=np.float32)
@@ -185,8 +189,8 @@ def bwd(dy, h, w, *, dtype, eps, offset, rstd=None, dres=None, want_dx=True, nth
     dxc = np.empty((M, N), dtype=np.float64) if want_dx else None
     dw64 = np.empty((N,), dtype=np.float64)
     dwa = np.empty((N,), dtype=np.float64)
-    dw = np.empty((N,), dtype=st)
-    bad = _load().oracle_rmsnorm_bwd(_DTYPE_CODE[dtype], M, N, _ptr(dy), _ptr(h), _ptr(w),
+    dw = np.empty((N,), dtype=_NP_STORAGE[wdtype])
+    bad = _load().oracle_rmsnorm_bwd(_DTYPE_CODE[dtype], _DTYPE_CODE[wdtype], M, N, _ptr(dy), _ptr(h), _ptr(w),
                                      _ptr(rstd), _ptr(dres), float(eps), float(offset),
                                      _ptr(dx), _ptr(dx64), _ptr(dxs), _ptr(dxc), _ptr(dw64), _ptr(dwa),
                                      _ptr(dw), int(nthreads))

@@ -32,6 +32,9 @@
  *   d rstd / d h_k = -rstd^3 h_k / N, hence
  *   dL/dh_k = rstd g_k - (rstd^3 h_k / N) sum_j g_j h_j = rstd (g_k - xhat_k c).
  *
+ * The weight w and its gradient dW may have their own storage type
+ * (wdtype), e.g. fp32 master weights with bf16 activations.
+ *
  * Non-affine RMSNorm (w == NULL): the weight factor (offset + w_j) is
  * replaced by 1, so y_j = h_j * rstd, g_j = dy_j, and there is no dW (the
  * Liger-Kernel page's "non-affine" case, Validation).
@@ -206,7 +209,7 @@ static double round_to(int dtype, double v)
 /* ------------------------------------------------------------- forward -- */
 
 typedef struct {
-    int dtype;
+    int dtype, wdtype;  /* activations / weight storage types */
     int64_t row0, row1, N;
     const void *x, *residual, *w;
     double eps, offset;
@@ -237,7 +240,7 @@ static void fwd_rows(fwd_job *jb)
         const double ms = ss / (double)N;
         const double rstd = 1.0 / sqrt(ms + jb->eps);
         for (int64_t j = 0; j < N; ++j) {
-            const double factor = jb->w ? jb->offset + load_elem(jb->dtype, jb->w, j) : 1.0;
+            const double factor = jb->w ? jb->offset + load_elem(jb->wdtype, jb->w, j) : 1.0;
             const double yj = h[j] * rstd * factor;
             if (jb->y64) jb->y64[base + j] = yj;
             if (jb->y) jb->bad |= store_elem(jb->dtype, jb->y, base + j, yj);
@@ -259,7 +262,7 @@ static void *fwd_thread(void *arg) { fwd_rows((fwd_job *)arg); return NULL; }
  * the thread count does not change any result).
  * Returns the number of non-finite or overflowing stores (0 expected).
  */
-int oracle_rmsnorm_fwd(int dtype, int64_t M, int64_t N,
+int oracle_rmsnorm_fwd(int dtype, int wdtype, int64_t M, int64_t N,
                        const void *x, const void *residual, const void *w,
                        double eps, double offset,
                        void *y, double *y64, void *h_out,
@@ -271,7 +274,7 @@ int oracle_rmsnorm_fwd(int dtype, int64_t M, int64_t N,
     pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     for (int t = 0; t < nthreads; ++t) {
         fwd_job *jb = &jobs[t];
-        jb->dtype = dtype; jb->N = N;
+        jb->dtype = dtype; jb->wdtype = wdtype; jb->N = N;
         jb->row0 = M * t / nthreads; jb->row1 = M * (t + 1) / nthreads;
         jb->x = x; jb->residual = residual; jb->w = w;
         jb->eps = eps; jb->offset = offset;
@@ -293,7 +296,7 @@ int oracle_rmsnorm_fwd(int dtype, int64_t M, int64_t N,
 /* ------------------------------------------------------------ backward -- */
 
 typedef struct {
-    int dtype;
+    int dtype, wdtype;  /* activations / weight storage types */
     int64_t row0, row1, N;
     const void *dy, *h, *w, *dres;
     const float *rstd_in;
@@ -309,7 +312,7 @@ static void bwd_rows(bwd_job *jb)
     const int64_t N = jb->N;
     double *hv = (double *)malloc((size_t)N * sizeof(double));
     double *wpo = (double *)malloc((size_t)N * sizeof(double));
-    for (int64_t j = 0; j < N; ++j) wpo[j] = jb->w ? jb->offset + load_elem(jb->dtype, jb->w, j) : 1.0;
+    for (int64_t j = 0; j < N; ++j) wpo[j] = jb->w ? jb->offset + load_elem(jb->wdtype, jb->w, j) : 1.0;
     for (int64_t i = jb->row0; i < jb->row1; ++i) {
         const int64_t base = i * N;
         for (int64_t j = 0; j < N; ++j) hv[j] = load_elem(jb->dtype, jb->h, base + j);
@@ -373,12 +376,12 @@ static void *bwd_thread(void *arg) { bwd_rows((bwd_job *)arg); return NULL; }
  *            of magnitudes, not with |c|)
  *   dw64     sum over rows of dy * xhat (length N)
  *   dw_abs   sum over rows of |dy * xhat| (length N)
- *   dw       R(dw64) in the storage type
+ *   dw       R(dw64) in the weight's storage type
  * Rows are split into nthreads contiguous ranges; each range keeps its own
  * dW partial and the partials are added in range order.
  * Returns the number of non-finite or overflowing stores.
  */
-int oracle_rmsnorm_bwd(int dtype, int64_t M, int64_t N,
+int oracle_rmsnorm_bwd(int dtype, int wdtype, int64_t M, int64_t N,
                        const void *dy, const void *h, const void *w,
                        const float *rstd_in, const void *dres,
                        double eps, double offset,
@@ -391,7 +394,7 @@ int oracle_rmsnorm_bwd(int dtype, int64_t M, int64_t N,
     pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     for (int t = 0; t < nthreads; ++t) {
         bwd_job *jb = &jobs[t];
-        jb->dtype = dtype; jb->N = N;
+        jb->dtype = dtype; jb->wdtype = wdtype; jb->N = N;
         jb->row0 = M * t / nthreads; jb->row1 = M * (t + 1) / nthreads;
         jb->dy = dy; jb->h = h; jb->w = w; jb->dres = dres; jb->rstd_in = rstd_in;
         jb->eps = eps; jb->offset = offset;
@@ -411,7 +414,7 @@ int oracle_rmsnorm_bwd(int dtype, int64_t M, int64_t N,
         for (int t = 0; t < nthreads; ++t) { s += jobs[t].dw[j]; sa += jobs[t].dw_abs[j]; }
         dw64[j] = s;
         if (dw_abs) dw_abs[j] = sa;
-        if (dw) bad |= store_elem(dtype, dw, j, s);
+        if (dw) bad |= store_elem(wdtype, dw, j, s);
     }
     for (int t = 0; t < nthreads; ++t) {
         bad += jobs[t].bad;

@@ -72,9 +72,10 @@ def outlier_columns(N: int, seed: int, frac: float) -> np.ndarray:
 
 def make_inputs(M: int, N: int, dtype: str, seed: int, *, dy_scale: float = 1.0,
                 w_mode: str = "llama", residual: bool = False, dres: bool = False,
-                outlier_frac: float = 0.0, outlier_scale: float = 20.0) -> dict:
+                outlier_frac: float = 0.0, outlier_scale: float = 20.0, wdtype: str | None = None) -> dict:
     """Return a dict of storage-typed numpy arrays: x, dy, w and, on request,
-    residual and dres. ``w_mode`` "llama" pairs with offset 0, "gemma" with 1."""
+    residual and dres. ``w_mode`` "llama" pairs with offset 0, "gemma" with 1.
+    ``wdtype`` is the weight's storage type (default ``dtype``)."""
     x = _normal(seed, STREAM_X, (M, N))
     if outlier_frac > 0.0:
         cols = outlier_columns(N, seed, outlier_frac)
@@ -89,7 +90,7 @@ def make_inputs(M: int, N: int, dtype: str, seed: int, *, dy_scale: float = 1.0,
         w = np.float32(0.1) * wn
     else:
         raise ValueError(f"unknown w_mode {w_mode!r}")
-    out["w"] = to_storage(w, dtype)
+    out["w"] = to_storage(w, wdtype or dtype)
     if residual:
         out["residual"] = to_storage(_normal(seed, STREAM_RES, (M, N)), dtype)
     if dres:

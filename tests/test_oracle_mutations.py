@@ -19,8 +19,8 @@ MUTATIONS = {
     "eps_outside_root": ("1.0 / sqrt(ms + jb->eps)", "1.0 / (sqrt(ms) + jb->eps)"),
     "offset_dropped_fwd": ("const double factor = jb->w ? jb->offset + load_elem",
                            "const double factor = jb->w ? load_elem"),
-    "w_index_reversed": ("load_elem(jb->dtype, jb->w, j) : 1.0;\n            const double yj",
-                         "load_elem(jb->dtype, jb->w, N - 1 - j) : 1.0;\n            const double yj"),
+    "w_index_reversed": ("load_elem(jb->wdtype, jb->w, j) : 1.0;\n            const double yj",
+                         "load_elem(jb->wdtype, jb->w, N - 1 - j) : 1.0;\n            const double yj"),
     "bwd_sign_flip": ("rstd * (g - xhat * c)", "rstd * (g + xhat * c)"),
     "bwd_c_not_mean": ("c /= (double)N;", "c /= 1.0;"),
     "bwd_offset_dropped": ("wpo[j] = jb->w ? jb->offset + load_elem", "wpo[j] = jb->w ? 0.0 * jb->offset + load_elem"),
@@ -36,8 +36,10 @@ MUTATIONS = {
     "bf16_ties_away": ("double q = rint(ldexp(m, 8));", "double q = round(ldexp(m, 8));"),
     "f16_ties_away": ("double q = rint(ldexp(m, 11));", "double q = round(ldexp(m, 11));"),
     "f16_subnormal_quantum": ("double q = rint(ldexp(a, 24));", "double q = rint(ldexp(a, 23));"),
-    "non_affine_keeps_offset": ("load_elem(jb->dtype, jb->w, j) : 1.0;\n            const double yj",
-                                "load_elem(jb->dtype, jb->w, j) : jb->offset + 1.0;\n            const double yj"),
+    "non_affine_keeps_offset": ("load_elem(jb->wdtype, jb->w, j) : 1.0;\n            const double yj",
+                                "load_elem(jb->wdtype, jb->w, j) : jb->offset + 1.0;\n            const double yj"),
+    "weight_read_as_activation_type": ("wpo[j] = jb->w ? jb->offset + load_elem(jb->wdtype",
+                                       "wpo[j] = jb->w ? jb->offset + load_elem(jb->dtype"),
 }
 
 

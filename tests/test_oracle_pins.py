@@ -392,3 +392,20 @@ def test_f16_storage_forward_rounds_once():
     r2 = oracle.fwd(oracle.to_f64(d["x"], "f16"), oracle.to_f64(d["w"], "f16"), dtype="f64", eps=1e-6,
                     offset=0.0)
     assert np.array_equal(r["y64"], r2["y64"])
+
+
+# ------------------------------------------------- separate weight dtype --
+
+def test_weight_dtype_only_changes_how_w_and_dw_are_stored():
+    # bf16 activations with an fp32 weight: the arithmetic is the same as
+    # with the weight's values given in double, and dW is stored as fp32
+    d = inputs.make_inputs(12, 80, "bf16", 44, wdtype="f32")
+    assert d["w"].dtype == np.float32
+    a = oracle.fwd(d["x"], d["w"], dtype="bf16", wdtype="f32", eps=1e-6, offset=1.0)
+    b = oracle.fwd(oracle.to_f64(d["x"], "bf16"), d["w"].astype(np.float64), dtype="f64", eps=1e-6, offset=1.0)
+    assert np.array_equal(a["y64"], b["y64"]) and np.array_equal(a["y"], oracle.bf16_round(b["y64"]))
+    ga = oracle.bwd(d["dy"], d["x"], d["w"], dtype="bf16", wdtype="f32", eps=1e-6, offset=1.0)
+    gb = oracle.bwd(oracle.to_f64(d["dy"], "bf16"), oracle.to_f64(d["x"], "bf16"), d["w"].astype(np.float64),
+                    dtype="f64", eps=1e-6, offset=1.0)
+    assert np.array_equal(ga["dx64"], gb["dx64"]) and np.array_equal(ga["dw64"], gb["dw64"])
+    assert ga["dw"].dtype == np.float32 and np.array_equal(ga["dw"], gb["dw64"].astype(np.float32))
