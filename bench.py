@@ -269,6 +269,9 @@ def sweep_points():
         pts.append((f"f16 {M}x{N}", "f16", M, N, False, False))
     pts.append(("nonaffine bf16 16384x8192", "bf16", 16384, 8192, False, False))
     pts.append(("nonaffine f32 16384x6144", "f32", 16384, 6144, False, False))
+    # fp32 weight and dW beside 16-bit activations
+    pts.append(("w32 bf16 16384x8192", "bf16", 16384, 8192, False, False))
+    pts.append(("w32 f16 4096x8192", "f16", 4096, 8192, False, False))
     pts.append(("misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
     pts.append(("misaligned f32 4096x2048", "f32", 4096, 2048, False, True))
     pts.append(("wide f32 16384x6144", "f32", 16384, 6144, False, False))
@@ -308,9 +311,11 @@ def run_sweep(args):
             return buf[off:off + n]
 
         affine = not label.startswith("nonaffine")
+        wtd = torch.float32 if label.startswith("w32") else td
+        sw = 4 if wtd == torch.float32 else s
         x = mk(M * N).view(M, N)
         dy = mk(M * N).view(M, N)
-        w = (1 + 0.1 * mk(N).float()).to(td)
+        w = (1 + 0.1 * mk(N).float()).to(wtd)
         if mis:
             wb = torch.empty(N + 1, dtype=td, device=dev)
             wb[1:].copy_(w)
@@ -324,7 +329,7 @@ def run_sweep(args):
         res = mk(M * N).view(M, N) if fused else None
         hout = torch.empty_like(x) if fused else None
         dres = mk(M * N).view(M, N) if fused else None
-        nb = rn.rmsnorm_bwd_workspace_bytes(M, N, td)
+        nb = rn.rmsnorm_bwd_workspace_bytes(M, N, rn.TORCH_DTYPE[td] | (rn.RMSNORM_WEIGHT_F32 if sw != s else 0))
         ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
         if fused:
             fwd = lambda: rn.rmsnorm_add_fwd(x, res, w, y=y, residual_out=hout, rstd=rstd)  # noqa: E731
@@ -338,8 +343,8 @@ def run_sweep(args):
         P = bplan["ctas"]
         k = 1 if fused else 0
         wb = 1 if affine else 0   # the weight, dW and the workspace exist only with a weight
-        by = {"fwd": (2 + 2 * k) * M * N * s + wb * N * s + 4 * M,
-              "bwd": (3 + k) * M * N * s + wb * (2 * N * s + 8 * P * N) + 4 * M}
+        by = {"fwd": (2 + 2 * k) * M * N * s + wb * N * sw + 4 * M,
+              "bwd": (3 + k) * M * N * s + wb * (2 * N * sw + 8 * P * N) + 4 * M}
         for op, fn, plan in (("fwd", fwd, fplan), ("bwd", bwd, bplan)):
             for _ in range(3):
                 fn()

@@ -31,10 +31,14 @@
  *     pointer after the call returns.
  *   - Matrices are contiguous row-major [M, N] (row stride N elements).
  *     w, dw are [N]; rstd is [M] fp32.
- *   - x, residual, w, y, dy, dx, dw, residual_out, dresidual_out all share
- *     the storage type `dt`. Pointers must be aligned to the element size;
- *     16-byte alignment of every pointer (and N * sizeof(elem) % 16 == 0)
- *     selects the vectorised kernels, anything else the generic kernels.
+ *   - x, residual, y, dy, dx, residual_out, dresidual_out share the
+ *     activations' storage type `dt`; w and dw have the same type, or fp32
+ *     when `dt` carries RMSNORM_WEIGHT_F32. Pointers must be aligned to
+ *     their element size; 16-byte alignment of every pointer (and
+ *     N * sizeof(activation) % 16 == 0) selects the vectorised kernels,
+ *     anything else the generic kernels. With an fp32 weight only the
+ *     default plans are compiled: forcing an alternative plan id returns
+ *     UNSUPPORTED.
  *   - Every call is asynchronous on `stream` (NULL = legacy default
  *     stream). The library never synchronises and never copies between
  *     host and device.
@@ -68,7 +72,13 @@ typedef struct CUstream_st *rmsnorm_stream_t; /* same type as cudaStream_t */
 typedef enum {
     RMSNORM_F32 = 0,  /* IEEE binary32 storage */
     RMSNORM_BF16 = 1, /* bfloat16 storage, fp32 compute */
-    RMSNORM_F16 = 2   /* IEEE binary16 storage, fp32 compute */
+    RMSNORM_F16 = 2,  /* IEEE binary16 storage, fp32 compute */
+    /* Flag OR'ed into the activations' type: w and dw are stored in fp32
+     * (an fp32 master weight beside 16-bit activations). fp32 | flag is the
+     * same as fp32. */
+    RMSNORM_WEIGHT_F32 = 0x100,
+    RMSNORM_BF16_W32 = 0x101, /* bf16 activations, fp32 w and dw */
+    RMSNORM_F16_W32 = 0x102   /* fp16 activations, fp32 w and dw */
 } rmsnorm_dtype_t;
 
 typedef enum {

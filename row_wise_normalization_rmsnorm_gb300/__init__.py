@@ -1,7 +1,8 @@
 """GB300-native RMSNorm forward and backward (sm_103a CUDA kernels behind a C ABI).
 
 The public functions take contiguous CUDA tensors (bf16, fp16 or fp32, rows of
-length N on the last dimension) and launch on the current stream:
+length N on the last dimension; w and dw in the activations' type, or fp32
+beside 16-bit activations) and launch on the current stream:
 
   rmsnorm_fwd(x, w)                       -> y, rstd
   rmsnorm_add_fwd(x, residual, w)         -> y, residual_out, rstd
@@ -19,6 +20,8 @@ from ._binding import (  # noqa: F401
     RMSNORM_BF16,
     RMSNORM_F16,
     RMSNORM_F32,
+    RMSNORM_WEIGHT_F32,
+    TORCH_DTYPE,
     LIB_PATH,
     Plan,
     RMSNormError,

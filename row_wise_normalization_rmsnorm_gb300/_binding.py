@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "librmsnorm_gb300.so")
 
 RMSNORM_F32, RMSNORM_BF16, RMSNORM_F16 = 0, 1, 2
+RMSNORM_WEIGHT_F32 = 0x100  # OR'ed into a 16-bit type: w and dw are fp32
 STATUS = {0: "SUCCESS", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_WORKSPACE", 4: "ERR_CUDA"}
 PATH_NAMES = {0: "vector", 1: "staged", 2: "generic"}
 OP_FWD, OP_BWD = 0, 1
@@ -119,6 +120,25 @@ def _dtype_code(t: torch.Tensor) -> int:
         raise TypeError(f"unsupported dtype {t.dtype}; use torch.float32, torch.bfloat16 or torch.float16") from None
 
 
+def _dtype_code_w(x: torch.Tensor, w) -> int:
+    """Type code for activations x and weight w: w in x's type, or fp32
+    beside 16-bit activations (RMSNORM_WEIGHT_F32)."""
+    code = _dtype_code(x)
+    if w is None or w.dtype == x.dtype:
+        return code
+    if w.dtype == torch.float32:
+        return code | RMSNORM_WEIGHT_F32
+    raise ValueError(f"w must be {x.dtype} or torch.float32, is {w.dtype}")
+
+
+def _check_w(w, name: str, x: torch.Tensor, N: int):
+    _check(w, name, numel=N)
+    if w.device != x.device:
+        raise ValueError(f"{name} must be on the input's device")
+    if w.dtype not in (x.dtype, torch.float32):
+        raise ValueError(f"{name} must be {x.dtype} or torch.float32, is {w.dtype}")
+
+
 def _check(t: torch.Tensor, name: str, like: torch.Tensor | None = None, numel: int | None = None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -155,12 +175,12 @@ def rmsnorm_fwd(x, w, *, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=No
     M, N = _rows(x)
     _check(x, "x")
     if w is not None:
-        _check(w, "w", like=x, numel=N)
+        _check_w(w, "w", x, N)
     y = torch.empty_like(x) if y is None else y
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
     _check(y, "y", like=x, numel=x.numel())
     _check(rstd, "rstd", numel=M)
-    st = lib().rmsnorm_fwd(x.data_ptr(), _ptr(w), y.data_ptr(), rstd.data_ptr(), M, N, _dtype_code(x),
+    st = lib().rmsnorm_fwd(x.data_ptr(), _ptr(w), y.data_ptr(), rstd.data_ptr(), M, N, _dtype_code_w(x, w),
                            eps, offset, _stream_handle(stream, x.device))
     _raise(st, "rmsnorm_fwd")
     return y, rstd
@@ -173,7 +193,7 @@ def rmsnorm_add_fwd(x, residual, w, *, eps: float = 1e-6, offset: float = 0.0, y
     _check(x, "x")
     _check(residual, "residual", like=x, numel=x.numel())
     if w is not None:
-        _check(w, "w", like=x, numel=N)
+        _check_w(w, "w", x, N)
     y = torch.empty_like(x) if y is None else y
     residual_out = torch.empty_like(x) if residual_out is None else residual_out
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
@@ -181,7 +201,7 @@ def rmsnorm_add_fwd(x, residual, w, *, eps: float = 1e-6, offset: float = 0.0, y
     _check(residual_out, "residual_out", like=x, numel=x.numel())
     _check(rstd, "rstd", numel=M)
     st = lib().rmsnorm_add_fwd(x.data_ptr(), residual.data_ptr(), _ptr(w), y.data_ptr(),
-                               residual_out.data_ptr(), rstd.data_ptr(), M, N, _dtype_code(x), eps, offset,
+                               residual_out.data_ptr(), rstd.data_ptr(), M, N, _dtype_code_w(x, w), eps, offset,
                                _stream_handle(stream, x.device))
     _raise(st, "rmsnorm_add_fwd")
     return y, residual_out, rstd
@@ -197,14 +217,14 @@ def rmsnorm_bwd(dy, x, w, rstd, *, eps: float = 1e-6, offset: float = 0.0, dx=No
     dx = torch.empty_like(x) if dx is None else dx
     _check(dx, "dx", like=x, numel=x.numel())
     if w is not None:
-        _check(w, "w", like=x, numel=N)
+        _check_w(w, "w", x, N)
         dw = torch.empty_like(w) if dw is None else dw
-        _check(dw, "dw", like=x, numel=N)
+        _check(dw, "dw", like=w, numel=N)
     else:
         dw = None
     wp, wb = _ws(workspace)
     st = lib().rmsnorm_bwd(dy.data_ptr(), x.data_ptr(), _ptr(w), rstd.data_ptr(), dx.data_ptr(),
-                           _ptr(dw), wp, wb, M, N, _dtype_code(x), eps, offset,
+                           _ptr(dw), wp, wb, M, N, _dtype_code_w(x, w), eps, offset,
                            _stream_handle(stream, x.device))
     _raise(st, "rmsnorm_bwd")
     return dx, dw
@@ -222,14 +242,14 @@ def rmsnorm_add_bwd(dy, dresidual_out, h, w, rstd, *, eps: float = 1e-6, offset:
     dx = torch.empty_like(h) if dx is None else dx
     _check(dx, "dx", like=h, numel=h.numel())
     if w is not None:
-        _check(w, "w", like=h, numel=N)
+        _check_w(w, "w", h, N)
         dw = torch.empty_like(w) if dw is None else dw
-        _check(dw, "dw", like=h, numel=N)
+        _check(dw, "dw", like=w, numel=N)
     else:
         dw = None
     wp, wb = _ws(workspace)
     st = lib().rmsnorm_add_bwd(dy.data_ptr(), _ptr(dresidual_out), h.data_ptr(), _ptr(w), rstd.data_ptr(),
-                               dx.data_ptr(), _ptr(dw), wp, wb, M, N, _dtype_code(h), eps, offset,
+                               dx.data_ptr(), _ptr(dw), wp, wb, M, N, _dtype_code_w(h, w), eps, offset,
                                _stream_handle(stream, h.device))
     _raise(st, "rmsnorm_add_bwd")
     return dx, dw
@@ -260,7 +280,7 @@ def rmsnorm_fwd_ex(x, w, *, residual=None, eps=1e-6, offset=0.0, y=None, residua
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
     p = Plan()
     st = lib().rmsnorm_fwd_ex(_ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(residual_out), _ptr(rstd), M, N,
-                              _dtype_code(x), eps, offset, _stream_handle(stream, x.device), force_plan,
+                              _dtype_code_w(x, w), eps, offset, _stream_handle(stream, x.device), force_plan,
                               ctypes.byref(p))
     _raise(st, "rmsnorm_fwd_ex")
     return y, residual_out, rstd, p.as_dict()
@@ -278,7 +298,7 @@ def rmsnorm_bwd_ex(dy, x, w, rstd, *, dresidual_out=None, fused=False, eps=1e-6,
     ev = None if event_after_main is None else event_after_main.cuda_event
     p = Plan()
     st = lib().rmsnorm_bwd_ex(_ptr(dy), _ptr(dresidual_out), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw),
-                              wp, wb, M, N, _dtype_code(x), eps, offset, _stream_handle(stream, x.device),
+                              wp, wb, M, N, _dtype_code_w(x, w), eps, offset, _stream_handle(stream, x.device),
                               int(fused), force_plan, force_ctas, force_packed, ev, ctypes.byref(p))
     _raise(st, "rmsnorm_bwd_ex")
     return dx, dw, p.as_dict()

@@ -39,10 +39,30 @@ static const PlanDesc *find_plan(int id) {
     return nullptr;
 }
 
-static bool valid_dtype(int dt) { return dt == RMSNORM_F32 || dt == RMSNORM_BF16 || dt == RMSNORM_F16; }
-static int elem_size(int dt) { return dt == RMSNORM_F32 ? 4 : 2; }
+// The dtype argument: the activations' storage type, optionally OR'ed with
+// RMSNORM_WEIGHT_F32 (w and dW in fp32). Kernel variants are indexed by
+// "kind": 0 fp32, 1 bf16, 2 fp16 (weight in the same type), 3 bf16 and
+// 4 fp16 activations with an fp32 weight. fp32 | RMSNORM_WEIGHT_F32 is fp32.
+constexpr int kNumKinds = 5;
+static bool valid_dtype(int dt) {
+    const int base = dt & ~RMSNORM_WEIGHT_F32;
+    return base == RMSNORM_F32 || base == RMSNORM_BF16 || base == RMSNORM_F16;
+}
+static int base_dtype(int dt) { return dt & ~RMSNORM_WEIGHT_F32; }
+static int kind_of(int dt) {
+    const int base = base_dtype(dt);
+    if (base == RMSNORM_F32 || !(dt & RMSNORM_WEIGHT_F32)) return base;
+    return base == RMSNORM_BF16 ? 3 : 4;
+}
+static bool mixed_kind(int kind) { return kind >= 3; }
+// Bytes per activation element and per weight element.
+static int elem_size(int dt) { return base_dtype(dt) == RMSNORM_F32 ? 4 : 2; }
+static int weight_size(int dt) { return (base_dtype(dt) == RMSNORM_F32 || (dt & RMSNORM_WEIGHT_F32)) ? 4 : 2; }
 
-static int dtype_bit(int dt) { return dt == RMSNORM_BF16 ? DT_BF16 : (dt == RMSNORM_F16 ? DT_F16 : DT_F32); }
+static int dtype_bit(int dt) {
+    const int base = base_dtype(dt);
+    return base == RMSNORM_BF16 ? DT_BF16 : (base == RMSNORM_F16 ? DT_F16 : DT_F32);
+}
 
 // Default plan for (op, dtype, chunks per row); nullptr when no vector plan
 // covers C.
@@ -98,6 +118,8 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
         if (!d || d->op != op) return RMSNORM_ERR_UNSUPPORTED;
         if (d->path == PATH_VECTOR && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
         if (d->path == PATH_STAGED) return RMSNORM_ERR_UNSUPPORTED;
+        // with an fp32 weight only the default plans (and the generic one) are compiled
+        if (mixed_kind(kind_of(dt)) && d->path == PATH_VECTOR && d->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
     } else {
         d = vec_ok ? default_vector_plan(op, dt, C) : nullptr;
         if (!d) d = generic_plan(op);
@@ -181,34 +203,41 @@ static cudaError_t device_sms(int *dev_out, int *sms_out) {
 }
 
 static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed) {
-    switch (dt) {
-    case RMSNORM_BF16: return bwd_main_kernel_ptr_bf16(plan_id, fused, packed);
-    case RMSNORM_F16: return bwd_main_kernel_ptr_f16(plan_id, fused, packed);
+    switch (kind_of(dt)) {
+    case 1: return bwd_main_kernel_ptr_bf16(plan_id, fused, packed);
+    case 2: return bwd_main_kernel_ptr_f16(plan_id, fused, packed);
+    case 3: return bwd_main_kernel_ptr_bf16w32(plan_id, fused, packed);
+    case 4: return bwd_main_kernel_ptr_f16w32(plan_id, fused, packed);
     default: return bwd_main_kernel_ptr_f32(plan_id, fused, packed);
     }
 }
 
 static int launch_fwd_dt(int dt, int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
-    switch (dt) {
-    case RMSNORM_BF16: return launch_fwd_bf16(plan_id, fused, p, grid, stream);
-    case RMSNORM_F16: return launch_fwd_f16(plan_id, fused, p, grid, stream);
+    switch (kind_of(dt)) {
+    case 1: return launch_fwd_bf16(plan_id, fused, p, grid, stream);
+    case 2: return launch_fwd_f16(plan_id, fused, p, grid, stream);
+    case 3: return launch_fwd_bf16w32(plan_id, fused, p, grid, stream);
+    case 4: return launch_fwd_f16w32(plan_id, fused, p, grid, stream);
     default: return launch_fwd_f32(plan_id, fused, p, grid, stream);
     }
 }
 
 static int launch_bwd_dt(int dt, int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem,
                          void *stream) {
-    switch (dt) {
-    case RMSNORM_BF16: return launch_bwd_main_bf16(plan_id, fused, packed, p, grid, smem, stream);
-    case RMSNORM_F16: return launch_bwd_main_f16(plan_id, fused, packed, p, grid, smem, stream);
+    switch (kind_of(dt)) {
+    case 1: return launch_bwd_main_bf16(plan_id, fused, packed, p, grid, smem, stream);
+    case 2: return launch_bwd_main_f16(plan_id, fused, packed, p, grid, smem, stream);
+    case 3: return launch_bwd_main_bf16w32(plan_id, fused, packed, p, grid, smem, stream);
+    case 4: return launch_bwd_main_f16w32(plan_id, fused, packed, p, grid, smem, stream);
     default: return launch_bwd_main_f32(plan_id, fused, packed, p, grid, smem, stream);
     }
 }
 
+// dW is written in the weight's storage type.
 static int launch_finalize_dt(int dt, const float *ws, int parts, int N, void *dw, void *stream, bool serial) {
-    switch (dt) {
-    case RMSNORM_BF16: return launch_dw_finalize_bf16(ws, parts, N, dw, stream, serial);
-    case RMSNORM_F16: return launch_dw_finalize_f16(ws, parts, N, dw, stream, serial);
+    switch (kind_of(dt)) {
+    case 1: return launch_dw_finalize_bf16(ws, parts, N, dw, stream, serial);
+    case 2: return launch_dw_finalize_f16(ws, parts, N, dw, stream, serial);
     default: return launch_dw_finalize_f32(ws, parts, N, dw, stream, serial);
     }
 }
@@ -217,16 +246,16 @@ static int launch_finalize_dt(int dt, const float *ws, int parts, int N, void *d
 // resident CTAs on the device (resident clusters for a cluster plan), the
 // minimum over its packed and scalar variants for the given fusion mode, so
 // those two variants use the same count (and dW the same summation order).
-// Cached per device, dtype, plan and mode.
+// Cached per device, kernel kind, plan and mode.
 static std::mutex g_occ_mutex;
-static int g_parts_cache[kMaxDevices][3][2][64];
-static int g_cps_cache[kMaxDevices][3][2][64];
+static int g_parts_cache[kMaxDevices][kNumKinds][2][64];
+static int g_cps_cache[kMaxDevices][kNumKinds][2][64];
 
 static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, int64_t N, bool fused,
                                  int *parts_out, int *cps_out) {
     const int slot = d.id;
     if (slot < 0 || slot >= 64) return cudaErrorInvalidValue;
-    const int dti = dt;  // 0 fp32, 1 bf16, 2 fp16
+    const int dti = kind_of(dt);
     const int fi = fused ? 1 : 0;
     {
         std::lock_guard<std::mutex> lk(g_occ_mutex);
@@ -290,7 +319,7 @@ static std::atomic<int> g_table_ok{-1};
 int self_check_impl() {
     int bad = 0;
     for (int op = 0; op < 2; ++op) {
-        for (int dt = 0; dt < 3; ++dt) {
+        for (int dt = 0; dt < 3; ++dt) {  // the activations' type decides the defaults
             int64_t expect = 1;
             for (int i = 0; i < kNumPlans; ++i) {
                 const PlanDesc &d = kPlans[i];
@@ -351,7 +380,8 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (fused && (!residual || !residual_out)) return RMSNORM_ERR_INVALID_ARG;
     if (!x || !y || !rstd) return RMSNORM_ERR_INVALID_ARG;  // w NULL: non-affine
     const uintptr_t s = (uintptr_t)elem_size(dt);
-    if (!aligned_to(x, s) || (w && !aligned_to(w, s)) || !aligned_to(y, s) || !aligned_to(rstd, 4))
+    const uintptr_t ws_ = (uintptr_t)weight_size(dt);
+    if (!aligned_to(x, s) || (w && !aligned_to(w, ws_)) || !aligned_to(y, s) || !aligned_to(rstd, 4))
         return RMSNORM_ERR_INVALID_ARG;
     if (fused && (!aligned_to(residual, s) || !aligned_to(residual_out, s))) return RMSNORM_ERR_INVALID_ARG;
 
@@ -393,19 +423,20 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     if (force_packed < -1 || force_packed > 1) return RMSNORM_ERR_INVALID_ARG;
     if (!fused) dres = nullptr;
     const uintptr_t s = (uintptr_t)elem_size(dt);
+    const uintptr_t wsz = (uintptr_t)weight_size(dt);
     // Non-affine (w NULL): there is no dW, so dw must be NULL as well.
     if ((w == nullptr) != (dw == nullptr)) return RMSNORM_ERR_INVALID_ARG;
     const bool affine = w != nullptr;
     if (M == 0) {
         // dw is the empty sum; the empty [0, N] tensors may be NULL
         if (!affine) return RMSNORM_SUCCESS;
-        if (!aligned_to(dw, s)) return RMSNORM_ERR_INVALID_ARG;
-        cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)N * s, stream);
+        if (!aligned_to(dw, wsz)) return RMSNORM_ERR_INVALID_ARG;
+        cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)N * wsz, stream);
         if (e != cudaSuccess) return cuda_fail(e);
         return RMSNORM_SUCCESS;
     }
     if (!dy || !x || !rstd || !dx) return RMSNORM_ERR_INVALID_ARG;
-    if (!aligned_to(dy, s) || !aligned_to(x, s) || (affine && (!aligned_to(w, s) || !aligned_to(dw, s))) ||
+    if (!aligned_to(dy, s) || !aligned_to(x, s) || (affine && (!aligned_to(w, wsz) || !aligned_to(dw, wsz))) ||
         !aligned_to(dx, s) || !aligned_to(rstd, 4) || (dres && !aligned_to(dres, s)))
         return RMSNORM_ERR_INVALID_ARG;
     if (workspace && !aligned_to(workspace, 16)) return RMSNORM_ERR_WORKSPACE;

@@ -1,13 +1,13 @@
-// bwd_bf16.cu -- bf16 instantiations of the backward kernels.
+// bwd_bf16.cu -- backward kernels for bf16.
 #include "bwd_kernels.cuh"
 
 namespace rmsn {
 int launch_bwd_main_bf16(int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem,
                          void *stream) {
-    return bwd_launch_t<__nv_bfloat16>(plan_id, fused, packed, p, grid, smem, stream);
+    return bwd_launch_t<__nv_bfloat16, __nv_bfloat16>(plan_id, fused, packed, p, grid, smem, stream);
 }
 const void *bwd_main_kernel_ptr_bf16(int plan_id, bool fused, bool packed) {
-    return bwd_ptr_t<__nv_bfloat16>(plan_id, fused, packed);
+    return bwd_ptr_t<__nv_bfloat16, __nv_bfloat16>(plan_id, fused, packed);
 }
 int launch_dw_finalize_bf16(const float *ws, int parts, int N, void *dw, void *stream, bool serial) {
     return finalize_launch_t<__nv_bfloat16>(ws, parts, N, dw, stream, serial);

@@ -1,13 +1,13 @@
-// bwd_f32.cu -- fp32 instantiations of the backward kernels.
+// bwd_f32.cu -- backward kernels for fp32.
 #include "bwd_kernels.cuh"
 
 namespace rmsn {
 int launch_bwd_main_f32(int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem,
-                        void *stream) {
-    return bwd_launch_t<float>(plan_id, fused, packed, p, grid, smem, stream);
+                         void *stream) {
+    return bwd_launch_t<float, float>(plan_id, fused, packed, p, grid, smem, stream);
 }
 const void *bwd_main_kernel_ptr_f32(int plan_id, bool fused, bool packed) {
-    return bwd_ptr_t<float>(plan_id, fused, packed);
+    return bwd_ptr_t<float, float>(plan_id, fused, packed);
 }
 int launch_dw_finalize_f32(const float *ws, int parts, int N, void *dw, void *stream, bool serial) {
     return finalize_launch_t<float>(ws, parts, N, dw, stream, serial);

@@ -59,7 +59,7 @@ __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, in
 // CS > 1: the CTAs of a cluster share each row (CTA rank r holds chunks
 // [r TPR V, (r+1) TPR V)); the row sum meets in distributed shared memory
 // and the cluster, not the CTA, owns one dW partial row.
-template <typename T, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool FUSED>
 __global__ void __launch_bounds__(TPR *TEAMS)
     rmsnorm_bwd_vector(const BwdParams p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
@@ -92,8 +92,12 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
         float2 wv[NP];
-        unpack<T>((has_w && c < C) ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + c) : make_uint4(0, 0, 0, 0),
-                  wv);
+        if (has_w && c < C) {
+            load_w_chunk<T, TW>(p.w, c, wv);
+        } else {
+#pragma unroll
+            for (int k = 0; k < NP; ++k) wv[k] = make_float2(0.f, 0.f);
+        }
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
             wp[v][k] = has_w ? Pk::add(o2, wv[k]) : make_float2(1.f, 1.f);
@@ -299,11 +303,11 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 // partial row lives in the workspace itself: the thread that owns column j
 // writes ws[cta, j] on its first row and updates it on later rows, so no
 // other thread touches it and no atomics are needed.
-template <typename T, bool FUSED>
+template <typename T, typename TW, bool FUSED>
 __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
     __shared__ float red[32];
     const int N = p.N;
-    const T *w = reinterpret_cast<const T *>(p.w);
+    const TW *w = reinterpret_cast<const TW *>(p.w);
     float *wsrow = p.ws + (int64_t)blockIdx.x * N;
     const bool has_dres = FUSED && p.dres != nullptr;
     bool first = true;
@@ -411,13 +415,13 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int 
 
 // ------------------------------------------------------------- dispatch --
 
-template <typename T, int TPR, int V, int TEAMS, int D, int CS, bool PACKED>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED>
 static int bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     if constexpr (CS == 1) {
         if (fused)
-            rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, 1, PACKED, true><<<grid, TPR * TEAMS, smem, s>>>(p);
+            rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, 1, PACKED, true><<<grid, TPR * TEAMS, smem, s>>>(p);
         else
-            rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, 1, PACKED, false><<<grid, TPR * TEAMS, smem, s>>>(p);
+            rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, 1, PACKED, false><<<grid, TPR * TEAMS, smem, s>>>(p);
         return (int)cudaGetLastError();
     } else {
         cudaLaunchConfig_t cfg = {};
@@ -432,53 +436,62 @@ static int bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cu
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, PACKED, true>, p)
-                     : (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, PACKED, false>, p);
+        return fused
+                   ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, PACKED, true>, p)
+                   : (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, PACKED, false>, p);
     }
 }
 
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
+// A weight type other than the activations' is compiled for the default
+// plans (and the generic one) only; alternatives are for tuning.
+template <typename T, typename TW, int PATH, int CMIN>
+constexpr bool bwd_instantiated() {
+    return std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0;
+}
+
+template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
 static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    if constexpr (OP != OP_BWD) {
+    if constexpr (OP != OP_BWD || !bwd_instantiated<T, TW, PATH, CMIN>()) {
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
         if (fused)
-            rmsnorm_bwd_generic<T, true><<<grid, 256, 0, s>>>(p);
+            rmsnorm_bwd_generic<T, TW, true><<<grid, 256, 0, s>>>(p);
         else
-            rmsnorm_bwd_generic<T, false><<<grid, 256, 0, s>>>(p);
+            rmsnorm_bwd_generic<T, TW, false><<<grid, 256, 0, s>>>(p);
         return (int)cudaGetLastError();
     } else if constexpr (PATH == PATH_VECTOR) {
-        return packed ? bwd_launch_vec<T, TPR, V, TEAMS, D, CS, true>(fused, p, grid, smem, s)
-                      : bwd_launch_vec<T, TPR, V, TEAMS, D, CS, false>(fused, p, grid, smem, s);
+        return packed ? bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, true>(fused, p, grid, smem, s)
+                      : bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, false>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
 }
 
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
+template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
 static const void *bwd_ptr_entry(bool fused, bool packed) {
-    if constexpr (OP != OP_BWD) {
+    if constexpr (OP != OP_BWD || !bwd_instantiated<T, TW, PATH, CMIN>()) {
         return nullptr;
     } else if constexpr (PATH == PATH_GENERIC) {
-        return fused ? (const void *)rmsnorm_bwd_generic<T, true> : (const void *)rmsnorm_bwd_generic<T, false>;
+        return fused ? (const void *)rmsnorm_bwd_generic<T, TW, true> : (const void *)rmsnorm_bwd_generic<T, TW, false>;
     } else if constexpr (PATH == PATH_VECTOR) {
         if (packed)
-            return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true, true>
-                         : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true, false>;
-        return fused ? (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false, true>
-                     : (const void *)rmsnorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false, false>;
+            return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, true>
+                         : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, false>;
+        return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, true>
+                     : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, false>;
     } else {
         return nullptr;
     }
 }
 
-template <typename T>
+template <typename T, typename TW>
 static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem,
                         void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (plan_id) {
 #define RMSN_BWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return bwd_launch_entry<T, op, path, tpr, v, teams, depth, cs>(fused, packed, p, grid, smem, s);
+    case id:                                                                    \
+        return bwd_launch_entry<T, TW, op, path, tpr, v, teams, depth, cs, cmin>(fused, packed, p, grid, smem, s);
         RMSNORM_PLAN_TABLE(RMSN_BWD_CASE)
 #undef RMSN_BWD_CASE
     default:
@@ -486,11 +499,11 @@ static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p
     }
 }
 
-template <typename T>
+template <typename T, typename TW>
 static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
     switch (plan_id) {
 #define RMSN_BWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return bwd_ptr_entry<T, op, path, tpr, v, teams, depth, cs>(fused, packed);
+    case id: return bwd_ptr_entry<T, TW, op, path, tpr, v, teams, depth, cs, cmin>(fused, packed);
         RMSNORM_PLAN_TABLE(RMSN_BWD_PTR)
 #undef RMSN_BWD_PTR
     default:

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace rmsn {
 
 // Elements per 16-byte chunk and per register pair.
@@ -79,6 +81,27 @@ template <> __device__ __forceinline__ uint4 pack<__nv_bfloat16>(const float2 (&
 template <> __device__ __forceinline__ uint4 pack<float>(const float2 (&p)[2]) {
     return make_uint4(__float_as_uint(p[0].x), __float_as_uint(p[0].y), __float_as_uint(p[1].x),
                       __float_as_uint(p[1].y));
+}
+
+// Weight values for activation chunk c (chunk = 16 bytes of activations).
+// The weight is stored either in the activations' type (one 16-byte load)
+// or in fp32 next to 2-byte activations (two 16-byte loads); the pairs come
+// out in the chunk's (even, odd) column order either way.
+template <typename T, typename TW>
+__device__ __forceinline__ void load_w_chunk(const void *w, int c, float2 (&wv)[Elem<T>::NP]) {
+    if constexpr (std::is_same<T, TW>::value) {
+        unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(w) + c), wv);
+    } else {
+        static_assert(std::is_same<TW, float>::value && Elem<T>::E == 8, "fp32 weight with 2-byte activations");
+        const uint4 *w4 = reinterpret_cast<const uint4 *>(w) + 2 * c;
+        float2 a[2], b[2];
+        unpack<float>(ld_keep(w4), a);
+        unpack<float>(ld_keep(w4 + 1), b);
+        wv[0] = a[0];
+        wv[1] = a[1];
+        wv[2] = b[0];
+        wv[3] = b[1];
+    }
 }
 
 // Scalar element access for the generic kernels.

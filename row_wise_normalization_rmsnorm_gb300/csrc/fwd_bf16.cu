@@ -1,9 +1,9 @@
-// fwd_bf16.cu -- bf16 instantiations of the forward kernels.
+// fwd_bf16.cu -- forward kernels for bf16.
 #include "fwd_kernels.cuh"
 
 namespace rmsn {
 int launch_fwd_bf16(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
-    return launch_t<__nv_bfloat16>(plan_id, fused, p, grid, stream);
+    return launch_t<__nv_bfloat16, __nv_bfloat16>(plan_id, fused, p, grid, stream);
 }
-const void *fwd_kernel_ptr_bf16(int plan_id, bool fused) { return ptr_t<__nv_bfloat16>(plan_id, fused); }
+const void *fwd_kernel_ptr_bf16(int plan_id, bool fused) { return ptr_t<__nv_bfloat16, __nv_bfloat16>(plan_id, fused); }
 }  // namespace rmsn

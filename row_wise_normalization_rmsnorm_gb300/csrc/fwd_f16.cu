@@ -1,9 +1,9 @@
-// fwd_f16.cu -- f16 instantiations of the forward kernels.
+// fwd_f16.cu -- forward kernels for fp16.
 #include "fwd_kernels.cuh"
 
 namespace rmsn {
 int launch_fwd_f16(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
-    return launch_t<__half>(plan_id, fused, p, grid, stream);
+    return launch_t<__half, __half>(plan_id, fused, p, grid, stream);
 }
-const void *fwd_kernel_ptr_f16(int plan_id, bool fused) { return ptr_t<__half>(plan_id, fused); }
+const void *fwd_kernel_ptr_f16(int plan_id, bool fused) { return ptr_t<__half, __half>(plan_id, fused); }
 }  // namespace rmsn

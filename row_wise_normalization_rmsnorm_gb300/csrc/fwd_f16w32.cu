@@ -1,0 +1,9 @@
+// fwd_f16w32.cu -- forward kernels for fp16 activations with an fp32 weight.
+#include "fwd_kernels.cuh"
+
+namespace rmsn {
+int launch_fwd_f16w32(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
+    return launch_t<__half, float>(plan_id, fused, p, grid, stream);
+}
+const void *fwd_kernel_ptr_f16w32(int plan_id, bool fused) { return ptr_t<__half, float>(plan_id, fused); }
+}  // namespace rmsn

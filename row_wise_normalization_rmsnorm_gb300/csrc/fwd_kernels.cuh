@@ -24,7 +24,7 @@ namespace rmsn {
 // CS > 1: the CTAs of a cluster share one row; CTA rank r holds chunks
 // [r TPR V, (r+1) TPR V) and the sum of squares meets in distributed shared
 // memory (wide rows whose chunks exceed one CTA's registers).
-template <typename T, int TPR, int V, int TEAMS, int CS, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED>
 __global__ void __launch_bounds__(TPR *TEAMS)
     rmsnorm_fwd_vector(const FwdParams p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             unpack<T>(xv[v], a);
             if (has_w) {
                 float2 wv[NP];
-                unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.w) + c), wv);
+                load_w_chunk<T, TW>(p.w, c, wv);
 #pragma unroll
                 for (int k = 0; k < NP; ++k) a[k] = Pk::mul(Pk::mul(a[k], r2), Pk::add(o2, wv[k]));
             } else {
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     }
 }
 
-template <typename T, bool FUSED>
+template <typename T, typename TW, bool FUSED>
 __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     const T *x = reinterpret_cast<const T *>(p.x) + row * N;
     const T *res = reinterpret_cast<const T *>(p.residual) + row * N;
     T *hout = reinterpret_cast<T *>(p.residual_out) + row * N;
-    const T *w = reinterpret_cast<const T *>(p.w);
+    const TW *w = reinterpret_cast<const TW *>(p.w);
     T *y = reinterpret_cast<T *>(p.y) + row * N;
 
     float ss = 0.f;
@@ -155,14 +155,14 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
 
 // ------------------------------------------------------------- dispatch --
 
-template <typename T, int TPR, int V, int TEAMS, int CS>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int CS>
 static int launch_vec(bool fused, const FwdParams &p, int grid, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if constexpr (CS == 1) {
         if (fused)
-            rmsnorm_fwd_vector<T, TPR, V, TEAMS, 1, true><<<grid, TPR * TEAMS, 0, s>>>(p);
+            rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, 1, true><<<grid, TPR * TEAMS, 0, s>>>(p);
         else
-            rmsnorm_fwd_vector<T, TPR, V, TEAMS, 1, false><<<grid, TPR * TEAMS, 0, s>>>(p);
+            rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, 1, false><<<grid, TPR * TEAMS, 0, s>>>(p);
         return (int)cudaGetLastError();
     } else {
         cudaLaunchConfig_t cfg = {};
@@ -176,55 +176,62 @@ static int launch_vec(bool fused, const FwdParams &p, int grid, void *stream) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TPR, V, TEAMS, CS, true>, p)
-                     : (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TPR, V, TEAMS, CS, false>, p);
+        return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true>, p)
+                     : (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false>, p);
     }
 }
 
-template <typename T, int TPR, int V, int TEAMS, int CS>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int CS>
 static const void *ptr_vec(bool fused) {
-    return fused ? (const void *)rmsnorm_fwd_vector<T, TPR, V, TEAMS, CS, true>
-                 : (const void *)rmsnorm_fwd_vector<T, TPR, V, TEAMS, CS, false>;
+    return fused ? (const void *)rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true>
+                 : (const void *)rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false>;
 }
 
-template <typename T>
+template <typename T, typename TW>
 static int launch_gen(bool fused, const FwdParams &p, int grid, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (fused)
-        rmsnorm_fwd_generic<T, true><<<grid, 256, 0, s>>>(p);
+        rmsnorm_fwd_generic<T, TW, true><<<grid, 256, 0, s>>>(p);
     else
-        rmsnorm_fwd_generic<T, false><<<grid, 256, 0, s>>>(p);
+        rmsnorm_fwd_generic<T, TW, false><<<grid, 256, 0, s>>>(p);
     return (int)cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, typename TW>
 static const void *ptr_gen(bool fused) {
-    return fused ? (const void *)rmsnorm_fwd_generic<T, true> : (const void *)rmsnorm_fwd_generic<T, false>;
+    return fused ? (const void *)rmsnorm_fwd_generic<T, TW, true> : (const void *)rmsnorm_fwd_generic<T, TW, false>;
+}
+
+// A weight type other than the activations' is compiled for the default
+// plans (and the generic one) only; alternatives are for tuning.
+template <typename T, typename TW, int PATH, int CMIN>
+constexpr bool instantiated() {
+    return std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0;
 }
 
 // One switch case per table entry; `if constexpr` keeps kernels of other
-// ops and paths from being instantiated here.
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int CS>
+// ops, paths and weight types from being instantiated here.
+template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
 static int launch_entry(bool fused, const FwdParams &p, int grid, void *stream) {
-    if constexpr (OP != OP_FWD) return (int)cudaErrorInvalidValue;
-    else if constexpr (PATH == PATH_GENERIC) return launch_gen<T>(fused, p, grid, stream);
-    else if constexpr (PATH == PATH_VECTOR) return launch_vec<T, TPR, V, TEAMS, CS>(fused, p, grid, stream);
+    if constexpr (OP != OP_FWD || !instantiated<T, TW, PATH, CMIN>()) return (int)cudaErrorInvalidValue;
+    else if constexpr (PATH == PATH_GENERIC) return launch_gen<T, TW>(fused, p, grid, stream);
+    else if constexpr (PATH == PATH_VECTOR) return launch_vec<T, TW, TPR, V, TEAMS, CS>(fused, p, grid, stream);
     else return (int)cudaErrorInvalidValue;
 }
 
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int CS>
+template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
 static const void *ptr_entry(bool fused) {
-    if constexpr (OP != OP_FWD) return nullptr;
-    else if constexpr (PATH == PATH_GENERIC) return ptr_gen<T>(fused);
-    else if constexpr (PATH == PATH_VECTOR) return ptr_vec<T, TPR, V, TEAMS, CS>(fused);
+    if constexpr (OP != OP_FWD || !instantiated<T, TW, PATH, CMIN>()) return nullptr;
+    else if constexpr (PATH == PATH_GENERIC) return ptr_gen<T, TW>(fused);
+    else if constexpr (PATH == PATH_VECTOR) return ptr_vec<T, TW, TPR, V, TEAMS, CS>(fused);
     else return nullptr;
 }
 
-template <typename T>
+template <typename T, typename TW>
 static int launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
     switch (plan_id) {
 #define RMSN_FWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return launch_entry<T, op, path, tpr, v, teams, cs>(fused, p, grid, stream);
+    case id: return launch_entry<T, TW, op, path, tpr, v, teams, cs, cmin>(fused, p, grid, stream);
         RMSNORM_PLAN_TABLE(RMSN_FWD_CASE)
 #undef RMSN_FWD_CASE
     default:
@@ -232,11 +239,11 @@ static int launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void 
     }
 }
 
-template <typename T>
+template <typename T, typename TW>
 static const void *ptr_t(int plan_id, bool fused) {
     switch (plan_id) {
 #define RMSN_FWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return ptr_entry<T, op, path, tpr, v, teams, cs>(fused);
+    case id: return ptr_entry<T, TW, op, path, tpr, v, teams, cs, cmin>(fused);
         RMSNORM_PLAN_TABLE(RMSN_FWD_PTR)
 #undef RMSN_FWD_PTR
     default:

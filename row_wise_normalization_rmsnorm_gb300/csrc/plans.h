@@ -122,26 +122,25 @@ constexpr int kStatusClusterWaitTimeout = 1;
 // Polls of an mbarrier before a wait gives up (at most seconds).
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-// Launchers, defined in the per-dtype translation units that instantiate
-// the kernels. They return the launch's cudaError_t.
-int launch_fwd_f32(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);
-int launch_fwd_bf16(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);
-int launch_fwd_f16(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);
-const void *fwd_kernel_ptr_f32(int plan_id, bool fused);
-const void *fwd_kernel_ptr_bf16(int plan_id, bool fused);
-const void *fwd_kernel_ptr_f16(int plan_id, bool fused);
+// Launchers, defined in the per-type translation units that instantiate
+// the kernels (suffix: activations' type, "w32" = fp32 weight). They return
+// the launch's cudaError_t.
+#define RMSN_DECLARE_LAUNCHERS(suf)                                                                       \
+    int launch_fwd_##suf(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);           \
+    const void *fwd_kernel_ptr_##suf(int plan_id, bool fused);                                           \
+    int launch_bwd_main_##suf(int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem, \
+                              void *stream);                                                           \
+    const void *bwd_main_kernel_ptr_##suf(int plan_id, bool fused, bool packed);
+RMSN_DECLARE_LAUNCHERS(f32)
+RMSN_DECLARE_LAUNCHERS(bf16)
+RMSN_DECLARE_LAUNCHERS(f16)
+RMSN_DECLARE_LAUNCHERS(bf16w32)
+RMSN_DECLARE_LAUNCHERS(f16w32)
+#undef RMSN_DECLARE_LAUNCHERS
 
-int launch_bwd_main_bf16(int plan_id, bool fused, bool packed, const BwdParams &p, int grid,
-                         int smem, void *stream);
-int launch_bwd_main_f32(int plan_id, bool fused, bool packed, const BwdParams &p, int grid,
-                        int smem, void *stream);
-int launch_bwd_main_f16(int plan_id, bool fused, bool packed, const BwdParams &p, int grid,
-                        int smem, void *stream);
-const void *bwd_main_kernel_ptr_bf16(int plan_id, bool fused, bool packed);
-const void *bwd_main_kernel_ptr_f32(int plan_id, bool fused, bool packed);
-const void *bwd_main_kernel_ptr_f16(int plan_id, bool fused, bool packed);
-int launch_dw_finalize_bf16(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
+// dW finalizers, by dW's storage type.
 int launch_dw_finalize_f32(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
+int launch_dw_finalize_bf16(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
 int launch_dw_finalize_f16(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
 
 }  // namespace rmsn

@@ -88,6 +88,41 @@ def test_dtype_specific_backward_defaults(rn):
     assert (f["threads_per_row"], f["chunks_per_thread"]) == (b["threads_per_row"], b["chunks_per_thread"])
 
 
+def test_fp32_weight_flag_plans(rn):
+    """dt | RMSNORM_WEIGHT_F32 selects the activations' default plans; forced
+    alternative vector plans are refused (not compiled for that pairing);
+    the flag on fp32 activations is the same as fp32."""
+    W = rn.RMSNORM_WEIGHT_F32
+    for op in (rn.OP_FWD, rn.OP_BWD):
+        for N in (128, 2048, 8192, 16384):
+            for base in (rn.RMSNORM_BF16, rn.RMSNORM_F16):
+                a = rn.plan_query(op, 4096, N, base, num_sms=152, ctas_per_sm=1)
+                b = rn.plan_query(op, 4096, N, base | W, num_sms=152, ctas_per_sm=1)
+                assert a == b
+            assert (rn.plan_query(op, 4096, N, rn.RMSNORM_F32 | W, num_sms=152, ctas_per_sm=1) ==
+                    rn.plan_query(op, 4096, N, rn.RMSNORM_F32, num_sms=152, ctas_per_sm=1))
+    default = rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16)["plan_id"]
+    defaults = {rn.plan_query(rn.OP_FWD, 64, n, t)["plan_id"] for n in range(8, 65537, 8) for t in (0, 1, 2)}
+    refused = 0
+    for i in range(rn.lib().rmsnorm_plan_count()):
+        pid = rn.lib().rmsnorm_plan_id_at(i)
+        try:
+            p = rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16, force_plan=pid)
+        except rn.RMSNormError:
+            continue
+        if p["path_name"] == "vector" and pid not in defaults:
+            with pytest.raises(rn.RMSNormError):
+                rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16 | W, force_plan=pid)
+            refused += 1
+    assert refused > 0
+    assert rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16 | W, force_plan=default)["plan_id"] == default
+    # the generic plan serves any pairing
+    assert rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_F16 | W, force_plan=16)["path_name"] == "generic"
+    # unknown flag bits are rejected
+    with pytest.raises(rn.RMSNormError):
+        rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16 | 0x200)
+
+
 def test_misaligned_pointers_take_generic(rn):
     assert rn.plan_query(rn.OP_FWD, 4096, 7168, 1, aligned=False)["path_name"] == "generic"
     assert rn.plan_query(rn.OP_BWD, 4096, 2048, 0, aligned=False)["path_name"] == "generic"
@@ -138,6 +173,9 @@ def test_invalid_arguments_without_gpu(rn):
     assert L.rmsnorm_fwd(x, x, x, r, 4, 8, 1, float("nan"), 0.0, None) == 1
     assert L.rmsnorm_fwd(x, x, x, r, 4, 8, 1, 1e-6, float("inf"), None) == 1
     assert L.rmsnorm_fwd(x, x, x, r, 4, 8, 7, 1e-6, 0.0, None) == 1           # unknown dtype
+    assert L.rmsnorm_fwd(x, x, x, r, 4, 8, 0x201, 1e-6, 0.0, None) == 1       # unknown flag
+    # an fp32 weight must be 4-byte aligned
+    assert L.rmsnorm_fwd(x, ctypes.c_void_p(258), x, r, 4, 8, 0x101, 1e-6, 0.0, None) == 1
     assert L.rmsnorm_fwd(x, x, x, r, -1, 8, 1, 1e-6, 0.0, None) == 1          # negative M
     assert L.rmsnorm_fwd(ctypes.c_void_p(257), x, x, r, 4, 8, 1, 1e-6, 0.0, None) == 1  # odd bf16 address
     assert L.rmsnorm_add_fwd(x, None, x, x, x, r, 4, 8, 1, 1e-6, 0.0, None) == 1

@@ -27,10 +27,12 @@ def rn():
     return pkg
 
 
-def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_path=None):
+def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_path=None, wdt=None):
+    """wdt: the weight's (and dW's) storage type, default the activations'."""
+    wdt = wdt or dt
     M, N = d["x"].shape
     x = to_dev(d["x"], dt, offset=offset_elems)
-    w = to_dev(d["w"], dt, offset=offset_elems)
+    w = to_dev(d["w"], wdt, offset=offset_elems)
     dy = to_dev(d["dy"], dt, offset=offset_elems)
     y = empty_dev((M, N), dt, offset=offset_elems)
     rstd = torch.full((M,), float("nan"), device="cuda")
@@ -38,7 +40,8 @@ def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_p
     hout = empty_dev((M, N), dt, offset=offset_elems) if fused else None
     _, _, _, fplan = rn.rmsnorm_fwd_ex(x, w, residual=res, residual_out=hout, y=y, rstd=rstd, eps=eps,
                                        offset=offset)
-    f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=eps, offset=offset, residual=d.get("residual") if fused else None)
+    f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=eps, offset=offset, residual=d.get("residual") if fused else None,
+                   wdtype=wdt)
     torch.cuda.synchronize()
     check_y(to_host(y, dt), f, dt)
     check_rstd(rstd.cpu().numpy(), f["rstd64"])
@@ -50,15 +53,16 @@ def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_p
     r32 = torch.from_numpy(f["rstd32"]).cuda()
     hdev = to_dev(h_np, dt, offset=offset_elems)
     dx = empty_dev((M, N), dt, offset=offset_elems)
-    dw = empty_dev((N,), dt, offset=offset_elems)
+    dw = empty_dev((N,), wdt, offset=offset_elems)
     dres_np = d.get("dres") if fused else None
     dres = to_dev(dres_np, dt, offset=offset_elems) if dres_np is not None else None
     _, _, bplan = rn.rmsnorm_bwd_ex(dy, hdev, w, r32, dresidual_out=dres, fused=fused, dx=dx, dw=dw, eps=eps,
                                     offset=offset)
-    b = oracle.bwd(d["dy"], h_np, d["w"], dtype=dt, eps=eps, offset=offset, rstd=f["rstd32"], dres=dres_np)
+    b = oracle.bwd(d["dy"], h_np, d["w"], dtype=dt, eps=eps, offset=offset, rstd=f["rstd32"], dres=dres_np,
+                   wdtype=wdt)
     torch.cuda.synchronize()
     needed = check_dx(to_host(dx, dt), b, dt)
-    check_dw(to_host(dw, dt), b, dt)
+    check_dw(to_host(dw, wdt), b, wdt)
     if expect_path is not None:
         assert fplan["path_name"] == expect_path and bplan["path_name"] == expect_path, (fplan, bplan)
     # The floor is for cancellation only: it should be needed rarely on
@@ -248,3 +252,72 @@ def test_f16_non_affine(rn):
     assert dw is None
     check_y(to_host(y, "f16"), f, "f16")
     check_dx(to_host(dx, "f16"), b, "f16")
+
+
+# ---- fp32 weight beside 16-bit activations (w and dW stored in fp32) ----
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N", [(333, 64), (257, 1024), (300, 4096), (1031, 8192), (129, 12288), (65, 16384),
+                                 (17, 65536), (101, 8193)])
+def test_fp32_weight_shapes(rn, dt, M, N):
+    d = inputs.make_inputs(M, N, dt, 140 + N % 13, wdtype="f32")
+    exp = "generic" if N % 8 else "vector"
+    _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, wdt="f32", expect_path=exp)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_fp32_weight_fused_add_gemma(rn, dt):
+    d = inputs.make_inputs(513, 4096, dt, 141, w_mode="gemma", residual=True, dres=True, wdtype="f32")
+    _fwd_bwd_check(rn, d, dt, 1e-6, 1.0, fused=True, wdt="f32", expect_path="vector")
+
+
+def test_fp32_weight_misaligned_takes_generic(rn):
+    d = inputs.make_inputs(300, 2048, "bf16", 142, wdtype="f32")
+    _fwd_bwd_check(rn, d, "bf16", 1e-6, 0.0, offset_elems=1, wdt="f32", expect_path="generic")
+
+
+def test_fp32_weight_full_size(rn):
+    """The bench's shape with an fp32 master weight, checked on sampled rows
+    (y, dx) and on every column of dW against the oracle."""
+    M, N = 16384, 8192
+    d = inputs.make_inputs(M, N, "bf16", inputs.SWEEP_SEED, wdtype="f32", outlier_frac=0.01)
+    x, dy = to_dev(d["x"], "bf16"), to_dev(d["dy"], "bf16")
+    w = to_dev(d["w"], "f32")
+    y, rstd = rn.rmsnorm_fwd(x, w)
+    dx, dw = rn.rmsnorm_bwd(dy, x, w, rstd)
+    assert dw.dtype == torch.float32
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(7).choice(M, 256, replace=False)
+    f = oracle.fwd(d["x"][rows], d["w"], dtype="bf16", eps=1e-6, offset=0.0, wdtype="f32")
+    check_y(to_host(y, "bf16")[rows], f, "bf16")
+    bs = oracle.bwd(d["dy"][rows], d["x"][rows], d["w"], dtype="bf16", eps=1e-6, offset=0.0,
+                    rstd=rstd.cpu().numpy()[rows], wdtype="f32")
+    check_dx(to_host(dx, "bf16")[rows], bs, "bf16")
+    b = oracle.bwd(d["dy"], d["x"], d["w"], dtype="bf16", eps=1e-6, offset=0.0, rstd=rstd.cpu().numpy(),
+                   want_dx=False, wdtype="f32")
+    check_dw(to_host(dw, "f32"), b, "f32")
+
+
+def test_fp32_weight_refuses_alternative_plans(rn):
+    """Only the default plans are compiled with an fp32 weight: a forced
+    alternative is refused before launch, the default runs."""
+    d = inputs.make_inputs(64, 2048, "bf16", 143, wdtype="f32")
+    x, w = to_dev(d["x"], "bf16"), to_dev(d["w"], "f32")
+    default = rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16)["plan_id"]
+    defaults = {rn.plan_query(rn.OP_FWD, 64, n, t)["plan_id"] for n in range(8, 65537, 8) for t in (0, 1, 2)}
+    alternatives = []
+    for i in range(rn.lib().rmsnorm_plan_count()):
+        pid = rn.lib().rmsnorm_plan_id_at(i)
+        try:
+            p = rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16, force_plan=pid)
+        except rn.RMSNormError:
+            continue
+        if p["path_name"] == "vector" and pid not in defaults:
+            alternatives.append(pid)
+    assert alternatives
+    for pid in alternatives:
+        with pytest.raises(rn.RMSNormError):
+            rn.rmsnorm_fwd_ex(x, w, force_plan=pid)
+    y, _, _, plan = rn.rmsnorm_fwd_ex(x, w, force_plan=default)
+    torch.cuda.synchronize()
+    assert plan["plan_id"] == default
