@@ -75,6 +75,13 @@ def _load():
             lib.oracle_bf16_decode.argtypes = [ctypes.c_uint16]
             lib.oracle_f16_round_array.restype = i32
             lib.oracle_f16_round_array.argtypes = [vp, i64, vp]
+            lib.oracle_e4m3_round_array.restype = i32
+            lib.oracle_e4m3_round_array.argtypes = [vp, i64, vp]
+            lib.oracle_e4m3_decode_array.restype = None
+            lib.oracle_e4m3_decode_array.argtypes = [vp, i64, vp]
+            lib.oracle_rmsnorm_fwd_fp8.restype = i32
+            lib.oracle_rmsnorm_fwd_fp8.argtypes = [i32, i32, i64, i64, vp, vp, vp, dbl, dbl, i32, dbl,
+                                                   vp, vp, vp, vp, vp, vp, vp, vp, i32]
             _lib = lib
     return _lib
 
@@ -117,6 +124,22 @@ def f16_round(v) -> np.ndarray:
     return out.view(np.float16)
 
 
+def e4m3_round(v) -> np.ndarray:
+    """Round float64 values to E4M3 codes (nearest-even, saturating at +-448) in one step."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e4m3_round_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e4m3_decode(b) -> np.ndarray:
+    """Exact values of E4M3 codes as float64 (NaN for the two NaN codes)."""
+    b = np.ascontiguousarray(b, dtype=np.uint8)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_e4m3_decode_array(_ptr(b), b.size, _ptr(out))
+    return out
+
+
 def to_f64(a, dtype) -> np.ndarray:
     """Decode storage-type data to float64 exactly."""
     if dtype == "bf16":
@@ -153,6 +176,43 @@ def fwd(x, w, *, dtype, eps, offset, residual=None, nthreads=1, wdtype=None):
     if bad:
         raise FloatingPointError(f"oracle fwd: {bad} non-finite or overflowing stores")
     return {"y": y, "y64": y64, "h": h, "rstd64": r64, "rstd32": r32}
+
+
+def fwd_fp8(x, w, *, dtype, eps, offset, scaling, scale=None, residual=None, nthreads=1, wdtype=None):
+    """RMSNorm forward with E4M3 output: yq = E4M3(y * s).
+
+    ``scaling`` "tensor": ``s = scale`` (given); "row": s_i = 448 / max_j |y_ij|
+    (1 for an all-zero row). Returns a dict with ``yq`` (uint8 codes),
+    ``y64`` (unrounded y), ``scaled64`` (y * s before rounding), ``amax_row``
+    (max_j |y_ij|), ``amax`` (max over the block), ``scale_inv`` (1 / s per
+    row), ``h`` (fused only), ``rstd64``, ``rstd32``.
+    """
+    wdtype = wdtype or dtype
+    mode = {"tensor": 0, "row": 1}[scaling]
+    if mode == 0 and scale is None:
+        raise ValueError("oracle fwd_fp8: per-tensor scaling needs a scale")
+    x = _as_storage(x, dtype)
+    M, N = x.shape
+    w = _as_storage(w, wdtype, (N,))
+    residual = _as_storage(residual, dtype, (M, N))
+    yq = np.empty((M, N), dtype=np.uint8)
+    y64 = np.empty((M, N), dtype=np.float64)
+    sc64 = np.empty((M, N), dtype=np.float64)
+    amax_row = np.empty((M,), dtype=np.float64)
+    sinv = np.empty((M,), dtype=np.float64)
+    h = np.empty((M, N), dtype=_NP_STORAGE[dtype]) if residual is not None else None
+    r64 = np.empty((M,), dtype=np.float64)
+    r32 = np.empty((M,), dtype=np.float32)
+    bad = _load().oracle_rmsnorm_fwd_fp8(_DTYPE_CODE[dtype], _DTYPE_CODE[wdtype], M, N, _ptr(x), _ptr(residual),
+                                         _ptr(w), float(eps), float(offset), mode,
+                                         float(scale) if scale is not None else 1.0,
+                                         _ptr(yq), _ptr(y64), _ptr(sc64), _ptr(amax_row), _ptr(sinv), _ptr(h),
+                                         _ptr(r64), _ptr(r32), int(nthreads))
+    if bad:
+        raise FloatingPointError(f"oracle fwd_fp8: {bad} non-finite values")
+    return {"yq": yq, "y64": y64, "scaled64": sc64, "amax_row": amax_row,
+            "amax": float(amax_row.max()) if M else 0.0, "scale_inv": sinv, "h": h,
+            "rstd64": r64, "rstd32": r32}
 
 
 def bwd(dy, h, w, *, dtype, eps, offset, rstd=None, dres=None, want_dx=True, nthreads=1, wdtype=None):

@@ -44,6 +44,17 @@
  * fp32 by the C cast. f64 "storage" (dtype 2) means no rounding at all; the pins use it
  * for finite differences.
  *
+ * fp8 output (E4M3, the output type of a norm whose consumer is an fp8
+ * GEMM; the TransformerEngine page's kernel key carries otype kFloat8E4M3,
+ * "[ROCm] RMSNorm tuning", Description and the key round-trip check in the
+ * review): the unrounded y is multiplied by a scale s and rounded once to
+ * E4M3 (nearest-even, saturating to +-448). Two scalings:
+ *   per tensor  s is given (delayed scaling); amax = max_ij |y_ij| is reported
+ *   per row     a_i = max_j |y_ij|, s_i = 448 / a_i (1 when a_i = 0), so each
+ *               row uses the full E4M3 range; 1 / s_i is reported per row
+ * The pages give the output type only; the scalings are the two plain
+ * readings (a given scale, or one derived from the row's own maximum).
+ *
  * Parity pins live in tests/test_oracle_pins.py.
  */
 #include <math.h>
@@ -148,6 +159,55 @@ int oracle_f16_round(double v, uint16_t *out)
     return 0;
 }
 
+/* ---------------------------------------------------------------- E4M3 -- */
+
+/* E4M3 (the "fn" variant): 1 sign bit, 4 exponent bits (bias 7), 3 fraction
+ * bits; exponent field 0 is subnormal (f * 2^-9); no infinities; S.1111.111
+ * is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448. */
+double oracle_e4m3_decode(uint8_t b)
+{
+    const int sign = (b >> 7) & 1;
+    const int e = (b >> 3) & 0xf;
+    const int f = b & 0x7;
+    double v;
+    if (e == 15 && f == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);
+    else
+        v = ldexp((double)(f + 8), e - 10);         /* (8 + f) * 2^(e-7-3) */
+    return sign ? -v : v;
+}
+
+/*
+ * Round a double to E4M3, nearest with ties to even, in one step; finite
+ * values beyond the largest finite magnitude saturate to +-448 (no
+ * infinities in this format). NaN maps to the NaN code. Returns 1 for NaN,
+ * 0 otherwise.
+ */
+int oracle_e4m3_round(double v, uint8_t *out)
+{
+    uint8_t sign = signbit(v) ? 0x80u : 0u;
+    double a = fabs(v);
+    if (isnan(v)) { *out = (uint8_t)(sign | 0x7fu); return 1; }
+    if (a >= 448.0) { *out = (uint8_t)(sign | 0x7eu); return 0; }
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range, quantum 2^-9; q = 8 is the smallest normal,
+         * whose encoding is also 8 (0x08) */
+        double q = rint(ldexp(a, 9));
+        *out = (uint8_t)(sign | (uint8_t)q);
+        return 0;
+    }
+    int e;
+    double m = frexp(a, &e);          /* a = m * 2^e, 0.5 <= m < 1 */
+    double q = rint(ldexp(m, 4));     /* 4 significant bits: 8..16 */
+    if (q == 16.0) { q = 8.0; e += 1; }
+    const int be = e - 1 + 7;
+    /* a < 448 rounds to at most 448 (ties at 464 are not reachable here) */
+    *out = (uint8_t)(sign | (uint8_t)(be << 3) | (uint8_t)((int)q - 8));
+    return 0;
+}
+
 /* ------------------------------------------------------- storage access -- */
 
 static double load_elem(int dtype, const void *p, int64_t i)
@@ -218,6 +278,13 @@ typedef struct {
     void *h_out;        /* storage type (fused: residual_out), may be NULL */
     double *rstd64;     /* may be NULL */
     float *rstd32;      /* may be NULL */
+    /* fp8 output: mode -1 none, 0 per-tensor scale, 1 per-row scale */
+    int fp8_mode;
+    double fp8_scale;   /* per-tensor mode: the given scale */
+    uint8_t *yq;        /* E4M3 codes, may be NULL */
+    double *scaled64;   /* y * s before the E4M3 rounding, may be NULL */
+    double *amax_row;   /* max_j |y_ij| per row, may be NULL */
+    double *scale_inv;  /* 1 / s per row, may be NULL */
     int bad;
 } fwd_job;
 
@@ -225,6 +292,7 @@ static void fwd_rows(fwd_job *jb)
 {
     const int64_t N = jb->N;
     double *h = (double *)malloc((size_t)N * sizeof(double));
+    double *yrow = (double *)malloc((size_t)N * sizeof(double));
     for (int64_t i = jb->row0; i < jb->row1; ++i) {
         const int64_t base = i * N;
         /* h: the row that is normalised */
@@ -239,47 +307,50 @@ static void fwd_rows(fwd_job *jb)
         for (int64_t j = 0; j < N; ++j) ss += h[j] * h[j];
         const double ms = ss / (double)N;
         const double rstd = 1.0 / sqrt(ms + jb->eps);
+        double amax = 0.0;
         for (int64_t j = 0; j < N; ++j) {
             const double factor = jb->w ? jb->offset + load_elem(jb->wdtype, jb->w, j) : 1.0;
             const double yj = h[j] * rstd * factor;
+            yrow[j] = yj;
+            if (fabs(yj) > amax) amax = fabs(yj);
             if (jb->y64) jb->y64[base + j] = yj;
             if (jb->y) jb->bad |= store_elem(jb->dtype, jb->y, base + j, yj);
             if (jb->h_out) jb->bad |= store_elem(jb->dtype, jb->h_out, base + j, h[j]);
         }
         if (jb->rstd64) jb->rstd64[i] = rstd;
         if (jb->rstd32) jb->rstd32[i] = (float)rstd;
+        if (jb->fp8_mode >= 0) {
+            double sc = jb->fp8_scale;
+            if (jb->fp8_mode == 1) sc = amax > 0.0 ? 448.0 / amax : 1.0;
+            for (int64_t j = 0; j < N; ++j) {
+                const double v = yrow[j] * sc;
+                if (jb->scaled64) jb->scaled64[base + j] = v;
+                if (jb->yq) jb->bad |= oracle_e4m3_round(v, &jb->yq[base + j]);
+            }
+            if (jb->amax_row) jb->amax_row[i] = amax;
+            if (jb->scale_inv) jb->scale_inv[i] = 1.0 / sc;
+        }
     }
     free(h);
+    free(yrow);
 }
 
 static void *fwd_thread(void *arg) { fwd_rows((fwd_job *)arg); return NULL; }
 
-/*
- * Forward over an M x N row-major block. residual == NULL gives plain
- * RMSNorm; otherwise h = R(x + residual) is normalised and, if h_out is
- * given, stored there (the fused variant's residual_out). Rows are split
- * into contiguous ranges over nthreads threads (rows are independent, so
- * the thread count does not change any result).
- * Returns the number of non-finite or overflowing stores (0 expected).
- */
-int oracle_rmsnorm_fwd(int dtype, int wdtype, int64_t M, int64_t N,
-                       const void *x, const void *residual, const void *w,
-                       double eps, double offset,
-                       void *y, double *y64, void *h_out,
-                       double *rstd64, float *rstd32, int nthreads)
+/* Runs the forward rows of `proto` over nthreads threads in contiguous row
+ * ranges (rows are independent, so the thread count changes no result).
+ * Returns the number of non-finite or overflowing stores. */
+static int run_fwd(const fwd_job *proto, int64_t M, int nthreads)
 {
     if (nthreads < 1) nthreads = 1;
     if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
     fwd_job *jobs = (fwd_job *)calloc((size_t)nthreads, sizeof(fwd_job));
     pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     for (int t = 0; t < nthreads; ++t) {
-        fwd_job *jb = &jobs[t];
-        jb->dtype = dtype; jb->wdtype = wdtype; jb->N = N;
-        jb->row0 = M * t / nthreads; jb->row1 = M * (t + 1) / nthreads;
-        jb->x = x; jb->residual = residual; jb->w = w;
-        jb->eps = eps; jb->offset = offset;
-        jb->y = y; jb->y64 = y64; jb->h_out = h_out;
-        jb->rstd64 = rstd64; jb->rstd32 = rstd32;
+        jobs[t] = *proto;
+        jobs[t].row0 = M * t / nthreads;
+        jobs[t].row1 = M * (t + 1) / nthreads;
+        jobs[t].bad = 0;
     }
     if (nthreads == 1) {
         fwd_rows(&jobs[0]);
@@ -291,6 +362,53 @@ int oracle_rmsnorm_fwd(int dtype, int wdtype, int64_t M, int64_t N,
     for (int t = 0; t < nthreads; ++t) bad += jobs[t].bad;
     free(jobs); free(tid);
     return bad;
+}
+
+/*
+ * Forward over an M x N row-major block. residual == NULL gives plain
+ * RMSNorm; otherwise h = R(x + residual) is normalised and, if h_out is
+ * given, stored there (the fused variant's residual_out).
+ * Returns the number of non-finite or overflowing stores (0 expected).
+ */
+int oracle_rmsnorm_fwd(int dtype, int wdtype, int64_t M, int64_t N,
+                       const void *x, const void *residual, const void *w,
+                       double eps, double offset,
+                       void *y, double *y64, void *h_out,
+                       double *rstd64, float *rstd32, int nthreads)
+{
+    fwd_job jb;
+    memset(&jb, 0, sizeof jb);
+    jb.dtype = dtype; jb.wdtype = wdtype; jb.N = N;
+    jb.x = x; jb.residual = residual; jb.w = w;
+    jb.eps = eps; jb.offset = offset;
+    jb.y = y; jb.y64 = y64; jb.h_out = h_out;
+    jb.rstd64 = rstd64; jb.rstd32 = rstd32;
+    jb.fp8_mode = -1;
+    return run_fwd(&jb, M, nthreads);
+}
+
+/*
+ * Forward with E4M3 output: yq = E4M3(y * s), s the given scale (mode 0)
+ * or 448 / max_j |y_ij| per row (mode 1). y64, scaled64, amax_row,
+ * scale_inv, h_out, rstd64, rstd32 may each be NULL.
+ */
+int oracle_rmsnorm_fwd_fp8(int dtype, int wdtype, int64_t M, int64_t N,
+                           const void *x, const void *residual, const void *w,
+                           double eps, double offset, int mode, double scale,
+                           uint8_t *yq, double *y64, double *scaled64, double *amax_row, double *scale_inv,
+                           void *h_out, double *rstd64, float *rstd32, int nthreads)
+{
+    if (mode != 0 && mode != 1) return -1;
+    fwd_job jb;
+    memset(&jb, 0, sizeof jb);
+    jb.dtype = dtype; jb.wdtype = wdtype; jb.N = N;
+    jb.x = x; jb.residual = residual; jb.w = w;
+    jb.eps = eps; jb.offset = offset;
+    jb.y64 = y64; jb.h_out = h_out;
+    jb.rstd64 = rstd64; jb.rstd32 = rstd32;
+    jb.fp8_mode = mode; jb.fp8_scale = scale;
+    jb.yq = yq; jb.scaled64 = scaled64; jb.amax_row = amax_row; jb.scale_inv = scale_inv;
+    return run_fwd(&jb, M, nthreads);
 }
 
 /* ------------------------------------------------------------ backward -- */
@@ -439,4 +557,18 @@ int oracle_f16_round_array(const double *v, int64_t n, uint16_t *out)
     int bad = 0;
     for (int64_t i = 0; i < n; ++i) bad += oracle_f16_round(v[i], &out[i]);
     return bad;
+}
+
+/* Round an array of doubles to E4M3 codes (for the tests of the rounding rule). */
+int oracle_e4m3_round_array(const double *v, int64_t n, uint8_t *out)
+{
+    int bad = 0;
+    for (int64_t i = 0; i < n; ++i) bad += oracle_e4m3_round(v[i], &out[i]);
+    return bad;
+}
+
+/* Decode an array of E4M3 codes. */
+void oracle_e4m3_decode_array(const uint8_t *b, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(b[i]);
 }

@@ -38,6 +38,15 @@ MUTATIONS = {
     "f16_subnormal_quantum": ("double q = rint(ldexp(a, 24));", "double q = rint(ldexp(a, 23));"),
     "non_affine_keeps_offset": ("load_elem(jb->wdtype, jb->w, j) : 1.0;\n            const double yj",
                                 "load_elem(jb->wdtype, jb->w, j) : jb->offset + 1.0;\n            const double yj"),
+    "e4m3_ties_away": ("double q = rint(ldexp(m, 4));", "double q = round(ldexp(m, 4));"),
+    "e4m3_exponent_bias": ("const int be = e - 1 + 7;", "const int be = e - 1 + 8;"),
+    "e4m3_subnormal_quantum": ("double q = rint(ldexp(a, 9));", "double q = rint(ldexp(a, 8));"),
+    "e4m3_decode_bias": ("ldexp((double)(f + 8), e - 10)", "ldexp((double)(f + 8), e - 11)"),
+    "e4m3_overflow_to_nan": ("if (a >= 448.0) { *out = (uint8_t)(sign | 0x7eu); return 0; }",
+                             "if (a >= 448.0) { *out = (uint8_t)(sign | 0x7fu); return 0; }"),
+    "fp8_row_scale_not_to_448": ("sc = amax > 0.0 ? 448.0 / amax : 1.0;", "sc = amax > 0.0 ? 256.0 / amax : 1.0;"),
+    "fp8_scale_divides": ("const double v = yrow[j] * sc;", "const double v = yrow[j] / sc;"),
+    "fp8_amax_of_h": ("if (fabs(yj) > amax) amax = fabs(yj);", "if (fabs(h[j]) > amax) amax = fabs(h[j]);"),
     "weight_read_as_activation_type": ("wpo[j] = jb->w ? jb->offset + load_elem(jb->wdtype",
                                        "wpo[j] = jb->w ? jb->offset + load_elem(jb->dtype"),
 }

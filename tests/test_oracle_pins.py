@@ -409,3 +409,139 @@ def test_weight_dtype_only_changes_how_w_and_dw_are_stored():
                     dtype="f64", eps=1e-6, offset=1.0)
     assert np.array_equal(ga["dx64"], gb["dx64"]) and np.array_equal(ga["dw64"], gb["dw64"])
     assert ga["dw"].dtype == np.float32 and np.array_equal(ga["dw"], gb["dw64"].astype(np.float32))
+
+
+# ------------------------------------------------------------------ E4M3 --
+# The format (OCP "E4M3FN": bias 7, 3 fraction bits, no infinities, one NaN
+# pattern per sign, largest finite 448) is pinned to torch's float8_e4m3fn,
+# an independent implementation of the same format.
+
+def _torch_e4m3_decode(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn) \
+        .to(torch.float64).numpy()
+
+
+def _torch_e4m3_round(v):
+    # in-range float32-representable values only (torch maps overflow to NaN)
+    return torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_torch_exhaustive():
+    codes = np.arange(256, dtype=np.uint8)
+    a, b = oracle.e4m3_decode(codes), _torch_e4m3_decode(codes)
+    assert np.array_equal(np.isnan(a), np.isnan(b)) and np.isnan(a).sum() == 2
+    assert np.array_equal(a[~np.isnan(a)], b[~np.isnan(b)])
+    assert np.nanmax(a) == 448.0 and a[1] == 2.0 ** -9 and a[8] == 2.0 ** -6
+
+
+def test_e4m3_round_identity_exhaustive():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_round(oracle.e4m3_decode(codes)), codes)
+
+
+def test_e4m3_round_ties_to_even_and_neighbours():
+    lo = np.arange(0, 0x7E, dtype=np.uint8)               # adjacent finite pairs
+    a, b = oracle.e4m3_decode(lo), oracle.e4m3_decode(lo + 1)
+    mid = (a + b) / 2.0
+    even = np.where((lo & 1) == 0, lo, lo + 1).astype(np.uint8)
+    assert np.array_equal(oracle.e4m3_round(mid), even)
+    assert np.array_equal(oracle.e4m3_round(np.nextafter(mid, -np.inf)), lo)
+    assert np.array_equal(oracle.e4m3_round(np.nextafter(mid, np.inf)), (lo + 1).astype(np.uint8))
+    assert np.array_equal(oracle.e4m3_round(-mid), even | 0x80)
+
+
+def test_e4m3_round_saturates_and_keeps_nan():
+    big = np.array([448.0, np.nextafter(448.0, np.inf), 463.9, 464.0, 480.0, 1e6, np.inf])
+    assert np.all(oracle.e4m3_round(big) == 0x7E)
+    assert np.all(oracle.e4m3_round(-big) == 0xFE)
+    assert np.isnan(oracle.e4m3_decode(oracle.e4m3_round(np.array([np.nan])))[0])
+    assert oracle.e4m3_round(np.array([2.0 ** -10]))[0] == 0            # half the smallest quantum, tie to 0
+    assert oracle.e4m3_round(np.array([3 * 2.0 ** -10]))[0] == 2        # 1.5 quanta, tie to even (2)
+
+
+def test_e4m3_round_matches_torch_on_float32_values():
+    rng = np.random.default_rng(21)
+    v = np.concatenate([rng.uniform(-447.0, 447.0, 200_000), rng.standard_normal(200_000) * 0.02,
+                        rng.standard_normal(50_000) * 2.0 ** -8])
+    v = v.astype(np.float32).astype(np.float64)
+    assert np.array_equal(oracle.e4m3_round(v), _torch_e4m3_round(v))
+
+
+# ------------------------------------------------------- fp8 forward --
+
+def _quant_check(r, scale_of_row):
+    """Codes of the fp8 forward against torch's E4M3 rounding of y * s.
+    y * s can land exactly on a midpoint between two codes (bf16 inputs have
+    few significant bits), and then the last bit of the double arithmetic
+    decides; there either neighbour is accepted."""
+    s = scale_of_row[:, None]
+    v = r["y64"] * s
+    inside = np.abs(v) < 447.0
+    got, ref = r["yq"][inside], _torch_e4m3_round(v[inside])
+    diff = got != ref
+    if diff.any():
+        g, f = got[diff].astype(np.int32), ref[diff].astype(np.int32)
+        assert np.all((g >> 7) == (f >> 7)) and np.all(np.abs(g - f) == 1), "codes not adjacent"
+        a, b = oracle.e4m3_decode(got[diff]), oracle.e4m3_decode(ref[diff])
+        vv = v[inside][diff]
+        assert np.all(np.abs(vv - (a + b) / 2.0) <= 1e-12 * np.abs(vv)), "not a tie"
+        assert diff.sum() <= max(2, got.size // 500)
+    assert np.all((r["yq"][~inside] & 0x7F) >= 0x7D)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+def test_fp8_tensor_scaling_is_fwd_times_scale_rounded(dt):
+    d = inputs.make_inputs(24, 160, dt, 61, outlier_frac=0.02)
+    base = oracle.fwd(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0)
+    for scale in (1.0, 37.5, 0.125):
+        r = oracle.fwd_fp8(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0, scaling="tensor", scale=scale)
+        assert np.array_equal(r["y64"], base["y64"]) and np.array_equal(r["rstd32"], base["rstd32"])
+        _quant_check(r, np.full(24, scale))
+        assert r["amax"] == np.abs(base["y64"]).max()
+        assert np.all(r["scale_inv"] == 1.0 / scale)
+        # dequantised values are within half an E4M3 step of y
+        deq = oracle.e4m3_decode(r["yq"]) / scale
+        y = base["y64"]
+        ok = np.abs(deq - y) <= 2.0 ** -4 * np.abs(y) + 2.0 ** -10 / scale
+        sat = np.abs(y * scale) >= 448.0
+        assert np.all(ok | sat)
+
+
+def test_fp8_tensor_scaling_saturates():
+    d = inputs.make_inputs(8, 64, "bf16", 62)
+    r = oracle.fwd_fp8(d["x"], d["w"], dtype="bf16", eps=1e-6, offset=0.0, scaling="tensor", scale=1000.0)
+    big = np.abs(r["y64"] * 1000.0) >= 448.0
+    assert big.any() and np.all((r["yq"][big] & 0x7F) == 0x7E)
+    assert np.array_equal(r["yq"][big] >> 7, (r["y64"][big] < 0).astype(np.uint8))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_fp8_row_scaling_uses_each_rows_maximum(dt):
+    d = inputs.make_inputs(32, 256, dt, 63, outlier_frac=0.02)
+    base = oracle.fwd(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0)
+    r = oracle.fwd_fp8(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0, scaling="row")
+    amax = np.abs(base["y64"]).max(axis=1)
+    assert np.array_equal(r["amax_row"], amax)
+    assert np.allclose(r["scale_inv"] * 448.0, amax, rtol=1e-15, atol=0)
+    _quant_check(r, 448.0 / amax)
+    # the largest element of every row maps to the largest finite code
+    assert np.all((r["yq"] & 0x7F).max(axis=1) == 0x7E)
+
+
+def test_fp8_row_scaling_zero_row():
+    x = np.zeros((2, 16), dtype=np.float32)
+    x[1] = np.arange(16) - 7.5
+    w = np.ones(16, dtype=np.float32)
+    r = oracle.fwd_fp8(x, w, dtype="f32", eps=1e-6, offset=0.0, scaling="row")
+    assert np.all(r["yq"][0] == 0) and r["scale_inv"][0] == 1.0 and r["amax_row"][0] == 0.0
+    assert r["scale_inv"][1] > 0 and (r["yq"][1] & 0x7F).max() == 0x7E
+
+
+def test_fp8_fused_add_quantises_the_fused_forward():
+    d = inputs.make_inputs(16, 128, "bf16", 64, residual=True, w_mode="gemma")
+    base = oracle.fwd(d["x"], d["w"], dtype="bf16", eps=1e-6, offset=1.0, residual=d["residual"])
+    r = oracle.fwd_fp8(d["x"], d["w"], dtype="bf16", eps=1e-6, offset=1.0, residual=d["residual"],
+                       scaling="row")
+    assert np.array_equal(r["h"], base["h"]) and np.array_equal(r["y64"], base["y64"])
+    _quant_check(r, 448.0 / np.abs(base["y64"]).max(axis=1))
