@@ -272,6 +272,10 @@ def sweep_points():
     # fp32 weight and dW beside 16-bit activations
     pts.append(("w32 bf16 16384x8192", "bf16", 16384, 8192, False, False))
     pts.append(("w32 f16 4096x8192", "f16", 4096, 8192, False, False))
+    # E4M3 output of the forward (forward only)
+    pts.append(("fp8row bf16 16384x8192", "bf16", 16384, 8192, False, False))
+    pts.append(("fp8tensor bf16 16384x8192", "bf16", 16384, 8192, False, False))
+    pts.append(("fp8row bf16 4096x4096", "bf16", 4096, 4096, False, False))
     pts.append(("misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
     pts.append(("misaligned f32 4096x2048", "f32", 4096, 2048, False, True))
     pts.append(("wide f32 16384x6144", "f32", 16384, 6144, False, False))
@@ -345,7 +349,19 @@ def run_sweep(args):
         wb = 1 if affine else 0   # the weight, dW and the workspace exist only with a weight
         by = {"fwd": (2 + 2 * k) * M * N * s + wb * N * sw + 4 * M,
               "bwd": (3 + k) * M * N * s + wb * (2 * N * sw + 8 * P * N) + 4 * M}
-        for op, fn, plan in (("fwd", fwd, fplan), ("bwd", bwd, bplan)):
+        ops = (("fwd", fwd, fplan), ("bwd", bwd, bplan))
+        if label.startswith("fp8"):
+            # reads x and w, writes one byte per element, rstd and (per row) 1/s
+            row = label.startswith("fp8row")
+            sc = None if row else torch.tensor([2.0], dtype=torch.float32, device=dev)
+            yq = torch.empty((M, N), dtype=torch.uint8, device=dev)
+            sinv = torch.empty(M if row else 1, dtype=torch.float32, device=dev)
+            fwd = lambda: rn.rmsnorm_fwd_fp8(x, w, scaling="row" if row else "tensor", scale=sc, y=yq,  # noqa: E731
+                                             rstd=rstd, scale_inv=sinv)
+            fplan = fwd()["plan"]
+            by["fwd"] = M * N * s + N * s + M * N + 4 * M + (4 * M if row else 0)
+            ops = (("fwd", fwd, fplan),)
+        for op, fn, plan in ops:
             for _ in range(3):
                 fn()
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

@@ -149,6 +149,43 @@ rmsnorm_status_t rmsnorm_add_bwd(const void *dy, const void *dresidual_out, cons
                                  int64_t M, int64_t N, rmsnorm_dtype_t dt,
                                  float eps, float offset, rmsnorm_stream_t stream);
 
+/* Scaling of the E4M3 output of rmsnorm_fwd_fp8. */
+typedef enum {
+    RMSNORM_FP8_TENSOR = 0, /* one given scale for the whole tensor */
+    RMSNORM_FP8_ROW = 1     /* each row scaled by 448 / max_j |y_ij| */
+} rmsnorm_fp8_scaling_t;
+
+/*
+ * Forward with an fp8 E4M3 output, the quantised output of a norm that
+ * feeds an fp8 GEMM (the TransformerEngine tuning page, "[ROCm] RMSNorm
+ * tuning", Description and review: the norm kernel key's output type
+ * kFloat8E4M3, beside the input, weight and compute types).
+ * y [M,N] holds one E4M3 byte per element: y_ij = E4M3(y'_ij * s), where y'
+ * is the fp32 forward value (as rmsnorm_fwd computes it, not rounded to the
+ * input type), the product is rounded to fp32, and E4M3() rounds to
+ * nearest-even, saturating to +-448. rstd [M] as in rmsnorm_fwd.
+ *   RMSNORM_FP8_TENSOR: s = *scale (a device pointer to one fp32, required);
+ *     scale_inv (optional, one fp32) receives 1/s.
+ *   RMSNORM_FP8_ROW: scale must be NULL; a_i = max_j |y'_ij| (fp32),
+ *     s_i = 448 / a_i (1 when a_i == 0); scale_inv [M] (required) receives
+ *     a_i / 448 (1 when a_i == 0), so y'_ij ~ decode(y_ij) * scale_inv_i.
+ *   amax (optional, one fp32, either scaling) receives max_ij |y'_ij| over
+ *     this call (set to 0 first, then combined with an atomic maximum; 0
+ *     when M == 0).
+ * residual / residual_out: both NULL (plain) or both set (fused add, as in
+ * rmsnorm_add_fwd). w may be NULL (non-affine). dt is fp32, bf16 or fp16
+ * with the weight in the same type (RMSNORM_WEIGHT_F32 is UNSUPPORTED
+ * here). y needs no alignment beyond 1 byte; 16-byte alignment of x, w, y
+ * (and the residual buffers) with N * sizeof(elem) % 16 == 0 selects the
+ * vectorised kernels. With M == 0 nothing but amax is written. All
+ * pointers are device pointers; argument errors as for rmsnorm_fwd.
+ */
+rmsnorm_status_t rmsnorm_fwd_fp8(const void *x, const void *residual, const void *w, void *y,
+                                 void *residual_out, float *rstd, rmsnorm_fp8_scaling_t scaling,
+                                 const float *scale, float *scale_inv, float *amax,
+                                 int64_t M, int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
+                                 rmsnorm_stream_t stream);
+
 /*
  * Backward without any allocation, for callers that cannot allocate device
  * memory when they call (an engine that reserves all device memory at
@@ -233,6 +270,17 @@ int rmsnorm_plan_count(void);
 
 /* Plan id of table entry `index` (0 <= index < rmsnorm_plan_count()), or -1. */
 int rmsnorm_plan_id_at(int index);
+
+/*
+ * rmsnorm_fwd_fp8 with a forced plan (force_plan < 0: default; the E4M3
+ * kernels exist for the default plans and the generic one, other ids give
+ * UNSUPPORTED). Reports the plan that ran in *plan_used (may be NULL).
+ */
+rmsnorm_status_t rmsnorm_fwd_fp8_ex(const void *x, const void *residual, const void *w, void *y,
+                                    void *residual_out, float *rstd, rmsnorm_fp8_scaling_t scaling,
+                                    const float *scale, float *scale_inv, float *amax,
+                                    int64_t M, int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
+                                    rmsnorm_stream_t stream, int force_plan, rmsnorm_plan_t *plan_used);
 
 /*
  * Forward with a forced plan (force_plan < 0: default). residual and

@@ -6,6 +6,7 @@ beside 16-bit activations) and launch on the current stream:
 
   rmsnorm_fwd(x, w)                       -> y, rstd
   rmsnorm_add_fwd(x, residual, w)         -> y, residual_out, rstd
+  rmsnorm_fwd_fp8(x, w, scaling=...)      -> E4M3 y, rstd, scale_inv, amax
   rmsnorm_bwd(dy, x, w, rstd)             -> dx, dw
   rmsnorm_add_bwd(dy, dres, h, w, rstd)   -> dx (= dresidual), dw
   rmsnorm_bwd_workspace_bytes(M, N, dt)
@@ -34,4 +35,5 @@ from ._binding import (  # noqa: F401
     rmsnorm_bwd_workspace_bytes,
     rmsnorm_fwd,
     rmsnorm_fwd_ex,
+    rmsnorm_fwd_fp8,
 )

@@ -72,6 +72,9 @@ SIGNATURES = {
     "rmsnorm_plan_query": (_i, [_i, _i64, _i64, _i, _i, _i, _i, _i, _i, _PPlan]),
     "rmsnorm_plan_count": (_i, []),
     "rmsnorm_plan_id_at": (_i, [_i]),
+    "rmsnorm_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp]),
+    "rmsnorm_fwd_fp8_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp,
+                                _i, _PPlan]),
     "rmsnorm_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp, _i, _PPlan]),
     "rmsnorm_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i, _f, _f, _vp,
                             _i, _i, _i, _i, _vp, _PPlan]),
@@ -205,6 +208,61 @@ def rmsnorm_add_fwd(x, residual, w, *, eps: float = 1e-6, offset: float = 0.0, y
                                _stream_handle(stream, x.device))
     _raise(st, "rmsnorm_add_fwd")
     return y, residual_out, rstd
+
+
+FP8_SCALING = {"tensor": 0, "row": 1}
+
+
+def rmsnorm_fwd_fp8(x, w, *, scaling="row", scale=None, residual=None, eps: float = 1e-6, offset: float = 0.0,
+                    y=None, residual_out=None, rstd=None, scale_inv=None, amax=False, force_plan=-1,
+                    stream=None):
+    """RMSNorm forward with an E4M3 output: y = E4M3(y' * s), y' the fp32 forward.
+
+    scaling "row": s_i = 448 / max_j |y'_ij|; "tensor": s = scale (a CUDA
+    fp32 tensor of one element). Returns a dict with ``y`` (torch.uint8
+    codes, view as torch.float8_e4m3fn to compute), ``residual_out`` (fused
+    only), ``rstd``, ``scale_inv`` (per row, or one value) and ``amax`` (one
+    fp32, when requested), plus ``plan``.
+    """
+    M, N = _rows(x)
+    _check(x, "x")
+    if w is not None:
+        _check_w(w, "w", x, N)
+        if w.dtype != x.dtype:
+            raise ValueError("the E4M3 forward takes the weight in the activations' type")
+    mode = FP8_SCALING[scaling]
+    if mode == 0:
+        if scale is None:
+            raise ValueError("per-tensor scaling needs `scale`")
+        _check(scale, "scale", numel=1)
+        if scale.dtype != torch.float32:
+            raise ValueError("scale must be float32")
+    elif scale is not None:
+        raise ValueError("per-row scaling derives its scales; pass no `scale`")
+    y = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if y is None else y
+    _check(y, "y", numel=x.numel())
+    if y.element_size() != 1:
+        raise ValueError("y must have one-byte elements")
+    if residual is not None:
+        _check(residual, "residual", like=x, numel=x.numel())
+        residual_out = torch.empty_like(x) if residual_out is None else residual_out
+        _check(residual_out, "residual_out", like=x, numel=x.numel())
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
+    _check(rstd, "rstd", numel=M)
+    if scale_inv is None:
+        scale_inv = torch.empty(x.shape[:-1] if mode == 1 else (1,), dtype=torch.float32, device=x.device)
+    _check(scale_inv, "scale_inv", numel=M if mode == 1 else 1)
+    amax_t = torch.empty(1, dtype=torch.float32, device=x.device) if amax is True else (amax or None)
+    if amax_t is not None:
+        _check(amax_t, "amax", numel=1)
+    p = Plan()
+    st = lib().rmsnorm_fwd_fp8_ex(x.data_ptr(), _ptr(residual), _ptr(w), y.data_ptr(), _ptr(residual_out),
+                                  rstd.data_ptr(), mode, _ptr(scale), scale_inv.data_ptr(), _ptr(amax_t), M, N,
+                                  _dtype_code(x), eps, offset, _stream_handle(stream, x.device), force_plan,
+                                  ctypes.byref(p))
+    _raise(st, "rmsnorm_fwd_fp8")
+    return {"y": y, "residual_out": residual_out, "rstd": rstd, "scale_inv": scale_inv, "amax": amax_t,
+            "plan": p.as_dict()}
 
 
 def rmsnorm_bwd(dy, x, w, rstd, *, eps: float = 1e-6, offset: float = 0.0, dx=None, dw=None, workspace=None,

@@ -367,21 +367,48 @@ static const bool g_loaded_check = [] {
 
 // --------------------------------------------------------------- forward --
 
+// Quantised output of the forward (E4M3); qmode QOUT_NONE is the plain
+// forward and ignores the other three.
+struct QuantOut {
+    int qmode;
+    const float *scale;
+    float *scale_inv;
+    float *amax;
+};
+
 static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void *w, void *y,
                                  void *residual_out, float *rstd, int64_t M, int64_t N, int dt, float eps,
-                                 float offset, cudaStream_t stream, int force_plan, rmsnorm_plan_t *used) {
+                                 float offset, cudaStream_t stream, int force_plan, rmsnorm_plan_t *used,
+                                 const QuantOut &q = QuantOut{QOUT_NONE, nullptr, nullptr, nullptr}) {
     if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
     if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
+    const bool quant = q.qmode != QOUT_NONE;
+    if (quant) {
+        // E4M3 output: the weight in the activations' type only
+        if (mixed_kind(kind_of(dt))) return RMSNORM_ERR_UNSUPPORTED;
+        if (q.qmode == QOUT_FP8_TENSOR && (!q.scale || !aligned_to(q.scale, 4))) return RMSNORM_ERR_INVALID_ARG;
+        if (q.qmode == QOUT_FP8_ROW && (q.scale || (M > 0 && !q.scale_inv))) return RMSNORM_ERR_INVALID_ARG;
+        if ((q.scale_inv && !aligned_to(q.scale_inv, 4)) || (q.amax && !aligned_to(q.amax, 4)))
+            return RMSNORM_ERR_INVALID_ARG;
+    }
+    // The max over this call's rows starts from 0 (also the empty max).
+    auto clear_amax = [&]() -> cudaError_t {
+        return (quant && q.amax) ? cudaMemsetAsync(q.amax, 0, sizeof(float), stream) : cudaSuccess;
+    };
     // An empty batch reads and writes nothing; its (empty) tensors may be NULL.
-    if (M == 0) return RMSNORM_SUCCESS;
+    if (M == 0) {
+        cudaError_t e = clear_amax();
+        return e == cudaSuccess ? RMSNORM_SUCCESS : cuda_fail(e);
+    }
     const bool fused = residual != nullptr || residual_out != nullptr;
     if (fused && (!residual || !residual_out)) return RMSNORM_ERR_INVALID_ARG;
     if (!x || !y || !rstd) return RMSNORM_ERR_INVALID_ARG;  // w NULL: non-affine
     const uintptr_t s = (uintptr_t)elem_size(dt);
     const uintptr_t ws_ = (uintptr_t)weight_size(dt);
-    if (!aligned_to(x, s) || (w && !aligned_to(w, ws_)) || !aligned_to(y, s) || !aligned_to(rstd, 4))
+    const uintptr_t ys = quant ? 1 : s;
+    if (!aligned_to(x, s) || (w && !aligned_to(w, ws_)) || !aligned_to(y, ys) || !aligned_to(rstd, 4))
         return RMSNORM_ERR_INVALID_ARG;
     if (fused && (!aligned_to(residual, s) || !aligned_to(residual_out, s))) return RMSNORM_ERR_INVALID_ARG;
 
@@ -391,6 +418,9 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     rmsnorm_plan_t plan;
     rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, 1, 0, force_plan, 0, &plan);
     if (st != RMSNORM_SUCCESS) return st;
+    // the E4M3 kernels are compiled for the default plans and the generic one
+    if (quant && force_plan >= 0 && plan.path == PATH_VECTOR && find_plan(plan.plan_id)->cmin == 0)
+        return RMSNORM_ERR_UNSUPPORTED;
 
     FwdParams p;
     p.x = x;
@@ -403,7 +433,21 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     p.N = (int)N;
     p.eps = eps;
     p.offset = offset;
-    const int le = launch_fwd_dt(dt, plan.plan_id, fused, p, plan.ctas, stream);
+    p.qscale = q.scale;
+    p.qscale_inv = q.scale_inv;
+    p.qamax = reinterpret_cast<unsigned int *>(q.amax);
+    int le;
+    if (quant) {
+        cudaError_t e = clear_amax();
+        if (e != cudaSuccess) return cuda_fail(e);
+        switch (base_dtype(dt)) {
+        case RMSNORM_BF16: le = launch_fwd8_bf16(plan.plan_id, fused, q.qmode, p, plan.ctas, stream); break;
+        case RMSNORM_F16: le = launch_fwd8_f16(plan.plan_id, fused, q.qmode, p, plan.ctas, stream); break;
+        default: le = launch_fwd8_f32(plan.plan_id, fused, q.qmode, p, plan.ctas, stream); break;
+        }
+    } else {
+        le = launch_fwd_dt(dt, plan.plan_id, fused, p, plan.ctas, stream);
+    }
     if (le != 0) return cuda_fail((cudaError_t)le);
     if (used) *used = plan;
     return RMSNORM_SUCCESS;
@@ -523,6 +567,31 @@ rmsnorm_status_t rmsnorm_add_fwd(const void *x, const void *residual, const void
     if (!residual || !residual_out) return RMSNORM_ERR_INVALID_ARG;
     return fwd_impl(x, residual, w, y, residual_out, rstd, M, N, dt, eps, offset, (cudaStream_t)stream, -1,
                     nullptr);
+}
+
+rmsnorm_status_t rmsnorm_fwd_fp8(const void *x, const void *residual, const void *w, void *y, void *residual_out,
+                                 float *rstd, rmsnorm_fp8_scaling_t scaling, const float *scale, float *scale_inv,
+                                 float *amax, int64_t M, int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
+                                 rmsnorm_stream_t stream) {
+    int mode;
+    if (scaling == RMSNORM_FP8_TENSOR) mode = QOUT_FP8_TENSOR;
+    else if (scaling == RMSNORM_FP8_ROW) mode = QOUT_FP8_ROW;
+    else return RMSNORM_ERR_INVALID_ARG;
+    return fwd_impl(x, residual, w, y, residual_out, rstd, M, N, dt, eps, offset, (cudaStream_t)stream, -1,
+                    nullptr, QuantOut{mode, scale, scale_inv, amax});
+}
+
+rmsnorm_status_t rmsnorm_fwd_fp8_ex(const void *x, const void *residual, const void *w, void *y,
+                                    void *residual_out, float *rstd, rmsnorm_fp8_scaling_t scaling,
+                                    const float *scale, float *scale_inv, float *amax, int64_t M, int64_t N,
+                                    rmsnorm_dtype_t dt, float eps, float offset, rmsnorm_stream_t stream,
+                                    int force_plan, rmsnorm_plan_t *plan_used) {
+    int mode;
+    if (scaling == RMSNORM_FP8_TENSOR) mode = QOUT_FP8_TENSOR;
+    else if (scaling == RMSNORM_FP8_ROW) mode = QOUT_FP8_ROW;
+    else return RMSNORM_ERR_INVALID_ARG;
+    return fwd_impl(x, residual, w, y, residual_out, rstd, M, N, dt, eps, offset, (cudaStream_t)stream,
+                    force_plan, plan_used, QuantOut{mode, scale, scale_inv, amax});
 }
 
 rmsnorm_status_t rmsnorm_fwd_ex(const void *x, const void *residual, const void *w, void *y,

@@ -5,6 +5,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -185,11 +186,21 @@ template <> struct Pair<false> {
 };
 
 // --------------------------------------------------------- team reduce --
-// Sum of the S slots red[0..S) (S a power of two), computed by every warp:
-// lane i starts from red[i mod S] (S <= 32) or from red[i] + red[i+32] + ...
-// (S > 32), then a butterfly over min(S, 32) lanes. Every lane of every warp
-// ends with the same bits (same values, same association).
-template <int S>
+// The combining operation of a reduction: fp32 addition (row sums) or the
+// maximum (a row's largest magnitude, for a quantised output's scale).
+struct OpAdd {
+    static __device__ __forceinline__ float f(float a, float b) { return __fadd_rn(a, b); }
+};
+struct OpMax {
+    static __device__ __forceinline__ float f(float a, float b) { return fmaxf(a, b); }
+};
+
+// Combination of the S slots red[0..S) (S a power of two), computed by
+// every warp: lane i starts from red[i mod S] (S <= 32) or from
+// red[i] + red[i+32] + ... (S > 32), then a butterfly over min(S, 32)
+// lanes. Every lane of every warp ends with the same bits (same values,
+// same association).
+template <int S, class Op = OpAdd>
 __device__ __forceinline__ float sum_slots(const float *red, int lane) {
     static_assert((S & (S - 1)) == 0, "slot count must be a power of two");
     float s;
@@ -198,11 +209,11 @@ __device__ __forceinline__ float sum_slots(const float *red, int lane) {
     } else {
         s = red[lane];
 #pragma unroll
-        for (int j = 1; j < S / 32; ++j) s = __fadd_rn(s, red[lane + 32 * j]);
+        for (int j = 1; j < S / 32; ++j) s = Op::f(s, red[lane + 32 * j]);
     }
     constexpr int WIDTH = S < 32 ? S : 32;
 #pragma unroll
-    for (int o = WIDTH / 2; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+    for (int o = WIDTH / 2; o > 0; o >>= 1) s = Op::f(s, __shfl_xor_sync(0xffffffffu, s, o));
     return s;
 }
 
@@ -213,30 +224,31 @@ __device__ __forceinline__ float sum_slots(const float *red, int lane) {
 // warp combines the W slots with a second butterfly (sum_slots). The
 // barrier is CTA-wide, so every thread of the CTA must call this the same
 // number of times.
-template <int TPR>
+template <int TPR, class Op = OpAdd>
 __device__ __forceinline__ float team_allreduce(float v, float *red, int t) {
     constexpr int WIDTH = TPR < 32 ? TPR : 32;
 #pragma unroll
-    for (int o = WIDTH / 2; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = WIDTH / 2; o > 0; o >>= 1) v = Op::f(v, __shfl_xor_sync(0xffffffffu, v, o));
     if constexpr (TPR > 32) {
         constexpr int W = TPR / 32;
         if ((t & 31) == 0) red[t >> 5] = v;
         __syncthreads();
-        v = sum_slots<W>(red, t & 31);
+        v = sum_slots<W, Op>(red, t & 31);
     }
     return v;
 }
 
 // CTA-wide sum for the generic kernels (blockDim.x a multiple of 32, at most
 // 1024). Same ordering rules as team_allreduce; `red` holds 32 floats.
+template <class Op = OpAdd>
 __device__ __forceinline__ float cta_allreduce(float v, float *red) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = 16; o > 0; o >>= 1) v = Op::f(v, __shfl_xor_sync(0xffffffffu, v, o));
     const int W = blockDim.x >> 5;
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
     float s = red[0];
-    for (int i = 1; i < W; ++i) s = __fadd_rn(s, red[i]);
+    for (int i = 1; i < W; ++i) s = Op::f(s, red[i]);
     __syncthreads();  // red is reused by the next call
     return s;
 }
@@ -333,12 +345,12 @@ __device__ __forceinline__ void st_async_cluster(float *local_slot, uint64_t *lo
 //  end:   barrier wait; every warp combines the CS * W slots (sum_slots),
 //         so every thread of the cluster obtains the same bits.
 // `red` holds CS * W floats; callers alternate buffers between rows.
-template <int TPR, int CS>
+template <int TPR, int CS, class Op = OpAdd>
 __device__ __forceinline__ void cluster_allreduce_begin(float v, float *red, int t, uint32_t rank) {
     static_assert(TPR >= 32, "cluster rows need whole warps");
     constexpr int W = TPR / 32;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = 16; o > 0; o >>= 1) v = Op::f(v, __shfl_xor_sync(0xffffffffu, v, o));
     if ((t & 31) == 0) {
 #pragma unroll
         for (int c = 0; c < CS; ++c) st_cluster(&red[rank * W + (t >> 5)], (uint32_t)c, v);
@@ -346,16 +358,28 @@ __device__ __forceinline__ void cluster_allreduce_begin(float v, float *red, int
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
-template <int TPR, int CS>
+template <int TPR, int CS, class Op = OpAdd>
 __device__ __forceinline__ float cluster_allreduce_end(const float *red, int t) {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    return sum_slots<CS *(TPR / 32)>(red, t & 31);
+    return sum_slots<CS *(TPR / 32), Op>(red, t & 31);
 }
 
-template <int TPR, int CS>
+template <int TPR, int CS, class Op = OpAdd>
 __device__ __forceinline__ float cluster_allreduce(float v, float *red, int t, uint32_t rank) {
-    cluster_allreduce_begin<TPR, CS>(v, red, t, rank);
-    return cluster_allreduce_end<TPR, CS>(red, t);
+    cluster_allreduce_begin<TPR, CS, Op>(v, red, t, rank);
+    return cluster_allreduce_end<TPR, CS, Op>(red, t);
+}
+
+// ------------------------------------------------------------ E4M3 out --
+// Two fp32 values to two E4M3 codes (nearest-even, saturating to +-448):
+// a.x in the low byte. Four values packed into 32 bits, lowest first.
+__device__ __forceinline__ uint32_t e4m3x4(float2 a, float2 b) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+__device__ __forceinline__ uint8_t e4m3x1(float v) {
+    return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
 }
 
 }  // namespace rmsn

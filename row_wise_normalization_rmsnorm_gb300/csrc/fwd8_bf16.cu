@@ -1,0 +1,8 @@
+// fwd8_bf16.cu -- forward kernels with E4M3 output for bf16 activations.
+#include "fwd_kernels.cuh"
+
+namespace rmsn {
+int launch_fwd8_bf16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream) {
+    return launch_q<__nv_bfloat16>(plan_id, fused, mode, p, grid, stream);
+}
+}  // namespace rmsn

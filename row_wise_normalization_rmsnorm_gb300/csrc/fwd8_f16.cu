@@ -1,0 +1,8 @@
+// fwd8_f16.cu -- forward kernels with E4M3 output for fp16 activations.
+#include "fwd_kernels.cuh"
+
+namespace rmsn {
+int launch_fwd8_f16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream) {
+    return launch_q<__half>(plan_id, fused, mode, p, grid, stream);
+}
+}  // namespace rmsn

@@ -24,7 +24,11 @@ namespace rmsn {
 // CS > 1: the CTAs of a cluster share one row; CTA rank r holds chunks
 // [r TPR V, (r+1) TPR V) and the sum of squares meets in distributed shared
 // memory (wide rows whose chunks exceed one CTA's registers).
-template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED>
+//
+// Q selects the output: QOUT_NONE stores y in T; the E4M3 modes store
+// E4M3(y * s), one byte per element, with s the given per-tensor scale or
+// 448 / max|y| of the row (a second, max-combining row reduction).
+template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED, int Q = QOUT_NONE>
 __global__ void __launch_bounds__(TPR *TEAMS)
     rmsnorm_fwd_vector(const FwdParams p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
@@ -32,6 +36,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     constexpr int NP = Elem<T>::NP;
     constexpr int W = TPR > 32 ? TPR / 32 : 1;
     __shared__ float red[TEAMS][W * CS];
+    __shared__ float redm[Q == QOUT_NONE ? 1 : TEAMS][W * CS];  // the max reduction's slots
 
     const int team = threadIdx.x / TPR;
     const int t = threadIdx.x % TPR;
@@ -97,32 +102,88 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     }
     const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(s, (float)p.N), p.eps));
     if (valid && t == 0 && rank == 0) p.rstd[row] = rstd;
-    if (!valid) return;
 
     const float2 r2 = make_float2(rstd, rstd);
     const float2 o2 = make_float2(p.offset, p.offset);
     const bool has_w = p.w != nullptr;  // no weight: non-affine, factor 1
+    if constexpr (Q == QOUT_NONE) {
+        if (!valid) return;
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-        const int c = cbase + v * TPR + t;
-        if (c < C) {
-            float2 a[NP];
-            unpack<T>(xv[v], a);
-            if (has_w) {
-                float2 wv[NP];
+        for (int v = 0; v < V; ++v) {
+            const int c = cbase + v * TPR + t;
+            if (c < C) {
+                float2 a[NP];
+                unpack<T>(xv[v], a);
+                if (has_w) {
+                    float2 wv[NP];
+                    load_w_chunk<T, TW>(p.w, c, wv);
+#pragma unroll
+                    for (int k = 0; k < NP; ++k) a[k] = Pk::mul(Pk::mul(a[k], r2), Pk::add(o2, wv[k]));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < NP; ++k) a[k] = Pk::mul(a[k], r2);
+                }
+                st_chunk(reinterpret_cast<uint4 *>(p.y) + base + c, pack<T>(a));
+            }
+        }
+    } else {
+        // y in fp32, kept in registers until the scale is known
+        float2 yv[V][NP];
+        float m = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = cbase + v * TPR + t;
+            unpack<T>(xv[v], yv[v]);  // zero chunks beyond the row give y = 0
+            float2 wv[NP];
+            if (has_w && c < C) {
                 load_w_chunk<T, TW>(p.w, c, wv);
-#pragma unroll
-                for (int k = 0; k < NP; ++k) a[k] = Pk::mul(Pk::mul(a[k], r2), Pk::add(o2, wv[k]));
             } else {
 #pragma unroll
-                for (int k = 0; k < NP; ++k) a[k] = Pk::mul(a[k], r2);
+                for (int k = 0; k < NP; ++k) wv[k] = make_float2(1.f - p.offset, 1.f - p.offset);
             }
-            st_chunk(reinterpret_cast<uint4 *>(p.y) + base + c, pack<T>(a));
+#pragma unroll
+            for (int k = 0; k < NP; ++k) {
+                yv[v][k] = has_w ? Pk::mul(Pk::mul(yv[v][k], r2), Pk::add(o2, wv[k])) : Pk::mul(yv[v][k], r2);
+                m = fmaxf(m, fmaxf(fabsf(yv[v][k].x), fabsf(yv[v][k].y)));
+            }
+        }
+        float amax = 0.f;
+        if (Q == QOUT_FP8_ROW || p.qamax != nullptr) {  // uniform over the grid
+            if constexpr (CS > 1) {
+                amax = cluster_allreduce<TPR, CS, OpMax>(m, &redm[0][0], t, rank);
+            } else {
+                amax = team_allreduce<TPR, OpMax>(m, &redm[team][0], t);
+            }
+        }
+        if (!valid) return;
+        float sc;
+        if constexpr (Q == QOUT_FP8_ROW) {
+            sc = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+            if (t == 0 && rank == 0) p.qscale_inv[row] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+        } else {
+            sc = __ldg(p.qscale);
+            if (row == 0 && t == 0 && rank == 0 && p.qscale_inv) p.qscale_inv[0] = __fdiv_rn(1.f, sc);
+        }
+        if (p.qamax != nullptr && t == 0 && rank == 0) atomicMax(p.qamax, __float_as_uint(amax));
+        const float2 s2 = make_float2(sc, sc);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = cbase + v * TPR + t;
+            if (c < C) {
+                float2 q[NP];
+#pragma unroll
+                for (int k = 0; k < NP; ++k) q[k] = Pk::mul(yv[v][k], s2);
+                if constexpr (NP == 4) {
+                    __stcs(reinterpret_cast<uint2 *>(p.y) + base + c, make_uint2(e4m3x4(q[0], q[1]), e4m3x4(q[2], q[3])));
+                } else {
+                    __stcs(reinterpret_cast<unsigned int *>(p.y) + base + c, e4m3x4(q[0], q[1]));
+                }
+            }
         }
     }
 }
 
-template <typename T, typename TW, bool FUSED>
+template <typename T, typename TW, bool FUSED, int Q = QOUT_NONE>
 __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
@@ -145,24 +206,45 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     const float s = cta_allreduce(ss, red);
     const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(s, (float)N), p.eps));
     if (threadIdx.x == 0) p.rstd[row] = rstd;
-    for (int j = threadIdx.x; j < N; j += blockDim.x) {
-        // The same thread wrote hout[j] above, so it reads its own value.
+    // The same thread wrote hout[j] above, so it reads its own value.
+    auto y_at = [&](int j) {
         const float h = FUSED ? load_elem(static_cast<const T *>(hout), j) : load_elem(x, j);
         const float hr = __fmul_rn(h, rstd);
-        store_elem(y, j, w ? __fmul_rn(hr, __fadd_rn(p.offset, load_w(w, j))) : hr);
+        return w ? __fmul_rn(hr, __fadd_rn(p.offset, load_w(w, j))) : hr;
+    };
+    if constexpr (Q == QOUT_NONE) {
+        for (int j = threadIdx.x; j < N; j += blockDim.x) store_elem(y, j, y_at(j));
+    } else {
+        float amax = 0.f;
+        if (Q == QOUT_FP8_ROW || p.qamax != nullptr) {
+            float m = 0.f;
+            for (int j = threadIdx.x; j < N; j += blockDim.x) m = fmaxf(m, fabsf(y_at(j)));
+            amax = cta_allreduce<OpMax>(m, red);
+        }
+        float sc;
+        if constexpr (Q == QOUT_FP8_ROW) {
+            sc = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+            if (threadIdx.x == 0) p.qscale_inv[row] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+        } else {
+            sc = __ldg(p.qscale);
+            if (row == 0 && threadIdx.x == 0 && p.qscale_inv) p.qscale_inv[0] = __fdiv_rn(1.f, sc);
+        }
+        if (p.qamax != nullptr && threadIdx.x == 0) atomicMax(p.qamax, __float_as_uint(amax));
+        uint8_t *yq = reinterpret_cast<uint8_t *>(p.y) + row * N;
+        for (int j = threadIdx.x; j < N; j += blockDim.x) yq[j] = e4m3x1(__fmul_rn(y_at(j), sc));
     }
 }
 
 // ------------------------------------------------------------- dispatch --
 
-template <typename T, typename TW, int TPR, int V, int TEAMS, int CS>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, int Q>
 static int launch_vec(bool fused, const FwdParams &p, int grid, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if constexpr (CS == 1) {
         if (fused)
-            rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, 1, true><<<grid, TPR * TEAMS, 0, s>>>(p);
+            rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, 1, true, Q><<<grid, TPR * TEAMS, 0, s>>>(p);
         else
-            rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, 1, false><<<grid, TPR * TEAMS, 0, s>>>(p);
+            rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, 1, false, Q><<<grid, TPR * TEAMS, 0, s>>>(p);
         return (int)cudaGetLastError();
     } else {
         cudaLaunchConfig_t cfg = {};
@@ -176,8 +258,8 @@ static int launch_vec(bool fused, const FwdParams &p, int grid, void *stream) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true>, p)
-                     : (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false>, p);
+        return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true, Q>, p)
+                     : (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false, Q>, p);
     }
 }
 
@@ -187,13 +269,13 @@ static const void *ptr_vec(bool fused) {
                  : (const void *)rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false>;
 }
 
-template <typename T, typename TW>
+template <typename T, typename TW, int Q>
 static int launch_gen(bool fused, const FwdParams &p, int grid, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (fused)
-        rmsnorm_fwd_generic<T, TW, true><<<grid, 256, 0, s>>>(p);
+        rmsnorm_fwd_generic<T, TW, true, Q><<<grid, 256, 0, s>>>(p);
     else
-        rmsnorm_fwd_generic<T, TW, false><<<grid, 256, 0, s>>>(p);
+        rmsnorm_fwd_generic<T, TW, false, Q><<<grid, 256, 0, s>>>(p);
     return (int)cudaGetLastError();
 }
 
@@ -202,36 +284,37 @@ static const void *ptr_gen(bool fused) {
     return fused ? (const void *)rmsnorm_fwd_generic<T, TW, true> : (const void *)rmsnorm_fwd_generic<T, TW, false>;
 }
 
-// A weight type other than the activations' is compiled for the default
-// plans (and the generic one) only; alternatives are for tuning.
-template <typename T, typename TW, int PATH, int CMIN>
+// A weight type other than the activations', and the E4M3 outputs, are
+// compiled for the default plans (and the generic one) only; alternatives
+// are for tuning.
+template <typename T, typename TW, int PATH, int CMIN, int Q>
 constexpr bool instantiated() {
-    return std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0;
+    return (std::is_same<T, TW>::value && Q == QOUT_NONE) || PATH == PATH_GENERIC || CMIN > 0;
 }
 
 // One switch case per table entry; `if constexpr` keeps kernels of other
-// ops, paths and weight types from being instantiated here.
-template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
+// ops, paths, weight types and outputs from being instantiated here.
+template <typename T, typename TW, int Q, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
 static int launch_entry(bool fused, const FwdParams &p, int grid, void *stream) {
-    if constexpr (OP != OP_FWD || !instantiated<T, TW, PATH, CMIN>()) return (int)cudaErrorInvalidValue;
-    else if constexpr (PATH == PATH_GENERIC) return launch_gen<T, TW>(fused, p, grid, stream);
-    else if constexpr (PATH == PATH_VECTOR) return launch_vec<T, TW, TPR, V, TEAMS, CS>(fused, p, grid, stream);
+    if constexpr (OP != OP_FWD || !instantiated<T, TW, PATH, CMIN, Q>()) return (int)cudaErrorInvalidValue;
+    else if constexpr (PATH == PATH_GENERIC) return launch_gen<T, TW, Q>(fused, p, grid, stream);
+    else if constexpr (PATH == PATH_VECTOR) return launch_vec<T, TW, TPR, V, TEAMS, CS, Q>(fused, p, grid, stream);
     else return (int)cudaErrorInvalidValue;
 }
 
 template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
 static const void *ptr_entry(bool fused) {
-    if constexpr (OP != OP_FWD || !instantiated<T, TW, PATH, CMIN>()) return nullptr;
+    if constexpr (OP != OP_FWD || !instantiated<T, TW, PATH, CMIN, QOUT_NONE>()) return nullptr;
     else if constexpr (PATH == PATH_GENERIC) return ptr_gen<T, TW>(fused);
     else if constexpr (PATH == PATH_VECTOR) return ptr_vec<T, TW, TPR, V, TEAMS, CS>(fused);
     else return nullptr;
 }
 
-template <typename T, typename TW>
+template <typename T, typename TW, int Q = QOUT_NONE>
 static int launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
     switch (plan_id) {
 #define RMSN_FWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return launch_entry<T, TW, op, path, tpr, v, teams, cs, cmin>(fused, p, grid, stream);
+    case id: return launch_entry<T, TW, Q, op, path, tpr, v, teams, cs, cmin>(fused, p, grid, stream);
         RMSNORM_PLAN_TABLE(RMSN_FWD_CASE)
 #undef RMSN_FWD_CASE
     default:
@@ -249,6 +332,14 @@ static const void *ptr_t(int plan_id, bool fused) {
     default:
         return nullptr;
     }
+}
+
+// E4M3 output: the mode picks the instantiation.
+template <typename T>
+static int launch_q(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream) {
+    if (mode == QOUT_FP8_TENSOR) return launch_t<T, T, QOUT_FP8_TENSOR>(plan_id, fused, p, grid, stream);
+    if (mode == QOUT_FP8_ROW) return launch_t<T, T, QOUT_FP8_ROW>(plan_id, fused, p, grid, stream);
+    return (int)cudaErrorInvalidValue;
 }
 
 }  // namespace rmsn

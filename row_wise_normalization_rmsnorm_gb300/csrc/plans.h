@@ -101,7 +101,17 @@ struct FwdParams {
     int N;
     float eps;
     float offset;
+    // E4M3 output (y holds one byte per element): the given per-tensor
+    // scale, the reported 1/scale (one value, or one per row) and the
+    // tensor's max |y| as fp32 bits (atomic max; NULL: not reported).
+    const float *qscale;
+    float *qscale_inv;
+    unsigned int *qamax;
 };
+
+// Output of the forward: the activations' type, or E4M3 with a per-tensor
+// scale, or E4M3 with a per-row scale from the row's own max |y|.
+enum { QOUT_NONE = 0, QOUT_FP8_TENSOR = 1, QOUT_FP8_ROW = 2 };
 
 struct BwdParams {
     const void *dy;
@@ -137,6 +147,12 @@ RMSN_DECLARE_LAUNCHERS(f16)
 RMSN_DECLARE_LAUNCHERS(bf16w32)
 RMSN_DECLARE_LAUNCHERS(f16w32)
 #undef RMSN_DECLARE_LAUNCHERS
+
+// Forward with E4M3 output (mode QOUT_FP8_TENSOR or QOUT_FP8_ROW), for
+// fp32, bf16 and fp16 activations with the weight in the same type.
+int launch_fwd8_f32(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
+int launch_fwd8_bf16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
+int launch_fwd8_f16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
 
 // dW finalizers, by dW's storage type.
 int launch_dw_finalize_f32(const float *ws, int parts, int N, void *dw, void *stream, bool serial);

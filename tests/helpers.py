@@ -16,6 +16,12 @@ Tolerances (the RMSNorm definition and bounds are restated in the oracle):
        with ref the unrounded double sum and S = sum_i |dy xhat| (the scale
        of the fp32 summation error).
   rstd relative 2e-6.
+  E4M3 codes: equal (as values) to the oracle's nearest-even rounding of the
+       exact y * s, except where the exact scaled value lies within
+       2^-19 |v| of the midpoint between two adjacent codes: the kernel's
+       fp32 y * s carries a relative error of a few 2^-24 (rstd, the three
+       products, the scale), so there either neighbour is correct.
+       Row scales 1/s and amax: relative 2^-19.
 """
 from __future__ import annotations
 
@@ -134,3 +140,32 @@ def cuda_bits_equal(a: torch.Tensor, b: torch.Tensor) -> bool:
     if a.dtype == torch.bfloat16:
         return torch.equal(a.view(torch.int16), b.view(torch.int16))
     return torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+FP8_TIE_REL = 2.0 ** -19
+
+
+def check_fp8(got_codes: np.ndarray, ref: dict, rows=None):
+    """E4M3 codes of the kernel against the oracle's (see the module
+    docstring); returns the number of elements decided at a near-tie."""
+    want = ref["yq"] if rows is None else ref["yq"][rows]
+    v = ref["scaled64"] if rows is None else ref["scaled64"][rows]
+    g, w = oracle.e4m3_decode(got_codes), oracle.e4m3_decode(want)
+    diff = g != w
+    if not diff.any():
+        return 0
+    gd, wd, vd = g[diff], w[diff], v[diff]
+    gc, wc = got_codes[diff].astype(np.int32), want[diff].astype(np.int32)
+    adjacent = ((gc >> 7) == (wc >> 7)) & (np.abs(gc - wc) == 1)
+    tie = np.abs(vd - (gd + wd) / 2.0) <= FP8_TIE_REL * np.abs(vd)
+    bad = ~(adjacent & tie)
+    assert not bad.any(), (f"E4M3: {bad.sum()} codes off; first scaled value {vd[bad][0]!r}, "
+                           f"kernel {gd[bad][0]!r}, oracle {wd[bad][0]!r}")
+    return int(diff.sum())
+
+
+def check_rel(got, ref, rel, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    assert np.all(err <= rel * np.abs(ref)), f"{what}: worst rel {(err / np.maximum(np.abs(ref), 1e-300)).max()}"

@@ -181,6 +181,16 @@ def test_invalid_arguments_without_gpu(rn):
     assert L.rmsnorm_add_fwd(x, None, x, x, x, r, 4, 8, 1, 1e-6, 0.0, None) == 1
     assert L.rmsnorm_bwd(x, x, x, r, x, None, None, 0, 4, 8, 1, 1e-6, 0.0, None) == 1
     assert L.rmsnorm_bwd(x, x, x, r, x, x, ctypes.c_void_p(264), 1 << 20, 4, 8, 1, 1e-6, 0.0, None) == 3
+    # E4M3 forward: unknown scaling, per-tensor without a scale, per-row
+    # with a given scale or without scale_inv, an fp32 weight (unsupported)
+    f8 = L.rmsnorm_fwd_fp8
+    assert f8(x, None, x, x, None, r, 2, None, r, None, 4, 8, 1, 1e-6, 0.0, None) == 1
+    assert f8(x, None, x, x, None, r, 0, None, r, None, 4, 8, 1, 1e-6, 0.0, None) == 1
+    assert f8(x, None, x, x, None, r, 1, r, r, None, 4, 8, 1, 1e-6, 0.0, None) == 1
+    assert f8(x, None, x, x, None, r, 1, None, None, None, 4, 8, 1, 1e-6, 0.0, None) == 1
+    assert f8(x, None, x, x, None, r, 0, ctypes.c_void_p(514), None, None, 4, 8, 1, 1e-6, 0.0, None) == 1
+    assert f8(x, None, x, x, None, r, 1, None, r, None, 4, 8, 0x101, 1e-6, 0.0, None) == 2
+    assert f8(x, x, x, x, None, r, 1, None, r, None, 4, 8, 1, 1e-6, 0.0, None) == 1   # residual without out
     # M == 0 forward is a no-op that needs no device
     assert L.rmsnorm_fwd(x, x, x, r, 0, 8, 1, 1e-6, 0.0, None) == 0
     assert L.rmsnorm_status_string(3) == b"workspace too small or misaligned"
