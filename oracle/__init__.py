@@ -1,4 +1,4 @@
-"""CPU fp64 oracle for RMSNorm forward and backward.
+"""CPU fp64 oracle for RMSNorm (and LayerNorm) forward and backward.
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU legs of ``bench.py`` (``cpu_baseline`` and ``--impl reference``) may
@@ -13,6 +13,10 @@ add, and the exact gradient dx = rstd (g - xhat c), dW = sum dy xhat, as
 described by the Liger-Kernel page "perf(cutedsl): add Blackwell fast path
 to RMSNorm" (Summary, section 2) and the FlyDSL page "[Perf] Optimize
 RMSNorm backward with staged reduction and vec8 I/O" (Implementation).
+
+The same library holds the E4M3 (fp8) output of the forward (``fwd_fp8``)
+and LayerNorm forward and backward (``ln_fwd``, ``ln_bwd``), defined in the
+C file's header.
 
 Storage types: ``"bf16"`` arrays are numpy ``uint16`` bit patterns,
 ``"f16"`` arrays are ``float16``, ``"f32"`` arrays are ``float32``,
@@ -79,6 +83,12 @@ def _load():
             lib.oracle_e4m3_round_array.argtypes = [vp, i64, vp]
             lib.oracle_e4m3_decode_array.restype = None
             lib.oracle_e4m3_decode_array.argtypes = [vp, i64, vp]
+            lib.oracle_layernorm_fwd.restype = i32
+            lib.oracle_layernorm_fwd.argtypes = [i32, i32, i64, i64, vp, vp, vp, vp, dbl, dbl,
+                                                 vp, vp, vp, vp, vp, vp, vp, i32]
+            lib.oracle_layernorm_bwd.restype = i32
+            lib.oracle_layernorm_bwd.argtypes = [i32, i32, i64, i64, vp, vp, vp, vp, vp, vp, dbl, dbl,
+                                                 vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32]
             lib.oracle_rmsnorm_fwd_fp8.restype = i32
             lib.oracle_rmsnorm_fwd_fp8.argtypes = [i32, i32, i64, i64, vp, vp, vp, dbl, dbl, i32, dbl,
                                                    vp, vp, vp, vp, vp, vp, vp, vp, i32]
@@ -257,3 +267,68 @@ def bwd(dy, h, w, *, dtype, eps, offset, rstd=None, dres=None, want_dx=True, nth
     if bad:
         raise FloatingPointError(f"oracle bwd: {bad} non-finite or overflowing stores")
     return {"dx": dx, "dx64": dx64, "dx_scale": dxs, "dx_cscale": dxc, "dw64": dw64, "dw_abs": dwa, "dw": dw}
+
+
+# ------------------------------------------------------------- LayerNorm --
+
+def ln_fwd(x, gamma, beta, *, dtype, eps, offset, residual=None, nthreads=1, wdtype=None):
+    """LayerNorm forward (y = (h - mean) rstd (offset + gamma) + beta, biased
+    variance, h = x or R(x + residual)); gamma None: factor 1; beta None: no
+    bias. Returns ``y``, ``y64``, ``h`` (fused only), ``mean64``, ``mean32``,
+    ``rstd64``, ``rstd32``."""
+    wdtype = wdtype or dtype
+    x = _as_storage(x, dtype)
+    M, N = x.shape
+    gamma = _as_storage(gamma, wdtype, (N,))
+    beta = _as_storage(beta, wdtype, (N,))
+    residual = _as_storage(residual, dtype, (M, N))
+    st = _NP_STORAGE[dtype]
+    y = np.empty((M, N), dtype=st)
+    y64 = np.empty((M, N), dtype=np.float64)
+    h = np.empty((M, N), dtype=st) if residual is not None else None
+    m64, r64 = np.empty((M,), dtype=np.float64), np.empty((M,), dtype=np.float64)
+    m32, r32 = np.empty((M,), dtype=np.float32), np.empty((M,), dtype=np.float32)
+    bad = _load().oracle_layernorm_fwd(_DTYPE_CODE[dtype], _DTYPE_CODE[wdtype], M, N, _ptr(x), _ptr(residual),
+                                       _ptr(gamma), _ptr(beta), float(eps), float(offset), _ptr(y), _ptr(y64),
+                                       _ptr(h), _ptr(m64), _ptr(m32), _ptr(r64), _ptr(r32), int(nthreads))
+    if bad:
+        raise FloatingPointError(f"oracle ln_fwd: {bad} non-finite or overflowing stores")
+    return {"y": y, "y64": y64, "h": h, "mean64": m64, "mean32": m32, "rstd64": r64, "rstd32": r32}
+
+
+def ln_bwd(dy, h, gamma, *, dtype, eps, offset, mean=None, rstd=None, dres=None, want_dx=True, nthreads=1,
+           wdtype=None):
+    """LayerNorm backward. ``mean``/``rstd`` None: recomputed in double from
+    h; otherwise the forward's float32 values. Returns ``dx``, ``dx64``,
+    ``dx_scale``, ``dx_cscale``, ``dg64``, ``dg_abs``, ``dg`` (dgamma in
+    the weight type), ``db64``, ``db_abs``, ``db`` (dbeta)."""
+    wdtype = wdtype or dtype
+    dy = _as_storage(dy, dtype)
+    M, N = dy.shape
+    h = _as_storage(h, dtype, (M, N))
+    gamma = _as_storage(gamma, wdtype, (N,))
+    dres = _as_storage(dres, dtype, (M, N))
+    if (mean is None) != (rstd is None):
+        raise ValueError("oracle ln_bwd: give both mean and rstd, or neither")
+    if rstd is not None:
+        mean = np.ascontiguousarray(mean, dtype=np.float32)
+        rstd = np.ascontiguousarray(rstd, dtype=np.float32)
+        if mean.size != M or rstd.size != M:
+            raise ValueError("oracle ln_bwd: mean and rstd must have M entries")
+    st = _NP_STORAGE[dtype]
+    dx = np.empty((M, N), dtype=st) if want_dx else None
+    dx64 = np.empty((M, N), dtype=np.float64) if want_dx else None
+    dxs = np.empty((M, N), dtype=np.float64) if want_dx else None
+    dxc = np.empty((M, N), dtype=np.float64) if want_dx else None
+    dg64, dga = np.empty((N,), dtype=np.float64), np.empty((N,), dtype=np.float64)
+    db64, dba = np.empty((N,), dtype=np.float64), np.empty((N,), dtype=np.float64)
+    dg = np.empty((N,), dtype=_NP_STORAGE[wdtype])
+    db = np.empty((N,), dtype=_NP_STORAGE[wdtype])
+    bad = _load().oracle_layernorm_bwd(_DTYPE_CODE[dtype], _DTYPE_CODE[wdtype], M, N, _ptr(dy), _ptr(h),
+                                       _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dres), float(eps), float(offset),
+                                       _ptr(dx), _ptr(dx64), _ptr(dxs), _ptr(dxc), _ptr(dg64), _ptr(dga), _ptr(dg),
+                                       _ptr(db64), _ptr(dba), _ptr(db), int(nthreads))
+    if bad:
+        raise FloatingPointError(f"oracle ln_bwd: {bad} non-finite or overflowing stores")
+    return {"dx": dx, "dx64": dx64, "dx_scale": dxs, "dx_cscale": dxc, "dg64": dg64, "dg_abs": dga, "dg": dg,
+            "db64": db64, "db_abs": dba, "db": db}

@@ -55,6 +55,21 @@
  * The pages give the output type only; the scalings are the two plain
  * readings (a given scale, or one derived from the row's own maximum).
  *
+ * LayerNorm (the sibling norm the TransformerEngine tuning page registers
+ * tuned configs for beside RMSNorm, "[ROCm] RMSNorm tuning", Description),
+ * in the same precision rules, with the standard definition:
+ *   forward   mu    = (1/N) sum_j h_j
+ *             var   = (1/N) sum_j (h_j - mu)^2        (biased, two-pass)
+ *             rstd  = 1 / sqrt(var + eps)
+ *             xhat  = (h_j - mu) * rstd
+ *             y_j   = xhat_j * (offset + gamma_j) + beta_j
+ *   backward  g_j   = dy_j * (offset + gamma_j)
+ *             dx_j  = rstd * (g_j - mean(g) - xhat_j * mean(g xhat)) [+ dres_j]
+ *             dgamma_j = sum_rows dy_j xhat_j,  dbeta_j = sum_rows dy_j
+ * gamma == NULL: factor 1 (no dgamma); beta == NULL: no bias (no dbeta).
+ * The gradient follows from d mu / d h_k = 1/N and
+ * d rstd / d h_k = -rstd^3 (h_k - mu) / N.
+ *
  * Parity pins live in tests/test_oracle_pins.py.
  */
 #include <math.h>
@@ -538,6 +553,233 @@ int oracle_rmsnorm_bwd(int dtype, int wdtype, int64_t M, int64_t N,
         bad += jobs[t].bad;
         free(jobs[t].dw);
         free(jobs[t].dw_abs);
+    }
+    free(jobs); free(tid);
+    return bad;
+}
+
+/* ----------------------------------------------------------- LayerNorm -- */
+
+typedef struct {
+    int dtype, wdtype;
+    int64_t row0, row1, N;
+    const void *x, *residual, *gamma, *beta;
+    double eps, offset;
+    void *y;
+    double *y64;
+    void *h_out;
+    double *mean64, *rstd64;
+    float *mean32, *rstd32;
+    int bad;
+} ln_fwd_job;
+
+static void ln_fwd_rows(ln_fwd_job *jb)
+{
+    const int64_t N = jb->N;
+    double *h = (double *)malloc((size_t)N * sizeof(double));
+    for (int64_t i = jb->row0; i < jb->row1; ++i) {
+        const int64_t base = i * N;
+        for (int64_t j = 0; j < N; ++j) {
+            double xv = load_elem(jb->dtype, jb->x, base + j);
+            if (jb->residual)
+                h[j] = round_to(jb->dtype, xv + load_elem(jb->dtype, jb->residual, base + j));
+            else
+                h[j] = xv;
+        }
+        double sum = 0.0;
+        for (int64_t j = 0; j < N; ++j) sum += h[j];
+        const double mu = sum / (double)N;
+        double sq = 0.0;
+        for (int64_t j = 0; j < N; ++j) sq += (h[j] - mu) * (h[j] - mu);
+        const double var = sq / (double)N;
+        const double rstd = 1.0 / sqrt(var + jb->eps);
+        for (int64_t j = 0; j < N; ++j) {
+            const double factor = jb->gamma ? jb->offset + load_elem(jb->wdtype, jb->gamma, j) : 1.0;
+            const double bias = jb->beta ? load_elem(jb->wdtype, jb->beta, j) : 0.0;
+            const double yj = (h[j] - mu) * rstd * factor + bias;
+            if (jb->y64) jb->y64[base + j] = yj;
+            if (jb->y) jb->bad |= store_elem(jb->dtype, jb->y, base + j, yj);
+            if (jb->h_out) jb->bad |= store_elem(jb->dtype, jb->h_out, base + j, h[j]);
+        }
+        if (jb->mean64) jb->mean64[i] = mu;
+        if (jb->mean32) jb->mean32[i] = (float)mu;
+        if (jb->rstd64) jb->rstd64[i] = rstd;
+        if (jb->rstd32) jb->rstd32[i] = (float)rstd;
+    }
+    free(h);
+}
+
+static void *ln_fwd_thread(void *arg) { ln_fwd_rows((ln_fwd_job *)arg); return NULL; }
+
+/*
+ * LayerNorm forward over an M x N block; residual, h_out, gamma, beta and
+ * every output may be NULL as in oracle_rmsnorm_fwd (gamma NULL: factor 1,
+ * beta NULL: no bias). mean and rstd are reported in double and rounded to
+ * float32. Returns the number of non-finite or overflowing stores.
+ */
+int oracle_layernorm_fwd(int dtype, int wdtype, int64_t M, int64_t N,
+                         const void *x, const void *residual, const void *gamma, const void *beta,
+                         double eps, double offset,
+                         void *y, double *y64, void *h_out,
+                         double *mean64, float *mean32, double *rstd64, float *rstd32, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
+    ln_fwd_job *jobs = (ln_fwd_job *)calloc((size_t)nthreads, sizeof(ln_fwd_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    for (int t = 0; t < nthreads; ++t) {
+        ln_fwd_job *jb = &jobs[t];
+        jb->dtype = dtype; jb->wdtype = wdtype; jb->N = N;
+        jb->row0 = M * t / nthreads; jb->row1 = M * (t + 1) / nthreads;
+        jb->x = x; jb->residual = residual; jb->gamma = gamma; jb->beta = beta;
+        jb->eps = eps; jb->offset = offset;
+        jb->y = y; jb->y64 = y64; jb->h_out = h_out;
+        jb->mean64 = mean64; jb->mean32 = mean32; jb->rstd64 = rstd64; jb->rstd32 = rstd32;
+    }
+    if (nthreads == 1) {
+        ln_fwd_rows(&jobs[0]);
+    } else {
+        for (int t = 0; t < nthreads; ++t) pthread_create(&tid[t], NULL, ln_fwd_thread, &jobs[t]);
+        for (int t = 0; t < nthreads; ++t) pthread_join(tid[t], NULL);
+    }
+    int bad = 0;
+    for (int t = 0; t < nthreads; ++t) bad += jobs[t].bad;
+    free(jobs); free(tid);
+    return bad;
+}
+
+typedef struct {
+    int dtype, wdtype;
+    int64_t row0, row1, N;
+    const void *dy, *h, *gamma, *dres;
+    const float *mean_in, *rstd_in;
+    double eps, offset;
+    void *dx;
+    double *dx64, *dx_scale, *dx_cscale;
+    double *dg, *dg_abs, *db, *db_abs;   /* this job's partial sums, length N */
+    int bad;
+} ln_bwd_job;
+
+static void ln_bwd_rows(ln_bwd_job *jb)
+{
+    const int64_t N = jb->N;
+    double *hv = (double *)malloc((size_t)N * sizeof(double));
+    double *gpo = (double *)malloc((size_t)N * sizeof(double));
+    for (int64_t j = 0; j < N; ++j)
+        gpo[j] = jb->gamma ? jb->offset + load_elem(jb->wdtype, jb->gamma, j) : 1.0;
+    for (int64_t i = jb->row0; i < jb->row1; ++i) {
+        const int64_t base = i * N;
+        for (int64_t j = 0; j < N; ++j) hv[j] = load_elem(jb->dtype, jb->h, base + j);
+        double mu, rstd;
+        if (jb->rstd_in) {
+            mu = (double)jb->mean_in[i];
+            rstd = (double)jb->rstd_in[i];
+        } else {
+            double sum = 0.0;
+            for (int64_t j = 0; j < N; ++j) sum += hv[j];
+            mu = sum / (double)N;
+            double sq = 0.0;
+            for (int64_t j = 0; j < N; ++j) sq += (hv[j] - mu) * (hv[j] - mu);
+            rstd = 1.0 / sqrt(sq / (double)N + jb->eps);
+        }
+        /* mg = mean(g), c = mean(g xhat), and their absolute counterparts */
+        double mg = 0.0, c = 0.0, mgabs = 0.0, cabs = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            const double g = load_elem(jb->dtype, jb->dy, base + j) * gpo[j];
+            const double xhat = (hv[j] - mu) * rstd;
+            mg += g;
+            c += g * xhat;
+            mgabs += fabs(g);
+            cabs += fabs(g * xhat);
+        }
+        mg /= (double)N;
+        c /= (double)N;
+        mgabs /= (double)N;
+        cabs /= (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            const double dyj = load_elem(jb->dtype, jb->dy, base + j);
+            const double xhat = (hv[j] - mu) * rstd;
+            const double g = dyj * gpo[j];
+            double dxj = rstd * (g - mg - xhat * c);
+            double scale = rstd * (fabs(g) + fabs(mg) + fabs(xhat * c));
+            if (jb->dres) {
+                const double d = load_elem(jb->dtype, jb->dres, base + j);
+                dxj += d;
+                scale += fabs(d);
+            }
+            if (jb->dx64) jb->dx64[base + j] = dxj;
+            if (jb->dx_scale) jb->dx_scale[base + j] = scale;
+            if (jb->dx_cscale) jb->dx_cscale[base + j] = rstd * (mgabs + fabs(xhat) * cabs);
+            if (jb->dx) jb->bad |= store_elem(jb->dtype, jb->dx, base + j, dxj);
+            jb->dg[j] += dyj * xhat;
+            jb->dg_abs[j] += fabs(dyj * xhat);
+            jb->db[j] += dyj;
+            jb->db_abs[j] += fabs(dyj);
+        }
+    }
+    free(hv);
+    free(gpo);
+}
+
+static void *ln_bwd_thread(void *arg) { ln_bwd_rows((ln_bwd_job *)arg); return NULL; }
+
+/*
+ * LayerNorm backward over an M x N block. mean_in/rstd_in: both NULL
+ * (recomputed in double from h) or both the forward's fp32 values.
+ * Outputs as in oracle_rmsnorm_bwd, with dx_cscale = rstd (mean|g| + |xhat|
+ * mean|g xhat|) (the sensitivity of dx to the two row sums), plus dgamma
+ * (dg64, dg_abs = sum |dy xhat|, dg in the weight type) and dbeta (db64,
+ * db_abs = sum |dy|, db). Each output may be NULL except dg64 and db64.
+ */
+int oracle_layernorm_bwd(int dtype, int wdtype, int64_t M, int64_t N,
+                         const void *dy, const void *h, const void *gamma,
+                         const float *mean_in, const float *rstd_in, const void *dres,
+                         double eps, double offset,
+                         void *dx, double *dx64, double *dx_scale, double *dx_cscale,
+                         double *dg64, double *dg_abs, void *dg,
+                         double *db64, double *db_abs, void *db, int nthreads)
+{
+    if ((mean_in == NULL) != (rstd_in == NULL)) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
+    ln_bwd_job *jobs = (ln_bwd_job *)calloc((size_t)nthreads, sizeof(ln_bwd_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    for (int t = 0; t < nthreads; ++t) {
+        ln_bwd_job *jb = &jobs[t];
+        jb->dtype = dtype; jb->wdtype = wdtype; jb->N = N;
+        jb->row0 = M * t / nthreads; jb->row1 = M * (t + 1) / nthreads;
+        jb->dy = dy; jb->h = h; jb->gamma = gamma; jb->dres = dres;
+        jb->mean_in = mean_in; jb->rstd_in = rstd_in;
+        jb->eps = eps; jb->offset = offset;
+        jb->dx = dx; jb->dx64 = dx64; jb->dx_scale = dx_scale; jb->dx_cscale = dx_cscale;
+        jb->dg = (double *)calloc((size_t)N, sizeof(double));
+        jb->dg_abs = (double *)calloc((size_t)N, sizeof(double));
+        jb->db = (double *)calloc((size_t)N, sizeof(double));
+        jb->db_abs = (double *)calloc((size_t)N, sizeof(double));
+    }
+    if (nthreads == 1) {
+        ln_bwd_rows(&jobs[0]);
+    } else {
+        for (int t = 0; t < nthreads; ++t) pthread_create(&tid[t], NULL, ln_bwd_thread, &jobs[t]);
+        for (int t = 0; t < nthreads; ++t) pthread_join(tid[t], NULL);
+    }
+    int bad = 0;
+    for (int64_t j = 0; j < N; ++j) {
+        double sg = 0.0, sga = 0.0, sb = 0.0, sba = 0.0;
+        for (int t = 0; t < nthreads; ++t) {
+            sg += jobs[t].dg[j]; sga += jobs[t].dg_abs[j];
+            sb += jobs[t].db[j]; sba += jobs[t].db_abs[j];
+        }
+        dg64[j] = sg;
+        db64[j] = sb;
+        if (dg_abs) dg_abs[j] = sga;
+        if (db_abs) db_abs[j] = sba;
+        if (dg) bad |= store_elem(wdtype, dg, j, sg);
+        if (db) bad |= store_elem(wdtype, db, j, sb);
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        bad += jobs[t].bad;
+        free(jobs[t].dg); free(jobs[t].dg_abs); free(jobs[t].db); free(jobs[t].db_abs);
     }
     free(jobs); free(tid);
     return bad;

@@ -14,6 +14,9 @@ Recipe (numpy PCG64, ``default_rng([seed, stream])``):
   stream 4  dres     ~ N(0, 1)           (incoming residual-stream gradient)
   stream 5  outlier columns: ceil(frac * N) columns chosen by a seeded
             permutation, whose x values are multiplied by 20
+  stream 6  beta     ~ 0.1 N(0, 1)       (LayerNorm bias, on request)
+  x_shift   added to every x draw before the outlier scaling (LayerNorm
+            inputs with a non-zero row mean)
 Draws are float32; bf16 values are the float32 draws rounded to nearest
 (ties to even) on their bit patterns, fp16 values numpy's float32 -> float16
 conversion (nearest, ties to even). bf16 arrays are numpy uint16 bit
@@ -29,7 +32,7 @@ import math
 
 import numpy as np
 
-STREAM_X, STREAM_DY, STREAM_W, STREAM_RES, STREAM_DRES, STREAM_OUTLIER = range(6)
+STREAM_X, STREAM_DY, STREAM_W, STREAM_RES, STREAM_DRES, STREAM_OUTLIER, STREAM_BETA = range(7)
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -72,11 +75,15 @@ def outlier_columns(N: int, seed: int, frac: float) -> np.ndarray:
 
 def make_inputs(M: int, N: int, dtype: str, seed: int, *, dy_scale: float = 1.0,
                 w_mode: str = "llama", residual: bool = False, dres: bool = False,
-                outlier_frac: float = 0.0, outlier_scale: float = 20.0, wdtype: str | None = None) -> dict:
+                outlier_frac: float = 0.0, outlier_scale: float = 20.0, wdtype: str | None = None,
+                beta: bool = False, x_shift: float = 0.0) -> dict:
     """Return a dict of storage-typed numpy arrays: x, dy, w and, on request,
-    residual and dres. ``w_mode`` "llama" pairs with offset 0, "gemma" with 1.
-    ``wdtype`` is the weight's storage type (default ``dtype``)."""
+    residual, dres and beta. ``w_mode`` "llama" pairs with offset 0, "gemma"
+    with 1. ``wdtype`` is the weight's (and beta's) storage type (default
+    ``dtype``)."""
     x = _normal(seed, STREAM_X, (M, N))
+    if x_shift != 0.0:
+        x += np.float32(x_shift)
     if outlier_frac > 0.0:
         cols = outlier_columns(N, seed, outlier_frac)
         x[:, cols] *= np.float32(outlier_scale)
@@ -95,6 +102,8 @@ def make_inputs(M: int, N: int, dtype: str, seed: int, *, dy_scale: float = 1.0,
         out["residual"] = to_storage(_normal(seed, STREAM_RES, (M, N)), dtype)
     if dres:
         out["dres"] = to_storage(_normal(seed, STREAM_DRES, (M, N)), dtype)
+    if beta:
+        out["beta"] = to_storage(_normal(seed, STREAM_BETA, (N,), 0.1), wdtype or dtype)
     return out
 
 

@@ -22,13 +22,34 @@ MUTATIONS = {
     "w_index_reversed": ("load_elem(jb->wdtype, jb->w, j) : 1.0;\n            const double yj",
                          "load_elem(jb->wdtype, jb->w, N - 1 - j) : 1.0;\n            const double yj"),
     "bwd_sign_flip": ("rstd * (g - xhat * c)", "rstd * (g + xhat * c)"),
-    "bwd_c_not_mean": ("c /= (double)N;", "c /= 1.0;"),
+    "bwd_c_not_mean": ("c /= (double)N;\n        cabs /= (double)N;", "c /= 1.0;\n        cabs /= (double)N;"),
     "bwd_offset_dropped": ("wpo[j] = jb->w ? jb->offset + load_elem", "wpo[j] = jb->w ? 0.0 * jb->offset + load_elem"),
     "dw_uses_g": ("jb->dw[j] += dyj * xhat;", "jb->dw[j] += g * xhat;"),
     "dw_missing_rstd": ("jb->dw[j] += dyj * xhat;", "jb->dw[j] += dyj * hv[j];"),
-    "dres_dropped": ("dxj += d;", "dxj += 0.0 * d;"),
-    "fused_h_unrounded": ("h[j] = round_to(jb->dtype, xv + load_elem(jb->dtype, jb->residual, base + j));",
-                          "h[j] = xv + load_elem(jb->dtype, jb->residual, base + j);"),
+    "dres_dropped": ("rstd * (fabs(g) + fabs(xhat * c));\n            if (jb->dres) {\n"
+                     "                const double d = load_elem(jb->dtype, jb->dres, base + j);\n"
+                     "                dxj += d;",
+                     "rstd * (fabs(g) + fabs(xhat * c));\n            if (jb->dres) {\n"
+                     "                const double d = load_elem(jb->dtype, jb->dres, base + j);\n"
+                     "                dxj += 0.0 * d;"),
+    "ln_fused_h_unrounded": ("h[j] = round_to(jb->dtype, xv + load_elem(jb->dtype, jb->residual, base + j));\n"
+                             "            else\n                h[j] = xv;\n        }\n        double sum = 0.0;",
+                             "h[j] = xv + load_elem(jb->dtype, jb->residual, base + j);\n"
+                             "            else\n                h[j] = xv;\n        }\n        double sum = 0.0;"),
+    "ln_dres_dropped": ("rstd * (fabs(g) + fabs(mg) + fabs(xhat * c));\n            if (jb->dres) {\n"
+                        "                const double d = load_elem(jb->dtype, jb->dres, base + j);\n"
+                        "                dxj += d;",
+                        "rstd * (fabs(g) + fabs(mg) + fabs(xhat * c));\n            if (jb->dres) {\n"
+                        "                const double d = load_elem(jb->dtype, jb->dres, base + j);\n"
+                        "                dxj += 0.0 * d;"),
+    "fused_h_unrounded": ("/* h: the row that is normalised */\n        for (int64_t j = 0; j < N; ++j) {\n"
+                          "            double xv = load_elem(jb->dtype, jb->x, base + j);\n"
+                          "            if (jb->residual)\n"
+                          "                h[j] = round_to(jb->dtype, xv + load_elem(jb->dtype, jb->residual, base + j));",
+                          "/* h: the row that is normalised */\n        for (int64_t j = 0; j < N; ++j) {\n"
+                          "            double xv = load_elem(jb->dtype, jb->x, base + j);\n"
+                          "            if (jb->residual)\n"
+                          "                h[j] = xv + load_elem(jb->dtype, jb->residual, base + j);"),
     "bf16_via_binary32": ("int oracle_bf16_round(double v, uint16_t *out)\n{\n",
                           "int oracle_bf16_round(double v, uint16_t *out)\n{\n    v = (double)(float)v;\n"),
     "f16_via_binary32": ("int oracle_f16_round(double v, uint16_t *out)\n{\n",
@@ -47,6 +68,19 @@ MUTATIONS = {
     "fp8_row_scale_not_to_448": ("sc = amax > 0.0 ? 448.0 / amax : 1.0;", "sc = amax > 0.0 ? 256.0 / amax : 1.0;"),
     "fp8_scale_divides": ("const double v = yrow[j] * sc;", "const double v = yrow[j] / sc;"),
     "fp8_amax_of_h": ("if (fabs(yj) > amax) amax = fabs(yj);", "if (fabs(h[j]) > amax) amax = fabs(h[j]);"),
+    "ln_unbiased_variance": ("const double var = sq / (double)N;", "const double var = sq / (double)(N > 1 ? N - 1 : 1);"),
+    "ln_variance_not_centred": ("for (int64_t j = 0; j < N; ++j) sq += (h[j] - mu) * (h[j] - mu);",
+                                "for (int64_t j = 0; j < N; ++j) sq += h[j] * h[j];"),
+    "ln_beta_dropped": ("const double yj = (h[j] - mu) * rstd * factor + bias;",
+                        "const double yj = (h[j] - mu) * rstd * factor + 0.0 * bias;"),
+    "ln_mean_not_subtracted_in_y": ("const double yj = (h[j] - mu) * rstd * factor + bias;",
+                                    "const double yj = h[j] * rstd * factor + bias;"),
+    "ln_offset_dropped": ("gpo[j] = jb->gamma ? jb->offset + load_elem", "gpo[j] = jb->gamma ? 0.0 * jb->offset + load_elem"),
+    "ln_dx_missing_mean_g": ("double dxj = rstd * (g - mg - xhat * c);", "double dxj = rstd * (g - xhat * c);"),
+    "ln_dx_missing_xhat_term": ("double dxj = rstd * (g - mg - xhat * c);", "double dxj = rstd * (g - mg);"),
+    "ln_dbeta_uses_g": ("jb->db[j] += dyj;", "jb->db[j] += g;"),
+    "ln_dgamma_uses_h": ("jb->dg[j] += dyj * xhat;", "jb->dg[j] += dyj * hv[j];"),
+    "ln_bwd_ignores_given_mean": ("mu = (double)jb->mean_in[i];", "mu = 0.0 * (double)jb->mean_in[i];"),
     "weight_read_as_activation_type": ("wpo[j] = jb->w ? jb->offset + load_elem(jb->wdtype",
                                        "wpo[j] = jb->w ? jb->offset + load_elem(jb->dtype"),
 }

@@ -545,3 +545,149 @@ def test_fp8_fused_add_quantises_the_fused_forward():
                        scaling="row")
     assert np.array_equal(r["h"], base["h"]) and np.array_equal(r["y64"], base["y64"])
     _quant_check(r, 448.0 / np.abs(base["y64"]).max(axis=1))
+
+
+# ------------------------------------------------------------- LayerNorm --
+
+def test_ln_fwd_hand_example():
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    g = np.array([1.0, 2.0, 0.5, -1.0])
+    b = np.array([0.0, 1.0, -1.0, 0.25])
+    r = oracle.ln_fwd(x, g, b, dtype="f64", eps=0.25, offset=0.0)
+    # mean 2.5, biased variance 1.25, rstd = 1 / sqrt(1.25 + 0.25)
+    rstd = 1.0 / math.sqrt(1.5)
+    assert r["mean64"][0] == 2.5 and abs(r["rstd64"][0] - rstd) < 1e-15
+    want = (x[0] - 2.5) * rstd * g + b
+    assert np.allclose(r["y64"][0], want, rtol=1e-15, atol=1e-15)
+
+
+@pytest.mark.parametrize("N", [2, 7, 64, 1000])
+def test_ln_fwd_output_is_standardised(N):
+    # gamma = 1, beta = 0, eps = 0: every row has mean 0 and (biased) variance 1
+    x = inputs.make_inputs(5, N, "f32", 81, x_shift=3.0)["x"]
+    r = oracle.ln_fwd(x, None, None, dtype="f32", eps=0.0, offset=0.0)
+    y = r["y64"]
+    assert np.allclose(y.mean(axis=1), 0.0, atol=1e-12)
+    assert np.allclose((y * y).mean(axis=1), 1.0, rtol=1e-12)
+
+
+def test_ln_fwd_shift_invariance():
+    x = inputs.make_inputs(6, 96, "f32", 82)["x"].astype(np.float64)
+    g = inputs.make_inputs(1, 96, "f32", 83)["w"].astype(np.float64)
+    a = oracle.ln_fwd(x, g, None, dtype="f64", eps=1e-3, offset=0.0)
+    b = oracle.ln_fwd(x + 1024.0, g, None, dtype="f64", eps=1e-3, offset=0.0)
+    assert np.allclose(a["y64"], b["y64"], rtol=0, atol=1e-9)
+    assert np.allclose(b["mean64"] - a["mean64"], 1024.0, rtol=0, atol=1e-9)
+
+
+def test_ln_on_zero_mean_rows_is_rmsnorm():
+    # a row with zero mean: var = mean(x^2), so LayerNorm = RMSNorm (+ beta)
+    x = inputs.make_inputs(4, 64, "f32", 84)["x"].astype(np.float64)
+    x = np.concatenate([x, -x], axis=1)               # exact zero mean
+    w = np.linspace(0.5, 1.5, 128)
+    b = np.linspace(-0.2, 0.2, 128)
+    ln = oracle.ln_fwd(x, w, b, dtype="f64", eps=1e-5, offset=1.0)
+    rms = oracle.fwd(x, w, dtype="f64", eps=1e-5, offset=1.0)
+    assert np.allclose(ln["y64"] - b, rms["y64"], rtol=1e-13, atol=1e-13)
+    assert np.allclose(ln["rstd64"], rms["rstd64"], rtol=1e-14)
+
+
+def test_ln_n1_and_constant_rows():
+    # N = 1 or a constant row: xhat = 0, y = beta, rstd = 1/sqrt(eps) and
+    # dx = rstd (g - mean(g)) (zero for N = 1), dgamma = 0, dbeta = dy
+    eps = 1e-6
+    for x in (np.array([[3.5]]), np.full((1, 8), -2.0)):
+        N = x.shape[1]
+        gam = np.linspace(0.5, 1.7, N)
+        b = np.linspace(-1, 1, N)
+        r = oracle.ln_fwd(x, gam, b, dtype="f64", eps=eps, offset=0.0)
+        assert np.array_equal(r["y64"], b[None, :])
+        assert abs(r["rstd64"][0] - 1000.0) < 1e-9
+        dy = np.linspace(0.3, 2.0, N)[None, :]
+        d = oracle.ln_bwd(dy, x, gam, dtype="f64", eps=eps, offset=0.0)
+        g = dy[0] * gam
+        assert np.allclose(d["dx64"][0], 1000.0 * (g - g.mean()), rtol=1e-12, atol=1e-12)
+        if N == 1:
+            assert d["dx64"][0, 0] == 0.0
+        assert np.array_equal(d["db64"], dy[0]) and np.all(d["dg64"] == 0.0)
+
+
+def test_ln_fwd_storage_rounding_and_fused():
+    d = inputs.make_inputs(8, 128, "bf16", 85, residual=True, beta=True, x_shift=0.5)
+    r = oracle.ln_fwd(d["x"], d["w"], d["beta"], dtype="bf16", eps=1e-5, offset=0.0)
+    assert np.array_equal(r["y"], oracle.bf16_round(r["y64"]))
+    f = oracle.ln_fwd(d["x"], d["w"], d["beta"], dtype="bf16", eps=1e-5, offset=0.0, residual=d["residual"])
+    hsum = oracle.bf16_round(oracle.to_f64(d["x"], "bf16") + oracle.to_f64(d["residual"], "bf16"))
+    assert np.array_equal(f["h"], hsum)
+    p = oracle.ln_fwd(hsum, d["w"], d["beta"], dtype="bf16", eps=1e-5, offset=0.0)
+    assert np.array_equal(f["y"], p["y"]) and np.array_equal(f["rstd64"], p["rstd64"])
+
+
+@pytest.mark.parametrize("eps", [1e-5, 0.0])
+def test_ln_bwd_sums_and_orthogonality(eps):
+    # y is invariant to shifting h, so sum_j dx_j = 0; at eps = 0 it is also
+    # invariant to scaling (h - mean), so sum_j dx_j xhat_j = 0
+    d = inputs.make_inputs(6, 200, "f32", 86, x_shift=1.0, w_mode="gemma")
+    h = d["x"].astype(np.float64)
+    r = oracle.ln_bwd(d["dy"].astype(np.float64), h, d["w"].astype(np.float64), dtype="f64", eps=eps,
+                      offset=1.0)
+    scale = np.abs(r["dx64"]).sum(axis=1)
+    assert np.all(np.abs(r["dx64"].sum(axis=1)) <= 1e-12 * scale)
+    if eps == 0.0:
+        f = oracle.ln_fwd(h, None, None, dtype="f64", eps=0.0, offset=0.0)
+        xhat = f["y64"]
+        assert np.all(np.abs((r["dx64"] * xhat).sum(axis=1)) <= 1e-12 * scale * np.abs(xhat).max())
+
+
+@pytest.mark.parametrize("N,eps,offset,fused", [(1, 0.1, 0.0, False), (5, 0.1, 1.0, False), (8, 1e-6, 0.0, True),
+                                                 (13, 0.5, 1.0, True)])
+def test_ln_bwd_matches_finite_differences(N, eps, offset, fused):
+    rng = np.random.default_rng(87 + N)
+    M = 3
+    x = rng.standard_normal((M, N)) + 0.7
+    r = rng.standard_normal((M, N)) if fused else None
+    g = rng.standard_normal(N) * 0.3 + (0.0 if offset else 1.0)
+    b = rng.standard_normal(N) * 0.1
+    dy = rng.standard_normal((M, N))
+    dres = rng.standard_normal((M, N)) if fused else None
+
+    def loss(xv, gv, bv, rv):
+        f = oracle.ln_fwd(xv, gv, bv, dtype="f64", eps=eps, offset=offset, residual=rv)
+        L = (f["y64"] * dy).sum()
+        if fused:
+            L += ((xv + rv) * dres).sum()
+        return L
+
+    h = x + r if fused else x
+    d = oracle.ln_bwd(dy, h, g, dtype="f64", eps=eps, offset=offset, dres=dres)
+    step = 1e-6
+    for arr, grad in ((x, d["dx64"]), (g, d["dg64"]), (b, d["db64"])) + (((r, d["dx64"]),) if fused else ()):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + step
+            lp = loss(x, g, b, r)
+            arr[idx] = old - step
+            lm = loss(x, g, b, r)
+            arr[idx] = old
+            num[idx] = (lp - lm) / (2 * step)
+        assert np.allclose(num, grad, rtol=1e-6, atol=1e-7), (num, grad)
+
+
+def test_ln_bwd_param_grads_brute_force_and_given_stats():
+    d = inputs.make_inputs(9, 40, "bf16", 88, x_shift=0.3)
+    f = oracle.ln_fwd(d["x"], d["w"], None, dtype="bf16", eps=1e-5, offset=0.0)
+    r = oracle.ln_bwd(d["dy"], d["x"], d["w"], dtype="bf16", eps=1e-5, offset=0.0, mean=f["mean32"],
+                      rstd=f["rstd32"], nthreads=3)
+    x = oracle.to_f64(d["x"], "bf16")
+    dy = oracle.to_f64(d["dy"], "bf16")
+    xhat = (x - f["mean32"].astype(np.float64)[:, None]) * f["rstd32"].astype(np.float64)[:, None]
+    dg = np.zeros(40)
+    db = np.zeros(40)
+    for i in range(9):
+        for j in range(40):
+            dg[j] += dy[i, j] * xhat[i, j]
+            db[j] += dy[i, j]
+    assert np.allclose(r["dg64"], dg, rtol=1e-13, atol=1e-13)
+    assert np.allclose(r["db64"], db, rtol=1e-13, atol=1e-13)
+    assert np.array_equal(r["dg"], oracle.bf16_round(r["dg64"]))
