@@ -187,6 +187,56 @@ rmsnorm_status_t rmsnorm_fwd_fp8(const void *x, const void *residual, const void
                                  rmsnorm_stream_t stream);
 
 /*
+ * LayerNorm, the sibling norm the TransformerEngine tuning page registers
+ * tuned kernels for beside RMSNorm ("[ROCm] RMSNorm tuning", Description:
+ * matching tuned configs for LayerNorm), on the same kernels' geometry:
+ *
+ *   forward   mean_i = (1/N) sum_j h_ij
+ *             rstd_i = 1 / sqrt( (1/N) sum_j (h_ij - mean_i)^2 + eps )
+ *             y_ij   = (h_ij - mean_i) * rstd_i * (offset + gamma_j) + beta_j
+ *   backward  xhat = (h - mean) * rstd,  g = dy * (offset + gamma),
+ *             dx   = rstd * (g - mean_j(g) - xhat * mean_j(g xhat)) [+ dresidual_out]
+ *             dgamma_j = sum_i dy_ij xhat_ij,  dbeta_j = sum_i dy_ij
+ *
+ * Every step in fp32, each output rounded once (as for RMSNorm); the
+ * variance is the biased one, computed from the row held in registers in
+ * two passes (sum, then squared deviations from the mean).
+ * gamma == NULL: factor 1 (offset unused); beta == NULL: no bias.
+ * gamma, beta, dgamma, dbeta have the activations' storage type
+ * (RMSNORM_WEIGHT_F32 is UNSUPPORTED). mean and rstd [M] are fp32.
+ * residual / residual_out: both NULL, or both set for the fused add
+ * (h = R(x + residual), stored to residual_out, as in rmsnorm_add_fwd).
+ * Pointers, alignment, errors and aliasing as for the RMSNorm calls.
+ */
+rmsnorm_status_t layernorm_fwd(const void *x, const void *residual, const void *gamma, const void *beta,
+                               void *y, void *residual_out, float *mean, float *rstd,
+                               int64_t M, int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
+                               rmsnorm_stream_t stream);
+
+/*
+ * LayerNorm backward. Reads dy, x (h of the fused forward) [M,N], gamma
+ * [N] and the forward's mean and rstd; writes dx [M,N] (plus
+ * dresidual_out when that is non-NULL: the fused add's gradient of both x
+ * and residual) and, when non-NULL, dgamma [N] and dbeta [N]. dgamma
+ * requires gamma. Persistent main kernel with fp32 partial rows
+ * [units, 2N] (dgamma | dbeta) in the workspace, then one finalizer that
+ * sums them in a fixed order (as rmsnorm_bwd). workspace: NULL (stream-
+ * ordered allocation) or at least layernorm_bwd_workspace_bytes(M, N, dt)
+ * bytes, 16-byte aligned. With dgamma and dbeta both NULL no workspace is
+ * used and only the main kernel runs. M == 0 sets dgamma and dbeta to 0.
+ */
+rmsnorm_status_t layernorm_bwd(const void *dy, const void *dresidual_out, const void *x,
+                               const void *gamma, const float *mean, const float *rstd,
+                               void *dx, void *dgamma, void *dbeta,
+                               void *workspace, size_t workspace_bytes,
+                               int64_t M, int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
+                               rmsnorm_stream_t stream);
+
+/* Workspace bytes layernorm_bwd needs for (M, N, dt) on the current device
+ * (2 * units * N * 4, rounded up to 256; 0 without a device). */
+size_t layernorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt);
+
+/*
  * Backward without any allocation, for callers that cannot allocate device
  * memory when they call (an engine that reserves all device memory at
  * start-up, a plug-in host that passes its ops no workspace, code running
@@ -251,6 +301,7 @@ typedef struct {
 
 #define RMSNORM_OP_FWD 0
 #define RMSNORM_OP_BWD 1
+#define RMSNORM_OP_LN_BWD 2 /* LayerNorm backward (its forward uses RMSNORM_OP_FWD plans) */
 
 /*
  * Host-only plan query: no CUDA call, usable without a GPU. `aligned` says
@@ -281,6 +332,24 @@ rmsnorm_status_t rmsnorm_fwd_fp8_ex(const void *x, const void *residual, const v
                                     const float *scale, float *scale_inv, float *amax,
                                     int64_t M, int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
                                     rmsnorm_stream_t stream, int force_plan, rmsnorm_plan_t *plan_used);
+
+/*
+ * LayerNorm with a forced plan (force_plan < 0: default; the forward takes
+ * RMSNORM_OP_FWD plan ids, the default ones and the generic one; the
+ * backward RMSNORM_OP_LN_BWD ids) and, for the backward, a forced CTA
+ * count (force_ctas > 0). Report the plan that ran in *plan_used.
+ */
+rmsnorm_status_t layernorm_fwd_ex(const void *x, const void *residual, const void *gamma,
+                                  const void *beta, void *y, void *residual_out, float *mean, float *rstd,
+                                  int64_t M, int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
+                                  rmsnorm_stream_t stream, int force_plan, rmsnorm_plan_t *plan_used);
+rmsnorm_status_t layernorm_bwd_ex(const void *dy, const void *dresidual_out, const void *x,
+                                  const void *gamma, const float *mean, const float *rstd,
+                                  void *dx, void *dgamma, void *dbeta,
+                                  void *workspace, size_t workspace_bytes,
+                                  int64_t M, int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
+                                  rmsnorm_stream_t stream, int force_plan, int force_ctas,
+                                  rmsnorm_plan_t *plan_used);
 
 /*
  * Forward with a forced plan (force_plan < 0: default). residual and

@@ -7,6 +7,8 @@ beside 16-bit activations) and launch on the current stream:
   rmsnorm_fwd(x, w)                       -> y, rstd
   rmsnorm_add_fwd(x, residual, w)         -> y, residual_out, rstd
   rmsnorm_fwd_fp8(x, w, scaling=...)      -> E4M3 y, rstd, scale_inv, amax
+  layernorm_fwd(x, gamma, beta)           -> y, mean, rstd (dict)
+  layernorm_bwd(dy, x, gamma, mean, rstd) -> dx, dgamma, dbeta (dict)
   rmsnorm_bwd(dy, x, w, rstd)             -> dx, dw
   rmsnorm_add_bwd(dy, dres, h, w, rstd)   -> dx (= dresidual), dw
   rmsnorm_bwd_workspace_bytes(M, N, dt)
@@ -18,6 +20,7 @@ fallback. ``inputs`` holds the seeded synthetic workloads.
 from ._binding import (  # noqa: F401
     OP_BWD,
     OP_FWD,
+    OP_LN_BWD,
     RMSNORM_BF16,
     RMSNORM_F16,
     RMSNORM_F32,
@@ -26,6 +29,9 @@ from ._binding import (  # noqa: F401
     LIB_PATH,
     Plan,
     RMSNormError,
+    layernorm_bwd,
+    layernorm_bwd_workspace_bytes,
+    layernorm_fwd,
     lib,
     plan_query,
     rmsnorm_add_bwd,

@@ -19,7 +19,7 @@ RMSNORM_F32, RMSNORM_BF16, RMSNORM_F16 = 0, 1, 2
 RMSNORM_WEIGHT_F32 = 0x100  # OR'ed into a 16-bit type: w and dw are fp32
 STATUS = {0: "SUCCESS", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_WORKSPACE", 4: "ERR_CUDA"}
 PATH_NAMES = {0: "vector", 1: "staged", 2: "generic"}
-OP_FWD, OP_BWD = 0, 1
+OP_FWD, OP_BWD, OP_LN_BWD = 0, 1, 2
 TORCH_DTYPE = {torch.float32: RMSNORM_F32, torch.bfloat16: RMSNORM_BF16, torch.float16: RMSNORM_F16}
 
 
@@ -75,6 +75,12 @@ SIGNATURES = {
     "rmsnorm_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp]),
     "rmsnorm_fwd_fp8_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp,
                                 _i, _PPlan]),
+    "layernorm_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp]),
+    "layernorm_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp, _i, _PPlan]),
+    "layernorm_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i, _f, _f, _vp]),
+    "layernorm_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i, _f, _f, _vp,
+                              _i, _i, _PPlan]),
+    "layernorm_bwd_workspace_bytes": (_sz, [_i64, _i64, _i]),
     "rmsnorm_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp, _i, _PPlan]),
     "rmsnorm_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i, _f, _f, _vp,
                             _i, _i, _i, _i, _vp, _PPlan]),
@@ -360,3 +366,75 @@ def rmsnorm_bwd_ex(dy, x, w, rstd, *, dresidual_out=None, fused=False, eps=1e-6,
                               int(fused), force_plan, force_ctas, force_packed, ev, ctypes.byref(p))
     _raise(st, "rmsnorm_bwd_ex")
     return dx, dw, p.as_dict()
+
+
+# ------------------------------------------------------------- LayerNorm --
+
+def layernorm_fwd(x, gamma, beta, *, residual=None, eps: float = 1e-5, offset: float = 0.0, y=None,
+                  residual_out=None, mean=None, rstd=None, force_plan=-1, stream=None):
+    """LayerNorm over the last dimension: y = (h - mean) rstd (offset + gamma) + beta,
+    h = x or x + residual (fused, h also returned). gamma / beta may be None.
+    Returns a dict with y, residual_out (fused only), mean, rstd, plan."""
+    M, N = _rows(x)
+    _check(x, "x")
+    for t, n in ((gamma, "gamma"), (beta, "beta")):
+        if t is not None:
+            _check(t, n, like=x, numel=N)
+    y = torch.empty_like(x) if y is None else y
+    _check(y, "y", like=x, numel=x.numel())
+    if residual is not None:
+        _check(residual, "residual", like=x, numel=x.numel())
+        residual_out = torch.empty_like(x) if residual_out is None else residual_out
+        _check(residual_out, "residual_out", like=x, numel=x.numel())
+    mean = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if mean is None else mean
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
+    _check(mean, "mean", numel=M)
+    _check(rstd, "rstd", numel=M)
+    p = Plan()
+    st = lib().layernorm_fwd_ex(x.data_ptr(), _ptr(residual), _ptr(gamma), _ptr(beta), y.data_ptr(),
+                                _ptr(residual_out), mean.data_ptr(), rstd.data_ptr(), M, N, _dtype_code(x), eps,
+                                offset, _stream_handle(stream, x.device), force_plan, ctypes.byref(p))
+    _raise(st, "layernorm_fwd")
+    return {"y": y, "residual_out": residual_out, "mean": mean, "rstd": rstd, "plan": p.as_dict()}
+
+
+def layernorm_bwd(dy, x, gamma, mean, rstd, *, dresidual_out=None, want_dgamma=True, want_dbeta=True,
+                  eps: float = 1e-5, offset: float = 0.0, dx=None, dgamma=None, dbeta=None, workspace=None,
+                  force_plan=-1, force_ctas=0, stream=None):
+    """dx (plus dresidual_out, fused), dgamma and dbeta of LayerNorm given the
+    forward's mean and rstd. dgamma is None without gamma or when not wanted;
+    dbeta is None when not wanted. Returns a dict with dx, dgamma, dbeta, plan."""
+    M, N = _rows(x)
+    for t, n in ((dy, "dy"), (x, "x")):
+        _check(t, n, like=x, numel=x.numel())
+    _check(mean, "mean", numel=M)
+    _check(rstd, "rstd", numel=M)
+    if dresidual_out is not None:
+        _check(dresidual_out, "dresidual_out", like=x, numel=x.numel())
+    dx = torch.empty_like(x) if dx is None else dx
+    _check(dx, "dx", like=x, numel=x.numel())
+    if gamma is not None:
+        _check(gamma, "gamma", like=x, numel=N)
+    if gamma is not None and want_dgamma:
+        dgamma = torch.empty(N, dtype=x.dtype, device=x.device) if dgamma is None else dgamma
+        _check(dgamma, "dgamma", like=x, numel=N)
+    else:
+        dgamma = None
+    if want_dbeta:
+        dbeta = torch.empty(N, dtype=x.dtype, device=x.device) if dbeta is None else dbeta
+        _check(dbeta, "dbeta", like=x, numel=N)
+    else:
+        dbeta = None
+    wp, wb = _ws(workspace)
+    p = Plan()
+    st = lib().layernorm_bwd_ex(dy.data_ptr(), _ptr(dresidual_out), x.data_ptr(), _ptr(gamma), mean.data_ptr(),
+                                rstd.data_ptr(), dx.data_ptr(), _ptr(dgamma), _ptr(dbeta), wp, wb, M, N,
+                                _dtype_code(x), eps, offset, _stream_handle(stream, x.device), force_plan,
+                                force_ctas, ctypes.byref(p))
+    _raise(st, "layernorm_bwd")
+    return {"dx": dx, "dgamma": dgamma, "dbeta": dbeta, "plan": p.as_dict()}
+
+
+def layernorm_bwd_workspace_bytes(M: int, N: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else TORCH_DTYPE[dtype]
+    return int(lib().layernorm_bwd_workspace_bytes(M, N, code))

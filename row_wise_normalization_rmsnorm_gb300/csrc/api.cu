@@ -90,9 +90,12 @@ static int nominal_ctas_per_sm(const PlanDesc &d) {
     return c < 1 ? 1 : c;
 }
 
+// Partial rows per backward unit: dW (RMSNorm) or dgamma and dbeta (LayerNorm).
+static int partial_rows(int op) { return op == OP_LN_BWD ? 2 : 1; }
+
 static int bwd_smem_bytes(const PlanDesc &d, int64_t N) {
     if (d.path != PATH_VECTOR || d.teams <= 1) return 0;
-    return (int)((d.teams - 1) * N * 4);
+    return (int)((d.teams - 1) * partial_rows(d.op) * N * 4);
 }
 
 // Chunks one plan can hold per row.
@@ -104,7 +107,7 @@ static int64_t plan_capacity(const PlanDesc &d) { return (int64_t)d.tpr * d.v * 
 static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool aligned, int64_t max_parts,
                                     int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
     if (!out) return RMSNORM_ERR_INVALID_ARG;
-    if (op != RMSNORM_OP_FWD && op != RMSNORM_OP_BWD) return RMSNORM_ERR_INVALID_ARG;
+    if (op != RMSNORM_OP_FWD && op != RMSNORM_OP_BWD && op != RMSNORM_OP_LN_BWD) return RMSNORM_ERR_INVALID_ARG;
     if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (max_parts < 1) return RMSNORM_ERR_INVALID_ARG;
@@ -148,7 +151,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     out->ctas_per_sm = ctas_per_sm;
     out->smem_bytes = bwd_smem_bytes(*d, N);
     if (out->smem_bytes > 48 * 1024) return RMSNORM_ERR_UNSUPPORTED;
-    const int64_t bytes = P * N * 4;
+    const int64_t bytes = P * partial_rows(op) * N * 4;
     out->workspace_bytes = (bytes + 255) / 256 * 256;
     return RMSNORM_SUCCESS;
 }
@@ -212,6 +215,14 @@ static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed) {
     }
 }
 
+static const void *ln_bwd_kernel(int plan_id, int dt, bool fused) {
+    switch (base_dtype(dt)) {
+    case RMSNORM_BF16: return ln_bwd_kernel_ptr_bf16(plan_id, fused);
+    case RMSNORM_F16: return ln_bwd_kernel_ptr_f16(plan_id, fused);
+    default: return ln_bwd_kernel_ptr_f32(plan_id, fused);
+    }
+}
+
 static int launch_fwd_dt(int dt, int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
     switch (kind_of(dt)) {
     case 1: return launch_fwd_bf16(plan_id, fused, p, grid, stream);
@@ -234,11 +245,12 @@ static int launch_bwd_dt(int dt, int plan_id, bool fused, bool packed, const Bwd
 }
 
 // dW is written in the weight's storage type.
-static int launch_finalize_dt(int dt, const float *ws, int parts, int N, void *dw, void *stream, bool serial) {
+static int launch_finalize_dt(int dt, const float *ws, int parts, int ncols, void *out0, void *out1, int split,
+                              void *stream, bool serial) {
     switch (kind_of(dt)) {
-    case 1: return launch_dw_finalize_bf16(ws, parts, N, dw, stream, serial);
-    case 2: return launch_dw_finalize_f16(ws, parts, N, dw, stream, serial);
-    default: return launch_dw_finalize_f32(ws, parts, N, dw, stream, serial);
+    case 1: return launch_dw_finalize_bf16(ws, parts, ncols, out0, out1, split, stream, serial);
+    case 2: return launch_dw_finalize_f16(ws, parts, ncols, out0, out1, split, stream, serial);
+    default: return launch_dw_finalize_f32(ws, parts, ncols, out0, out1, split, stream, serial);
     }
 }
 
@@ -248,13 +260,13 @@ static int launch_finalize_dt(int dt, const float *ws, int parts, int N, void *d
 // those two variants use the same count (and dW the same summation order).
 // Cached per device, kernel kind, plan and mode.
 static std::mutex g_occ_mutex;
-static int g_parts_cache[kMaxDevices][kNumKinds][2][64];
-static int g_cps_cache[kMaxDevices][kNumKinds][2][64];
+static int g_parts_cache[kMaxDevices][kNumKinds][2][kMaxPlanId];
+static int g_cps_cache[kMaxDevices][kNumKinds][2][kMaxPlanId];
 
 static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, int64_t N, bool fused,
                                  int *parts_out, int *cps_out) {
     const int slot = d.id;
-    if (slot < 0 || slot >= 64) return cudaErrorInvalidValue;
+    if (slot < 0 || slot >= kMaxPlanId) return cudaErrorInvalidValue;
     const int dti = kind_of(dt);
     const int fi = fused ? 1 : 0;
     {
@@ -273,8 +285,9 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
     const int smem = bwd_smem_bytes(d, nmax);
     int best = 1 << 30;
     for (int pk = 0; pk < 2; ++pk) {
-        if (d.path == PATH_GENERIC && pk == 1) continue;
-        const void *k = bwd_kernel(d.id, dt, fused, pk != 0);
+        // the LayerNorm kernels and the generic ones have one variant
+        if ((d.path == PATH_GENERIC || d.op == OP_LN_BWD) && pk == 1) continue;
+        const void *k = d.op == OP_LN_BWD ? ln_bwd_kernel(d.id, dt, fused) : bwd_kernel(d.id, dt, fused, pk != 0);
         if (!k) return cudaErrorInvalidDeviceFunction;
         int n = 0;
         cudaError_t e;
@@ -318,7 +331,7 @@ static std::atomic<int> g_table_ok{-1};
 
 int self_check_impl() {
     int bad = 0;
-    for (int op = 0; op < 2; ++op) {
+    for (int op = 0; op < 3; ++op) {
         for (int dt = 0; dt < 3; ++dt) {  // the activations' type decides the defaults
             int64_t expect = 1;
             for (int i = 0; i < kNumPlans; ++i) {
@@ -345,7 +358,7 @@ int self_check_impl() {
             if (d.cs < 1 || d.cs > 8 || (d.cs > 1 && (d.teams != 1 || d.tpr < 32))) ++bad;
         }
         if (d.dtm < 1 || d.dtm > DT_ANY) ++bad;
-        if (d.id < 0 || d.id >= 64) ++bad;
+        if (d.id < 0 || d.id >= kMaxPlanId) ++bad;
     }
     return bad;
 }
@@ -436,6 +449,8 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     p.qscale = q.scale;
     p.qscale_inv = q.scale_inv;
     p.qamax = reinterpret_cast<unsigned int *>(q.amax);
+    p.beta = nullptr;
+    p.mean = nullptr;
     int le;
     if (quant) {
         cudaError_t e = clear_amax();
@@ -534,18 +549,206 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     p.dres = dres;
     p.dx = dx;
     p.ws = ws;
+    p.mean = nullptr;
     p.M = M;
     p.N = (int)N;
     p.offset = offset;
     int le = launch_bwd_dt(dt, plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream);
     if (le == 0 && event_after_main) le = (int)cudaEventRecord(static_cast<cudaEvent_t>(event_after_main), stream);
     if (le == 0 && affine)
-        le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)N, dw, stream, event_after_main != nullptr);
+        le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)N, dw, nullptr, (int)N, stream,
+                                event_after_main != nullptr);
     if (owned) {
         cudaError_t fe = cudaFreeAsync(ws, stream);
         if (le == 0 && fe != cudaSuccess) le = (int)fe;
     }
     if (le != 0) return cuda_fail((cudaError_t)le);
+    if (used) *used = plan;
+    return RMSNORM_SUCCESS;
+}
+
+// Bytes of workspace a backward (op RMSNORM_OP_BWD or RMSNORM_OP_LN_BWD)
+// needs on the current device: the largest need over the aligned and generic
+// plans and the plain and fused variants, so one size serves every call.
+static size_t bwd_workspace_bytes(int op, int64_t M, int64_t N, int dt) {
+    if (M <= 0 || N < 1 || N > RMSNORM_MAX_N || !valid_dtype(dt)) return 0;
+    if (M > 0x7fffffffLL || !table_ok()) return 0;
+    int dev = 0, sms = 0;
+    if (device_sms(&dev, &sms) != cudaSuccess) return 0;
+    size_t best = 0;
+    // The largest requirement over the aligned and generic plans and the
+    // plain and fused variants, so one size serves every call.
+    for (int aligned = 0; aligned < 2; ++aligned) {
+        for (int fused = 0; fused < 2; ++fused) {
+            rmsnorm_plan_t plan;
+            if (select_plan(op, M, N, dt, aligned != 0, 1, 0, -1, 0, &plan) != RMSNORM_SUCCESS)
+                return 0;
+            int parts = 1, cps = 1;
+            if (bwd_max_parts(dev, sms, dt, *find_plan(plan.plan_id), N, fused != 0, &parts, &cps) !=
+                cudaSuccess)
+                return 0;
+            if (select_plan(op, M, N, dt, aligned != 0, parts, cps, -1, 0, &plan) !=
+                RMSNORM_SUCCESS)
+                return 0;
+            if ((size_t)plan.workspace_bytes > best) best = (size_t)plan.workspace_bytes;
+        }
+    }
+    return best;
+}
+
+// ------------------------------------------------------------- LayerNorm --
+
+static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const void *gamma, const void *beta,
+                                    void *y, void *residual_out, float *mean, float *rstd, int64_t M, int64_t N,
+                                    int dt, float eps, float offset, cudaStream_t stream, int force_plan,
+                                    rmsnorm_plan_t *used) {
+    if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
+    if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
+    if (mixed_kind(kind_of(dt))) return RMSNORM_ERR_UNSUPPORTED;  // gamma, beta in the activations' type
+    if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
+    if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
+    if (M == 0) return RMSNORM_SUCCESS;
+    const bool fused = residual != nullptr || residual_out != nullptr;
+    if (fused && (!residual || !residual_out)) return RMSNORM_ERR_INVALID_ARG;
+    if (!x || !y || !mean || !rstd) return RMSNORM_ERR_INVALID_ARG;
+    const uintptr_t s = (uintptr_t)elem_size(dt);
+    if (!aligned_to(x, s) || !aligned_to(y, s) || (gamma && !aligned_to(gamma, s)) || (beta && !aligned_to(beta, s)) ||
+        !aligned_to(mean, 4) || !aligned_to(rstd, 4))
+        return RMSNORM_ERR_INVALID_ARG;
+    if (fused && (!aligned_to(residual, s) || !aligned_to(residual_out, s))) return RMSNORM_ERR_INVALID_ARG;
+    bool aligned = aligned_to(x, 16) && aligned_to(y, 16) && (!gamma || aligned_to(gamma, 16)) &&
+                   (!beta || aligned_to(beta, 16));
+    if (fused) aligned = aligned && aligned_to(residual, 16) && aligned_to(residual_out, 16);
+
+    rmsnorm_plan_t plan;
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, 1, 0, force_plan, 0, &plan);
+    if (st != RMSNORM_SUCCESS) return st;
+    // the LayerNorm forward is compiled for the default plans and the generic one
+    if (plan.path == PATH_VECTOR && find_plan(plan.plan_id)->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
+
+    FwdParams p;
+    std::memset(&p, 0, sizeof p);
+    p.x = x;
+    p.residual = residual;
+    p.w = gamma;
+    p.beta = beta;
+    p.y = y;
+    p.residual_out = residual_out;
+    p.rstd = rstd;
+    p.mean = mean;
+    p.M = M;
+    p.N = (int)N;
+    p.eps = eps;
+    p.offset = offset;
+    int le;
+    switch (base_dtype(dt)) {
+    case RMSNORM_BF16: le = launch_ln_fwd_bf16(plan.plan_id, fused, p, plan.ctas, stream); break;
+    case RMSNORM_F16: le = launch_ln_fwd_f16(plan.plan_id, fused, p, plan.ctas, stream); break;
+    default: le = launch_ln_fwd_f32(plan.plan_id, fused, p, plan.ctas, stream); break;
+    }
+    if (le != 0) return cuda_fail((cudaError_t)le);
+    if (used) *used = plan;
+    return RMSNORM_SUCCESS;
+}
+
+static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void *x, const void *gamma,
+                                    const float *mean, const float *rstd, void *dx, void *dgamma, void *dbeta,
+                                    void *workspace, size_t ws_bytes, int64_t M, int64_t N, int dt, float eps,
+                                    float offset, cudaStream_t stream, int force_plan, int force_ctas,
+                                    rmsnorm_plan_t *used) {
+    if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
+    if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
+    if (mixed_kind(kind_of(dt))) return RMSNORM_ERR_UNSUPPORTED;
+    if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
+    if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
+    const uintptr_t s = (uintptr_t)elem_size(dt);
+    // dgamma needs gamma; without gamma the weight factor is 1 and there is no dgamma
+    if (dgamma && !gamma) return RMSNORM_ERR_INVALID_ARG;
+    if ((gamma && !aligned_to(gamma, s)) || (dgamma && !aligned_to(dgamma, s)) || (dbeta && !aligned_to(dbeta, s)))
+        return RMSNORM_ERR_INVALID_ARG;
+    const bool want = dgamma != nullptr || dbeta != nullptr;
+    if (M == 0) {  // the parameter gradients are the empty sums
+        cudaError_t e = cudaSuccess;
+        if (dgamma) e = cudaMemsetAsync(dgamma, 0, (size_t)N * s, stream);
+        if (e == cudaSuccess && dbeta) e = cudaMemsetAsync(dbeta, 0, (size_t)N * s, stream);
+        return e == cudaSuccess ? RMSNORM_SUCCESS : cuda_fail(e);
+    }
+    if (!dy || !x || !mean || !rstd || !dx) return RMSNORM_ERR_INVALID_ARG;
+    if (!aligned_to(dy, s) || !aligned_to(x, s) || !aligned_to(dx, s) || !aligned_to(mean, 4) ||
+        !aligned_to(rstd, 4) || (dres && !aligned_to(dres, s)))
+        return RMSNORM_ERR_INVALID_ARG;
+    if (workspace && !aligned_to(workspace, 16)) return RMSNORM_ERR_WORKSPACE;
+    const bool fused = dres != nullptr;
+    bool aligned = aligned_to(dy, 16) && aligned_to(x, 16) && aligned_to(dx, 16) && (!gamma || aligned_to(gamma, 16));
+    if (dres) aligned = aligned && aligned_to(dres, 16);
+
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess) return cuda_fail(e);
+    rmsnorm_plan_t plan;
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_LN_BWD, M, N, dt, aligned, 1, 0, force_plan, force_ctas, &plan);
+    if (st != RMSNORM_SUCCESS) return st;
+    int parts = 1, cps = 1;
+    e = bwd_max_parts(dev, sms, dt, *find_plan(plan.plan_id), N, fused, &parts, &cps);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = select_plan(RMSNORM_OP_LN_BWD, M, N, dt, aligned, parts, cps, force_plan, force_ctas, &plan);
+    if (st != RMSNORM_SUCCESS) return st;
+
+    float *ws = static_cast<float *>(workspace);
+    bool owned = false;
+    if (!want) {
+        ws = nullptr;  // no parameter gradients: no partial rows, no finalizer
+    } else if (ws) {
+        if (ws_bytes < (size_t)plan.workspace_bytes) return RMSNORM_ERR_WORKSPACE;
+    } else {
+        void *tmp = nullptr;
+        e = cudaMallocAsync(&tmp, (size_t)plan.workspace_bytes, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+        ws = static_cast<float *>(tmp);
+        owned = true;
+    }
+    int *status = nullptr;
+    e = status_word(dev, &status);
+    if (e != cudaSuccess) {
+        if (owned) cudaFreeAsync(ws, stream);
+        return cuda_fail(e);
+    }
+
+    BwdParams p;
+    std::memset(&p, 0, sizeof p);
+    p.status = status;
+    p.dy = dy;
+    p.x = x;
+    p.w = gamma;
+    p.rstd = rstd;
+    p.mean = mean;
+    p.dres = dres;
+    p.dx = dx;
+    p.ws = ws;
+    p.M = M;
+    p.N = (int)N;
+    p.offset = offset;
+    int le;
+    switch (base_dtype(dt)) {
+    case RMSNORM_BF16: le = launch_ln_bwd_bf16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+    case RMSNORM_F16: le = launch_ln_bwd_f16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+    default: le = launch_ln_bwd_f32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+    }
+    // one finalizer over the [units, 2N] partial rows: dgamma | dbeta
+    if (le == 0 && want) {
+        void *out0 = dgamma, *out1 = dbeta;
+        int split = (int)N;
+        if (!dgamma) {  // dbeta only: columns [N, 2N) go to out1, [0, N) nowhere
+            out0 = nullptr;
+        }
+        le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)(2 * N), out0, out1, split, stream, false);
+    }
+    if (owned) {
+        cudaError_t fe = cudaFreeAsync(ws, stream);
+        if (le == 0 && fe != cudaSuccess) le = (int)fe;
+    }
+    if (le != 0) return cuda_fail((cudaError_t)le);
+    plan.packed = plan.path == PATH_VECTOR ? 1 : 0;
     if (used) *used = plan;
     return RMSNORM_SUCCESS;
 }
@@ -628,29 +831,44 @@ rmsnorm_status_t rmsnorm_bwd_ex(const void *dy, const void *dresidual_out, const
 }
 
 size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt) {
-    if (M <= 0 || N < 1 || N > RMSNORM_MAX_N || !valid_dtype(dt)) return 0;
-    if (M > 0x7fffffffLL || !table_ok()) return 0;
-    int dev = 0, sms = 0;
-    if (device_sms(&dev, &sms) != cudaSuccess) return 0;
-    size_t best = 0;
-    // The largest requirement over the aligned and generic plans and the
-    // plain and fused variants, so one size serves every call.
-    for (int aligned = 0; aligned < 2; ++aligned) {
-        for (int fused = 0; fused < 2; ++fused) {
-            rmsnorm_plan_t plan;
-            if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, 1, 0, -1, 0, &plan) != RMSNORM_SUCCESS)
-                return 0;
-            int parts = 1, cps = 1;
-            if (bwd_max_parts(dev, sms, dt, *find_plan(plan.plan_id), N, fused != 0, &parts, &cps) !=
-                cudaSuccess)
-                return 0;
-            if (select_plan(RMSNORM_OP_BWD, M, N, dt, aligned != 0, parts, cps, -1, 0, &plan) !=
-                RMSNORM_SUCCESS)
-                return 0;
-            if ((size_t)plan.workspace_bytes > best) best = (size_t)plan.workspace_bytes;
-        }
-    }
-    return best;
+    return bwd_workspace_bytes(RMSNORM_OP_BWD, M, N, dt);
+}
+
+rmsnorm_status_t layernorm_fwd(const void *x, const void *residual, const void *gamma, const void *beta, void *y,
+                               void *residual_out, float *mean, float *rstd, int64_t M, int64_t N,
+                               rmsnorm_dtype_t dt, float eps, float offset, rmsnorm_stream_t stream) {
+    return ln_fwd_impl(x, residual, gamma, beta, y, residual_out, mean, rstd, M, N, dt, eps, offset,
+                       (cudaStream_t)stream, -1, nullptr);
+}
+
+rmsnorm_status_t layernorm_fwd_ex(const void *x, const void *residual, const void *gamma, const void *beta,
+                                  void *y, void *residual_out, float *mean, float *rstd, int64_t M, int64_t N,
+                                  rmsnorm_dtype_t dt, float eps, float offset, rmsnorm_stream_t stream,
+                                  int force_plan, rmsnorm_plan_t *plan_used) {
+    return ln_fwd_impl(x, residual, gamma, beta, y, residual_out, mean, rstd, M, N, dt, eps, offset,
+                       (cudaStream_t)stream, force_plan, plan_used);
+}
+
+rmsnorm_status_t layernorm_bwd(const void *dy, const void *dresidual_out, const void *x, const void *gamma,
+                               const float *mean, const float *rstd, void *dx, void *dgamma, void *dbeta,
+                               void *workspace, size_t workspace_bytes, int64_t M, int64_t N, rmsnorm_dtype_t dt,
+                               float eps, float offset, rmsnorm_stream_t stream) {
+    return ln_bwd_impl(dy, dresidual_out, x, gamma, mean, rstd, dx, dgamma, dbeta, workspace, workspace_bytes, M,
+                       N, dt, eps, offset, (cudaStream_t)stream, -1, 0, nullptr);
+}
+
+rmsnorm_status_t layernorm_bwd_ex(const void *dy, const void *dresidual_out, const void *x, const void *gamma,
+                                  const float *mean, const float *rstd, void *dx, void *dgamma, void *dbeta,
+                                  void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                                  rmsnorm_dtype_t dt, float eps, float offset, rmsnorm_stream_t stream,
+                                  int force_plan, int force_ctas, rmsnorm_plan_t *plan_used) {
+    return ln_bwd_impl(dy, dresidual_out, x, gamma, mean, rstd, dx, dgamma, dbeta, workspace, workspace_bytes, M,
+                       N, dt, eps, offset, (cudaStream_t)stream, force_plan, force_ctas, plan_used);
+}
+
+size_t layernorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt) {
+    if (mixed_kind(kind_of(dt))) return 0;
+    return bwd_workspace_bytes(RMSNORM_OP_LN_BWD, M, N, dt);
 }
 
 rmsnorm_status_t rmsnorm_plan_query(int op, int64_t M, int64_t N, rmsnorm_dtype_t dt, int aligned, int num_sms,

@@ -21,7 +21,16 @@
 // packed math where the wide-row backward is issue-bound); without it they
 // are two fp32 intrinsics per pair. The association is the same, so the two
 // variants produce identical bits.
+//
+// The LayerNorm backward runs on the same machinery (LN = true): the row
+// carries the forward's mean as well as rstd, pass 1 reduces the pair
+// (sum g, sum g (x - mean)), pass 2 writes
+// dx = rstd (g - mean(g) - xhat mean(g xhat)), and each unit keeps two
+// partial rows, dgamma = sum dy xhat and dbeta = sum dy, written as one
+// [units, 2N] workspace row that one finalizer launch reduces.
 #pragma once
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "plans.h"
@@ -31,10 +40,10 @@ namespace rmsn {
 // x, dy (and dres) chunks of one row, and its rstd, into registers. Rows
 // past M are clamped to the last row (their results are masked later), so
 // every thread of the CTA keeps taking part in the reductions.
-template <typename T, int TPR, int V>
+template <typename T, int TPR, int V, bool LN>
 __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, int C, int cbase, int t,
                                              bool has_dres, uint4 (&x)[V], uint4 (&d)[V], uint4 (&r)[V],
-                                             float &rs) {
+                                             float &rs, float &mu) {
     const int64_t rr = row < p.M ? row : p.M - 1;
     const int64_t base = rr * C;
     const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x) + base;
@@ -49,6 +58,7 @@ __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, in
         r[v] = (has_dres && in) ? ld_stream(r4 + c) : make_uint4(0, 0, 0, 0);
     }
     rs = p.rstd[rr];
+    if constexpr (LN) mu = p.mean[rr];
 }
 
 // Persistent main kernel. Rows are software-pipelined through a register
@@ -59,19 +69,20 @@ __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, in
 // CS > 1: the CTAs of a cluster share each row (CTA rank r holds chunks
 // [r TPR V, (r+1) TPR V)); the row sum meets in distributed shared memory
 // and the cluster, not the CTA, owns one dW partial row.
-template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool FUSED>
-__global__ void __launch_bounds__(TPR *TEAMS)
-    rmsnorm_bwd_vector(const BwdParams p) {
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool FUSED, bool LN>
+__device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
     using Pk = Pair<PACKED>;
+    using RT = typename std::conditional<LN, float2, float>::type;  // what a row reduces
     constexpr int E = Elem<T>::E;
     constexpr int NP = Elem<T>::NP;
     constexpr int W = TPR > 32 ? TPR / 32 : 1;
     constexpr int B = D + 1;              // ring slots
     constexpr int BR = FUSED ? B : 1;     // dres slots
-    __shared__ float red[2][TEAMS][W * CS];           // row partials, double-buffered
+    constexpr int NACC = LN ? 2 : 1;      // partial rows per unit
+    __shared__ RT red[2][TEAMS][W * CS];              // row partials, double-buffered
     __shared__ __align__(8) uint64_t rbar[2][1];      // cluster rows: arrival of the peers' partials
-    extern __shared__ float4 comb_smem[];      // (TEAMS - 1) * N floats
+    extern __shared__ float4 comb_smem[];      // (TEAMS - 1) * NACC * N floats
 
     const int team = threadIdx.x / TPR;
     const int t = threadIdx.x % TPR;
@@ -86,8 +97,12 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     // (offset + w) for this thread's columns: loaded once per CTA. Without
     // a weight (non-affine) the factor is 1 and there is no dW.
     const bool has_w = p.w != nullptr;
+    // partial rows wanted: RMSNorm with a weight; LayerNorm when the host
+    // passes a workspace (dgamma and/or dbeta requested)
+    const bool want_acc = LN ? p.ws != nullptr : has_w;
     const float2 o2 = make_float2(p.offset, p.offset);
     float2 wp[V][NP], acc[V][NP];
+    float2 accb[LN ? V : 1][NP];  // LayerNorm: sum dy (dbeta)
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
@@ -102,6 +117,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
         for (int k = 0; k < NP; ++k) {
             wp[v][k] = has_w ? Pk::add(o2, wv[k]) : make_float2(1.f, 1.f);
             acc[v][k] = make_float2(0.f, 0.f);
+            if constexpr (LN) accb[v][k] = make_float2(0.f, 0.f);
         }
     }
 
@@ -116,28 +132,42 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     const int64_t iters = (p.M - unit * TEAMS + G - 1) / G;
 
     uint4 xb[B][V], db[B][V], rb[BR][V];
-    float rs[B];
+    float rs[B], mus[B];
 
-    constexpr uint32_t kSlotBytes = CS * W * 4;  // one row's partials from the whole cluster
+    constexpr uint32_t kSlotBytes = CS * W * sizeof(RT);  // one row's partials from the whole cluster
     bool failed = false;
 
-    auto process = [&](uint4 (&xv)[V], uint4 (&dv)[V], uint4 (&rv)[V], float r, int64_t k) {
+    auto process = [&](uint4 (&xv)[V], uint4 (&dv)[V], uint4 (&rv)[V], float r, float mu, int64_t k) {
         const int64_t row = first + k * G;
         const bool valid = row < p.M;
         const float2 r2 = make_float2(r, r);
-        // pass 1: sum of g * x (g = dy (offset + w)); even and odd columns
-        // accumulate in separate lanes and are folded before the reduction
-        float2 dot = make_float2(0.f, 0.f);
+        const float2 nmu2 = make_float2(-mu, -mu);  // LayerNorm: x - mean as x + (-mean)
+        // the row's xhat for this pair of columns
+        auto xhat = [&](float2 xf) { return LN ? Pk::mul(Pk::add(xf, nmu2), r2) : Pk::mul(xf, r2); };
+        // pass 1: sum of g * x (g = dy (offset + w)); LayerNorm: the pair
+        // (sum g, sum g (x - mean)). Even and odd columns accumulate in
+        // separate lanes and are folded before the reduction.
+        float2 dot = make_float2(0.f, 0.f), gsum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             float2 xf[NP], df[NP];
             unpack<T>(xv[v], xf);
             unpack<T>(dv[v], df);
 #pragma unroll
-            for (int q = 0; q < NP; ++q) dot = Pk::fma(Pk::mul(df[q], wp[v][q]), xf[q], dot);
+            for (int q = 0; q < NP; ++q) {
+                const float2 g = Pk::mul(df[q], wp[v][q]);
+                if constexpr (LN) {
+                    dot = Pk::fma(g, Pk::add(xf[q], nmu2), dot);
+                    gsum = Pk::add(gsum, g);
+                } else {
+                    dot = Pk::fma(g, xf[q], dot);
+                }
+            }
         }
-        const float part = __fadd_rn(dot.x, dot.y);
-        float s;
+        RT part;
+        if constexpr (LN) part = make_float2(__fadd_rn(gsum.x, gsum.y), __fadd_rn(dot.x, dot.y));
+        else part = __fadd_rn(dot.x, dot.y);
+        RT s;
         if constexpr (CS > 1) {
             // Split-phase row sum across the cluster. Row k uses slot buffer
             // b = k & 1, whose barrier phase for it has parity (k >> 1) & 1.
@@ -147,36 +177,58 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             // warp of the row has sent its row k + 1 partial, which each
             // warp does after reading buffer b for row k.
             const int b = (int)(k & 1);
-            float wsum = part;
+            RT wsum = part;
+            if constexpr (LN) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(0xffffffffu, wsum, o));
+                for (int o = 16; o > 0; o >>= 1) wsum = add2(wsum, shfl_xor2(wsum, o));
+            } else {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(0xffffffffu, wsum, o));
+            }
             if ((t & 31) == 0) {
 #pragma unroll
-                for (int c = 0; c < CS; ++c)
-                    st_async_cluster(&red[b][0][rank * W + (t >> 5)], &rbar[b][0], (uint32_t)c, wsum);
+                for (int c = 0; c < CS; ++c) {
+                    if constexpr (LN)
+                        st_async_cluster2(&red[b][0][rank * W + (t >> 5)], &rbar[b][0], (uint32_t)c, wsum);
+                    else
+                        st_async_cluster(&red[b][0][rank * W + (t >> 5)], &rbar[b][0], (uint32_t)c, wsum);
+                }
             }
-            // while the partials travel: the dW partial, which does not
-            // need the row sum
-            if (valid && has_w) {
+            // while the partials travel: the parameter partials, which do
+            // not need the row sums
+            if (valid && want_acc) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     float2 xf[NP], df[NP];
                     unpack<T>(xv[v], xf);
                     unpack<T>(dv[v], df);
 #pragma unroll
-                    for (int q = 0; q < NP; ++q) acc[v][q] = Pk::fma(df[q], Pk::mul(xf[q], r2), acc[v][q]);
+                    for (int q = 0; q < NP; ++q) {
+                        acc[v][q] = Pk::fma(df[q], xhat(xf[q]), acc[v][q]);
+                        if constexpr (LN) accb[v][q] = Pk::add(accb[v][q], df[q]);
+                    }
                 }
             }
             if (!mbar_wait(&rbar[b][0], (uint32_t)((k >> 1) & 1), kWaitLimit)) failed = true;
-            s = sum_slots<CS * W>(&red[b][0][0], t & 31);
+            if constexpr (LN) s = sum_slots2<CS * W>(&red[b][0][0], t & 31);
+            else s = sum_slots<CS * W>(&red[b][0][0], t & 31);
             // re-arm this buffer for row k + 2 (its phase for row k is done)
             if (t == 0) mbar_arrive_expect_tx(&rbar[b][0], kSlotBytes);
         } else {
-            s = team_allreduce<TPR>(part, &red[k & 1][team][0], t);
+            if constexpr (LN) s = team_allreduce2<TPR>(part, &red[k & 1][team][0], t);
+            else s = team_allreduce<TPR>(part, &red[k & 1][team][0], t);
         }
-        // c = (1/N) sum g xhat = rstd * (sum g x) / N
-        const float cm = -__fdiv_rn(__fmul_rn(s, r), (float)N);
+        // c = (1/N) sum g xhat = rstd * (sum g x) / N  (LayerNorm: sum g (x - mean));
+        // LayerNorm also subtracts mean(g) = (sum g) / N
+        float cm, nmg = 0.f;
+        if constexpr (LN) {
+            cm = -__fdiv_rn(__fmul_rn(s.y, r), (float)N);
+            nmg = -__fdiv_rn(s.x, (float)N);
+        } else {
+            cm = -__fdiv_rn(__fmul_rn(s, r), (float)N);
+        }
         const float2 nc2 = make_float2(cm, cm);
+        const float2 nmg2 = make_float2(nmg, nmg);
         // pass 2: dx = rstd (g - xhat c) [+ dres], stored directly; dW partial
         const int64_t base = (valid ? row : p.M - 1) * C;
 #pragma unroll
@@ -187,10 +239,14 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             unpack<T>(dv[v], df);
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
-                const float2 xh = Pk::mul(xf[q], r2);
-                const float2 g = Pk::mul(df[q], wp[v][q]);
+                const float2 xh = xhat(xf[q]);
+                float2 g = Pk::mul(df[q], wp[v][q]);
+                if constexpr (LN) g = Pk::add(g, nmg2);
                 out[q] = Pk::mul(Pk::fma(xh, nc2, g), r2);
-                if (CS == 1 && valid && has_w) acc[v][q] = Pk::fma(df[q], xh, acc[v][q]);
+                if (CS == 1 && valid && want_acc) {
+                    acc[v][q] = Pk::fma(df[q], xh, acc[v][q]);
+                    if constexpr (LN) accb[v][q] = Pk::add(accb[v][q], df[q]);
+                }
             }
             if (has_dres) {
                 float2 rf[NP];
@@ -217,8 +273,8 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 #pragma unroll
     for (int s = 0; s < D; ++s)
         if (s < iters)
-            bwd_load_row<T, TPR, V>(p, first + s * G, C, cbase, t, has_dres, xb[s], db[s], rb[FUSED ? s : 0],
-                                    rs[s]);
+            bwd_load_row<T, TPR, V, LN>(p, first + s * G, C, cbase, t, has_dres, xb[s], db[s],
+                                        rb[FUSED ? s : 0], rs[s], mus[s]);
     // every CTA of the cluster runs, with its barriers initialised, before
     // any peer stores into its shared memory
     if constexpr (CS > 1) cluster_sync();
@@ -231,9 +287,9 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                 // slot (s + D) % B held row k - 1, already done: refill it with row k + D
                 const int sn = (s + D) % B;
                 if (k + D < iters)
-                    bwd_load_row<T, TPR, V>(p, first + (k + D) * G, C, cbase, t, has_dres, xb[sn], db[sn],
-                                            rb[FUSED ? sn : 0], rs[sn]);
-                process(xb[s], db[s], rb[FUSED ? s : 0], rs[s], k);
+                    bwd_load_row<T, TPR, V, LN>(p, first + (k + D) * G, C, cbase, t, has_dres, xb[sn], db[sn],
+                                                rb[FUSED ? sn : 0], rs[sn], mus[sn]);
+                process(xb[s], db[s], rb[FUSED ? s : 0], rs[s], mus[s], k);
                 if (failed) break;
             }
         }
@@ -250,11 +306,12 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     // finish (griddepcontrol.wait) before it reads the workspace.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (!has_w) return;  // non-affine: no dW partials
+    if (!want_acc) return;  // no parameter partials (non-affine)
 
     // Combine the CTA's teams in team order, then write the unit's partial
-    // row ws[unit, :] (a cluster's CTAs each write their slice of it).
-    float *wsrow = p.ws + unit * N;
+    // row(s) ws[unit, :] (a cluster's CTAs each write their slice of it).
+    // LayerNorm rows hold dgamma in [0, N) and dbeta in [N, 2N).
+    float *wsrow = p.ws + unit * (int64_t)(NACC * N);
     if constexpr (TEAMS > 1) {
         float *comb = reinterpret_cast<float *>(comb_smem);
         if (team > 0) {
@@ -262,11 +319,15 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             for (int v = 0; v < V; ++v) {
                 const int c = v * TPR + t;
                 if (c < C) {
-                    float *d = comb + (int64_t)(team - 1) * N + c * E;
+                    float *d = comb + (int64_t)(team - 1) * NACC * N + c * E;
 #pragma unroll
                     for (int q = 0; q < NP; ++q) {
                         d[2 * q] = acc[v][q].x;
                         d[2 * q + 1] = acc[v][q].y;
+                        if constexpr (LN) {
+                            d[N + 2 * q] = accb[v][q].x;
+                            d[N + 2 * q + 1] = accb[v][q].y;
+                        }
                     }
                 }
             }
@@ -278,10 +339,13 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             const int c = v * TPR + t;
             if (c < C) {
                 for (int tm = 1; tm < TEAMS; ++tm) {
-                    const float *s2 = comb + (int64_t)(tm - 1) * N + c * E;
+                    const float *s2 = comb + (int64_t)(tm - 1) * NACC * N + c * E;
 #pragma unroll
-                    for (int q = 0; q < NP; ++q)
+                    for (int q = 0; q < NP; ++q) {
                         acc[v][q] = Pk::add(acc[v][q], make_float2(s2[2 * q], s2[2 * q + 1]));
+                        if constexpr (LN)
+                            accb[v][q] = Pk::add(accb[v][q], make_float2(s2[N + 2 * q], s2[N + 2 * q + 1]));
+                    }
                 }
             }
         }
@@ -294,8 +358,25 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 #pragma unroll
             for (int q = 0; q < NP / 2; ++q)
                 d[q] = make_float4(acc[v][2 * q].x, acc[v][2 * q].y, acc[v][2 * q + 1].x, acc[v][2 * q + 1].y);
+            if constexpr (LN) {
+                float4 *db4 = reinterpret_cast<float4 *>(wsrow + N + c * E);
+#pragma unroll
+                for (int q = 0; q < NP / 2; ++q)
+                    db4[q] = make_float4(accb[v][2 * q].x, accb[v][2 * q].y, accb[v][2 * q + 1].x,
+                                         accb[v][2 * q + 1].y);
+            }
         }
     }
+}
+
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool FUSED>
+__global__ void __launch_bounds__(TPR *TEAMS) rmsnorm_bwd_vector(const BwdParams p) {
+    bwd_vector_body<T, TW, TPR, V, TEAMS, D, CS, PACKED, FUSED, false>(p);
+}
+
+template <typename T, int TPR, int V, int TEAMS, int D, int CS, bool FUSED>
+__global__ void __launch_bounds__(TPR *TEAMS) layernorm_bwd_vector(const BwdParams p) {
+    bwd_vector_body<T, T, TPR, V, TEAMS, D, CS, true, FUSED, true>(p);
 }
 
 // Generic main kernel: one 256-thread CTA per row at a time, element loads,
@@ -337,6 +418,50 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
     }
 }
 
+// Generic LayerNorm backward, same scheme: per row the pair (sum g,
+// sum g (x - mean)), then dx; the partial row ws[cta, 0..2N) holds dgamma
+// and dbeta, each column owned by one thread.
+template <typename T, bool FUSED>
+__global__ void __launch_bounds__(256) layernorm_bwd_generic(const BwdParams p) {
+    __shared__ float2 red[32];
+    const int N = p.N;
+    const T *w = reinterpret_cast<const T *>(p.w);
+    float *wsrow = p.ws ? p.ws + (int64_t)blockIdx.x * 2 * N : nullptr;
+    const bool has_dres = FUSED && p.dres != nullptr;
+    bool first = true;
+    for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+        const T *x = reinterpret_cast<const T *>(p.x) + row * N;
+        const T *dy = reinterpret_cast<const T *>(p.dy) + row * N;
+        const T *dr = reinterpret_cast<const T *>(p.dres) + row * N;
+        T *dx = reinterpret_cast<T *>(p.dx) + row * N;
+        const float r = p.rstd[row];
+        const float nmu = -p.mean[row];
+        float2 part = make_float2(0.f, 0.f);
+        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+            const float dyj = load_elem(dy, j);
+            const float g = w ? __fmul_rn(dyj, __fadd_rn(p.offset, load_w(w, j))) : dyj;
+            part.x = __fadd_rn(part.x, g);
+            part.y = __fmaf_rn(g, __fadd_rn(load_elem(x, j), nmu), part.y);
+        }
+        const float2 s = cta_allreduce2(part, red);
+        const float cm = -__fdiv_rn(__fmul_rn(s.y, r), (float)N);
+        const float nmg = -__fdiv_rn(s.x, (float)N);
+        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+            const float dyj = load_elem(dy, j);
+            const float xh = __fmul_rn(__fadd_rn(load_elem(x, j), nmu), r);
+            const float g = w ? __fmul_rn(dyj, __fadd_rn(p.offset, load_w(w, j))) : dyj;
+            float d = __fmul_rn(__fmaf_rn(xh, cm, __fadd_rn(g, nmg)), r);
+            if (has_dres) d = __fadd_rn(d, load_elem(dr, j));
+            store_elem(dx, j, d);
+            if (wsrow) {
+                wsrow[j] = first ? __fmul_rn(dyj, xh) : __fmaf_rn(dyj, xh, wsrow[j]);
+                wsrow[N + j] = first ? dyj : __fadd_rn(wsrow[N + j], dyj);
+            }
+        }
+        first = false;
+    }
+}
+
 // Finalizer. When launched as a programmatic dependent of the main kernel
 // it starts early and waits here until the main grid has completed and its
 // workspace writes are visible; otherwise the wait returns at once.
@@ -346,8 +471,20 @@ __device__ __forceinline__ void wait_for_main_grid() { asm volatile("griddepcont
 // splits the P partial rows into 32 groups; group q sums rows
 // [q P / 32, (q+1) P / 32) in order, then each column adds the 32 group sums
 // in order. A few float4 loads per thread keep the L2 round trips short.
+// Columns c < split go to out0[c], the rest to out1[c - split] (a NULL
+// output's columns are not written); N is the workspace's row length.
 template <typename T>
-__global__ void __launch_bounds__(256) rmsnorm_dw_finalize4(const float *ws, int parts, int N, T *dw) {
+__device__ __forceinline__ void store_param(T *out0, T *out1, int split, int c, float v) {
+    if (c < split) {
+        if (out0) store_elem(out0, c, v);
+    } else if (out1) {
+        store_elem(out1, c - split, v);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_dw_finalize4(const float *ws, int parts, int N, T *dw, T *dw1,
+                                                            int split) {
     constexpr int RG = 32;
     __shared__ float part[RG][33];
     wait_for_main_grid();
@@ -380,7 +517,7 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize4(const float *ws, int
             float tot = part[0][threadIdx.x];
 #pragma unroll
             for (int g = 1; g < RG; ++g) tot = __fadd_rn(tot, part[g][threadIdx.x]);
-            store_elem(dw, c, tot);
+            store_param(dw, dw1, split, c, tot);
         }
     }
 }
@@ -388,7 +525,8 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize4(const float *ws, int
 // Scalar finalizer for any N: 32 columns per CTA, 8 groups of partial rows,
 // same fixed order rules.
 template <typename T>
-__global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int parts, int N, T *dw) {
+__global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int parts, int N, T *dw, T *dw1,
+                                                           int split) {
     constexpr int RG = 8;
     __shared__ float part[RG][32];
     wait_for_main_grid();
@@ -409,7 +547,7 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int 
         float tot = part[0][lane];
 #pragma unroll
         for (int g = 1; g < RG; ++g) tot = __fadd_rn(tot, part[g][lane]);
-        store_elem(dw, col, tot);
+        store_param(dw, dw1, split, col, tot);
     }
 }
 
@@ -515,7 +653,8 @@ static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
 // (its launch overlaps the main kernel's tail) unless `serial` asks for a
 // plain launch (when the caller records an event between the two).
 template <typename T>
-static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *stream, bool serial) {
+static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *dw1, int split, void *stream,
+                             bool serial) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((N + 31) / 32));
     cfg.blockDim = dim3(256);
@@ -527,9 +666,96 @@ static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *
     cfg.attrs = attr;
     cfg.numAttrs = serial ? 0 : 1;
     T *out = static_cast<T *>(dw);
-    cudaError_t e = (N % 4 == 0) ? cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize4<T>, ws, parts, N, out)
-                                 : cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize<T>, ws, parts, N, out);
+    T *out1 = static_cast<T *>(dw1);
+    // float4 columns need every group of 4 on one side of the split
+    const bool vec = N % 4 == 0 && split % 4 == 0;
+    cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize4<T>, ws, parts, N, out, out1, split)
+                        : cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize<T>, ws, parts, N, out, out1, split);
     return (int)e;
+}
+
+// ------------------------------------------------- LayerNorm dispatch --
+
+template <typename T, int TPR, int V, int TEAMS, int D, int CS>
+static int ln_bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
+    if constexpr (CS == 1) {
+        if (fused)
+            layernorm_bwd_vector<T, TPR, V, TEAMS, D, 1, true><<<grid, TPR * TEAMS, smem, s>>>(p);
+        else
+            layernorm_bwd_vector<T, TPR, V, TEAMS, D, 1, false><<<grid, TPR * TEAMS, smem, s>>>(p);
+        return (int)cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(TPR * TEAMS);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return fused ? (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true>, p)
+                     : (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false>, p);
+    }
+}
+
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
+static int ln_bwd_launch_entry(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
+    if constexpr (OP != OP_LN_BWD) {
+        return (int)cudaErrorInvalidValue;
+    } else if constexpr (PATH == PATH_GENERIC) {
+        if (fused)
+            layernorm_bwd_generic<T, true><<<grid, 256, 0, s>>>(p);
+        else
+            layernorm_bwd_generic<T, false><<<grid, 256, 0, s>>>(p);
+        return (int)cudaGetLastError();
+    } else if constexpr (PATH == PATH_VECTOR) {
+        return ln_bwd_launch_vec<T, TPR, V, TEAMS, D, CS>(fused, p, grid, smem, s);
+    } else {
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
+static const void *ln_bwd_ptr_entry(bool fused) {
+    if constexpr (OP != OP_LN_BWD) {
+        return nullptr;
+    } else if constexpr (PATH == PATH_GENERIC) {
+        return fused ? (const void *)layernorm_bwd_generic<T, true> : (const void *)layernorm_bwd_generic<T, false>;
+    } else if constexpr (PATH == PATH_VECTOR) {
+        return fused ? (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true>
+                     : (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false>;
+    } else {
+        return nullptr;
+    }
+}
+
+template <typename T>
+static int ln_bwd_launch_t(int plan_id, bool fused, const BwdParams &p, int grid, int smem, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (plan_id) {
+#define RMSN_LN_BWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
+    case id: return ln_bwd_launch_entry<T, op, path, tpr, v, teams, depth, cs>(fused, p, grid, smem, s);
+        RMSNORM_PLAN_TABLE(RMSN_LN_BWD_CASE)
+#undef RMSN_LN_BWD_CASE
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+static const void *ln_bwd_ptr_t(int plan_id, bool fused) {
+    switch (plan_id) {
+#define RMSN_LN_BWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
+    case id: return ln_bwd_ptr_entry<T, op, path, tpr, v, teams, depth, cs>(fused);
+        RMSNORM_PLAN_TABLE(RMSN_LN_BWD_PTR)
+#undef RMSN_LN_BWD_PTR
+    default:
+        return nullptr;
+    }
 }
 
 }  // namespace rmsn

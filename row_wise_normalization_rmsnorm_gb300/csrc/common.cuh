@@ -370,6 +370,68 @@ __device__ __forceinline__ float cluster_allreduce(float v, float *red, int t, u
     return cluster_allreduce_end<TPR, CS, Op>(red, t);
 }
 
+// ------------------------------------------------- two sums at once --
+// The same reductions on a pair of sums (the LayerNorm backward's sum of g
+// and sum of g (x - mean)); each component is combined exactly as the
+// single-value versions combine theirs.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y)); }
+__device__ __forceinline__ float2 shfl_xor2(float2 v, int o) {
+    return make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
+}
+
+template <int S>
+__device__ __forceinline__ float2 sum_slots2(const float2 *red, int lane) {
+    static_assert((S & (S - 1)) == 0, "slot count must be a power of two");
+    float2 s;
+    if constexpr (S <= 32) {
+        s = red[lane & (S - 1)];
+    } else {
+        s = red[lane];
+#pragma unroll
+        for (int j = 1; j < S / 32; ++j) s = add2(s, red[lane + 32 * j]);
+    }
+    constexpr int WIDTH = S < 32 ? S : 32;
+#pragma unroll
+    for (int o = WIDTH / 2; o > 0; o >>= 1) s = add2(s, shfl_xor2(s, o));
+    return s;
+}
+
+template <int TPR>
+__device__ __forceinline__ float2 team_allreduce2(float2 v, float2 *red, int t) {
+    constexpr int WIDTH = TPR < 32 ? TPR : 32;
+#pragma unroll
+    for (int o = WIDTH / 2; o > 0; o >>= 1) v = add2(v, shfl_xor2(v, o));
+    if constexpr (TPR > 32) {
+        constexpr int W = TPR / 32;
+        if ((t & 31) == 0) red[t >> 5] = v;
+        __syncthreads();
+        v = sum_slots2<W>(red, t & 31);
+    }
+    return v;
+}
+
+__device__ __forceinline__ float2 cta_allreduce2(float2 v, float2 *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = add2(v, shfl_xor2(v, o));
+    const int W = blockDim.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float2 s = red[0];
+    for (int i = 1; i < W; ++i) s = add2(s, red[i]);
+    __syncthreads();  // red is reused by the next call
+    return s;
+}
+
+// st_async_cluster for a pair: 8 bytes counted on the receiver's barrier.
+__device__ __forceinline__ void st_async_cluster2(float2 *local_slot, uint64_t *local_bar, uint32_t cta, float2 v) {
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local_slot)), "r"(cta));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(local_bar)), "r"(cta));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(ra),
+                 "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(rb)
+                 : "memory");
+}
+
 // ------------------------------------------------------------ E4M3 out --
 // Two fp32 values to two E4M3 codes (nearest-even, saturating to +-448):
 // a.x in the low byte. Four values packed into 32 bits, lowest first.

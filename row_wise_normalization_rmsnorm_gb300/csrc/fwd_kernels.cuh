@@ -21,6 +21,44 @@
 
 namespace rmsn {
 
+// The row's chunks into registers; with FUSED, h = R(x + residual) is
+// formed in place and stored to residual_out. Chunks past the row are zero.
+template <typename T, int TPR, int V, bool FUSED>
+__device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, int cbase, int t, int C, bool valid,
+                                             uint4 (&xv)[V]) {
+    using Pk = Pair<true>;
+    constexpr int NP = Elem<T>::NP;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = cbase + v * TPR + t;
+        xv[v] = c < C ? ld_stream(reinterpret_cast<const uint4 *>(p.x) + base + c) : make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (FUSED) {
+        // h = R(x + residual). For bf16 inputs the fp32 sum is exact unless
+        // the exponents differ by more than 15, and then both it and the
+        // exact sum round to the larger operand: one rounding to bf16 gives
+        // the correctly rounded sum. For fp32 the add is the rounding.
+        uint4 rv[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = cbase + v * TPR + t;
+            rv[v] = c < C ? ld_stream(reinterpret_cast<const uint4 *>(p.residual) + base + c)
+                          : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float2 a[NP], b[NP];
+            unpack<T>(xv[v], a);
+            unpack<T>(rv[v], b);
+#pragma unroll
+            for (int k = 0; k < NP; ++k) a[k] = Pk::add(a[k], b[k]);
+            xv[v] = pack<T>(a);
+            const int c = cbase + v * TPR + t;
+            if (valid && c < C) st_chunk(reinterpret_cast<uint4 *>(p.residual_out) + base + c, xv[v]);
+        }
+    }
+}
+
 // CS > 1: the CTAs of a cluster share one row; CTA rank r holds chunks
 // [r TPR V, (r+1) TPR V) and the sum of squares meets in distributed shared
 // memory (wide rows whose chunks exceed one CTA's registers).
@@ -55,35 +93,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     const int64_t base = rr * C;
 
     uint4 xv[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-        const int c = cbase + v * TPR + t;
-        xv[v] = c < C ? ld_stream(reinterpret_cast<const uint4 *>(p.x) + base + c) : make_uint4(0, 0, 0, 0);
-    }
-    if constexpr (FUSED) {
-        // h = R(x + residual). For bf16 inputs the fp32 sum is exact unless
-        // the exponents differ by more than 15, and then both it and the
-        // exact sum round to the larger operand: one rounding to bf16 gives
-        // the correctly rounded sum. For fp32 the add is the rounding.
-        uint4 rv[V];
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-            const int c = cbase + v * TPR + t;
-            rv[v] = c < C ? ld_stream(reinterpret_cast<const uint4 *>(p.residual) + base + c)
-                          : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-            float2 a[NP], b[NP];
-            unpack<T>(xv[v], a);
-            unpack<T>(rv[v], b);
-#pragma unroll
-            for (int k = 0; k < NP; ++k) a[k] = Pk::add(a[k], b[k]);
-            xv[v] = pack<T>(a);
-            const int c = cbase + v * TPR + t;
-            if (valid && c < C) st_chunk(reinterpret_cast<uint4 *>(p.residual_out) + base + c, xv[v]);
-        }
-    }
+    fwd_load_row<T, TPR, V, FUSED>(p, base, cbase, t, C, valid, xv);
 
     float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
@@ -235,6 +245,153 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     }
 }
 
+// LayerNorm forward on the RMSNorm forward's geometry: the row stays in
+// registers through two row reductions, the sum (for the mean) and then the
+// sum of squared deviations from it (a two-pass variance, which loses
+// nothing to cancellation when the mean is large), then
+// y = (h - mean) rstd (offset + gamma) + beta, rounded once.
+template <typename T, int TPR, int V, int TEAMS, int CS, bool FUSED>
+__global__ void __launch_bounds__(TPR *TEAMS)
+    layernorm_fwd_vector(const FwdParams p) {
+    static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
+    using Pk = Pair<true>;
+    constexpr int NP = Elem<T>::NP;
+    constexpr int W = TPR > 32 ? TPR / 32 : 1;
+    __shared__ float red[TEAMS][W * CS], red2[TEAMS][W * CS];
+
+    const int team = threadIdx.x / TPR;
+    const int t = threadIdx.x % TPR;
+    uint32_t rank = 0;
+    int64_t row;
+    if constexpr (CS > 1) {
+        rank = cluster_ctarank();
+        row = cluster_id_x();
+    } else {
+        row = (int64_t)blockIdx.x * TEAMS + team;
+    }
+    const int cbase = (int)rank * TPR * V;
+    const bool valid = row < p.M;
+    const int64_t rr = valid ? row : p.M - 1;
+    const int C = p.N / Elem<T>::E;
+    const int64_t base = rr * C;
+
+    uint4 xv[V];
+    fwd_load_row<T, TPR, V, FUSED>(p, base, cbase, t, C, valid, xv);
+
+    float2 sm = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        float2 a[NP];
+        unpack<T>(xv[v], a);  // chunks past the row are zero
+#pragma unroll
+        for (int k = 0; k < NP; ++k) sm = Pk::add(sm, a[k]);
+    }
+    float s;
+    if constexpr (CS > 1) {
+        cluster_sync();  // every CTA of the cluster runs before any distributed-shared store
+        s = cluster_allreduce<TPR, CS>(__fadd_rn(sm.x, sm.y), &red[0][0], t, rank);
+    } else {
+        s = team_allreduce<TPR>(__fadd_rn(sm.x, sm.y), &red[team][0], t);
+    }
+    const float mu = __fdiv_rn(s, (float)p.N);
+    const float2 nmu2 = make_float2(-mu, -mu);
+    float2 sq = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = cbase + v * TPR + t;
+        if (c < C) {
+            float2 a[NP];
+            unpack<T>(xv[v], a);
+#pragma unroll
+            for (int k = 0; k < NP; ++k) {
+                const float2 d = Pk::add(a[k], nmu2);
+                sq = Pk::fma(d, d, sq);
+            }
+        }
+    }
+    if constexpr (CS > 1) {
+        s = cluster_allreduce<TPR, CS>(__fadd_rn(sq.x, sq.y), &red2[0][0], t, rank);
+    } else {
+        s = team_allreduce<TPR>(__fadd_rn(sq.x, sq.y), &red2[team][0], t);
+    }
+    const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(s, (float)p.N), p.eps));
+    if (!valid) return;
+    if (t == 0 && rank == 0) {
+        p.rstd[row] = rstd;
+        p.mean[row] = mu;
+    }
+    const float2 r2 = make_float2(rstd, rstd);
+    const float2 o2 = make_float2(p.offset, p.offset);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = cbase + v * TPR + t;
+        if (c < C) {
+            float2 a[NP], gv[NP], bv[NP];
+            unpack<T>(xv[v], a);
+            if (p.w) {
+                unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.w) + c), gv);
+#pragma unroll
+                for (int k = 0; k < NP; ++k) gv[k] = Pk::add(o2, gv[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < NP; ++k) gv[k] = make_float2(1.f, 1.f);
+            }
+            if (p.beta) {
+                unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.beta) + c), bv);
+            } else {
+#pragma unroll
+                for (int k = 0; k < NP; ++k) bv[k] = make_float2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < NP; ++k) a[k] = Pk::fma(Pk::mul(Pk::add(a[k], nmu2), r2), gv[k], bv[k]);
+            st_chunk(reinterpret_cast<uint4 *>(p.y) + base + c, pack<T>(a));
+        }
+    }
+}
+
+// Generic LayerNorm forward: one 256-thread CTA per row, three passes over
+// the row (the later ones served by L1/L2).
+template <typename T, bool FUSED>
+__global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) {
+    __shared__ float red[32];
+    const int64_t row = blockIdx.x;
+    const int N = p.N;
+    const T *x = reinterpret_cast<const T *>(p.x) + row * N;
+    const T *res = reinterpret_cast<const T *>(p.residual) + row * N;
+    T *hout = reinterpret_cast<T *>(p.residual_out) + row * N;
+    const T *g = reinterpret_cast<const T *>(p.w);
+    const T *b = reinterpret_cast<const T *>(p.beta);
+    T *y = reinterpret_cast<T *>(p.y) + row * N;
+    // The same thread wrote hout[j], so it reads its own value back.
+    auto h_at = [&](int j) { return FUSED ? load_elem(static_cast<const T *>(hout), j) : load_elem(x, j); };
+
+    float sm = 0.f;
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        float h = load_elem(x, j);
+        if constexpr (FUSED) {
+            h = round_to(__fadd_rn(h, load_elem(res, j)), x);
+            store_elem(hout, j, h);
+        }
+        sm = __fadd_rn(sm, h);
+    }
+    const float mu = __fdiv_rn(cta_allreduce(sm, red), (float)N);
+    float sq = 0.f;
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        const float d = __fadd_rn(h_at(j), -mu);
+        sq = __fmaf_rn(d, d, sq);
+    }
+    const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(cta_allreduce(sq, red), (float)N), p.eps));
+    if (threadIdx.x == 0) {
+        p.rstd[row] = rstd;
+        p.mean[row] = mu;
+    }
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        const float xh = __fmul_rn(__fadd_rn(h_at(j), -mu), rstd);
+        const float f = g ? __fadd_rn(p.offset, load_elem(g, j)) : 1.f;
+        store_elem(y, j, __fmaf_rn(xh, f, b ? load_elem(b, j) : 0.f));
+    }
+}
+
 // ------------------------------------------------------------- dispatch --
 
 template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, int Q>
@@ -340,6 +497,54 @@ static int launch_q(int plan_id, bool fused, int mode, const FwdParams &p, int g
     if (mode == QOUT_FP8_TENSOR) return launch_t<T, T, QOUT_FP8_TENSOR>(plan_id, fused, p, grid, stream);
     if (mode == QOUT_FP8_ROW) return launch_t<T, T, QOUT_FP8_ROW>(plan_id, fused, p, grid, stream);
     return (int)cudaErrorInvalidValue;
+}
+
+// LayerNorm forward: the forward plans' geometry, default plans and the
+// generic one.
+template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
+static int ln_launch_entry(bool fused, const FwdParams &p, int grid, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if constexpr (OP != OP_FWD || !(PATH == PATH_GENERIC || CMIN > 0)) {
+        return (int)cudaErrorInvalidValue;
+    } else if constexpr (PATH == PATH_GENERIC) {
+        if (fused)
+            layernorm_fwd_generic<T, true><<<grid, 256, 0, s>>>(p);
+        else
+            layernorm_fwd_generic<T, false><<<grid, 256, 0, s>>>(p);
+        return (int)cudaGetLastError();
+    } else if constexpr (CS == 1) {
+        if (fused)
+            layernorm_fwd_vector<T, TPR, V, TEAMS, 1, true><<<grid, TPR * TEAMS, 0, s>>>(p);
+        else
+            layernorm_fwd_vector<T, TPR, V, TEAMS, 1, false><<<grid, TPR * TEAMS, 0, s>>>(p);
+        return (int)cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(TPR * TEAMS);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return fused ? (int)cudaLaunchKernelEx(&cfg, layernorm_fwd_vector<T, TPR, V, TEAMS, CS, true>, p)
+                     : (int)cudaLaunchKernelEx(&cfg, layernorm_fwd_vector<T, TPR, V, TEAMS, CS, false>, p);
+    }
+}
+
+template <typename T>
+static int ln_launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
+    switch (plan_id) {
+#define RMSN_LN_FWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
+    case id: return ln_launch_entry<T, op, path, tpr, v, teams, cs, cmin>(fused, p, grid, stream);
+        RMSNORM_PLAN_TABLE(RMSN_LN_FWD_CASE)
+#undef RMSN_LN_FWD_CASE
+    default:
+        return (int)cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace rmsn

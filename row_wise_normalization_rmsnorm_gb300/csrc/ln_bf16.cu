@@ -1,0 +1,13 @@
+// ln_bf16.cu -- LayerNorm forward and backward kernels for bf16.
+#include "bwd_kernels.cuh"
+#include "fwd_kernels.cuh"
+
+namespace rmsn {
+int launch_ln_fwd_bf16(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
+    return ln_launch_t<__nv_bfloat16>(plan_id, fused, p, grid, stream);
+}
+int launch_ln_bwd_bf16(int plan_id, bool fused, const BwdParams &p, int grid, int smem, void *stream) {
+    return ln_bwd_launch_t<__nv_bfloat16>(plan_id, fused, p, grid, smem, stream);
+}
+const void *ln_bwd_kernel_ptr_bf16(int plan_id, bool fused) { return ln_bwd_ptr_t<__nv_bfloat16>(plan_id, fused); }
+}  // namespace rmsn

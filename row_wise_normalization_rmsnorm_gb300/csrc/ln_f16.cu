@@ -1,0 +1,13 @@
+// ln_f16.cu -- LayerNorm forward and backward kernels for fp16.
+#include "bwd_kernels.cuh"
+#include "fwd_kernels.cuh"
+
+namespace rmsn {
+int launch_ln_fwd_f16(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
+    return ln_launch_t<__half>(plan_id, fused, p, grid, stream);
+}
+int launch_ln_bwd_f16(int plan_id, bool fused, const BwdParams &p, int grid, int smem, void *stream) {
+    return ln_bwd_launch_t<__half>(plan_id, fused, p, grid, smem, stream);
+}
+const void *ln_bwd_kernel_ptr_f16(int plan_id, bool fused) { return ln_bwd_ptr_t<__half>(plan_id, fused); }
+}  // namespace rmsn

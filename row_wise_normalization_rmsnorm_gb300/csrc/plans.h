@@ -16,7 +16,10 @@
 
 namespace rmsn {
 
-enum PlanOp { OP_FWD = 0, OP_BWD = 1 };
+// OP_FWD plans serve the RMSNorm and the LayerNorm forward; OP_LN_BWD
+// plans the LayerNorm backward, whose rows carry two sums and two parameter
+// gradients (more registers per chunk than the RMSNorm backward).
+enum PlanOp { OP_FWD = 0, OP_BWD = 1, OP_LN_BWD = 2 };
 enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2 };
 // Storage types a default plan applies to (bit 0: fp32, bit 1: bf16,
 // bit 2: fp16; DT_16 = both 2-byte types).
@@ -85,10 +88,26 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(54, OP_BWD, PATH_VECTOR ,  256, 2,  1, 1, 4, DT_ANY,     0,     0) \
     X(55, OP_BWD, PATH_VECTOR ,  128, 2,  1, 1, 4, DT_ANY,     0,     0) \
     /* backward main kernel, any N and alignment */ \
-    X(36, OP_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0)
+    X(36, OP_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0) \
+    /* LayerNorm backward main kernel, persistent, row in registers */ \
+    X(60, OP_LN_BWD, PATH_VECTOR,    8, 1, 32, 1, 1, DT_ANY,     1,     8) \
+    X(61, OP_LN_BWD, PATH_VECTOR,   16, 1, 16, 1, 1, DT_ANY,     9,    16) \
+    X(62, OP_LN_BWD, PATH_VECTOR,   32, 1,  8, 1, 1, DT_ANY,    17,    32) \
+    X(63, OP_LN_BWD, PATH_VECTOR,   64, 1,  4, 1, 1, DT_ANY,    33,    64) \
+    X(64, OP_LN_BWD, PATH_VECTOR,  128, 1,  2, 1, 1, DT_ANY,    65,   128) \
+    X(65, OP_LN_BWD, PATH_VECTOR,  256, 1,  1, 1, 1, DT_ANY,   129,   256) \
+    X(66, OP_LN_BWD, PATH_VECTOR,  512, 1,  1, 1, 1, DT_ANY,   257,   512) \
+    X(67, OP_LN_BWD, PATH_VECTOR,  512, 1,  1, 1, 2, DT_ANY,   513,  1024) \
+    X(68, OP_LN_BWD, PATH_VECTOR,  512, 1,  1, 1, 4, DT_ANY,  1025,  2048) \
+    X(69, OP_LN_BWD, PATH_VECTOR,  512, 1,  1, 1, 8, DT_ANY,  2049,  4096) \
+    X(70, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 8, DT_ANY,  4097,  8192) \
+    X(71, OP_LN_BWD, PATH_VECTOR,  512, 1,  1, 2, 1, DT_ANY,     0,     0) \
+    X(72, OP_LN_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0)
 
 // Largest CTA any plan uses.
 constexpr int kMaxCtaThreads = 1024;
+// Plan ids are below this bound (host caches are indexed by id).
+constexpr int kMaxPlanId = 96;
 
 struct FwdParams {
     const void *x;
@@ -107,6 +126,9 @@ struct FwdParams {
     const float *qscale;
     float *qscale_inv;
     unsigned int *qamax;
+    // LayerNorm: the bias (NULL: none) and the per-row mean output
+    const void *beta;
+    float *mean;
 };
 
 // Output of the forward: the activations' type, or E4M3 with a per-tensor
@@ -120,11 +142,12 @@ struct BwdParams {
     const float *rstd;
     const void *dres;        // fused only, may be NULL
     void *dx;
-    float *ws;               // [ctas, N] fp32 partial rows of dw
+    float *ws;               // [units, N] fp32 partial rows of dw (LayerNorm: [units, 2N], dgamma | dbeta)
     int *status;             // device word: set non-zero if a bounded wait gave up
     int64_t M;
     int N;
     float offset;
+    const float *mean;       // LayerNorm: the forward's per-row mean
 };
 
 // Codes written to BwdParams::status.
@@ -154,9 +177,25 @@ int launch_fwd8_f32(int plan_id, bool fused, int mode, const FwdParams &p, int g
 int launch_fwd8_bf16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
 int launch_fwd8_f16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
 
-// dW finalizers, by dW's storage type.
-int launch_dw_finalize_f32(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
-int launch_dw_finalize_bf16(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
-int launch_dw_finalize_f16(const float *ws, int parts, int N, void *dw, void *stream, bool serial);
+// Parameter-gradient finalizers, by the parameters' storage type: column
+// c < split of the [parts, ncols] workspace goes to out0[c], the others to
+// out1[c - split] (out1 may be NULL: those columns are not written).
+int launch_dw_finalize_f32(const float *ws, int parts, int ncols, void *out0, void *out1, int split, void *stream,
+                           bool serial);
+int launch_dw_finalize_bf16(const float *ws, int parts, int ncols, void *out0, void *out1, int split,
+                            void *stream, bool serial);
+int launch_dw_finalize_f16(const float *ws, int parts, int ncols, void *out0, void *out1, int split, void *stream,
+                           bool serial);
+
+// LayerNorm forward and backward main kernels (weight in the activations'
+// type; the default plans and the generic one).
+#define RMSN_DECLARE_LN(suf)                                                                               \
+    int launch_ln_fwd_##suf(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);         \
+    int launch_ln_bwd_##suf(int plan_id, bool fused, const BwdParams &p, int grid, int smem, void *stream); \
+    const void *ln_bwd_kernel_ptr_##suf(int plan_id, bool fused);
+RMSN_DECLARE_LN(f32)
+RMSN_DECLARE_LN(bf16)
+RMSN_DECLARE_LN(f16)
+#undef RMSN_DECLARE_LN
 
 }  // namespace rmsn

@@ -169,3 +169,44 @@ def check_rel(got, ref, rel, what):
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(got - ref)
     assert np.all(err <= rel * np.abs(ref)), f"{what}: worst rel {(err / np.maximum(np.abs(ref), 1e-300)).max()}"
+
+
+def check_ln_y(got: np.ndarray, ref: dict, dtype: str, h64: np.ndarray, factor: np.ndarray, bias: np.ndarray):
+    """LayerNorm y: as check_y, or -- where y comes from cancelling terms
+    (xhat (offset + gamma) against beta, or h against the mean) -- within
+    2^-24 (8 (|xhat f| + |beta|) + (N/256 + 56) rstd |f| mean|h|): the fp32
+    rounding of the two terms plus the fp32 error of the mean, carried
+    through rstd and the weight factor. Returns the elements that needed it."""
+    v = decode(got, dtype)
+    N = got.shape[-1]
+    xf = np.abs(ref["y64"] - bias[None, :])
+    mh = np.abs(h64).mean(axis=1, keepdims=True)
+    floor = 2.0 ** -24 * (8.0 * (xf + np.abs(bias)[None, :]) +
+                          (N / 256.0 + 56.0) * ref["rstd64"][:, None] * np.abs(factor)[None, :] * mh)
+    near = np.abs(v - ref["y64"]) <= floor
+    if dtype in ("bf16", "f16"):
+        ok = ulp16_distance(got, ref["y"]) <= 1
+    else:
+        r = ref["y64"]
+        ok = np.abs(v - r) <= 1e-5 * np.abs(r) + 1e-6
+    needed = int((~ok & near).sum())
+    ok = ok | near
+    assert ok.all(), f"y: {(~ok).sum()} elements off, first {v[~ok][0]!r} vs {ref['y64'][~ok][0]!r}"
+    return needed
+
+
+def check_ln_stats(mean: np.ndarray, rstd: np.ndarray, ref: dict, h64: np.ndarray):
+    """mean within the fp32 summation error (N/256 + 48) 2^-24 mean|h|;
+    rstd relative within (N/256 + 64) 2^-24 (the variance's summation error,
+    halved by the root, plus rsqrt's own)."""
+    N = h64.shape[-1]
+    mh = np.abs(h64).mean(axis=1)
+    tol = (N / 256.0 + 48.0) * 2.0 ** -24 * mh
+    err = np.abs(mean.astype(np.float64) - ref["mean64"])
+    assert np.all(err <= tol), f"mean: worst {(err / tol).max()} of tolerance"
+    rel = np.abs(rstd.astype(np.float64) - ref["rstd64"]) / ref["rstd64"]
+    assert rel.max() <= (N / 256.0 + 64.0) * 2.0 ** -24, f"rstd rel err {rel.max()}"
+
+
+def check_param_grad(got: np.ndarray, ref64: np.ndarray, ref_abs: np.ndarray, dtype: str):
+    return check_dw(got, {"dw64": ref64, "dw_abs": ref_abs}, dtype)

@@ -123,6 +123,35 @@ def test_fp32_weight_flag_plans(rn):
         rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16 | 0x200)
 
 
+@pytest.mark.parametrize("dt,N,tpr,v,cs", [(1, 64, 8, 1, 1), (1, 1024, 128, 1, 1), (1, 4096, 512, 1, 1),
+                                           (1, 8192, 512, 1, 2), (0, 8192, 512, 1, 4), (1, 65536, 512, 2, 8)])
+def test_layernorm_backward_plans(rn, dt, N, tpr, v, cs):
+    p = rn.plan_query(rn.OP_LN_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)
+    assert p["path_name"] == "vector"
+    assert (p["threads_per_row"], p["chunks_per_thread"], p["cluster_size"]) == (tpr, v, cs)
+    # two partial rows (dgamma | dbeta) per unit
+    assert p["workspace_bytes"] == (p["ws_rows"] * 2 * N * 4 + 255) // 256 * 256
+    assert rn.plan_query(rn.OP_LN_BWD, 100, N - 1, dt)["path_name"] == "generic"
+
+
+def test_layernorm_invalid_arguments_without_gpu(rn):
+    L = rn.lib()
+    x = ctypes.c_void_p(256)
+    r = ctypes.c_void_p(512)
+    # forward: residual without residual_out, missing mean, fp32 weight flag
+    assert L.layernorm_fwd(x, x, x, None, x, None, r, r, 4, 8, 1, 1e-5, 0.0, None) == 1
+    assert L.layernorm_fwd(x, None, x, None, x, None, None, r, 4, 8, 1, 1e-5, 0.0, None) == 1
+    assert L.layernorm_fwd(x, None, x, None, x, None, r, r, 4, 8, 0x101, 1e-5, 0.0, None) == 2
+    assert L.layernorm_fwd(x, None, x, None, x, None, r, r, 0, 8, 1, 1e-5, 0.0, None) == 0
+    # backward: dgamma without gamma, odd bf16 address, negative eps
+    assert L.layernorm_bwd(x, None, x, None, r, r, x, x, None, None, 0, 4, 8, 1, 1e-5, 0.0, None) == 1
+    assert L.layernorm_bwd(x, None, ctypes.c_void_p(257), x, r, r, x, x, x, None, 0, 4, 8, 1, 1e-5, 0.0,
+                           None) == 1
+    assert L.layernorm_bwd(x, None, x, x, r, r, x, x, x, None, 0, 4, 8, 1, -1.0, 0.0, None) == 1
+    # a forced alternative forward plan is not compiled for LayerNorm
+    assert L.layernorm_fwd_ex(x, None, x, None, x, None, r, r, 4, 2048, 1, 1e-5, 0.0, None, 9, None) == 2
+
+
 def test_misaligned_pointers_take_generic(rn):
     assert rn.plan_query(rn.OP_FWD, 4096, 7168, 1, aligned=False)["path_name"] == "generic"
     assert rn.plan_query(rn.OP_BWD, 4096, 2048, 0, aligned=False)["path_name"] == "generic"

@@ -1,0 +1,198 @@
+"""GPU parity of LayerNorm forward and backward against the fp64 oracle.
+
+The forward's y, mean and rstd are compared with the oracle's; the backward
+is fed the oracle forward's fp32 mean and rstd (inputs of the backward), and
+an end-to-end test runs both directions on the GPU against the exact
+gradient. Shapes cover every LayerNorm plan family: sub-warp and multi-warp
+teams, 512-thread rows, cluster rows, and the generic kernels.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import (check_dx, check_ln_stats, check_ln_y, check_param_grad, decode, empty_dev, to_dev,
+                     to_host, cuda_bits_equal)
+from row_wise_normalization_rmsnorm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rn():
+    from row_wise_normalization_rmsnorm_gb300 import build
+    build.build()
+    import row_wise_normalization_rmsnorm_gb300 as pkg
+    return pkg
+
+
+def _factor(d, dt, offset):
+    return offset + oracle.to_f64(d["w"], dt) if d.get("w") is not None else np.ones(d["x"].shape[1])
+
+
+def _ln_check(rn, d, dt, eps=1e-5, offset=0.0, fused=False, offset_elems=0, expect_path=None, gamma=True,
+              beta=True, want_dgamma=True, want_dbeta=True):
+    M, N = d["x"].shape
+    dg_np = d["w"] if gamma else None
+    b_np = d.get("beta") if beta else None
+    x = to_dev(d["x"], dt, offset=offset_elems)
+    g = to_dev(dg_np, dt, offset=offset_elems) if gamma else None
+    b = to_dev(b_np, dt, offset=offset_elems) if beta else None
+    y = empty_dev((M, N), dt, offset=offset_elems)
+    res = to_dev(d["residual"], dt, offset=offset_elems) if fused else None
+    hout = empty_dev((M, N), dt, offset=offset_elems) if fused else None
+    out = rn.layernorm_fwd(x, g, b, residual=res, residual_out=hout, y=y, eps=eps, offset=offset)
+    f = oracle.ln_fwd(d["x"], dg_np, b_np, dtype=dt, eps=eps, offset=offset,
+                      residual=d.get("residual") if fused else None)
+    torch.cuda.synchronize()
+    h_np = f["h"] if fused else d["x"]
+    h64 = oracle.to_f64(h_np, dt)
+    factor = (offset + oracle.to_f64(dg_np, dt)) if gamma else np.ones(N)
+    bias = oracle.to_f64(b_np, dt) if beta else np.zeros(N)
+    check_ln_y(to_host(y, dt), f, dt, h64, factor, bias)
+    check_ln_stats(out["mean"].cpu().numpy(), out["rstd"].cpu().numpy(), f, h64)
+    if fused:
+        assert np.array_equal(to_host(hout, dt), f["h"])
+
+    # backward, fed the oracle's fp32 statistics
+    m32 = torch.from_numpy(f["mean32"]).cuda()
+    r32 = torch.from_numpy(f["rstd32"]).cuda()
+    hdev = to_dev(h_np, dt, offset=offset_elems)
+    dy = to_dev(d["dy"], dt, offset=offset_elems)
+    dx = empty_dev((M, N), dt, offset=offset_elems)
+    dgam = empty_dev((N,), dt, offset=offset_elems) if (gamma and want_dgamma) else None
+    dbet = empty_dev((N,), dt, offset=offset_elems) if want_dbeta else None
+    dres_np = d.get("dres") if fused else None
+    dres = to_dev(dres_np, dt, offset=offset_elems) if dres_np is not None else None
+    bo = rn.layernorm_bwd(dy, hdev, g, m32, r32, dresidual_out=dres, eps=eps, offset=offset, dx=dx, dgamma=dgam,
+                          dbeta=dbet, want_dgamma=want_dgamma, want_dbeta=want_dbeta)
+    r = oracle.ln_bwd(d["dy"], h_np, dg_np, dtype=dt, eps=eps, offset=offset, mean=f["mean32"],
+                      rstd=f["rstd32"], dres=dres_np)
+    torch.cuda.synchronize()
+    needed = check_dx(to_host(dx, dt), r, dt)
+    if dgam is not None:
+        check_param_grad(to_host(dgam, dt), r["dg64"], r["dg_abs"], dt)
+    if dbet is not None:
+        check_param_grad(to_host(dbet, dt), r["db64"], r["db_abs"], dt)
+    if expect_path is not None:
+        assert out["plan"]["path_name"] == expect_path and bo["plan"]["path_name"] == expect_path
+    if N >= 64:
+        assert needed <= max(2, M * N // 20000), needed
+    return out, bo
+
+
+SHAPES = [(333, 64), (257, 1024), (300, 4096), (129, 8192), (65, 16384), (101, 8193), (40, 3), (5, 1)]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("M,N", SHAPES)
+def test_ln_shapes(rn, dt, M, N):
+    d = inputs.make_inputs(M, N, dt, 170 + N % 19, beta=True, x_shift=0.5)
+    es = 4 if dt == "f32" else 2
+    _ln_check(rn, d, dt, expect_path="vector" if (N * es) % 16 == 0 else "generic")
+
+
+@pytest.mark.parametrize("dt,N", [("bf16", 32768), ("bf16", 65536), ("f32", 16384), ("f32", 32768)])
+def test_ln_cluster_rows(rn, dt, N):
+    d = inputs.make_inputs(33, N, dt, 171, beta=True, x_shift=0.25)
+    _, bo = _ln_check(rn, d, dt, expect_path="vector")
+    assert bo["plan"]["cluster_size"] > 1
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+def test_ln_fused_add_gemma(rn, dt):
+    d = inputs.make_inputs(513, 4096, dt, 172, w_mode="gemma", residual=True, dres=True, beta=True)
+    _ln_check(rn, d, dt, offset=1.0, fused=True, expect_path="vector")
+
+
+@pytest.mark.parametrize("gamma,beta,want_dgamma,want_dbeta", [(False, False, False, False), (True, False, True, True),
+                                                                (False, True, False, True), (True, True, False, True),
+                                                                (True, True, True, False), (True, True, False, False)])
+def test_ln_optional_parameters(rn, gamma, beta, want_dgamma, want_dbeta):
+    d = inputs.make_inputs(300, 2048, "bf16", 173, beta=True, x_shift=1.0)
+    _ln_check(rn, d, "bf16", gamma=gamma, beta=beta, want_dgamma=want_dgamma, want_dbeta=want_dbeta,
+              expect_path="vector")
+
+
+def test_ln_misaligned_takes_generic(rn):
+    d = inputs.make_inputs(257, 2048, "bf16", 174, beta=True)
+    _ln_check(rn, d, "bf16", offset_elems=1, expect_path="generic")
+
+
+def test_ln_large_mean_two_pass_variance(rn):
+    # rows with mean 300 and unit spread: a one-pass E[x^2] - E[x]^2 in fp32
+    # would lose most of the variance's bits
+    d = inputs.make_inputs(256, 4096, "f32", 175, x_shift=300.0, beta=True)
+    _ln_check(rn, d, "f32", expect_path="vector")
+
+
+def test_ln_end_to_end_against_exact_gradient(rn):
+    for dt, M, N in (("bf16", 1024, 8192), ("f32", 512, 4096)):
+        d = inputs.make_inputs(M, N, dt, 176, beta=True, x_shift=0.5)
+        x, g, b, dy = (to_dev(d[k], dt) for k in ("x", "w", "beta", "dy"))
+        out = rn.layernorm_fwd(x, g, b)
+        bo = rn.layernorm_bwd(dy, x, g, out["mean"], out["rstd"])
+        torch.cuda.synchronize()
+        r = oracle.ln_bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=1e-5, offset=0.0)
+        # the GPU's statistics carry fp32 error: the floor grows accordingly
+        check_dx(to_host(bo["dx"], dt), r, dt, floor_mult=4.0)
+        check_param_grad(to_host(bo["dgamma"], dt), r["dg64"], r["dg_abs"], dt)
+        check_param_grad(to_host(bo["dbeta"], dt), r["db64"], r["db_abs"], dt)
+
+
+def test_ln_full_size_sampled(rn):
+    M, N = 16384, 8192
+    d = inputs.make_inputs(M, N, "bf16", inputs.SWEEP_SEED, beta=True, x_shift=0.5, outlier_frac=0.01)
+    x, g, b, dy = (to_dev(d[k], "bf16") for k in ("x", "w", "beta", "dy"))
+    out = rn.layernorm_fwd(x, g, b)
+    bo = rn.layernorm_bwd(dy, x, g, out["mean"], out["rstd"])
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(11).choice(M, 256, replace=False)
+    f = oracle.ln_fwd(d["x"][rows], d["w"], d["beta"], dtype="bf16", eps=1e-5, offset=0.0)
+    h64 = oracle.to_f64(d["x"][rows], "bf16")
+    check_ln_y(to_host(out["y"], "bf16")[rows], f, "bf16", h64, oracle.to_f64(d["w"], "bf16"),
+               oracle.to_f64(d["beta"], "bf16"))
+    check_ln_stats(out["mean"].cpu().numpy()[rows], out["rstd"].cpu().numpy()[rows], f, h64)
+    m, r_ = out["mean"].cpu().numpy(), out["rstd"].cpu().numpy()
+    rs = oracle.ln_bwd(d["dy"][rows], d["x"][rows], d["w"], dtype="bf16", eps=1e-5, offset=0.0, mean=m[rows],
+                       rstd=r_[rows])
+    check_dx(to_host(bo["dx"], "bf16")[rows], rs, "bf16")
+    full = oracle.ln_bwd(d["dy"], d["x"], d["w"], dtype="bf16", eps=1e-5, offset=0.0, mean=m, rstd=r_,
+                         want_dx=False, nthreads=8)
+    check_param_grad(to_host(bo["dgamma"], "bf16"), full["dg64"], full["dg_abs"], "bf16")
+    check_param_grad(to_host(bo["dbeta"], "bf16"), full["db64"], full["db_abs"], "bf16")
+    assert bo["plan"]["path_name"] == "vector" and bo["plan"]["cluster_size"] == 2
+
+
+def test_ln_dx_independent_of_cta_count(rn):
+    d = inputs.make_inputs(2048, 2048, "bf16", 177, beta=True)
+    x, g, dy = (to_dev(d[k], "bf16") for k in ("x", "w", "dy"))
+    out = rn.layernorm_fwd(x, g, None)
+    a = rn.layernorm_bwd(dy, x, g, out["mean"], out["rstd"], force_ctas=37)
+    b = rn.layernorm_bwd(dy, x, g, out["mean"], out["rstd"], force_ctas=152)
+    torch.cuda.synchronize()
+    assert a["plan"]["ctas"] == 37 and b["plan"]["ctas"] == 152
+    assert cuda_bits_equal(a["dx"], b["dx"])
+    da, db = a["dgamma"].float(), b["dgamma"].float()
+    assert torch.allclose(da, db, rtol=8e-3, atol=1e-3)
+
+
+def test_ln_fused_forward_equals_plain_forward_on_rounded_sum(rn):
+    d = inputs.make_inputs(300, 4096, "bf16", 178, residual=True, beta=True)
+    x, r, g, b = (to_dev(d[k], "bf16") for k in ("x", "residual", "w", "beta"))
+    fo = rn.layernorm_fwd(x, g, b, residual=r)
+    po = rn.layernorm_fwd(fo["residual_out"].clone(), g, b)
+    torch.cuda.synchronize()
+    assert cuda_bits_equal(fo["y"], po["y"]) and cuda_bits_equal(fo["rstd"], po["rstd"])
+    assert cuda_bits_equal(fo["mean"], po["mean"])
+
+
+def test_ln_empty_batch_zeroes_parameter_grads(rn):
+    x = torch.empty((0, 512), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(512, dtype=torch.bfloat16, device="cuda")
+    m = torch.empty(0, device="cuda")
+    dg = torch.full((512,), 3.0, dtype=torch.bfloat16, device="cuda")
+    db = torch.full((512,), 3.0, dtype=torch.bfloat16, device="cuda")
+    rn.layernorm_bwd(x, x, g, m, m, dgamma=dg, dbeta=db)
+    torch.cuda.synchronize()
+    assert torch.all(dg == 0) and torch.all(db == 0)
