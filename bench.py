@@ -276,6 +276,10 @@ def sweep_points():
     pts.append(("fp8row bf16 16384x8192", "bf16", 16384, 8192, False, False))
     pts.append(("fp8tensor bf16 16384x8192", "bf16", 16384, 8192, False, False))
     pts.append(("fp8row bf16 4096x4096", "bf16", 4096, 4096, False, False))
+    # LayerNorm (gamma and beta, dgamma and dbeta)
+    for dt, M, N in (("bf16", 16384, 8192), ("bf16", 4096, 4096), ("bf16", 16384, 2048), ("f32", 16384, 4096),
+                     ("bf16", 4096, 16384)):
+        pts.append((f"ln {dt} {M}x{N}", dt, M, N, False, False))
     pts.append(("misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
     pts.append(("misaligned f32 4096x2048", "f32", 4096, 2048, False, True))
     pts.append(("wide f32 16384x6144", "f32", 16384, 6144, False, False))
@@ -344,12 +348,30 @@ def run_sweep(args):
         _, _, _, fplan = rn.rmsnorm_fwd_ex(x, w, residual=res, residual_out=hout, y=y, rstd=rstd)
         _, _, bplan = rn.rmsnorm_bwd_ex(dy, hout if fused else x, w, rstd, dresidual_out=dres, fused=fused,
                                         dx=dx, dw=dw, workspace=ws)
-        P = bplan["ctas"]
+        P = bplan["ws_rows"]   # partial rows (a cluster shares one)
         k = 1 if fused else 0
         wb = 1 if affine else 0   # the weight, dW and the workspace exist only with a weight
         by = {"fwd": (2 + 2 * k) * M * N * s + wb * N * sw + 4 * M,
               "bwd": (3 + k) * M * N * s + wb * (2 * N * sw + 8 * P * N) + 4 * M}
         ops = (("fwd", fwd, fplan), ("bwd", bwd, bplan))
+        if label.startswith("ln "):
+            # LayerNorm: forward reads x, gamma, beta and writes y, mean, rstd;
+            # backward reads dy, x, gamma, mean, rstd, writes dx, and moves
+            # the [P, 2N] partial rows and dgamma, dbeta
+            bvec = (0.1 * mk(N).float()).to(td)
+            mean = torch.empty(M, dtype=torch.float32, device=dev)
+            dbv = torch.empty_like(bvec)
+            lnb = rn.layernorm_bwd_workspace_bytes(M, N, td)
+            lws = torch.empty(max(lnb, 256), dtype=torch.uint8, device=dev)
+            fwd = lambda: rn.layernorm_fwd(x, w, bvec, y=y, mean=mean, rstd=rstd)  # noqa: E731
+            bwd = lambda: rn.layernorm_bwd(dy, x, w, mean, rstd, dx=dx, dgamma=dw, dbeta=dbv,  # noqa: E731
+                                           workspace=lws)
+            fplan = fwd()["plan"]
+            bplan = bwd()["plan"]
+            P = bplan["ws_rows"]
+            by["fwd"] = 2 * M * N * s + 2 * N * s + 8 * M
+            by["bwd"] = 3 * M * N * s + N * s + 8 * M + 2 * (8 * P * N) + 2 * N * s
+            ops = (("fwd", fwd, fplan), ("bwd", bwd, bplan))
         if label.startswith("fp8"):
             # reads x and w, writes one byte per element, rstd and (per row) 1/s
             row = label.startswith("fp8row")
@@ -428,7 +450,7 @@ def main():
 
     _, _, _, fplan = rn.rmsnorm_fwd_ex(x, w, y=y, rstd=rstd, eps=eps)
     _, _, bplan = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dx=dx, dw=dw, workspace=ws, eps=eps)
-    P = bplan["ctas"]
+    P = bplan["ws_rows"]   # partial rows (a cluster shares one)
 
     K, W = args.steps, args.warmup
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]

@@ -150,7 +150,9 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     out->ctas = (int32_t)(P * d->cs);
     out->ctas_per_sm = ctas_per_sm;
     out->smem_bytes = bwd_smem_bytes(*d, N);
-    if (out->smem_bytes > 48 * 1024) return RMSNORM_ERR_UNSUPPORTED;
+    // dynamic shared memory stays below 48 KB with room for the kernels'
+    // static arrays (a few KB at most)
+    if (out->smem_bytes > 44 * 1024) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t bytes = P * partial_rows(op) * N * 4;
     out->workspace_bytes = (bytes + 255) / 256 * 256;
     return RMSNORM_SUCCESS;
@@ -311,7 +313,9 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
         if (e != cudaSuccess) return e;
         if (n < best) best = n;
     }
-    if (best < 1) best = 1;
+    // A kernel that cannot be resident at all (its shared memory or
+    // registers exceed an SM) must not run as one serial CTA: refuse it.
+    if (best < 1) return cudaErrorInvalidConfiguration;
     const int cps = (int)(((int64_t)best * d.cs + sms - 1) / sms);
     std::lock_guard<std::mutex> lk(g_occ_mutex);
     g_parts_cache[dev][dti][fi][slot] = best;

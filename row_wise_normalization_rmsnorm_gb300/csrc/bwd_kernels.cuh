@@ -101,11 +101,25 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     // passes a workspace (dgamma and/or dbeta requested)
     const bool want_acc = LN ? p.ws != nullptr : has_w;
     const float2 o2 = make_float2(p.offset, p.offset);
-    float2 wp[V][NP], acc[V][NP];
+    // The LayerNorm backward on 2-byte types keeps gamma as loaded (4
+    // registers a chunk instead of 8) and forms offset + gamma when used:
+    // the same fp32 add, so the same bits, and room for two chunks a thread.
+    constexpr bool RAWW = LN && std::is_same<T, TW>::value && Elem<T>::E == 8;
+    float2 wp[RAWW ? 1 : V][NP], acc[V][NP];
+    uint4 wraw[RAWW ? V : 1];
     float2 accb[LN ? V : 1][NP];  // LayerNorm: sum dy (dbeta)
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
+        if constexpr (RAWW) {
+            wraw[v] = (has_w && c < C) ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int k = 0; k < NP; ++k) {
+                acc[v][k] = make_float2(0.f, 0.f);
+                accb[v][k] = make_float2(0.f, 0.f);
+            }
+            continue;
+        }
         float2 wv[NP];
         if (has_w && c < C) {
             load_w_chunk<T, TW>(p.w, c, wv);
@@ -120,6 +134,17 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
             if constexpr (LN) accb[v][k] = make_float2(0.f, 0.f);
         }
     }
+    // the weight factors (offset + w) of chunk v
+    auto wfac = [&](int v, float2 (&f)[NP]) {
+        if constexpr (RAWW) {
+            unpack<T>(wraw[v], f);
+#pragma unroll
+            for (int k = 0; k < NP; ++k) f[k] = has_w ? Pk::add(o2, f[k]) : make_float2(1.f, 1.f);
+        } else {
+#pragma unroll
+            for (int k = 0; k < NP; ++k) f[k] = wp[v][k];
+        }
+    };
 
     // Every team of the CTA runs the same number of iterations (that of
     // team 0, which has the lowest first row) so the CTA-wide barrier in the
@@ -150,12 +175,13 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
         float2 dot = make_float2(0.f, 0.f), gsum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int v = 0; v < V; ++v) {
-            float2 xf[NP], df[NP];
+            float2 xf[NP], df[NP], wf[NP];
             unpack<T>(xv[v], xf);
             unpack<T>(dv[v], df);
+            wfac(v, wf);
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
-                const float2 g = Pk::mul(df[q], wp[v][q]);
+                const float2 g = Pk::mul(df[q], wf[q]);
                 if constexpr (LN) {
                     dot = Pk::fma(g, Pk::add(xf[q], nmu2), dot);
                     gsum = Pk::add(gsum, g);
@@ -237,10 +263,12 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
             float2 xf[NP], df[NP], out[NP];
             unpack<T>(xv[v], xf);
             unpack<T>(dv[v], df);
+            float2 wf[NP];
+            wfac(v, wf);
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
                 const float2 xh = xhat(xf[q]);
-                float2 g = Pk::mul(df[q], wp[v][q]);
+                float2 g = Pk::mul(df[q], wf[q]);
                 if constexpr (LN) g = Pk::add(g, nmg2);
                 out[q] = Pk::mul(Pk::fma(xh, nc2, g), r2);
                 if (CS == 1 && valid && want_acc) {

@@ -161,7 +161,7 @@ def test_ln_full_size_sampled(rn):
                          want_dx=False, nthreads=8)
     check_param_grad(to_host(bo["dgamma"], "bf16"), full["dg64"], full["dg_abs"], "bf16")
     check_param_grad(to_host(bo["dbeta"], "bf16"), full["db64"], full["db_abs"], "bf16")
-    assert bo["plan"]["path_name"] == "vector" and bo["plan"]["cluster_size"] == 2
+    assert bo["plan"]["path_name"] == "vector"
 
 
 def test_ln_dx_independent_of_cta_count(rn):
