@@ -104,7 +104,10 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     // The LayerNorm backward on 2-byte types keeps gamma as loaded (4
     // registers a chunk instead of 8) and forms offset + gamma when used:
     // the same fp32 add, so the same bits, and room for two chunks a thread.
-    constexpr bool RAWW = LN && std::is_same<T, TW>::value && Elem<T>::E == 8;
+    // The fp16 RMSNorm backward does the same (its fused variant otherwise
+    // spills); for bf16 RMSNorm holding the fp32 factors measured faster.
+    constexpr bool RAWW = std::is_same<T, TW>::value && Elem<T>::E == 8 &&
+                          (LN || std::is_same<T, __half>::value);
     float2 wp[RAWW ? 1 : V][NP], acc[V][NP];
     uint4 wraw[RAWW ? V : 1];
     float2 accb[LN ? V : 1][NP];  // LayerNorm: sum dy (dbeta)
