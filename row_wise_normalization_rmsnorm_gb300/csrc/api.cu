@@ -64,13 +64,14 @@ static int dtype_bit(int dt) {
     return base == RMSNORM_BF16 ? DT_BF16 : (base == RMSNORM_F16 ? DT_F16 : DT_F32);
 }
 
-// Default plan for (op, dtype, chunks per row); nullptr when no vector plan
-// covers C.
+// Default plan for (op, dtype, chunks per row): a row-in-registers
+// (vector) or staged plan; nullptr when none covers C.
+static bool row_path(int path) { return path == PATH_VECTOR || path == PATH_STAGED; }
+
 static const PlanDesc *default_vector_plan(int op, int dt, int64_t C) {
     for (int i = 0; i < kNumPlans; ++i) {
         const PlanDesc &d = kPlans[i];
-        if (d.op == op && d.path == PATH_VECTOR && d.cmin > 0 && (d.dtm & dtype_bit(dt)) && C >= d.cmin &&
-            C <= d.cmax)
+        if (d.op == op && row_path(d.path) && d.cmin > 0 && (d.dtm & dtype_bit(dt)) && C >= d.cmin && C <= d.cmax)
             return &d;
     }
     return nullptr;
@@ -83,6 +84,15 @@ static const PlanDesc *generic_plan(int op) {
 }
 
 static int cta_threads(const PlanDesc &d) { return d.path == PATH_GENERIC ? 256 : d.tpr * d.teams; }
+
+// Largest dynamic shared memory a CTA may take (227 KB on sm_103a).
+constexpr int kMaxDynamicSmem = 227 * 1024;
+
+// A staged plan's shared memory: `depth` stages of x and dy (and dres for
+// the fused variant) rows of es-byte elements.
+static int64_t staged_smem_bytes(const PlanDesc &d, int64_t N, int es, bool fused) {
+    return (int64_t)d.depth * (fused ? 3 : 2) * N * es;
+}
 
 static int nominal_ctas_per_sm(const PlanDesc &d) {
     const int t = cta_threads(d);
@@ -120,9 +130,11 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
         d = find_plan(force_plan);
         if (!d || d->op != op) return RMSNORM_ERR_UNSUPPORTED;
         if (d->path == PATH_VECTOR && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
-        if (d->path == PATH_STAGED) return RMSNORM_ERR_UNSUPPORTED;
+        // staged plans: backward only, aligned rows that fit, one type
+        if (d->path == PATH_STAGED && (op != RMSNORM_OP_BWD || !vec_ok || C > plan_capacity(*d)))
+            return RMSNORM_ERR_UNSUPPORTED;
         // with an fp32 weight only the default plans (and the generic one) are compiled
-        if (mixed_kind(kind_of(dt)) && d->path == PATH_VECTOR && d->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
+        if (mixed_kind(kind_of(dt)) && row_path(d->path) && d->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
     } else {
         d = vec_ok ? default_vector_plan(op, dt, C) : nullptr;
         if (!d) d = generic_plan(op);
@@ -152,7 +164,13 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     out->smem_bytes = bwd_smem_bytes(*d, N);
     // dynamic shared memory stays below 48 KB with room for the kernels'
     // static arrays (a few KB at most)
-    if (out->smem_bytes > 44 * 1024) return RMSNORM_ERR_UNSUPPORTED;
+    if (d->path == PATH_STAGED) {
+        // the plain variant's stages; the fused one is checked by the backward
+        const int64_t sm = staged_smem_bytes(*d, N, s, false);
+        if (sm > kMaxDynamicSmem) return RMSNORM_ERR_UNSUPPORTED;
+        out->smem_bytes = (int32_t)sm;
+    }
+    if (d->path != PATH_STAGED && out->smem_bytes > 44 * 1024) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t bytes = P * partial_rows(op) * N * 4;
     out->workspace_bytes = (bytes + 255) / 256 * 256;
     return RMSNORM_SUCCESS;
@@ -283,14 +301,20 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
     const int E = 16 / elem_size(dt);
     // The dynamic shared memory of the team combine depends on N; occupancy
     // is taken for the largest N the plan serves (the conservative value).
-    const int64_t nmax = d.path == PATH_VECTOR ? plan_capacity(d) * E : N;
-    const int smem = bwd_smem_bytes(d, nmax);
+    const int64_t nmax = d.path != PATH_GENERIC ? plan_capacity(d) * E : N;
+    const int smem = d.path == PATH_STAGED ? (int)staged_smem_bytes(d, nmax, elem_size(dt), fused)
+                                           : bwd_smem_bytes(d, nmax);
+    if (smem > kMaxDynamicSmem) return cudaErrorInvalidConfiguration;
     int best = 1 << 30;
     for (int pk = 0; pk < 2; ++pk) {
-        // the LayerNorm kernels and the generic ones have one variant
-        if ((d.path == PATH_GENERIC || d.op == OP_LN_BWD) && pk == 1) continue;
+        // the LayerNorm, staged and generic kernels have one variant
+        if ((d.path != PATH_VECTOR || d.op == OP_LN_BWD) && pk == 1) continue;
         const void *k = d.op == OP_LN_BWD ? ln_bwd_kernel(d.id, dt, fused) : bwd_kernel(d.id, dt, fused, pk != 0);
         if (!k) return cudaErrorInvalidDeviceFunction;
+        if (d.path == PATH_STAGED) {  // more than 48 KB of dynamic shared memory needs an opt-in
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+        }
         int n = 0;
         cudaError_t e;
         if (d.cs > 1) {
@@ -340,7 +364,7 @@ int self_check_impl() {
             int64_t expect = 1;
             for (int i = 0; i < kNumPlans; ++i) {
                 const PlanDesc &d = kPlans[i];
-                if (d.op != op || d.path != PATH_VECTOR || d.cmin == 0 || !(d.dtm & dtype_bit(dt))) continue;
+                if (d.op != op || !row_path(d.path) || d.cmin == 0 || !(d.dtm & dtype_bit(dt))) continue;
                 // ranges of a dtype's default plans must tile [1, max] in table order
                 if (d.cmin != expect || d.cmax < d.cmin) ++bad;
                 expect = d.cmax + 1;
@@ -360,6 +384,12 @@ int self_check_impl() {
             if (!pow2 || d.tpr * d.teams > kMaxCtaThreads || d.tpr * d.teams < 32 || d.v < 1) ++bad;
             // a cluster row has one team per CTA, of whole warps, and at most 8 CTAs
             if (d.cs < 1 || d.cs > 8 || (d.cs > 1 && (d.teams != 1 || d.tpr < 32))) ++bad;
+        }
+        if (d.path == PATH_STAGED) {
+            // one team per CTA of whole warps, no cluster, at least two stages, backward only
+            if (d.op != OP_BWD || d.teams != 1 || d.cs != 1 || d.depth < 2 || d.tpr % 32 != 0 || d.tpr < 64 ||
+                d.tpr > kMaxCtaThreads || d.v < 1)
+                ++bad;
         }
         if (d.dtm < 1 || d.dtm > DT_ANY) ++bad;
         if (d.id < 0 || d.id >= kMaxPlanId) ++bad;
@@ -521,6 +551,12 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     bool packed = plan.packed != 0;
     if (force_packed == 0) packed = false;
     if (force_packed == 1 && plan.path == PATH_VECTOR) packed = true;
+    if (plan.path == PATH_STAGED) {
+        packed = true;  // the staged kernel has the packed variant only
+        const int64_t sm = staged_smem_bytes(*d, N, (int)s, fused);
+        if (sm > kMaxDynamicSmem) return RMSNORM_ERR_UNSUPPORTED;
+        plan.smem_bytes = (int32_t)sm;
+    }
     plan.packed = packed ? 1 : 0;
 
     float *ws = static_cast<float *>(workspace);

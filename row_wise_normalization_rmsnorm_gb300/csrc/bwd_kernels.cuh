@@ -410,6 +410,193 @@ __global__ void __launch_bounds__(TPR *TEAMS) layernorm_bwd_vector(const BwdPara
     bwd_vector_body<T, T, TPR, V, TEAMS, D, CS, true, FUSED, true>(p);
 }
 
+// Staged persistent main kernel (bulk-copy pipeline). Each row's x and dy
+// (and dres) stream from HBM into one of S shared-memory stages with
+// cp.async.bulk, counted in bytes on the stage's mbarrier; the row team
+// copies the stage into registers and runs the same two passes as the
+// register kernel. The row reduction's barrier also proves that every warp
+// has copied the stage out, so right after it thread 0 refills the stage
+// with row k + S: S rows stay in flight whatever the register budget, no
+// producer warp is needed (an extra warp would cut the registers a thread
+// may use), and a row's loads never stall a consumer between its passes.
+// Every wait is bounded: a wait that gives up records the status word and
+// the kernel carries on (its outputs are then incomplete), so every thread
+// still reaches every barrier and the kernel always ends.
+template <typename T, typename TW, int TPR, int V, int S, bool FUSED>
+__global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) {
+    using Pk = Pair<true>;
+    constexpr int E = Elem<T>::E;
+    constexpr int NP = Elem<T>::NP;
+    constexpr int W = TPR / 32;          // warps of the row team
+    constexpr int NB = FUSED ? 3 : 2;    // rows a stage holds: x, dy (, dres)
+    static_assert(TPR % 32 == 0 && TPR >= 64, "whole warps");
+    __shared__ float red[2][W];
+    __shared__ __align__(8) uint64_t full[S];
+    extern __shared__ float4 stage_smem[];  // S * NB * C chunks of 16 bytes
+
+    const int N = p.N;
+    const int C = N / E;
+    const int tid = threadIdx.x;
+    const int64_t unit = blockIdx.x;
+    const int64_t G = gridDim.x;
+    const int64_t iters = unit < p.M ? (p.M - unit + G - 1) / G : 0;
+    const bool has_dres = FUSED && p.dres != nullptr;
+    const uint32_t row_bytes = (uint32_t)C * 16u;
+    uint4 *stages = reinterpret_cast<uint4 *>(stage_smem);
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x);
+    const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dy);
+    const uint4 *r4 = reinterpret_cast<const uint4 *>(p.dres);
+    // thread 0: stream row k into stage s
+    auto issue = [&](int64_t k, int s) {
+        const int64_t off = (unit + k * G) * C;
+        uint4 *dst = stages + (size_t)s * NB * C;
+        mbar_arrive_expect_tx(&full[s], row_bytes * (has_dres ? 3u : 2u));
+        bulk_g2s(dst, x4 + off, row_bytes, &full[s]);
+        bulk_g2s(dst + C, d4 + off, row_bytes, &full[s]);
+        if (has_dres) bulk_g2s(dst + 2 * C, r4 + off, row_bytes, &full[s]);
+    };
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        mbar_init_fence();
+        for (int s = 0; s < S && s < iters; ++s) issue(s, s);
+    }
+    __syncthreads();
+
+    const int t = tid;
+    const int lane = t & 31;
+    uint4 *dx4 = reinterpret_cast<uint4 *>(p.dx);
+    const bool has_w = p.w != nullptr;
+    const float2 o2 = make_float2(p.offset, p.offset);
+    // (offset + w) for this thread's chunks, in fp32; with three or more
+    // chunks of a 2-byte type, w is held as loaded instead (one uint4 a
+    // chunk) and offset + w formed when used (the same fp32 add each time),
+    // which keeps the thread within its registers
+    constexpr bool RAW = V >= 3 && E == 8 && std::is_same<T, TW>::value;
+    uint4 wraw[RAW ? V : 1];
+    float2 wp[RAW ? 1 : V][NP], acc[V][NP];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * TPR + t;
+        if constexpr (RAW) {
+            wraw[v] = (has_w && c < C) ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + c) : make_uint4(0, 0, 0, 0);
+        } else {
+            float2 wv[NP];
+            if (has_w && c < C) {
+                load_w_chunk<T, TW>(p.w, c, wv);
+            } else {
+#pragma unroll
+                for (int q = 0; q < NP; ++q) wv[q] = make_float2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < NP; ++q) wp[v][q] = has_w ? Pk::add(o2, wv[q]) : make_float2(1.f, 1.f);
+        }
+#pragma unroll
+        for (int q = 0; q < NP; ++q) acc[v][q] = make_float2(0.f, 0.f);
+    }
+    auto wfac = [&](int v, float2 (&f)[NP]) {
+        if constexpr (RAW) {
+            unpack<T>(wraw[v], f);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) f[q] = has_w ? Pk::add(o2, f[q]) : make_float2(1.f, 1.f);
+        } else {
+#pragma unroll
+            for (int q = 0; q < NP; ++q) f[q] = wp[v][q];
+        }
+    };
+
+    bool failed = false;
+    int s = 0;          // stage of row k (k mod S)
+    uint32_t ph = 0;    // parity of k / S
+    for (int64_t k = 0; k < iters; ++k) {
+        const int64_t row = unit + k * G;
+        const float r = p.rstd[row];
+        if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
+        const uint4 *src = stages + (size_t)s * NB * C;
+        uint4 xv[V], dv[V], rv[FUSED ? V : 1];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * TPR + t;
+            const bool in = c < C;
+            xv[v] = in ? src[c] : make_uint4(0, 0, 0, 0);
+            dv[v] = in ? src[C + c] : make_uint4(0, 0, 0, 0);
+            if constexpr (FUSED) rv[v] = (in && has_dres) ? src[2 * C + c] : make_uint4(0, 0, 0, 0);
+        }
+
+        const float2 r2 = make_float2(r, r);
+        float2 dot = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float2 xf[NP], df[NP], wf[NP];
+            unpack<T>(xv[v], xf);
+            unpack<T>(dv[v], df);
+            wfac(v, wf);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) dot = Pk::fma(Pk::mul(df[q], wf[q]), xf[q], dot);
+        }
+        float part = __fadd_rn(dot.x, dot.y);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
+        float *slots = &red[k & 1][0];
+        if (lane == 0) slots[t >> 5] = part;
+        __syncthreads();
+        // every warp has copied stage s into registers: refill it with row k + S
+        if (tid == 0 && k + S < iters) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(k + S, s);
+        }
+        if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+        }
+        const float sum = sum_slots<W>(slots, lane);
+        const float cm = -__fdiv_rn(__fmul_rn(sum, r), (float)N);
+        const float2 nc2 = make_float2(cm, cm);
+        const int64_t base = row * C;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * TPR + t;
+            float2 xf[NP], df[NP], out[NP], wf[NP];
+            unpack<T>(xv[v], xf);
+            unpack<T>(dv[v], df);
+            wfac(v, wf);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const float2 xh = Pk::mul(xf[q], r2);
+                const float2 g = Pk::mul(df[q], wf[q]);
+                out[q] = Pk::mul(Pk::fma(xh, nc2, g), r2);
+                if (has_w) acc[v][q] = Pk::fma(df[q], xh, acc[v][q]);
+            }
+            if constexpr (FUSED) {
+                if (has_dres) {
+                    float2 rf[NP];
+                    unpack<T>(rv[v], rf);
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) out[q] = Pk::add(out[q], rf[q]);
+                }
+            }
+            if (c < C) st_chunk(dx4 + base + c, pack<T>(out));
+        }
+    }
+    if (failed && p.status) *p.status = kStatusClusterWaitTimeout;
+
+    // The finalizer may start launching now; it waits for this grid to
+    // finish (griddepcontrol.wait) before it reads the workspace.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!has_w) return;
+    float *wsrow = p.ws + unit * N;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * TPR + t;
+        if (c < C) {
+            float4 *d = reinterpret_cast<float4 *>(wsrow + c * E);
+#pragma unroll
+            for (int q = 0; q < NP / 2; ++q)
+                d[q] = make_float4(acc[v][2 * q].x, acc[v][2 * q].y, acc[v][2 * q + 1].x, acc[v][2 * q + 1].y);
+        }
+    }
+}
+
 // Generic main kernel: one 256-thread CTA per row at a time, element loads,
 // each row read twice (the second read is served by L1/L2). The CTA's dW
 // partial row lives in the workspace itself: the thread that owns column j
@@ -618,6 +805,30 @@ constexpr bool bwd_instantiated() {
     return std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0;
 }
 
+// Staged kernel: launched as a cluster of one CTA (its bulk copies name a
+// shared::cluster destination) with the stages' dynamic shared memory.
+template <typename T, typename TW, int TPR, int V, int S>
+static int bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
+    const void *k = fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, true>
+                          : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(TPR);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, true>, p)
+                 : (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, false>, p);
+}
+
 template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
 static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     if constexpr (OP != OP_BWD || !bwd_instantiated<T, TW, PATH, CMIN>()) {
@@ -631,6 +842,8 @@ static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int gri
     } else if constexpr (PATH == PATH_VECTOR) {
         return packed ? bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, true>(fused, p, grid, smem, s)
                       : bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, false>(fused, p, grid, smem, s);
+    } else if constexpr (PATH == PATH_STAGED && TEAMS == 1 && CS == 1) {
+        return bwd_launch_staged<T, TW, TPR, V, D>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
@@ -648,6 +861,9 @@ static const void *bwd_ptr_entry(bool fused, bool packed) {
                          : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, false>;
         return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, true>
                      : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, false>;
+    } else if constexpr (PATH == PATH_STAGED && TEAMS == 1 && CS == 1) {
+        return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, true>
+                     : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, false>;
     } else {
         return nullptr;
     }

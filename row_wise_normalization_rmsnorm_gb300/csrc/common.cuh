@@ -326,6 +326,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// One plain arrival (release at CTA scope: this thread's earlier shared
+// memory reads are complete before the phase can complete).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Bulk copy (the TMA engine's 1-D form) of `bytes` from global memory into
+// this CTA's shared memory, counted in bytes on `bar`. Both addresses
+// 16-byte aligned, `bytes` a multiple of 16. The kernel is launched as a
+// cluster (of one CTA), so the shared::cluster destination is this CTA's.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// Barrier over the first `count` threads of the CTA (named barrier 1); the
+// other threads (a producer warp) do not take part.
+__device__ __forceinline__ void named_sync(uint32_t count) {
+    asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");
+}
+
 // Store v at the address of `local_slot` in cluster CTA `cta` and count 4
 // bytes on that CTA's barrier at the address of `local_bar`.
 __device__ __forceinline__ void st_async_cluster(float *local_slot, uint64_t *local_bar, uint32_t cta, float v) {

@@ -30,7 +30,8 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
 // storage types in `dtypes`; 0, 0 marks an alternative that runs only when
 // forced (tuning and A/B tests).
 // depth (backward only): rows whose x/dy loads are in flight while the
-// current row is computed (a register ring of depth + 1 rows).
+// current row is computed (a register ring of depth + 1 rows); for staged
+// plans the number of shared-memory stages the producer warp fills.
 // cluster: CTAs of a thread-block cluster that share one row; each holds
 // threads_per_row * chunks_per_thread chunks of it in registers and the row
 // sums meet in distributed shared memory (1: no cluster).
@@ -58,21 +59,26 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(15, OP_FWD, PATH_VECTOR ,   16, 2, 16, 0, 1, DT_ANY,     0,     0) \
     /* forward, any N and alignment */ \
     X(16, OP_FWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0) \
-    /* backward main kernel, persistent, row in registers */ \
+    /* backward main kernel, persistent: rows in registers (vector) or \
+       streamed into `depth` shared-memory stages by bulk copies (staged) */ \
     X(20, OP_BWD, PATH_VECTOR ,    8, 1, 32, 1, 1, DT_ANY,     1,     8) \
     X(21, OP_BWD, PATH_VECTOR ,   16, 1, 16, 1, 1, DT_ANY,     9,    16) \
     X(22, OP_BWD, PATH_VECTOR ,   32, 1,  8, 1, 1, DT_ANY,    17,    32) \
     X(23, OP_BWD, PATH_VECTOR ,   32, 2,  8, 1, 1, DT_ANY,    33,    64) \
     X(24, OP_BWD, PATH_VECTOR ,   64, 2,  4, 1, 1, DT_ANY,    65,   128) \
     X(25, OP_BWD, PATH_VECTOR ,  128, 2,  2, 1, 1, DT_ANY,   129,   256) \
-    X(26, OP_BWD, PATH_VECTOR ,  256, 2,  2, 1, 1, DT_16,     257,   512) \
-    X(38, OP_BWD, PATH_VECTOR ,  256, 2,  2, 2, 1, DT_F32,   257,   512) \
-    X(27, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 1, DT_16,     513,  1024) \
-    X(34, OP_BWD, PATH_VECTOR ,  512, 2,  1, 2, 1, DT_F32,   513,  1024) \
-    X(42, OP_BWD, PATH_VECTOR ,  512, 3,  1, 1, 1, DT_ANY,  1025,  1536) \
-    X(45, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 2, DT_ANY,  1537,  2048) \
+    X(95, OP_BWD, PATH_STAGED ,  256, 2,  1, 4, 1, DT_ANY,   257,   512) \
+    X(88, OP_BWD, PATH_STAGED ,  512, 2,  1, 4, 1, DT_ANY,   513,  1024) \
+    X(96, OP_BWD, PATH_STAGED ,  512, 3,  1, 3, 1, DT_ANY,  1025,  1536) \
+    X(97, OP_BWD, PATH_STAGED ,  512, 4,  1, 2, 1, DT_ANY,  1537,  2048) \
     X(46, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 4, DT_ANY,  2049,  4096) \
     X(47, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 8, DT_ANY,  4097,  8192) \
+    X(26, OP_BWD, PATH_VECTOR ,  256, 2,  2, 1, 1, DT_ANY,     0,     0) \
+    X(38, OP_BWD, PATH_VECTOR ,  256, 2,  2, 2, 1, DT_ANY,     0,     0) \
+    X(27, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 1, DT_ANY,     0,     0) \
+    X(34, OP_BWD, PATH_VECTOR ,  512, 2,  1, 2, 1, DT_ANY,     0,     0) \
+    X(42, OP_BWD, PATH_VECTOR ,  512, 3,  1, 1, 1, DT_ANY,     0,     0) \
+    X(45, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 2, DT_ANY,     0,     0) \
     X(32, OP_BWD, PATH_VECTOR ,  256, 1,  2, 2, 1, DT_ANY,     0,     0) \
     X(33, OP_BWD, PATH_VECTOR ,   16, 2, 16, 1, 1, DT_ANY,     0,     0) \
     X(35, OP_BWD, PATH_VECTOR ,  512, 2,  1, 0, 1, DT_ANY,     0,     0) \
@@ -87,6 +93,13 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(53, OP_BWD, PATH_VECTOR ,  256, 1,  1, 1, 2, DT_ANY,     0,     0) \
     X(54, OP_BWD, PATH_VECTOR ,  256, 2,  1, 1, 4, DT_ANY,     0,     0) \
     X(55, OP_BWD, PATH_VECTOR ,  128, 2,  1, 1, 4, DT_ANY,     0,     0) \
+    X(89, OP_BWD, PATH_STAGED ,  512, 2,  1, 3, 1, DT_ANY,     0,     0) \
+    X(90, OP_BWD, PATH_STAGED ,  256, 4,  1, 4, 1, DT_ANY,     0,     0) \
+    X(91, OP_BWD, PATH_STAGED ,  512, 1,  1, 6, 1, DT_ANY,     0,     0) \
+    X(92, OP_BWD, PATH_STAGED ,  256, 2,  1, 6, 1, DT_ANY,     0,     0) \
+    X(93, OP_BWD, PATH_STAGED ,  256, 1,  1, 8, 1, DT_ANY,     0,     0) \
+    X(94, OP_BWD, PATH_STAGED ,  128, 2,  1, 8, 1, DT_ANY,     0,     0) \
+    X(98, OP_BWD, PATH_STAGED ,  512, 3,  1, 2, 1, DT_ANY,     0,     0) \
     /* backward main kernel, any N and alignment */ \
     X(36, OP_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0) \
     /* LayerNorm backward main kernel, persistent, row in registers: two \
@@ -118,7 +131,7 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
 // Largest CTA any plan uses.
 constexpr int kMaxCtaThreads = 1024;
 // Plan ids are below this bound (host caches are indexed by id).
-constexpr int kMaxPlanId = 96;
+constexpr int kMaxPlanId = 128;
 
 struct FwdParams {
     const void *x;

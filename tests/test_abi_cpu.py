@@ -65,7 +65,7 @@ def test_fwd_default_plans(rn, dt, N, tpr, v, cs):
     assert p["ctas"] == 4096 // p["rows_per_cta"] * cs
 
 
-@pytest.mark.parametrize("dt,N,cs", [(1, 16384, 2), (0, 8192, 2), (0, 16384, 4), (1, 32768, 4), (1, 65536, 8)])
+@pytest.mark.parametrize("dt,N,cs", [(0, 16384, 4), (1, 32768, 4), (1, 65536, 8), (0, 32768, 8)])
 def test_bwd_wide_rows_use_clusters(rn, dt, N, cs):
     p = rn.plan_query(rn.OP_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)
     assert p["path_name"] == "vector" and p["cluster_size"] == cs
@@ -79,13 +79,29 @@ def test_fwd_generic_when_vector_cannot_serve(rn, dt, N):
     assert p["path_name"] == "generic"
 
 
-def test_dtype_specific_backward_defaults(rn):
-    # fp32 rows of 2052..4096 elements keep two rows of loads in flight;
-    # bf16 rows of the same byte width keep one
-    f = rn.plan_query(rn.OP_BWD, 16384, 4096, 0, num_sms=152, ctas_per_sm=1)
-    b = rn.plan_query(rn.OP_BWD, 16384, 8192, 1, num_sms=152, ctas_per_sm=1)
-    assert f["plan_id"] != b["plan_id"]
-    assert (f["threads_per_row"], f["chunks_per_thread"]) == (b["threads_per_row"], b["chunks_per_thread"])
+def test_staged_backward_defaults(rn):
+    """Rows of 257..2048 chunks take the staged (bulk-copy pipeline)
+    backward: one row team per CTA, `depth` shared-memory stages of x and dy
+    rows, a partial row per CTA."""
+    for dt, N, tpr, v, stages in ((1, 4096, 256, 2, 4), (1, 8192, 512, 2, 4), (0, 4096, 512, 2, 4),
+                                  (1, 12288, 512, 3, 3), (1, 16384, 512, 4, 2), (0, 8192, 512, 4, 2),
+                                  (2, 8192, 512, 2, 4)):
+        p = rn.plan_query(rn.OP_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)
+        assert p["path_name"] == "staged", (dt, N, p)
+        assert (p["threads_per_row"], p["chunks_per_thread"], p["cluster_size"]) == (tpr, v, 1)
+        es = 4 if dt == 0 else 2
+        assert p["smem_bytes"] == stages * 2 * N * es        # plain variant: x and dy rows
+        assert p["ctas"] == 152 and p["ws_rows"] == 152
+    # the same rows with an fp32 weight take the same plans
+    assert rn.plan_query(rn.OP_BWD, 16384, 8192, rn.RMSNORM_BF16 | rn.RMSNORM_WEIGHT_F32)["path_name"] == "staged"
+    # misaligned rows still take the generic kernel; short rows stay in registers
+    assert rn.plan_query(rn.OP_BWD, 4096, 8192, 1, aligned=False)["path_name"] == "generic"
+    assert rn.plan_query(rn.OP_BWD, 4096, 2048, 1)["path_name"] == "vector"
+    # a staged plan is refused for the forward and for rows it cannot hold
+    with pytest.raises(rn.RMSNormError):
+        rn.plan_query(rn.OP_FWD, 10, 8192, 1, force_plan=88)
+    with pytest.raises(rn.RMSNormError):
+        rn.plan_query(rn.OP_BWD, 10, 16384, 1, force_plan=88)
 
 
 def test_fp32_weight_flag_plans(rn):

@@ -64,7 +64,10 @@ def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_p
     needed = check_dx(to_host(dx, dt), b, dt)
     check_dw(to_host(dw, wdt), b, wdt)
     if expect_path is not None:
-        assert fplan["path_name"] == expect_path and bplan["path_name"] == expect_path, (fplan, bplan)
+        # "vector": the fast paths (rows in registers; the backward may
+        # instead stage rows in shared memory)
+        fast = ("vector", "staged") if expect_path == "vector" else (expect_path,)
+        assert fplan["path_name"] == expect_path and bplan["path_name"] in fast, (fplan, bplan)
     # The floor is for cancellation only: it should be needed rarely on
     # ordinary rows. Very short rows cancel by construction (at N = 1,
     # dx = rstd g eps / (x^2 + eps) is the difference of two near-equal terms).
@@ -76,13 +79,13 @@ def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_p
 def test_config_small_f32_64x256(rn):
     d, p = inputs.workload_inputs("small_f32")
     fp, bp = _fwd_bwd_check(rn, d, "f32", p["eps"], p["offset"])
-    assert fp["path_name"] == "vector" and bp["path_name"] == "vector"
+    assert fp["path_name"] == "vector" and bp["path_name"] in ("vector", "staged")
 
 
 def test_config_llama_bf16_4096x2048(rn):
     d, p = inputs.workload_inputs("llama_bf16_4096x2048")
     fp, bp = _fwd_bwd_check(rn, d, "bf16", p["eps"], p["offset"])
-    assert fp["path_name"] == "vector" and bp["path_name"] == "vector"
+    assert fp["path_name"] == "vector" and bp["path_name"] in ("vector", "staged")
 
 
 @pytest.mark.parametrize("name", ["add_bf16_1024x8192", "add_gemma_bf16_1024x8192",

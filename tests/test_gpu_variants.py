@@ -36,9 +36,15 @@ def dev_inputs(M, N, dt, seed, **kw):
 def test_packed_matches_scalar_bitwise(rn, dt, M, N, fused):
     _, t = dev_inputs(M, N, dt, 90, residual=fused, dres=fused)
     _, rstd = rn.rmsnorm_fwd(t["x"], t["w"])
-    kw = dict(dresidual_out=t.get("dres"), fused=fused)
+    # the register kernel of the same geometry where the default is staged
+    # (the staged kernel has the packed variant only)
+    code = {"bf16": rn.RMSNORM_BF16, "f32": rn.RMSNORM_F32, "f16": rn.RMSNORM_F16}[dt]
+    default = rn.plan_query(rn.OP_BWD, M, N, code)
+    plan = {88: 27, 95: 26, 96: 42, 97: 45}.get(default["plan_id"], -1) if default["path_name"] == "staged" else -1
+    kw = dict(dresidual_out=t.get("dres"), fused=fused, force_plan=plan)
     dx1, dw1, p1 = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], rstd, force_packed=1, **kw)
     dx0, dw0, p0 = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], rstd, force_packed=0, **kw)
+    assert p1["path_name"] == "vector"
     assert p1["packed"] == 1 and p0["packed"] == 0 and p1["plan_id"] == p0["plan_id"]
     assert p1["ctas"] == p0["ctas"]
     assert cuda_bits_equal(dx1, dx0) and cuda_bits_equal(dw1, dw0)
@@ -282,3 +288,34 @@ def test_non_affine_argument_rules(rn):
                          t["dy"].data_ptr(), None, None, 0, 16, 256, 1, 1e-6, 0.0, s) == 1
     assert L.rmsnorm_bwd(t["dy"].data_ptr(), t["x"].data_ptr(), None, r.data_ptr(),
                          t["dy"].data_ptr(), t["w"].data_ptr(), None, 0, 16, 256, 1, 1e-6, 0.0, s) == 1
+
+
+@pytest.mark.parametrize("dt,M,N,staged,vector,same_dw", [("bf16", 4096, 8192, 88, 27, True),
+                                                          ("f32", 1031, 4096, 88, 27, True),
+                                                          ("bf16", 2049, 4096, 95, 26, False),
+                                                          ("f16", 777, 8192, 88, 27, True),
+                                                          ("bf16", 301, 12288, 96, 42, True)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_staged_backward_matches_register_backward_bitwise(rn, dt, M, N, staged, vector, same_dw, fused):
+    """The staged backward (rows streamed into shared memory by bulk copies)
+    does the register kernel's arithmetic on the same chunk mapping: dx is
+    bit-identical, and so is dW where the register plan also keeps one
+    partial row per CTA (with two row teams a CTA it adds them first)."""
+    d = inputs.make_inputs(M, N, dt, 190 + N % 7, residual=fused, dres=fused)
+    x, dy, w = (to_dev(d[k], dt) for k in ("x", "dy", "w"))
+    dres = to_dev(d["dres"], dt) if fused else None
+    _, rstd = rn.rmsnorm_fwd(x, w)
+    a_dx, a_dw, ap = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dresidual_out=dres, fused=fused, force_plan=staged,
+                                       force_ctas=120)
+    b_dx, b_dw, bp = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dresidual_out=dres, fused=fused, force_plan=vector,
+                                       force_ctas=120)
+    torch.cuda.synchronize()
+    assert ap["path_name"] == "staged" and bp["path_name"] == "vector"
+    assert ap["ctas"] == bp["ctas"] == 120
+    assert cuda_bits_equal(a_dx, b_dx)
+    if same_dw:
+        assert cuda_bits_equal(a_dw, b_dw)
+    else:
+        assert torch.allclose(a_dw.float(), b_dw.float(), rtol=1e-2, atol=1e-3)
+    assert rn.lib().rmsnorm_device_status(1) == 0
+
