@@ -521,7 +521,9 @@ def main():
                       "gbs": by / (avg * 1e-3) / 1e9, "frac_of_peak": by / (avg * 1e-3) / 1e9 / peak}
     comp["bwd"]["kernels"] = "main + finalizer (programmatic dependent launch)"
     dom = "bwd" if comp["bwd"]["us"] >= comp["fwd"]["us"] else "fwd"
-    kname = {"fwd": "rmsnorm_fwd_vector", "bwd": "rmsnorm_bwd_vector + rmsnorm_dw_finalize4"}[dom]
+    bwd_main = {"staged": "rmsnorm_bwd_staged", "vector": "rmsnorm_bwd_vector"}.get(bplan["path_name"],
+                                                                                   "rmsnorm_bwd_generic")
+    kname = {"fwd": "rmsnorm_fwd_vector", "bwd": bwd_main + " + rmsnorm_dw_finalize4"}[dom]
     roof = {"kernel": kname, "bound": "hbm", "achieved": comp[dom]["gbs"], "peak": peak, "unit": "GB/s",
             "frac": comp[dom]["gbs"] / peak, "traffic": ncu_traffic(dom), "peak_source": peak_kind,
             "bytes_per_launch": comp[dom]["bytes"]}
