@@ -131,7 +131,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
         if (!d || d->op != op) return RMSNORM_ERR_UNSUPPORTED;
         if (d->path == PATH_VECTOR && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
         // staged plans: backward only, aligned rows that fit, one type
-        if (d->path == PATH_STAGED && (op != RMSNORM_OP_BWD || !vec_ok || C > plan_capacity(*d)))
+        if (d->path == PATH_STAGED && (op == RMSNORM_OP_FWD || !vec_ok || C > plan_capacity(*d)))
             return RMSNORM_ERR_UNSUPPORTED;
         // with an fp32 weight only the default plans (and the generic one) are compiled
         if (mixed_kind(kind_of(dt)) && row_path(d->path) && d->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
@@ -387,7 +387,7 @@ int self_check_impl() {
         }
         if (d.path == PATH_STAGED) {
             // one team per CTA of whole warps, no cluster, at least two stages, backward only
-            if (d.op != OP_BWD || d.teams != 1 || d.cs != 1 || d.depth < 2 || d.tpr % 32 != 0 || d.tpr < 64 ||
+            if (d.op == OP_FWD || d.teams != 1 || d.cs != 1 || d.depth < 2 || d.tpr % 32 != 0 || d.tpr < 64 ||
                 d.tpr > kMaxCtaThreads || d.v < 1)
                 ++bad;
         }
@@ -733,6 +733,11 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
     if (e != cudaSuccess) return cuda_fail(e);
     st = select_plan(RMSNORM_OP_LN_BWD, M, N, dt, aligned, parts, cps, force_plan, force_ctas, &plan);
     if (st != RMSNORM_SUCCESS) return st;
+    if (plan.path == PATH_STAGED) {
+        const int64_t sm = staged_smem_bytes(*find_plan(plan.plan_id), N, (int)s, fused);
+        if (sm > kMaxDynamicSmem) return RMSNORM_ERR_UNSUPPORTED;
+        plan.smem_bytes = (int32_t)sm;
+    }
 
     float *ws = static_cast<float *>(workspace);
     bool owned = false;

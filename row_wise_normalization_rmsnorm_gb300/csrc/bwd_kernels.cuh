@@ -422,15 +422,17 @@ __global__ void __launch_bounds__(TPR *TEAMS) layernorm_bwd_vector(const BwdPara
 // Every wait is bounded: a wait that gives up records the status word and
 // the kernel carries on (its outputs are then incomplete), so every thread
 // still reaches every barrier and the kernel always ends.
-template <typename T, typename TW, int TPR, int V, int S, bool FUSED>
-__global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) {
+template <typename T, typename TW, int TPR, int V, int S, bool FUSED, bool LN>
+__device__ __forceinline__ void staged_body(const BwdParams &p) {
     using Pk = Pair<true>;
+    using RT = typename std::conditional<LN, float2, float>::type;  // what a row reduces
+    constexpr int NACC = LN ? 2 : 1;     // partial rows per CTA
     constexpr int E = Elem<T>::E;
     constexpr int NP = Elem<T>::NP;
     constexpr int W = TPR / 32;          // warps of the row team
     constexpr int NB = FUSED ? 3 : 2;    // rows a stage holds: x, dy (, dres)
     static_assert(TPR % 32 == 0 && TPR >= 64, "whole warps");
-    __shared__ float red[2][W];
+    __shared__ RT red[2][W];
     __shared__ __align__(8) uint64_t full[S];
     extern __shared__ float4 stage_smem[];  // S * NB * C chunks of 16 bytes
 
@@ -467,6 +469,9 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
     const int lane = t & 31;
     uint4 *dx4 = reinterpret_cast<uint4 *>(p.dx);
     const bool has_w = p.w != nullptr;
+    // partial rows wanted: RMSNorm with a weight; LayerNorm when the host
+    // passes a workspace (dgamma and/or dbeta requested)
+    const bool want_acc = LN ? p.ws != nullptr : has_w;
     const float2 o2 = make_float2(p.offset, p.offset);
     // (offset + w) for this thread's chunks, in fp32; with three or more
     // chunks of a 2-byte type, w is held as loaded instead (one uint4 a
@@ -475,6 +480,7 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
     constexpr bool RAW = V >= 3 && E == 8 && std::is_same<T, TW>::value;
     uint4 wraw[RAW ? V : 1];
     float2 wp[RAW ? 1 : V][NP], acc[V][NP];
+    float2 accb[LN ? V : 1][NP];  // LayerNorm: sum dy (dbeta)
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = v * TPR + t;
@@ -492,7 +498,10 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
             for (int q = 0; q < NP; ++q) wp[v][q] = has_w ? Pk::add(o2, wv[q]) : make_float2(1.f, 1.f);
         }
 #pragma unroll
-        for (int q = 0; q < NP; ++q) acc[v][q] = make_float2(0.f, 0.f);
+        for (int q = 0; q < NP; ++q) {
+            acc[v][q] = make_float2(0.f, 0.f);
+            if constexpr (LN) accb[v][q] = make_float2(0.f, 0.f);
+        }
     }
     auto wfac = [&](int v, float2 (&f)[NP]) {
         if constexpr (RAW) {
@@ -508,9 +517,17 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
     bool failed = false;
     int s = 0;          // stage of row k (k mod S)
     uint32_t ph = 0;    // parity of k / S
+    // the row statistics are loaded one row ahead, like the rows themselves
+    float r_next = iters > 0 ? p.rstd[unit] : 0.f;
+    float mu_next = (LN && iters > 0) ? p.mean[unit] : 0.f;
     for (int64_t k = 0; k < iters; ++k) {
         const int64_t row = unit + k * G;
-        const float r = p.rstd[row];
+        const float r = r_next;
+        const float mu = mu_next;
+        if (k + 1 < iters) {
+            r_next = p.rstd[row + G];
+            if constexpr (LN) mu_next = p.mean[row + G];
+        }
         if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
         const uint4 *src = stages + (size_t)s * NB * C;
         uint4 xv[V], dv[V], rv[FUSED ? V : 1];
@@ -524,7 +541,8 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
         }
 
         const float2 r2 = make_float2(r, r);
-        float2 dot = make_float2(0.f, 0.f);
+        const float2 nmu2 = make_float2(-mu, -mu);  // LayerNorm: x - mean as x + (-mean)
+        float2 dot = make_float2(0.f, 0.f), gsum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             float2 xf[NP], df[NP], wf[NP];
@@ -532,12 +550,27 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
             unpack<T>(dv[v], df);
             wfac(v, wf);
 #pragma unroll
-            for (int q = 0; q < NP; ++q) dot = Pk::fma(Pk::mul(df[q], wf[q]), xf[q], dot);
+            for (int q = 0; q < NP; ++q) {
+                const float2 g = Pk::mul(df[q], wf[q]);
+                if constexpr (LN) {
+                    dot = Pk::fma(g, Pk::add(xf[q], nmu2), dot);
+                    gsum = Pk::add(gsum, g);
+                } else {
+                    dot = Pk::fma(g, xf[q], dot);
+                }
+            }
         }
-        float part = __fadd_rn(dot.x, dot.y);
+        RT part;
+        if constexpr (LN) {
+            part = make_float2(__fadd_rn(gsum.x, gsum.y), __fadd_rn(dot.x, dot.y));
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
-        float *slots = &red[k & 1][0];
+            for (int o = 16; o > 0; o >>= 1) part = add2(part, shfl_xor2(part, o));
+        } else {
+            part = __fadd_rn(dot.x, dot.y);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
+        }
+        RT *slots = &red[k & 1][0];
         if (lane == 0) slots[t >> 5] = part;
         __syncthreads();
         // every warp has copied stage s into registers: refill it with row k + S
@@ -549,9 +582,19 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
             s = 0;
             ph ^= 1u;
         }
-        const float sum = sum_slots<W>(slots, lane);
-        const float cm = -__fdiv_rn(__fmul_rn(sum, r), (float)N);
+        // c = rstd (sum g x) / N (LayerNorm: sum g (x - mean)); LayerNorm
+        // also subtracts mean(g) = (sum g) / N
+        float cm, nmg = 0.f;
+        if constexpr (LN) {
+            const float2 sum = sum_slots2<W>(slots, lane);
+            cm = -__fdiv_rn(__fmul_rn(sum.y, r), (float)N);
+            nmg = -__fdiv_rn(sum.x, (float)N);
+        } else {
+            const float sum = sum_slots<W>(slots, lane);
+            cm = -__fdiv_rn(__fmul_rn(sum, r), (float)N);
+        }
         const float2 nc2 = make_float2(cm, cm);
+        const float2 nmg2 = make_float2(nmg, nmg);
         const int64_t base = row * C;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
@@ -562,10 +605,14 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
             wfac(v, wf);
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
-                const float2 xh = Pk::mul(xf[q], r2);
-                const float2 g = Pk::mul(df[q], wf[q]);
+                const float2 xh = LN ? Pk::mul(Pk::add(xf[q], nmu2), r2) : Pk::mul(xf[q], r2);
+                float2 g = Pk::mul(df[q], wf[q]);
+                if constexpr (LN) g = Pk::add(g, nmg2);
                 out[q] = Pk::mul(Pk::fma(xh, nc2, g), r2);
-                if (has_w) acc[v][q] = Pk::fma(df[q], xh, acc[v][q]);
+                if (want_acc) {
+                    acc[v][q] = Pk::fma(df[q], xh, acc[v][q]);
+                    if constexpr (LN) accb[v][q] = Pk::add(accb[v][q], df[q]);
+                }
             }
             if constexpr (FUSED) {
                 if (has_dres) {
@@ -583,8 +630,9 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
     // The finalizer may start launching now; it waits for this grid to
     // finish (griddepcontrol.wait) before it reads the workspace.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (!has_w) return;
-    float *wsrow = p.ws + unit * N;
+    if (!want_acc) return;
+    // the CTA's partial row(s): dW, or LayerNorm's dgamma | dbeta
+    float *wsrow = p.ws + unit * (int64_t)(NACC * N);
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = v * TPR + t;
@@ -593,8 +641,25 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
 #pragma unroll
             for (int q = 0; q < NP / 2; ++q)
                 d[q] = make_float4(acc[v][2 * q].x, acc[v][2 * q].y, acc[v][2 * q + 1].x, acc[v][2 * q + 1].y);
+            if constexpr (LN) {
+                float4 *db4 = reinterpret_cast<float4 *>(wsrow + N + c * E);
+#pragma unroll
+                for (int q = 0; q < NP / 2; ++q)
+                    db4[q] = make_float4(accb[v][2 * q].x, accb[v][2 * q].y, accb[v][2 * q + 1].x,
+                                         accb[v][2 * q + 1].y);
+            }
         }
     }
+}
+
+template <typename T, typename TW, int TPR, int V, int S, bool FUSED>
+__global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) {
+    staged_body<T, TW, TPR, V, S, FUSED, false>(p);
+}
+
+template <typename T, int TPR, int V, int S, bool FUSED>
+__global__ void __launch_bounds__(TPR, 1) layernorm_bwd_staged(const BwdParams p) {
+    staged_body<T, T, TPR, V, S, FUSED, true>(p);
 }
 
 // Generic main kernel: one 256-thread CTA per row at a time, element loads,
@@ -949,6 +1014,28 @@ static int ln_bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem,
     }
 }
 
+template <typename T, int TPR, int V, int S>
+static int ln_bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
+    const void *k = fused ? (const void *)layernorm_bwd_staged<T, TPR, V, S, true>
+                          : (const void *)layernorm_bwd_staged<T, TPR, V, S, false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(TPR);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return fused ? (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, true>, p)
+                 : (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, false>, p);
+}
+
 template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
 static int ln_bwd_launch_entry(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     if constexpr (OP != OP_LN_BWD) {
@@ -961,6 +1048,8 @@ static int ln_bwd_launch_entry(bool fused, const BwdParams &p, int grid, int sme
         return (int)cudaGetLastError();
     } else if constexpr (PATH == PATH_VECTOR) {
         return ln_bwd_launch_vec<T, TPR, V, TEAMS, D, CS>(fused, p, grid, smem, s);
+    } else if constexpr (PATH == PATH_STAGED && TEAMS == 1 && CS == 1) {
+        return ln_bwd_launch_staged<T, TPR, V, D>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
@@ -975,6 +1064,9 @@ static const void *ln_bwd_ptr_entry(bool fused) {
     } else if constexpr (PATH == PATH_VECTOR) {
         return fused ? (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true>
                      : (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false>;
+    } else if constexpr (PATH == PATH_STAGED && TEAMS == 1 && CS == 1) {
+        return fused ? (const void *)layernorm_bwd_staged<T, TPR, V, D, true>
+                     : (const void *)layernorm_bwd_staged<T, TPR, V, D, false>;
     } else {
         return nullptr;
     }

@@ -109,12 +109,15 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(62, OP_LN_BWD, PATH_VECTOR,   32, 1,  8, 1, 1, DT_ANY,    17,    32) \
     X(63, OP_LN_BWD, PATH_VECTOR,   64, 1,  4, 1, 1, DT_ANY,    33,    64) \
     X(64, OP_LN_BWD, PATH_VECTOR,  128, 1,  2, 1, 1, DT_ANY,    65,   128) \
-    X(81, OP_LN_BWD, PATH_VECTOR,  128, 2,  2, 1, 1, DT_ANY,   129,   256) \
-    X(82, OP_LN_BWD, PATH_VECTOR,  256, 2,  1, 1, 1, DT_ANY,   257,   512) \
+    X(103, OP_LN_BWD, PATH_STAGED, 128, 2,  1, 6, 1, DT_ANY,   129,   256) \
+    X(100, OP_LN_BWD, PATH_STAGED, 256, 2,  1, 4, 1, DT_ANY,   257,   512) \
     X(76, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 1, DT_ANY,   513,  1024) \
-    X(86, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 2, DT_ANY,  1025,  2048) \
+    X(101, OP_LN_BWD, PATH_STAGED, 512, 3,  1, 3, 1, DT_ANY,  1025,  1536) \
+    X(86, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 2, DT_ANY,  1537,  2048) \
     X(87, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 4, DT_ANY,  2049,  4096) \
     X(70, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 8, DT_ANY,  4097,  8192) \
+    X(81, OP_LN_BWD, PATH_VECTOR,  128, 2,  2, 1, 1, DT_ANY,     0,     0) \
+    X(82, OP_LN_BWD, PATH_VECTOR,  256, 2,  1, 1, 1, DT_ANY,     0,     0) \
     X(65, OP_LN_BWD, PATH_VECTOR,  256, 1,  1, 1, 1, DT_ANY,     0,     0) \
     X(66, OP_LN_BWD, PATH_VECTOR,  512, 1,  1, 1, 1, DT_ANY,     0,     0) \
     X(67, OP_LN_BWD, PATH_VECTOR,  512, 1,  1, 1, 2, DT_ANY,     0,     0) \
@@ -126,6 +129,8 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(77, OP_LN_BWD, PATH_VECTOR,  256, 2,  1, 1, 2, DT_ANY,     0,     0) \
     X(79, OP_LN_BWD, PATH_VECTOR,  256, 1,  2, 1, 1, DT_ANY,     0,     0) \
     X(83, OP_LN_BWD, PATH_VECTOR,  256, 2,  2, 1, 1, DT_ANY,     0,     0) \
+    X(99, OP_LN_BWD, PATH_STAGED,  512, 2,  1, 4, 1, DT_ANY,     0,     0) \
+    X(102, OP_LN_BWD, PATH_STAGED, 512, 4,  1, 2, 1, DT_ANY,     0,     0) \
     X(72, OP_LN_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0)
 
 // Largest CTA any plan uses.

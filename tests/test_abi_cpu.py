@@ -144,7 +144,7 @@ def test_fp32_weight_flag_plans(rn):
                                            (1, 32768, 512, 2, 4), (1, 65536, 512, 2, 8)])
 def test_layernorm_backward_plans(rn, dt, N, tpr, v, cs):
     p = rn.plan_query(rn.OP_LN_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)
-    assert p["path_name"] == "vector"
+    assert p["path_name"] in ("vector", "staged")
     assert (p["threads_per_row"], p["chunks_per_thread"], p["cluster_size"]) == (tpr, v, cs)
     # two partial rows (dgamma | dbeta) per unit
     assert p["workspace_bytes"] == (p["ws_rows"] * 2 * N * 4 + 255) // 256 * 256
