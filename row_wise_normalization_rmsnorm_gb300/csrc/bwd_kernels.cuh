@@ -535,9 +535,9 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         for (int v = 0; v < V; ++v) {
             const int c = v * TPR + t;
             const bool in = c < C;
-            xv[v] = in ? src[c] : make_uint4(0, 0, 0, 0);
-            dv[v] = in ? src[C + c] : make_uint4(0, 0, 0, 0);
-            if constexpr (FUSED) rv[v] = (in && has_dres) ? src[2 * C + c] : make_uint4(0, 0, 0, 0);
+            xv[v] = in ? lds128(src + c) : make_uint4(0, 0, 0, 0);
+            dv[v] = in ? lds128(src + C + c) : make_uint4(0, 0, 0, 0);
+            if constexpr (FUSED) rv[v] = (in && has_dres) ? lds128(src + 2 * C + c) : make_uint4(0, 0, 0, 0);
         }
 
         const float2 r2 = make_float2(r, r);

@@ -326,6 +326,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// 16-byte load from this CTA's shared memory, addressed in the shared
+// window (so it never takes the generic load path).
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+
 // One plain arrival (release at CTA scope: this thread's earlier shared
 // memory reads are complete before the phase can complete).
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
