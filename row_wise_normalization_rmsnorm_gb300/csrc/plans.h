@@ -70,7 +70,8 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(95, OP_BWD, PATH_STAGED ,  256, 2,  1, 4, 1, DT_ANY,   257,   512) \
     X(88, OP_BWD, PATH_STAGED ,  512, 2,  1, 4, 1, DT_ANY,   513,  1024) \
     X(96, OP_BWD, PATH_STAGED ,  512, 3,  1, 3, 1, DT_ANY,  1025,  1536) \
-    X(97, OP_BWD, PATH_STAGED ,  512, 4,  1, 2, 1, DT_ANY,  1537,  2048) \
+    X(97, OP_BWD, PATH_STAGED ,  512, 4,  1, 2, 1, DT_BF16 | DT_F32, 1537, 2048) \
+    X(45, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 2, DT_F16,  1537,  2048) \
     X(46, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 4, DT_ANY,  2049,  4096) \
     X(47, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 8, DT_ANY,  4097,  8192) \
     X(26, OP_BWD, PATH_VECTOR ,  256, 2,  2, 1, 1, DT_ANY,     0,     0) \
@@ -78,7 +79,6 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(27, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 1, DT_ANY,     0,     0) \
     X(34, OP_BWD, PATH_VECTOR ,  512, 2,  1, 2, 1, DT_ANY,     0,     0) \
     X(42, OP_BWD, PATH_VECTOR ,  512, 3,  1, 1, 1, DT_ANY,     0,     0) \
-    X(45, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 2, DT_ANY,     0,     0) \
     X(32, OP_BWD, PATH_VECTOR ,  256, 1,  2, 2, 1, DT_ANY,     0,     0) \
     X(33, OP_BWD, PATH_VECTOR ,   16, 2, 16, 1, 1, DT_ANY,     0,     0) \
     X(35, OP_BWD, PATH_VECTOR ,  512, 2,  1, 0, 1, DT_ANY,     0,     0) \
