@@ -11,6 +11,7 @@
 // owned per call).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -85,8 +86,9 @@ static const PlanDesc *generic_plan(int op) {
 
 static int cta_threads(const PlanDesc &d) { return d.path == PATH_GENERIC ? 256 : d.tpr * d.teams; }
 
-// Largest dynamic shared memory a CTA may take (227 KB on sm_103a).
-constexpr int kMaxDynamicSmem = 227 * 1024;
+// Largest dynamic shared memory a plan may ask for: the 227 KB a CTA may
+// opt into on sm_103a, less room for the kernels' static arrays.
+constexpr int kMaxDynamicSmem = 226 * 1024;
 
 // A staged plan's shared memory: `depth` stages of x and dy (and dres for
 // the fused variant) rows of es-byte elements.
@@ -174,6 +176,41 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     const int64_t bytes = P * partial_rows(op) * N * 4;
     out->workspace_bytes = (bytes + 255) / 256 * 256;
     return RMSNORM_SUCCESS;
+}
+
+// A staged kernel takes more than 48 KB of dynamic shared memory, which
+// needs an opt-in per kernel and device. It is given once, for the most a
+// CTA of this kernel may take (the device's opt-in limit less the kernel's
+// static shared memory), so later launches make no extra runtime call. A
+// failed call's error is cleared so that it cannot surface at a later launch.
+int allow_staged_smem(const void *k) {
+    constexpr int kSlots = 256;
+    static std::mutex mu;
+    static const void *kern[kSlots];
+    static uint64_t devs[kSlots];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return (int)e;
+    std::lock_guard<std::mutex> lk(mu);
+    int i = 0;
+    for (; i < kSlots && kern[i] != nullptr && kern[i] != k; ++i) {
+    }
+    if (dev >= 0 && dev < 64 && i < kSlots && kern[i] == k && (devs[i] >> dev & 1u)) return 0;
+    int optin = 0;
+    cudaFuncAttributes fa;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return (int)e;
+    }
+    if (dev >= 0 && dev < 64 && i < kSlots) {
+        kern[i] = k;
+        devs[i] |= 1ull << dev;
+    }
+    return 0;
 }
 
 // ------------------------------------------------------ device queries --
@@ -302,9 +339,11 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
     // The dynamic shared memory of the team combine depends on N; occupancy
     // is taken for the largest N the plan serves (the conservative value).
     const int64_t nmax = d.path != PATH_GENERIC ? plan_capacity(d) * E : N;
-    const int smem = d.path == PATH_STAGED ? (int)staged_smem_bytes(d, nmax, elem_size(dt), fused)
-                                           : bwd_smem_bytes(d, nmax);
-    if (smem > kMaxDynamicSmem) return cudaErrorInvalidConfiguration;
+    // (a staged plan's rows may need less than its capacity: the occupancy
+    // query is capped at the largest shared memory a CTA may take)
+    const int smem = d.path == PATH_STAGED
+                         ? (int)std::min<int64_t>(staged_smem_bytes(d, nmax, elem_size(dt), fused), kMaxDynamicSmem)
+                         : bwd_smem_bytes(d, nmax);
     int best = 1 << 30;
     for (int pk = 0; pk < 2; ++pk) {
         // the LayerNorm, staged and generic kernels have one variant
@@ -312,7 +351,7 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
         const void *k = d.op == OP_LN_BWD ? ln_bwd_kernel(d.id, dt, fused) : bwd_kernel(d.id, dt, fused, pk != 0);
         if (!k) return cudaErrorInvalidDeviceFunction;
         if (d.path == PATH_STAGED) {  // more than 48 KB of dynamic shared memory needs an opt-in
-            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            cudaError_t e = (cudaError_t)allow_staged_smem(k);
             if (e != cudaSuccess) return e;
         }
         int n = 0;
@@ -543,6 +582,8 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     rmsnorm_status_t st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, 1, 0, force_plan, force_ctas, &plan);
     if (st != RMSNORM_SUCCESS) return st;
     const PlanDesc *d = find_plan(plan.plan_id);
+    if (d->path == PATH_STAGED && staged_smem_bytes(*d, N, (int)s, fused) > kMaxDynamicSmem)
+        return RMSNORM_ERR_UNSUPPORTED;
     int parts = 1, cps = 1;
     e = bwd_max_parts(dev, sms, dt, *d, N, fused, &parts, &cps);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -728,6 +769,9 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
     rmsnorm_plan_t plan;
     rmsnorm_status_t st = select_plan(RMSNORM_OP_LN_BWD, M, N, dt, aligned, 1, 0, force_plan, force_ctas, &plan);
     if (st != RMSNORM_SUCCESS) return st;
+    if (plan.path == PATH_STAGED &&
+        staged_smem_bytes(*find_plan(plan.plan_id), N, (int)s, fused) > kMaxDynamicSmem)
+        return RMSNORM_ERR_UNSUPPORTED;
     int parts = 1, cps = 1;
     e = bwd_max_parts(dev, sms, dt, *find_plan(plan.plan_id), N, fused, &parts, &cps);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -836,6 +836,7 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int 
 
 // ------------------------------------------------------------- dispatch --
 
+
 template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED>
 static int bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     if constexpr (CS == 1) {
@@ -876,8 +877,8 @@ template <typename T, typename TW, int TPR, int V, int S>
 static int bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     const void *k = fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, true>
                           : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, false>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return (int)e;
+    const int e = allow_staged_smem(k);
+    if (e != 0) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(TPR);
@@ -1018,8 +1019,8 @@ template <typename T, int TPR, int V, int S>
 static int ln_bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     const void *k = fused ? (const void *)layernorm_bwd_staged<T, TPR, V, S, true>
                           : (const void *)layernorm_bwd_staged<T, TPR, V, S, false>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return (int)e;
+    const int e = allow_staged_smem(k);
+    if (e != 0) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(TPR);

@@ -111,7 +111,7 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(64, OP_LN_BWD, PATH_VECTOR,  128, 1,  2, 1, 1, DT_ANY,    65,   128) \
     X(103, OP_LN_BWD, PATH_STAGED, 128, 2,  1, 6, 1, DT_ANY,   129,   256) \
     X(100, OP_LN_BWD, PATH_STAGED, 256, 2,  1, 4, 1, DT_ANY,   257,   512) \
-    X(76, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 1, DT_ANY,   513,  1024) \
+    X(112, OP_LN_BWD, PATH_STAGED, 256, 4,  1, 4, 1, DT_ANY,   513,  1024) \
     X(101, OP_LN_BWD, PATH_STAGED, 512, 3,  1, 3, 1, DT_ANY,  1025,  1536) \
     X(86, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 2, DT_ANY,  1537,  2048) \
     X(87, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 4, DT_ANY,  2049,  4096) \
@@ -131,6 +131,9 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(83, OP_LN_BWD, PATH_VECTOR,  256, 2,  2, 1, 1, DT_ANY,     0,     0) \
     X(99, OP_LN_BWD, PATH_STAGED,  512, 2,  1, 4, 1, DT_ANY,     0,     0) \
     X(102, OP_LN_BWD, PATH_STAGED, 512, 4,  1, 2, 1, DT_ANY,     0,     0) \
+    X(76, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 1, DT_ANY,     0,     0) \
+    X(113, OP_LN_BWD, PATH_STAGED, 512, 2,  1, 3, 1, DT_ANY,     0,     0) \
+    X(114, OP_LN_BWD, PATH_STAGED, 512, 2,  1, 6, 1, DT_ANY,     0,     0) \
     X(72, OP_LN_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0)
 
 // Largest CTA any plan uses.
@@ -205,6 +208,10 @@ RMSN_DECLARE_LAUNCHERS(f16w32)
 int launch_fwd8_f32(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
 int launch_fwd8_bf16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
 int launch_fwd8_f16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
+
+// Opt a staged kernel into its largest dynamic shared memory on the current
+// device (once per kernel and device); returns a cudaError_t.
+int allow_staged_smem(const void *kernel);
 
 // Parameter-gradient finalizers, by the parameters' storage type: column
 // c < split of the [parts, ncols] workspace goes to out0[c], the others to

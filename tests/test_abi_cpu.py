@@ -140,7 +140,7 @@ def test_fp32_weight_flag_plans(rn):
 
 
 @pytest.mark.parametrize("dt,N,tpr,v,cs", [(1, 64, 8, 1, 1), (1, 1024, 128, 1, 1), (1, 2048, 128, 2, 1),
-                                           (1, 4096, 256, 2, 1), (1, 8192, 512, 2, 1), (0, 8192, 512, 2, 2),
+                                           (1, 4096, 256, 2, 1), (1, 8192, 256, 4, 1), (0, 8192, 512, 2, 2),
                                            (1, 32768, 512, 2, 4), (1, 65536, 512, 2, 8)])
 def test_layernorm_backward_plans(rn, dt, N, tpr, v, cs):
     p = rn.plan_query(rn.OP_LN_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)

@@ -200,11 +200,13 @@ def test_ln_empty_batch_zeroes_parameter_grads(rn):
     assert torch.all(dg == 0) and torch.all(db == 0)
 
 
-@pytest.mark.parametrize("M,N,staged,vector", [(2049, 4096, 100, 82), (999, 8192, 99, 76), (300, 12288, 101, 86)])
+@pytest.mark.parametrize("M,N,staged,vector", [(2049, 4096, 100, 82), (999, 8192, 99, 76), (300, 12288, 101, 86),
+                                               (777, 8192, 112, 76)])
 def test_ln_staged_backward_matches_register_backward(rn, M, N, staged, vector):
-    """The staged LayerNorm backward does the register kernel's arithmetic
-    on the same chunk mapping: dx is bit-identical (dgamma and dbeta differ
-    only in how partial rows are grouped)."""
+    """The staged LayerNorm backward does the register kernel's arithmetic:
+    on the same chunk mapping dx is bit-identical (dgamma and dbeta differ
+    only in how partial rows are grouped); on another mapping the row sums
+    associate differently and the results agree to rounding."""
     d = inputs.make_inputs(M, N, "bf16", 195, beta=True, x_shift=0.5)
     x, g, b, dy = (to_dev(d[k], "bf16") for k in ("x", "w", "beta", "dy"))
     out = rn.layernorm_fwd(x, g, b)
@@ -212,7 +214,10 @@ def test_ln_staged_backward_matches_register_backward(rn, M, N, staged, vector):
     v = rn.layernorm_bwd(dy, x, g, out["mean"], out["rstd"], force_plan=vector)
     torch.cuda.synchronize()
     assert a["plan"]["path_name"] == "staged" and v["plan"]["path_name"] == "vector"
-    if v["plan"]["cluster_size"] == 1:
+    same_mapping = (v["plan"]["cluster_size"] == 1 and
+                    (a["plan"]["threads_per_row"], a["plan"]["chunks_per_thread"]) ==
+                    (v["plan"]["threads_per_row"], v["plan"]["chunks_per_thread"]))
+    if same_mapping:
         assert cuda_bits_equal(a["dx"], v["dx"])
     else:
         assert torch.allclose(a["dx"].float(), v["dx"].float(), rtol=1e-2, atol=1e-2)
