@@ -336,11 +336,6 @@ __device__ __forceinline__ uint4 lds128(const void *p) {
     return v;
 }
 
-// One plain arrival (release at CTA scope: this thread's earlier shared
-// memory reads are complete before the phase can complete).
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 // Bulk copy (the TMA engine's 1-D form) of `bytes` from global memory into
 // this CTA's shared memory, counted in bytes on `bar`. Both addresses
 // 16-byte aligned, `bytes` a multiple of 16. The kernel is launched as a
@@ -351,11 +346,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
-}
-// Barrier over the first `count` threads of the CTA (named barrier 1); the
-// other threads (a producer warp) do not take part.
-__device__ __forceinline__ void named_sync(uint32_t count) {
-    asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");
 }
 
 // Store v at the address of `local_slot` in cluster CTA `cta` and count 4
