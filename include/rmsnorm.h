@@ -379,11 +379,12 @@ rmsnorm_status_t rmsnorm_bwd_ex(const void *dy, const void *dresidual_out, const
                                 void *event_after_main, rmsnorm_plan_t *plan_used);
 
 /*
- * Device status word of the current device, for diagnostics: 0 normally; 1
- * if a backward kernel that shares rows across a thread-block cluster gave
- * up waiting for a peer's partial sum (its bounded wait expired; that call's
- * outputs are incomplete). Synchronises the device; clear != 0 resets the
- * word. Returns -1 if the device cannot be queried.
+ * Device status word of the current device, for diagnostics: 0 normally;
+ * 1 if a backward kernel gave up one of its bounded waits: a cluster row's
+ * wait for a peer's partial sum, or a staged kernel's wait for a row's bulk
+ * copy into shared memory (that call's outputs are then incomplete).
+ * Synchronises the device; clear != 0 resets the word. Returns -1 if the
+ * device cannot be queried.
  */
 int rmsnorm_device_status(int clear);
 

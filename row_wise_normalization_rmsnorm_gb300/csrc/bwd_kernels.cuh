@@ -330,7 +330,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
         // A peer's partial never arrived: record it and stop taking rows
         // (this call's outputs are incomplete). The host reads the word
         // with rmsnorm_device_status().
-        if (p.status) *p.status = kStatusClusterWaitTimeout;
+        if (p.status) *p.status = kStatusWaitTimeout;
     }
 
     // The finalizer may start launching now; it waits for this grid to
@@ -625,7 +625,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
             if (c < C) st_chunk(dx4 + base + c, pack<T>(out));
         }
     }
-    if (failed && p.status) *p.status = kStatusClusterWaitTimeout;
+    if (failed && p.status) *p.status = kStatusWaitTimeout;
 
     // The finalizer may start launching now; it waits for this grid to
     // finish (griddepcontrol.wait) before it reads the workspace.

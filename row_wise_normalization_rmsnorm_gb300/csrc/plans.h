@@ -182,8 +182,9 @@ struct BwdParams {
     const float *mean;       // LayerNorm: the forward's per-row mean
 };
 
-// Codes written to BwdParams::status.
-constexpr int kStatusClusterWaitTimeout = 1;
+// Codes written to the status word: a bounded wait (a cluster row's peer
+// partial, or a staged row's bulk copy) gave up.
+constexpr int kStatusWaitTimeout = 1;
 // Polls of an mbarrier before a wait gives up (at most seconds).
 constexpr uint32_t kWaitLimit = 1u << 22;
 
