@@ -765,15 +765,15 @@ __device__ __forceinline__ void store_param(T *out0, T *out1, int split, int c, 
     }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(256) rmsnorm_dw_finalize4(const float *ws, int parts, int N, T *dw, T *dw1,
-                                                            int split) {
-    constexpr int RG = 32;
-    __shared__ float part[RG][33];
+template <typename T, int LANES = 8, int RG = 32>
+__global__ void __launch_bounds__(LANES *RG) rmsnorm_dw_finalize4(const float *ws, int parts, int N, T *dw, T *dw1,
+                                                                  int split) {
+    constexpr int COLS = 4 * LANES;       // columns per CTA
+    __shared__ float part[RG][COLS + 1];
     wait_for_main_grid();
-    const int lane = threadIdx.x & 7;     // float4 column within the CTA's 32 columns
-    const int rg = threadIdx.x >> 3;      // row group
-    const int col = blockIdx.x * 32 + lane * 4;
+    const int lane = threadIdx.x % LANES;  // float4 column within the CTA's columns
+    const int rg = threadIdx.x / LANES;    // row group
+    const int col = blockIdx.x * COLS + lane * 4;
     const int p0 = (int)((int64_t)parts * rg / RG);
     const int p1 = (int)((int64_t)parts * (rg + 1) / RG);
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -794,8 +794,8 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize4(const float *ws, int
     part[rg][lane * 4 + 2] = s.z;
     part[rg][lane * 4 + 3] = s.w;
     __syncthreads();
-    if (threadIdx.x < 32) {
-        const int c = blockIdx.x * 32 + threadIdx.x;
+    if (threadIdx.x < COLS) {
+        const int c = blockIdx.x * COLS + threadIdx.x;
         if (c < N) {
             float tot = part[0][threadIdx.x];
 #pragma unroll
@@ -968,9 +968,12 @@ static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
 template <typename T>
 static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *dw1, int split, void *stream,
                              bool serial) {
+    constexpr int kLanes = 8, kGroups = 32;  // vector finalizer: 4 * kLanes columns a CTA
+    // float4 columns need every group of 4 on one side of the split
+    const bool vec = N % 4 == 0 && split % 4 == 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + 31) / 32));
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3(vec ? (unsigned)((N + 4 * kLanes - 1) / (4 * kLanes)) : (unsigned)((N + 31) / 32));
+    cfg.blockDim = dim3(vec ? kLanes * kGroups : 256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
@@ -980,9 +983,8 @@ static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *
     cfg.numAttrs = serial ? 0 : 1;
     T *out = static_cast<T *>(dw);
     T *out1 = static_cast<T *>(dw1);
-    // float4 columns need every group of 4 on one side of the split
-    const bool vec = N % 4 == 0 && split % 4 == 0;
-    cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize4<T>, ws, parts, N, out, out1, split)
+    cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize4<T, kLanes, kGroups>, ws, parts, N, out, out1,
+                                             split)
                         : cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize<T>, ws, parts, N, out, out1, split);
     return (int)e;
 }
