@@ -1,4 +1,6 @@
-// bwd_kernels.cuh -- RMSNorm backward kernels (plain and fused residual add).
+// bwd_kernels.cuh -- RMSNorm and LayerNorm backward kernels (plain and fused
+// residual add): the register kernel, the staged (bulk-copy) kernel, the
+// generic kernel and the parameter-gradient finalizer.
 //
 // Two launches, no global atomics and no inter-CTA waits (the kernel
 // boundary is the only grid-wide barrier), after ROCm/FlyDSL PR #855

@@ -1,6 +1,7 @@
-// common.cuh -- device helpers shared by the RMSNorm kernels: 16-byte
-// chunk access, bf16/fp32 pair conversion, packed f32x2 arithmetic and
-// team (sub-warp, warp or multi-warp) all-reduce.
+// common.cuh -- device helpers shared by the kernels: 16-byte chunk access,
+// bf16/fp16/fp32 pair conversion, packed f32x2 arithmetic, team (sub-warp,
+// warp, multi-warp) and cluster all-reduces, mbarrier waits, bulk copies
+// into shared memory and E4M3 conversion.
 #pragma once
 
 #include <cuda_bf16.h>

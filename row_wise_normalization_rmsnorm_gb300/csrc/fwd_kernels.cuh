@@ -1,4 +1,5 @@
-// fwd_kernels.cuh -- RMSNorm forward kernels (plain and fused residual add).
+// fwd_kernels.cuh -- RMSNorm forward kernels (plain and fused residual add,
+// bf16/fp16/fp32 or E4M3 output) and the LayerNorm forward.
 //
 // Vector kernel: a team of TPR threads owns one row; each thread loads V
 // 16-byte chunks of it (chunk c = v * TPR + t, so a warp's loads are

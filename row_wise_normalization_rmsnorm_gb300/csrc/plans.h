@@ -31,7 +31,7 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
 // forced (tuning and A/B tests).
 // depth (backward only): rows whose x/dy loads are in flight while the
 // current row is computed (a register ring of depth + 1 rows); for staged
-// plans the number of shared-memory stages the producer warp fills.
+// plans the number of shared-memory stages rows are streamed into.
 // cluster: CTAs of a thread-block cluster that share one row; each holds
 // threads_per_row * chunks_per_thread chunks of it in registers and the row
 // sums meet in distributed shared memory (1: no cluster).
