@@ -101,11 +101,18 @@ def peaks():
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources' code: comments and blank space are dropped
+    first, so that a change of wording alone keeps the stored counters."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_wise_normalization_rmsnorm_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8", errors="replace") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
+        h.update(f.encode() + text.encode())
     return h.hexdigest()[:16]
 
 
