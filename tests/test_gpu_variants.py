@@ -178,7 +178,7 @@ def test_in_place_aliasing(rn, dt, N):
     assert cuda_bits_equal(res, h) and cuda_bits_equal(dr, dxa)
 
 
-@pytest.mark.parametrize("dt,N", [("bf16", 2048), ("bf16", 4097), ("f32", 130)])
+@pytest.mark.parametrize("dt,N", [("bf16", 2048), ("bf16", 4097), ("f32", 130), ("bf16", 8192), ("f32", 6144)])
 def test_guard_regions_untouched(rn, dt, N):
     M, G = 301, 4096
     d, t = dev_inputs(M, N, dt, 99)
@@ -237,7 +237,7 @@ def test_forced_forward_plans_match_oracle(rn, plan):
     check_rstd(r.cpu().numpy(), f["rstd64"])
 
 
-@pytest.mark.parametrize("plan", [27, 34, 35, 36, 44, 45, 48, 49])
+@pytest.mark.parametrize("plan", [27, 34, 35, 36, 44, 45, 48, 49, 88, 89, 90, 96, 97, 98])
 def test_forced_backward_plans_match_oracle(rn, plan):
     M, N, dt = 777, 8192, "bf16"
     d, t = dev_inputs(M, N, dt, 102)
