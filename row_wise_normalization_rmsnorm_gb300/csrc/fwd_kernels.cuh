@@ -68,7 +68,7 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
 // E4M3(y * s), one byte per element, with s the given per-tensor scale or
 // 448 / max|y| of the row (a second, max-combining row reduction).
 template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED, int Q = QOUT_NONE>
-__global__ void __launch_bounds__(TPR *TEAMS)
+__global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR * TEAMS) > 0 ? 1280 / (TPR * TEAMS) : 1))
     rmsnorm_fwd_vector(const FwdParams p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
     using Pk = Pair<true>;
