@@ -270,7 +270,7 @@ def sweep_points():
     for dt in ("bf16", "f32"):
         for M, N in inputs.sweep_points(dt):
             pts.append((f"{dt} {M}x{N}", dt, M, N, False, False))
-    for M, N in ((4096, 4096), (1024, 8192)):
+    for M, N in ((4096, 4096), (1024, 8192), (4096, 16384)):
         pts.append((f"add bf16 {M}x{N}", "bf16", M, N, True, False))
     for M, N in ((16384, 8192), (4096, 8192), (16384, 16384)):
         pts.append((f"f16 {M}x{N}", "f16", M, N, False, False))
@@ -285,7 +285,7 @@ def sweep_points():
     pts.append(("fp8row bf16 4096x4096", "bf16", 4096, 4096, False, False))
     # LayerNorm (gamma and beta, dgamma and dbeta)
     for dt, M, N in (("bf16", 16384, 8192), ("bf16", 4096, 4096), ("bf16", 16384, 2048), ("f32", 16384, 4096),
-                     ("bf16", 4096, 16384)):
+                     ("bf16", 4096, 16384), ("bf16", 16384, 16384), ("bf16", 8192, 12288)):
         pts.append((f"ln {dt} {M}x{N}", dt, M, N, False, False))
     pts.append(("misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
     pts.append(("misaligned f32 4096x2048", "f32", 4096, 2048, False, True))

@@ -280,6 +280,7 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt);
 typedef enum {
     RMSNORM_PATH_VECTOR = 0,   /* 128-bit loads, row held in registers       */
     RMSNORM_PATH_STAGED = 1,   /* row staged in shared memory by bulk copies */
+                               /* (held in registers or re-read, by plan)    */
     RMSNORM_PATH_GENERIC = 2   /* any N and alignment, element loads         */
 } rmsnorm_path_t;
 

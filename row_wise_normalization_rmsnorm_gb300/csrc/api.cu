@@ -67,7 +67,7 @@ static int dtype_bit(int dt) {
 
 // Default plan for (op, dtype, chunks per row): a row-in-registers
 // (vector) or staged plan; nullptr when none covers C.
-static bool row_path(int path) { return path == PATH_VECTOR || path == PATH_STAGED; }
+static bool row_path(int path) { return path == PATH_VECTOR || staged_path(path); }
 
 static const PlanDesc *default_vector_plan(int op, int dt, int64_t C) {
     for (int i = 0; i < kNumPlans; ++i) {
@@ -91,9 +91,11 @@ static int cta_threads(const PlanDesc &d) { return d.path == PATH_GENERIC ? 256 
 constexpr int kMaxDynamicSmem = 226 * 1024;
 
 // A staged plan's shared memory: `depth` stages of x and dy (and dres for
-// the fused variant) rows of es-byte elements.
+// the fused variant) rows of es-byte elements; the LayerNorm's re-read
+// schedule also keeps gamma there.
 static int64_t staged_smem_bytes(const PlanDesc &d, int64_t N, int es, bool fused) {
-    return (int64_t)d.depth * (fused ? 3 : 2) * N * es;
+    const int64_t gamma = d.path == PATH_RESTAGED && d.op == OP_LN_BWD ? N * es : 0;
+    return (int64_t)d.depth * (fused ? 3 : 2) * N * es + gamma;
 }
 
 static int nominal_ctas_per_sm(const PlanDesc &d) {
@@ -133,7 +135,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
         if (!d || d->op != op) return RMSNORM_ERR_UNSUPPORTED;
         if (d->path == PATH_VECTOR && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
         // staged plans: backward only, aligned rows that fit, one type
-        if (d->path == PATH_STAGED && (op == RMSNORM_OP_FWD || !vec_ok || C > plan_capacity(*d)))
+        if (staged_path(d->path) && (op == RMSNORM_OP_FWD || !vec_ok || C > plan_capacity(*d)))
             return RMSNORM_ERR_UNSUPPORTED;
         // with an fp32 weight only the default plans (and the generic one) are compiled
         if (mixed_kind(kind_of(dt)) && row_path(d->path) && d->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
@@ -144,7 +146,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     if (!d) return RMSNORM_ERR_UNSUPPORTED;
 
     std::memset(out, 0, sizeof(*out));
-    out->path = d->path;
+    out->path = staged_path(d->path) ? PATH_STAGED : d->path;  // the ABI names one staged path
     out->plan_id = d->id;
     out->threads_per_row = d->path == PATH_GENERIC ? 256 : d->tpr;
     out->chunks_per_thread = d->v;
@@ -166,13 +168,13 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     out->smem_bytes = bwd_smem_bytes(*d, N);
     // dynamic shared memory stays below 48 KB with room for the kernels'
     // static arrays (a few KB at most)
-    if (d->path == PATH_STAGED) {
+    if (staged_path(d->path)) {
         // the plain variant's stages; the fused one is checked by the backward
         const int64_t sm = staged_smem_bytes(*d, N, s, false);
         if (sm > kMaxDynamicSmem) return RMSNORM_ERR_UNSUPPORTED;
         out->smem_bytes = (int32_t)sm;
     }
-    if (d->path != PATH_STAGED && out->smem_bytes > 44 * 1024) return RMSNORM_ERR_UNSUPPORTED;
+    if (!staged_path(d->path) && out->smem_bytes > 44 * 1024) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t bytes = P * partial_rows(op) * N * 4;
     out->workspace_bytes = (bytes + 255) / 256 * 256;
     return RMSNORM_SUCCESS;
@@ -341,7 +343,7 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
     const int64_t nmax = d.path != PATH_GENERIC ? plan_capacity(d) * E : N;
     // (a staged plan's rows may need less than its capacity: the occupancy
     // query is capped at the largest shared memory a CTA may take)
-    const int smem = d.path == PATH_STAGED
+    const int smem = staged_path(d.path)
                          ? (int)std::min<int64_t>(staged_smem_bytes(d, nmax, elem_size(dt), fused), kMaxDynamicSmem)
                          : bwd_smem_bytes(d, nmax);
     int best = 1 << 30;
@@ -350,7 +352,7 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
         if ((d.path != PATH_VECTOR || d.op == OP_LN_BWD) && pk == 1) continue;
         const void *k = d.op == OP_LN_BWD ? ln_bwd_kernel(d.id, dt, fused) : bwd_kernel(d.id, dt, fused, pk != 0);
         if (!k) return cudaErrorInvalidDeviceFunction;
-        if (d.path == PATH_STAGED) {  // more than 48 KB of dynamic shared memory needs an opt-in
+        if (staged_path(d.path)) {  // more than 48 KB of dynamic shared memory needs an opt-in
             cudaError_t e = (cudaError_t)allow_staged_smem(k);
             if (e != cudaSuccess) return e;
         }
@@ -424,7 +426,7 @@ int self_check_impl() {
             // a cluster row has one team per CTA, of whole warps, and at most 8 CTAs
             if (d.cs < 1 || d.cs > 8 || (d.cs > 1 && (d.teams != 1 || d.tpr < 32))) ++bad;
         }
-        if (d.path == PATH_STAGED) {
+        if (staged_path(d.path)) {
             // one team per CTA of whole warps, no cluster, at least two stages, backward only
             if (d.op == OP_FWD || d.teams != 1 || d.cs != 1 || d.depth < 2 || d.tpr % 32 != 0 || d.tpr < 64 ||
                 d.tpr > kMaxCtaThreads || d.v < 1)
@@ -582,7 +584,7 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     rmsnorm_status_t st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, 1, 0, force_plan, force_ctas, &plan);
     if (st != RMSNORM_SUCCESS) return st;
     const PlanDesc *d = find_plan(plan.plan_id);
-    if (d->path == PATH_STAGED && staged_smem_bytes(*d, N, (int)s, fused) > kMaxDynamicSmem)
+    if (staged_path(d->path) && staged_smem_bytes(*d, N, (int)s, fused) > kMaxDynamicSmem)
         return RMSNORM_ERR_UNSUPPORTED;
     int parts = 1, cps = 1;
     e = bwd_max_parts(dev, sms, dt, *d, N, fused, &parts, &cps);

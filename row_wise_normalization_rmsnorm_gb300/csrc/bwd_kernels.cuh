@@ -424,7 +424,15 @@ __global__ void __launch_bounds__(TPR *TEAMS) layernorm_bwd_vector(const BwdPara
 // Every wait is bounded: a wait that gives up records the status word and
 // the kernel carries on (its outputs are then incomplete), so every thread
 // still reaches every barrier and the kernel always ends.
-template <typename T, typename TW, int TPR, int V, int S, bool FUSED, bool LN>
+//
+// HOLD = false is the re-read schedule, for plans whose registers cannot
+// hold a row's chunks across the reduction next to the parameter-gradient
+// accumulators (the LayerNorm backward keeps two of them): both passes read
+// the chunks from the stage, so the stage stays busy until the second pass
+// ends. Each warp then counts itself done on the stage's counter and the
+// last one to arrive refills the stage; no thread waits for the others. The
+// arithmetic, and so every output bit, is that of HOLD = true.
+template <typename T, typename TW, int TPR, int V, int S, bool FUSED, bool LN, bool HOLD>
 __device__ __forceinline__ void staged_body(const BwdParams &p) {
     using Pk = Pair<true>;
     using RT = typename std::conditional<LN, float2, float>::type;  // what a row reduces
@@ -436,7 +444,11 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     static_assert(TPR % 32 == 0 && TPR >= 64, "whole warps");
     __shared__ RT red[2][W];
     __shared__ __align__(8) uint64_t full[S];
-    extern __shared__ float4 stage_smem[];  // S * NB * C chunks of 16 bytes
+    __shared__ unsigned done[HOLD ? 1 : S];  // re-read: warps through the stage's row
+    extern __shared__ float4 stage_smem[];  // S * NB * C chunks of 16 bytes (+ C for gamma)
+    // The LayerNorm re-read schedule keeps gamma in shared memory after the
+    // stages rather than in registers (its two accumulators fill them).
+    constexpr bool WSM = LN && !HOLD;
 
     const int N = p.N;
     const int C = N / E;
@@ -459,9 +471,18 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         bulk_g2s(dst + C, d4 + off, row_bytes, &full[s]);
         if (has_dres) bulk_g2s(dst + 2 * C, r4 + off, row_bytes, &full[s]);
     };
+    uint4 *wsm = stages + (size_t)S * NB * C;
+    if constexpr (WSM) {
+        if (p.w != nullptr)
+            for (int c = tid; c < C; c += TPR) wsm[c] = ld_keep(reinterpret_cast<const uint4 *>(p.w) + c);
+    }
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        if constexpr (!HOLD) {
+#pragma unroll
+            for (int s = 0; s < S; ++s) done[s] = 0;
+        }
         mbar_init_fence();
         for (int s = 0; s < S && s < iters; ++s) issue(s, s);
     }
@@ -479,14 +500,15 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     // chunks of a 2-byte type, w is held as loaded instead (one uint4 a
     // chunk) and offset + w formed when used (the same fp32 add each time),
     // which keeps the thread within its registers
-    constexpr bool RAW = V >= 3 && E == 8 && std::is_same<T, TW>::value;
+    constexpr bool RAW = V >= 3 && E == 8 && std::is_same<T, TW>::value && !WSM;
     uint4 wraw[RAW ? V : 1];
-    float2 wp[RAW ? 1 : V][NP], acc[V][NP];
+    float2 wp[RAW || WSM ? 1 : V][NP], acc[V][NP];
     float2 accb[LN ? V : 1][NP];  // LayerNorm: sum dy (dbeta)
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = v * TPR + t;
-        if constexpr (RAW) {
+        if constexpr (WSM) {
+        } else if constexpr (RAW) {
             wraw[v] = (has_w && c < C) ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + c) : make_uint4(0, 0, 0, 0);
         } else {
             float2 wv[NP];
@@ -506,8 +528,12 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         }
     }
     auto wfac = [&](int v, float2 (&f)[NP]) {
-        if constexpr (RAW) {
-            unpack<T>(wraw[v], f);
+        if constexpr (WSM || RAW) {
+            const int c = v * TPR + t;
+            if constexpr (WSM)
+                unpack<T>(has_w && c < C ? lds128(wsm + c) : make_uint4(0, 0, 0, 0), f);
+            else
+                unpack<T>(wraw[v], f);
 #pragma unroll
             for (int q = 0; q < NP; ++q) f[q] = has_w ? Pk::add(o2, f[q]) : make_float2(1.f, 1.f);
         } else {
@@ -531,16 +557,25 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
             if constexpr (LN) mu_next = p.mean[row + G];
         }
         if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
+        const int sk = s;  // this row's stage
         const uint4 *src = stages + (size_t)s * NB * C;
-        uint4 xv[V], dv[V], rv[FUSED ? V : 1];
+        // HOLD: the row's chunks, read once and kept for both passes
+        uint4 xv[HOLD ? V : 1], dv[HOLD ? V : 1], rv[FUSED && HOLD ? V : 1];
+        if constexpr (HOLD) {
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
-            const int c = v * TPR + t;
-            const bool in = c < C;
-            xv[v] = in ? lds128(src + c) : make_uint4(0, 0, 0, 0);
-            dv[v] = in ? lds128(src + C + c) : make_uint4(0, 0, 0, 0);
-            if constexpr (FUSED) rv[v] = (in && has_dres) ? lds128(src + 2 * C + c) : make_uint4(0, 0, 0, 0);
+            for (int v = 0; v < V; ++v) {
+                const int c = v * TPR + t;
+                const bool in = c < C;
+                xv[v] = in ? lds128(src + c) : make_uint4(0, 0, 0, 0);
+                dv[v] = in ? lds128(src + C + c) : make_uint4(0, 0, 0, 0);
+                if constexpr (FUSED) rv[v] = (in && has_dres) ? lds128(src + 2 * C + c) : make_uint4(0, 0, 0, 0);
+            }
         }
+        // chunk v of the stage's x (b = 0), dy (1) or dres (2) row
+        auto chunk = [&](int b, int v) {
+            const int c = v * TPR + t;
+            return c < C ? lds128(src + b * C + c) : make_uint4(0, 0, 0, 0);
+        };
 
         const float2 r2 = make_float2(r, r);
         const float2 nmu2 = make_float2(-mu, -mu);  // LayerNorm: x - mean as x + (-mean)
@@ -548,8 +583,8 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             float2 xf[NP], df[NP], wf[NP];
-            unpack<T>(xv[v], xf);
-            unpack<T>(dv[v], df);
+            unpack<T>(HOLD ? xv[HOLD ? v : 0] : chunk(0, v), xf);
+            unpack<T>(HOLD ? dv[HOLD ? v : 0] : chunk(1, v), df);
             wfac(v, wf);
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
@@ -576,7 +611,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         if (lane == 0) slots[t >> 5] = part;
         __syncthreads();
         // every warp has copied stage s into registers: refill it with row k + S
-        if (tid == 0 && k + S < iters) {
+        if (HOLD && tid == 0 && k + S < iters) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(k + S, s);
         }
@@ -602,8 +637,8 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         for (int v = 0; v < V; ++v) {
             const int c = v * TPR + t;
             float2 xf[NP], df[NP], out[NP], wf[NP];
-            unpack<T>(xv[v], xf);
-            unpack<T>(dv[v], df);
+            unpack<T>(HOLD ? xv[HOLD ? v : 0] : chunk(0, v), xf);
+            unpack<T>(HOLD ? dv[HOLD ? v : 0] : chunk(1, v), df);
             wfac(v, wf);
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
@@ -619,12 +654,27 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
             if constexpr (FUSED) {
                 if (has_dres) {
                     float2 rf[NP];
-                    unpack<T>(rv[v], rf);
+                    unpack<T>(HOLD ? rv[HOLD ? v : 0] : chunk(2, v), rf);
 #pragma unroll
                     for (int q = 0; q < NP; ++q) out[q] = Pk::add(out[q], rf[q]);
                 }
             }
             if (c < C) st_chunk(dx4 + base + c, pack<T>(out));
+        }
+        if constexpr (!HOLD) {
+            // re-read: the warp is through stage sk; the last warp to say so
+            // refills it with row k + S (the fences order every warp's reads
+            // of the stage before the bulk copies that overwrite it)
+            __syncwarp();
+            if (lane == 0 && k + S < iters) {
+                __threadfence_block();
+                if (atomicAdd(&done[sk], 1u) == (unsigned)(W - 1)) {
+                    __threadfence_block();
+                    done[sk] = 0;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue(k + S, sk);
+                }
+            }
         }
     }
     if (failed && p.status) *p.status = kStatusWaitTimeout;
@@ -654,14 +704,14 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     }
 }
 
-template <typename T, typename TW, int TPR, int V, int S, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int S, bool FUSED, bool HOLD>
 __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) {
-    staged_body<T, TW, TPR, V, S, FUSED, false>(p);
+    staged_body<T, TW, TPR, V, S, FUSED, false, HOLD>(p);
 }
 
-template <typename T, int TPR, int V, int S, bool FUSED>
+template <typename T, int TPR, int V, int S, bool FUSED, bool HOLD>
 __global__ void __launch_bounds__(TPR, 1) layernorm_bwd_staged(const BwdParams p) {
-    staged_body<T, T, TPR, V, S, FUSED, true>(p);
+    staged_body<T, T, TPR, V, S, FUSED, true, HOLD>(p);
 }
 
 // Generic main kernel: one 256-thread CTA per row at a time, element loads,
@@ -875,10 +925,10 @@ constexpr bool bwd_instantiated() {
 
 // Staged kernel: launched as a cluster of one CTA (its bulk copies name a
 // shared::cluster destination) with the stages' dynamic shared memory.
-template <typename T, typename TW, int TPR, int V, int S>
+template <typename T, typename TW, int TPR, int V, int S, bool HOLD>
 static int bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    const void *k = fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, true>
-                          : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, false>;
+    const void *k = fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, true, HOLD>
+                          : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, false, HOLD>;
     const int e = allow_staged_smem(k);
     if (e != 0) return e;
     cudaLaunchConfig_t cfg = {};
@@ -893,8 +943,8 @@ static int bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, true>, p)
-                 : (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, false>, p);
+    return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, true, HOLD>, p)
+                 : (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, false, HOLD>, p);
 }
 
 template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
@@ -910,8 +960,8 @@ static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int gri
     } else if constexpr (PATH == PATH_VECTOR) {
         return packed ? bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, true>(fused, p, grid, smem, s)
                       : bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, false>(fused, p, grid, smem, s);
-    } else if constexpr (PATH == PATH_STAGED && TEAMS == 1 && CS == 1) {
-        return bwd_launch_staged<T, TW, TPR, V, D>(fused, p, grid, smem, s);
+    } else if constexpr (staged_path(PATH) && TEAMS == 1 && CS == 1) {
+        return bwd_launch_staged<T, TW, TPR, V, D, PATH == PATH_STAGED>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
@@ -929,9 +979,9 @@ static const void *bwd_ptr_entry(bool fused, bool packed) {
                          : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, false>;
         return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, true>
                      : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, false>;
-    } else if constexpr (PATH == PATH_STAGED && TEAMS == 1 && CS == 1) {
-        return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, true>
-                     : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, false>;
+    } else if constexpr (staged_path(PATH) && TEAMS == 1 && CS == 1) {
+        return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, true, PATH == PATH_STAGED>
+                     : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, false, PATH == PATH_STAGED>;
     } else {
         return nullptr;
     }
@@ -1019,10 +1069,10 @@ static int ln_bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem,
     }
 }
 
-template <typename T, int TPR, int V, int S>
+template <typename T, int TPR, int V, int S, bool HOLD>
 static int ln_bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    const void *k = fused ? (const void *)layernorm_bwd_staged<T, TPR, V, S, true>
-                          : (const void *)layernorm_bwd_staged<T, TPR, V, S, false>;
+    const void *k = fused ? (const void *)layernorm_bwd_staged<T, TPR, V, S, true, HOLD>
+                          : (const void *)layernorm_bwd_staged<T, TPR, V, S, false, HOLD>;
     const int e = allow_staged_smem(k);
     if (e != 0) return e;
     cudaLaunchConfig_t cfg = {};
@@ -1037,8 +1087,8 @@ static int ln_bwd_launch_staged(bool fused, const BwdParams &p, int grid, int sm
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return fused ? (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, true>, p)
-                 : (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, false>, p);
+    return fused ? (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, true, HOLD>, p)
+                 : (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, false, HOLD>, p);
 }
 
 template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
@@ -1053,8 +1103,8 @@ static int ln_bwd_launch_entry(bool fused, const BwdParams &p, int grid, int sme
         return (int)cudaGetLastError();
     } else if constexpr (PATH == PATH_VECTOR) {
         return ln_bwd_launch_vec<T, TPR, V, TEAMS, D, CS>(fused, p, grid, smem, s);
-    } else if constexpr (PATH == PATH_STAGED && TEAMS == 1 && CS == 1) {
-        return ln_bwd_launch_staged<T, TPR, V, D>(fused, p, grid, smem, s);
+    } else if constexpr (staged_path(PATH) && TEAMS == 1 && CS == 1) {
+        return ln_bwd_launch_staged<T, TPR, V, D, PATH == PATH_STAGED>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
@@ -1069,9 +1119,9 @@ static const void *ln_bwd_ptr_entry(bool fused) {
     } else if constexpr (PATH == PATH_VECTOR) {
         return fused ? (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true>
                      : (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false>;
-    } else if constexpr (PATH == PATH_STAGED && TEAMS == 1 && CS == 1) {
-        return fused ? (const void *)layernorm_bwd_staged<T, TPR, V, D, true>
-                     : (const void *)layernorm_bwd_staged<T, TPR, V, D, false>;
+    } else if constexpr (staged_path(PATH) && TEAMS == 1 && CS == 1) {
+        return fused ? (const void *)layernorm_bwd_staged<T, TPR, V, D, true, PATH == PATH_STAGED>
+                     : (const void *)layernorm_bwd_staged<T, TPR, V, D, false, PATH == PATH_STAGED>;
     } else {
         return nullptr;
     }

@@ -20,7 +20,12 @@ namespace rmsn {
 // plans the LayerNorm backward, whose rows carry two sums and two parameter
 // gradients (more registers per chunk than the RMSNorm backward).
 enum PlanOp { OP_FWD = 0, OP_BWD = 1, OP_LN_BWD = 2 };
-enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2 };
+// PATH_STAGED and PATH_RESTAGED stream rows into shared memory; the first
+// copies a row's chunks into registers for both passes, the second reads
+// them from the stage in each pass (fewer registers, the stage stays busy
+// for the whole row). The C ABI reports both as the staged path.
+enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2, PATH_RESTAGED = 3 };
+constexpr bool staged_path(int path) { return path == PATH_STAGED || path == PATH_RESTAGED; }
 // Storage types a default plan applies to (bit 0: fp32, bit 1: bf16,
 // bit 2: fp16; DT_16 = both 2-byte types).
 enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
@@ -60,7 +65,9 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     /* forward, any N and alignment */ \
     X(16, OP_FWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0) \
     /* backward main kernel, persistent: rows in registers (vector) or \
-       streamed into `depth` shared-memory stages by bulk copies (staged) */ \
+       streamed into `depth` shared-memory stages by bulk copies (staged; \
+       re-read from the stage in both passes from 1025 chunks on, where \
+       holding four chunks a thread in registers spills) */ \
     X(20, OP_BWD, PATH_VECTOR ,    8, 1, 32, 1, 1, DT_ANY,     1,     8) \
     X(21, OP_BWD, PATH_VECTOR ,   16, 1, 16, 1, 1, DT_ANY,     9,    16) \
     X(22, OP_BWD, PATH_VECTOR ,   32, 1,  8, 1, 1, DT_ANY,    17,    32) \
@@ -69,12 +76,14 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(25, OP_BWD, PATH_VECTOR ,  128, 2,  2, 1, 1, DT_ANY,   129,   256) \
     X(95, OP_BWD, PATH_STAGED ,  256, 2,  1, 4, 1, DT_ANY,   257,   512) \
     X(88, OP_BWD, PATH_STAGED ,  512, 2,  1, 4, 1, DT_ANY,   513,  1024) \
-    X(96, OP_BWD, PATH_STAGED ,  512, 3,  1, 3, 1, DT_ANY,  1025,  1536) \
-    X(97, OP_BWD, PATH_STAGED ,  512, 4,  1, 2, 1, DT_BF16 | DT_F32, 1537, 2048) \
-    X(45, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 2, DT_F16,  1537,  2048) \
+    X(121, OP_BWD, PATH_RESTAGED, 512, 3, 1, 3, 1, DT_ANY,  1025,  1536) \
+    X(118, OP_BWD, PATH_RESTAGED, 512, 4, 1, 2, 1, DT_ANY,  1537,  2048) \
     X(46, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 4, DT_ANY,  2049,  4096) \
     X(47, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 8, DT_ANY,  4097,  8192) \
     X(26, OP_BWD, PATH_VECTOR ,  256, 2,  2, 1, 1, DT_ANY,     0,     0) \
+    X(96, OP_BWD, PATH_STAGED ,  512, 3,  1, 3, 1, DT_ANY,     0,     0) \
+    X(97, OP_BWD, PATH_STAGED ,  512, 4,  1, 2, 1, DT_ANY,     0,     0) \
+    X(45, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 2, DT_ANY,     0,     0) \
     X(38, OP_BWD, PATH_VECTOR ,  256, 2,  2, 2, 1, DT_ANY,     0,     0) \
     X(27, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 1, DT_ANY,     0,     0) \
     X(34, OP_BWD, PATH_VECTOR ,  512, 2,  1, 2, 1, DT_ANY,     0,     0) \
@@ -100,10 +109,12 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(93, OP_BWD, PATH_STAGED ,  256, 1,  1, 8, 1, DT_ANY,     0,     0) \
     X(94, OP_BWD, PATH_STAGED ,  128, 2,  1, 8, 1, DT_ANY,     0,     0) \
     X(98, OP_BWD, PATH_STAGED ,  512, 3,  1, 2, 1, DT_ANY,     0,     0) \
+    X(119, OP_BWD, PATH_RESTAGED, 512, 4, 1, 3, 1, DT_ANY,     0,     0) \
     /* backward main kernel, any N and alignment */ \
     X(36, OP_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0) \
-    /* LayerNorm backward main kernel, persistent, row in registers: two \
-       chunks a thread where the row allows (more bytes in flight a thread) */ \
+    /* LayerNorm backward main kernel, persistent, row in registers (two \
+       chunks a thread where the row allows) or staged; from 1025 chunks of \
+       a 2-byte type on the re-read schedule with gamma in shared memory */ \
     X(60, OP_LN_BWD, PATH_VECTOR,    8, 1, 32, 1, 1, DT_ANY,     1,     8) \
     X(61, OP_LN_BWD, PATH_VECTOR,   16, 1, 16, 1, 1, DT_ANY,     9,    16) \
     X(62, OP_LN_BWD, PATH_VECTOR,   32, 1,  8, 1, 1, DT_ANY,    17,    32) \
@@ -112,11 +123,13 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(103, OP_LN_BWD, PATH_STAGED, 128, 2,  1, 6, 1, DT_ANY,   129,   256) \
     X(100, OP_LN_BWD, PATH_STAGED, 256, 2,  1, 4, 1, DT_ANY,   257,   512) \
     X(112, OP_LN_BWD, PATH_STAGED, 256, 4,  1, 4, 1, DT_ANY,   513,  1024) \
-    X(101, OP_LN_BWD, PATH_STAGED, 512, 3,  1, 3, 1, DT_ANY,  1025,  1536) \
-    X(86, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 2, DT_ANY,  1537,  2048) \
+    X(101, OP_LN_BWD, PATH_STAGED, 512, 3,  1, 3, 1, DT_F32,  1025,  1536) \
+    X(122, OP_LN_BWD, PATH_RESTAGED, 512, 3, 1, 2, 1, DT_16,  1025,  1536) \
+    X(116, OP_LN_BWD, PATH_RESTAGED, 512, 4, 1, 2, 1, DT_ANY,  1537,  2048) \
     X(87, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 4, DT_ANY,  2049,  4096) \
     X(70, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 8, DT_ANY,  4097,  8192) \
     X(81, OP_LN_BWD, PATH_VECTOR,  128, 2,  2, 1, 1, DT_ANY,     0,     0) \
+    X(86, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 2, DT_ANY,     0,     0) \
     X(82, OP_LN_BWD, PATH_VECTOR,  256, 2,  1, 1, 1, DT_ANY,     0,     0) \
     X(65, OP_LN_BWD, PATH_VECTOR,  256, 1,  1, 1, 1, DT_ANY,     0,     0) \
     X(66, OP_LN_BWD, PATH_VECTOR,  512, 1,  1, 1, 1, DT_ANY,     0,     0) \
@@ -134,6 +147,9 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(76, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 1, DT_ANY,     0,     0) \
     X(113, OP_LN_BWD, PATH_STAGED, 512, 2,  1, 3, 1, DT_ANY,     0,     0) \
     X(114, OP_LN_BWD, PATH_STAGED, 512, 2,  1, 6, 1, DT_ANY,     0,     0) \
+    X(115, OP_LN_BWD, PATH_RESTAGED, 512, 4, 1, 3, 1, DT_ANY,    0,     0) \
+    X(117, OP_LN_BWD, PATH_RESTAGED, 512, 3, 1, 3, 1, DT_ANY,    0,     0) \
+    X(120, OP_LN_BWD, PATH_RESTAGED, 512, 2, 1, 4, 1, DT_ANY,    0,     0) \
     X(72, OP_LN_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0)
 
 // Largest CTA any plan uses.

@@ -85,13 +85,18 @@ def test_staged_backward_defaults(rn):
     rows, a partial row per CTA."""
     for dt, N, tpr, v, stages in ((1, 4096, 256, 2, 4), (1, 8192, 512, 2, 4), (0, 4096, 512, 2, 4),
                                   (1, 12288, 512, 3, 3), (1, 16384, 512, 4, 2), (0, 8192, 512, 4, 2),
-                                  (2, 8192, 512, 2, 4)):
+                                  (2, 8192, 512, 2, 4), (2, 16384, 512, 4, 2)):
         p = rn.plan_query(rn.OP_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)
         assert p["path_name"] == "staged", (dt, N, p)
         assert (p["threads_per_row"], p["chunks_per_thread"], p["cluster_size"]) == (tpr, v, 1)
         es = 4 if dt == 0 else 2
         assert p["smem_bytes"] == stages * 2 * N * es        # plain variant: x and dy rows
         assert p["ctas"] == 152 and p["ws_rows"] == 152
+    # the LayerNorm backward's re-read stages keep gamma after the stages
+    for dt, N, stages, extra in ((1, 16384, 2, 1), (2, 12288, 2, 1), (0, 6144, 3, 0)):
+        p = rn.plan_query(rn.OP_LN_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)
+        es = 4 if dt == 0 else 2
+        assert p["path_name"] == "staged" and p["smem_bytes"] == (2 * stages + extra) * N * es, (dt, N, p)
     # the same rows with an fp32 weight take the same plans
     assert rn.plan_query(rn.OP_BWD, 16384, 8192, rn.RMSNORM_BF16 | rn.RMSNORM_WEIGHT_F32)["path_name"] == "staged"
     # misaligned rows still take the generic kernel; short rows stay in registers
@@ -140,7 +145,8 @@ def test_fp32_weight_flag_plans(rn):
 
 
 @pytest.mark.parametrize("dt,N,tpr,v,cs", [(1, 64, 8, 1, 1), (1, 1024, 128, 1, 1), (1, 2048, 128, 2, 1),
-                                           (1, 4096, 256, 2, 1), (1, 8192, 256, 4, 1), (0, 8192, 512, 2, 2),
+                                           (1, 4096, 256, 2, 1), (1, 8192, 256, 4, 1), (0, 8192, 512, 4, 1),
+                                           (1, 16384, 512, 4, 1), (1, 12288, 512, 3, 1),
                                            (1, 32768, 512, 2, 4), (1, 65536, 512, 2, 8)])
 def test_layernorm_backward_plans(rn, dt, N, tpr, v, cs):
     p = rn.plan_query(rn.OP_LN_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)

@@ -225,3 +225,44 @@ def test_ln_staged_backward_matches_register_backward(rn, M, N, staged, vector):
     assert torch.allclose(a["dbeta"].float(), v["dbeta"].float(), rtol=1e-2, atol=1e-2)
     assert rn.lib().rmsnorm_device_status(1) == 0
 
+
+@pytest.mark.parametrize("M,N,reread,held", [(1001, 16384, 116, 102), (300, 8192, 115, 102), (517, 12288, 122, 101),
+                                             (777, 8192, 120, 99), (45, 6144, 120, 99)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_ln_reread_staged_backward_matches_held_bitwise(rn, M, N, reread, held, fused):
+    """The LayerNorm backward's re-read staged schedule (chunks read from
+    the stage in each pass, so the two parameter-gradient accumulators fit
+    in registers) gives the held schedule's dx, dgamma and dbeta bit for bit
+    on the same geometry and number of partial rows."""
+    d = inputs.make_inputs(M, N, "bf16", 240 + N % 7, beta=True, x_shift=0.5, residual=fused, dres=fused)
+    x, g, b, dy = (to_dev(d[k], "bf16") for k in ("x", "w", "beta", "dy"))
+    dres = to_dev(d["dres"], "bf16") if fused else None
+    out = rn.layernorm_fwd(x, g, b)
+    a = rn.layernorm_bwd(dy, x, g, out["mean"], out["rstd"], dresidual_out=dres, force_plan=reread,
+                         force_ctas=100)
+    v = rn.layernorm_bwd(dy, x, g, out["mean"], out["rstd"], dresidual_out=dres, force_plan=held,
+                         force_ctas=100)
+    torch.cuda.synchronize()
+    assert a["plan"]["plan_id"] == reread and a["plan"]["path_name"] == "staged"
+    assert a["plan"]["ctas"] == v["plan"]["ctas"] == min(100, M)
+    for k in ("dx", "dgamma", "dbeta"):
+        assert cuda_bits_equal(a[k], v[k]), k
+    assert rn.lib().rmsnorm_device_status(1) == 0
+
+
+@pytest.mark.parametrize("plan,N", [(115, 12288), (116, 16384), (117, 12288), (120, 8192), (122, 10240)])
+def test_ln_forced_reread_plans_match_oracle(rn, plan, N):
+    M, dt = 203, "bf16"
+    d = inputs.make_inputs(M, N, dt, 250 + plan, beta=True, x_shift=0.5)
+    x, g, b, dy = (to_dev(d[k], dt) for k in ("x", "w", "beta", "dy"))
+    f = oracle.ln_fwd(d["x"], d["w"], d["beta"], dtype=dt, eps=1e-5, offset=0.0)
+    mean = torch.from_numpy(f["mean32"]).cuda()
+    rstd = torch.from_numpy(f["rstd32"]).cuda()
+    o = rn.layernorm_bwd(dy, x, g, mean, rstd, force_plan=plan)
+    assert o["plan"]["plan_id"] == plan
+    r = oracle.ln_bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=1e-5, offset=0.0, mean=f["mean32"], rstd=f["rstd32"])
+    torch.cuda.synchronize()
+    check_dx(to_host(o["dx"], dt), r, dt)
+    check_param_grad(to_host(o["dgamma"], dt), r["dg64"], r["dg_abs"], dt)
+    check_param_grad(to_host(o["dbeta"], dt), r["db64"], r["db_abs"], dt)
+

@@ -40,7 +40,7 @@ def test_packed_matches_scalar_bitwise(rn, dt, M, N, fused):
     # (the staged kernel has the packed variant only)
     code = {"bf16": rn.RMSNORM_BF16, "f32": rn.RMSNORM_F32, "f16": rn.RMSNORM_F16}[dt]
     default = rn.plan_query(rn.OP_BWD, M, N, code)
-    plan = {88: 27, 95: 26, 96: 42, 97: 45}.get(default["plan_id"], -1) if default["path_name"] == "staged" else -1
+    plan = {88: 27, 95: 26, 121: 42, 118: 45}.get(default["plan_id"], -1) if default["path_name"] == "staged" else -1
     kw = dict(dresidual_out=t.get("dres"), fused=fused, force_plan=plan)
     dx1, dw1, p1 = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], rstd, force_packed=1, **kw)
     dx0, dw0, p0 = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], rstd, force_packed=0, **kw)
@@ -237,7 +237,7 @@ def test_forced_forward_plans_match_oracle(rn, plan):
     check_rstd(r.cpu().numpy(), f["rstd64"])
 
 
-@pytest.mark.parametrize("plan", [27, 34, 35, 36, 44, 45, 48, 49, 88, 89, 90, 96, 97, 98])
+@pytest.mark.parametrize("plan", [27, 34, 35, 36, 44, 45, 48, 49, 88, 89, 90, 96, 97, 98, 118, 119, 121])
 def test_forced_backward_plans_match_oracle(rn, plan):
     M, N, dt = 777, 8192, "bf16"
     d, t = dev_inputs(M, N, dt, 102)
@@ -317,5 +317,30 @@ def test_staged_backward_matches_register_backward_bitwise(rn, dt, M, N, staged,
         assert cuda_bits_equal(a_dw, b_dw)
     else:
         assert torch.allclose(a_dw.float(), b_dw.float(), rtol=1e-2, atol=1e-3)
+    assert rn.lib().rmsnorm_device_status(1) == 0
+
+
+@pytest.mark.parametrize("dt,M,N,reread,held", [("bf16", 1001, 16384, 118, 97), ("f16", 333, 12288, 119, 97),
+                                                ("f32", 517, 8192, 118, 97), ("bf16", 61, 12288, 119, 97)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_reread_staged_backward_matches_held_bitwise(rn, dt, M, N, reread, held, fused):
+    """The re-read schedule of the staged backward (both passes read the
+    row from its shared-memory stage; the last warp through a stage refills
+    it) does the held schedule's arithmetic on the same geometry: dx and dW
+    are bit-identical for the same number of partial rows, whatever the
+    stage count."""
+    d = inputs.make_inputs(M, N, dt, 230 + N % 5, residual=fused, dres=fused)
+    x, dy, w = (to_dev(d[k], dt) for k in ("x", "dy", "w"))
+    dres = to_dev(d["dres"], dt) if fused else None
+    _, rstd = rn.rmsnorm_fwd(x, w)
+    a_dx, a_dw, ap = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dresidual_out=dres, fused=fused, force_plan=reread,
+                                       force_ctas=120)
+    b_dx, b_dw, bp = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dresidual_out=dres, fused=fused, force_plan=held,
+                                       force_ctas=120)
+    torch.cuda.synchronize()
+    assert ap["plan_id"] == reread and ap["path_name"] == "staged" and bp["plan_id"] == held
+    assert ap["ctas"] == bp["ctas"] == min(120, M)
+    assert cuda_bits_equal(a_dx, b_dx)
+    assert cuda_bits_equal(a_dw, b_dw)
     assert rn.lib().rmsnorm_device_status(1) == 0
 
