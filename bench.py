@@ -289,6 +289,9 @@ def sweep_points():
         pts.append((f"ln {dt} {M}x{N}", dt, M, N, False, False))
     pts.append(("misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
     pts.append(("misaligned f32 4096x2048", "f32", 4096, 2048, False, True))
+    pts.append(("ln misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
+    # a row length that is no multiple of 16 bytes: the generic kernels
+    pts.append(("oddn bf16 4096x7169", "bf16", 4096, 7169, False, False))
     pts.append(("wide f32 16384x6144", "f32", 16384, 6144, False, False))
     pts.append(("small f32 64x256", "f32", 64, 256, False, False))
     return pts

@@ -714,18 +714,26 @@ __global__ void __launch_bounds__(TPR, 1) layernorm_bwd_staged(const BwdParams p
     staged_body<T, T, TPR, V, S, FUSED, true, HOLD>(p);
 }
 
-// Generic main kernel: one 256-thread CTA per row at a time, element loads,
-// each row read twice (the second read is served by L1/L2). The CTA's dW
-// partial row lives in the workspace itself: the thread that owns column j
-// writes ws[cta, j] on its first row and updates it on later rows, so no
-// other thread touches it and no atomics are needed.
+// Generic main kernel: one 256-thread CTA per row at a time, any N and
+// alignment, each row read twice (the second read is served by L1/L2). The
+// CTA's dW partial row lives in the workspace itself: the thread that
+// handles column j writes ws[cta, j] on the CTA's first row and updates it
+// on later rows; the row reduction's barrier orders those updates, so no
+// atomics are needed. Rows split by x's address into an element-wise head,
+// 16-byte chunks and an element-wise tail; dy, dx and dres take 16-byte
+// accesses where they share x's address mod 16. The workspace is updated
+// one column a thread (coalesced) in a loop of its own.
 template <typename T, typename TW, bool FUSED>
 __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
     __shared__ float red[32];
+    constexpr int NP = Elem<T>::NP;
     const int N = p.N;
     const TW *w = reinterpret_cast<const TW *>(p.w);
     float *wsrow = p.ws + (int64_t)blockIdx.x * N;
     const bool has_dres = FUSED && p.dres != nullptr;
+    const uint32_t a16 = addr_mod16(p.x);
+    const bool vdy = addr_mod16(p.dy) == a16, vdx = addr_mod16(p.dx) == a16;
+    const bool vdr = has_dres && addr_mod16(p.dres) == a16;
     bool first = true;
     for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
         const T *x = reinterpret_cast<const T *>(p.x) + row * N;
@@ -733,36 +741,92 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
         const T *dr = reinterpret_cast<const T *>(p.dres) + row * N;
         T *dx = reinterpret_cast<T *>(p.dx) + row * N;
         const float r = p.rstd[row];
+        const RowSplit sp = row_split(x, N, true);
+        // the chunk at column j0: dy, x and the weight factors
+        auto chunk = [&](int64_t j0, float2 (&dv)[NP], float2 (&xv)[NP], float2 (&wf)[NP]) {
+            load_chunk_at(dy, j0, vdy, dv);
+            load_chunk_at(x, j0, true, xv);
+            if (w) {
+                w_chunk_at<T, TW>(w, (int)j0, wf);
+#pragma unroll
+                for (int q = 0; q < NP; ++q) wf[q] = make_float2(__fadd_rn(p.offset, wf[q].x), __fadd_rn(p.offset, wf[q].y));
+            }
+        };
         float dot = 0.f;
-        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        auto dot_elem = [&](int j) {
             const float dyj = load_elem(dy, j);
             const float g = w ? __fmul_rn(dyj, __fadd_rn(p.offset, load_w(w, j))) : dyj;
             dot = __fmaf_rn(g, __fmul_rn(load_elem(x, j), r), dot);
+        };
+        for (int j = threadIdx.x; j < sp.head; j += blockDim.x) dot_elem(j);
+        for (int c = threadIdx.x; c < sp.nb; c += blockDim.x) {
+            float2 dv[NP], xv[NP], wf[NP];
+            chunk(sp.head + (int64_t)c * Elem<T>::E, dv, xv, wf);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const float gx = w ? __fmul_rn(dv[q].x, wf[q].x) : dv[q].x;
+                const float gy = w ? __fmul_rn(dv[q].y, wf[q].y) : dv[q].y;
+                dot = __fmaf_rn(gx, __fmul_rn(xv[q].x, r), dot);
+                dot = __fmaf_rn(gy, __fmul_rn(xv[q].y, r), dot);
+            }
+        }
+        for (int j = sp.tail0 + threadIdx.x; j < N; j += blockDim.x) dot_elem(j);
+        // the dW partial, one column a thread (coalesced; the reads are L1
+        // hits), before the reduction's barrier: dx may overwrite dy later
+        if (w) {
+            for (int j = threadIdx.x; j < N; j += blockDim.x) {
+                const float dyj = load_elem(dy, j), xh = __fmul_rn(load_elem(x, j), r);
+                wsrow[j] = first ? __fmul_rn(dyj, xh) : __fmaf_rn(dyj, xh, wsrow[j]);
+            }
         }
         const float cm = -__fdiv_rn(cta_allreduce(dot, red), (float)N);
-        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        // dx of column j from xhat_j and g_j
+        auto out_elem = [&](float xh, float g, float drj) {
+            float d = __fmul_rn(__fmaf_rn(xh, cm, g), r);
+            if (has_dres) d = __fadd_rn(d, drj);
+            return d;
+        };
+        auto dx_elem = [&](int j) {
             const float dyj = load_elem(dy, j);
             const float xh = __fmul_rn(load_elem(x, j), r);
             const float g = w ? __fmul_rn(dyj, __fadd_rn(p.offset, load_w(w, j))) : dyj;
-            float d = __fmul_rn(__fmaf_rn(xh, cm, g), r);
-            if (has_dres) d = __fadd_rn(d, load_elem(dr, j));
-            store_elem(dx, j, d);
-            if (w) wsrow[j] = first ? __fmul_rn(dyj, xh) : __fmaf_rn(dyj, xh, wsrow[j]);
+            store_elem(dx, j, out_elem(xh, g, has_dres ? load_elem(dr, j) : 0.f));
+        };
+        for (int j = threadIdx.x; j < sp.head; j += blockDim.x) dx_elem(j);
+        for (int c = threadIdx.x; c < sp.nb; c += blockDim.x) {
+            const int64_t j0 = sp.head + (int64_t)c * Elem<T>::E;
+            float2 dv[NP], xv[NP], wf[NP], rv[NP];
+            chunk(j0, dv, xv, wf);
+            if (has_dres) load_chunk_at(dr, j0, vdr, rv);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const float xhx = __fmul_rn(xv[q].x, r), xhy = __fmul_rn(xv[q].y, r);
+                const float gx = w ? __fmul_rn(dv[q].x, wf[q].x) : dv[q].x;
+                const float gy = w ? __fmul_rn(dv[q].y, wf[q].y) : dv[q].y;
+                xv[q] = make_float2(out_elem(xhx, gx, has_dres ? rv[q].x : 0.f), out_elem(xhy, gy, has_dres ? rv[q].y : 0.f));
+            }
+            store_chunk_at(dx, j0, vdx, xv);
         }
+        for (int j = sp.tail0 + threadIdx.x; j < N; j += blockDim.x) dx_elem(j);
         first = false;
     }
 }
 
 // Generic LayerNorm backward, same scheme: per row the pair (sum g,
 // sum g (x - mean)), then dx; the partial row ws[cta, 0..2N) holds dgamma
-// and dbeta, each column owned by one thread.
+// and dbeta, updated one column a thread.
 template <typename T, bool FUSED>
 __global__ void __launch_bounds__(256) layernorm_bwd_generic(const BwdParams p) {
     __shared__ float2 red[32];
+    constexpr int E = Elem<T>::E;
+    constexpr int NP = Elem<T>::NP;
     const int N = p.N;
     const T *w = reinterpret_cast<const T *>(p.w);
     float *wsrow = p.ws ? p.ws + (int64_t)blockIdx.x * 2 * N : nullptr;
     const bool has_dres = FUSED && p.dres != nullptr;
+    const uint32_t a16 = addr_mod16(p.x);
+    const bool vdy = addr_mod16(p.dy) == a16, vdx = addr_mod16(p.dx) == a16;
+    const bool vdr = has_dres && addr_mod16(p.dres) == a16;
     bool first = true;
     for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
         const T *x = reinterpret_cast<const T *>(p.x) + row * N;
@@ -771,28 +835,65 @@ __global__ void __launch_bounds__(256) layernorm_bwd_generic(const BwdParams p) 
         T *dx = reinterpret_cast<T *>(p.dx) + row * N;
         const float r = p.rstd[row];
         const float nmu = -p.mean[row];
+        const RowSplit sp = row_split(x, N, true);
+        auto gof = [&](float dyj, float wj) { return w ? __fmul_rn(dyj, __fadd_rn(p.offset, wj)) : dyj; };
+        // the chunk at column j0: dy, x and gamma
+        auto chunk = [&](int j0, float2 (&dv)[NP], float2 (&xv)[NP], float2 (&wv)[NP]) {
+            load_chunk_at(dy, j0, vdy, dv);
+            load_chunk_at(x, j0, true, xv);
+            if (w) w_chunk_at<T, T>(w, j0, wv);
+        };
         float2 part = make_float2(0.f, 0.f);
-        for (int j = threadIdx.x; j < N; j += blockDim.x) {
-            const float dyj = load_elem(dy, j);
-            const float g = w ? __fmul_rn(dyj, __fadd_rn(p.offset, load_w(w, j))) : dyj;
+        auto sums = [&](float g, float xj) {
             part.x = __fadd_rn(part.x, g);
-            part.y = __fmaf_rn(g, __fadd_rn(load_elem(x, j), nmu), part.y);
-        }
-        const float2 s = cta_allreduce2(part, red);
-        const float cm = -__fdiv_rn(__fmul_rn(s.y, r), (float)N);
-        const float nmg = -__fdiv_rn(s.x, (float)N);
-        for (int j = threadIdx.x; j < N; j += blockDim.x) {
-            const float dyj = load_elem(dy, j);
-            const float xh = __fmul_rn(__fadd_rn(load_elem(x, j), nmu), r);
-            const float g = w ? __fmul_rn(dyj, __fadd_rn(p.offset, load_w(w, j))) : dyj;
-            float d = __fmul_rn(__fmaf_rn(xh, cm, __fadd_rn(g, nmg)), r);
-            if (has_dres) d = __fadd_rn(d, load_elem(dr, j));
-            store_elem(dx, j, d);
-            if (wsrow) {
+            part.y = __fmaf_rn(g, __fadd_rn(xj, nmu), part.y);
+        };
+        row_visit<E>(
+            sp, N, [&](int j) { sums(gof(load_elem(dy, j), w ? load_w(w, j) : 0.f), load_elem(x, j)); },
+            [&](int j0) {
+                float2 dv[NP], xv[NP], wv[NP];
+                chunk(j0, dv, xv, wv);
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    sums(gof(dv[q].x, w ? wv[q].x : 0.f), xv[q].x);
+                    sums(gof(dv[q].y, w ? wv[q].y : 0.f), xv[q].y);
+                }
+            });
+        // the dgamma and dbeta partials, one column a thread (coalesced), before
+        // the reduction's barrier: dx may overwrite dy later
+        if (wsrow) {
+            for (int j = threadIdx.x; j < N; j += blockDim.x) {
+                const float dyj = load_elem(dy, j), xh = __fmul_rn(__fadd_rn(load_elem(x, j), nmu), r);
                 wsrow[j] = first ? __fmul_rn(dyj, xh) : __fmaf_rn(dyj, xh, wsrow[j]);
                 wsrow[N + j] = first ? dyj : __fadd_rn(wsrow[N + j], dyj);
             }
         }
+        const float2 s = cta_allreduce2(part, red);
+        const float cm = -__fdiv_rn(__fmul_rn(s.y, r), (float)N);
+        const float nmg = -__fdiv_rn(s.x, (float)N);
+        // dx of a column
+        auto out = [&](float dyj, float xj, float wj, float drj) {
+            const float xh = __fmul_rn(__fadd_rn(xj, nmu), r);
+            float d = __fmul_rn(__fmaf_rn(xh, cm, __fadd_rn(gof(dyj, wj), nmg)), r);
+            if (has_dres) d = __fadd_rn(d, drj);
+            return d;
+        };
+        row_visit<E>(
+            sp, N,
+            [&](int j) {
+                store_elem(dx, j, out(load_elem(dy, j), load_elem(x, j), w ? load_w(w, j) : 0.f,
+                                      has_dres ? load_elem(dr, j) : 0.f));
+            },
+            [&](int j0) {
+                float2 dv[NP], xv[NP], wv[NP], rv[NP];
+                chunk(j0, dv, xv, wv);
+                if (has_dres) load_chunk_at(dr, j0, vdr, rv);
+#pragma unroll
+                for (int q = 0; q < NP; ++q)
+                    xv[q] = make_float2(out(dv[q].x, xv[q].x, w ? wv[q].x : 0.f, has_dres ? rv[q].x : 0.f),
+                                        out(dv[q].y, xv[q].y, w ? wv[q].y : 0.f, has_dres ? rv[q].y : 0.f));
+                store_chunk_at(dx, j0, vdx, xv);
+            });
         first = false;
     }
 }

@@ -129,6 +129,79 @@ __device__ __forceinline__ float round_to(float v, const __nv_bfloat16 *) {
     return __bfloat162float(__float2bfloat16_rn(v));
 }
 
+// --------------------------------------------------- peeled generic rows --
+// The generic kernels take rows of any length and alignment. A row is split
+// by the address of its x (or h) row: `head` elements up to the first
+// 16-byte boundary, `nb` whole 16-byte chunks, then a tail from element
+// `tail0`; each thread visits its share in that order, so the row's
+// arithmetic depends on that address and N alone. Each other array of the
+// row is moved a chunk at a time with one 16-byte access where it shares
+// x's address mod 16, and element by element otherwise (the same values).
+__device__ __forceinline__ uint32_t addr_mod16(const void *p) {
+    return (uint32_t)reinterpret_cast<uintptr_t>(p) & 15u;
+}
+
+struct RowSplit {
+    int head, nb, tail0;
+};
+
+template <typename T>
+__device__ __forceinline__ RowSplit row_split(const T *row, int N, bool peel) {
+    RowSplit r{N, 0, N};
+    if (peel) {
+        const int h = (int)(((16u - addr_mod16(row)) & 15u) / sizeof(T));
+        r.head = h < N ? h : N;
+        r.nb = (N - r.head) / Elem<T>::E;
+        r.tail0 = r.head + r.nb * Elem<T>::E;
+    }
+    return r;
+}
+
+// Chunk of a row at column j0 as fp32 pairs, and back (round to nearest
+// even, as the element stores do).
+template <typename T>
+__device__ __forceinline__ void load_chunk_at(const T *p, int64_t j0, bool vec, float2 (&v)[Elem<T>::NP]) {
+    if (vec) {
+        unpack<T>(*reinterpret_cast<const uint4 *>(p + j0), v);
+    } else {
+#pragma unroll
+        for (int q = 0; q < Elem<T>::NP; ++q) v[q] = make_float2(load_elem(p, j0 + 2 * q), load_elem(p, j0 + 2 * q + 1));
+    }
+}
+template <typename T>
+__device__ __forceinline__ void store_chunk_at(T *p, int64_t j0, bool vec, const float2 (&v)[Elem<T>::NP]) {
+    if (vec) {
+        *reinterpret_cast<uint4 *>(p + j0) = pack<T>(v);
+    } else {
+#pragma unroll
+        for (int q = 0; q < Elem<T>::NP; ++q) {
+            store_elem(p, j0 + 2 * q, v[q].x);
+            store_elem(p, j0 + 2 * q + 1, v[q].y);
+        }
+    }
+}
+
+// This thread's share of a split row, in a fixed order: the head's columns
+// one by one, the 16-byte chunks (by first column), then the tail's columns.
+template <int E, typename FE, typename FC>
+__device__ __forceinline__ void row_visit(const RowSplit &sp, int N, FE &&elem, FC &&chunk) {
+    for (int j = threadIdx.x; j < sp.head; j += blockDim.x) elem(j);
+    for (int c = threadIdx.x; c < sp.nb; c += blockDim.x) chunk(sp.head + c * E);
+    for (int j = sp.tail0 + threadIdx.x; j < N; j += blockDim.x) elem(j);
+}
+
+// The weight values of the chunk starting at column j0: one or two 16-byte
+// loads when w + j0 is 16-byte aligned, else element loads.
+template <typename T, typename TW>
+__device__ __forceinline__ void w_chunk_at(const TW *w, int j0, float2 (&wv)[Elem<T>::NP]) {
+    if (addr_mod16(w + j0) == 0) {
+        load_w_chunk<T, TW>(w + j0, 0, wv);
+    } else {
+#pragma unroll
+        for (int q = 0; q < Elem<T>::NP; ++q) wv[q] = make_float2(load_w(w, j0 + 2 * q), load_w(w, j0 + 2 * q + 1));
+    }
+}
+
 // ------------------------------------------------------- pair arithmetic --
 // Two implementations with identical IEEE results lane by lane: packed
 // f32x2 instructions (one instruction for two fp32 lanes on data-centre

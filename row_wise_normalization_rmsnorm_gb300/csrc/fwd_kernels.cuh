@@ -194,9 +194,13 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
     }
 }
 
+// Generic forward: one 256-thread CTA per row, any N and alignment; the
+// output pass reads the row again (from L1/L2). Rows are split into an
+// element-wise head, 16-byte chunks and an element-wise tail.
 template <typename T, typename TW, bool FUSED, int Q = QOUT_NONE>
 __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     __shared__ float red[32];
+    constexpr int NP = Elem<T>::NP;
     const int64_t row = blockIdx.x;
     const int N = p.N;
     const T *x = reinterpret_cast<const T *>(p.x) + row * N;
@@ -205,13 +209,48 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     const TW *w = reinterpret_cast<const TW *>(p.w);
     T *y = reinterpret_cast<T *>(p.y) + row * N;
 
+    // the row splits by x's address (the E4M3 output, one byte an element,
+    // stays element by element); the other arrays take 16-byte accesses
+    // where they share x's address mod 16
+    const uint32_t a16 = addr_mod16(p.x);
+    const bool vy = addr_mod16(p.y) == a16;
+    const bool vr = FUSED && addr_mod16(p.residual) == a16;
+    const bool vh = FUSED && addr_mod16(p.residual_out) == a16;
+    const RowSplit sp = row_split(x, N, Q == QOUT_NONE);
+
     float ss = 0.f;
-    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+    auto h_elem = [&](int j) {
         float h = load_elem(x, j);
         if constexpr (FUSED) {
             h = round_to(__fadd_rn(h, load_elem(res, j)), x);
             store_elem(hout, j, h);
         }
+        return h;
+    };
+    for (int j = threadIdx.x; j < sp.head; j += blockDim.x) {
+        const float h = h_elem(j);
+        ss = __fmaf_rn(h, h, ss);
+    }
+    for (int c = threadIdx.x; c < sp.nb; c += blockDim.x) {
+        const int64_t j0 = sp.head + (int64_t)c * Elem<T>::E;
+        float2 h[NP];
+        load_chunk_at(x, j0, true, h);
+        if constexpr (FUSED) {
+            float2 r[NP];
+            load_chunk_at(res, j0, vr, r);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) h[q] = make_float2(__fadd_rn(h[q].x, r[q].x), __fadd_rn(h[q].y, r[q].y));
+            unpack<T>(pack<T>(h), h);  // the stored (rounded) sum is what is normalised
+            store_chunk_at(hout, j0, vh, h);
+        }
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            ss = __fmaf_rn(h[q].x, h[q].x, ss);
+            ss = __fmaf_rn(h[q].y, h[q].y, ss);
+        }
+    }
+    for (int j = sp.tail0 + threadIdx.x; j < N; j += blockDim.x) {
+        const float h = h_elem(j);
         ss = __fmaf_rn(h, h, ss);
     }
     const float s = cta_allreduce(ss, red);
@@ -224,7 +263,25 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
         return w ? __fmul_rn(hr, __fadd_rn(p.offset, load_w(w, j))) : hr;
     };
     if constexpr (Q == QOUT_NONE) {
-        for (int j = threadIdx.x; j < N; j += blockDim.x) store_elem(y, j, y_at(j));
+        for (int j = threadIdx.x; j < sp.head; j += blockDim.x) store_elem(y, j, y_at(j));
+        for (int c = threadIdx.x; c < sp.nb; c += blockDim.x) {
+            const int64_t j0 = sp.head + (int64_t)c * Elem<T>::E;
+            float2 h[NP];
+            load_chunk_at(FUSED ? static_cast<const T *>(hout) : x, j0, FUSED ? vh : true, h);
+            if (w) {
+                float2 wv[NP];
+                w_chunk_at<T, TW>(w, (int)j0, wv);
+#pragma unroll
+                for (int q = 0; q < NP; ++q)
+                    h[q] = make_float2(__fmul_rn(__fmul_rn(h[q].x, rstd), __fadd_rn(p.offset, wv[q].x)),
+                                       __fmul_rn(__fmul_rn(h[q].y, rstd), __fadd_rn(p.offset, wv[q].y)));
+            } else {
+#pragma unroll
+                for (int q = 0; q < NP; ++q) h[q] = make_float2(__fmul_rn(h[q].x, rstd), __fmul_rn(h[q].y, rstd));
+            }
+            store_chunk_at(y, j0, vy, h);
+        }
+        for (int j = sp.tail0 + threadIdx.x; j < N; j += blockDim.x) store_elem(y, j, y_at(j));
     } else {
         float amax = 0.f;
         if (Q == QOUT_FP8_ROW || p.qamax != nullptr) {
@@ -351,10 +408,12 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 }
 
 // Generic LayerNorm forward: one 256-thread CTA per row, three passes over
-// the row (the later ones served by L1/L2).
+// the row (the later ones served by L1/L2), split like the RMSNorm one.
 template <typename T, bool FUSED>
 __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) {
     __shared__ float red[32];
+    constexpr int E = Elem<T>::E;
+    constexpr int NP = Elem<T>::NP;
     const int64_t row = blockIdx.x;
     const int N = p.N;
     const T *x = reinterpret_cast<const T *>(p.x) + row * N;
@@ -363,34 +422,81 @@ __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) 
     const T *g = reinterpret_cast<const T *>(p.w);
     const T *b = reinterpret_cast<const T *>(p.beta);
     T *y = reinterpret_cast<T *>(p.y) + row * N;
+    const uint32_t a16 = addr_mod16(p.x);
+    const bool vy = addr_mod16(p.y) == a16;
+    const bool vr = FUSED && addr_mod16(p.residual) == a16;
+    const bool vh = FUSED && addr_mod16(p.residual_out) == a16;
+    const RowSplit sp = row_split(x, N, true);
     // The same thread wrote hout[j], so it reads its own value back.
-    auto h_at = [&](int j) { return FUSED ? load_elem(static_cast<const T *>(hout), j) : load_elem(x, j); };
+    const T *hsrc = FUSED ? static_cast<const T *>(hout) : x;
+    auto h_at = [&](int j) { return load_elem(hsrc, j); };
+    auto h_chunk = [&](int j0, float2 (&h)[NP]) { load_chunk_at(hsrc, j0, FUSED ? vh : true, h); };
 
     float sm = 0.f;
-    for (int j = threadIdx.x; j < N; j += blockDim.x) {
-        float h = load_elem(x, j);
-        if constexpr (FUSED) {
-            h = round_to(__fadd_rn(h, load_elem(res, j)), x);
-            store_elem(hout, j, h);
-        }
-        sm = __fadd_rn(sm, h);
-    }
+    row_visit<E>(
+        sp, N,
+        [&](int j) {
+            float h = load_elem(x, j);
+            if constexpr (FUSED) {
+                h = round_to(__fadd_rn(h, load_elem(res, j)), x);
+                store_elem(hout, j, h);
+            }
+            sm = __fadd_rn(sm, h);
+        },
+        [&](int j0) {
+            float2 h[NP];
+            load_chunk_at(x, j0, true, h);
+            if constexpr (FUSED) {
+                float2 r[NP];
+                load_chunk_at(res, j0, vr, r);
+#pragma unroll
+                for (int q = 0; q < NP; ++q) h[q] = make_float2(__fadd_rn(h[q].x, r[q].x), __fadd_rn(h[q].y, r[q].y));
+                unpack<T>(pack<T>(h), h);
+                store_chunk_at(hout, j0, vh, h);
+            }
+#pragma unroll
+            for (int q = 0; q < NP; ++q) sm = __fadd_rn(__fadd_rn(sm, h[q].x), h[q].y);
+        });
     const float mu = __fdiv_rn(cta_allreduce(sm, red), (float)N);
     float sq = 0.f;
-    for (int j = threadIdx.x; j < N; j += blockDim.x) {
-        const float d = __fadd_rn(h_at(j), -mu);
-        sq = __fmaf_rn(d, d, sq);
-    }
+    row_visit<E>(
+        sp, N,
+        [&](int j) {
+            const float d = __fadd_rn(h_at(j), -mu);
+            sq = __fmaf_rn(d, d, sq);
+        },
+        [&](int j0) {
+            float2 h[NP];
+            h_chunk(j0, h);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const float d0 = __fadd_rn(h[q].x, -mu), d1 = __fadd_rn(h[q].y, -mu);
+                sq = __fmaf_rn(d1, d1, __fmaf_rn(d0, d0, sq));
+            }
+        });
     const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(cta_allreduce(sq, red), (float)N), p.eps));
     if (threadIdx.x == 0) {
         p.rstd[row] = rstd;
         p.mean[row] = mu;
     }
-    for (int j = threadIdx.x; j < N; j += blockDim.x) {
-        const float xh = __fmul_rn(__fadd_rn(h_at(j), -mu), rstd);
-        const float f = g ? __fadd_rn(p.offset, load_elem(g, j)) : 1.f;
-        store_elem(y, j, __fmaf_rn(xh, f, b ? load_elem(b, j) : 0.f));
-    }
+    auto y_of = [&](float h, float gj, float bj) {
+        const float xh = __fmul_rn(__fadd_rn(h, -mu), rstd);
+        return __fmaf_rn(xh, g ? __fadd_rn(p.offset, gj) : 1.f, bj);
+    };
+    row_visit<E>(
+        sp, N,
+        [&](int j) { store_elem(y, j, y_of(h_at(j), g ? load_elem(g, j) : 0.f, b ? load_elem(b, j) : 0.f)); },
+        [&](int j0) {
+            float2 h[NP], gv[NP], bv[NP];
+            h_chunk(j0, h);
+            if (g) w_chunk_at<T, T>(g, j0, gv);
+            if (b) w_chunk_at<T, T>(b, j0, bv);
+#pragma unroll
+            for (int q = 0; q < NP; ++q)
+                h[q] = make_float2(y_of(h[q].x, g ? gv[q].x : 0.f, b ? bv[q].x : 0.f),
+                                   y_of(h[q].y, g ? gv[q].y : 0.f, b ? bv[q].y : 0.f));
+            store_chunk_at(y, j0, vy, h);
+        });
 }
 
 // ------------------------------------------------------------- dispatch --

@@ -137,9 +137,10 @@ def check_dw(got: np.ndarray, ref: dict, dtype: str):
 
 
 def cuda_bits_equal(a: torch.Tensor, b: torch.Tensor) -> bool:
-    if a.dtype == torch.bfloat16:
-        return torch.equal(a.view(torch.int16), b.view(torch.int16))
-    return torch.equal(a.view(torch.int32), b.view(torch.int32))
+    if a.dtype != b.dtype or a.shape != b.shape:
+        return False
+    iv = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64}[a.element_size()]
+    return torch.equal(a.contiguous().view(iv), b.contiguous().view(iv))
 
 
 FP8_TIE_REL = 2.0 ** -19

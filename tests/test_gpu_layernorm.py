@@ -32,15 +32,22 @@ def _factor(d, dt, offset):
 
 def _ln_check(rn, d, dt, eps=1e-5, offset=0.0, fused=False, offset_elems=0, expect_path=None, gamma=True,
               beta=True, want_dgamma=True, want_dbeta=True):
+    """offset_elems: one element offset for every array, or a dict of
+    offsets by array name (x, gamma, beta, y, residual, residual_out, dy,
+    dx, dgamma, dbeta, dres; missing names: 0)."""
     M, N = d["x"].shape
+    offs = offset_elems if isinstance(offset_elems, dict) else None
+
+    def o(name):
+        return offs.get(name, 0) if offs is not None else offset_elems
     dg_np = d["w"] if gamma else None
     b_np = d.get("beta") if beta else None
-    x = to_dev(d["x"], dt, offset=offset_elems)
-    g = to_dev(dg_np, dt, offset=offset_elems) if gamma else None
-    b = to_dev(b_np, dt, offset=offset_elems) if beta else None
-    y = empty_dev((M, N), dt, offset=offset_elems)
-    res = to_dev(d["residual"], dt, offset=offset_elems) if fused else None
-    hout = empty_dev((M, N), dt, offset=offset_elems) if fused else None
+    x = to_dev(d["x"], dt, offset=o("x"))
+    g = to_dev(dg_np, dt, offset=o("gamma")) if gamma else None
+    b = to_dev(b_np, dt, offset=o("beta")) if beta else None
+    y = empty_dev((M, N), dt, offset=o("y"))
+    res = to_dev(d["residual"], dt, offset=o("residual")) if fused else None
+    hout = empty_dev((M, N), dt, offset=o("residual_out")) if fused else None
     out = rn.layernorm_fwd(x, g, b, residual=res, residual_out=hout, y=y, eps=eps, offset=offset)
     f = oracle.ln_fwd(d["x"], dg_np, b_np, dtype=dt, eps=eps, offset=offset,
                       residual=d.get("residual") if fused else None)
@@ -57,13 +64,13 @@ def _ln_check(rn, d, dt, eps=1e-5, offset=0.0, fused=False, offset_elems=0, expe
     # backward, fed the oracle's fp32 statistics
     m32 = torch.from_numpy(f["mean32"]).cuda()
     r32 = torch.from_numpy(f["rstd32"]).cuda()
-    hdev = to_dev(h_np, dt, offset=offset_elems)
-    dy = to_dev(d["dy"], dt, offset=offset_elems)
-    dx = empty_dev((M, N), dt, offset=offset_elems)
-    dgam = empty_dev((N,), dt, offset=offset_elems) if (gamma and want_dgamma) else None
-    dbet = empty_dev((N,), dt, offset=offset_elems) if want_dbeta else None
+    hdev = to_dev(h_np, dt, offset=o("x"))
+    dy = to_dev(d["dy"], dt, offset=o("dy"))
+    dx = empty_dev((M, N), dt, offset=o("dx"))
+    dgam = empty_dev((N,), dt, offset=o("dgamma")) if (gamma and want_dgamma) else None
+    dbet = empty_dev((N,), dt, offset=o("dbeta")) if want_dbeta else None
     dres_np = d.get("dres") if fused else None
-    dres = to_dev(dres_np, dt, offset=offset_elems) if dres_np is not None else None
+    dres = to_dev(dres_np, dt, offset=o("dres")) if dres_np is not None else None
     bo = rn.layernorm_bwd(dy, hdev, g, m32, r32, dresidual_out=dres, eps=eps, offset=offset, dx=dx, dgamma=dgam,
                           dbeta=dbet, want_dgamma=want_dgamma, want_dbeta=want_dbeta)
     r = oracle.ln_bwd(d["dy"], h_np, dg_np, dtype=dt, eps=eps, offset=offset, mean=f["mean32"],
@@ -119,6 +126,23 @@ def test_ln_optional_parameters(rn, gamma, beta, want_dgamma, want_dbeta):
 def test_ln_misaligned_takes_generic(rn):
     d = inputs.make_inputs(257, 2048, "bf16", 174, beta=True)
     _ln_check(rn, d, "bf16", offset_elems=1, expect_path="generic")
+
+
+@pytest.mark.parametrize("dt,M,N,offs", [
+    ("bf16", 129, 4099, {"x": 3, "gamma": 3, "beta": 1, "y": 3, "dy": 3, "dx": 3, "dgamma": 1}),
+    ("f32", 100, 1030, {"x": 1, "gamma": 2, "beta": 1, "y": 1, "dy": 1, "dx": 1, "dbeta": 3}),
+    ("bf16", 64, 6, {"x": 1, "gamma": 1, "beta": 1, "y": 1, "dy": 1, "dx": 1}),
+    ("f16", 80, 2048, {"x": 1, "y": 2, "dy": 3, "dx": 0}),
+])
+@pytest.mark.parametrize("fused", [False, True])
+def test_ln_generic_peeled_and_scalar_rows(rn, dt, M, N, offs, fused):
+    """Generic LayerNorm rows split into a scalar head, 16-byte chunks and a
+    scalar tail (the arrays share their address mod 16; gamma and beta may
+    not) or not split (they do not share it), against the oracle."""
+    d = inputs.make_inputs(M, N, dt, 320 + N % 13, beta=True, residual=fused, dres=fused)
+    if fused:
+        offs = dict(offs, residual=offs.get("x", 0), residual_out=offs.get("x", 0), dres=offs.get("dy", 0))
+    _ln_check(rn, d, dt, fused=fused, offset_elems=offs, expect_path="generic")
 
 
 def test_ln_large_mean_two_pass_variance(rn):

@@ -28,16 +28,23 @@ def rn():
 
 
 def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_path=None, wdt=None):
-    """wdt: the weight's (and dW's) storage type, default the activations'."""
+    """wdt: the weight's (and dW's) storage type, default the activations'.
+    offset_elems: one element offset for every array, or a dict of offsets
+    by array name (x, w, dy, y, residual, residual_out, h, dx, dw, dres;
+    missing names: 0)."""
     wdt = wdt or dt
     M, N = d["x"].shape
-    x = to_dev(d["x"], dt, offset=offset_elems)
-    w = to_dev(d["w"], wdt, offset=offset_elems)
-    dy = to_dev(d["dy"], dt, offset=offset_elems)
-    y = empty_dev((M, N), dt, offset=offset_elems)
+    offs = offset_elems if isinstance(offset_elems, dict) else None
+
+    def o(name):
+        return offs.get(name, 0) if offs is not None else offset_elems
+    x = to_dev(d["x"], dt, offset=o("x"))
+    w = to_dev(d["w"], wdt, offset=o("w"))
+    dy = to_dev(d["dy"], dt, offset=o("dy"))
+    y = empty_dev((M, N), dt, offset=o("y"))
     rstd = torch.full((M,), float("nan"), device="cuda")
-    res = to_dev(d["residual"], dt, offset=offset_elems) if fused else None
-    hout = empty_dev((M, N), dt, offset=offset_elems) if fused else None
+    res = to_dev(d["residual"], dt, offset=o("residual")) if fused else None
+    hout = empty_dev((M, N), dt, offset=o("residual_out")) if fused else None
     _, _, _, fplan = rn.rmsnorm_fwd_ex(x, w, residual=res, residual_out=hout, y=y, rstd=rstd, eps=eps,
                                        offset=offset)
     f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=eps, offset=offset, residual=d.get("residual") if fused else None,
@@ -51,11 +58,11 @@ def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_p
 
     # backward, fed the oracle's fp32 rstd
     r32 = torch.from_numpy(f["rstd32"]).cuda()
-    hdev = to_dev(h_np, dt, offset=offset_elems)
-    dx = empty_dev((M, N), dt, offset=offset_elems)
-    dw = empty_dev((N,), wdt, offset=offset_elems)
+    hdev = to_dev(h_np, dt, offset=o("h"))
+    dx = empty_dev((M, N), dt, offset=o("dx"))
+    dw = empty_dev((N,), wdt, offset=o("dw"))
     dres_np = d.get("dres") if fused else None
-    dres = to_dev(dres_np, dt, offset=offset_elems) if dres_np is not None else None
+    dres = to_dev(dres_np, dt, offset=o("dres")) if dres_np is not None else None
     _, _, bplan = rn.rmsnorm_bwd_ex(dy, hdev, w, r32, dresidual_out=dres, fused=fused, dx=dx, dw=dw, eps=eps,
                                     offset=offset)
     b = oracle.bwd(d["dy"], h_np, d["w"], dtype=dt, eps=eps, offset=offset, rstd=f["rstd32"], dres=dres_np,
@@ -130,6 +137,38 @@ def test_misaligned_storage_offset(rn, dt, M, N):
     """All of x, w, y, dy, dx at +1 element from a 256-byte-aligned allocation."""
     d = inputs.make_inputs(M, N, dt, inputs.SWEEP_SEED)
     _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, offset_elems=1, expect_path="generic")
+
+
+# Generic rows with 16-byte chunks between a scalar head and tail (the
+# arrays share their address mod 16, the weight may not) and without them
+# (the arrays do not share it): every combination against the oracle.
+PEEL_CASES = [
+    ("bf16", 301, 7168, {"x": 1, "w": 1, "dy": 1, "y": 1, "h": 1, "dx": 1, "dw": 1}),
+    ("bf16", 300, 7171, {"x": 3, "w": 5, "dy": 3, "y": 3, "h": 3, "dx": 3, "dw": 2}),
+    ("bf16", 64, 5, {"x": 3, "w": 1, "dy": 3, "y": 3, "h": 3, "dx": 3}),
+    ("f16", 129, 4100, {"x": 2, "w": 2, "dy": 2, "y": 2, "h": 2, "dx": 2}),
+    ("f32", 257, 2050, {"x": 1, "w": 3, "dy": 1, "y": 1, "h": 1, "dx": 1, "dw": 1}),
+    ("bf16", 200, 4096, {"x": 1, "y": 0, "dy": 2, "h": 1, "dx": 0}),
+    ("f32", 100, 1000, {"x": 0, "y": 1, "dy": 1, "h": 3, "dx": 1}),
+]
+
+
+@pytest.mark.parametrize("dt,M,N,offs", PEEL_CASES)
+@pytest.mark.parametrize("fused", [False, True])
+def test_generic_peeled_and_scalar_rows(rn, dt, M, N, offs, fused):
+    d = inputs.make_inputs(M, N, dt, 300 + N % 11, residual=fused, dres=fused)
+    if fused:
+        offs = dict(offs, residual=offs.get("x", 0), residual_out=offs.get("x", 0), dres=offs.get("dy", 0))
+    _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, fused=fused, offset_elems=offs, expect_path="generic")
+
+
+def test_generic_fused_residual_alone_misaligned(rn):
+    """A residual at another address mod 16 than x turns the forward's peel
+    off (element accesses); the result is the same arithmetic."""
+    d = inputs.make_inputs(96, 4104, "bf16", 311, residual=True, dres=True)
+    _fwd_bwd_check(rn, d, "bf16", 1e-6, 0.0, fused=True, expect_path="generic",
+                   offset_elems={"x": 1, "y": 1, "residual": 2, "residual_out": 1, "dy": 1, "h": 1, "dx": 1,
+                                 "dres": 3})
 
 
 @pytest.mark.parametrize("eps", [0.0, 1e-2, 10.0])

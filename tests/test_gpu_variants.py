@@ -344,3 +344,35 @@ def test_reread_staged_backward_matches_held_bitwise(rn, dt, M, N, reread, held,
     assert cuda_bits_equal(a_dw, b_dw)
     assert rn.lib().rmsnorm_device_status(1) == 0
 
+
+
+@pytest.mark.parametrize("dt,N,xoff", [("bf16", 4097, 0), ("bf16", 7168, 1), ("f32", 2050, 1), ("f16", 1003, 3)])
+def test_generic_rows_independent_of_other_arrays_alignment(rn, dt, N, xoff):
+    """A generic row splits by x's address alone: y, h, dy, dx and the
+    residual buffers moved with 16-byte accesses (sharing x's address mod 16)
+    or element by element (not sharing it) give the same bits, and so do
+    the LayerNorm kernels."""
+    M = 67
+    d = inputs.make_inputs(M, N, dt, 330 + N % 9, residual=True, dres=True, beta=True)
+    x = to_dev(d["x"], dt, offset=xoff)
+    w = to_dev(d["w"], dt, offset=xoff)
+    b = to_dev(d["beta"], dt, offset=xoff)
+    outs = []
+    for off in (xoff, xoff + 1, xoff + 2):
+        res = to_dev(d["residual"], dt, offset=off)
+        dy = to_dev(d["dy"], dt, offset=off)
+        dres = to_dev(d["dres"], dt, offset=off)
+        y = empty_dev((M, N), dt, offset=off)
+        hout = empty_dev((M, N), dt, offset=off)
+        dx = empty_dev((M, N), dt, offset=off)
+        _, _, rstd, fp = rn.rmsnorm_fwd_ex(x, w, residual=res, residual_out=hout, y=y)
+        _, dw, bp = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dresidual_out=dres, fused=True, dx=dx)
+        assert fp["path_name"] == "generic" and bp["path_name"] == "generic"
+        lo = rn.layernorm_fwd(x, w, b, y=empty_dev((M, N), dt, offset=off))
+        lb = rn.layernorm_bwd(dy, x, w, lo["mean"], lo["rstd"], dx=empty_dev((M, N), dt, offset=off))
+        torch.cuda.synchronize()
+        outs.append([t.clone() for t in (y, hout, rstd, dx, dw, lo["y"], lo["mean"], lo["rstd"], lb["dx"],
+                                         lb["dgamma"], lb["dbeta"])])
+    for other in outs[1:]:
+        for a, c in zip(outs[0], other):
+            assert cuda_bits_equal(a, c)
