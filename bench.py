@@ -293,6 +293,10 @@ def sweep_points():
     # a row length that is no multiple of 16 bytes: the generic kernels
     pts.append(("oddn bf16 4096x7169", "bf16", 4096, 7169, False, False))
     pts.append(("wide f32 16384x6144", "f32", 16384, 6144, False, False))
+    # rows wider than one CTA's stages: a cluster of CTAs shares each row
+    for M, N in ((16384, 20480), (8192, 32768), (2048, 65536)):
+        pts.append((f"wide bf16 {M}x{N}", "bf16", M, N, False, False))
+    pts.append(("ln bf16 4096x32768", "bf16", 4096, 32768, False, False))
     pts.append(("small f32 64x256", "f32", 64, 256, False, False))
     return pts
 

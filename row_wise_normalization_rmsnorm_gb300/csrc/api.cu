@@ -91,11 +91,28 @@ static int cta_threads(const PlanDesc &d) { return d.path == PATH_GENERIC ? 256 
 constexpr int kMaxDynamicSmem = 226 * 1024;
 
 // A staged plan's shared memory: `depth` stages of x and dy (and dres for
-// the fused variant) rows of es-byte elements; the LayerNorm's re-read
-// schedule also keeps gamma there.
+// the fused variant) rows of es-byte elements, or of one CTA's slice (a
+// cs-th, rounded up to whole chunks) of a row shared by a cluster; the
+// LayerNorm's re-read schedule also keeps (its slice of) gamma there.
+static int64_t staged_smem_at(const PlanDesc &d, int64_t N, int es, bool fused, int depth) {
+    const int64_t C = (N * es + 15) / 16;
+    const int64_t row = (C + d.cs - 1) / d.cs * 16;
+    const int64_t gamma = d.path == PATH_RESTAGED && d.op == OP_LN_BWD ? row : 0;
+    return (int64_t)depth * (fused ? 3 : 2) * row + gamma;
+}
+
+// Stages a call takes: the plan's depth, or fewer (at least two) where the
+// rows (three a stage for the fused variant) would not fit; 0: none fits.
+static int staged_depth(const PlanDesc &d, int64_t N, int es, bool fused) {
+    for (int k = d.depth; k >= 2; --k)
+        if (staged_smem_at(d, N, es, fused, k) <= kMaxDynamicSmem) return k;
+    return 0;
+}
+
+// Shared memory at the stages a call takes (above the limit when none fits).
 static int64_t staged_smem_bytes(const PlanDesc &d, int64_t N, int es, bool fused) {
-    const int64_t gamma = d.path == PATH_RESTAGED && d.op == OP_LN_BWD ? N * es : 0;
-    return (int64_t)d.depth * (fused ? 3 : 2) * N * es + gamma;
+    const int k = staged_depth(d, N, es, fused);
+    return staged_smem_at(d, N, es, fused, k > 0 ? k : 2);
 }
 
 static int nominal_ctas_per_sm(const PlanDesc &d) {
@@ -427,9 +444,10 @@ int self_check_impl() {
             if (d.cs < 1 || d.cs > 8 || (d.cs > 1 && (d.teams != 1 || d.tpr < 32))) ++bad;
         }
         if (staged_path(d.path)) {
-            // one team per CTA of whole warps, no cluster, at least two stages, backward only
-            if (d.op == OP_FWD || d.teams != 1 || d.cs != 1 || d.depth < 2 || d.tpr % 32 != 0 || d.tpr < 64 ||
-                d.tpr > kMaxCtaThreads || d.v < 1)
+            // one team per CTA of whole warps, at least two stages, backward
+            // only; a cluster (2, 4 or 8 CTAs) only on the re-read schedule
+            if (d.op == OP_FWD || !staged_plan(d.path, d.teams, d.cs) || d.depth < 2 || d.tpr % 32 != 0 ||
+                d.tpr < 64 || d.tpr > kMaxCtaThreads || d.v < 1)
                 ++bad;
         }
         if (d.dtm < 1 || d.dtm > DT_ANY) ++bad;
@@ -636,6 +654,7 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     p.M = M;
     p.N = (int)N;
     p.offset = offset;
+    p.stages = staged_path(d->path) ? staged_depth(*d, N, (int)s, fused) : 0;
     int le = launch_bwd_dt(dt, plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream);
     if (le == 0 && event_after_main) le = (int)cudaEventRecord(static_cast<cudaEvent_t>(event_after_main), stream);
     if (le == 0 && affine)
@@ -819,6 +838,8 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
     p.M = M;
     p.N = (int)N;
     p.offset = offset;
+    const PlanDesc *pd = find_plan(plan.plan_id);
+    p.stages = staged_path(pd->path) ? staged_depth(*pd, N, (int)s, fused) : 0;
     int le;
     switch (base_dtype(dt)) {
     case RMSNORM_BF16: le = launch_ln_bwd_bf16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;

@@ -432,8 +432,9 @@ __global__ void __launch_bounds__(TPR *TEAMS) layernorm_bwd_vector(const BwdPara
 // ends. Each warp then counts itself done on the stage's counter and the
 // last one to arrive refills the stage; no thread waits for the others. The
 // arithmetic, and so every output bit, is that of HOLD = true.
-template <typename T, typename TW, int TPR, int V, int S, bool FUSED, bool LN, bool HOLD>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool LN, bool HOLD>
 __device__ __forceinline__ void staged_body(const BwdParams &p) {
+    static_assert(CS == 1 || !HOLD, "cluster rows use the re-read schedule (no CTA barrier orders their refills)");
     using Pk = Pair<true>;
     using RT = typename std::conditional<LN, float2, float>::type;  // what a row reduces
     constexpr int NACC = LN ? 2 : 1;     // partial rows per CTA
@@ -442,10 +443,11 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     constexpr int W = TPR / 32;          // warps of the row team
     constexpr int NB = FUSED ? 3 : 2;    // rows a stage holds: x, dy (, dres)
     static_assert(TPR % 32 == 0 && TPR >= 64, "whole warps");
-    __shared__ RT red[2][W];
+    __shared__ RT red[2][CS * W];
     __shared__ __align__(8) uint64_t full[S];
+    __shared__ __align__(8) uint64_t rbar[2];  // cluster rows: arrival of the peers' partials
     __shared__ unsigned done[HOLD ? 1 : S];  // re-read: warps through the stage's row
-    extern __shared__ float4 stage_smem[];  // S * NB * C chunks of 16 bytes (+ C for gamma)
+    extern __shared__ float4 stage_smem[];  // ns * NB * Cst chunks of 16 bytes (+ Cst for gamma)
     // The LayerNorm re-read schedule keeps gamma in shared memory after the
     // stages rather than in registers (its two accumulators fill them).
     constexpr bool WSM = LN && !HOLD;
@@ -453,29 +455,42 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     const int N = p.N;
     const int C = N / E;
     const int tid = threadIdx.x;
-    const int64_t unit = blockIdx.x;
-    const int64_t G = gridDim.x;
+    // CS > 1: the CTAs of a cluster share each row in equal slices; CTA
+    // rank r streams and owns chunks [r Cst, (r+1) Cst) of it (Cs of them,
+    // fewer in the last slices, maybe none), the row sums meet in
+    // distributed shared memory and the cluster is the unit that walks the
+    // rows and owns a parameter-gradient partial row
+    uint32_t rank = 0;
+    if constexpr (CS > 1) rank = cluster_ctarank();
+    const int Cst = (C + CS - 1) / CS;  // chunks a stage buffer holds (at most TPR V)
+    const int cbase = (int)rank * Cst;
+    const int Cs = C - cbase <= 0 ? 0 : (C - cbase < Cst ? C - cbase : Cst);
+    const int64_t unit = CS > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
+    const int64_t G = CS > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
     const int64_t iters = unit < p.M ? (p.M - unit + G - 1) / G : 0;
     const bool has_dres = FUSED && p.dres != nullptr;
-    const uint32_t row_bytes = (uint32_t)C * 16u;
+    const uint32_t row_bytes = (uint32_t)Cs * 16u;
+    const int ns = p.stages >= 2 && p.stages < S ? p.stages : S;  // stages in use
     uint4 *stages = reinterpret_cast<uint4 *>(stage_smem);
     const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x);
     const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dy);
     const uint4 *r4 = reinterpret_cast<const uint4 *>(p.dres);
     // thread 0: stream row k into stage s
     auto issue = [&](int64_t k, int s) {
-        const int64_t off = (unit + k * G) * C;
-        uint4 *dst = stages + (size_t)s * NB * C;
+        const int64_t off = (unit + k * G) * C + cbase;
+        uint4 *dst = stages + (size_t)s * NB * Cst;
         mbar_arrive_expect_tx(&full[s], row_bytes * (has_dres ? 3u : 2u));
+        if (row_bytes == 0) return;  // an empty slice: the arrival alone completes the phase
         bulk_g2s(dst, x4 + off, row_bytes, &full[s]);
-        bulk_g2s(dst + C, d4 + off, row_bytes, &full[s]);
-        if (has_dres) bulk_g2s(dst + 2 * C, r4 + off, row_bytes, &full[s]);
+        bulk_g2s(dst + Cst, d4 + off, row_bytes, &full[s]);
+        if (has_dres) bulk_g2s(dst + 2 * Cst, r4 + off, row_bytes, &full[s]);
     };
-    uint4 *wsm = stages + (size_t)S * NB * C;
+    uint4 *wsm = stages + (size_t)ns * NB * Cst;
     if constexpr (WSM) {
         if (p.w != nullptr)
-            for (int c = tid; c < C; c += TPR) wsm[c] = ld_keep(reinterpret_cast<const uint4 *>(p.w) + c);
+            for (int c = tid; c < Cs; c += TPR) wsm[c] = ld_keep(reinterpret_cast<const uint4 *>(p.w) + cbase + c);
     }
+    constexpr uint32_t kSlotBytes = CS * W * sizeof(RT);  // one row's partials from the whole cluster
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
@@ -483,10 +498,20 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
 #pragma unroll
             for (int s = 0; s < S; ++s) done[s] = 0;
         }
+        if constexpr (CS > 1) {
+            // one arrival (the re-arm) plus the row's bytes; rows 0 and 1 armed here
+            mbar_init(&rbar[0], 1);
+            mbar_init(&rbar[1], 1);
+            mbar_arrive_expect_tx(&rbar[0], kSlotBytes);
+            mbar_arrive_expect_tx(&rbar[1], kSlotBytes);
+        }
         mbar_init_fence();
-        for (int s = 0; s < S && s < iters; ++s) issue(s, s);
+        for (int s = 0; s < ns && s < iters; ++s) issue(s, s);
     }
     __syncthreads();
+    // every CTA of the cluster runs, with its barriers initialised, before
+    // any peer stores into its shared memory
+    if constexpr (CS > 1) cluster_sync();
 
     const int t = tid;
     const int lane = t & 31;
@@ -506,14 +531,15 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     float2 accb[LN ? V : 1][NP];  // LayerNorm: sum dy (dbeta)
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        const int c = v * TPR + t;
+        const int cl = v * TPR + t;  // chunk of this CTA's slice; cbase + cl in the row
         if constexpr (WSM) {
         } else if constexpr (RAW) {
-            wraw[v] = (has_w && c < C) ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + c) : make_uint4(0, 0, 0, 0);
+            wraw[v] = (has_w && cl < Cs) ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + cbase + cl)
+                                         : make_uint4(0, 0, 0, 0);
         } else {
             float2 wv[NP];
-            if (has_w && c < C) {
-                load_w_chunk<T, TW>(p.w, c, wv);
+            if (has_w && cl < Cs) {
+                load_w_chunk<T, TW>(p.w, cbase + cl, wv);
             } else {
 #pragma unroll
                 for (int q = 0; q < NP; ++q) wv[q] = make_float2(0.f, 0.f);
@@ -529,9 +555,9 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     }
     auto wfac = [&](int v, float2 (&f)[NP]) {
         if constexpr (WSM || RAW) {
-            const int c = v * TPR + t;
+            const int cl = v * TPR + t;
             if constexpr (WSM)
-                unpack<T>(has_w && c < C ? lds128(wsm + c) : make_uint4(0, 0, 0, 0), f);
+                unpack<T>(has_w && cl < Cs ? lds128(wsm + cl) : make_uint4(0, 0, 0, 0), f);
             else
                 unpack<T>(wraw[v], f);
 #pragma unroll
@@ -543,7 +569,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     };
 
     bool failed = false;
-    int s = 0;          // stage of row k (k mod S)
+    int s = 0;          // stage of row k (k mod ns)
     uint32_t ph = 0;    // parity of k / S
     // the row statistics are loaded one row ahead, like the rows themselves
     float r_next = iters > 0 ? p.rstd[unit] : 0.f;
@@ -558,23 +584,23 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         }
         if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
         const int sk = s;  // this row's stage
-        const uint4 *src = stages + (size_t)s * NB * C;
+        const uint4 *src = stages + (size_t)s * NB * Cst;
         // HOLD: the row's chunks, read once and kept for both passes
         uint4 xv[HOLD ? V : 1], dv[HOLD ? V : 1], rv[FUSED && HOLD ? V : 1];
         if constexpr (HOLD) {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                const int c = v * TPR + t;
-                const bool in = c < C;
-                xv[v] = in ? lds128(src + c) : make_uint4(0, 0, 0, 0);
-                dv[v] = in ? lds128(src + C + c) : make_uint4(0, 0, 0, 0);
-                if constexpr (FUSED) rv[v] = (in && has_dres) ? lds128(src + 2 * C + c) : make_uint4(0, 0, 0, 0);
+                const int cl = v * TPR + t;
+                const bool in = cl < Cs;
+                xv[v] = in ? lds128(src + cl) : make_uint4(0, 0, 0, 0);
+                dv[v] = in ? lds128(src + Cst + cl) : make_uint4(0, 0, 0, 0);
+                if constexpr (FUSED) rv[v] = (in && has_dres) ? lds128(src + 2 * Cst + cl) : make_uint4(0, 0, 0, 0);
             }
         }
         // chunk v of the stage's x (b = 0), dy (1) or dres (2) row
         auto chunk = [&](int b, int v) {
-            const int c = v * TPR + t;
-            return c < C ? lds128(src + b * C + c) : make_uint4(0, 0, 0, 0);
+            const int cl = v * TPR + t;
+            return cl < Cs ? lds128(src + b * Cst + cl) : make_uint4(0, 0, 0, 0);
         };
 
         const float2 r2 = make_float2(r, r);
@@ -608,14 +634,34 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
             for (int o = 16; o > 0; o >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
         }
         RT *slots = &red[k & 1][0];
-        if (lane == 0) slots[t >> 5] = part;
-        __syncthreads();
-        // every warp has copied stage s into registers: refill it with row k + S
-        if (HOLD && tid == 0 && k + S < iters) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(k + S, s);
+        if constexpr (CS > 1) {
+            // Row k's warp sums go to slot buffer b = k & 1 of every CTA of
+            // the cluster (st.async, counted in bytes on the receiver's
+            // barrier, whose phase for row k has parity (k >> 1) & 1). A
+            // buffer is written again (row k + 2) only after every warp of
+            // the cluster sent its row k + 1 sum, which each warp does after
+            // reading the buffer for row k.
+            const int b = (int)(k & 1);
+            if (lane == 0) {
+#pragma unroll
+                for (int c = 0; c < CS; ++c) {
+                    if constexpr (LN)
+                        st_async_cluster2(&red[b][rank * W + (t >> 5)], &rbar[b], (uint32_t)c, part);
+                    else
+                        st_async_cluster(&red[b][rank * W + (t >> 5)], &rbar[b], (uint32_t)c, part);
+                }
+            }
+            if (!mbar_wait(&rbar[b], (uint32_t)((k >> 1) & 1), kWaitLimit)) failed = true;
+        } else {
+            if (lane == 0) slots[t >> 5] = part;
+            __syncthreads();
+            // every warp has copied stage s into registers: refill it with row k + ns
+            if (HOLD && tid == 0 && k + ns < iters) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(k + ns, s);
+            }
         }
-        if (++s == S) {
+        if (++s == ns) {
             s = 0;
             ph ^= 1u;
         }
@@ -623,19 +669,21 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         // also subtracts mean(g) = (sum g) / N
         float cm, nmg = 0.f;
         if constexpr (LN) {
-            const float2 sum = sum_slots2<W>(slots, lane);
+            const float2 sum = sum_slots2<CS * W>(slots, lane);
             cm = -__fdiv_rn(__fmul_rn(sum.y, r), (float)N);
             nmg = -__fdiv_rn(sum.x, (float)N);
         } else {
-            const float sum = sum_slots<W>(slots, lane);
+            const float sum = sum_slots<CS * W>(slots, lane);
             cm = -__fdiv_rn(__fmul_rn(sum, r), (float)N);
         }
+        // re-arm the slot buffer's barrier for row k + 2 (its phase for row k is done)
+        if (CS > 1 && t == 0) mbar_arrive_expect_tx(&rbar[k & 1], kSlotBytes);
         const float2 nc2 = make_float2(cm, cm);
         const float2 nmg2 = make_float2(nmg, nmg);
         const int64_t base = row * C;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
-            const int c = v * TPR + t;
+            const int cl = v * TPR + t;
             float2 xf[NP], df[NP], out[NP], wf[NP];
             unpack<T>(HOLD ? xv[HOLD ? v : 0] : chunk(0, v), xf);
             unpack<T>(HOLD ? dv[HOLD ? v : 0] : chunk(1, v), df);
@@ -659,36 +707,40 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
                     for (int q = 0; q < NP; ++q) out[q] = Pk::add(out[q], rf[q]);
                 }
             }
-            if (c < C) st_chunk(dx4 + base + c, pack<T>(out));
+            if (cl < Cs) st_chunk(dx4 + base + cbase + cl, pack<T>(out));
         }
         if constexpr (!HOLD) {
             // re-read: the warp is through stage sk; the last warp to say so
-            // refills it with row k + S (the fences order every warp's reads
+            // refills it with row k + ns (the fences order every warp's reads
             // of the stage before the bulk copies that overwrite it)
             __syncwarp();
-            if (lane == 0 && k + S < iters) {
+            if (lane == 0 && k + ns < iters) {
                 __threadfence_block();
                 if (atomicAdd(&done[sk], 1u) == (unsigned)(W - 1)) {
                     __threadfence_block();
                     done[sk] = 0;
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    issue(k + S, sk);
+                    issue(k + ns, sk);
                 }
             }
         }
     }
     if (failed && p.status) *p.status = kStatusWaitTimeout;
+    // no CTA leaves while a peer may still store into its shared memory
+    if constexpr (CS > 1) cluster_sync();
 
     // The finalizer may start launching now; it waits for this grid to
     // finish (griddepcontrol.wait) before it reads the workspace.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!want_acc) return;
-    // the CTA's partial row(s): dW, or LayerNorm's dgamma | dbeta
+    // the unit's partial row(s): dW, or LayerNorm's dgamma | dbeta (a
+    // cluster CTA writes the columns of its slice)
     float *wsrow = p.ws + unit * (int64_t)(NACC * N);
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        const int c = v * TPR + t;
-        if (c < C) {
+        const int cl = v * TPR + t;
+        if (cl < Cs) {
+            const int c = cbase + cl;
             float4 *d = reinterpret_cast<float4 *>(wsrow + c * E);
 #pragma unroll
             for (int q = 0; q < NP / 2; ++q)
@@ -704,14 +756,14 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     }
 }
 
-template <typename T, typename TW, int TPR, int V, int S, bool FUSED, bool HOLD>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool HOLD>
 __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) {
-    staged_body<T, TW, TPR, V, S, FUSED, false, HOLD>(p);
+    staged_body<T, TW, TPR, V, S, CS, FUSED, false, HOLD>(p);
 }
 
-template <typename T, int TPR, int V, int S, bool FUSED, bool HOLD>
+template <typename T, int TPR, int V, int S, int CS, bool FUSED, bool HOLD>
 __global__ void __launch_bounds__(TPR, 1) layernorm_bwd_staged(const BwdParams p) {
-    staged_body<T, T, TPR, V, S, FUSED, true, HOLD>(p);
+    staged_body<T, T, TPR, V, S, CS, FUSED, true, HOLD>(p);
 }
 
 // Generic main kernel: one 256-thread CTA per row at a time, any N and
@@ -1024,12 +1076,13 @@ constexpr bool bwd_instantiated() {
     return std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0;
 }
 
-// Staged kernel: launched as a cluster of one CTA (its bulk copies name a
-// shared::cluster destination) with the stages' dynamic shared memory.
-template <typename T, typename TW, int TPR, int V, int S, bool HOLD>
+// Staged kernel: launched as a cluster of CS CTAs (of one where a CTA
+// holds the whole row; its bulk copies name a shared::cluster destination)
+// with the stages' dynamic shared memory.
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool HOLD>
 static int bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    const void *k = fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, true, HOLD>
-                          : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, false, HOLD>;
+    const void *k = fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD>
+                          : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD>;
     const int e = allow_staged_smem(k);
     if (e != 0) return e;
     cudaLaunchConfig_t cfg = {};
@@ -1039,13 +1092,13 @@ static int bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem,
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.x = CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, true, HOLD>, p)
-                 : (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, false, HOLD>, p);
+    return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD>, p)
+                 : (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD>, p);
 }
 
 template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
@@ -1061,8 +1114,8 @@ static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int gri
     } else if constexpr (PATH == PATH_VECTOR) {
         return packed ? bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, true>(fused, p, grid, smem, s)
                       : bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, false>(fused, p, grid, smem, s);
-    } else if constexpr (staged_path(PATH) && TEAMS == 1 && CS == 1) {
-        return bwd_launch_staged<T, TW, TPR, V, D, PATH == PATH_STAGED>(fused, p, grid, smem, s);
+    } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
+        return bwd_launch_staged<T, TW, TPR, V, D, CS, PATH == PATH_STAGED>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
@@ -1080,9 +1133,9 @@ static const void *bwd_ptr_entry(bool fused, bool packed) {
                          : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, false>;
         return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, true>
                      : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, false>;
-    } else if constexpr (staged_path(PATH) && TEAMS == 1 && CS == 1) {
-        return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, true, PATH == PATH_STAGED>
-                     : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, false, PATH == PATH_STAGED>;
+    } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
+        return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, true, PATH == PATH_STAGED>
+                     : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, false, PATH == PATH_STAGED>;
     } else {
         return nullptr;
     }
@@ -1170,10 +1223,10 @@ static int ln_bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem,
     }
 }
 
-template <typename T, int TPR, int V, int S, bool HOLD>
+template <typename T, int TPR, int V, int S, int CS, bool HOLD>
 static int ln_bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    const void *k = fused ? (const void *)layernorm_bwd_staged<T, TPR, V, S, true, HOLD>
-                          : (const void *)layernorm_bwd_staged<T, TPR, V, S, false, HOLD>;
+    const void *k = fused ? (const void *)layernorm_bwd_staged<T, TPR, V, S, CS, true, HOLD>
+                          : (const void *)layernorm_bwd_staged<T, TPR, V, S, CS, false, HOLD>;
     const int e = allow_staged_smem(k);
     if (e != 0) return e;
     cudaLaunchConfig_t cfg = {};
@@ -1183,13 +1236,13 @@ static int ln_bwd_launch_staged(bool fused, const BwdParams &p, int grid, int sm
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.x = CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return fused ? (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, true, HOLD>, p)
-                 : (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, false, HOLD>, p);
+    return fused ? (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, CS, true, HOLD>, p)
+                 : (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, CS, false, HOLD>, p);
 }
 
 template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
@@ -1204,8 +1257,8 @@ static int ln_bwd_launch_entry(bool fused, const BwdParams &p, int grid, int sme
         return (int)cudaGetLastError();
     } else if constexpr (PATH == PATH_VECTOR) {
         return ln_bwd_launch_vec<T, TPR, V, TEAMS, D, CS>(fused, p, grid, smem, s);
-    } else if constexpr (staged_path(PATH) && TEAMS == 1 && CS == 1) {
-        return ln_bwd_launch_staged<T, TPR, V, D, PATH == PATH_STAGED>(fused, p, grid, smem, s);
+    } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
+        return ln_bwd_launch_staged<T, TPR, V, D, CS, PATH == PATH_STAGED>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
@@ -1220,9 +1273,9 @@ static const void *ln_bwd_ptr_entry(bool fused) {
     } else if constexpr (PATH == PATH_VECTOR) {
         return fused ? (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true>
                      : (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false>;
-    } else if constexpr (staged_path(PATH) && TEAMS == 1 && CS == 1) {
-        return fused ? (const void *)layernorm_bwd_staged<T, TPR, V, D, true, PATH == PATH_STAGED>
-                     : (const void *)layernorm_bwd_staged<T, TPR, V, D, false, PATH == PATH_STAGED>;
+    } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
+        return fused ? (const void *)layernorm_bwd_staged<T, TPR, V, D, CS, true, PATH == PATH_STAGED>
+                     : (const void *)layernorm_bwd_staged<T, TPR, V, D, CS, false, PATH == PATH_STAGED>;
     } else {
         return nullptr;
     }

@@ -26,6 +26,11 @@ enum PlanOp { OP_FWD = 0, OP_BWD = 1, OP_LN_BWD = 2 };
 // for the whole row). The C ABI reports both as the staged path.
 enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2, PATH_RESTAGED = 3 };
 constexpr bool staged_path(int path) { return path == PATH_STAGED || path == PATH_RESTAGED; }
+// The staged kernels run one row team a CTA; a row may be shared by a
+// cluster of CTAs only on the re-read schedule.
+constexpr bool staged_plan(int path, int teams, int cs) {
+    return teams == 1 && ((path == PATH_STAGED && cs == 1) || (path == PATH_RESTAGED && (cs == 1 || cs == 2 || cs == 4 || cs == 8)));
+}
 // Storage types a default plan applies to (bit 0: fp32, bit 1: bf16,
 // bit 2: fp16; DT_16 = both 2-byte types).
 enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
@@ -36,7 +41,8 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
 // forced (tuning and A/B tests).
 // depth (backward only): rows whose x/dy loads are in flight while the
 // current row is computed (a register ring of depth + 1 rows); for staged
-// plans the number of shared-memory stages rows are streamed into.
+// plans the most shared-memory stages rows are streamed into (a call takes
+// as many of them as fit its rows, at least two).
 // cluster: CTAs of a thread-block cluster that share one row; each holds
 // threads_per_row * chunks_per_thread chunks of it in registers and the row
 // sums meet in distributed shared memory (1: no cluster).
@@ -67,7 +73,8 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     /* backward main kernel, persistent: rows in registers (vector) or \
        streamed into `depth` shared-memory stages by bulk copies (staged; \
        re-read from the stage in both passes from 1025 chunks on, where \
-       holding four chunks a thread in registers spills) */ \
+       holding four chunks a thread in registers spills; rows wider than \
+       2048 chunks shared by a cluster of 2 or 4 staged CTAs) */ \
     X(20, OP_BWD, PATH_VECTOR ,    8, 1, 32, 1, 1, DT_ANY,     1,     8) \
     X(21, OP_BWD, PATH_VECTOR ,   16, 1, 16, 1, 1, DT_ANY,     9,    16) \
     X(22, OP_BWD, PATH_VECTOR ,   32, 1,  8, 1, 1, DT_ANY,    17,    32) \
@@ -78,8 +85,12 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(88, OP_BWD, PATH_STAGED ,  512, 2,  1, 4, 1, DT_ANY,   513,  1024) \
     X(121, OP_BWD, PATH_RESTAGED, 512, 3, 1, 3, 1, DT_ANY,  1025,  1536) \
     X(118, OP_BWD, PATH_RESTAGED, 512, 4, 1, 2, 1, DT_ANY,  1537,  2048) \
-    X(46, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 4, DT_ANY,  2049,  4096) \
-    X(47, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 8, DT_ANY,  4097,  8192) \
+    X(127, OP_BWD, PATH_RESTAGED, 512, 3, 1, 3, 2, DT_ANY,  2049,  3072) \
+    X(123, OP_BWD, PATH_RESTAGED, 512, 4, 1, 2, 2, DT_ANY,  3073,  4096) \
+    X(128, OP_BWD, PATH_RESTAGED, 512, 3, 1, 3, 4, DT_ANY,  4097,  6144) \
+    X(124, OP_BWD, PATH_RESTAGED, 512, 4, 1, 2, 4, DT_ANY,  6145,  8192) \
+    X(46, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 4, DT_ANY,     0,     0) \
+    X(47, OP_BWD, PATH_VECTOR ,  512, 2,  1, 1, 8, DT_ANY,     0,     0) \
     X(26, OP_BWD, PATH_VECTOR ,  256, 2,  2, 1, 1, DT_ANY,     0,     0) \
     X(96, OP_BWD, PATH_STAGED ,  512, 3,  1, 3, 1, DT_ANY,     0,     0) \
     X(97, OP_BWD, PATH_STAGED ,  512, 4,  1, 2, 1, DT_ANY,     0,     0) \
@@ -110,6 +121,7 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(94, OP_BWD, PATH_STAGED ,  128, 2,  1, 8, 1, DT_ANY,     0,     0) \
     X(98, OP_BWD, PATH_STAGED ,  512, 3,  1, 2, 1, DT_ANY,     0,     0) \
     X(119, OP_BWD, PATH_RESTAGED, 512, 4, 1, 3, 1, DT_ANY,     0,     0) \
+    X(131, OP_BWD, PATH_RESTAGED, 512, 4, 1, 3, 2, DT_ANY,     0,     0) \
     /* backward main kernel, any N and alignment */ \
     X(36, OP_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0) \
     /* LayerNorm backward main kernel, persistent, row in registers (two \
@@ -126,8 +138,12 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(101, OP_LN_BWD, PATH_STAGED, 512, 3,  1, 3, 1, DT_F32,  1025,  1536) \
     X(122, OP_LN_BWD, PATH_RESTAGED, 512, 3, 1, 2, 1, DT_16,  1025,  1536) \
     X(116, OP_LN_BWD, PATH_RESTAGED, 512, 4, 1, 2, 1, DT_ANY,  1537,  2048) \
-    X(87, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 4, DT_ANY,  2049,  4096) \
-    X(70, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 8, DT_ANY,  4097,  8192) \
+    X(129, OP_LN_BWD, PATH_RESTAGED, 512, 3, 1, 3, 2, DT_ANY, 2049,  3072) \
+    X(125, OP_LN_BWD, PATH_RESTAGED, 512, 4, 1, 2, 2, DT_ANY, 3073,  4096) \
+    X(130, OP_LN_BWD, PATH_RESTAGED, 512, 3, 1, 3, 4, DT_ANY, 4097,  6144) \
+    X(126, OP_LN_BWD, PATH_RESTAGED, 512, 4, 1, 2, 4, DT_ANY, 6145,  8192) \
+    X(87, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 4, DT_ANY,     0,     0) \
+    X(70, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 8, DT_ANY,     0,     0) \
     X(81, OP_LN_BWD, PATH_VECTOR,  128, 2,  2, 1, 1, DT_ANY,     0,     0) \
     X(86, OP_LN_BWD, PATH_VECTOR,  512, 2,  1, 1, 2, DT_ANY,     0,     0) \
     X(82, OP_LN_BWD, PATH_VECTOR,  256, 2,  1, 1, 1, DT_ANY,     0,     0) \
@@ -155,7 +171,7 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
 // Largest CTA any plan uses.
 constexpr int kMaxCtaThreads = 1024;
 // Plan ids are below this bound (host caches are indexed by id).
-constexpr int kMaxPlanId = 128;
+constexpr int kMaxPlanId = 160;
 
 struct FwdParams {
     const void *x;
@@ -196,6 +212,7 @@ struct BwdParams {
     int N;
     float offset;
     const float *mean;       // LayerNorm: the forward's per-row mean
+    int stages = 0;          // staged kernels: stages in use (2 .. the plan's depth; 0: the depth)
 };
 
 // Codes written to the status word: a bounded wait (a cluster row's peer

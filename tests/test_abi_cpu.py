@@ -65,12 +65,22 @@ def test_fwd_default_plans(rn, dt, N, tpr, v, cs):
     assert p["ctas"] == 4096 // p["rows_per_cta"] * cs
 
 
-@pytest.mark.parametrize("dt,N,cs", [(0, 16384, 4), (1, 32768, 4), (1, 65536, 8), (0, 32768, 8)])
-def test_bwd_wide_rows_use_clusters(rn, dt, N, cs):
-    p = rn.plan_query(rn.OP_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)
-    assert p["path_name"] == "vector" and p["cluster_size"] == cs
+@pytest.mark.parametrize("dt,N,cs,v,stages", [(0, 16384, 2, 4, 2), (1, 32768, 2, 4, 2), (1, 65536, 4, 4, 2),
+                                              (0, 32768, 4, 4, 2), (1, 20480, 2, 3, 3), (1, 40960, 4, 3, 3)])
+@pytest.mark.parametrize("op", ["bwd", "ln"])
+def test_bwd_wide_rows_use_clusters(rn, dt, N, cs, v, stages, op):
+    """Rows wider than 2048 chunks: a cluster of cs staged CTAs shares each
+    row, each streaming an equal slice (a cs-th of the row, whole chunks)
+    into its stages; the cluster owns one partial row (two for LayerNorm)."""
+    code = rn.OP_BWD if op == "bwd" else rn.OP_LN_BWD
+    p = rn.plan_query(code, 16384, N, dt, num_sms=152, ctas_per_sm=1)
+    assert p["path_name"] == "staged" and p["cluster_size"] == cs and p["chunks_per_thread"] == v
     assert p["ws_rows"] == 152 // cs and p["ctas"] == p["ws_rows"] * cs
-    assert p["workspace_bytes"] == (p["ws_rows"] * N * 4 + 255) // 256 * 256
+    rows = 1 if op == "bwd" else 2
+    assert p["workspace_bytes"] == (p["ws_rows"] * rows * N * 4 + 255) // 256 * 256
+    es = 4 if dt == 0 else 2
+    slice_bytes = -(-N * es // (16 * cs)) * 16
+    assert p["smem_bytes"] == (2 * stages + (op == "ln")) * slice_bytes
 
 
 @pytest.mark.parametrize("dt,N", [(1, 4097), (1, 8191), (1, 8193), (0, 4097), (1, 65535), (0, 32767), (1, 1), (0, 3)])
@@ -147,7 +157,7 @@ def test_fp32_weight_flag_plans(rn):
 @pytest.mark.parametrize("dt,N,tpr,v,cs", [(1, 64, 8, 1, 1), (1, 1024, 128, 1, 1), (1, 2048, 128, 2, 1),
                                            (1, 4096, 256, 2, 1), (1, 8192, 256, 4, 1), (0, 8192, 512, 4, 1),
                                            (1, 16384, 512, 4, 1), (1, 12288, 512, 3, 1),
-                                           (1, 32768, 512, 2, 4), (1, 65536, 512, 2, 8)])
+                                           (1, 32768, 512, 4, 2), (1, 65536, 512, 4, 4), (1, 20480, 512, 3, 2)])
 def test_layernorm_backward_plans(rn, dt, N, tpr, v, cs):
     p = rn.plan_query(rn.OP_LN_BWD, 16384, N, dt, num_sms=152, ctas_per_sm=1)
     assert p["path_name"] in ("vector", "staged")

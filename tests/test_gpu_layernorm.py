@@ -274,7 +274,8 @@ def test_ln_reread_staged_backward_matches_held_bitwise(rn, M, N, reread, held, 
     assert rn.lib().rmsnorm_device_status(1) == 0
 
 
-@pytest.mark.parametrize("plan,N", [(115, 12288), (116, 16384), (117, 12288), (120, 8192), (122, 10240)])
+@pytest.mark.parametrize("plan,N", [(115, 12288), (116, 16384), (117, 12288), (120, 8192), (122, 10240), (129, 20488),
+                                    (130, 40968)])
 def test_ln_forced_reread_plans_match_oracle(rn, plan, N):
     M, dt = 203, "bf16"
     d = inputs.make_inputs(M, N, dt, 250 + plan, beta=True, x_shift=0.5)
@@ -289,4 +290,44 @@ def test_ln_forced_reread_plans_match_oracle(rn, plan, N):
     check_dx(to_host(o["dx"], dt), r, dt)
     check_param_grad(to_host(o["dgamma"], dt), r["dg64"], r["dg_abs"], dt)
     check_param_grad(to_host(o["dbeta"], dt), r["db64"], r["db_abs"], dt)
+
+
+@pytest.mark.parametrize("M,N,cluster", [(301, 16384, 125), (90, 12288, 126), (50, 24, 126)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_ln_cluster_staged_rows_independent_of_partial_rows(rn, M, N, cluster, fused):
+    """The LayerNorm backward on a cluster of staged CTAs: dx keeps its bits
+    over another number of partial rows, and dgamma, dbeta agree."""
+    d = inputs.make_inputs(M, N, "bf16", 360 + N % 7, beta=True, x_shift=0.5, residual=fused, dres=fused)
+    x, g, b, dy = (to_dev(d[k], "bf16") for k in ("x", "w", "beta", "dy"))
+    dres = to_dev(d["dres"], "bf16") if fused else None
+    out = rn.layernorm_fwd(x, g, b)
+    a = rn.layernorm_bwd(dy, x, g, out["mean"], out["rstd"], dresidual_out=dres, force_plan=cluster, force_ctas=30)
+    v = rn.layernorm_bwd(dy, x, g, out["mean"], out["rstd"], dresidual_out=dres, force_plan=cluster, force_ctas=7)
+    torch.cuda.synchronize()
+    assert a["plan"]["cluster_size"] > 1 and a["plan"]["ws_rows"] == 30 and v["plan"]["ws_rows"] == 7
+    assert cuda_bits_equal(a["dx"], v["dx"])
+    for k in ("dgamma", "dbeta"):
+        assert torch.allclose(a[k].float(), v[k].float(), rtol=1e-2, atol=1e-2), k
+    assert rn.lib().rmsnorm_device_status(1) == 0
+
+
+@pytest.mark.parametrize("dt,M,N,plan", [("bf16", 101, 20488, 125), ("f32", 64, 16384, 125), ("bf16", 33, 40968, 126),
+                                         ("bf16", 77, 8192, 125), ("f32", 29, 12, 126)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_ln_cluster_staged_wide_rows_match_oracle(rn, dt, M, N, plan, fused):
+    d = inputs.make_inputs(M, N, dt, 370 + N % 13, beta=True, x_shift=0.5, residual=fused, dres=fused)
+    x, g, dy = (to_dev(d[k], dt) for k in ("x", "w", "dy"))
+    dres = to_dev(d["dres"], dt) if fused else None
+    f = oracle.ln_fwd(d["x"], d["w"], d["beta"], dtype=dt, eps=1e-5, offset=0.0)
+    mean = torch.from_numpy(f["mean32"]).cuda()
+    rstd = torch.from_numpy(f["rstd32"]).cuda()
+    o = rn.layernorm_bwd(dy, x, g, mean, rstd, dresidual_out=dres, force_plan=plan)
+    assert o["plan"]["plan_id"] == plan
+    r = oracle.ln_bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=1e-5, offset=0.0, mean=f["mean32"], rstd=f["rstd32"],
+                      dres=d.get("dres") if fused else None)
+    torch.cuda.synchronize()
+    check_dx(to_host(o["dx"], dt), r, dt)
+    check_param_grad(to_host(o["dgamma"], dt), r["dg64"], r["dg_abs"], dt)
+    check_param_grad(to_host(o["dbeta"], dt), r["db64"], r["db_abs"], dt)
+    assert rn.lib().rmsnorm_device_status(1) == 0
 

@@ -40,7 +40,7 @@ def test_packed_matches_scalar_bitwise(rn, dt, M, N, fused):
     # (the staged kernel has the packed variant only)
     code = {"bf16": rn.RMSNORM_BF16, "f32": rn.RMSNORM_F32, "f16": rn.RMSNORM_F16}[dt]
     default = rn.plan_query(rn.OP_BWD, M, N, code)
-    plan = {88: 27, 95: 26, 121: 42, 118: 45}.get(default["plan_id"], -1) if default["path_name"] == "staged" else -1
+    plan = {88: 27, 95: 26, 121: 42, 118: 45, 127: 46, 123: 46, 128: 47, 124: 47}.get(default["plan_id"], -1) if default["path_name"] == "staged" else -1
     kw = dict(dresidual_out=t.get("dres"), fused=fused, force_plan=plan)
     dx1, dw1, p1 = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], rstd, force_packed=1, **kw)
     dx0, dw0, p0 = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], rstd, force_packed=0, **kw)
@@ -237,7 +237,7 @@ def test_forced_forward_plans_match_oracle(rn, plan):
     check_rstd(r.cpu().numpy(), f["rstd64"])
 
 
-@pytest.mark.parametrize("plan", [27, 34, 35, 36, 44, 45, 48, 49, 88, 89, 90, 96, 97, 98, 118, 119, 121])
+@pytest.mark.parametrize("plan", [27, 34, 35, 36, 44, 45, 48, 49, 88, 89, 90, 96, 97, 98, 118, 119, 121, 123, 124, 127, 128, 131])
 def test_forced_backward_plans_match_oracle(rn, plan):
     M, N, dt = 777, 8192, "bf16"
     d, t = dev_inputs(M, N, dt, 102)
@@ -376,3 +376,50 @@ def test_generic_rows_independent_of_other_arrays_alignment(rn, dt, N, xoff):
     for other in outs[1:]:
         for a, c in zip(outs[0], other):
             assert cuda_bits_equal(a, c)
+
+
+@pytest.mark.parametrize("dt,M,N,cluster", [("bf16", 301, 16384, 123), ("f32", 77, 8192, 124), ("f16", 150, 12288, 123),
+                                            ("bf16", 40, 16, 124), ("f32", 33, 4, 123), ("bf16", 64, 20480, 123)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_cluster_staged_rows_match_oracle_any_partial_rows(rn, dt, M, N, cluster, fused):
+    """A row shared by a cluster of staged CTAs (each streams an equal slice,
+    the last ones shorter or empty; the row sums meet in distributed shared
+    memory) against the oracle; dx is a function of the row alone, so it
+    keeps its bits when the rows are spread over another number of units."""
+    d, t = dev_inputs(M, N, dt, 340 + N % 7, residual=fused, dres=fused)
+    f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0)
+    r = torch.from_numpy(f["rstd32"]).cuda()
+    kw = dict(dresidual_out=t.get("dres"), fused=fused, force_plan=cluster)
+    a_dx, a_dw, ap = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], r, force_ctas=30, **kw)
+    b_dx, b_dw, bp = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], r, force_ctas=7, **kw)
+    b = oracle.bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0, rstd=f["rstd32"],
+                   dres=d.get("dres") if fused else None)
+    torch.cuda.synchronize()
+    assert ap["path_name"] == "staged" and ap["cluster_size"] > 1 and ap["ws_rows"] == min(30, M)
+    assert bp["ws_rows"] == 7 and bp["ctas"] == 7 * bp["cluster_size"]
+    check_dx(to_host(a_dx, dt), b, dt)
+    check_dw(to_host(a_dw, dt), b, dt)
+    check_dw(to_host(b_dw, dt), b, dt)
+    assert cuda_bits_equal(a_dx, b_dx)
+    assert rn.lib().rmsnorm_device_status(1) == 0
+
+
+@pytest.mark.parametrize("dt,M,N,plan", [("bf16", 203, 20488, 123), ("f32", 130, 16384, 123), ("bf16", 67, 40968, 124),
+                                         ("f16", 45, 65536, 124), ("bf16", 3, 32768, 123)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_cluster_staged_wide_rows_match_oracle(rn, dt, M, N, plan, fused):
+    """Rows wider than one CTA's stages, each CTA of the cluster streaming a
+    (ragged) slice, against the oracle."""
+    d, t = dev_inputs(M, N, dt, 350 + N % 11, residual=fused, dres=fused)
+    f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0)
+    r = torch.from_numpy(f["rstd32"]).cuda()
+    dx, dw, p = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], r, dresidual_out=t.get("dres"), fused=fused,
+                                  force_plan=plan)
+    assert p["plan_id"] == plan and p["ctas"] == p["ws_rows"] * p["cluster_size"]
+    b = oracle.bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0, rstd=f["rstd32"],
+                   dres=d.get("dres") if fused else None)
+    torch.cuda.synchronize()
+    check_dx(to_host(dx, dt), b, dt)
+    check_dw(to_host(dw, dt), b, dt)
+    assert rn.lib().rmsnorm_device_status(1) == 0
+
