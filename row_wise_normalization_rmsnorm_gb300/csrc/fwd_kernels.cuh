@@ -25,14 +25,14 @@ namespace rmsn {
 // The row's chunks into registers; with FUSED, h = R(x + residual) is
 // formed in place and stored to residual_out. Chunks past the row are zero.
 template <typename T, int TPR, int V, bool FUSED>
-__device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, int cbase, int t, int C, bool valid,
+__device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, int cbase, int t, int cend, bool valid,
                                              uint4 (&xv)[V]) {
     using Pk = Pair<true>;
     constexpr int NP = Elem<T>::NP;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
-        xv[v] = c < C ? ld_stream(reinterpret_cast<const uint4 *>(p.x) + base + c) : make_uint4(0, 0, 0, 0);
+        xv[v] = c < cend ? ld_stream(reinterpret_cast<const uint4 *>(p.x) + base + c) : make_uint4(0, 0, 0, 0);
     }
     if constexpr (FUSED) {
         // h = R(x + residual). For bf16 inputs the fp32 sum is exact unless
@@ -43,7 +43,7 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = cbase + v * TPR + t;
-            rv[v] = c < C ? ld_stream(reinterpret_cast<const uint4 *>(p.residual) + base + c)
+            rv[v] = c < cend ? ld_stream(reinterpret_cast<const uint4 *>(p.residual) + base + c)
                           : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -55,7 +55,7 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
             for (int k = 0; k < NP; ++k) a[k] = Pk::add(a[k], b[k]);
             xv[v] = pack<T>(a);
             const int c = cbase + v * TPR + t;
-            if (valid && c < C) st_chunk(reinterpret_cast<uint4 *>(p.residual_out) + base + c, xv[v]);
+            if (valid && c < cend) st_chunk(reinterpret_cast<uint4 *>(p.residual_out) + base + c, xv[v]);
         }
     }
 }
@@ -87,14 +87,17 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
     } else {
         row = (int64_t)blockIdx.x * TEAMS + team;
     }
-    const int cbase = (int)rank * TPR * V;  // first chunk of this CTA's slice
     const bool valid = row < p.M;
     const int64_t rr = valid ? row : p.M - 1;  // keep every thread in the reductions
     const int C = p.N / Elem<T>::E;
     const int64_t base = rr * C;
+    // a cluster row: equal slices of ceil(C / CS) chunks, the last shorter
+    const int cslice = (C + CS - 1) / CS;
+    const int cbase = (int)rank * cslice;  // first chunk of this CTA's slice
+    const int cend = cbase + cslice < C ? cbase + cslice : C;
 
     uint4 xv[V];
-    fwd_load_row<T, TPR, V, FUSED>(p, base, cbase, t, C, valid, xv);
+    fwd_load_row<T, TPR, V, FUSED>(p, base, cbase, t, cend, valid, xv);
 
     float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = cbase + v * TPR + t;
-            if (c < C) {
+            if (c < cend) {
                 float2 a[NP];
                 unpack<T>(xv[v], a);
                 if (has_w) {
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
             const int c = cbase + v * TPR + t;
             unpack<T>(xv[v], yv[v]);  // zero chunks beyond the row give y = 0
             float2 wv[NP];
-            if (has_w && c < C) {
+            if (has_w && c < cend) {
                 load_w_chunk<T, TW>(p.w, c, wv);
             } else {
 #pragma unroll
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = cbase + v * TPR + t;
-            if (c < C) {
+            if (c < cend) {
                 float2 q[NP];
 #pragma unroll
                 for (int k = 0; k < NP; ++k) q[k] = Pk::mul(yv[v][k], s2);
@@ -327,20 +330,22 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     } else {
         row = (int64_t)blockIdx.x * TEAMS + team;
     }
-    const int cbase = (int)rank * TPR * V;
     const bool valid = row < p.M;
     const int64_t rr = valid ? row : p.M - 1;
     const int C = p.N / Elem<T>::E;
     const int64_t base = rr * C;
+    const int cslice = (C + CS - 1) / CS;  // a cluster row: equal slices
+    const int cbase = (int)rank * cslice;
+    const int cend = cbase + cslice < C ? cbase + cslice : C;
 
     uint4 xv[V];
-    fwd_load_row<T, TPR, V, FUSED>(p, base, cbase, t, C, valid, xv);
+    fwd_load_row<T, TPR, V, FUSED>(p, base, cbase, t, cend, valid, xv);
 
     float2 sm = make_float2(0.f, 0.f);
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         float2 a[NP];
-        unpack<T>(xv[v], a);  // chunks past the row are zero
+        unpack<T>(xv[v], a);  // chunks past the slice are zero
 #pragma unroll
         for (int k = 0; k < NP; ++k) sm = Pk::add(sm, a[k]);
     }
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
-        if (c < C) {
+        if (c < cend) {
             float2 a[NP];
             unpack<T>(xv[v], a);
 #pragma unroll
@@ -383,7 +388,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
-        if (c < C) {
+        if (c < cend) {
             float2 a[NP], gv[NP], bv[NP];
             unpack<T>(xv[v], a);
             if (p.w) {
