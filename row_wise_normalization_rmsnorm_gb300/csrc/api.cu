@@ -98,7 +98,9 @@ static int64_t staged_smem_at(const PlanDesc &d, int64_t N, int es, bool fused, 
     const int64_t C = (N * es + 15) / 16;
     const int64_t row = (C + d.cs - 1) / d.cs * 16;
     const int64_t gamma = d.path == PATH_RESTAGED && d.op == OP_LN_BWD ? row : 0;
-    return (int64_t)depth * (fused ? 3 : 2) * row + gamma;
+    // a stage holds x and dy (and dres) rows; the staged forward's x (and residual)
+    const int rows = d.op == OP_FWD_STAGED ? (fused ? 2 : 1) : (fused ? 3 : 2);
+    return (int64_t)depth * rows * row + gamma;
 }
 
 // Stages a call takes: the plan's depth, or fewer (at least two) where the
@@ -136,7 +138,8 @@ static int64_t plan_capacity(const PlanDesc &d) { return (int64_t)d.tpr * d.v * 
 // backward dW partial rows: resident CTAs (or, for cluster plans, resident
 // clusters) on the device; ctas_per_sm is reported only.
 static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool aligned, int64_t max_parts,
-                                    int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
+                                    int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out,
+                                    bool regs_only = false) {
     if (!out) return RMSNORM_ERR_INVALID_ARG;
     if (op != RMSNORM_OP_FWD && op != RMSNORM_OP_BWD && op != RMSNORM_OP_LN_BWD) return RMSNORM_ERR_INVALID_ARG;
     if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
@@ -149,15 +152,21 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     const PlanDesc *d = nullptr;
     if (force_plan >= 0) {
         d = find_plan(force_plan);
-        if (!d || d->op != op) return RMSNORM_ERR_UNSUPPORTED;
+        // a forward may take a staged forward plan (not for the E4M3 outputs)
+        const bool staged_fwd = d && op == RMSNORM_OP_FWD && d->op == OP_FWD_STAGED && !regs_only;
+        if (!d || (d->op != op && !staged_fwd)) return RMSNORM_ERR_UNSUPPORTED;
         if (d->path == PATH_VECTOR && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
-        // staged plans: backward only, aligned rows that fit, one type
-        if (staged_path(d->path) && (op == RMSNORM_OP_FWD || !vec_ok || C > plan_capacity(*d)))
-            return RMSNORM_ERR_UNSUPPORTED;
+        // staged plans: aligned rows that fit
+        if (staged_path(d->path) && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
         // with an fp32 weight only the default plans (and the generic one) are compiled
         if (mixed_kind(kind_of(dt)) && row_path(d->path) && d->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
     } else {
         d = vec_ok ? default_vector_plan(op, dt, C) : nullptr;
+        // a staged forward plan that covers the row is preferred
+        if (op == RMSNORM_OP_FWD && vec_ok && !regs_only) {
+            const PlanDesc *sd = default_vector_plan(OP_FWD_STAGED, dt, C);
+            if (sd) d = sd;
+        }
         if (!d) d = generic_plan(op);
     }
     if (!d) return RMSNORM_ERR_UNSUPPORTED;
@@ -172,7 +181,8 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     out->packed = d->path == PATH_GENERIC ? 0 : 1;
     out->cluster_size = d->cs;
     const int64_t units = (M + out->rows_per_cta - 1) / out->rows_per_cta;  // CTAs (or clusters) with rows
-    if (op == RMSNORM_OP_FWD) {
+    const bool staged_fwd = d->op == OP_FWD_STAGED;
+    if (op == RMSNORM_OP_FWD && !staged_fwd) {
         out->ctas = (int32_t)(units * d->cs);
         return RMSNORM_SUCCESS;
     }
@@ -192,7 +202,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
         out->smem_bytes = (int32_t)sm;
     }
     if (!staged_path(d->path) && out->smem_bytes > 44 * 1024) return RMSNORM_ERR_UNSUPPORTED;
-    const int64_t bytes = P * partial_rows(op) * N * 4;
+    const int64_t bytes = staged_fwd ? 0 : P * partial_rows(op) * N * 4;  // the forward has no partial rows
     out->workspace_bytes = (bytes + 255) / 256 * 256;
     return RMSNORM_SUCCESS;
 }
@@ -296,6 +306,41 @@ static const void *ln_bwd_kernel(int plan_id, int dt, bool fused) {
     case RMSNORM_BF16: return ln_bwd_kernel_ptr_bf16(plan_id, fused);
     case RMSNORM_F16: return ln_bwd_kernel_ptr_f16(plan_id, fused);
     default: return ln_bwd_kernel_ptr_f32(plan_id, fused);
+    }
+}
+
+static const void *fwd_staged_kernel(int plan_id, int dt, bool fused, bool ln) {
+    if (ln) {
+        switch (base_dtype(dt)) {
+        case RMSNORM_BF16: return ln_fwd_staged_kernel_ptr_bf16(plan_id, fused);
+        case RMSNORM_F16: return ln_fwd_staged_kernel_ptr_f16(plan_id, fused);
+        default: return ln_fwd_staged_kernel_ptr_f32(plan_id, fused);
+        }
+    }
+    switch (kind_of(dt)) {
+    case 1: return fwd_staged_kernel_ptr_bf16(plan_id, fused);
+    case 2: return fwd_staged_kernel_ptr_f16(plan_id, fused);
+    case 3: return fwd_staged_kernel_ptr_bf16w32(plan_id, fused);
+    case 4: return fwd_staged_kernel_ptr_f16w32(plan_id, fused);
+    default: return fwd_staged_kernel_ptr_f32(plan_id, fused);
+    }
+}
+
+static int launch_fwd_staged_dt(int dt, bool ln, int plan_id, bool fused, const FwdParams &p, int grid, int smem,
+                                void *stream) {
+    if (ln) {
+        switch (base_dtype(dt)) {
+        case RMSNORM_BF16: return launch_ln_fwd_staged_bf16(plan_id, fused, p, grid, smem, stream);
+        case RMSNORM_F16: return launch_ln_fwd_staged_f16(plan_id, fused, p, grid, smem, stream);
+        default: return launch_ln_fwd_staged_f32(plan_id, fused, p, grid, smem, stream);
+        }
+    }
+    switch (kind_of(dt)) {
+    case 1: return launch_fwd_staged_bf16(plan_id, fused, p, grid, smem, stream);
+    case 2: return launch_fwd_staged_f16(plan_id, fused, p, grid, smem, stream);
+    case 3: return launch_fwd_staged_bf16w32(plan_id, fused, p, grid, smem, stream);
+    case 4: return launch_fwd_staged_f16w32(plan_id, fused, p, grid, smem, stream);
+    default: return launch_fwd_staged_f32(plan_id, fused, p, grid, smem, stream);
     }
 }
 
@@ -413,6 +458,80 @@ static bool aligned_to(const void *p, uintptr_t a) { return ((uintptr_t)p % a) =
 
 static bool finite_scalar(float v) { return std::isfinite(v); }
 
+// Resident units (CTAs, or clusters) of a staged forward plan on the
+// device, taken at the plan's largest rows (the conservative value) and
+// cached per device, type, fusion mode and RMSNorm/LayerNorm.
+static int g_sfwd_parts[kMaxDevices][kNumKinds][2][2][kMaxPlanId];
+
+static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d, bool fused, bool ln, int *parts_out) {
+    if (d.id < 0 || d.id >= kMaxPlanId) return cudaErrorInvalidValue;
+    int &slot = g_sfwd_parts[dev][kind_of(dt)][fused ? 1 : 0][ln ? 1 : 0][d.id];
+    {
+        std::lock_guard<std::mutex> lk(g_occ_mutex);
+        if (slot > 0) {
+            *parts_out = slot;
+            return cudaSuccess;
+        }
+    }
+    const void *k = fwd_staged_kernel(d.id, dt, fused, ln);
+    if (!k) return cudaErrorInvalidDeviceFunction;
+    cudaError_t e = (cudaError_t)allow_staged_smem(k);
+    if (e != cudaSuccess) return e;
+    const int64_t nmax = plan_capacity(d) * (16 / elem_size(dt));
+    const int smem = (int)std::min<int64_t>(staged_smem_bytes(d, nmax, elem_size(dt), fused), kMaxDynamicSmem);
+    int n = 0;
+    if (d.cs > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(d.cs * sms));
+        cfg.blockDim = dim3((unsigned)d.tpr);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)d.cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+    } else {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, d.tpr, smem);
+        n *= sms;
+    }
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;  // not resident at all: refuse
+    std::lock_guard<std::mutex> lk(g_occ_mutex);
+    slot = n;
+    *parts_out = n;
+    return cudaSuccess;
+}
+
+// A forward on a staged plan: the grid becomes the resident units walking
+// the rows, and the stages in use, the shared memory and the status word
+// are set. Other plans are left as they are.
+static rmsnorm_status_t prepare_staged_fwd(int64_t M, int64_t N, int dt, bool aligned, bool fused, bool ln,
+                                           int force_plan, rmsnorm_plan_t *plan, int *stages, int **status) {
+    *stages = 0;
+    *status = nullptr;
+    const PlanDesc *d = find_plan(plan->plan_id);
+    if (!d || d->op != OP_FWD_STAGED) return RMSNORM_SUCCESS;
+    const int es = elem_size(dt);
+    const int depth = staged_depth(*d, N, es, fused);
+    if (depth == 0) return RMSNORM_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int parts = 1;
+    e = staged_fwd_parts(dev, sms, dt, *d, fused, ln, &parts);
+    if (e != cudaSuccess) return cuda_fail(e);
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, parts, 0, force_plan, 0, plan);
+    if (st != RMSNORM_SUCCESS) return st;
+    plan->smem_bytes = (int32_t)staged_smem_bytes(*d, N, es, fused);
+    e = status_word(dev, status);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *stages = depth;
+    return RMSNORM_SUCCESS;
+}
+
 static std::atomic<int> g_table_ok{-1};
 
 int self_check_impl() {
@@ -434,9 +553,24 @@ int self_check_impl() {
         }
         if (!generic_plan(op)) ++bad;
     }
+    // staged forward defaults: contiguous ranges (they need not start at 1),
+    // each selecting its entry and held by it
+    for (int dt = 0; dt < 3; ++dt) {
+        int64_t expect = -1;
+        for (int i = 0; i < kNumPlans; ++i) {
+            const PlanDesc &d = kPlans[i];
+            if (d.op != OP_FWD_STAGED || d.cmin == 0 || !(d.dtm & dtype_bit(dt))) continue;
+            if ((expect >= 0 && d.cmin != expect) || d.cmax < d.cmin || plan_capacity(d) < d.cmax) ++bad;
+            expect = d.cmax + 1;
+            if (default_vector_plan(OP_FWD_STAGED, dt, d.cmin) != &d ||
+                default_vector_plan(OP_FWD_STAGED, dt, d.cmax) != &d)
+                ++bad;
+        }
+    }
     for (int i = 0; i < kNumPlans; ++i) {
         const PlanDesc &d = kPlans[i];
         if (find_plan(d.id) != &d) ++bad;  // ids unique
+        if (d.op == OP_FWD_STAGED && d.path != PATH_RESTAGED) ++bad;
         if (d.path == PATH_VECTOR) {
             const bool pow2 = d.tpr > 0 && (d.tpr & (d.tpr - 1)) == 0;
             if (!pow2 || d.tpr * d.teams > kMaxCtaThreads || d.tpr * d.teams < 32 || d.v < 1) ++bad;
@@ -446,8 +580,9 @@ int self_check_impl() {
         if (staged_path(d.path)) {
             // one team per CTA of whole warps, at least two stages, backward
             // only; a cluster (2, 4 or 8 CTAs) only on the re-read schedule
-            if (d.op == OP_FWD || !staged_plan(d.path, d.teams, d.cs) || d.depth < 2 || d.tpr % 32 != 0 ||
-                d.tpr < 64 || d.tpr > kMaxCtaThreads || d.v < 1)
+            if (d.op == OP_FWD || (d.op == OP_FWD_STAGED && d.path != PATH_RESTAGED) ||
+                !staged_plan(d.path, d.teams, d.cs) || d.depth < 2 || d.tpr % 32 != 0 || d.tpr < 64 ||
+                d.tpr > kMaxCtaThreads || d.v < 1)
                 ++bad;
         }
         if (d.dtm < 1 || d.dtm > DT_ANY) ++bad;
@@ -522,11 +657,16 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (fused) aligned = aligned && aligned_to(residual, 16) && aligned_to(residual_out, 16);
 
     rmsnorm_plan_t plan;
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, 1, 0, force_plan, 0, &plan);
+    // the E4M3 outputs stay on the register kernels
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, 1, 0, force_plan, 0, &plan, quant);
     if (st != RMSNORM_SUCCESS) return st;
     // the E4M3 kernels are compiled for the default plans and the generic one
     if (quant && force_plan >= 0 && plan.path == PATH_VECTOR && find_plan(plan.plan_id)->cmin == 0)
         return RMSNORM_ERR_UNSUPPORTED;
+    int stages = 0;
+    int *status = nullptr;
+    st = prepare_staged_fwd(M, N, dt, aligned, fused, false, force_plan, &plan, &stages, &status);
+    if (st != RMSNORM_SUCCESS) return st;
 
     FwdParams p;
     p.x = x;
@@ -544,6 +684,8 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     p.qamax = reinterpret_cast<unsigned int *>(q.amax);
     p.beta = nullptr;
     p.mean = nullptr;
+    p.stages = stages;
+    p.status = status;
     int le;
     if (quant) {
         cudaError_t e = clear_amax();
@@ -553,6 +695,8 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
         case RMSNORM_F16: le = launch_fwd8_f16(plan.plan_id, fused, q.qmode, p, plan.ctas, stream); break;
         default: le = launch_fwd8_f32(plan.plan_id, fused, q.qmode, p, plan.ctas, stream); break;
         }
+    } else if (stages > 0) {
+        le = launch_fwd_staged_dt(dt, false, plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream);
     } else {
         le = launch_fwd_dt(dt, plan.plan_id, fused, p, plan.ctas, stream);
     }
@@ -727,6 +871,10 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
     if (st != RMSNORM_SUCCESS) return st;
     // the LayerNorm forward is compiled for the default plans and the generic one
     if (plan.path == PATH_VECTOR && find_plan(plan.plan_id)->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
+    int stages = 0;
+    int *status = nullptr;
+    st = prepare_staged_fwd(M, N, dt, aligned, fused, true, force_plan, &plan, &stages, &status);
+    if (st != RMSNORM_SUCCESS) return st;
 
     FwdParams p;
     std::memset(&p, 0, sizeof p);
@@ -742,11 +890,17 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
     p.N = (int)N;
     p.eps = eps;
     p.offset = offset;
+    p.stages = stages;
+    p.status = status;
     int le;
-    switch (base_dtype(dt)) {
-    case RMSNORM_BF16: le = launch_ln_fwd_bf16(plan.plan_id, fused, p, plan.ctas, stream); break;
-    case RMSNORM_F16: le = launch_ln_fwd_f16(plan.plan_id, fused, p, plan.ctas, stream); break;
-    default: le = launch_ln_fwd_f32(plan.plan_id, fused, p, plan.ctas, stream); break;
+    if (stages > 0) {
+        le = launch_fwd_staged_dt(dt, true, plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream);
+    } else {
+        switch (base_dtype(dt)) {
+        case RMSNORM_BF16: le = launch_ln_fwd_bf16(plan.plan_id, fused, p, plan.ctas, stream); break;
+        case RMSNORM_F16: le = launch_ln_fwd_f16(plan.plan_id, fused, p, plan.ctas, stream); break;
+        default: le = launch_ln_fwd_f32(plan.plan_id, fused, p, plan.ctas, stream); break;
+        }
     }
     if (le != 0) return cuda_fail((cudaError_t)le);
     if (used) *used = plan;

@@ -6,4 +6,10 @@ int launch_fwd_f32(int plan_id, bool fused, const FwdParams &p, int grid, void *
     return launch_t<float, float>(plan_id, fused, p, grid, stream);
 }
 const void *fwd_kernel_ptr_f32(int plan_id, bool fused) { return ptr_t<float, float>(plan_id, fused); }
+int launch_fwd_staged_f32(int plan_id, bool fused, const FwdParams &p, int grid, int smem, void *stream) {
+    return staged_fwd_launch_t<float, float, false>(plan_id, fused, p, grid, smem, stream);
+}
+const void *fwd_staged_kernel_ptr_f32(int plan_id, bool fused) {
+    return staged_fwd_ptr_t<float, float, false>(plan_id, fused);
+}
 }  // namespace rmsn

@@ -504,6 +504,262 @@ __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) 
         });
 }
 
+// Staged persistent forward, for rows that one CTA's registers serve badly
+// (wider than 2048 chunks: one row per short-lived cluster keeps too few
+// loads in flight). A unit (a CTA, or a cluster whose CTAs take equal
+// slices of each row) walks rows unit, unit + G, ...; each row's x (and
+// residual) slice streams by cp.async.bulk into one of the stages, counted
+// in bytes on the stage's mbarrier. Pass 1 forms h (fused: R(x + r), stored
+// to residual_out) and the row sum of squares (LayerNorm: the sum, then in
+// a pass of its own the squared deviations); pass 2 reads the stage again
+// and writes y. The last warp through a stage refills it, as in the
+// backward's re-read schedule. A thread's chunks, their order and the
+// reduction tree are the register forward's, so y and rstd are the same
+// bits. Every wait is bounded; one that gives up writes the status word and
+// the kernel carries on.
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool LN>
+__device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
+    using Pk = Pair<true>;
+    constexpr int E = Elem<T>::E;
+    constexpr int NP = Elem<T>::NP;
+    constexpr int W = TPR / 32;
+    constexpr int NB = FUSED ? 2 : 1;  // rows a stage holds: x (, residual)
+    static_assert(TPR % 32 == 0 && TPR >= 64, "whole warps");
+    __shared__ float red[2][CS * W];
+    __shared__ __align__(8) uint64_t full[S];
+    __shared__ __align__(8) uint64_t rbar[2];  // cluster rows: arrival of the peers' sums
+    __shared__ unsigned done[S];               // warps through the stage's row
+    extern __shared__ float4 fstage_smem[];    // ns * NB * Cst chunks of 16 bytes
+
+    const int N = p.N;
+    const int C = N / E;
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    uint32_t rank = 0;
+    if constexpr (CS > 1) rank = cluster_ctarank();
+    const int Cst = (C + CS - 1) / CS;  // this CTA's slice: chunks [cbase, cbase + Cs)
+    const int cbase = (int)rank * Cst;
+    const int Cs = C - cbase <= 0 ? 0 : (C - cbase < Cst ? C - cbase : Cst);
+    const int64_t unit = CS > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
+    const int64_t G = CS > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
+    const int64_t iters = unit < p.M ? (p.M - unit + G - 1) / G : 0;
+    const int ns = p.stages >= 2 && p.stages < S ? p.stages : S;
+    const uint32_t row_bytes = (uint32_t)Cs * 16u;
+    uint4 *stages = reinterpret_cast<uint4 *>(fstage_smem);
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x);
+    const uint4 *r4 = reinterpret_cast<const uint4 *>(p.residual);
+    auto issue = [&](int64_t k, int s) {
+        const int64_t off = (unit + k * G) * C + cbase;
+        uint4 *dst = stages + (size_t)s * NB * Cst;
+        mbar_arrive_expect_tx(&full[s], row_bytes * NB);
+        if (row_bytes == 0) return;  // an empty slice: the arrival alone completes the phase
+        bulk_g2s(dst, x4 + off, row_bytes, &full[s]);
+        if constexpr (FUSED) bulk_g2s(dst + Cst, r4 + off, row_bytes, &full[s]);
+    };
+    constexpr uint32_t kSlotBytes = CS * W * sizeof(float);
+    if (t == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            done[s] = 0;
+        }
+        if constexpr (CS > 1) {
+            mbar_init(&rbar[0], 1);
+            mbar_init(&rbar[1], 1);
+            mbar_arrive_expect_tx(&rbar[0], kSlotBytes);
+            mbar_arrive_expect_tx(&rbar[1], kSlotBytes);
+        }
+        mbar_init_fence();
+        for (int s = 0; s < ns && s < iters; ++s) issue(s, s);
+    }
+    __syncthreads();
+    if constexpr (CS > 1) cluster_sync();
+
+    bool failed = false;
+    // Row sum across the unit. Reduction q uses slot buffer q & 1; a cluster
+    // sends each warp's sum to every CTA (st.async, counted in bytes on the
+    // receiver's barrier, phase parity (q >> 1) & 1) and re-arms the barrier
+    // after reading; a buffer is written again (q + 2) only after every warp
+    // sent its q + 1 sum, which it does after reading the buffer for q.
+    uint32_t q = 0;
+    auto rowsum = [&](float v) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        const int b = (int)(q & 1);
+        float sum;
+        if constexpr (CS > 1) {
+            if (lane == 0) {
+#pragma unroll
+                for (int c = 0; c < CS; ++c) st_async_cluster(&red[b][rank * W + (t >> 5)], &rbar[b], (uint32_t)c, v);
+            }
+            if (!mbar_wait(&rbar[b], (q >> 1) & 1u, kWaitLimit)) failed = true;
+            sum = sum_slots<CS * W>(&red[b][0], lane);
+            if (t == 0) mbar_arrive_expect_tx(&rbar[b], kSlotBytes);
+        } else {
+            if (lane == 0) red[b][t >> 5] = v;
+            __syncthreads();
+            sum = sum_slots<W>(&red[b][0], lane);
+        }
+        ++q;
+        return sum;
+    };
+
+    const float2 o2 = make_float2(p.offset, p.offset);
+    int s = 0;
+    uint32_t ph = 0;
+    for (int64_t k = 0; k < iters; ++k) {
+        const int64_t row = unit + k * G;
+        if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
+        const int sk = s;
+        const uint4 *src = stages + (size_t)s * NB * Cst;
+        const int64_t base = row * C + cbase;
+        // h of chunk v of the slice (fused: R(x + r), stored once in pass 1)
+        auto hchunk = [&](int v, float2 (&h)[NP], bool store) {
+            const int cl = v * TPR + t;
+            if (cl < Cs) {
+                unpack<T>(lds128(src + cl), h);
+                if constexpr (FUSED) {
+                    float2 rr[NP];
+                    unpack<T>(lds128(src + Cst + cl), rr);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) h[j] = Pk::add(h[j], rr[j]);
+                    const uint4 hp = pack<T>(h);
+                    if (store) st_chunk(reinterpret_cast<uint4 *>(p.residual_out) + base + cl, hp);
+                    unpack<T>(hp, h);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < NP; ++j) h[j] = make_float2(0.f, 0.f);
+            }
+        };
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float2 h[NP];
+            hchunk(v, h, true);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) acc = LN ? Pk::add(acc, h[j]) : Pk::fma(h[j], h[j], acc);
+        }
+        float rstd, mu = 0.f;
+        if constexpr (LN) {
+            mu = __fdiv_rn(rowsum(__fadd_rn(acc.x, acc.y)), (float)N);
+            const float2 nmu2 = make_float2(-mu, -mu);
+            float2 sq = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                if (v * TPR + t < Cs) {
+                    float2 h[NP];
+                    hchunk(v, h, false);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) {
+                        const float2 d = Pk::add(h[j], nmu2);
+                        sq = Pk::fma(d, d, sq);
+                    }
+                }
+            }
+            rstd = rsqrtf(__fadd_rn(__fdiv_rn(rowsum(__fadd_rn(sq.x, sq.y)), (float)N), p.eps));
+        } else {
+            rstd = rsqrtf(__fadd_rn(__fdiv_rn(rowsum(__fadd_rn(acc.x, acc.y)), (float)N), p.eps));
+        }
+        if (t == 0 && rank == 0) {
+            p.rstd[row] = rstd;
+            if constexpr (LN) p.mean[row] = mu;
+        }
+        const float2 r2 = make_float2(rstd, rstd);
+        const float2 nmu2 = make_float2(-mu, -mu);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int cl = v * TPR + t;
+            if (cl < Cs) {
+                const int c = cbase + cl;
+                float2 a[NP];
+                hchunk(v, a, false);
+                if constexpr (LN) {
+                    float2 gv[NP], bv[NP];
+                    if (p.w) {
+                        unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.w) + c), gv);
+#pragma unroll
+                        for (int j = 0; j < NP; ++j) gv[j] = Pk::add(o2, gv[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < NP; ++j) gv[j] = make_float2(1.f, 1.f);
+                    }
+                    if (p.beta) {
+                        unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.beta) + c), bv);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < NP; ++j) bv[j] = make_float2(0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) a[j] = Pk::fma(Pk::mul(Pk::add(a[j], nmu2), r2), gv[j], bv[j]);
+                } else if (p.w) {
+                    float2 wv[NP];
+                    load_w_chunk<T, TW>(p.w, c, wv);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) a[j] = Pk::mul(Pk::mul(a[j], r2), Pk::add(o2, wv[j]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) a[j] = Pk::mul(a[j], r2);
+                }
+                st_chunk(reinterpret_cast<uint4 *>(p.y) + base + cl, pack<T>(a));
+            }
+        }
+        // the warp is through stage sk; the last warp to say so refills it
+        // with row k + ns (the fences order every warp's reads of the stage
+        // before the bulk copies that overwrite it)
+        __syncwarp();
+        if (lane == 0 && k + ns < iters) {
+            __threadfence_block();
+            if (atomicAdd(&done[sk], 1u) == (unsigned)(W - 1)) {
+                __threadfence_block();
+                done[sk] = 0;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(k + ns, sk);
+            }
+        }
+        if (++s == ns) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    if (failed && p.status) *p.status = kStatusWaitTimeout;
+    // no CTA leaves while a peer may still store into its shared memory
+    if constexpr (CS > 1) cluster_sync();
+}
+
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED>
+__global__ void __launch_bounds__(TPR, 1) rmsnorm_fwd_staged(const FwdParams p) {
+    staged_fwd_body<T, TW, TPR, V, S, CS, FUSED, false>(p);
+}
+
+template <typename T, int TPR, int V, int S, int CS, bool FUSED>
+__global__ void __launch_bounds__(TPR, 1) layernorm_fwd_staged(const FwdParams p) {
+    staged_fwd_body<T, T, TPR, V, S, CS, FUSED, true>(p);
+}
+
+// Launch of a staged forward kernel: a cluster of CS CTAs (of one where a
+// CTA holds the whole row; its bulk copies name a shared::cluster
+// destination) with the stages' dynamic shared memory.
+static int launch_fwd_staged_kernel(const void *k, int cs, int threads, const FwdParams &p, int grid, int smem,
+                                    void *stream) {
+    const int e = allow_staged_smem(k);
+    if (e != 0) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {const_cast<FwdParams *>(&p)};
+    return (int)cudaLaunchKernelExC(&cfg, k, args);
+}
+
 // ------------------------------------------------------------- dispatch --
 
 template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, int Q>
@@ -600,6 +856,54 @@ static const void *ptr_t(int plan_id, bool fused) {
 #undef RMSN_FWD_PTR
     default:
         return nullptr;
+    }
+}
+
+// Staged forward plans (OP_FWD_STAGED): one entry per table row; kernels of
+// other ops are not instantiated, and a weight type other than the
+// activations' only for the default plans.
+template <typename T, typename TW, bool LN, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
+static const void *staged_fwd_ptr_entry(bool fused) {
+    if constexpr (OP != OP_FWD_STAGED || PATH != PATH_RESTAGED || !staged_plan(PATH, TEAMS, CS) ||
+                  !(std::is_same<T, TW>::value || CMIN > 0)) {
+        return nullptr;
+    } else if constexpr (LN) {
+        return fused ? (const void *)layernorm_fwd_staged<T, TPR, V, D, CS, true>
+                     : (const void *)layernorm_fwd_staged<T, TPR, V, D, CS, false>;
+    } else {
+        return fused ? (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, true>
+                     : (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, false>;
+    }
+}
+
+template <typename T, typename TW, bool LN, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
+static int staged_fwd_launch_entry(bool fused, const FwdParams &p, int grid, int smem, void *stream) {
+    const void *k = staged_fwd_ptr_entry<T, TW, LN, OP, PATH, TPR, V, TEAMS, D, CS, CMIN>(fused);
+    if (!k) return (int)cudaErrorInvalidValue;
+    return launch_fwd_staged_kernel(k, CS, TPR, p, grid, smem, stream);
+}
+
+template <typename T, typename TW, bool LN>
+static const void *staged_fwd_ptr_t(int plan_id, bool fused) {
+    switch (plan_id) {
+#define RMSN_SFWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
+    case id: return staged_fwd_ptr_entry<T, TW, LN, op, path, tpr, v, teams, depth, cs, cmin>(fused);
+        RMSNORM_PLAN_TABLE(RMSN_SFWD_PTR)
+#undef RMSN_SFWD_PTR
+    default:
+        return nullptr;
+    }
+}
+
+template <typename T, typename TW, bool LN>
+static int staged_fwd_launch_t(int plan_id, bool fused, const FwdParams &p, int grid, int smem, void *stream) {
+    switch (plan_id) {
+#define RMSN_SFWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
+    case id: return staged_fwd_launch_entry<T, TW, LN, op, path, tpr, v, teams, depth, cs, cmin>(fused, p, grid, smem, stream);
+        RMSNORM_PLAN_TABLE(RMSN_SFWD_CASE)
+#undef RMSN_SFWD_CASE
+    default:
+        return (int)cudaErrorInvalidValue;
     }
 }
 

@@ -10,4 +10,8 @@ int launch_ln_bwd_bf16(int plan_id, bool fused, const BwdParams &p, int grid, in
     return ln_bwd_launch_t<__nv_bfloat16>(plan_id, fused, p, grid, smem, stream);
 }
 const void *ln_bwd_kernel_ptr_bf16(int plan_id, bool fused) { return ln_bwd_ptr_t<__nv_bfloat16>(plan_id, fused); }
+int launch_ln_fwd_staged_bf16(int plan_id, bool fused, const FwdParams &p, int grid, int smem, void *stream) {
+    return staged_fwd_launch_t<__nv_bfloat16, __nv_bfloat16, true>(plan_id, fused, p, grid, smem, stream);
+}
+const void *ln_fwd_staged_kernel_ptr_bf16(int plan_id, bool fused) { return staged_fwd_ptr_t<__nv_bfloat16, __nv_bfloat16, true>(plan_id, fused); }
 }  // namespace rmsn

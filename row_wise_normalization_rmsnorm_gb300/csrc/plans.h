@@ -19,7 +19,10 @@ namespace rmsn {
 // OP_FWD plans serve the RMSNorm and the LayerNorm forward; OP_LN_BWD
 // plans the LayerNorm backward, whose rows carry two sums and two parameter
 // gradients (more registers per chunk than the RMSNorm backward).
-enum PlanOp { OP_FWD = 0, OP_BWD = 1, OP_LN_BWD = 2 };
+// OP_FWD_STAGED plans are forward plans that stream rows through shared
+// memory; where one covers a row it is preferred to the OP_FWD plan, except
+// for the E4M3 outputs, which stay on the register kernels.
+enum PlanOp { OP_FWD = 0, OP_BWD = 1, OP_LN_BWD = 2, OP_FWD_STAGED = 3 };
 // PATH_STAGED and PATH_RESTAGED stream rows into shared memory; the first
 // copies a row's chunks into registers for both passes, the second reads
 // them from the stage in each pass (fewer registers, the stage stays busy
@@ -68,6 +71,15 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(13, OP_FWD, PATH_VECTOR ,  256, 2,  2, 0, 1, DT_ANY,     0,     0) \
     X(14, OP_FWD, PATH_VECTOR ,   64, 8,  4, 0, 1, DT_ANY,     0,     0) \
     X(15, OP_FWD, PATH_VECTOR ,   16, 2, 16, 0, 1, DT_ANY,     0,     0) \
+    /* forward rows wider than 2048 chunks, streamed through two \
+       shared-memory stages by a persistent grid of 2- or 4-CTA clusters \
+       (two stages leave room for 2-3 CTAs an SM); E4M3 outputs keep the \
+       register plans above */ \
+    X(141, OP_FWD_STAGED, PATH_RESTAGED, 512, 3, 1, 2, 2, DT_ANY, 2049,  3072) \
+    X(139, OP_FWD_STAGED, PATH_RESTAGED, 512, 4, 1, 2, 2, DT_ANY, 3073,  4096) \
+    X(145, OP_FWD_STAGED, PATH_RESTAGED, 512, 3, 1, 2, 4, DT_ANY, 4097,  6144) \
+    X(143, OP_FWD_STAGED, PATH_RESTAGED, 512, 4, 1, 2, 4, DT_ANY, 6145,  8192) \
+    X(138, OP_FWD_STAGED, PATH_RESTAGED, 512, 4, 1, 4, 1, DT_ANY,    0,     0) \
     /* forward, any N and alignment */ \
     X(16, OP_FWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0) \
     /* backward main kernel, persistent: rows in registers (vector) or \
@@ -193,6 +205,10 @@ struct FwdParams {
     // LayerNorm: the bias (NULL: none) and the per-row mean output
     const void *beta;
     float *mean;
+    // staged forward: stages in use (0: the plan's depth) and the device
+    // status word a bounded wait that gives up writes
+    int stages = 0;
+    int *status = nullptr;
 };
 
 // Output of the forward: the activations' type, or E4M3 with a per-tensor
@@ -229,7 +245,9 @@ constexpr uint32_t kWaitLimit = 1u << 22;
     const void *fwd_kernel_ptr_##suf(int plan_id, bool fused);                                           \
     int launch_bwd_main_##suf(int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem, \
                               void *stream);                                                           \
-    const void *bwd_main_kernel_ptr_##suf(int plan_id, bool fused, bool packed);
+    const void *bwd_main_kernel_ptr_##suf(int plan_id, bool fused, bool packed);                          \
+    int launch_fwd_staged_##suf(int plan_id, bool fused, const FwdParams &p, int grid, int smem, void *stream); \
+    const void *fwd_staged_kernel_ptr_##suf(int plan_id, bool fused);
 RMSN_DECLARE_LAUNCHERS(f32)
 RMSN_DECLARE_LAUNCHERS(bf16)
 RMSN_DECLARE_LAUNCHERS(f16)
@@ -262,7 +280,9 @@ int launch_dw_finalize_f16(const float *ws, int parts, int ncols, void *out0, vo
 #define RMSN_DECLARE_LN(suf)                                                                               \
     int launch_ln_fwd_##suf(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);         \
     int launch_ln_bwd_##suf(int plan_id, bool fused, const BwdParams &p, int grid, int smem, void *stream); \
-    const void *ln_bwd_kernel_ptr_##suf(int plan_id, bool fused);
+    const void *ln_bwd_kernel_ptr_##suf(int plan_id, bool fused);                                        \
+    int launch_ln_fwd_staged_##suf(int plan_id, bool fused, const FwdParams &p, int grid, int smem, void *stream); \
+    const void *ln_fwd_staged_kernel_ptr_##suf(int plan_id, bool fused);
 RMSN_DECLARE_LN(f32)
 RMSN_DECLARE_LN(bf16)
 RMSN_DECLARE_LN(f16)

@@ -53,7 +53,7 @@ def test_plan_table_self_check(rn):
 @pytest.mark.parametrize("dt,N,tpr,v,cs", [
     (1, 128, 16, 1, 1), (1, 2048, 64, 4, 1), (1, 4096, 128, 4, 1), (1, 7168, 256, 4, 1), (1, 8192, 256, 4, 1),
     (1, 16384, 512, 4, 1), (0, 256, 32, 2, 1), (0, 2048, 128, 4, 1), (0, 6144, 512, 4, 1),
-    (0, 16384, 512, 4, 2), (1, 65536, 512, 4, 4), (0, 65536, 512, 4, 8),
+    (0, 65536, 512, 4, 8),
 ])
 def test_fwd_default_plans(rn, dt, N, tpr, v, cs):
     p = rn.plan_query(rn.OP_FWD, 4096, N, dt)
@@ -63,6 +63,22 @@ def test_fwd_default_plans(rn, dt, N, tpr, v, cs):
     per_chunk = 8 if dt == 1 else 4
     assert tpr * v * cs * per_chunk >= N
     assert p["ctas"] == 4096 // p["rows_per_cta"] * cs
+
+
+@pytest.mark.parametrize("dt,N,cs,v", [(0, 16384, 2, 4), (1, 32768, 2, 4), (1, 65536, 4, 4), (1, 20480, 2, 3),
+                                       (1, 40960, 4, 3), (0, 32768, 4, 4), (2, 24576, 2, 3)])
+def test_fwd_wide_rows_stream_through_staged_clusters(rn, dt, N, cs, v):
+    """Forward rows of 2049..8192 chunks: a persistent grid of clusters whose
+    CTAs stream equal slices through two shared-memory stages (x only, or
+    x and the residual for the fused variant); no workspace. The E4M3
+    outputs keep the register cluster plans."""
+    p = rn.plan_query(rn.OP_FWD, 16384, N, dt, num_sms=152, ctas_per_sm=3)
+    assert p["path_name"] == "staged" and p["cluster_size"] == cs and p["chunks_per_thread"] == v
+    assert p["threads_per_row"] == 512 and p["workspace_bytes"] == 0
+    assert p["ctas"] == p["ws_rows"] * cs and p["ws_rows"] == 3 * 152 // cs
+    es = 4 if dt == 0 else 2
+    slice_bytes = -(-N * es // (16 * cs)) * 16
+    assert p["smem_bytes"] == 2 * slice_bytes
 
 
 @pytest.mark.parametrize("dt,N,cs,v,stages", [(0, 16384, 2, 4, 2), (1, 32768, 2, 4, 2), (1, 65536, 4, 4, 2),
@@ -122,7 +138,9 @@ def test_staged_backward_defaults(rn):
 def test_fp32_weight_flag_plans(rn):
     """dt | RMSNORM_WEIGHT_F32 selects the activations' default plans; forced
     alternative vector plans are refused (not compiled for that pairing);
-    the flag on fp32 activations is the same as fp32."""
+    the flag on fp32 activations is the same as fp32. (The register cluster
+    plans stay table defaults, for the E4M3 outputs, so they are compiled
+    for every pairing although a plain forward streams those rows.)"""
     W = rn.RMSNORM_WEIGHT_F32
     for op in (rn.OP_FWD, rn.OP_BWD):
         for N in (128, 2048, 8192, 16384):
@@ -141,7 +159,7 @@ def test_fp32_weight_flag_plans(rn):
             p = rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16, force_plan=pid)
         except rn.RMSNormError:
             continue
-        if p["path_name"] == "vector" and pid not in defaults:
+        if p["path_name"] == "vector" and p["cluster_size"] == 1 and pid not in defaults:
             with pytest.raises(rn.RMSNormError):
                 rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16 | W, force_plan=pid)
             refused += 1

@@ -71,10 +71,10 @@ def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_p
     needed = check_dx(to_host(dx, dt), b, dt)
     check_dw(to_host(dw, wdt), b, wdt)
     if expect_path is not None:
-        # "vector": the fast paths (rows in registers; the backward may
+        # "vector": the fast paths (rows in registers; either direction may
         # instead stage rows in shared memory)
         fast = ("vector", "staged") if expect_path == "vector" else (expect_path,)
-        assert fplan["path_name"] == expect_path and bplan["path_name"] in fast, (fplan, bplan)
+        assert fplan["path_name"] in fast and bplan["path_name"] in fast, (fplan, bplan)
     # The floor is for cancellation only: it should be needed rarely on
     # ordinary rows. Very short rows cancel by construction (at N = 1,
     # dx = rstd g eps / (x^2 + eps) is the difference of two near-equal terms).
@@ -354,7 +354,9 @@ def test_fp32_weight_refuses_alternative_plans(rn):
             p = rn.plan_query(rn.OP_FWD, 64, 2048, rn.RMSNORM_BF16, force_plan=pid)
         except rn.RMSNormError:
             continue
-        if p["path_name"] == "vector" and pid not in defaults:
+        # (the register cluster plans stay table defaults, for the E4M3
+        # outputs, and so are compiled for every pairing)
+        if p["path_name"] == "vector" and p["cluster_size"] == 1 and pid not in defaults:
             alternatives.append(pid)
     assert alternatives
     for pid in alternatives:

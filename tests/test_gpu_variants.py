@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import check_dw, check_dx, cuda_bits_equal, empty_dev, to_dev, to_host
+from helpers import check_dw, check_dx, check_rstd, check_y, cuda_bits_equal, empty_dev, to_dev, to_host
 from row_wise_normalization_rmsnorm_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -423,3 +423,52 @@ def test_cluster_staged_wide_rows_match_oracle(rn, dt, M, N, plan, fused):
     check_dw(to_host(dw, dt), b, dt)
     assert rn.lib().rmsnorm_device_status(1) == 0
 
+
+
+@pytest.mark.parametrize("dt,M,N,staged,vector", [("bf16", 97, 32768, 139, 17), ("bf16", 130, 20480, 139, 17),
+                                                  ("f32", 64, 16384, 139, 17), ("bf16", 33, 65536, 143, 18),
+                                                  ("f16", 50, 40960, 143, 18), ("bf16", 200, 16384, 138, 8),
+                                                  ("f32", 77, 6144, 138, 8), ("bf16", 70, 64, 139, 17)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_staged_forward_matches_register_forward_bitwise(rn, dt, M, N, staged, vector, fused):
+    """The staged forward (rows streamed through shared-memory stages by a
+    persistent grid of CTAs or clusters) takes each thread's chunks in the
+    register forward's order and reduces them in its tree: y, rstd and the
+    fused residual_out are the same bits for the same geometry."""
+    d, t = dev_inputs(M, N, dt, 380 + N % 7, residual=fused)
+    res = t.get("residual")
+    a_y, a_h, a_r, ap = rn.rmsnorm_fwd_ex(t["x"], t["w"], residual=res,
+                                          residual_out=torch.empty_like(t["x"]) if fused else None, force_plan=staged)
+    b_y, b_h, b_r, bp = rn.rmsnorm_fwd_ex(t["x"], t["w"], residual=res,
+                                          residual_out=torch.empty_like(t["x"]) if fused else None, force_plan=vector)
+    torch.cuda.synchronize()
+    assert ap["plan_id"] == staged and ap["path_name"] == "staged" and bp["path_name"] == "vector"
+    assert cuda_bits_equal(a_y, b_y) and cuda_bits_equal(a_r, b_r)
+    if fused:
+        assert cuda_bits_equal(a_h, b_h)
+    assert rn.lib().rmsnorm_device_status(1) == 0
+
+
+@pytest.mark.parametrize("dt,M,N,plan", [("bf16", 211, 20488, 141), ("f32", 67, 12280, 141), ("bf16", 45, 40968, 145),
+                                         ("bf16", 19, 65536, 143), ("f16", 5, 24, 145), ("bf16", 301, 8192, 138)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_staged_forward_matches_oracle(rn, dt, M, N, plan, fused):
+    d, t = dev_inputs(M, N, dt, 390 + N % 5, residual=fused)
+    y, h, r, p = rn.rmsnorm_fwd_ex(t["x"], t["w"], residual=t.get("residual"),
+                                   residual_out=torch.empty_like(t["x"]) if fused else None, force_plan=plan)
+    f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0, residual=d.get("residual") if fused else None)
+    torch.cuda.synchronize()
+    assert p["plan_id"] == plan and p["ctas"] == p["ws_rows"] * p["cluster_size"] and p["workspace_bytes"] == 0
+    check_y(to_host(y, dt), f, dt)
+    check_rstd(r.cpu().numpy(), f["rstd64"])
+    if fused:
+        assert np.array_equal(to_host(h, dt), f["h"])
+    assert rn.lib().rmsnorm_device_status(1) == 0
+
+
+def test_e4m3_forward_refuses_staged_plans_and_wide_rows_stay_in_registers(rn):
+    _, t = dev_inputs(64, 32768, "bf16", 395)
+    with pytest.raises(rn.RMSNormError):
+        rn.rmsnorm_fwd_fp8(t["x"], t["w"], scaling="row", force_plan=139)
+    q = rn.rmsnorm_fwd_fp8(t["x"], t["w"], scaling="row")
+    assert q["plan"]["path_name"] == "vector" and q["plan"]["cluster_size"] == 2
