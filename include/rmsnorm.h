@@ -281,7 +281,8 @@ typedef enum {
     RMSNORM_PATH_VECTOR = 0,   /* 128-bit loads, row held in registers       */
     RMSNORM_PATH_STAGED = 1,   /* row staged in shared memory by bulk copies */
                                /* (held in registers or re-read, by plan)    */
-    RMSNORM_PATH_GENERIC = 2   /* any N and alignment, element loads         */
+    RMSNORM_PATH_GENERIC = 2   /* any N and alignment: element head and tail */
+                               /* around 16-byte chunks                      */
 } rmsnorm_path_t;
 
 typedef struct {
@@ -293,10 +294,13 @@ typedef struct {
     int32_t cta_threads;
     int32_t packed;             /* 1: packed f32x2 arithmetic                   */
     int32_t ctas;               /* grid size in CTAs                            */
-    int32_t ctas_per_sm;        /* backward: resident CTAs per SM used for `ctas` */
+    int32_t ctas_per_sm;        /* backward: resident CTAs per SM used for `ctas`
+                                   (0 where the library queried the device)     */
     int32_t smem_bytes;         /* dynamic shared memory per CTA                */
     int32_t cluster_size;       /* CTAs of a thread-block cluster sharing a row (1: none) */
-    int32_t ws_rows;            /* backward: dW partial rows (CTAs, or clusters) */
+    int32_t ws_rows;            /* persistent grids (the backward and a staged
+                                   forward): units walking the rows, CTAs or
+                                   clusters; backward: dW partial rows          */
     int64_t workspace_bytes;    /* backward only                                */
 } rmsnorm_plan_t;
 

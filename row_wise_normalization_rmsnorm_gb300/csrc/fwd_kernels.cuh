@@ -11,10 +11,16 @@
 // the warps per row chosen by N as in the tuned per-hidden-size kernels of
 // ROCm/TransformerEngine PR #583 (Description).
 //
-// Generic kernel: one 256-thread CTA per row, element loads, the row read
-// twice (the second read hits L1/L2). Serves any N and any element-aligned
-// pointers (Liger-Kernel PR #1388, "Behavior when the fast path does not
-// apply": irregular or unaligned shapes take scalar paths).
+// Rows wider than 2048 chunks are shared by a thread-block cluster: the
+// register kernel holds each CTA's slice (the E4M3 outputs and rows above
+// 8192 chunks), the staged kernel streams the slices through shared-memory
+// stages on a persistent grid of clusters (every other forward of such rows).
+//
+// Generic kernel: one 256-thread CTA per row, the row read twice (the
+// second read hits L1/L2), split into an element-wise head, 16-byte chunks
+// and an element-wise tail. Serves any N and any element-aligned pointers
+// (Liger-Kernel PR #1388, "Behavior when the fast path does not apply":
+// irregular or unaligned shapes take scalar paths).
 #pragma once
 
 #include "common.cuh"
