@@ -472,3 +472,43 @@ def test_e4m3_forward_refuses_staged_plans_and_wide_rows_stay_in_registers(rn):
         rn.rmsnorm_fwd_fp8(t["x"], t["w"], scaling="row", force_plan=139)
     q = rn.rmsnorm_fwd_fp8(t["x"], t["w"], scaling="row")
     assert q["plan"]["path_name"] == "vector" and q["plan"]["cluster_size"] == 2
+
+
+@pytest.mark.parametrize("N", [20480, 65536])
+def test_graph_replay_wide_rows_matches_direct(rn, N):
+    """The staged cluster kernels (forward and backward, RMSNorm and
+    LayerNorm, plain and fused) capture into a CUDA graph and replay to the
+    direct calls' bits."""
+    M = 64
+    d, t = dev_inputs(M, N, "bf16", 420 + N % 7, residual=True, dres=True, beta=True)
+    ws = torch.empty(rn.rmsnorm_bwd_workspace_bytes(M, N, torch.bfloat16), dtype=torch.uint8, device="cuda")
+    lws = torch.empty(rn.layernorm_bwd_workspace_bytes(M, N, torch.bfloat16), dtype=torch.uint8, device="cuda")
+
+    def run(out):
+        y, h, r = rn.rmsnorm_add_fwd(t["x"], t["residual"], t["w"], y=out[0], residual_out=out[1], rstd=out[2])
+        rn.rmsnorm_add_bwd(t["dy"], t["dres"], h, t["w"], r, dx=out[3], dw=out[4], workspace=ws)
+        o = rn.layernorm_fwd(t["x"], t["w"], t["beta"], y=out[5], mean=out[6], rstd=out[7])
+        rn.layernorm_bwd(t["dy"], t["x"], t["w"], o["mean"], o["rstd"], dx=out[8], dgamma=out[9], dbeta=out[10],
+                         workspace=lws)
+
+    def fresh():
+        return [torch.empty_like(t["x"]), torch.empty_like(t["x"]), torch.empty(M, device="cuda"),
+                torch.empty_like(t["x"]), torch.empty_like(t["w"]), torch.empty_like(t["x"]), torch.empty(M, device="cuda"),
+                torch.empty(M, device="cuda"), torch.empty_like(t["x"]), torch.empty_like(t["w"]), torch.empty_like(t["w"])]
+    ref = fresh()
+    run(ref)
+    out = fresh()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            run(out)
+    for a in out:
+        a.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(out, ref):
+        assert cuda_bits_equal(a, b)
+    assert rn.plan_query(rn.OP_FWD, M, N, rn.RMSNORM_BF16)["path_name"] == "staged"
+    assert rn.lib().rmsnorm_device_status(1) == 0
