@@ -372,3 +372,29 @@ def test_ln_staged_forward_matches_oracle(rn, dt, M, N, plan, fused):
     if fused:
         assert np.array_equal(to_host(out["residual_out"], dt), f["h"])
     assert rn.lib().rmsnorm_device_status(1) == 0
+
+
+@pytest.mark.parametrize("dt,N", [("bf16", 8192), ("bf16", 16384), ("bf16", 32768), ("f32", 12288), ("bf16", 7169)])
+def test_ln_in_place_aliasing(rn, dt, N):
+    """y may be x, residual_out may be residual, dx may be dy (and
+    dresidual_out): the in-place calls give the out-of-place bits on every
+    path (register, staged, cluster staged, generic)."""
+    M = 300
+    d = inputs.make_inputs(M, N, dt, 430 + N % 11, beta=True, residual=True, dres=True)
+    x, g, b, r, dy, dr = (to_dev(d[k], dt) for k in ("x", "w", "beta", "residual", "dy", "dres"))
+    o = rn.layernorm_fwd(x, g, b)
+    xa = x.clone()
+    rn.layernorm_fwd(xa, g, b, y=xa)
+    of = rn.layernorm_fwd(x, g, b, residual=r, residual_out=torch.empty_like(x))
+    ra = r.clone()
+    rn.layernorm_fwd(x, g, b, residual=ra, residual_out=ra)
+    bo = rn.layernorm_bwd(dy, x, g, o["mean"], o["rstd"])
+    dya = dy.clone()
+    rn.layernorm_bwd(dya, x, g, o["mean"], o["rstd"], dx=dya)
+    bf = rn.layernorm_bwd(dy, x, g, o["mean"], o["rstd"], dresidual_out=dr)
+    dra = dr.clone()
+    rn.layernorm_bwd(dy, x, g, o["mean"], o["rstd"], dresidual_out=dra, dx=dra)
+    torch.cuda.synchronize()
+    assert cuda_bits_equal(xa, o["y"]) and cuda_bits_equal(ra, of["residual_out"])
+    assert cuda_bits_equal(dya, bo["dx"]) and cuda_bits_equal(dra, bf["dx"])
+

@@ -157,7 +157,8 @@ def test_fused_backward_null_dres_equals_zero_buffer(rn):
     assert cuda_bits_equal(dx1, dx3) and cuda_bits_equal(dw1, dw3)
 
 
-@pytest.mark.parametrize("dt,N", [("bf16", 8192), ("f32", 257), ("bf16", 64)])
+@pytest.mark.parametrize("dt,N", [("bf16", 8192), ("f32", 257), ("bf16", 64), ("bf16", 16384), ("f32", 12288),
+                                  ("bf16", 32768), ("bf16", 7169)])
 def test_in_place_aliasing(rn, dt, N):
     M = 640
     _, t = dev_inputs(M, N, dt, 98, residual=True, dres=True)
