@@ -542,7 +542,13 @@ def main():
             "frac": comp[dom]["gbs"] / peak, "traffic": ncu_traffic(dom), "peak_source": peak_kind,
             "bytes_per_launch": comp[dom]["bytes"]}
 
-    # end to end: pinned host buffers, copies inside the timed region
+    # end to end: pinned host buffers, copies inside the timed region. Steps
+    # are independent batches, so they are pipelined over two sets of device
+    # buffers: step k+1's host-to-device copies (one stream) and step k-1's
+    # device-to-host copies (another) run while step k computes; events
+    # order each buffer's reuse, and the timed region brackets every copy.
+    # (Splitting a direction's copies over more streams measured no faster:
+    # the host link is the limit, about 165 GB/s each way with both busy.)
     h_x = torch.empty_like(x, device="cpu").pin_memory()
     h_dy = torch.empty_like(dy, device="cpu").pin_memory()
     h_w = torch.empty_like(w, device="cpu").pin_memory()
@@ -553,28 +559,48 @@ def main():
     o_dx = torch.empty_like(dx, device="cpu").pin_memory()
     o_dw = torch.empty_like(dw, device="cpu").pin_memory()
     o_r = torch.empty_like(rstd, device="cpu").pin_memory()
-    d_x, d_dy, d_w = torch.empty_like(x), torch.empty_like(dy), torch.empty_like(w)
+    bufs = [dict(x=torch.empty_like(x), dy=torch.empty_like(dy), w=torch.empty_like(w), y=torch.empty_like(y),
+                 r=torch.empty_like(rstd), dx=torch.empty_like(dx), dw=torch.empty_like(dw),
+                 ws=torch.empty_like(ws), loaded=torch.cuda.Event(), computed=torch.cuda.Event(),
+                 drained=torch.cuda.Event()) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    for bf in bufs:  # every buffer starts free
+        bf["computed"].record(stream)
+        bf["drained"].record(stream)
 
-    def e2e_step():
-        d_x.copy_(h_x, non_blocking=True)
-        d_dy.copy_(h_dy, non_blocking=True)
-        d_w.copy_(h_w, non_blocking=True)
-        rn.rmsnorm_fwd(d_x, d_w, y=y, rstd=rstd, eps=eps)
-        rn.rmsnorm_bwd(d_dy, d_x, d_w, rstd, dx=dx, dw=dw, workspace=ws, eps=eps)
-        o_y.copy_(y, non_blocking=True)
-        o_r.copy_(rstd, non_blocking=True)
-        o_dx.copy_(dx, non_blocking=True)
-        o_dw.copy_(dw, non_blocking=True)
+    def e2e_step(k):
+        bf = bufs[k % 2]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(bf["computed"])   # the last kernels that read this buffer's inputs
+            bf["x"].copy_(h_x, non_blocking=True)
+            bf["dy"].copy_(h_dy, non_blocking=True)
+            bf["w"].copy_(h_w, non_blocking=True)
+            bf["loaded"].record(s_in)
+        stream.wait_event(bf["loaded"])
+        stream.wait_event(bf["drained"])      # the last copies out of this buffer's outputs
+        rn.rmsnorm_fwd(bf["x"], bf["w"], y=bf["y"], rstd=bf["r"], eps=eps)
+        rn.rmsnorm_bwd(bf["dy"], bf["x"], bf["w"], bf["r"], dx=bf["dx"], dw=bf["dw"], workspace=bf["ws"], eps=eps)
+        bf["computed"].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(bf["computed"])
+            o_y.copy_(bf["y"], non_blocking=True)
+            o_r.copy_(bf["r"], non_blocking=True)
+            o_dx.copy_(bf["dx"], non_blocking=True)
+            o_dw.copy_(bf["dw"], non_blocking=True)
+            bf["drained"].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    for k in range(3):
+        e2e_step(k)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    s_in.wait_event(e0)
+    for k in range(args.e2e_steps):
+        e2e_step(k)
+    stream.wait_stream(s_out)
+    stream.wait_stream(s_in)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dist if world > 1 else None, dev)
