@@ -283,6 +283,7 @@ def sweep_points():
     pts.append(("fp8row bf16 16384x8192", "bf16", 16384, 8192, False, False))
     pts.append(("fp8tensor bf16 16384x8192", "bf16", 16384, 8192, False, False))
     pts.append(("fp8row bf16 4096x4096", "bf16", 4096, 4096, False, False))
+    pts.append(("fp8row bf16 8192x32768", "bf16", 8192, 32768, False, False))
     # LayerNorm (gamma and beta, dgamma and dbeta)
     for dt, M, N in (("bf16", 16384, 8192), ("bf16", 4096, 4096), ("bf16", 16384, 2048), ("f32", 16384, 4096),
                      ("bf16", 4096, 16384), ("bf16", 16384, 16384), ("bf16", 8192, 12288)):

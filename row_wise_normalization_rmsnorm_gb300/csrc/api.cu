@@ -138,8 +138,7 @@ static int64_t plan_capacity(const PlanDesc &d) { return (int64_t)d.tpr * d.v * 
 // backward dW partial rows: resident CTAs (or, for cluster plans, resident
 // clusters) on the device; ctas_per_sm is reported only.
 static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool aligned, int64_t max_parts,
-                                    int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out,
-                                    bool regs_only = false) {
+                                    int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
     if (!out) return RMSNORM_ERR_INVALID_ARG;
     if (op != RMSNORM_OP_FWD && op != RMSNORM_OP_BWD && op != RMSNORM_OP_LN_BWD) return RMSNORM_ERR_INVALID_ARG;
     if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
@@ -152,8 +151,8 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     const PlanDesc *d = nullptr;
     if (force_plan >= 0) {
         d = find_plan(force_plan);
-        // a forward may take a staged forward plan (not for the E4M3 outputs)
-        const bool staged_fwd = d && op == RMSNORM_OP_FWD && d->op == OP_FWD_STAGED && !regs_only;
+        // a forward may take a staged forward plan
+        const bool staged_fwd = d && op == RMSNORM_OP_FWD && d->op == OP_FWD_STAGED;
         if (!d || (d->op != op && !staged_fwd)) return RMSNORM_ERR_UNSUPPORTED;
         if (d->path == PATH_VECTOR && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
         // staged plans: aligned rows that fit
@@ -163,7 +162,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     } else {
         d = vec_ok ? default_vector_plan(op, dt, C) : nullptr;
         // a staged forward plan that covers the row is preferred
-        if (op == RMSNORM_OP_FWD && vec_ok && !regs_only) {
+        if (op == RMSNORM_OP_FWD && vec_ok) {
             const PlanDesc *sd = default_vector_plan(OP_FWD_STAGED, dt, C);
             if (sd) d = sd;
         }
@@ -326,6 +325,14 @@ static const void *fwd_staged_kernel(int plan_id, int dt, bool fused, bool ln) {
     }
 }
 
+static const void *fwd8_staged_kernel(int plan_id, int dt, bool fused, int mode) {
+    switch (base_dtype(dt)) {
+    case RMSNORM_BF16: return fwd8_staged_kernel_ptr_bf16(plan_id, fused, mode);
+    case RMSNORM_F16: return fwd8_staged_kernel_ptr_f16(plan_id, fused, mode);
+    default: return fwd8_staged_kernel_ptr_f32(plan_id, fused, mode);
+    }
+}
+
 static int launch_fwd_staged_dt(int dt, bool ln, int plan_id, bool fused, const FwdParams &p, int grid, int smem,
                                 void *stream) {
     if (ln) {
@@ -461,11 +468,12 @@ static bool finite_scalar(float v) { return std::isfinite(v); }
 // Resident units (CTAs, or clusters) of a staged forward plan on the
 // device, taken at the plan's largest rows (the conservative value) and
 // cached per device, type, fusion mode and RMSNorm/LayerNorm.
-static int g_sfwd_parts[kMaxDevices][kNumKinds][2][2][kMaxPlanId];
+static int g_sfwd_parts[kMaxDevices][kNumKinds][2][2][3][kMaxPlanId];
 
-static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d, bool fused, bool ln, int *parts_out) {
-    if (d.id < 0 || d.id >= kMaxPlanId) return cudaErrorInvalidValue;
-    int &slot = g_sfwd_parts[dev][kind_of(dt)][fused ? 1 : 0][ln ? 1 : 0][d.id];
+static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d, bool fused, bool ln, int qmode,
+                                    int *parts_out) {
+    if (d.id < 0 || d.id >= kMaxPlanId || qmode < 0 || qmode > 2) return cudaErrorInvalidValue;
+    int &slot = g_sfwd_parts[dev][kind_of(dt)][fused ? 1 : 0][ln ? 1 : 0][qmode][d.id];
     {
         std::lock_guard<std::mutex> lk(g_occ_mutex);
         if (slot > 0) {
@@ -473,7 +481,7 @@ static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d,
             return cudaSuccess;
         }
     }
-    const void *k = fwd_staged_kernel(d.id, dt, fused, ln);
+    const void *k = qmode != QOUT_NONE ? fwd8_staged_kernel(d.id, dt, fused, qmode) : fwd_staged_kernel(d.id, dt, fused, ln);
     if (!k) return cudaErrorInvalidDeviceFunction;
     cudaError_t e = (cudaError_t)allow_staged_smem(k);
     if (e != cudaSuccess) return e;
@@ -509,7 +517,8 @@ static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d,
 // the rows, and the stages in use, the shared memory and the status word
 // are set. Other plans are left as they are.
 static rmsnorm_status_t prepare_staged_fwd(int64_t M, int64_t N, int dt, bool aligned, bool fused, bool ln,
-                                           int force_plan, rmsnorm_plan_t *plan, int *stages, int **status) {
+                                           int qmode, int force_plan, rmsnorm_plan_t *plan, int *stages,
+                                           int **status) {
     *stages = 0;
     *status = nullptr;
     const PlanDesc *d = find_plan(plan->plan_id);
@@ -521,7 +530,7 @@ static rmsnorm_status_t prepare_staged_fwd(int64_t M, int64_t N, int dt, bool al
     cudaError_t e = device_sms(&dev, &sms);
     if (e != cudaSuccess) return cuda_fail(e);
     int parts = 1;
-    e = staged_fwd_parts(dev, sms, dt, *d, fused, ln, &parts);
+    e = staged_fwd_parts(dev, sms, dt, *d, fused, ln, qmode, &parts);
     if (e != cudaSuccess) return cuda_fail(e);
     rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, parts, 0, force_plan, 0, plan);
     if (st != RMSNORM_SUCCESS) return st;
@@ -657,15 +666,14 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (fused) aligned = aligned && aligned_to(residual, 16) && aligned_to(residual_out, 16);
 
     rmsnorm_plan_t plan;
-    // the E4M3 outputs stay on the register kernels
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, 1, 0, force_plan, 0, &plan, quant);
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, 1, 0, force_plan, 0, &plan);
     if (st != RMSNORM_SUCCESS) return st;
     // the E4M3 kernels are compiled for the default plans and the generic one
-    if (quant && force_plan >= 0 && plan.path == PATH_VECTOR && find_plan(plan.plan_id)->cmin == 0)
+    if (quant && force_plan >= 0 && plan.path != PATH_GENERIC && find_plan(plan.plan_id)->cmin == 0)
         return RMSNORM_ERR_UNSUPPORTED;
     int stages = 0;
     int *status = nullptr;
-    st = prepare_staged_fwd(M, N, dt, aligned, fused, false, force_plan, &plan, &stages, &status);
+    st = prepare_staged_fwd(M, N, dt, aligned, fused, false, q.qmode, force_plan, &plan, &stages, &status);
     if (st != RMSNORM_SUCCESS) return st;
 
     FwdParams p;
@@ -690,10 +698,20 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (quant) {
         cudaError_t e = clear_amax();
         if (e != cudaSuccess) return cuda_fail(e);
+        const int sm = plan.smem_bytes;
         switch (base_dtype(dt)) {
-        case RMSNORM_BF16: le = launch_fwd8_bf16(plan.plan_id, fused, q.qmode, p, plan.ctas, stream); break;
-        case RMSNORM_F16: le = launch_fwd8_f16(plan.plan_id, fused, q.qmode, p, plan.ctas, stream); break;
-        default: le = launch_fwd8_f32(plan.plan_id, fused, q.qmode, p, plan.ctas, stream); break;
+        case RMSNORM_BF16:
+            le = stages > 0 ? launch_fwd8_staged_bf16(plan.plan_id, fused, q.qmode, p, plan.ctas, sm, stream)
+                            : launch_fwd8_bf16(plan.plan_id, fused, q.qmode, p, plan.ctas, stream);
+            break;
+        case RMSNORM_F16:
+            le = stages > 0 ? launch_fwd8_staged_f16(plan.plan_id, fused, q.qmode, p, plan.ctas, sm, stream)
+                            : launch_fwd8_f16(plan.plan_id, fused, q.qmode, p, plan.ctas, stream);
+            break;
+        default:
+            le = stages > 0 ? launch_fwd8_staged_f32(plan.plan_id, fused, q.qmode, p, plan.ctas, sm, stream)
+                            : launch_fwd8_f32(plan.plan_id, fused, q.qmode, p, plan.ctas, stream);
+            break;
         }
     } else if (stages > 0) {
         le = launch_fwd_staged_dt(dt, false, plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream);
@@ -873,7 +891,7 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
     if (plan.path == PATH_VECTOR && find_plan(plan.plan_id)->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
     int stages = 0;
     int *status = nullptr;
-    st = prepare_staged_fwd(M, N, dt, aligned, fused, true, force_plan, &plan, &stages, &status);
+    st = prepare_staged_fwd(M, N, dt, aligned, fused, true, QOUT_NONE, force_plan, &plan, &stages, &status);
     if (st != RMSNORM_SUCCESS) return st;
 
     FwdParams p;

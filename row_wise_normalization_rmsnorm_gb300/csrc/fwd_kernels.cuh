@@ -523,8 +523,9 @@ __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) 
 // reduction tree are the register forward's, so y and rstd are the same
 // bits. Every wait is bounded; one that gives up writes the status word and
 // the kernel carries on.
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool LN>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool LN, int Q = QOUT_NONE>
 __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
+    static_assert(Q == QOUT_NONE || !LN, "E4M3 output: RMSNorm only");
     using Pk = Pair<true>;
     constexpr int E = Elem<T>::E;
     constexpr int NP = Elem<T>::NP;
@@ -588,9 +589,11 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     // after reading; a buffer is written again (q + 2) only after every warp
     // sent its q + 1 sum, which it does after reading the buffer for q.
     uint32_t q = 0;
-    auto rowsum = [&](float v) {
+    // combines with Op (OpAdd: a row sum; OpMax: the E4M3 row max)
+    auto rowred = [&](auto op, float v) {
+        using Op = decltype(op);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        for (int o = 16; o > 0; o >>= 1) v = Op::f(v, __shfl_xor_sync(0xffffffffu, v, o));
         const int b = (int)(q & 1);
         float sum;
         if constexpr (CS > 1) {
@@ -599,16 +602,17 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                 for (int c = 0; c < CS; ++c) st_async_cluster(&red[b][rank * W + (t >> 5)], &rbar[b], (uint32_t)c, v);
             }
             if (!mbar_wait(&rbar[b], (q >> 1) & 1u, kWaitLimit)) failed = true;
-            sum = sum_slots<CS * W>(&red[b][0], lane);
+            sum = sum_slots<CS * W, Op>(&red[b][0], lane);
             if (t == 0) mbar_arrive_expect_tx(&rbar[b], kSlotBytes);
         } else {
             if (lane == 0) red[b][t >> 5] = v;
             __syncthreads();
-            sum = sum_slots<W>(&red[b][0], lane);
+            sum = sum_slots<W, Op>(&red[b][0], lane);
         }
         ++q;
         return sum;
     };
+    auto rowsum = [&](float v) { return rowred(OpAdd{}, v); };
 
     const float2 o2 = make_float2(p.offset, p.offset);
     int s = 0;
@@ -673,41 +677,89 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
         }
         const float2 r2 = make_float2(rstd, rstd);
         const float2 nmu2 = make_float2(-mu, -mu);
+        // y of chunk v of the slice (RMSNorm: x rstd (offset + w))
+        auto ychunk = [&](int v, float2 (&a)[NP]) {
+            const int c = cbase + v * TPR + t;
+            hchunk(v, a, false);
+            if constexpr (LN) {
+                float2 gv[NP], bv[NP];
+                if (p.w) {
+                    unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.w) + c), gv);
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
-            const int cl = v * TPR + t;
-            if (cl < Cs) {
-                const int c = cbase + cl;
-                float2 a[NP];
-                hchunk(v, a, false);
-                if constexpr (LN) {
-                    float2 gv[NP], bv[NP];
-                    if (p.w) {
-                        unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.w) + c), gv);
-#pragma unroll
-                        for (int j = 0; j < NP; ++j) gv[j] = Pk::add(o2, gv[j]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < NP; ++j) gv[j] = make_float2(1.f, 1.f);
-                    }
-                    if (p.beta) {
-                        unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.beta) + c), bv);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < NP; ++j) bv[j] = make_float2(0.f, 0.f);
-                    }
-#pragma unroll
-                    for (int j = 0; j < NP; ++j) a[j] = Pk::fma(Pk::mul(Pk::add(a[j], nmu2), r2), gv[j], bv[j]);
-                } else if (p.w) {
-                    float2 wv[NP];
-                    load_w_chunk<T, TW>(p.w, c, wv);
-#pragma unroll
-                    for (int j = 0; j < NP; ++j) a[j] = Pk::mul(Pk::mul(a[j], r2), Pk::add(o2, wv[j]));
+                    for (int j = 0; j < NP; ++j) gv[j] = Pk::add(o2, gv[j]);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < NP; ++j) a[j] = Pk::mul(a[j], r2);
+                    for (int j = 0; j < NP; ++j) gv[j] = make_float2(1.f, 1.f);
                 }
-                st_chunk(reinterpret_cast<uint4 *>(p.y) + base + cl, pack<T>(a));
+                if (p.beta) {
+                    unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.beta) + c), bv);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) bv[j] = make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < NP; ++j) a[j] = Pk::fma(Pk::mul(Pk::add(a[j], nmu2), r2), gv[j], bv[j]);
+            } else if (p.w) {
+                float2 wv[NP];
+                load_w_chunk<T, TW>(p.w, c, wv);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) a[j] = Pk::mul(Pk::mul(a[j], r2), Pk::add(o2, wv[j]));
+            } else {
+#pragma unroll
+                for (int j = 0; j < NP; ++j) a[j] = Pk::mul(a[j], r2);
+            }
+        };
+        if constexpr (Q == QOUT_NONE) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const int cl = v * TPR + t;
+                if (cl < Cs) {
+                    float2 a[NP];
+                    ychunk(v, a);
+                    st_chunk(reinterpret_cast<uint4 *>(p.y) + base + cl, pack<T>(a));
+                }
+            }
+        } else {
+            // E4M3: the row's max |y| (per-row scale, or the reported amax)
+            // from one pass over the stage, then the codes from another
+            float amax = 0.f;
+            if (Q == QOUT_FP8_ROW || p.qamax != nullptr) {  // uniform over the grid
+                float m = 0.f;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    if (v * TPR + t < Cs) {
+                        float2 a[NP];
+                        ychunk(v, a);
+#pragma unroll
+                        for (int j = 0; j < NP; ++j) m = fmaxf(m, fmaxf(fabsf(a[j].x), fabsf(a[j].y)));
+                    }
+                }
+                amax = rowred(OpMax{}, m);
+            }
+            float sc;
+            if constexpr (Q == QOUT_FP8_ROW) {
+                sc = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+                if (t == 0 && rank == 0) p.qscale_inv[row] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+            } else {
+                sc = __ldg(p.qscale);
+                if (row == 0 && t == 0 && rank == 0 && p.qscale_inv) p.qscale_inv[0] = __fdiv_rn(1.f, sc);
+            }
+            if (p.qamax != nullptr && t == 0 && rank == 0) atomicMax(p.qamax, __float_as_uint(amax));
+            const float2 s2 = make_float2(sc, sc);
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const int cl = v * TPR + t;
+                if (cl < Cs) {
+                    float2 a[NP];
+                    ychunk(v, a);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) a[j] = Pk::mul(a[j], s2);
+                    if constexpr (NP == 4) {
+                        __stcs(reinterpret_cast<uint2 *>(p.y) + base + cl, make_uint2(e4m3x4(a[0], a[1]), e4m3x4(a[2], a[3])));
+                    } else {
+                        __stcs(reinterpret_cast<unsigned int *>(p.y) + base + cl, e4m3x4(a[0], a[1]));
+                    }
+                }
             }
         }
         // the warp is through stage sk; the last warp to say so refills it
@@ -733,9 +785,9 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     if constexpr (CS > 1) cluster_sync();
 }
 
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, int Q = QOUT_NONE>
 __global__ void __launch_bounds__(TPR, 1) rmsnorm_fwd_staged(const FwdParams p) {
-    staged_fwd_body<T, TW, TPR, V, S, CS, FUSED, false>(p);
+    staged_fwd_body<T, TW, TPR, V, S, CS, FUSED, false, Q>(p);
 }
 
 template <typename T, int TPR, int V, int S, int CS, bool FUSED>
@@ -868,32 +920,34 @@ static const void *ptr_t(int plan_id, bool fused) {
 // Staged forward plans (OP_FWD_STAGED): one entry per table row; kernels of
 // other ops are not instantiated, and a weight type other than the
 // activations' only for the default plans.
-template <typename T, typename TW, bool LN, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
+template <typename T, typename TW, bool LN, int Q, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS,
+          int CMIN>
 static const void *staged_fwd_ptr_entry(bool fused) {
     if constexpr (OP != OP_FWD_STAGED || PATH != PATH_RESTAGED || !staged_plan(PATH, TEAMS, CS) ||
-                  !(std::is_same<T, TW>::value || CMIN > 0)) {
+                  !instantiated<T, TW, PATH, CMIN, Q>() || (LN && Q != QOUT_NONE)) {
         return nullptr;
     } else if constexpr (LN) {
         return fused ? (const void *)layernorm_fwd_staged<T, TPR, V, D, CS, true>
                      : (const void *)layernorm_fwd_staged<T, TPR, V, D, CS, false>;
     } else {
-        return fused ? (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, true>
-                     : (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, false>;
+        return fused ? (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, true, Q>
+                     : (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, false, Q>;
     }
 }
 
-template <typename T, typename TW, bool LN, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
+template <typename T, typename TW, bool LN, int Q, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS,
+          int CMIN>
 static int staged_fwd_launch_entry(bool fused, const FwdParams &p, int grid, int smem, void *stream) {
-    const void *k = staged_fwd_ptr_entry<T, TW, LN, OP, PATH, TPR, V, TEAMS, D, CS, CMIN>(fused);
+    const void *k = staged_fwd_ptr_entry<T, TW, LN, Q, OP, PATH, TPR, V, TEAMS, D, CS, CMIN>(fused);
     if (!k) return (int)cudaErrorInvalidValue;
     return launch_fwd_staged_kernel(k, CS, TPR, p, grid, smem, stream);
 }
 
-template <typename T, typename TW, bool LN>
+template <typename T, typename TW, bool LN, int Q = QOUT_NONE>
 static const void *staged_fwd_ptr_t(int plan_id, bool fused) {
     switch (plan_id) {
 #define RMSN_SFWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return staged_fwd_ptr_entry<T, TW, LN, op, path, tpr, v, teams, depth, cs, cmin>(fused);
+    case id: return staged_fwd_ptr_entry<T, TW, LN, Q, op, path, tpr, v, teams, depth, cs, cmin>(fused);
         RMSNORM_PLAN_TABLE(RMSN_SFWD_PTR)
 #undef RMSN_SFWD_PTR
     default:
@@ -901,16 +955,32 @@ static const void *staged_fwd_ptr_t(int plan_id, bool fused) {
     }
 }
 
-template <typename T, typename TW, bool LN>
+template <typename T, typename TW, bool LN, int Q = QOUT_NONE>
 static int staged_fwd_launch_t(int plan_id, bool fused, const FwdParams &p, int grid, int smem, void *stream) {
     switch (plan_id) {
 #define RMSN_SFWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return staged_fwd_launch_entry<T, TW, LN, op, path, tpr, v, teams, depth, cs, cmin>(fused, p, grid, smem, stream);
+    case id:                                                                    \
+        return staged_fwd_launch_entry<T, TW, LN, Q, op, path, tpr, v, teams, depth, cs, cmin>(fused, p, grid, smem, \
+                                                                                            stream);
         RMSNORM_PLAN_TABLE(RMSN_SFWD_CASE)
 #undef RMSN_SFWD_CASE
     default:
         return (int)cudaErrorInvalidValue;
     }
+}
+
+// E4M3 output of the staged forward: the mode picks the instantiation.
+template <typename T>
+static int staged_launch_q(int plan_id, bool fused, int mode, const FwdParams &p, int grid, int smem, void *stream) {
+    if (mode == QOUT_FP8_TENSOR) return staged_fwd_launch_t<T, T, false, QOUT_FP8_TENSOR>(plan_id, fused, p, grid, smem, stream);
+    if (mode == QOUT_FP8_ROW) return staged_fwd_launch_t<T, T, false, QOUT_FP8_ROW>(plan_id, fused, p, grid, smem, stream);
+    return (int)cudaErrorInvalidValue;
+}
+template <typename T>
+static const void *staged_ptr_q(int plan_id, bool fused, int mode) {
+    if (mode == QOUT_FP8_TENSOR) return staged_fwd_ptr_t<T, T, false, QOUT_FP8_TENSOR>(plan_id, fused);
+    if (mode == QOUT_FP8_ROW) return staged_fwd_ptr_t<T, T, false, QOUT_FP8_ROW>(plan_id, fused);
+    return nullptr;
 }
 
 // E4M3 output: the mode picks the instantiation.

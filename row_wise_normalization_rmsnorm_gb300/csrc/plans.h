@@ -20,8 +20,7 @@ namespace rmsn {
 // plans the LayerNorm backward, whose rows carry two sums and two parameter
 // gradients (more registers per chunk than the RMSNorm backward).
 // OP_FWD_STAGED plans are forward plans that stream rows through shared
-// memory; where one covers a row it is preferred to the OP_FWD plan, except
-// for the E4M3 outputs, which stay on the register kernels.
+// memory; where one covers a row it is preferred to the OP_FWD plan.
 enum PlanOp { OP_FWD = 0, OP_BWD = 1, OP_LN_BWD = 2, OP_FWD_STAGED = 3 };
 // PATH_STAGED and PATH_RESTAGED stream rows into shared memory; the first
 // copies a row's chunks into registers for both passes, the second reads
@@ -73,8 +72,8 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(15, OP_FWD, PATH_VECTOR ,   16, 2, 16, 0, 1, DT_ANY,     0,     0) \
     /* forward rows wider than 2048 chunks, streamed through two \
        shared-memory stages by a persistent grid of 2- or 4-CTA clusters \
-       (two stages leave room for 2-3 CTAs an SM); E4M3 outputs keep the \
-       register plans above */ \
+       (two stages leave room for 2-3 CTAs an SM); rows above 8192 chunks \
+       keep the register cluster plans */ \
     X(141, OP_FWD_STAGED, PATH_RESTAGED, 512, 3, 1, 2, 2, DT_ANY, 2049,  3072) \
     X(139, OP_FWD_STAGED, PATH_RESTAGED, 512, 4, 1, 2, 2, DT_ANY, 3073,  4096) \
     X(145, OP_FWD_STAGED, PATH_RESTAGED, 512, 3, 1, 2, 4, DT_ANY, 4097,  6144) \
@@ -260,6 +259,13 @@ RMSN_DECLARE_LAUNCHERS(f16w32)
 int launch_fwd8_f32(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
 int launch_fwd8_bf16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
 int launch_fwd8_f16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
+// ... and on the staged forward plans (OP_FWD_STAGED defaults)
+int launch_fwd8_staged_f32(int plan_id, bool fused, int mode, const FwdParams &p, int grid, int smem, void *stream);
+int launch_fwd8_staged_bf16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, int smem, void *stream);
+int launch_fwd8_staged_f16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, int smem, void *stream);
+const void *fwd8_staged_kernel_ptr_f32(int plan_id, bool fused, int mode);
+const void *fwd8_staged_kernel_ptr_bf16(int plan_id, bool fused, int mode);
+const void *fwd8_staged_kernel_ptr_f16(int plan_id, bool fused, int mode);
 
 // Opt a staged kernel into its largest dynamic shared memory on the current
 // device (once per kernel and device); returns a cudaError_t.

@@ -56,11 +56,14 @@ def _run(rn, d, dt, scaling, scale=None, eps=1e-6, offset=0.0, fused=False, offs
     if fused:
         assert np.array_equal(to_host(out["residual_out"], dt), f["h"])
     if expect_path is not None:
-        assert out["plan"]["path_name"] == expect_path, out["plan"]
+        # "vector": a fast path (rows wider than 2048 chunks stream through shared memory)
+        fast = ("vector", "staged") if expect_path == "vector" else (expect_path,)
+        assert out["plan"]["path_name"] in fast, out["plan"]
     return out, f
 
 
-SHAPES = [(333, 64), (257, 1024), (300, 4096), (129, 8192), (65, 16384), (101, 8193), (40, 3)]
+SHAPES = [(333, 64), (257, 1024), (300, 4096), (129, 8192), (65, 16384), (101, 8193), (40, 3), (33, 32768),
+          (17, 40968)]
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
@@ -137,7 +140,7 @@ def test_fp8_full_size_sampled(rn):
     # the tensor amax is the largest row amax: 448 * max_i scale_inv_i
     si = out["scale_inv"].cpu().numpy().astype(np.float64)
     check_rel(out["amax"].cpu().numpy(), [448.0 * si.max()], 2.0 ** -19, "amax")
-    assert out["plan"]["path_name"] == "vector"
+    assert out["plan"]["path_name"] in ("vector", "staged")
 
 
 def test_fp8_codes_match_plain_forward_dequantised(rn):

@@ -467,12 +467,25 @@ def test_staged_forward_matches_oracle(rn, dt, M, N, plan, fused):
     assert rn.lib().rmsnorm_device_status(1) == 0
 
 
-def test_e4m3_forward_refuses_staged_plans_and_wide_rows_stay_in_registers(rn):
-    _, t = dev_inputs(64, 32768, "bf16", 395)
+def test_e4m3_forward_on_staged_plans_matches_register_plans_bitwise(rn):
+    """Wide rows with an E4M3 output take the staged forward (the row max
+    from one pass over the stage, the codes from another); its codes,
+    1/scale and amax are the register cluster kernel's bits. A forced
+    staged alternative (not compiled for E4M3) is refused."""
+    _, t = dev_inputs(64, 32768, "bf16", 395, residual=True)
     with pytest.raises(rn.RMSNormError):
-        rn.rmsnorm_fwd_fp8(t["x"], t["w"], scaling="row", force_plan=139)
-    q = rn.rmsnorm_fwd_fp8(t["x"], t["w"], scaling="row")
-    assert q["plan"]["path_name"] == "vector" and q["plan"]["cluster_size"] == 2
+        rn.rmsnorm_fwd_fp8(t["x"], t["w"], scaling="row", force_plan=138)
+    for scaling, scale in (("row", None), ("tensor", torch.tensor([3.0], device="cuda"))):
+        for res in (None, t["residual"]):
+            kw = dict(scaling=scaling, scale=scale, residual=res, amax=True)
+            a = rn.rmsnorm_fwd_fp8(t["x"], t["w"], **kw)
+            b = rn.rmsnorm_fwd_fp8(t["x"], t["w"], force_plan=17, **kw)
+            torch.cuda.synchronize()
+            assert a["plan"]["path_name"] == "staged" and a["plan"]["cluster_size"] == 2
+            assert b["plan"]["path_name"] == "vector"
+            for k in ("y", "rstd", "scale_inv", "amax") + (("residual_out",) if res is not None else ()):
+                assert cuda_bits_equal(a[k], b[k]), (scaling, k)
+    assert rn.lib().rmsnorm_device_status(1) == 0
 
 
 @pytest.mark.parametrize("N", [20480, 65536])
