@@ -12,9 +12,9 @@
 // ROCm/TransformerEngine PR #583 (Description).
 //
 // Rows wider than 2048 chunks are shared by a thread-block cluster: the
-// register kernel holds each CTA's slice (the E4M3 outputs and rows above
-// 8192 chunks), the staged kernel streams the slices through shared-memory
-// stages on a persistent grid of clusters (every other forward of such rows).
+// staged kernel streams each CTA's slice through shared-memory stages on a
+// persistent grid of clusters (rows of up to 8192 chunks, every output
+// type), the register kernel holds the slices of wider rows.
 //
 // Generic kernel: one 256-thread CTA per row, the row read twice (the
 // second read hits L1/L2), split into an element-wise head, 16-byte chunks
