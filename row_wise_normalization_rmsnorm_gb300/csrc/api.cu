@@ -16,6 +16,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "../../include/rmsnorm.h"
@@ -212,7 +213,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
 // static shared memory), so later launches make no extra runtime call. A
 // failed call's error is cleared so that it cannot surface at a later launch.
 int allow_staged_smem(const void *k) {
-    constexpr int kSlots = 256;
+    constexpr int kSlots = 1024;  // staged kernels a process may use (more: opted in at every launch)
     static std::mutex mu;
     static const void *kern[kSlots];
     static uint64_t devs[kSlots];
@@ -468,16 +469,18 @@ static bool finite_scalar(float v) { return std::isfinite(v); }
 // Resident units (CTAs, or clusters) of a staged forward plan on the
 // device, taken at the plan's largest rows (the conservative value) and
 // cached per device, type, fusion mode and RMSNorm/LayerNorm.
-static int g_sfwd_parts[kMaxDevices][kNumKinds][2][2][3][kMaxPlanId];
+static std::map<uint64_t, int> g_sfwd_parts;
 
 static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d, bool fused, bool ln, int qmode,
                                     int *parts_out) {
     if (d.id < 0 || d.id >= kMaxPlanId || qmode < 0 || qmode > 2) return cudaErrorInvalidValue;
-    int &slot = g_sfwd_parts[dev][kind_of(dt)][fused ? 1 : 0][ln ? 1 : 0][qmode][d.id];
+    const uint64_t key = ((((((uint64_t)dev * kNumKinds + kind_of(dt)) * 2 + (fused ? 1 : 0)) * 2 + (ln ? 1 : 0)) * 3 +
+                          (uint64_t)qmode) * kMaxPlanId) + (uint64_t)d.id;
     {
         std::lock_guard<std::mutex> lk(g_occ_mutex);
-        if (slot > 0) {
-            *parts_out = slot;
+        auto it = g_sfwd_parts.find(key);
+        if (it != g_sfwd_parts.end()) {
+            *parts_out = it->second;
             return cudaSuccess;
         }
     }
@@ -508,7 +511,7 @@ static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d,
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;  // not resident at all: refuse
     std::lock_guard<std::mutex> lk(g_occ_mutex);
-    slot = n;
+    g_sfwd_parts[key] = n;
     *parts_out = n;
     return cudaSuccess;
 }
