@@ -90,6 +90,10 @@ static int cta_threads(const PlanDesc &d) { return d.path == PATH_GENERIC ? 256 
 // Largest dynamic shared memory a plan may ask for: the 227 KB a CTA may
 // opt into on sm_103a, less room for the kernels' static arrays.
 constexpr int kMaxDynamicSmem = 226 * 1024;
+// Longest row (bytes) the generic LayerNorm forward keeps in shared memory
+// between its three passes: eight 256-thread CTAs an SM still fit. (The
+// RMSNorm forward, two passes, measured slower with the cache.)
+constexpr int64_t kGenericRowCache = 24 * 1024;
 
 // A staged plan's shared memory: `depth` stages of x and dy (and dres for
 // the fused variant) rows of es-byte elements, or of one CTA's slice (a
@@ -913,6 +917,7 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
     p.offset = offset;
     p.stages = stages;
     p.status = status;
+    p.cache_row = plan.path == PATH_GENERIC && N * (int64_t)s <= kGenericRowCache ? 1 : 0;
     int le;
     if (stages > 0) {
         le = launch_fwd_staged_dt(dt, true, plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream);

@@ -423,6 +423,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 template <typename T, bool FUSED>
 __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) {
     __shared__ float red[32];
+    extern __shared__ uint4 gen_smem[];
     constexpr int E = Elem<T>::E;
     constexpr int NP = Elem<T>::NP;
     const int64_t row = blockIdx.x;
@@ -438,10 +439,14 @@ __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) 
     const bool vr = FUSED && addr_mod16(p.residual) == a16;
     const bool vh = FUSED && addr_mod16(p.residual_out) == a16;
     const RowSplit sp = row_split(x, N, true);
-    // The same thread wrote hout[j], so it reads its own value back.
-    const T *hsrc = FUSED ? static_cast<const T *>(hout) : x;
+    // h is re-read by the thread that wrote it: from the shared-memory row
+    // cache (16-byte chunks aligned as in x) where the host gave one, else
+    // from residual_out or x
+    const bool cache = p.cache_row != 0;
+    T *hs = reinterpret_cast<T *>(reinterpret_cast<char *>(gen_smem) + addr_mod16(x));
+    const T *hsrc = cache ? static_cast<const T *>(hs) : (FUSED ? static_cast<const T *>(hout) : x);
     auto h_at = [&](int j) { return load_elem(hsrc, j); };
-    auto h_chunk = [&](int j0, float2 (&h)[NP]) { load_chunk_at(hsrc, j0, FUSED ? vh : true, h); };
+    auto h_chunk = [&](int j0, float2 (&h)[NP]) { load_chunk_at(hsrc, j0, cache || !FUSED || vh, h); };
 
     float sm = 0.f;
     row_visit<E>(
@@ -452,6 +457,7 @@ __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) 
                 h = round_to(__fadd_rn(h, load_elem(res, j)), x);
                 store_elem(hout, j, h);
             }
+            if (cache) store_elem(hs, j, h);
             sm = __fadd_rn(sm, h);
         },
         [&](int j0) {
@@ -465,6 +471,7 @@ __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) 
                 unpack<T>(pack<T>(h), h);
                 store_chunk_at(hout, j0, vh, h);
             }
+            if (cache) store_chunk_at(hs, j0, true, h);
 #pragma unroll
             for (int q = 0; q < NP; ++q) sm = __fadd_rn(__fadd_rn(sm, h[q].x), h[q].y);
         });
@@ -852,6 +859,13 @@ static const void *ptr_vec(bool fused) {
                  : (const void *)rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false>;
 }
 
+// The generic LayerNorm forward's row cache: N elements and 16 bytes of
+// alignment slack (set by the host only for rows of up to 24 KB).
+template <typename T>
+static int gen_cache_bytes(const FwdParams &p) {
+    return p.cache_row ? p.N * (int)sizeof(T) + 16 : 0;
+}
+
 template <typename T, typename TW, int Q>
 static int launch_gen(bool fused, const FwdParams &p, int grid, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1000,9 +1014,9 @@ static int ln_launch_entry(bool fused, const FwdParams &p, int grid, void *strea
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
         if (fused)
-            layernorm_fwd_generic<T, true><<<grid, 256, 0, s>>>(p);
+            layernorm_fwd_generic<T, true><<<grid, 256, gen_cache_bytes<T>(p), s>>>(p);
         else
-            layernorm_fwd_generic<T, false><<<grid, 256, 0, s>>>(p);
+            layernorm_fwd_generic<T, false><<<grid, 256, gen_cache_bytes<T>(p), s>>>(p);
         return (int)cudaGetLastError();
     } else if constexpr (CS == 1) {
         if (fused)

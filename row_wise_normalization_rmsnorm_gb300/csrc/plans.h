@@ -208,6 +208,10 @@ struct FwdParams {
     // status word a bounded wait that gives up writes
     int stages = 0;
     int *status = nullptr;
+    // generic LayerNorm forward: the row's h is kept in dynamic shared
+    // memory between the passes (N elements + 16 bytes) instead of re-read
+    // from L1/L2
+    int cache_row = 0;
 };
 
 // Output of the forward: the activations' type, or E4M3 with a per-tensor
