@@ -83,6 +83,13 @@ MUTATIONS = {
     "ln_bwd_ignores_given_mean": ("mu = (double)jb->mean_in[i];", "mu = 0.0 * (double)jb->mean_in[i];"),
     "weight_read_as_activation_type": ("wpo[j] = jb->w ? jb->offset + load_elem(jb->wdtype",
                                        "wpo[j] = jb->w ? jb->offset + load_elem(jb->dtype"),
+    "fp8_scale_inv_not_reciprocal": ("if (jb->scale_inv) jb->scale_inv[i] = 1.0 / sc;",
+                                     "if (jb->scale_inv) jb->scale_inv[i] = sc;"),
+    "ln_mean_over_n_plus_1": ("const double mu = sum / (double)N;", "const double mu = sum / (double)(N + 1);"),
+    "bwd_ignores_given_rstd": ("double rstd;\n        if (jb->rstd_in) {\n            rstd = (double)jb->rstd_in[i];\n",
+                               "double rstd;\n        if (jb->rstd_in) {\n            rstd = 1.0 + 0.0 * (double)jb->rstd_in[i];\n"),
+    "e4m3_saturates_late": ("if (a >= 448.0) { *out = (uint8_t)(sign | 0x7eu); return 0; }",
+                            "if (a >= 480.0) { *out = (uint8_t)(sign | 0x7eu); return 0; }"),
 }
 
 
