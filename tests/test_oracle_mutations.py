@@ -90,6 +90,27 @@ MUTATIONS = {
                                "double rstd;\n        if (jb->rstd_in) {\n            rstd = 1.0 + 0.0 * (double)jb->rstd_in[i];\n"),
     "e4m3_saturates_late": ("if (a >= 448.0) { *out = (uint8_t)(sign | 0x7eu); return 0; }",
                             "if (a >= 480.0) { *out = (uint8_t)(sign | 0x7eu); return 0; }"),
+    "ln_dgamma_uncentred": ("jb->dg[j] += dyj * xhat;", "jb->dg[j] += dyj * (hv[j] * rstd);"),
+    "fp8_tensor_scale_ignored": ("double sc = jb->fp8_scale;", "double sc = 1.0;"),
+    "dres_subtracted": ("rstd * (fabs(g) + fabs(xhat * c));\n            if (jb->dres) {\n"
+                        "                const double d = load_elem(jb->dtype, jb->dres, base + j);\n"
+                        "                dxj += d;",
+                        "rstd * (fabs(g) + fabs(xhat * c));\n            if (jb->dres) {\n"
+                        "                const double d = load_elem(jb->dtype, jb->dres, base + j);\n"
+                        "                dxj -= d;"),
+    "bwd_recomputed_rstd_without_eps": ("rstd = 1.0 / sqrt(ss / (double)N + jb->eps);",
+                                        "rstd = 1.0 / sqrt(ss / (double)N);"),
+    "ln_mean_g_over_n_minus_1": ("mg /= (double)N;", "mg /= (double)(N > 1 ? N - 1 : 1);"),
+    "rstd_saved_as_std": ("if (jb->rstd32) jb->rstd32[i] = (float)rstd;\n        if (jb->fp8_mode",
+                          "if (jb->rstd32) jb->rstd32[i] = (float)(1.0 / rstd);\n        if (jb->fp8_mode"),
+    "ln_mean32_not_saved": ("if (jb->mean32) jb->mean32[i] = (float)mu;", "if (jb->mean32) jb->mean32[i] = 0.0f;"),
+    "fp8_amax_after_scaling": ("if (jb->amax_row) jb->amax_row[i] = amax;",
+                               "if (jb->amax_row) jb->amax_row[i] = amax * sc;"),
+    "ln_bwd_recomputed_var_uncentred": ("for (int64_t j = 0; j < N; ++j) sq += (hv[j] - mu) * (hv[j] - mu);",
+                                        "for (int64_t j = 0; j < N; ++j) sq += hv[j] * hv[j];"),
+    "ln_beta_takes_offset": ("const double bias = jb->beta ? load_elem(jb->wdtype, jb->beta, j) : 0.0;",
+                             "const double bias = jb->beta ? jb->offset + load_elem(jb->wdtype, jb->beta, j) : 0.0;"),
+    "fp8_zero_row_scale_zero": ("sc = amax > 0.0 ? 448.0 / amax : 1.0;", "sc = amax > 0.0 ? 448.0 / amax : 0.0;"),
 }
 
 

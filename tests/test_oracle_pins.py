@@ -557,6 +557,8 @@ def test_ln_fwd_hand_example():
     # mean 2.5, biased variance 1.25, rstd = 1 / sqrt(1.25 + 0.25)
     rstd = 1.0 / math.sqrt(1.5)
     assert r["mean64"][0] == 2.5 and abs(r["rstd64"][0] - rstd) < 1e-15
+    # the saved fp32 statistics are the same values rounded once to binary32
+    assert r["mean32"][0] == np.float32(2.5) and r["rstd32"][0] == np.float32(rstd)
     want = (x[0] - 2.5) * rstd * g + b
     assert np.allclose(r["y64"][0], want, rtol=1e-15, atol=1e-15)
 
