@@ -95,6 +95,26 @@ constexpr int kMaxDynamicSmem = 226 * 1024;
 // RMSNorm forward, two passes, measured slower with the cache.)
 constexpr int64_t kGenericRowCache = 24 * 1024;
 
+// Largest row cache (x and dy slots) the generic LayerNorm backward takes,
+// and what an SM's shared memory must hold for it: every CTA that the
+// registers let reside (the grid is sized by that count), each with the
+// driver's 1 KB reserve and the kernel's static arrays beside its cache.
+// (The RMSNorm generic backward measured slower with the same cache: 86 ->
+// 88 us on misaligned bf16 4096x7168; it re-reads global memory.)
+constexpr int64_t kGenericBwdRowCache = 40 * 1024;
+constexpr int64_t kSmemPerSM = 228 * 1024;
+constexpr int64_t kSmemPerCtaOverhead = 1024 + 256;
+
+// Whether a generic LayerNorm backward keeps the row in shared memory: only
+// where it updates partial rows (then each row is read three times) and the
+// cache lowers no SM's resident CTA count.
+static int generic_bwd_cache(int path, int64_t N, int es, bool partials, int cps) {
+    if (path != PATH_GENERIC || !partials) return 0;
+    const int64_t b = 2 * generic_bwd_cache_slot(N, es);
+    if (b > kGenericBwdRowCache || cps * (b + kSmemPerCtaOverhead) > kSmemPerSM) return 0;
+    return 1;
+}
+
 // A staged plan's shared memory: `depth` stages of x and dy (and dres for
 // the fused variant) rows of es-byte elements, or of one CTA's slice (a
 // cs-th, rounded up to whole chunks) of a row shared by a cluster; the
@@ -1020,6 +1040,8 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
     p.offset = offset;
     const PlanDesc *pd = find_plan(plan.plan_id);
     p.stages = staged_path(pd->path) ? staged_depth(*pd, N, (int)s, fused) : 0;
+    p.cache_row = generic_bwd_cache(pd->path, N, (int)s, ws != nullptr, cps);
+    if (p.cache_row) plan.smem_bytes = (int32_t)(2 * generic_bwd_cache_slot(N, (int)s));
     int le;
     switch (base_dtype(dt)) {
     case RMSNORM_BF16: le = launch_ln_bwd_bf16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;

@@ -864,12 +864,20 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
     }
 }
 
-// Generic LayerNorm backward, same scheme: per row the pair (sum g,
+// Generic LayerNorm backward, the same scheme: per row the pair (sum g,
 // sum g (x - mean)), then dx; the partial row ws[cta, 0..2N) holds dgamma
-// and dbeta, updated one column a thread.
-template <typename T, bool FUSED>
-__global__ void __launch_bounds__(256) layernorm_bwd_generic(const BwdParams p) {
+// and dbeta, updated one column a thread. Each row is read three times
+// (the sums, the dgamma and dbeta update, dx). Where the host gave a row
+// cache, the first read keeps x and dy in shared memory (at x's address
+// mod 16, so chunks stay aligned) and the other two read them there, the
+// update after the reduction's barrier; otherwise they re-read global
+// memory (L1/L2) and the update comes before the barrier, since dx may
+// overwrite dy. Both variants are held to the registers of five CTAs an
+// SM, the residency the grid is sized for.
+template <typename T, bool FUSED, bool CACHE>
+__global__ void __launch_bounds__(256, 5) layernorm_bwd_generic(const BwdParams p) {
     __shared__ float2 red[32];
+    extern __shared__ uint4 gen_smem[];
     constexpr int E = Elem<T>::E;
     constexpr int NP = Elem<T>::NP;
     const int N = p.N;
@@ -879,6 +887,8 @@ __global__ void __launch_bounds__(256) layernorm_bwd_generic(const BwdParams p) 
     const uint32_t a16 = addr_mod16(p.x);
     const bool vdy = addr_mod16(p.dy) == a16, vdx = addr_mod16(p.dx) == a16;
     const bool vdr = has_dres && addr_mod16(p.dres) == a16;
+    constexpr bool cache = CACHE;
+    const int64_t slot = generic_bwd_cache_slot(N, (int)sizeof(T));
     bool first = true;
     for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
         const T *x = reinterpret_cast<const T *>(p.x) + row * N;
@@ -888,39 +898,53 @@ __global__ void __launch_bounds__(256) layernorm_bwd_generic(const BwdParams p) 
         const float r = p.rstd[row];
         const float nmu = -p.mean[row];
         const RowSplit sp = row_split(x, N, true);
+        T *xs = reinterpret_cast<T *>(reinterpret_cast<char *>(gen_smem) + addr_mod16(x));
+        T *ds = reinterpret_cast<T *>(reinterpret_cast<char *>(gen_smem) + slot + addr_mod16(x));
+        const T *xr = cache ? static_cast<const T *>(xs) : x;
+        const T *dyr = cache ? static_cast<const T *>(ds) : dy;
+        const bool vdyr = cache || vdy;
         auto gof = [&](float dyj, float wj) { return w ? __fmul_rn(dyj, __fadd_rn(p.offset, wj)) : dyj; };
-        // the chunk at column j0: dy, x and gamma
-        auto chunk = [&](int j0, float2 (&dv)[NP], float2 (&xv)[NP], float2 (&wv)[NP]) {
-            load_chunk_at(dy, j0, vdy, dv);
-            load_chunk_at(x, j0, true, xv);
-            if (w) w_chunk_at<T, T>(w, j0, wv);
-        };
         float2 part = make_float2(0.f, 0.f);
         auto sums = [&](float g, float xj) {
             part.x = __fadd_rn(part.x, g);
             part.y = __fmaf_rn(g, __fadd_rn(xj, nmu), part.y);
         };
         row_visit<E>(
-            sp, N, [&](int j) { sums(gof(load_elem(dy, j), w ? load_w(w, j) : 0.f), load_elem(x, j)); },
+            sp, N,
+            [&](int j) {
+                const float dyj = load_elem(dy, j), xj = load_elem(x, j);
+                if (cache) {
+                    store_elem(xs, j, xj);
+                    store_elem(ds, j, dyj);
+                }
+                sums(gof(dyj, w ? load_w(w, j) : 0.f), xj);
+            },
             [&](int j0) {
                 float2 dv[NP], xv[NP], wv[NP];
-                chunk(j0, dv, xv, wv);
+                load_chunk_at(dy, j0, vdy, dv);
+                load_chunk_at(x, j0, true, xv);
+                if (w) w_chunk_at<T, T>(w, j0, wv);
+                if (cache) {
+                    store_chunk_at(xs, j0, true, xv);
+                    store_chunk_at(ds, j0, true, dv);
+                }
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
                     sums(gof(dv[q].x, w ? wv[q].x : 0.f), xv[q].x);
                     sums(gof(dv[q].y, w ? wv[q].y : 0.f), xv[q].y);
                 }
             });
-        // the dgamma and dbeta partials, one column a thread (coalesced), before
-        // the reduction's barrier: dx may overwrite dy later
-        if (wsrow) {
+        // the dgamma and dbeta partials, one column a thread (coalesced)
+        auto param_update = [&]() {
             for (int j = threadIdx.x; j < N; j += blockDim.x) {
-                const float dyj = load_elem(dy, j), xh = __fmul_rn(__fadd_rn(load_elem(x, j), nmu), r);
+                const float dyj = load_elem(dyr, j), xh = __fmul_rn(__fadd_rn(load_elem(xr, j), nmu), r);
                 wsrow[j] = first ? __fmul_rn(dyj, xh) : __fmaf_rn(dyj, xh, wsrow[j]);
                 wsrow[N + j] = first ? dyj : __fadd_rn(wsrow[N + j], dyj);
             }
-        }
+        };
+        if (wsrow && !cache) param_update();
         const float2 s = cta_allreduce2(part, red);
+        if (wsrow && cache) param_update();
         const float cm = -__fdiv_rn(__fmul_rn(s.y, r), (float)N);
         const float nmg = -__fdiv_rn(s.x, (float)N);
         // dx of a column
@@ -933,12 +957,14 @@ __global__ void __launch_bounds__(256) layernorm_bwd_generic(const BwdParams p) 
         row_visit<E>(
             sp, N,
             [&](int j) {
-                store_elem(dx, j, out(load_elem(dy, j), load_elem(x, j), w ? load_w(w, j) : 0.f,
+                store_elem(dx, j, out(load_elem(dyr, j), load_elem(xr, j), w ? load_w(w, j) : 0.f,
                                       has_dres ? load_elem(dr, j) : 0.f));
             },
             [&](int j0) {
                 float2 dv[NP], xv[NP], wv[NP], rv[NP];
-                chunk(j0, dv, xv, wv);
+                load_chunk_at(dyr, j0, vdyr, dv);
+                load_chunk_at(xr, j0, true, xv);
+                if (w) w_chunk_at<T, T>(w, j0, wv);
                 if (has_dres) load_chunk_at(dr, j0, vdr, rv);
 #pragma unroll
                 for (int q = 0; q < NP; ++q)
@@ -946,8 +972,17 @@ __global__ void __launch_bounds__(256) layernorm_bwd_generic(const BwdParams p) 
                                         out(dv[q].y, xv[q].y, w ? wv[q].y : 0.f, has_dres ? rv[q].y : 0.f));
                 store_chunk_at(dx, j0, vdx, xv);
             });
+        // the next row's first pass overwrites the cache
+        if (cache) __syncthreads();
         first = false;
     }
+}
+
+// Dynamic shared memory of a generic backward launch: the two row-cache
+// slots where the host asked for the cache (at most 40 KB), else none.
+template <typename T>
+static int generic_bwd_smem(const BwdParams &p) {
+    return p.cache_row ? (int)(2 * generic_bwd_cache_slot(p.N, (int)sizeof(T))) : 0;
 }
 
 // Finalizer. When launched as a programmatic dependent of the main kernel
@@ -1250,10 +1285,13 @@ static int ln_bwd_launch_entry(bool fused, const BwdParams &p, int grid, int sme
     if constexpr (OP != OP_LN_BWD) {
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
+        const int gs = generic_bwd_smem<T>(p);
         if (fused)
-            layernorm_bwd_generic<T, true><<<grid, 256, 0, s>>>(p);
+            gs ? layernorm_bwd_generic<T, true, true><<<grid, 256, gs, s>>>(p)
+               : layernorm_bwd_generic<T, true, false><<<grid, 256, 0, s>>>(p);
         else
-            layernorm_bwd_generic<T, false><<<grid, 256, 0, s>>>(p);
+            gs ? layernorm_bwd_generic<T, false, true><<<grid, 256, gs, s>>>(p)
+               : layernorm_bwd_generic<T, false, false><<<grid, 256, 0, s>>>(p);
         return (int)cudaGetLastError();
     } else if constexpr (PATH == PATH_VECTOR) {
         return ln_bwd_launch_vec<T, TPR, V, TEAMS, D, CS>(fused, p, grid, smem, s);
@@ -1269,7 +1307,7 @@ static const void *ln_bwd_ptr_entry(bool fused) {
     if constexpr (OP != OP_LN_BWD) {
         return nullptr;
     } else if constexpr (PATH == PATH_GENERIC) {
-        return fused ? (const void *)layernorm_bwd_generic<T, true> : (const void *)layernorm_bwd_generic<T, false>;
+        return fused ? (const void *)layernorm_bwd_generic<T, true, false> : (const void *)layernorm_bwd_generic<T, false, false>;
     } else if constexpr (PATH == PATH_VECTOR) {
         return fused ? (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true>
                      : (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false>;

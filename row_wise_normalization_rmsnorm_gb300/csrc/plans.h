@@ -232,7 +232,13 @@ struct BwdParams {
     float offset;
     const float *mean;       // LayerNorm: the forward's per-row mean
     int stages = 0;          // staged kernels: stages in use (2 .. the plan's depth; 0: the depth)
+    int cache_row = 0;       // generic LayerNorm kernel: keep the row's x and dy in shared memory
 };
+
+// The generic LayerNorm backward's row cache: x and dy of the current row, each in
+// a slot of this many bytes, placed at x's address mod 16 so that the
+// row's 16-byte chunks stay aligned.
+constexpr int64_t generic_bwd_cache_slot(int64_t N, int es) { return (N * es + 31) / 16 * 16; }
 
 // Codes written to the status word: a bounded wait (a cluster row's peer
 // partial, or a staged row's bulk copy) gave up.

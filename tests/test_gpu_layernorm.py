@@ -128,6 +128,19 @@ def test_ln_misaligned_takes_generic(rn):
     _ln_check(rn, d, "bf16", offset_elems=1, expect_path="generic")
 
 
+@pytest.mark.parametrize("dt,M,N", [("bf16", 160, 7169), ("bf16", 96, 10247), ("f32", 96, 5111)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_ln_generic_backward_row_cache_both_sides_of_its_limit(rn, dt, M, N, fused):
+    """x and dy of the row in shared memory where both fit 40 KB (slots of
+    (N es + 31) // 16 * 16 bytes), global re-reads beyond; the oracle's
+    result either way, and the plan reports the cache it took."""
+    d = inputs.make_inputs(M, N, dt, 340 + N % 5, beta=True, residual=fused, dres=fused)
+    _, bo = _ln_check(rn, d, dt, fused=fused, offset_elems=1, expect_path="generic")
+    es = 4 if dt == "f32" else 2
+    slot = (N * es + 31) // 16 * 16
+    assert bo["plan"]["smem_bytes"] == (2 * slot if 2 * slot <= 40 * 1024 else 0), bo["plan"]
+
+
 @pytest.mark.parametrize("dt,M,N,offs", [
     ("bf16", 129, 4099, {"x": 3, "gamma": 3, "beta": 1, "y": 3, "dy": 3, "dx": 3, "dgamma": 1}),
     ("f32", 100, 1030, {"x": 1, "gamma": 2, "beta": 1, "y": 1, "dy": 1, "dx": 1, "dbeta": 3}),

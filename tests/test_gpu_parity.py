@@ -171,6 +171,19 @@ def test_generic_fused_residual_alone_misaligned(rn):
                                  "dres": 3})
 
 
+@pytest.mark.parametrize("dt,M,N", [("bf16", 160, 7169), ("bf16", 96, 10223), ("bf16", 96, 10247),
+                                    ("f32", 130, 5111), ("f32", 64, 5121)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_generic_backward_rows_around_40kb(rn, dt, M, N, fused):
+    """Rows whose x and dy together come just under and just over 40 KB
+    (where the LayerNorm generic backward stops caching them): the RMSNorm
+    generic backward re-reads global memory at every length, takes no
+    dynamic shared memory, and gives the oracle's result."""
+    d = inputs.make_inputs(M, N, dt, 330 + N % 7, residual=fused, dres=fused)
+    _, bplan = _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, fused=fused, offset_elems=1, expect_path="generic")
+    assert bplan["smem_bytes"] == 0, (N, bplan)
+
+
 @pytest.mark.parametrize("eps", [0.0, 1e-2, 10.0])
 def test_eps_values(rn, eps):
     d = inputs.make_inputs(200, 2048, "bf16", 71)
