@@ -296,7 +296,10 @@ typedef struct {
     int32_t ctas;               /* grid size in CTAs                            */
     int32_t ctas_per_sm;        /* backward: resident CTAs per SM used for `ctas`
                                    (0 where the library queried the device)     */
-    int32_t smem_bytes;         /* dynamic shared memory per CTA                */
+    int32_t smem_bytes;         /* dynamic shared memory per CTA: a call's plan
+                                   counts it as launched (a generic LayerNorm
+                                   backward's row cache included); the host-only
+                                   query leaves that cache out               */
     int32_t cluster_size;       /* CTAs of a thread-block cluster sharing a row (1: none) */
     int32_t ws_rows;            /* persistent grids (the backward and a staged
                                    forward): units walking the rows, CTAs or
