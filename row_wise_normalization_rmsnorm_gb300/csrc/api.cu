@@ -100,7 +100,8 @@ constexpr int64_t kGenericRowCache = 24 * 1024;
 // registers let reside (the grid is sized by that count), each with the
 // driver's 1 KB reserve and the kernel's static arrays beside its cache.
 // (The RMSNorm generic backward measured slower with the same cache: 86 ->
-// 88 us on misaligned bf16 4096x7168; it re-reads global memory.)
+// 88 us on misaligned bf16 4096x7168, its re-reads being L1 hits already;
+// it re-reads global memory.)
 constexpr int64_t kGenericBwdRowCache = 40 * 1024;
 constexpr int64_t kSmemPerSM = 228 * 1024;
 constexpr int64_t kSmemPerCtaOverhead = 1024 + 256;
