@@ -1,6 +1,7 @@
 """Host logic of bench.py on CPU: the clock record's summary, the kernel
-source hash that keys the stored DRAM counters, the counters' lookup, and
-the algorithmic byte counts of the timed kernels."""
+source hash that keys the stored DRAM counters, the counters' lookup, the
+algorithmic byte counts of the timed kernels, and the reference arm's JSON
+line (the CPU oracle timed on a row sample)."""
 import json
 import os
 import sys
@@ -108,3 +109,24 @@ def test_peak_falls_back_without_measured_file(tmp_path, monkeypatch):
     assert bench.peaks() == (bench.FALLBACK_HBM_GBS, "fallback")
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6708.2}))
     assert bench.peaks() == (6708.2, "measured")
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` times the CPU oracle on a bounded row
+    sample of the bench workload and prints one JSON line with the same
+    metric and unit as the GPU arm, its own cpu_baseline and an e2e with no
+    host-device copies; it needs no GPU."""
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "1"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] >= 3 and d["gpu_launches"] == 0
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["data"] == "synthetic"
+    assert "16384x8192" in d["metric"] and d["config"]["M"] == 16384 and d["config"]["N"] == 8192
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
