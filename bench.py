@@ -138,8 +138,9 @@ class ClockSampler:
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index, enabled=True):
+        import tempfile
         self.index, self.proc, self.enabled = index, None, enabled
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"rmsnorm_bench_clocks_{os.getpid()}_{index}.csv")
 
     def __enter__(self):
         if not self.enabled:
@@ -204,7 +205,9 @@ def oracle_sample(arrays, p, rows, nthreads):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(arrays, p, target_s=8.0):
+def cpu_baseline(arrays, p, target_s=8.0, single_s=4.0):
+    """The oracle on the host's cores (row-parallel, one thread a core) and
+    on one thread, each on a bounded sample of the workload's rows."""
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
@@ -215,9 +218,15 @@ def cpu_baseline(arrays, p, target_s=8.0):
     rows = max(cores, rows // cores * cores)
     t = oracle_sample(arrays, p, rows, cores)
     by = bytes_fwd(rows, N, s) + bytes_bwd(rows, N, s, 0)
+    t1 = oracle_sample(arrays, p, 16, 1)
+    rows1 = int(min(M, max(16, 16 * single_s / max(t1, 1e-3))))
+    t1 = oracle_sample(arrays, p, rows1, 1)
+    by1 = bytes_fwd(rows1, N, s) + bytes_bwd(rows1, N, s, 0)
     return {"value": by / t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"first {rows} of {M} rows of the workload, fwd + bwd, fp64 C oracle, "
-                      f"row-parallel on {cores} threads, {t:.2f} s wall"}
+                      f"row-parallel on {cores} threads, {t:.2f} s wall",
+            "single_thread": {"value": by1 / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"first {rows1} rows, one thread, {t1:.2f} s wall"}}
 
 
 def run_reference(args):
@@ -526,15 +535,62 @@ def main():
     t_main = [e[0].elapsed_time(e[1]) for e in dg]
     t_fin = [e[1].elapsed_time(e[2]) for e in dg]
 
+    # Host cost of one ABI call (the wall time of enqueueing it, the
+    # counterpart of the per-call host cost the direct-call launch path was
+    # built to cut): ctypes calls with the arguments marshalled once, in
+    # bursts of 50 followed by a synchronize so the launch queue never fills
+    # (a full queue would make the call wait for the GPU); median per call.
+    L = rn.lib()
+    hs = stream.cuda_stream
+    fargs = (x.data_ptr(), w.data_ptr(), y.data_ptr(), rstd.data_ptr(), M, N, 1, eps, 0.0, hs)
+    bargs = (dy.data_ptr(), x.data_ptr(), w.data_ptr(), rstd.data_ptr(), dx.data_ptr(), dw.data_ptr(),
+             ws.data_ptr(), ws_bytes, M, N, 1, eps, 0.0, hs)
+    host = {}
+    for name, fn, args in (("fwd", L.rmsnorm_fwd, fargs), ("bwd", L.rmsnorm_bwd, bargs)):
+        per = []
+        for _ in range(20):
+            torch.cuda.synchronize()
+            for _ in range(50):
+                t0 = time.perf_counter_ns()
+                st = fn(*args)
+                per.append((time.perf_counter_ns() - t0) / 1e3)
+                assert st == 0, st
+        torch.cuda.synchronize()
+        host[name] = {"median_us": statistics.median(per), "p90_us": sorted(per)[int(0.9 * len(per))],
+                      "calls": len(per)}
+    host["how"] = ("wall time of the ctypes call into the C ABI, arguments marshalled once, "
+                   "bursts of 50 calls between synchronizes, median over 1000 calls")
+
+    # The backward with workspace NULL: the library takes stream-ordered
+    # memory (cudaMallocAsync / cudaFreeAsync on the stream) inside the call,
+    # so the allocation is inside the timed bracket.
+    nn = min(K, 200)
+    en = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nn)]
+    for a, b in en:
+        a.record(stream)
+        b.record(stream)
+    for _ in range(3):
+        rn.rmsnorm_bwd(dy, x, w, rstd, dx=dx, dw=dw, workspace=None, eps=eps)
+    torch.cuda.synchronize()
+    for a, b in en:
+        a.record(stream)
+        rn.rmsnorm_bwd(dy, x, w, rstd, dx=dx, dw=dw, workspace=None, eps=eps)
+        b.record(stream)
+    torch.cuda.synchronize()
+    t_null = [a.elapsed_time(b) for a, b in en]
+
     peak, peak_kind = peaks()
     comp = {}
     for name, ts, by in (("fwd", t_fwd, bytes_fwd(M, N, s)), ("bwd", t_bwd, bytes_bwd(M, N, s, P)),
+                         ("bwd_workspace_null", t_null, bytes_bwd(M, N, s, P)),
                          ("bwd_main_serialised", t_main, bytes_bwd_main(M, N, s, P)),
                          ("bwd_finalize_serialised", t_fin, bytes_bwd_finalize(N, s, P))):
         avg = sum(ts) / len(ts)
         comp[name] = {"us": avg * 1e3, "median_us": statistics.median(ts) * 1e3, "bytes": by,
                       "gbs": by / (avg * 1e-3) / 1e9, "frac_of_peak": by / (avg * 1e-3) / 1e9 / peak}
     comp["bwd"]["kernels"] = "main + finalizer (programmatic dependent launch)"
+    comp["bwd_workspace_null"]["kernels"] = ("main + finalizer, workspace NULL: stream-ordered allocation "
+                                             "and free inside the call")
     dom = "bwd" if comp["bwd"]["us"] >= comp["fwd"]["us"] else "fwd"
     bwd_main = {"staged": "rmsnorm_bwd_staged", "vector": "rmsnorm_bwd_vector"}.get(bplan["path_name"],
                                                                                    "rmsnorm_bwd_generic")
@@ -621,6 +677,7 @@ def main():
                    "workspace_bytes": ws_bytes},
         "frac_of_peak": value / world / peak,
         "components": comp,
+        "host_enqueue": host,
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": 3 * K,

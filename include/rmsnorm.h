@@ -239,17 +239,19 @@ size_t layernorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt);
 /*
  * Backward without any allocation, for callers that cannot allocate device
  * memory when they call (an engine that reserves all device memory at
- * start-up, a plug-in host that passes its ops no workspace, code running
- * while a global-mode stream capture forbids cudaMalloc). The pages have no
- * counterpart to this entry point.
- * Same arguments and results as rmsnorm_bwd, but the dW partial rows live
- * in a fixed array inside the library, RMSNORM_NOALLOC_SCRATCH_BYTES per
- * GPU, held from the time the library's kernels load on that GPU until the
- * process exits. Returns RMSNORM_ERR_WORKSPACE, launching nothing, when the
- * workspace this call needs (at most rmsnorm_bwd_workspace_bytes(M, N, dt))
- * exceeds that size.
+ * start-up and forbids later allocation, a plug-in host that passes its ops
+ * no workspace). The pages have no counterpart to this entry point.
+ * Same arguments and results as rmsnorm_bwd (every storage type, the
+ * fp32-weight ones included; w and dw NULL for the non-affine backward),
+ * but the dW partial rows live in a fixed array inside the library,
+ * RMSNORM_NOALLOC_SCRATCH_BYTES per GPU, held from the time the library's
+ * kernels load on that GPU until the process exits. Returns
+ * RMSNORM_ERR_WORKSPACE, launching nothing, when the workspace this call
+ * needs (at most rmsnorm_bwd_workspace_bytes(M, N, dt)) exceeds that size.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * The address is kept for the life of the process: do not use the library
+ * across a cudaDeviceReset.
  * Every call on a device uses the same array and leaves its partial rows
  * there; nothing needs clearing, because each call writes every partial it
  * reads. Calls that can overlap on the GPU (other streams, other threads)
@@ -395,6 +397,20 @@ rmsnorm_status_t rmsnorm_bwd_ex(const void *dy, const void *dresidual_out, const
  * device cannot be queried.
  */
 int rmsnorm_device_status(int clear);
+
+/*
+ * Optional one-time note on stderr when a call falls to the generic kernels
+ * (rows that are not whole 16-byte chunks, or arrays not 16-byte aligned at
+ * one common offset), which run well below the vectorised kernels' speed:
+ * the counterpart of the fallback warning printed the first time no tuned
+ * kernel serves a config (TransformerEngine tuning page, "[ROCm] RMSNorm
+ * tuning", Description). Off by default. enabled != 0 switches it on and
+ * re-arms it: the next fallback of each kind of call (RMSNorm forward and
+ * backward, LayerNorm forward and backward) prints one line; later ones of
+ * that kind print nothing. Calls that force a plan are not reported.
+ * Thread-safe; no CUDA call.
+ */
+void rmsnorm_set_generic_note(int enabled);
 
 /* Static description of a status code. */
 const char *rmsnorm_status_string(rmsnorm_status_t status);

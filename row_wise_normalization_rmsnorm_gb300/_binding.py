@@ -88,6 +88,7 @@ SIGNATURES = {
     "rmsnorm_last_cuda_error": (_i, []),
     "rmsnorm_self_check": (_i, []),
     "rmsnorm_device_status": (_i, [_i]),
+    "rmsnorm_set_generic_note": (None, [_i]),
 }
 
 

@@ -643,6 +643,43 @@ static const bool g_loaded_check = [] {
     return true;
 }();
 
+// ------------------------------------------------- generic-kernel note --
+// Optional one-time note on stderr when a call falls to the generic kernels
+// (the counterpart of the fallback warning the TransformerEngine tuning page
+// prints the first time no tuned kernel serves a config, "[ROCm] RMSNorm
+// tuning", Description). Off by default; rmsnorm_set_generic_note switches
+// it. One note per kind of call (forward, backward, LayerNorm forward and
+// backward) until the switch is set again.
+static std::atomic<int> g_note_on{0};
+static std::atomic<unsigned> g_noted{0};
+enum : unsigned { NOTE_FWD = 1, NOTE_BWD = 2, NOTE_LN_FWD = 4, NOTE_LN_BWD = 8 };
+
+static const char *dtype_name(int dt) {
+    switch (dt) {
+    case RMSNORM_F32: return "fp32";
+    case RMSNORM_BF16: return "bf16";
+    case RMSNORM_F16: return "fp16";
+    case RMSNORM_BF16_W32: return "bf16, fp32 weight";
+    case RMSNORM_F16_W32: return "fp16, fp32 weight";
+    default: return "?";
+    }
+}
+
+static void note_generic(unsigned kind, int64_t N, int dt) {
+    if (!g_note_on.load(std::memory_order_relaxed)) return;
+    if (g_noted.fetch_or(kind, std::memory_order_relaxed) & kind) return;
+    const char *op = kind == NOTE_FWD ? "rmsnorm forward"
+                     : kind == NOTE_BWD ? "rmsnorm backward"
+                     : kind == NOTE_LN_FWD ? "layernorm forward" : "layernorm backward";
+    const bool whole = (N * elem_size(dt)) % 16 == 0;
+    std::fprintf(stderr,
+                 "librmsnorm_gb300: %s, N=%lld, %s: falling back to the generic kernel (%s); "
+                 "later such calls are not reported\n",
+                 op, (long long)N, dtype_name(dt),
+                 whole ? "the arrays are not all 16-byte aligned at one common offset"
+                       : "a row is not a whole number of 16-byte chunks");
+}
+
 // --------------------------------------------------------------- forward --
 
 // Quantised output of the forward (E4M3); qmode QOUT_NONE is the plain
@@ -699,6 +736,7 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     // the E4M3 kernels are compiled for the default plans and the generic one
     if (quant && force_plan >= 0 && plan.path != PATH_GENERIC && find_plan(plan.plan_id)->cmin == 0)
         return RMSNORM_ERR_UNSUPPORTED;
+    if (plan.path == PATH_GENERIC && force_plan < 0) note_generic(NOTE_FWD, N, dt);
     int stages = 0;
     int *status = nullptr;
     st = prepare_staged_fwd(M, N, dt, aligned, fused, false, q.qmode, force_plan, &plan, &stages, &status);
@@ -799,6 +837,7 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     if (e != cudaSuccess) return cuda_fail(e);
     st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, parts, cps, force_plan, force_ctas, &plan);
     if (st != RMSNORM_SUCCESS) return st;
+    if (plan.path == PATH_GENERIC && force_plan < 0) note_generic(NOTE_BWD, N, dt);
     bool packed = plan.packed != 0;
     if (force_packed == 0) packed = false;
     if (force_packed == 1 && plan.path == PATH_VECTOR) packed = true;
@@ -917,6 +956,7 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
     if (st != RMSNORM_SUCCESS) return st;
     // the LayerNorm forward is compiled for the default plans and the generic one
     if (plan.path == PATH_VECTOR && find_plan(plan.plan_id)->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
+    if (plan.path == PATH_GENERIC && force_plan < 0) note_generic(NOTE_LN_FWD, N, dt);
     int stages = 0;
     int *status = nullptr;
     st = prepare_staged_fwd(M, N, dt, aligned, fused, true, QOUT_NONE, force_plan, &plan, &stages, &status);
@@ -999,6 +1039,7 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
     if (e != cudaSuccess) return cuda_fail(e);
     st = select_plan(RMSNORM_OP_LN_BWD, M, N, dt, aligned, parts, cps, force_plan, force_ctas, &plan);
     if (st != RMSNORM_SUCCESS) return st;
+    if (plan.path == PATH_GENERIC && force_plan < 0) note_generic(NOTE_LN_BWD, N, dt);
     if (plan.path == PATH_STAGED) {
         const int64_t sm = staged_smem_bytes(*find_plan(plan.plan_id), N, (int)s, fused);
         if (sm > kMaxDynamicSmem) return RMSNORM_ERR_UNSUPPORTED;
@@ -1232,6 +1273,11 @@ const char *rmsnorm_status_string(rmsnorm_status_t status) {
 int rmsnorm_last_cuda_error(void) { return g_last_cuda_error; }
 
 int rmsnorm_self_check(void) { return self_check_impl(); }
+
+void rmsnorm_set_generic_note(int enabled) {
+    g_noted.store(0, std::memory_order_relaxed);
+    g_note_on.store(enabled ? 1 : 0, std::memory_order_relaxed);
+}
 
 int rmsnorm_device_status(int clear) {
     int dev = 0;

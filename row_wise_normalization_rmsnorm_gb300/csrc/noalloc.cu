@@ -2,20 +2,20 @@
 // cannot allocate device memory at call time.
 //
 // Who needs this: code that may not call cudaMalloc (or cudaMallocAsync)
-// when it runs, for example an inference engine that reserves all device
-// memory at start-up and forbids later allocation, a plug-in whose host
-// framework owns the allocator and hands the op no workspace, or code that
-// runs while another thread holds a global-mode stream capture, during
-// which cudaMalloc is not permitted. rmsnorm_bwd needs a workspace for its
-// per-CTA dW partial rows; this entry point takes it from a fixed array
-// compiled into the library instead of from the caller or an allocator.
+// when it runs, for example an inference or training engine that reserves
+// all device memory at start-up and forbids later allocation, or a plug-in
+// whose host framework owns the allocator and hands the op no workspace.
+// rmsnorm_bwd needs a workspace for its per-CTA dW partial rows; this entry
+// point takes it from a fixed array compiled into the library instead of
+// from the caller or an allocator.
 //
 // The array is a file-scope __device__ variable: every GPU on which the
 // library's kernels are loaded holds RMSNORM_NOALLOC_SCRATCH_BYTES of it
 // until the process exits. Host code must not pass the array's name to a
 // kernel: on the host that name is a stand-in object, not a device
 // address. The device address is looked up once per device with
-// cudaGetSymbolAddress, on that device's first call.
+// cudaGetSymbolAddress, on that device's first call, and kept for the life
+// of the process (a cudaDeviceReset would leave it stale).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -59,7 +59,8 @@ extern "C" rmsnorm_status_t rmsnorm_bwd_noalloc(const void *dy, const void *x, c
                                                 const float *rstd, void *dx, void *dw, int64_t M,
                                                 int64_t N, rmsnorm_dtype_t dt, float eps, float offset,
                                                 rmsnorm_stream_t stream) {
-    if (dt != RMSNORM_F32 && dt != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
+    // Every storage type rmsnorm_bwd takes is served; its own checks decide
+    // the arguments. Only the size is this entry point's to check (below).
     if (N < 1 || N > RMSNORM_MAX_N || M < 0) return RMSNORM_ERR_INVALID_ARG;
     void *scratch = nullptr;
     cudaError_t e = scratch_address(&scratch);

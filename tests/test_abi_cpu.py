@@ -282,3 +282,29 @@ def test_workspace_query_without_device_is_zero(rn):
         pytest.skip("host has a GPU")
     assert rn.rmsnorm_bwd_workspace_bytes(4096, 2048, 1) == 0
     assert rn.rmsnorm_bwd_workspace_bytes(0, 2048, 1) == 0
+
+
+def test_generic_note_is_optional_and_printed_once(rn, capfd):
+    """The generic-kernel note: off by default; once switched on, the first
+    call of a kind that falls to the generic kernel prints one line to
+    stderr and later ones print nothing; switching it on again re-arms it.
+    On a host without a GPU the call then fails at its launch (status 4)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host has a GPU: these addresses are not device memory")
+    L = rn.lib()
+    x, r = ctypes.c_void_p(258), ctypes.c_void_p(512)   # bf16 x not 16-byte aligned
+    L.rmsnorm_set_generic_note(0)
+    assert L.rmsnorm_fwd(x, None, x, r, 4, 8, 1, 1e-6, 0.0, None) == 4
+    assert "generic kernel" not in capfd.readouterr().err
+    L.rmsnorm_set_generic_note(1)
+    assert L.rmsnorm_fwd(x, None, x, r, 4, 8, 1, 1e-6, 0.0, None) == 4
+    err = capfd.readouterr().err
+    assert err.count("falling back to the generic kernel") == 1 and "N=8" in err and "bf16" in err
+    assert L.rmsnorm_fwd(x, None, x, r, 4, 8, 1, 1e-6, 0.0, None) == 4
+    assert "generic kernel" not in capfd.readouterr().err
+    # a row of 7 bf16 elements is not a whole number of 16-byte chunks
+    L.rmsnorm_set_generic_note(1)
+    assert L.rmsnorm_fwd(ctypes.c_void_p(256), None, ctypes.c_void_p(256), r, 4, 7, 1, 1e-6, 0.0, None) == 4
+    assert "whole number of 16-byte chunks" in capfd.readouterr().err
+    L.rmsnorm_set_generic_note(0)

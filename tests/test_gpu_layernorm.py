@@ -85,8 +85,6 @@ def _ln_check(rn, d, dt, eps=1e-5, offset=0.0, fused=False, offset_elems=0, expe
         # "vector": the fast paths (the backward may stage rows in shared memory)
         fast = ("vector", "staged") if expect_path == "vector" else (expect_path,)
         assert out["plan"]["path_name"] in fast and bo["plan"]["path_name"] in fast
-    if N >= 64:
-        assert needed <= max(2, M * N // 20000), needed
     return out, bo
 
 

@@ -111,6 +111,37 @@ MUTATIONS = {
     "ln_beta_takes_offset": ("const double bias = jb->beta ? load_elem(jb->wdtype, jb->beta, j) : 0.0;",
                              "const double bias = jb->beta ? jb->offset + load_elem(jb->wdtype, jb->beta, j) : 0.0;"),
     "fp8_zero_row_scale_zero": ("sc = amax > 0.0 ? 448.0 / amax : 1.0;", "sc = amax > 0.0 ? 448.0 / amax : 0.0;"),
+    # the tolerance scales the GPU checks are widened by
+    "cabs_not_mean": ("c /= (double)N;\n        cabs /= (double)N;",
+        "c /= (double)N;\n        cabs /= 1.0;"),
+    "dw_abs_signed": ("jb->dw_abs[j] += fabs(dyj * xhat);",
+        "jb->dw_abs[j] += dyj * xhat;"),
+    "dw_abs_double_counted": ("sa += jobs[t].dw_abs[j];",
+        "sa += 2.0 * jobs[t].dw_abs[j];"),
+    "dx_scale_drops_dres": ("rstd * (fabs(g) + fabs(xhat * c));\n            if (jb->dres) {\n                const double d = load_elem(jb->dtype, jb->dres, base + j);\n                dxj += d;\n                scale += fabs(d);",
+        "rstd * (fabs(g) + fabs(xhat * c));\n            if (jb->dres) {\n                const double d = load_elem(jb->dtype, jb->dres, base + j);\n                dxj += d;\n                scale += 0.0 * fabs(d);"),
+    "dx_scale_missing_xhat_c": ("double scale = rstd * (fabs(g) + fabs(xhat * c));",
+        "double scale = rstd * fabs(g);"),
+    "dx_scale_missing_rstd": ("double scale = rstd * (fabs(g) + fabs(xhat * c));",
+        "double scale = (fabs(g) + fabs(xhat * c));"),
+    "dx_cscale_missing_xhat": ("jb->dx_cscale[base + j] = rstd * fabs(xhat) * cabs;",
+        "jb->dx_cscale[base + j] = rstd * cabs;"),
+    "dx_cscale_signed_sum": ("cabs += fabs(g * (hv[j] * rstd));",
+        "cabs += g * (hv[j] * rstd);"),
+    "ln_dx_scale_missing_mean_g": ("double scale = rstd * (fabs(g) + fabs(mg) + fabs(xhat * c));",
+        "double scale = rstd * (fabs(g) + fabs(xhat * c));"),
+    "ln_dx_scale_drops_dres": ("rstd * (fabs(g) + fabs(mg) + fabs(xhat * c));\n            if (jb->dres) {\n                const double d = load_elem(jb->dtype, jb->dres, base + j);\n                dxj += d;\n                scale += fabs(d);",
+        "rstd * (fabs(g) + fabs(mg) + fabs(xhat * c));\n            if (jb->dres) {\n                const double d = load_elem(jb->dtype, jb->dres, base + j);\n                dxj += d;\n                scale += 0.0 * fabs(d);"),
+    "ln_cscale_missing_mean_abs_g": ("jb->dx_cscale[base + j] = rstd * (mgabs + fabs(xhat) * cabs);",
+        "jb->dx_cscale[base + j] = rstd * fabs(xhat) * cabs;"),
+    "ln_cscale_missing_xhat": ("jb->dx_cscale[base + j] = rstd * (mgabs + fabs(xhat) * cabs);",
+        "jb->dx_cscale[base + j] = rstd * (mgabs + cabs);"),
+    "ln_mean_abs_g_not_mean": ("mgabs /= (double)N;",
+        "mgabs /= 1.0;"),
+    "ln_dg_abs_signed": ("jb->dg_abs[j] += fabs(dyj * xhat);",
+        "jb->dg_abs[j] += dyj * xhat;"),
+    "ln_db_abs_signed": ("jb->db_abs[j] += fabs(dyj);",
+        "jb->db_abs[j] += dyj;"),
 }
 
 

@@ -693,3 +693,125 @@ def test_ln_bwd_param_grads_brute_force_and_given_stats():
     assert np.allclose(r["dg64"], dg, rtol=1e-13, atol=1e-13)
     assert np.allclose(r["db64"], db, rtol=1e-13, atol=1e-13)
     assert np.array_equal(r["dg"], oracle.bf16_round(r["dg64"]))
+
+
+# ---------------------------------------------------- tolerance scales --
+# The backward also returns the scales that widen the dx and dW checks in
+# the GPU parity tests: dx_scale = rstd (|g| + |xhat c|) [+ |dres|] (the
+# terms whose difference is dx), dx_cscale = rstd |xhat| (1/N) sum |g xhat|
+# (how far dx moves per unit relative error of the sum behind c) and
+# dw_abs = sum over rows of |dy xhat| (the scale of dW's summation error).
+# A scale that is too wide would let a wrong kernel pass, so each is pinned
+# to values worked out by hand below (not by re-running its formula).
+
+def test_bwd_tolerance_scales_hand_example():
+    # Both rows x = (3, 4), w = 1, offset 0, eps 0: rstd = sqrt(2)/5 and
+    # xhat = (3 sqrt(2)/5, 4 sqrt(2)/5).
+    #   row 0, dy = (1, -1): g xhat = (3, -4) sqrt(2)/5, so c = -sqrt(2)/10
+    #          and (1/N) sum |g xhat| = 7 sqrt(2)/10; |xhat c| = (0.12, 0.16)
+    #   row 1, dy = (-1, 2): g xhat = (-3, 8) sqrt(2)/5, so c = sqrt(2)/2
+    #          and (1/N) sum |g xhat| = 11 sqrt(2)/10; |xhat c| = (0.6, 0.8)
+    s2 = math.sqrt(2.0)
+    rs = s2 / 5
+    x = np.array([[3.0, 4.0], [3.0, 4.0]])
+    dy = np.array([[1.0, -1.0], [-1.0, 2.0]])
+    r = _bwd64(x, dy, np.ones(2), 0.0, 0.0)
+    np.testing.assert_allclose(r["dx64"], [[1.12 * rs, -0.84 * rs], [-1.6 * rs, 1.2 * rs]], rtol=1e-14)
+    np.testing.assert_allclose(r["dx_scale"], [[1.12 * rs, 1.16 * rs], [1.6 * rs, 2.8 * rs]], rtol=1e-14)
+    # rstd |xhat| cabs: row 0 (3, 4) 7/25 * rs ... = (0.84, 1.12) rs; row 1 (1.32, 1.76) rs
+    np.testing.assert_allclose(r["dx_cscale"], [[0.84 * rs, 1.12 * rs], [1.32 * rs, 1.76 * rs]], rtol=1e-14)
+    # column 0: |3| + |-3| (times sqrt(2)/5); column 1: |-4| + |8|. The signed
+    # sums are 0 and 4 sqrt(2)/5, so |dW| is not the scale.
+    np.testing.assert_allclose(r["dw_abs"], [6 * rs, 12 * rs], rtol=1e-14)
+    np.testing.assert_allclose(r["dw64"], [0.0, 4 * rs], rtol=1e-14, atol=1e-15)
+
+
+def test_bwd_tolerance_scales_with_dres_weight_and_offset():
+    # Row x = (3, 4), dy = (1, -1), w = (0.5, 1.5) with offset 1 (factor
+    # (1.5, 2.5)), dres = (0.5, -0.25): g = (1.5, -2.5),
+    # g xhat = (4.5, -10) sqrt(2)/5, c = -5.5 sqrt(2)/10 = -0.55 sqrt(2),
+    # (1/N) sum |g xhat| = 14.5 sqrt(2)/10; |xhat c| = (0.66, 0.88).
+    s2 = math.sqrt(2.0)
+    rs = s2 / 5
+    x = np.array([[3.0, 4.0]])
+    dy = np.array([[1.0, -1.0]])
+    w = np.array([0.5, 1.5])
+    dres = np.array([[0.5, -0.25]])
+    r = _bwd64(x, dy, w, 0.0, 1.0, dres=dres)
+    np.testing.assert_allclose(r["dx64"][0], [rs * (1.5 + 0.66) + 0.5, rs * (-2.5 + 0.88) - 0.25], rtol=1e-14)
+    np.testing.assert_allclose(r["dx_scale"][0], [rs * (1.5 + 0.66) + 0.5, rs * (2.5 + 0.88) + 0.25], rtol=1e-14)
+    # rstd |xhat| (1/N) sum |g xhat| = rs (3, 4) sqrt(2)/5 * 1.45 sqrt(2) = rs (1.74, 2.32)
+    np.testing.assert_allclose(r["dx_cscale"][0], [1.74 * rs, 2.32 * rs], rtol=1e-14)
+    # dW and its scale do not see the weight or the offset: sum |dy xhat|
+    np.testing.assert_allclose(r["dw_abs"], [3 * rs, 4 * rs], rtol=1e-14)
+
+
+def test_bwd_tolerance_scales_vanish_with_dy():
+    # dy = 0: dx = dres exactly, and the only scale left is |dres|
+    x = f64((3, 9), 40)
+    dres = f64((3, 9), 41)
+    r = _bwd64(x, np.zeros((3, 9)), f64(9, 42, 0.1, 1.0), 1e-3, 0.0, dres=dres)
+    np.testing.assert_array_equal(r["dx64"], dres)
+    np.testing.assert_array_equal(r["dx_scale"], np.abs(dres))
+    np.testing.assert_array_equal(r["dx_cscale"], np.zeros((3, 9)))
+    np.testing.assert_array_equal(r["dw_abs"], np.zeros(9))
+
+
+def test_bwd_tolerance_scales_bound_each_term():
+    # Random rows: each scale is at least the magnitude it bounds (the
+    # triangle inequality), and dw_abs is the brute-force sum of |dy xhat|.
+    x = f64((7, 33), 43)
+    dy = f64((7, 33), 44)
+    w = f64(33, 45, 0.1, 1.0)
+    dres = f64((7, 33), 46)
+    r = _bwd64(x, dy, w, 1e-6, 0.0, dres=dres)
+    assert np.all(np.abs(r["dx64"]) <= r["dx_scale"] * (1 + 1e-14))
+    rstd = 1 / np.sqrt(np.mean(x * x, axis=1) + 1e-6)
+    xhat = x * rstd[:, None]
+    g = dy * w[None, :]
+    c = np.mean(g * xhat, axis=1)
+    assert np.all(rstd[:, None] * np.abs(xhat * c[:, None]) <= r["dx_cscale"] * (1 + 1e-14))
+    brute = np.zeros(33)
+    for i in range(7):
+        for j in range(33):
+            brute[j] += abs(dy[i, j] * xhat[i, j])
+    np.testing.assert_allclose(r["dw_abs"], brute, rtol=1e-13)
+
+
+def test_ln_bwd_tolerance_scales_hand_example():
+    # gamma = 1, offset 0, eps 0.
+    #   row 0: x = (1, 1, 3, 3): mean 2, var 1, rstd 1, xhat = (-1, -1, 1, 1);
+    #          dy = (1, -2, 0, 3): mean(g) = 0.5, mean|g| = 1.5,
+    #          g xhat = (-1, 2, 0, 3): c = 1, mean|g xhat| = 1.5;
+    #          dx = g - 0.5 - xhat = (1.5, -1.5, -1.5, 1.5)
+    #   row 1: x = (0, 0, 0, 4): mean 1, var 3, rstd = 1/sqrt(3),
+    #          xhat = (-1, -1, -1, 3)/sqrt(3); dy = (1, 0, 0, 1):
+    #          mean(g) = mean|g| = 0.5, c = 1/(2 sqrt(3)), mean|g xhat| = 1/sqrt(3)
+    r3 = 1 / math.sqrt(3.0)
+    x = np.array([[1.0, 1.0, 3.0, 3.0], [0.0, 0.0, 0.0, 4.0]])
+    dy = np.array([[1.0, -2.0, 0.0, 3.0], [1.0, 0.0, 0.0, 1.0]])
+    r = oracle.ln_bwd(dy, x, np.ones(4), dtype="f64", eps=0.0, offset=0.0)
+    np.testing.assert_allclose(r["dx64"][0], [1.5, -1.5, -1.5, 1.5], rtol=1e-14)
+    # rstd (|g| + |mean g| + |xhat c|)
+    np.testing.assert_allclose(r["dx_scale"][0], [2.5, 3.5, 1.5, 4.5], rtol=1e-14)
+    np.testing.assert_allclose(r["dx_scale"][1], [r3 * (1 + 0.5 + 1 / 6), r3 * (0.5 + 1 / 6), r3 * (0.5 + 1 / 6),
+                                                  r3 * (1 + 0.5 + 0.5)], rtol=1e-14)
+    # rstd (mean|g| + |xhat| mean|g xhat|)
+    np.testing.assert_allclose(r["dx_cscale"][0], [3.0, 3.0, 3.0, 3.0], rtol=1e-14)
+    np.testing.assert_allclose(r["dx_cscale"][1], [r3 * (0.5 + 1 / 3)] * 3 + [r3 * 1.5], rtol=1e-14)
+    # dgamma: sum dy xhat = (-1 - r3, 2, 0, 3 + sqrt(3)); its scale sum |dy xhat|
+    np.testing.assert_allclose(r["dg64"], [-1 - r3, 2.0, 0.0, 3 + math.sqrt(3.0)], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(r["dg_abs"], [1 + r3, 2.0, 0.0, 3 + math.sqrt(3.0)], rtol=1e-14, atol=1e-15)
+    # dbeta: sum dy = (2, -2, 0, 4); its scale sum |dy| = (2, 2, 0, 4)
+    np.testing.assert_allclose(r["db64"], [2.0, -2.0, 0.0, 4.0], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(r["db_abs"], [2.0, 2.0, 0.0, 4.0], rtol=1e-14, atol=1e-15)
+
+
+def test_ln_bwd_tolerance_scale_takes_dres():
+    # the fused variant adds |dres| to the scale, as it adds dres to dx
+    x = np.array([[1.0, 1.0, 3.0, 3.0]])
+    dy = np.array([[1.0, -2.0, 0.0, 3.0]])
+    dres = np.array([[0.25, -0.5, 1.0, -2.0]])
+    r = oracle.ln_bwd(dy, x, np.ones(4), dtype="f64", eps=0.0, offset=0.0, dres=dres)
+    np.testing.assert_allclose(r["dx64"][0], [1.75, -2.0, -0.5, -0.5], rtol=1e-14)
+    np.testing.assert_allclose(r["dx_scale"][0], [2.75, 4.0, 2.5, 6.5], rtol=1e-14)
