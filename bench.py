@@ -383,6 +383,10 @@ def run_sweep(args):
             # backward reads dy, x, gamma, mean, rstd, writes dx, and moves
             # the [P, 2N] partial rows and dgamma, dbeta
             bvec = (0.1 * mk(N).float()).to(td)
+            if mis:   # at the rows' offset, like w
+                bb = torch.empty(N + 1, dtype=td, device=dev)
+                bb[1:].copy_(bvec)
+                bvec = bb[1:]
             mean = torch.empty(M, dtype=torch.float32, device=dev)
             dbv = torch.empty_like(bvec)
             lnb = rn.layernorm_bwd_workspace_bytes(M, N, td)
@@ -546,13 +550,13 @@ def main():
     bargs = (dy.data_ptr(), x.data_ptr(), w.data_ptr(), rstd.data_ptr(), dx.data_ptr(), dw.data_ptr(),
              ws.data_ptr(), ws_bytes, M, N, 1, eps, 0.0, hs)
     host = {}
-    for name, fn, args in (("fwd", L.rmsnorm_fwd, fargs), ("bwd", L.rmsnorm_bwd, bargs)):
+    for name, fn, cargs in (("fwd", L.rmsnorm_fwd, fargs), ("bwd", L.rmsnorm_bwd, bargs)):
         per = []
         for _ in range(20):
             torch.cuda.synchronize()
             for _ in range(50):
                 t0 = time.perf_counter_ns()
-                st = fn(*args)
+                st = fn(*cargs)
                 per.append((time.perf_counter_ns() - t0) / 1e3)
                 assert st == 0, st
         torch.cuda.synchronize()

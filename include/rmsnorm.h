@@ -34,11 +34,18 @@
  *   - x, residual, y, dy, dx, residual_out, dresidual_out share the
  *     activations' storage type `dt`; w and dw have the same type, or fp32
  *     when `dt` carries RMSNORM_WEIGHT_F32. Pointers must be aligned to
- *     their element size; 16-byte alignment of every pointer (and
- *     N * sizeof(activation) % 16 == 0) selects the vectorised kernels,
- *     anything else the generic kernels. With an fp32 weight only the
- *     default plans are compiled: forcing an alternative plan id returns
- *     UNSUPPORTED.
+ *     their element size. With N * sizeof(activation) % 16 == 0, the
+ *     vectorised kernels serve every call whose pointers are all 16-byte
+ *     aligned, and also every call whose row arrays (and the weight, in the
+ *     activations' type) all sit at one common offset past a 16-byte
+ *     boundary (e.g. each one element past an aligned allocation): a row's
+ *     head and tail, which share 16-byte blocks with the neighbouring rows,
+ *     are read as whole aligned blocks (never past the 16 bytes that hold
+ *     one of the row's elements), joined into one chunk, and written back
+ *     element by element; no element outside the arrays is ever written.
+ *     Anything else takes the generic kernels. With an fp32 weight only the default plans are compiled
+ *     (forcing an alternative plan id returns UNSUPPORTED) and only aligned
+ *     rows are vectorised.
  *   - Every call is asynchronous on `stream` (NULL = legacy default
  *     stream). The library never synchronises and never copies between
  *     host and device.
@@ -266,11 +273,29 @@ rmsnorm_status_t rmsnorm_bwd_noalloc(const void *dy, const void *x, const void *
 
 /*
  * Bytes of workspace the backward needs for (M, N, dt) on the current
- * device: (number of persistent CTAs) * N * 4, rounded up to 256 (FlyDSL
- * PR #855, Runtime configuration and ownership). Returns 0 for M == 0 and
- * for invalid arguments or when no CUDA device is usable.
+ * device, whatever the call's pointers and fusion: the largest need over
+ * the row layouts (aligned, at a common offset, generic) and the plain and
+ * fused variants, so one allocation of this size serves every call. A
+ * call's own need is (dW partial rows) * (row columns) * 4 rounded up to
+ * 256 (FlyDSL PR #855, Runtime configuration and ownership: one fp32
+ * partial row per program), where the partial rows are the persistent CTAs
+ * (or clusters) and the row columns N; rmsnorm_bwd_call_workspace_bytes
+ * gives it exactly.
+ * Returns 0 for M == 0 and for invalid arguments or when no CUDA device is
+ * usable.
  */
 size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt);
+
+/*
+ * Exact workspace need of one rmsnorm_bwd call (fused == 0) or
+ * rmsnorm_add_bwd call (fused != 0) with these arrays on the current
+ * device: the plan that call selects. dresidual_out is used only when
+ * fused (may be NULL). Returns 0 for the non-affine backward (w == NULL,
+ * no workspace), M == 0, invalid arguments or no usable device.
+ */
+size_t rmsnorm_bwd_call_workspace_bytes(const void *dy, const void *dresidual_out, const void *x,
+                                        const void *w, const void *dx, int64_t M, int64_t N,
+                                        rmsnorm_dtype_t dt, int fused);
 
 /* ------------------------------------------------------------------------
  * Plans: which kernel runs. Exposed for tests and benchmarks (the analogue
@@ -307,6 +332,12 @@ typedef struct {
                                    forward): units walking the rows, CTAs or
                                    clusters; backward: dW partial rows          */
     int64_t workspace_bytes;    /* backward only                                */
+    int32_t peel;               /* rows at a common offset: elements of the
+                                   16-byte block holding a row's first element
+                                   that precede it (the vectorised kernels join
+                                   the row's head and tail into one chunk); 0 for
+                                   aligned rows and the generic kernels         */
+    int32_t reserved;
 } rmsnorm_plan_t;
 
 #define RMSNORM_OP_FWD 0
@@ -314,8 +345,10 @@ typedef struct {
 #define RMSNORM_OP_LN_BWD 2 /* LayerNorm backward (its forward uses RMSNORM_OP_FWD plans) */
 
 /*
- * Host-only plan query: no CUDA call, usable without a GPU. `aligned` says
- * whether every pointer is 16-byte aligned; `num_sms` is the device's SM
+ * Host-only plan query: no CUDA call, usable without a GPU. `aligned` gives
+ * the row layout: 1 every pointer 16-byte aligned; 1 + k every row array
+ * (and the weight) k elements past a 16-byte boundary; 0 anything else
+ * (the generic kernels). `num_sms` is the device's SM
  * count and `ctas_per_sm` the resident backward CTAs per SM (<= 0: the
  * plan's nominal value). force_plan < 0 picks the default plan; otherwise
  * the plan with that id (UNSUPPORTED if it cannot serve N/dt/alignment).

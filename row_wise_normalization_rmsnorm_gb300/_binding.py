@@ -48,6 +48,8 @@ class Plan(ctypes.Structure):
         ("cluster_size", ctypes.c_int32),
         ("ws_rows", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
+        ("peel", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:
@@ -68,6 +70,7 @@ SIGNATURES = {
     "rmsnorm_add_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp]),
     "rmsnorm_add_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i, _f, _f, _vp]),
     "rmsnorm_bwd_workspace_bytes": (_sz, [_i64, _i64, _i]),
+    "rmsnorm_bwd_call_workspace_bytes": (_sz, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i]),
     "rmsnorm_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _f, _f, _vp]),
     "rmsnorm_plan_query": (_i, [_i, _i64, _i64, _i, _i, _i, _i, _i, _i, _PPlan]),
     "rmsnorm_plan_count": (_i, []),
@@ -327,7 +330,9 @@ def rmsnorm_bwd_workspace_bytes(M: int, N: int, dtype) -> int:
 
 def plan_query(op: int, M: int, N: int, dtype: int, *, aligned: bool = True, num_sms: int = 152,
                ctas_per_sm: int = 0, force_plan: int = -1, force_ctas: int = 0) -> dict:
-    """Host-only plan selection (no GPU needed)."""
+    """Host-only plan selection (no GPU needed). aligned: True (1) 16-byte
+    aligned rows, False (0) the generic kernels, 1 + k rows at a common offset
+    of k elements past a 16-byte boundary."""
     p = Plan()
     st = lib().rmsnorm_plan_query(op, M, N, dtype, int(aligned), num_sms, ctas_per_sm, force_plan, force_ctas,
                                   ctypes.byref(p))

@@ -13,6 +13,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <initializer_list>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -117,12 +118,13 @@ static int generic_bwd_cache(int path, int64_t N, int es, bool partials, int cps
 }
 
 // A staged plan's shared memory: `depth` stages of x and dy (and dres for
-// the fused variant) rows of es-byte elements, or of one CTA's slice (a
-// cs-th, rounded up to whole chunks) of a row shared by a cluster; the
-// LayerNorm's re-read schedule also keeps (its slice of) gamma there.
-static int64_t staged_smem_at(const PlanDesc &d, int64_t N, int es, bool fused, int depth) {
-    const int64_t C = (N * es + 15) / 16;
-    const int64_t row = (C + d.cs - 1) / d.cs * 16;
+// the fused variant) rows of C chunks, or of one CTA's slice (a cs-th,
+// rounded up to whole chunks) of a row shared by a cluster, each row buffer
+// one slot longer for rows at a common offset (peel > 0: aligned chunk C,
+// which wraps chunk 0); the LayerNorm's re-read schedule also keeps (its
+// slice of) gamma there.
+static int64_t staged_smem_at(const PlanDesc &d, int64_t C, int peel, bool fused, int depth) {
+    const int64_t row = ((C + d.cs - 1) / d.cs + (peel > 0 ? 1 : 0)) * 16;
     const int64_t gamma = d.path == PATH_RESTAGED && d.op == OP_LN_BWD ? row : 0;
     // a stage holds x and dy (and dres) rows; the staged forward's x (and residual)
     const int rows = d.op == OP_FWD_STAGED ? (fused ? 2 : 1) : (fused ? 3 : 2);
@@ -131,16 +133,16 @@ static int64_t staged_smem_at(const PlanDesc &d, int64_t N, int es, bool fused, 
 
 // Stages a call takes: the plan's depth, or fewer (at least two) where the
 // rows (three a stage for the fused variant) would not fit; 0: none fits.
-static int staged_depth(const PlanDesc &d, int64_t N, int es, bool fused) {
+static int staged_depth(const PlanDesc &d, int64_t C, int peel, bool fused) {
     for (int k = d.depth; k >= 2; --k)
-        if (staged_smem_at(d, N, es, fused, k) <= kMaxDynamicSmem) return k;
+        if (staged_smem_at(d, C, peel, fused, k) <= kMaxDynamicSmem) return k;
     return 0;
 }
 
 // Shared memory at the stages a call takes (above the limit when none fits).
-static int64_t staged_smem_bytes(const PlanDesc &d, int64_t N, int es, bool fused) {
-    const int k = staged_depth(d, N, es, fused);
-    return staged_smem_at(d, N, es, fused, k > 0 ? k : 2);
+static int64_t staged_smem_bytes(const PlanDesc &d, int64_t C, int peel, bool fused) {
+    const int k = staged_depth(d, C, peel, fused);
+    return staged_smem_at(d, C, peel, fused, k > 0 ? k : 2);
 }
 
 static int nominal_ctas_per_sm(const PlanDesc &d) {
@@ -160,10 +162,12 @@ static int bwd_smem_bytes(const PlanDesc &d, int64_t N) {
 // Chunks one plan can hold per row.
 static int64_t plan_capacity(const PlanDesc &d) { return (int64_t)d.tpr * d.v * d.cs; }
 
-// Pure selection: no CUDA calls. max_parts is the largest useful number of
-// backward dW partial rows: resident CTAs (or, for cluster plans, resident
-// clusters) on the device; ctas_per_sm is reported only.
-static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool aligned, int64_t max_parts,
+// Pure selection: no CUDA calls. `peel` is the call's row layout
+// (row_layout: 0 aligned, > 0 rows at a common offset, < 0 generic only).
+// max_parts is the largest useful number of backward dW partial rows:
+// resident CTAs (or, for cluster plans, resident clusters) on the device;
+// ctas_per_sm is reported only.
+static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, int peel, int64_t max_parts,
                                     int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
     if (!out) return RMSNORM_ERR_INVALID_ARG;
     if (op != RMSNORM_OP_FWD && op != RMSNORM_OP_BWD && op != RMSNORM_OP_LN_BWD) return RMSNORM_ERR_INVALID_ARG;
@@ -171,8 +175,8 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (max_parts < 1) return RMSNORM_ERR_INVALID_ARG;
     const int s = elem_size(dt);
-    const bool vec_ok = aligned && (N * s) % 16 == 0;
-    const int64_t C = vec_ok ? N * s / 16 : 0;
+    const bool vec_ok = peel >= 0 && (N * s) % 16 == 0 && peel < 16 / s;
+    const int64_t C = vec_ok ? N * s / 16 : 0;  // 16-byte chunks a row holds
 
     const PlanDesc *d = nullptr;
     if (force_plan >= 0) {
@@ -198,6 +202,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
 
     std::memset(out, 0, sizeof(*out));
     out->path = staged_path(d->path) ? PATH_STAGED : d->path;  // the ABI names one staged path
+    out->peel = (d->path != PATH_GENERIC && peel > 0) ? peel : 0;
     out->plan_id = d->id;
     out->threads_per_row = d->path == PATH_GENERIC ? 256 : d->tpr;
     out->chunks_per_thread = d->v;
@@ -222,7 +227,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, bool a
     // static arrays (a few KB at most)
     if (staged_path(d->path)) {
         // the plain variant's stages; the fused one is checked by the backward
-        const int64_t sm = staged_smem_bytes(*d, N, s, false);
+        const int64_t sm = staged_smem_bytes(*d, C, out->peel, false);
         if (sm > kMaxDynamicSmem) return RMSNORM_ERR_UNSUPPORTED;
         out->smem_bytes = (int32_t)sm;
     }
@@ -400,11 +405,11 @@ static int launch_bwd_dt(int dt, int plan_id, bool fused, bool packed, const Bwd
 
 // dW is written in the weight's storage type.
 static int launch_finalize_dt(int dt, const float *ws, int parts, int ncols, void *out0, void *out1, int split,
-                              void *stream, bool serial) {
+                              int peel, void *stream, bool serial) {
     switch (kind_of(dt)) {
-    case 1: return launch_dw_finalize_bf16(ws, parts, ncols, out0, out1, split, stream, serial);
-    case 2: return launch_dw_finalize_f16(ws, parts, ncols, out0, out1, split, stream, serial);
-    default: return launch_dw_finalize_f32(ws, parts, ncols, out0, out1, split, stream, serial);
+    case 1: return launch_dw_finalize_bf16(ws, parts, ncols, out0, out1, split, peel, stream, serial);
+    case 2: return launch_dw_finalize_f16(ws, parts, ncols, out0, out1, split, peel, stream, serial);
+    default: return launch_dw_finalize_f32(ws, parts, ncols, out0, out1, split, peel, stream, serial);
     }
 }
 
@@ -439,7 +444,7 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
     // (a staged plan's rows may need less than its capacity: the occupancy
     // query is capped at the largest shared memory a CTA may take)
     const int smem = staged_path(d.path)
-                         ? (int)std::min<int64_t>(staged_smem_bytes(d, nmax, elem_size(dt), fused), kMaxDynamicSmem)
+                         ? (int)std::min<int64_t>(staged_smem_bytes(d, plan_capacity(d), 1, fused), kMaxDynamicSmem)
                          : bwd_smem_bytes(d, nmax);
     int best = 1 << 30;
     for (int pk = 0; pk < 2; ++pk) {
@@ -489,6 +494,35 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
 
 static bool aligned_to(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
+// How a call's row arrays (and its weight, when given) sit in memory:
+//   0   every one 16-byte aligned: the vectorised kernels;
+//   k   every one k elements past a 16-byte boundary (one common offset),
+//       rows of whole 16-byte chunks, the weight in the activations' type:
+//       the vectorised kernels, each row spanning one chunk more, the two
+//       edge chunks split with the neighbouring rows;
+//  -1   anything else: the generic kernels.
+// Rows of whole chunks keep every row at the first row's offset.
+static int row_layout(int dt, int64_t N, std::initializer_list<const void *> rows, const void *w) {
+    const int s = elem_size(dt);
+    if ((N * s) % 16 != 0) return -1;
+    const uintptr_t a = (uintptr_t)*rows.begin() & 15u;
+    for (const void *p : rows)
+        if (((uintptr_t)p & 15u) != a) return -1;
+    if (w && ((uintptr_t)w & 15u) != a) return -1;
+    if (a == 0) return 0;
+    if (mixed_kind(kind_of(dt))) return -1;  // an fp32 weight: aligned rows only
+    return (int)(a / (uintptr_t)s);
+}
+
+// A row pointer as the vectorised kernels take it: moved back to the
+// 16-byte boundary below the rows' common offset.
+static const void *to_chunk_base(const void *p, int peel, int es) {
+    return (p && peel > 0) ? static_cast<const char *>(p) - (ptrdiff_t)peel * es : p;
+}
+static void *to_chunk_base(void *p, int peel, int es) {
+    return (p && peel > 0) ? static_cast<char *>(p) - (ptrdiff_t)peel * es : p;
+}
+
 static bool finite_scalar(float v) { return std::isfinite(v); }
 
 // Resident units (CTAs, or clusters) of a staged forward plan on the
@@ -513,8 +547,7 @@ static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d,
     if (!k) return cudaErrorInvalidDeviceFunction;
     cudaError_t e = (cudaError_t)allow_staged_smem(k);
     if (e != cudaSuccess) return e;
-    const int64_t nmax = plan_capacity(d) * (16 / elem_size(dt));
-    const int smem = (int)std::min<int64_t>(staged_smem_bytes(d, nmax, elem_size(dt), fused), kMaxDynamicSmem);
+    const int smem = (int)std::min<int64_t>(staged_smem_bytes(d, plan_capacity(d), 1, fused), kMaxDynamicSmem);
     int n = 0;
     if (d.cs > 1) {
         cudaLaunchConfig_t cfg = {};
@@ -544,15 +577,16 @@ static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d,
 // A forward on a staged plan: the grid becomes the resident units walking
 // the rows, and the stages in use, the shared memory and the status word
 // are set. Other plans are left as they are.
-static rmsnorm_status_t prepare_staged_fwd(int64_t M, int64_t N, int dt, bool aligned, bool fused, bool ln,
+static rmsnorm_status_t prepare_staged_fwd(int64_t M, int64_t N, int dt, int peel, bool fused, bool ln,
                                            int qmode, int force_plan, rmsnorm_plan_t *plan, int *stages,
                                            int **status) {
     *stages = 0;
     *status = nullptr;
     const PlanDesc *d = find_plan(plan->plan_id);
     if (!d || d->op != OP_FWD_STAGED) return RMSNORM_SUCCESS;
-    const int es = elem_size(dt);
-    const int depth = staged_depth(*d, N, es, fused);
+    const int64_t C = N * elem_size(dt) / 16;
+    const int pk = peel > 0 ? peel : 0;
+    const int depth = staged_depth(*d, C, pk, fused);
     if (depth == 0) return RMSNORM_ERR_UNSUPPORTED;
     int dev = 0, sms = 0;
     cudaError_t e = device_sms(&dev, &sms);
@@ -560,9 +594,9 @@ static rmsnorm_status_t prepare_staged_fwd(int64_t M, int64_t N, int dt, bool al
     int parts = 1;
     e = staged_fwd_parts(dev, sms, dt, *d, fused, ln, qmode, &parts);
     if (e != cudaSuccess) return cuda_fail(e);
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, parts, 0, force_plan, 0, plan);
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, parts, 0, force_plan, 0, plan);
     if (st != RMSNORM_SUCCESS) return st;
-    plan->smem_bytes = (int32_t)staged_smem_bytes(*d, N, es, fused);
+    plan->smem_bytes = (int32_t)staged_smem_bytes(*d, C, pk, fused);
     e = status_word(dev, status);
     if (e != cudaSuccess) return cuda_fail(e);
     *stages = depth;
@@ -727,11 +761,15 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
         return RMSNORM_ERR_INVALID_ARG;
     if (fused && (!aligned_to(residual, s) || !aligned_to(residual_out, s))) return RMSNORM_ERR_INVALID_ARG;
 
-    bool aligned = aligned_to(x, 16) && (!w || aligned_to(w, 16)) && aligned_to(y, 16);
-    if (fused) aligned = aligned && aligned_to(residual, 16) && aligned_to(residual_out, 16);
+    int peel = fused ? row_layout(dt, N, {x, y, residual, residual_out}, w) : row_layout(dt, N, {x, y}, w);
+    if (quant) {
+        // E4M3 output (one byte an element): 16-byte aligned rows only
+        const int in = fused ? row_layout(dt, N, {x, residual, residual_out}, w) : row_layout(dt, N, {x}, w);
+        peel = (in == 0 && aligned_to(y, 16)) ? 0 : -1;
+    }
 
     rmsnorm_plan_t plan;
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, 1, 0, force_plan, 0, &plan);
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, 1, 0, force_plan, 0, &plan);
     if (st != RMSNORM_SUCCESS) return st;
     // the E4M3 kernels are compiled for the default plans and the generic one
     if (quant && force_plan >= 0 && plan.path != PATH_GENERIC && find_plan(plan.plan_id)->cmin == 0)
@@ -739,15 +777,20 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (plan.path == PATH_GENERIC && force_plan < 0) note_generic(NOTE_FWD, N, dt);
     int stages = 0;
     int *status = nullptr;
-    st = prepare_staged_fwd(M, N, dt, aligned, fused, false, q.qmode, force_plan, &plan, &stages, &status);
+    st = prepare_staged_fwd(M, N, dt, peel, fused, false, q.qmode, force_plan, &plan, &stages, &status);
     if (st != RMSNORM_SUCCESS) return st;
 
+    // rows at a common offset: every row pointer moved back to the 16-byte
+    // boundary below it (plan.peel is 0 for aligned rows and the generic kernels)
+    const int pl = plan.peel;
+    const int es = (int)s;
     FwdParams p;
-    p.x = x;
-    p.residual = residual;
-    p.w = w;
-    p.y = y;
-    p.residual_out = residual_out;
+    p.x = to_chunk_base(x, pl, es);
+    p.residual = to_chunk_base(residual, pl, es);
+    p.w = to_chunk_base(w, pl, es);
+    p.y = to_chunk_base(y, pl, es);
+    p.residual_out = to_chunk_base(residual_out, pl, es);
+    p.peel = pl;
     p.rstd = rstd;
     p.M = M;
     p.N = (int)N;
@@ -791,6 +834,39 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
 
 // -------------------------------------------------------------- backward --
 
+// The plan a backward call (op RMSNORM_OP_BWD or RMSNORM_OP_LN_BWD) runs on
+// the current device: the row layout of its arrays, the table entry, the
+// CTA count from the device's occupancy, and a staged plan's shared memory.
+// The entry points and the exact workspace query share it.
+struct BwdCall {
+    rmsnorm_plan_t plan;
+    const PlanDesc *d;
+    int dev, sms, cps;
+};
+
+static rmsnorm_status_t plan_bwd_call(int op, const void *dy, const void *dres, const void *x, const void *w,
+                                      const void *dx, int64_t M, int64_t N, int dt, bool fused, int force_plan,
+                                      int force_ctas, BwdCall *c) {
+    const int peel = dres ? row_layout(dt, N, {dy, x, dx, dres}, w) : row_layout(dt, N, {dy, x, dx}, w);
+    cudaError_t e = device_sms(&c->dev, &c->sms);
+    if (e != cudaSuccess) return cuda_fail(e);
+    rmsnorm_status_t st = select_plan(op, M, N, dt, peel, 1, 0, force_plan, force_ctas, &c->plan);
+    if (st != RMSNORM_SUCCESS) return st;
+    c->d = find_plan(c->plan.plan_id);
+    const int64_t C = N * elem_size(dt) / 16;
+    if (staged_path(c->d->path) && staged_smem_bytes(*c->d, C, c->plan.peel, fused) > kMaxDynamicSmem)
+        return RMSNORM_ERR_UNSUPPORTED;
+    int parts = 1;
+    c->cps = 1;
+    e = bwd_max_parts(c->dev, c->sms, dt, *c->d, N, fused, &parts, &c->cps);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = select_plan(op, M, N, dt, peel, parts, c->cps, force_plan, force_ctas, &c->plan);
+    if (st != RMSNORM_SUCCESS) return st;
+    // the stages this call's rows take (the fused variant holds three rows a stage)
+    if (c->plan.path == PATH_STAGED) c->plan.smem_bytes = (int32_t)staged_smem_bytes(*c->d, C, c->plan.peel, fused);
+    return RMSNORM_SUCCESS;
+}
+
 static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x, const void *w,
                                  const float *rstd, void *dx, void *dw, void *workspace, size_t ws_bytes,
                                  int64_t M, int64_t N, int dt, float eps, float offset, cudaStream_t stream,
@@ -820,33 +896,19 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
         !aligned_to(dx, s) || !aligned_to(rstd, 4) || (dres && !aligned_to(dres, s)))
         return RMSNORM_ERR_INVALID_ARG;
     if (workspace && !aligned_to(workspace, 16)) return RMSNORM_ERR_WORKSPACE;
-    bool aligned = aligned_to(dy, 16) && aligned_to(x, 16) && (!affine || aligned_to(w, 16)) && aligned_to(dx, 16);
-    if (dres) aligned = aligned && aligned_to(dres, 16);
 
-    int dev = 0, sms = 0;
-    cudaError_t e = device_sms(&dev, &sms);
-    if (e != cudaSuccess) return cuda_fail(e);
-    rmsnorm_plan_t plan;
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, 1, 0, force_plan, force_ctas, &plan);
+    BwdCall call;
+    rmsnorm_status_t st = plan_bwd_call(RMSNORM_OP_BWD, dy, dres, x, w, dx, M, N, dt, fused, force_plan,
+                                        force_ctas, &call);
     if (st != RMSNORM_SUCCESS) return st;
-    const PlanDesc *d = find_plan(plan.plan_id);
-    if (staged_path(d->path) && staged_smem_bytes(*d, N, (int)s, fused) > kMaxDynamicSmem)
-        return RMSNORM_ERR_UNSUPPORTED;
-    int parts = 1, cps = 1;
-    e = bwd_max_parts(dev, sms, dt, *d, N, fused, &parts, &cps);
-    if (e != cudaSuccess) return cuda_fail(e);
-    st = select_plan(RMSNORM_OP_BWD, M, N, dt, aligned, parts, cps, force_plan, force_ctas, &plan);
-    if (st != RMSNORM_SUCCESS) return st;
+    rmsnorm_plan_t &plan = call.plan;
+    const PlanDesc *d = call.d;
+    cudaError_t e;
     if (plan.path == PATH_GENERIC && force_plan < 0) note_generic(NOTE_BWD, N, dt);
     bool packed = plan.packed != 0;
     if (force_packed == 0) packed = false;
     if (force_packed == 1 && plan.path == PATH_VECTOR) packed = true;
-    if (plan.path == PATH_STAGED) {
-        packed = true;  // the staged kernel has the packed variant only
-        const int64_t sm = staged_smem_bytes(*d, N, (int)s, fused);
-        if (sm > kMaxDynamicSmem) return RMSNORM_ERR_UNSUPPORTED;
-        plan.smem_bytes = (int32_t)sm;
-    }
+    if (plan.path == PATH_STAGED) packed = true;  // the staged kernel has the packed variant only
     plan.packed = packed ? 1 : 0;
 
     float *ws = static_cast<float *>(workspace);
@@ -864,30 +926,35 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     }
 
     int *status = nullptr;
-    e = status_word(dev, &status);
+    e = status_word(call.dev, &status);
     if (e != cudaSuccess) {
         if (owned) cudaFreeAsync(ws, stream);
         return cuda_fail(e);
     }
 
+    // rows at a common offset: every row pointer moved back to the 16-byte
+    // boundary below it (the partial rows come out rotated by pl columns)
+    const int pl = plan.peel;
+    const int es = (int)s;
     BwdParams p;
     p.status = status;
-    p.dy = dy;
-    p.x = x;
-    p.w = w;
+    p.dy = to_chunk_base(dy, pl, es);
+    p.x = to_chunk_base(x, pl, es);
+    p.w = to_chunk_base(w, pl, es);
     p.rstd = rstd;
-    p.dres = dres;
-    p.dx = dx;
+    p.dres = to_chunk_base(dres, pl, es);
+    p.dx = to_chunk_base(dx, pl, es);
     p.ws = ws;
     p.mean = nullptr;
     p.M = M;
     p.N = (int)N;
     p.offset = offset;
-    p.stages = staged_path(d->path) ? staged_depth(*d, N, (int)s, fused) : 0;
+    p.peel = pl;
+    p.stages = staged_path(d->path) ? staged_depth(*d, N * es / 16, pl, fused) : 0;
     int le = launch_bwd_dt(dt, plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream);
     if (le == 0 && event_after_main) le = (int)cudaEventRecord(static_cast<cudaEvent_t>(event_after_main), stream);
     if (le == 0 && affine)
-        le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)N, dw, nullptr, (int)N, stream,
+        le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)N, dw, nullptr, (int)N, pl, stream,
                                 event_after_main != nullptr);
     if (owned) {
         cudaError_t fe = cudaFreeAsync(ws, stream);
@@ -899,32 +966,44 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
 }
 
 // Bytes of workspace a backward (op RMSNORM_OP_BWD or RMSNORM_OP_LN_BWD)
-// needs on the current device: the largest need over the aligned and generic
-// plans and the plain and fused variants, so one size serves every call.
+// needs on the current device: the largest need over the row layouts
+// (aligned, at a common offset, generic) and the plain and fused variants,
+// so one size serves every call.
 static size_t bwd_workspace_bytes(int op, int64_t M, int64_t N, int dt) {
     if (M <= 0 || N < 1 || N > RMSNORM_MAX_N || !valid_dtype(dt)) return 0;
     if (M > 0x7fffffffLL || !table_ok()) return 0;
     int dev = 0, sms = 0;
     if (device_sms(&dev, &sms) != cudaSuccess) return 0;
     size_t best = 0;
-    // The largest requirement over the aligned and generic plans and the
-    // plain and fused variants, so one size serves every call.
-    for (int aligned = 0; aligned < 2; ++aligned) {
+    // (every common offset gives the same plan: rows one chunk longer)
+    for (int layout = -1; layout <= 1; ++layout) {
         for (int fused = 0; fused < 2; ++fused) {
             rmsnorm_plan_t plan;
-            if (select_plan(op, M, N, dt, aligned != 0, 1, 0, -1, 0, &plan) != RMSNORM_SUCCESS)
+            if (select_plan(op, M, N, dt, layout, 1, 0, -1, 0, &plan) != RMSNORM_SUCCESS)
                 return 0;
             int parts = 1, cps = 1;
             if (bwd_max_parts(dev, sms, dt, *find_plan(plan.plan_id), N, fused != 0, &parts, &cps) !=
                 cudaSuccess)
                 return 0;
-            if (select_plan(op, M, N, dt, aligned != 0, parts, cps, -1, 0, &plan) !=
-                RMSNORM_SUCCESS)
+            if (select_plan(op, M, N, dt, layout, parts, cps, -1, 0, &plan) != RMSNORM_SUCCESS)
                 return 0;
             if ((size_t)plan.workspace_bytes > best) best = (size_t)plan.workspace_bytes;
         }
     }
     return best;
+}
+
+// Bytes of workspace one RMSNorm backward call with these arrays needs on
+// the current device (the plan the call itself selects); 0 without dW.
+static size_t call_workspace_bytes(const void *dy, const void *dres, const void *x, const void *w, const void *dx,
+                                   int64_t M, int64_t N, int dt, bool fused) {
+    if (!w || !dy || !x || !dx || M <= 0 || M > 0x7fffffffLL || N < 1 || N > RMSNORM_MAX_N) return 0;
+    if (!valid_dtype(dt) || !table_ok()) return 0;
+    BwdCall call;
+    if (plan_bwd_call(RMSNORM_OP_BWD, dy, fused ? dres : nullptr, x, w, dx, M, N, dt, fused, -1, 0, &call) !=
+        RMSNORM_SUCCESS)
+        return 0;
+    return (size_t)call.plan.workspace_bytes;
 }
 
 // ------------------------------------------------------------- LayerNorm --
@@ -947,29 +1026,32 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
         !aligned_to(mean, 4) || !aligned_to(rstd, 4))
         return RMSNORM_ERR_INVALID_ARG;
     if (fused && (!aligned_to(residual, s) || !aligned_to(residual_out, s))) return RMSNORM_ERR_INVALID_ARG;
-    bool aligned = aligned_to(x, 16) && aligned_to(y, 16) && (!gamma || aligned_to(gamma, 16)) &&
-                   (!beta || aligned_to(beta, 16));
-    if (fused) aligned = aligned && aligned_to(residual, 16) && aligned_to(residual_out, 16);
+    // gamma and beta must share the rows' offset (beta as a second "row")
+    int peel = fused ? row_layout(dt, N, {x, y, residual, residual_out}, gamma)
+                     : row_layout(dt, N, {x, y}, gamma);
+    if (peel >= 0 && beta && row_layout(dt, N, {x, beta}, nullptr) != peel) peel = -1;
 
     rmsnorm_plan_t plan;
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, aligned, 1, 0, force_plan, 0, &plan);
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, 1, 0, force_plan, 0, &plan);
     if (st != RMSNORM_SUCCESS) return st;
     // the LayerNorm forward is compiled for the default plans and the generic one
     if (plan.path == PATH_VECTOR && find_plan(plan.plan_id)->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
     if (plan.path == PATH_GENERIC && force_plan < 0) note_generic(NOTE_LN_FWD, N, dt);
     int stages = 0;
     int *status = nullptr;
-    st = prepare_staged_fwd(M, N, dt, aligned, fused, true, QOUT_NONE, force_plan, &plan, &stages, &status);
+    st = prepare_staged_fwd(M, N, dt, peel, fused, true, QOUT_NONE, force_plan, &plan, &stages, &status);
     if (st != RMSNORM_SUCCESS) return st;
 
+    const int pl = plan.peel;  // rows at a common offset: pointers moved back to the 16-byte boundary
     FwdParams p;
     std::memset(&p, 0, sizeof p);
-    p.x = x;
-    p.residual = residual;
-    p.w = gamma;
-    p.beta = beta;
-    p.y = y;
-    p.residual_out = residual_out;
+    p.x = to_chunk_base(x, pl, (int)s);
+    p.residual = to_chunk_base(residual, pl, (int)s);
+    p.w = to_chunk_base(gamma, pl, (int)s);
+    p.beta = to_chunk_base(beta, pl, (int)s);
+    p.y = to_chunk_base(y, pl, (int)s);
+    p.residual_out = to_chunk_base(residual_out, pl, (int)s);
+    p.peel = pl;
     p.rstd = rstd;
     p.mean = mean;
     p.M = M;
@@ -1022,29 +1104,14 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
         return RMSNORM_ERR_INVALID_ARG;
     if (workspace && !aligned_to(workspace, 16)) return RMSNORM_ERR_WORKSPACE;
     const bool fused = dres != nullptr;
-    bool aligned = aligned_to(dy, 16) && aligned_to(x, 16) && aligned_to(dx, 16) && (!gamma || aligned_to(gamma, 16));
-    if (dres) aligned = aligned && aligned_to(dres, 16);
 
-    int dev = 0, sms = 0;
-    cudaError_t e = device_sms(&dev, &sms);
-    if (e != cudaSuccess) return cuda_fail(e);
-    rmsnorm_plan_t plan;
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_LN_BWD, M, N, dt, aligned, 1, 0, force_plan, force_ctas, &plan);
+    BwdCall call;
+    rmsnorm_status_t st = plan_bwd_call(RMSNORM_OP_LN_BWD, dy, dres, x, gamma, dx, M, N, dt, fused, force_plan,
+                                        force_ctas, &call);
     if (st != RMSNORM_SUCCESS) return st;
-    if (plan.path == PATH_STAGED &&
-        staged_smem_bytes(*find_plan(plan.plan_id), N, (int)s, fused) > kMaxDynamicSmem)
-        return RMSNORM_ERR_UNSUPPORTED;
-    int parts = 1, cps = 1;
-    e = bwd_max_parts(dev, sms, dt, *find_plan(plan.plan_id), N, fused, &parts, &cps);
-    if (e != cudaSuccess) return cuda_fail(e);
-    st = select_plan(RMSNORM_OP_LN_BWD, M, N, dt, aligned, parts, cps, force_plan, force_ctas, &plan);
-    if (st != RMSNORM_SUCCESS) return st;
+    rmsnorm_plan_t &plan = call.plan;
+    cudaError_t e;
     if (plan.path == PATH_GENERIC && force_plan < 0) note_generic(NOTE_LN_BWD, N, dt);
-    if (plan.path == PATH_STAGED) {
-        const int64_t sm = staged_smem_bytes(*find_plan(plan.plan_id), N, (int)s, fused);
-        if (sm > kMaxDynamicSmem) return RMSNORM_ERR_UNSUPPORTED;
-        plan.smem_bytes = (int32_t)sm;
-    }
 
     float *ws = static_cast<float *>(workspace);
     bool owned = false;
@@ -1060,29 +1127,34 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
         owned = true;
     }
     int *status = nullptr;
-    e = status_word(dev, &status);
+    e = status_word(call.dev, &status);
     if (e != cudaSuccess) {
         if (owned) cudaFreeAsync(ws, stream);
         return cuda_fail(e);
     }
 
+    // rows at a common offset: pointers moved back to the 16-byte boundary
+    // (the partial rows come out rotated by pl columns)
+    const int pl = plan.peel;
+    const int es = (int)s;
     BwdParams p;
     std::memset(&p, 0, sizeof p);
     p.status = status;
-    p.dy = dy;
-    p.x = x;
-    p.w = gamma;
+    p.dy = to_chunk_base(dy, pl, es);
+    p.x = to_chunk_base(x, pl, es);
+    p.w = to_chunk_base(gamma, pl, es);
     p.rstd = rstd;
     p.mean = mean;
-    p.dres = dres;
-    p.dx = dx;
+    p.dres = to_chunk_base(dres, pl, es);
+    p.dx = to_chunk_base(dx, pl, es);
     p.ws = ws;
     p.M = M;
     p.N = (int)N;
     p.offset = offset;
-    const PlanDesc *pd = find_plan(plan.plan_id);
-    p.stages = staged_path(pd->path) ? staged_depth(*pd, N, (int)s, fused) : 0;
-    p.cache_row = generic_bwd_cache(pd->path, N, (int)s, ws != nullptr, cps);
+    p.peel = pl;
+    const PlanDesc *pd = call.d;
+    p.stages = staged_path(pd->path) ? staged_depth(*pd, N * es / 16, pl, fused) : 0;
+    p.cache_row = generic_bwd_cache(pd->path, N, (int)s, ws != nullptr, call.cps);
     if (p.cache_row) plan.smem_bytes = (int32_t)(2 * generic_bwd_cache_slot(N, (int)s));
     int le;
     switch (base_dtype(dt)) {
@@ -1090,15 +1162,10 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
     case RMSNORM_F16: le = launch_ln_bwd_f16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
     default: le = launch_ln_bwd_f32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
     }
-    // one finalizer over the [units, 2N] partial rows: dgamma | dbeta
-    if (le == 0 && want) {
-        void *out0 = dgamma, *out1 = dbeta;
-        int split = (int)N;
-        if (!dgamma) {  // dbeta only: columns [N, 2N) go to out1, [0, N) nowhere
-            out0 = nullptr;
-        }
-        le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)(2 * N), out0, out1, split, stream, false);
-    }
+    // one finalizer over the [units, 2N] partial rows: dgamma | dbeta (a
+    // NULL output's half is not written)
+    if (le == 0 && want)
+        le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)(2 * N), dgamma, dbeta, (int)N, pl, stream, false);
     if (owned) {
         cudaError_t fe = cudaFreeAsync(ws, stream);
         if (le == 0 && fe != cudaSuccess) le = (int)fe;
@@ -1190,6 +1257,11 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt) {
     return bwd_workspace_bytes(RMSNORM_OP_BWD, M, N, dt);
 }
 
+size_t rmsnorm_bwd_call_workspace_bytes(const void *dy, const void *dresidual_out, const void *x, const void *w,
+                                        const void *dx, int64_t M, int64_t N, rmsnorm_dtype_t dt, int fused) {
+    return call_workspace_bytes(dy, dresidual_out, x, w, dx, M, N, dt, fused != 0);
+}
+
 rmsnorm_status_t layernorm_fwd(const void *x, const void *residual, const void *gamma, const void *beta, void *y,
                                void *residual_out, float *mean, float *rstd, int64_t M, int64_t N,
                                rmsnorm_dtype_t dt, float eps, float offset, rmsnorm_stream_t stream) {
@@ -1230,7 +1302,9 @@ size_t layernorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt) {
 rmsnorm_status_t rmsnorm_plan_query(int op, int64_t M, int64_t N, rmsnorm_dtype_t dt, int aligned, int num_sms,
                                     int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
     if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
-    if (num_sms < 1) return RMSNORM_ERR_INVALID_ARG;
+    if (num_sms < 1 || aligned < 0) return RMSNORM_ERR_INVALID_ARG;
+    // aligned: 0 generic, 1 aligned rows, 1 + k rows at a common offset of k elements
+    const int layout = aligned == 0 ? -1 : aligned - 1;
     // Without a device the resident-CTA count is the caller's (or the plan's
     // nominal 2048 threads per SM); a cluster plan packs cluster-size CTAs.
     int cps = ctas_per_sm;
@@ -1243,7 +1317,7 @@ rmsnorm_status_t rmsnorm_plan_query(int op, int64_t M, int64_t N, rmsnorm_dtype_
         }
     } else {
         rmsnorm_plan_t probe;
-        rmsnorm_status_t st = select_plan(op, M, N, dt, aligned != 0, 1, 0, -1, 0, &probe);
+        rmsnorm_status_t st = select_plan(op, M, N, dt, layout, 1, 0, -1, 0, &probe);
         if (st != RMSNORM_SUCCESS) return st;
         const PlanDesc *pd = find_plan(probe.plan_id);
         if (cps <= 0) cps = nominal_ctas_per_sm(*pd);
@@ -1252,7 +1326,7 @@ rmsnorm_status_t rmsnorm_plan_query(int op, int64_t M, int64_t N, rmsnorm_dtype_
     if (cps <= 0) cps = 1;
     int64_t parts = (int64_t)cps * num_sms / cs;
     if (parts < 1) parts = 1;
-    return select_plan(op, M, N, dt, aligned != 0, parts, cps, force_plan, force_ctas, out);
+    return select_plan(op, M, N, dt, layout, parts, cps, force_plan, force_ctas, out);
 }
 
 int rmsnorm_plan_count(void) { return kNumPlans; }

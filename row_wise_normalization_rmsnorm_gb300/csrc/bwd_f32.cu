@@ -9,8 +9,8 @@ int launch_bwd_main_f32(int plan_id, bool fused, bool packed, const BwdParams &p
 const void *bwd_main_kernel_ptr_f32(int plan_id, bool fused, bool packed) {
     return bwd_ptr_t<float, float>(plan_id, fused, packed);
 }
-int launch_dw_finalize_f32(const float *ws, int parts, int ncols, void *out0, void *out1, int split,
-                            void *stream, bool serial) {
-    return finalize_launch_t<float>(ws, parts, ncols, out0, out1, split, stream, serial);
+int launch_dw_finalize_f32(const float *ws, int parts, int ncols, void *out0, void *out1, int split, int peel,
+                           void *stream, bool serial) {
+    return finalize_launch_t<float>(ws, parts, ncols, out0, out1, split, peel, stream, serial);
 }
 }  // namespace rmsn

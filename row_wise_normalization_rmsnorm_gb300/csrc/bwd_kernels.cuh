@@ -41,7 +41,8 @@ namespace rmsn {
 
 // x, dy (and dres) chunks of one row, and its rstd, into registers. Rows
 // past M are clamped to the last row (their results are masked later), so
-// every thread of the CTA keeps taking part in the reductions.
+// every thread of the CTA keeps taking part in the reductions. Rows at a
+// common offset (p.peel) read their chunk 0 wrapped (ld_row_chunk).
 template <typename T, int TPR, int V, bool LN>
 __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, int C, int cbase, int t,
                                              bool has_dres, uint4 (&x)[V], uint4 (&d)[V], uint4 (&r)[V],
@@ -55,9 +56,9 @@ __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, in
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
         const bool in = c < C;
-        x[v] = in ? ld_stream(x4 + c) : make_uint4(0, 0, 0, 0);
-        d[v] = in ? ld_stream(d4 + c) : make_uint4(0, 0, 0, 0);
-        r[v] = (has_dres && in) ? ld_stream(r4 + c) : make_uint4(0, 0, 0, 0);
+        x[v] = in ? ld_row_chunk<T>(x4, c, C, p.peel) : make_uint4(0, 0, 0, 0);
+        d[v] = in ? ld_row_chunk<T>(d4, c, C, p.peel) : make_uint4(0, 0, 0, 0);
+        r[v] = (has_dres && in) ? ld_row_chunk<T>(r4, c, C, p.peel) : make_uint4(0, 0, 0, 0);
     }
     rs = p.rstd[rr];
     if constexpr (LN) mu = p.mean[rr];
@@ -117,7 +118,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
         if constexpr (RAWW) {
-            wraw[v] = (has_w && c < C) ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + c) : make_uint4(0, 0, 0, 0);
+            wraw[v] = (has_w && c < C) ? ld_w_raw<T>(p.w, c, C, p.peel) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int k = 0; k < NP; ++k) {
                 acc[v][k] = make_float2(0.f, 0.f);
@@ -127,7 +128,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
         }
         float2 wv[NP];
         if (has_w && c < C) {
-            load_w_chunk<T, TW>(p.w, c, wv);
+            load_w_chunk_row<T, TW>(p.w, c, C, p.peel, wv);
         } else {
 #pragma unroll
             for (int k = 0; k < NP; ++k) wv[k] = make_float2(0.f, 0.f);
@@ -287,7 +288,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
 #pragma unroll
                 for (int q = 0; q < NP; ++q) out[q] = Pk::add(out[q], rf[q]);
             }
-            if (valid && c < C) st_chunk(dx4 + base + c, pack<T>(out));
+            if (valid && c < C) st_row_chunk<T>(dx4 + base, c, C, p.peel, pack<T>(out));
         }
     };
 
@@ -447,7 +448,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     __shared__ __align__(8) uint64_t full[S];
     __shared__ __align__(8) uint64_t rbar[2];  // cluster rows: arrival of the peers' partials
     __shared__ unsigned done[HOLD ? 1 : S];  // re-read: warps through the stage's row
-    extern __shared__ float4 stage_smem[];  // ns * NB * Cst chunks of 16 bytes (+ Cst for gamma)
+    extern __shared__ float4 stage_smem[];  // ns * NB * Cb chunks of 16 bytes (+ Cb for gamma)
     // The LayerNorm re-read schedule keeps gamma in shared memory after the
     // stages rather than in registers (its two accumulators fill them).
     constexpr bool WSM = LN && !HOLD;
@@ -462,9 +463,19 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     // rows and owns a parameter-gradient partial row
     uint32_t rank = 0;
     if constexpr (CS > 1) rank = cluster_ctarank();
-    const int Cst = (C + CS - 1) / CS;  // chunks a stage buffer holds (at most TPR V)
+    const int Cst = (C + CS - 1) / CS;  // chunks of a CTA's slice (at most TPR V)
     const int cbase = (int)rank * Cst;
     const int Cs = C - cbase <= 0 ? 0 : (C - cbase < Cst ? C - cbase : Cst);
+    // rows at a common offset: the CTA holding chunk 0 also stages aligned
+    // chunk C (after its slice) to wrap chunk 0; a stage's row buffers are
+    // one slot longer
+    const int peel = p.peel;
+    const bool wrap = peel != 0 && cbase == 0;
+    const int Cb = Cst + (peel != 0 ? 1 : 0);  // slots of a stage's row buffer
+    // chunk cl of this CTA's slice from a staged row buffer
+    auto staged = [&](const uint4 *buf, int cl) {
+        return wrap && cl == 0 ? wrap_chunk<T>(lds128(buf), lds128(buf + Cst), peel) : lds128(buf + cl);
+    };
     const int64_t unit = CS > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
     const int64_t G = CS > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
     const int64_t iters = unit < p.M ? (p.M - unit + G - 1) / G : 0;
@@ -475,20 +486,31 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x);
     const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dy);
     const uint4 *r4 = reinterpret_cast<const uint4 *>(p.dres);
-    // thread 0: stream row k into stage s
+    // thread 0: stream row k into stage s (a CTA holding the whole row
+    // stages aligned chunks 0 .. C of a row at a common offset in one copy)
     auto issue = [&](int64_t k, int s) {
-        const int64_t off = (unit + k * G) * C + cbase;
-        uint4 *dst = stages + (size_t)s * NB * Cst;
-        mbar_arrive_expect_tx(&full[s], row_bytes * (has_dres ? 3u : 2u));
+        const int64_t row0 = (unit + k * G) * C;
+        const int64_t off = row0 + cbase;
+        uint4 *dst = stages + (size_t)s * NB * Cb;
+        const uint32_t extra = wrap ? 16u : 0u;
+        mbar_arrive_expect_tx(&full[s], (row_bytes + extra) * (has_dres ? 3u : 2u));
         if (row_bytes == 0) return;  // an empty slice: the arrival alone completes the phase
-        bulk_g2s(dst, x4 + off, row_bytes, &full[s]);
-        bulk_g2s(dst + Cst, d4 + off, row_bytes, &full[s]);
-        if (has_dres) bulk_g2s(dst + 2 * Cst, r4 + off, row_bytes, &full[s]);
+        auto copy = [&](uint4 *to, const uint4 *from) {
+            if (CS == 1 || !wrap) {
+                bulk_g2s(to, from + off, row_bytes + extra, &full[s]);
+            } else {
+                bulk_g2s(to, from + off, row_bytes, &full[s]);
+                bulk_g2s(to + Cst, from + row0 + C, 16u, &full[s]);
+            }
+        };
+        copy(dst, x4);
+        copy(dst + Cb, d4);
+        if (has_dres) copy(dst + 2 * Cb, r4);
     };
-    uint4 *wsm = stages + (size_t)ns * NB * Cst;
+    uint4 *wsm = stages + (size_t)ns * NB * Cb;
     if constexpr (WSM) {
         if (p.w != nullptr)
-            for (int c = tid; c < Cs; c += TPR) wsm[c] = ld_keep(reinterpret_cast<const uint4 *>(p.w) + cbase + c);
+            for (int c = tid; c < Cs; c += TPR) wsm[c] = ld_w_raw<T>(p.w, cbase + c, C, peel);
     }
     constexpr uint32_t kSlotBytes = CS * W * sizeof(RT);  // one row's partials from the whole cluster
     if (tid == 0) {
@@ -534,12 +556,11 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         const int cl = v * TPR + t;  // chunk of this CTA's slice; cbase + cl in the row
         if constexpr (WSM) {
         } else if constexpr (RAW) {
-            wraw[v] = (has_w && cl < Cs) ? ld_keep(reinterpret_cast<const uint4 *>(p.w) + cbase + cl)
-                                         : make_uint4(0, 0, 0, 0);
+            wraw[v] = (has_w && cl < Cs) ? ld_w_raw<T>(p.w, cbase + cl, C, peel) : make_uint4(0, 0, 0, 0);
         } else {
             float2 wv[NP];
             if (has_w && cl < Cs) {
-                load_w_chunk<T, TW>(p.w, cbase + cl, wv);
+                load_w_chunk_row<T, TW>(p.w, cbase + cl, C, peel, wv);
             } else {
 #pragma unroll
                 for (int q = 0; q < NP; ++q) wv[q] = make_float2(0.f, 0.f);
@@ -584,7 +605,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         }
         if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
         const int sk = s;  // this row's stage
-        const uint4 *src = stages + (size_t)s * NB * Cst;
+        const uint4 *src = stages + (size_t)s * NB * Cb;
         // HOLD: the row's chunks, read once and kept for both passes
         uint4 xv[HOLD ? V : 1], dv[HOLD ? V : 1], rv[FUSED && HOLD ? V : 1];
         if constexpr (HOLD) {
@@ -592,15 +613,15 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
             for (int v = 0; v < V; ++v) {
                 const int cl = v * TPR + t;
                 const bool in = cl < Cs;
-                xv[v] = in ? lds128(src + cl) : make_uint4(0, 0, 0, 0);
-                dv[v] = in ? lds128(src + Cst + cl) : make_uint4(0, 0, 0, 0);
-                if constexpr (FUSED) rv[v] = (in && has_dres) ? lds128(src + 2 * Cst + cl) : make_uint4(0, 0, 0, 0);
+                xv[v] = in ? staged(src, cl) : make_uint4(0, 0, 0, 0);
+                dv[v] = in ? staged(src + Cb, cl) : make_uint4(0, 0, 0, 0);
+                if constexpr (FUSED) rv[v] = (in && has_dres) ? staged(src + 2 * Cb, cl) : make_uint4(0, 0, 0, 0);
             }
         }
         // chunk v of the stage's x (b = 0), dy (1) or dres (2) row
         auto chunk = [&](int b, int v) {
             const int cl = v * TPR + t;
-            return cl < Cs ? lds128(src + b * Cst + cl) : make_uint4(0, 0, 0, 0);
+            return cl < Cs ? staged(src + b * Cb, cl) : make_uint4(0, 0, 0, 0);
         };
 
         const float2 r2 = make_float2(r, r);
@@ -707,7 +728,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
                     for (int q = 0; q < NP; ++q) out[q] = Pk::add(out[q], rf[q]);
                 }
             }
-            if (cl < Cs) st_chunk(dx4 + base + cbase + cl, pack<T>(out));
+            if (cl < Cs) st_row_chunk<T>(dx4 + base, cbase + cl, C, peel, pack<T>(out));
         }
         if constexpr (!HOLD) {
             // re-read: the warp is through stage sk; the last warp to say so
@@ -994,20 +1015,21 @@ __device__ __forceinline__ void wait_for_main_grid() { asm volatile("griddepcont
 // splits the P partial rows into 32 groups; group q sums rows
 // [q P / 32, (q+1) P / 32) in order, then each column adds the 32 group sums
 // in order. A few float4 loads per thread keep the L2 round trips short.
-// Columns c < split go to out0[c], the rest to out1[c - split] (a NULL
-// output's columns are not written); N is the workspace's row length.
+// Columns c < split go to out0, the rest to out1 (a NULL output's columns
+// are not written); within its half, workspace column c is parameter
+// column (c - peel) mod split (rows at a common offset wrap their first
+// chunk, peel > 0); N is the workspace's row length.
 template <typename T>
-__device__ __forceinline__ void store_param(T *out0, T *out1, int split, int c, float v) {
-    if (c < split) {
-        if (out0) store_elem(out0, c, v);
-    } else if (out1) {
-        store_elem(out1, c - split, v);
-    }
+__device__ __forceinline__ void store_param(T *out0, T *out1, int split, int peel, int c, float v) {
+    T *out = c < split ? out0 : out1;
+    int oc = (c < split ? c : c - split) - peel;
+    if (oc < 0) oc += split;
+    if (out) store_elem(out, oc, v);
 }
 
 template <typename T, int LANES = 8, int RG = 32>
 __global__ void __launch_bounds__(LANES *RG) rmsnorm_dw_finalize4(const float *ws, int parts, int N, T *dw, T *dw1,
-                                                                  int split) {
+                                                                  int split, int peel) {
     constexpr int COLS = 4 * LANES;       // columns per CTA
     __shared__ float part[RG][COLS + 1];
     wait_for_main_grid();
@@ -1040,7 +1062,7 @@ __global__ void __launch_bounds__(LANES *RG) rmsnorm_dw_finalize4(const float *w
             float tot = part[0][threadIdx.x];
 #pragma unroll
             for (int g = 1; g < RG; ++g) tot = __fadd_rn(tot, part[g][threadIdx.x]);
-            store_param(dw, dw1, split, c, tot);
+            store_param(dw, dw1, split, peel, c, tot);
         }
     }
 }
@@ -1049,7 +1071,7 @@ __global__ void __launch_bounds__(LANES *RG) rmsnorm_dw_finalize4(const float *w
 // same fixed order rules.
 template <typename T>
 __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int parts, int N, T *dw, T *dw1,
-                                                           int split) {
+                                                           int split, int peel) {
     constexpr int RG = 8;
     __shared__ float part[RG][32];
     wait_for_main_grid();
@@ -1070,7 +1092,7 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int 
         float tot = part[0][lane];
 #pragma unroll
         for (int g = 1; g < RG; ++g) tot = __fadd_rn(tot, part[g][lane]);
-        store_param(dw, dw1, split, col, tot);
+        store_param(dw, dw1, split, peel, col, tot);
     }
 }
 
@@ -1207,8 +1229,8 @@ static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
 // (its launch overlaps the main kernel's tail) unless `serial` asks for a
 // plain launch (when the caller records an event between the two).
 template <typename T>
-static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *dw1, int split, void *stream,
-                             bool serial) {
+static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *dw1, int split, int peel,
+                             void *stream, bool serial) {
     constexpr int kLanes = 8, kGroups = 32;  // vector finalizer: 4 * kLanes columns a CTA
     // float4 columns need every group of 4 on one side of the split
     const bool vec = N % 4 == 0 && split % 4 == 0;
@@ -1225,8 +1247,8 @@ static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *
     T *out = static_cast<T *>(dw);
     T *out1 = static_cast<T *>(dw1);
     cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize4<T, kLanes, kGroups>, ws, parts, N, out, out1,
-                                             split)
-                        : cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize<T>, ws, parts, N, out, out1, split);
+                                             split, peel)
+                        : cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize<T>, ws, parts, N, out, out1, split, peel);
     return (int)e;
 }
 

@@ -129,6 +129,109 @@ __device__ __forceinline__ float round_to(float v, const __nv_bfloat16 *) {
     return __bfloat162float(__float2bfloat16_rn(v));
 }
 
+// ----------------------------------------------- rows at a common offset --
+// When every array of a call starts `peel` elements past a 16-byte boundary
+// (0 < peel < E) and rows are whole 16-byte chunks long (C of them), the
+// host moves each pointer back by `peel` elements, to the boundary. Row r
+// then covers C + 1 aligned chunks from (base + r C): its first `E - peel`
+// elements are the last ones of aligned chunk 0 and its last `peel` ones
+// the first ones of aligned chunk C. The kernels keep C chunks per row,
+// exactly as for aligned rows: chunks 1 .. C-1 are aligned chunks 1 .. C-1,
+// and chunk 0 is "wrapped": elements l < peel come from aligned chunk C
+// (columns N - peel + l), elements l >= peel from aligned chunk 0 (columns
+// l - peel). Each of those two reads stays inside the aligned 16 bytes that
+// hold one of the row's elements; their stores write the row's own
+// elements one by one. A thread's wrapped chunk therefore holds columns
+// (16-byte lane l) -> (l - peel) mod N, and so does a partial row written
+// from it: the finalizer rotates columns back.
+
+// Keep the row's elements of aligned chunk 0 (`first`: l >= peel) or of
+// aligned chunk C (l < peel); the others become zero bits.
+template <typename T>
+__device__ __forceinline__ uint4 keep_part(uint4 v, bool first, int peel) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int l0 = 2 * k, l1 = 2 * k + 1;  // low half-word: element 2k
+            const bool k0 = first ? l0 >= peel : l0 < peel;
+            const bool k1 = first ? l1 >= peel : l1 < peel;
+            w[k] &= (k0 ? 0x0000ffffu : 0u) | (k1 ? 0xffff0000u : 0u);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const bool keep = first ? k >= peel : k < peel;
+            w[k] = keep ? w[k] : 0u;
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The wrapped chunk from aligned chunks 0 (`head`) and C (`tail`).
+template <typename T>
+__device__ __forceinline__ uint4 wrap_chunk(uint4 head, uint4 tail, int peel) {
+    const uint4 a = keep_part<T>(head, true, peel), b = keep_part<T>(tail, false, peel);
+    return make_uint4(a.x | b.x, a.y | b.y, a.z | b.z, a.w | b.w);
+}
+
+// Store the row's elements of `v` into aligned chunk 0 (`first`) or C.
+template <typename T>
+__device__ __forceinline__ void store_part(uint4 *p, uint4 v, bool first, int peel) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (sizeof(T) == 2) {
+        uint16_t *q = reinterpret_cast<uint16_t *>(p);
+#pragma unroll
+        for (int l = 0; l < 8; ++l)
+            if (first ? l >= peel : l < peel) q[l] = (uint16_t)(w[l >> 1] >> (16 * (l & 1)));
+    } else {
+        uint32_t *q = reinterpret_cast<uint32_t *>(p);
+#pragma unroll
+        for (int l = 0; l < 4; ++l)
+            if (first ? l >= peel : l < peel) q[l] = w[l];
+    }
+}
+
+// Chunk c of the row starting at `row` (C chunks a row): a streaming load,
+// or for a wrapped chunk two loads merged.
+template <typename T>
+__device__ __forceinline__ uint4 ld_row_chunk(const uint4 *row, int c, int C, int peel) {
+    if (peel != 0 && c == 0) return wrap_chunk<T>(ld_stream(row), ld_stream(row + C), peel);
+    return ld_stream(row + c);
+}
+
+// Store chunk c of the row starting at `row`: whole, or a wrapped chunk's
+// two parts element by element.
+template <typename T>
+__device__ __forceinline__ void st_row_chunk(uint4 *row, int c, int C, int peel, const uint4 &v) {
+    if (peel != 0 && c == 0) {
+        store_part<T>(row, v, true, peel);
+        store_part<T>(row + C, v, false, peel);
+    } else {
+        row[c] = v;
+    }
+}
+
+// load_w_chunk for chunk c of a row of C chunks (the weight vector shares
+// the rows' offset: its chunk 0 is wrapped as well). Rows at a common
+// offset take the weight in the activations' type; the fp32-weight kernels
+// always see peel == 0.
+template <typename T, typename TW>
+__device__ __forceinline__ void load_w_chunk_row(const void *w, int c, int C, int peel, float2 (&wv)[Elem<T>::NP]) {
+    if constexpr (std::is_same<T, TW>::value) {
+        const uint4 *w4 = reinterpret_cast<const uint4 *>(w);
+        unpack<T>(peel != 0 && c == 0 ? wrap_chunk<T>(ld_keep(w4), ld_keep(w4 + C), peel) : ld_keep(w4 + c), wv);
+    } else {
+        load_w_chunk<T, TW>(w, c, wv);
+    }
+}
+// The raw 16 bytes of the weight's chunk c (weight in the activations' type).
+template <typename T>
+__device__ __forceinline__ uint4 ld_w_raw(const void *w, int c, int C, int peel) {
+    const uint4 *w4 = reinterpret_cast<const uint4 *>(w);
+    return peel != 0 && c == 0 ? wrap_chunk<T>(ld_keep(w4), ld_keep(w4 + C), peel) : ld_keep(w4 + c);
+}
+
 // --------------------------------------------------- peeled generic rows --
 // The generic kernels take rows of any length and alignment. A row is split
 // by the address of its x (or h) row: `head` elements up to the first

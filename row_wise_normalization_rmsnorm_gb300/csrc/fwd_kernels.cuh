@@ -30,15 +30,17 @@ namespace rmsn {
 
 // The row's chunks into registers; with FUSED, h = R(x + residual) is
 // formed in place and stored to residual_out. Chunks past the row are zero.
+// Rows are C chunks apart; rows at a common offset (p.peel) wrap chunk 0.
 template <typename T, int TPR, int V, bool FUSED>
-__device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, int cbase, int t, int cend, bool valid,
-                                             uint4 (&xv)[V]) {
+__device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, int C, int cbase, int t, int cend,
+                                             bool valid, uint4 (&xv)[V]) {
     using Pk = Pair<true>;
     constexpr int NP = Elem<T>::NP;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
-        xv[v] = c < cend ? ld_stream(reinterpret_cast<const uint4 *>(p.x) + base + c) : make_uint4(0, 0, 0, 0);
+        xv[v] = c < cend ? ld_row_chunk<T>(reinterpret_cast<const uint4 *>(p.x) + base, c, C, p.peel)
+                         : make_uint4(0, 0, 0, 0);
     }
     if constexpr (FUSED) {
         // h = R(x + residual). For bf16 inputs the fp32 sum is exact unless
@@ -49,7 +51,7 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = cbase + v * TPR + t;
-            rv[v] = c < cend ? ld_stream(reinterpret_cast<const uint4 *>(p.residual) + base + c)
+            rv[v] = c < cend ? ld_row_chunk<T>(reinterpret_cast<const uint4 *>(p.residual) + base, c, C, p.peel)
                           : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -61,7 +63,7 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
             for (int k = 0; k < NP; ++k) a[k] = Pk::add(a[k], b[k]);
             xv[v] = pack<T>(a);
             const int c = cbase + v * TPR + t;
-            if (valid && c < cend) st_chunk(reinterpret_cast<uint4 *>(p.residual_out) + base + c, xv[v]);
+            if (valid && c < cend) st_row_chunk<T>(reinterpret_cast<uint4 *>(p.residual_out) + base, c, C, p.peel, xv[v]);
         }
     }
 }
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
     const int cend = cbase + cslice < C ? cbase + cslice : C;
 
     uint4 xv[V];
-    fwd_load_row<T, TPR, V, FUSED>(p, base, cbase, t, cend, valid, xv);
+    fwd_load_row<T, TPR, V, FUSED>(p, base, C, cbase, t, cend, valid, xv);
 
     float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
@@ -136,14 +138,14 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
                 unpack<T>(xv[v], a);
                 if (has_w) {
                     float2 wv[NP];
-                    load_w_chunk<T, TW>(p.w, c, wv);
+                    load_w_chunk_row<T, TW>(p.w, c, C, p.peel, wv);
 #pragma unroll
                     for (int k = 0; k < NP; ++k) a[k] = Pk::mul(Pk::mul(a[k], r2), Pk::add(o2, wv[k]));
                 } else {
 #pragma unroll
                     for (int k = 0; k < NP; ++k) a[k] = Pk::mul(a[k], r2);
                 }
-                st_chunk(reinterpret_cast<uint4 *>(p.y) + base + c, pack<T>(a));
+                st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, p.peel, pack<T>(a));
             }
         }
     } else {
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     const int cend = cbase + cslice < C ? cbase + cslice : C;
 
     uint4 xv[V];
-    fwd_load_row<T, TPR, V, FUSED>(p, base, cbase, t, cend, valid, xv);
+    fwd_load_row<T, TPR, V, FUSED>(p, base, C, cbase, t, cend, valid, xv);
 
     float2 sm = make_float2(0.f, 0.f);
 #pragma unroll
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             float2 a[NP], gv[NP], bv[NP];
             unpack<T>(xv[v], a);
             if (p.w) {
-                unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.w) + c), gv);
+                unpack<T>(ld_w_raw<T>(p.w, c, C, p.peel), gv);
 #pragma unroll
                 for (int k = 0; k < NP; ++k) gv[k] = Pk::add(o2, gv[k]);
             } else {
@@ -406,14 +408,14 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                 for (int k = 0; k < NP; ++k) gv[k] = make_float2(1.f, 1.f);
             }
             if (p.beta) {
-                unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.beta) + c), bv);
+                unpack<T>(ld_w_raw<T>(p.beta, c, C, p.peel), bv);
             } else {
 #pragma unroll
                 for (int k = 0; k < NP; ++k) bv[k] = make_float2(0.f, 0.f);
             }
 #pragma unroll
             for (int k = 0; k < NP; ++k) a[k] = Pk::fma(Pk::mul(Pk::add(a[k], nmu2), r2), gv[k], bv[k]);
-            st_chunk(reinterpret_cast<uint4 *>(p.y) + base + c, pack<T>(a));
+            st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, p.peel, pack<T>(a));
         }
     }
 }
@@ -543,7 +545,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     __shared__ __align__(8) uint64_t full[S];
     __shared__ __align__(8) uint64_t rbar[2];  // cluster rows: arrival of the peers' sums
     __shared__ unsigned done[S];               // warps through the stage's row
-    extern __shared__ float4 fstage_smem[];    // ns * NB * Cst chunks of 16 bytes
+    extern __shared__ float4 fstage_smem[];    // ns * NB * Cb chunks of 16 bytes
 
     const int N = p.N;
     const int C = N / E;
@@ -554,6 +556,14 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     const int Cst = (C + CS - 1) / CS;  // this CTA's slice: chunks [cbase, cbase + Cs)
     const int cbase = (int)rank * Cst;
     const int Cs = C - cbase <= 0 ? 0 : (C - cbase < Cst ? C - cbase : Cst);
+    // rows at a common offset: the CTA holding chunk 0 also stages aligned
+    // chunk C (after its slice) to wrap chunk 0; row buffers are one slot longer
+    const int peel = p.peel;
+    const bool wrap = peel != 0 && cbase == 0;
+    const int Cb = Cst + (peel != 0 ? 1 : 0);
+    auto staged = [&](const uint4 *buf, int cl) {
+        return wrap && cl == 0 ? wrap_chunk<T>(lds128(buf), lds128(buf + Cst), peel) : lds128(buf + cl);
+    };
     const int64_t unit = CS > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
     const int64_t G = CS > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
     const int64_t iters = unit < p.M ? (p.M - unit + G - 1) / G : 0;
@@ -563,12 +573,22 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x);
     const uint4 *r4 = reinterpret_cast<const uint4 *>(p.residual);
     auto issue = [&](int64_t k, int s) {
-        const int64_t off = (unit + k * G) * C + cbase;
-        uint4 *dst = stages + (size_t)s * NB * Cst;
-        mbar_arrive_expect_tx(&full[s], row_bytes * NB);
+        const int64_t row0 = (unit + k * G) * C;
+        const int64_t off = row0 + cbase;
+        uint4 *dst = stages + (size_t)s * NB * Cb;
+        const uint32_t extra = wrap ? 16u : 0u;
+        mbar_arrive_expect_tx(&full[s], (row_bytes + extra) * NB);
         if (row_bytes == 0) return;  // an empty slice: the arrival alone completes the phase
-        bulk_g2s(dst, x4 + off, row_bytes, &full[s]);
-        if constexpr (FUSED) bulk_g2s(dst + Cst, r4 + off, row_bytes, &full[s]);
+        auto copy = [&](uint4 *to, const uint4 *from) {
+            if (CS == 1 || !wrap) {
+                bulk_g2s(to, from + off, row_bytes + extra, &full[s]);
+            } else {
+                bulk_g2s(to, from + off, row_bytes, &full[s]);
+                bulk_g2s(to + Cst, from + row0 + C, 16u, &full[s]);
+            }
+        };
+        copy(dst, x4);
+        if constexpr (FUSED) copy(dst + Cb, r4);
     };
     constexpr uint32_t kSlotBytes = CS * W * sizeof(float);
     if (t == 0) {
@@ -628,20 +648,22 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
         const int64_t row = unit + k * G;
         if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
         const int sk = s;
-        const uint4 *src = stages + (size_t)s * NB * Cst;
+        const uint4 *src = stages + (size_t)s * NB * Cb;
         const int64_t base = row * C + cbase;
+        const int64_t rowbase = row * C;
         // h of chunk v of the slice (fused: R(x + r), stored once in pass 1)
         auto hchunk = [&](int v, float2 (&h)[NP], bool store) {
             const int cl = v * TPR + t;
             if (cl < Cs) {
-                unpack<T>(lds128(src + cl), h);
+                unpack<T>(staged(src, cl), h);
                 if constexpr (FUSED) {
                     float2 rr[NP];
-                    unpack<T>(lds128(src + Cst + cl), rr);
+                    unpack<T>(staged(src + Cb, cl), rr);
 #pragma unroll
                     for (int j = 0; j < NP; ++j) h[j] = Pk::add(h[j], rr[j]);
                     const uint4 hp = pack<T>(h);
-                    if (store) st_chunk(reinterpret_cast<uint4 *>(p.residual_out) + base + cl, hp);
+                    if (store)
+                        st_row_chunk<T>(reinterpret_cast<uint4 *>(p.residual_out) + rowbase, cbase + cl, C, peel, hp);
                     unpack<T>(hp, h);
                 }
             } else {
@@ -691,7 +713,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
             if constexpr (LN) {
                 float2 gv[NP], bv[NP];
                 if (p.w) {
-                    unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.w) + c), gv);
+                    unpack<T>(ld_w_raw<T>(p.w, c, C, peel), gv);
 #pragma unroll
                     for (int j = 0; j < NP; ++j) gv[j] = Pk::add(o2, gv[j]);
                 } else {
@@ -699,7 +721,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                     for (int j = 0; j < NP; ++j) gv[j] = make_float2(1.f, 1.f);
                 }
                 if (p.beta) {
-                    unpack<T>(ld_keep(reinterpret_cast<const uint4 *>(p.beta) + c), bv);
+                    unpack<T>(ld_w_raw<T>(p.beta, c, C, peel), bv);
                 } else {
 #pragma unroll
                     for (int j = 0; j < NP; ++j) bv[j] = make_float2(0.f, 0.f);
@@ -708,7 +730,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                 for (int j = 0; j < NP; ++j) a[j] = Pk::fma(Pk::mul(Pk::add(a[j], nmu2), r2), gv[j], bv[j]);
             } else if (p.w) {
                 float2 wv[NP];
-                load_w_chunk<T, TW>(p.w, c, wv);
+                load_w_chunk_row<T, TW>(p.w, c, C, peel, wv);
 #pragma unroll
                 for (int j = 0; j < NP; ++j) a[j] = Pk::mul(Pk::mul(a[j], r2), Pk::add(o2, wv[j]));
             } else {
@@ -723,7 +745,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                 if (cl < Cs) {
                     float2 a[NP];
                     ychunk(v, a);
-                    st_chunk(reinterpret_cast<uint4 *>(p.y) + base + cl, pack<T>(a));
+                    st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + rowbase, cbase + cl, C, peel, pack<T>(a));
                 }
             }
         } else {

@@ -212,6 +212,11 @@ struct FwdParams {
     // memory between the passes (N elements + 16 bytes) instead of re-read
     // from L1/L2
     int cache_row = 0;
+    // vectorised kernels: every row array starts `peel` elements past a
+    // 16-byte boundary and the host passed each pointer moved back by that
+    // many elements to the boundary; chunk 0 of a row is then wrapped
+    // (wrap_chunk in common.cuh). 0: rows start on 16-byte boundaries.
+    int peel = 0;
 };
 
 // Output of the forward: the activations' type, or E4M3 with a per-tensor
@@ -233,6 +238,9 @@ struct BwdParams {
     const float *mean;       // LayerNorm: the forward's per-row mean
     int stages = 0;          // staged kernels: stages in use (2 .. the plan's depth; 0: the depth)
     int cache_row = 0;       // generic LayerNorm kernel: keep the row's x and dy in shared memory
+    int peel = 0;            // vectorised kernels: rows at a common offset (as FwdParams::peel); a
+                             // workspace partial row then holds parameter column (i - peel) mod N
+                             // in its column i
 };
 
 // The generic LayerNorm backward's row cache: x and dy of the current row, each in
@@ -284,12 +292,14 @@ int allow_staged_smem(const void *kernel);
 // Parameter-gradient finalizers, by the parameters' storage type: column
 // c < split of the [parts, ncols] workspace goes to out0[c], the others to
 // out1[c - split] (out1 may be NULL: those columns are not written).
-int launch_dw_finalize_f32(const float *ws, int parts, int ncols, void *out0, void *out1, int split, void *stream,
-                           bool serial);
-int launch_dw_finalize_bf16(const float *ws, int parts, int ncols, void *out0, void *out1, int split,
+// Within each half (of split columns) the workspace column c holds
+// parameter column (c - peel) mod split (peel > 0: rows at a common offset).
+int launch_dw_finalize_f32(const float *ws, int parts, int ncols, void *out0, void *out1, int split, int peel,
+                           void *stream, bool serial);
+int launch_dw_finalize_bf16(const float *ws, int parts, int ncols, void *out0, void *out1, int split, int peel,
                             void *stream, bool serial);
-int launch_dw_finalize_f16(const float *ws, int parts, int ncols, void *out0, void *out1, int split, void *stream,
-                           bool serial);
+int launch_dw_finalize_f16(const float *ws, int parts, int ncols, void *out0, void *out1, int split, int peel,
+                           void *stream, bool serial);
 
 // LayerNorm forward and backward main kernels (weight in the activations'
 // type; the default plans and the generic one).

@@ -293,18 +293,39 @@ def test_generic_note_is_optional_and_printed_once(rn, capfd):
     if torch.cuda.is_available():
         pytest.skip("host has a GPU: these addresses are not device memory")
     L = rn.lib()
-    x, r = ctypes.c_void_p(258), ctypes.c_void_p(512)   # bf16 x not 16-byte aligned
+    # bf16 x and y at different offsets past a 16-byte boundary (at one
+    # common offset they would take the vectorised kernels)
+    x, y, r = ctypes.c_void_p(258), ctypes.c_void_p(260), ctypes.c_void_p(512)
     L.rmsnorm_set_generic_note(0)
-    assert L.rmsnorm_fwd(x, None, x, r, 4, 8, 1, 1e-6, 0.0, None) == 4
+    assert L.rmsnorm_fwd(x, None, y, r, 4, 8, 1, 1e-6, 0.0, None) == 4
     assert "generic kernel" not in capfd.readouterr().err
     L.rmsnorm_set_generic_note(1)
-    assert L.rmsnorm_fwd(x, None, x, r, 4, 8, 1, 1e-6, 0.0, None) == 4
+    assert L.rmsnorm_fwd(x, None, y, r, 4, 8, 1, 1e-6, 0.0, None) == 4
     err = capfd.readouterr().err
     assert err.count("falling back to the generic kernel") == 1 and "N=8" in err and "bf16" in err
-    assert L.rmsnorm_fwd(x, None, x, r, 4, 8, 1, 1e-6, 0.0, None) == 4
+    assert L.rmsnorm_fwd(x, None, y, r, 4, 8, 1, 1e-6, 0.0, None) == 4
     assert "generic kernel" not in capfd.readouterr().err
     # a row of 7 bf16 elements is not a whole number of 16-byte chunks
     L.rmsnorm_set_generic_note(1)
     assert L.rmsnorm_fwd(ctypes.c_void_p(256), None, ctypes.c_void_p(256), r, 4, 7, 1, 1e-6, 0.0, None) == 4
     assert "whole number of 16-byte chunks" in capfd.readouterr().err
     L.rmsnorm_set_generic_note(0)
+
+
+@pytest.mark.parametrize("dt,N,k", [(1, 7168, 1), (1, 8192, 7), (0, 2048, 3), (2, 128, 5), (1, 32768, 2)])
+def test_common_offset_plans_match_aligned_plans(rn, dt, N, k):
+    """Rows at one common offset (every array k elements past a 16-byte
+    boundary) take the plan, CTA count and workspace of aligned rows, with
+    the offset reported; an offset that is not a whole element of a chunk
+    (k >= 16 / element size) takes the generic kernels."""
+    for op in (rn.OP_FWD, rn.OP_BWD, rn.OP_LN_BWD):
+        a = rn.plan_query(op, 4096, N, dt, aligned=1, ctas_per_sm=1)
+        p = rn.plan_query(op, 4096, N, dt, aligned=1 + k, ctas_per_sm=1)
+        assert p["peel"] == k and a["peel"] == 0
+        for key in ("plan_id", "ctas", "ws_rows", "workspace_bytes", "threads_per_row", "chunks_per_thread"):
+            assert p[key] == a[key], (op, key, p, a)
+        if p["path_name"] == "staged":
+            # one more 16-byte slot a row buffer (the aligned block that ends the row)
+            assert p["smem_bytes"] > a["smem_bytes"]
+    es = 4 if dt == 0 else 2
+    assert rn.plan_query(rn.OP_BWD, 4096, N, dt, aligned=1 + 16 // es)["path_name"] == "generic"

@@ -121,9 +121,15 @@ def test_ln_optional_parameters(rn, gamma, beta, want_dgamma, want_dbeta):
               expect_path="vector")
 
 
-def test_ln_misaligned_takes_generic(rn):
-    d = inputs.make_inputs(257, 2048, "bf16", 174, beta=True)
-    _ln_check(rn, d, "bf16", offset_elems=1, expect_path="generic")
+@pytest.mark.parametrize("dt,M,N,k", [("bf16", 257, 2048, 1), ("bf16", 300, 7168, 3), ("bf16", 129, 8192, 7),
+                                      ("bf16", 33, 32768, 2), ("f32", 200, 4096, 1), ("f16", 77, 128, 5)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_ln_common_offset_takes_fast_kernels(rn, dt, M, N, k, fused):
+    """Every array k elements past a 16-byte boundary: the vectorised
+    LayerNorm kernels with each row's head and tail joined into one chunk."""
+    d = inputs.make_inputs(M, N, dt, 174 + k, beta=True, x_shift=0.5, residual=fused, dres=fused)
+    out, bo = _ln_check(rn, d, dt, fused=fused, offset_elems=k, expect_path="vector")
+    assert out["plan"]["peel"] == k and bo["plan"]["peel"] == k
 
 
 @pytest.mark.parametrize("dt,M,N", [("bf16", 160, 7169), ("bf16", 96, 10247), ("f32", 96, 5111)])

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import check_dw, check_dx, check_rstd, check_y, empty_dev, to_dev, to_host
+from helpers import check_dw, check_dx, check_rstd, check_y, cuda_bits_equal, empty_dev, to_dev, to_host
 from row_wise_normalization_rmsnorm_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -27,11 +27,16 @@ def rn():
     return pkg
 
 
-def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_path=None, wdt=None):
+GENERIC_FWD, GENERIC_BWD = 16, 36   # plan ids of the generic kernels
+
+
+def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_path=None, wdt=None,
+                   force_generic=False):
     """wdt: the weight's (and dW's) storage type, default the activations'.
     offset_elems: one element offset for every array, or a dict of offsets
     by array name (x, w, dy, y, residual, residual_out, h, dx, dw, dres;
-    missing names: 0)."""
+    missing names: 0). force_generic: run the generic kernels whatever the
+    layout."""
     wdt = wdt or dt
     M, N = d["x"].shape
     offs = offset_elems if isinstance(offset_elems, dict) else None
@@ -46,7 +51,7 @@ def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_p
     res = to_dev(d["residual"], dt, offset=o("residual")) if fused else None
     hout = empty_dev((M, N), dt, offset=o("residual_out")) if fused else None
     _, _, _, fplan = rn.rmsnorm_fwd_ex(x, w, residual=res, residual_out=hout, y=y, rstd=rstd, eps=eps,
-                                       offset=offset)
+                                       offset=offset, force_plan=GENERIC_FWD if force_generic else -1)
     f = oracle.fwd(d["x"], d["w"], dtype=dt, eps=eps, offset=offset, residual=d.get("residual") if fused else None,
                    wdtype=wdt)
     torch.cuda.synchronize()
@@ -64,7 +69,7 @@ def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_p
     dres_np = d.get("dres") if fused else None
     dres = to_dev(dres_np, dt, offset=o("dres")) if dres_np is not None else None
     _, _, bplan = rn.rmsnorm_bwd_ex(dy, hdev, w, r32, dresidual_out=dres, fused=fused, dx=dx, dw=dw, eps=eps,
-                                    offset=offset)
+                                    offset=offset, force_plan=GENERIC_BWD if force_generic else -1)
     b = oracle.bwd(d["dy"], h_np, d["w"], dtype=dt, eps=eps, offset=offset, rstd=f["rstd32"], dres=dres_np,
                    wdtype=wdt)
     torch.cuda.synchronize()
@@ -130,9 +135,64 @@ def test_fused_ragged_gemma(rn, dt, M, N):
 
 @pytest.mark.parametrize("dt,M,N", [("bf16", 4096, 7168), ("f32", 4096, 2048)])
 def test_misaligned_storage_offset(rn, dt, M, N):
-    """All of x, w, y, dy, dx at +1 element from a 256-byte-aligned allocation."""
+    """All of x, w, y, dy, dx at +1 element from a 256-byte-aligned
+    allocation (the sweep's misaligned case): the vectorised kernels with
+    each row's head and tail joined into one chunk."""
     d = inputs.make_inputs(M, N, dt, inputs.SWEEP_SEED)
-    _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, offset_elems=1, expect_path="generic")
+    fp, bp = _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, offset_elems=1, expect_path="vector")
+    assert fp["peel"] == 1 and bp["peel"] == 1, (fp, bp)
+
+
+# Rows at a common offset past a 16-byte boundary, on every fast kernel
+# family: sub-warp, warp and multi-warp register rows (one chunk a row
+# included), staged rows (held and re-read schedules), cluster rows in both
+# directions, the fused add with and without dres, gemma offset, fp16.
+COMMON_OFFSET = [
+    ("bf16", 257, 8, 3), ("bf16", 333, 64, 7), ("bf16", 129, 128, 1), ("bf16", 300, 2048, 5),
+    ("bf16", 301, 4096, 2), ("bf16", 211, 7168, 1), ("bf16", 257, 8192, 7), ("bf16", 97, 16384, 4),
+    ("bf16", 33, 32768, 1), ("bf16", 9, 65536, 3), ("f32", 333, 4, 1), ("f32", 129, 256, 3),
+    ("f32", 300, 2048, 2), ("f32", 101, 6144, 1), ("f32", 65, 16384, 3), ("f16", 257, 8192, 5),
+    ("f16", 77, 1024, 1),
+]
+
+
+@pytest.mark.parametrize("dt,M,N,k", COMMON_OFFSET)
+def test_common_offset_rows_take_fast_kernels(rn, dt, M, N, k):
+    d = inputs.make_inputs(M, N, dt, 360 + N % 17 + k)
+    fp, bp = _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, offset_elems=k, expect_path="vector")
+    assert fp["peel"] == k and bp["peel"] == k, (fp, bp)
+
+
+@pytest.mark.parametrize("dt,M,N,k", [("bf16", 257, 8192, 1), ("bf16", 65, 2048, 6), ("f32", 130, 5120, 2),
+                                      ("bf16", 33, 32768, 5)])
+@pytest.mark.parametrize("gemma", [False, True])
+def test_common_offset_fused_add(rn, dt, M, N, k, gemma):
+    d = inputs.make_inputs(M, N, dt, 370 + k, w_mode="gemma" if gemma else "llama", residual=True, dres=True)
+    fp, bp = _fwd_bwd_check(rn, d, dt, 1e-6, 1.0 if gemma else 0.0, fused=True, offset_elems=k,
+                            expect_path="vector")
+    assert fp["peel"] == k and bp["peel"] == k, (fp, bp)
+
+
+@pytest.mark.parametrize("dt,N,k", [("bf16", 7168, 1), ("bf16", 8192, 3), ("f32", 2048, 1), ("f32", 6144, 2)])
+def test_common_offset_dw_equals_generic_at_same_ctas(rn, dt, N, k):
+    """Rows at a common offset on the persistent staged backward (one row
+    team a CTA) and on the generic kernel forced to the same CTA count: each
+    CTA adds the same rows in the same order into its partial row, and one
+    finalizer sums those in a fixed order, so dW agrees bit for bit."""
+    M = 1000
+    d = inputs.make_inputs(M, N, dt, 380 + k)
+    x, w, dy = (to_dev(d[key], dt, offset=k) for key in ("x", "w", "dy"))
+    _, rstd = rn.rmsnorm_fwd(x, w)
+    dx_a = empty_dev((M, N), dt, offset=k)
+    dx_b = empty_dev((M, N), dt, offset=k)
+    dw_a = empty_dev((N,), dt)
+    dw_b = empty_dev((N,), dt)
+    _, _, pa = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dx=dx_a, dw=dw_a)
+    assert pa["path_name"] == "staged" and pa["peel"] == k and pa["rows_per_cta"] == 1 and pa["cluster_size"] == 1
+    _, _, pb = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dx=dx_b, dw=dw_b, force_plan=GENERIC_BWD, force_ctas=pa["ctas"])
+    torch.cuda.synchronize()
+    assert pb["path_name"] == "generic" and pb["ctas"] == pa["ctas"]
+    assert cuda_bits_equal(dw_a, dw_b)
 
 
 # Generic rows with 16-byte chunks between a scalar head and tail (the
@@ -152,10 +212,12 @@ PEEL_CASES = [
 @pytest.mark.parametrize("dt,M,N,offs", PEEL_CASES)
 @pytest.mark.parametrize("fused", [False, True])
 def test_generic_peeled_and_scalar_rows(rn, dt, M, N, offs, fused):
+    """The generic kernels' own row split (forced: arrays at one common
+    offset would otherwise take the vectorised kernels)."""
     d = inputs.make_inputs(M, N, dt, 300 + N % 11, residual=fused, dres=fused)
     if fused:
         offs = dict(offs, residual=offs.get("x", 0), residual_out=offs.get("x", 0), dres=offs.get("dy", 0))
-    _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, fused=fused, offset_elems=offs, expect_path="generic")
+    _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, fused=fused, offset_elems=offs, expect_path="generic", force_generic=True)
 
 
 def test_generic_fused_residual_alone_misaligned(rn):
@@ -317,7 +379,9 @@ def test_f16_fused_add_gemma(rn, M, N):
 
 def test_f16_misaligned(rn):
     d = inputs.make_inputs(1024, 7168, "f16", inputs.SWEEP_SEED)
-    _fwd_bwd_check(rn, d, "f16", 1e-6, 0.0, offset_elems=1, expect_path="generic")
+    fp, bp = _fwd_bwd_check(rn, d, "f16", 1e-6, 0.0, offset_elems=1, expect_path="vector")
+    assert fp["peel"] == 1 and bp["peel"] == 1
+    _fwd_bwd_check(rn, d, "f16", 1e-6, 0.0, offset_elems=1, expect_path="generic", force_generic=True)
 
 
 def test_f16_non_affine(rn):

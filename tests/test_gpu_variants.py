@@ -366,11 +366,13 @@ def test_generic_rows_independent_of_other_arrays_alignment(rn, dt, N, xoff):
         y = empty_dev((M, N), dt, offset=off)
         hout = empty_dev((M, N), dt, offset=off)
         dx = empty_dev((M, N), dt, offset=off)
-        _, _, rstd, fp = rn.rmsnorm_fwd_ex(x, w, residual=res, residual_out=hout, y=y)
-        _, dw, bp = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dresidual_out=dres, fused=True, dx=dx)
+        # (forced: arrays at one common offset would take the vectorised kernels)
+        _, _, rstd, fp = rn.rmsnorm_fwd_ex(x, w, residual=res, residual_out=hout, y=y, force_plan=16)
+        _, dw, bp = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dresidual_out=dres, fused=True, dx=dx, force_plan=36)
         assert fp["path_name"] == "generic" and bp["path_name"] == "generic"
-        lo = rn.layernorm_fwd(x, w, b, y=empty_dev((M, N), dt, offset=off))
-        lb = rn.layernorm_bwd(dy, x, w, lo["mean"], lo["rstd"], dx=empty_dev((M, N), dt, offset=off))
+        lo = rn.layernorm_fwd(x, w, b, y=empty_dev((M, N), dt, offset=off), force_plan=16)
+        lb = rn.layernorm_bwd(dy, x, w, lo["mean"], lo["rstd"], dx=empty_dev((M, N), dt, offset=off),
+                              force_plan=72)
         torch.cuda.synchronize()
         outs.append([t.clone() for t in (y, hout, rstd, dx, dw, lo["y"], lo["mean"], lo["rstd"], lb["dx"],
                                          lb["dgamma"], lb["dbeta"])])
