@@ -409,7 +409,10 @@ rmsnorm_status_t rmsnorm_fwd_ex(const void *x, const void *residual, const void 
  * Backward with a forced plan and CTA count (negative / zero: default),
  * plain when `fused` is 0 (dresidual_out ignored), fused otherwise.
  * force_packed: -1 default, 0 scalar fp32 arithmetic, 1 packed f32x2; both
- * use the same even/odd accumulator pairing, so they agree bit for bit.
+ * use the same even/odd accumulator pairing, so they agree bit for bit. The
+ * staged plans run packed by default; their scalar variant is compiled for
+ * the default plans of fp32 and bf16 (weight in the activations' type) and
+ * forcing it elsewhere returns UNSUPPORTED.
  * event_after_main: if non-NULL, a cudaEvent_t recorded on `stream` between
  * the main kernel and the finalizer (for timing the two separately).
  */

@@ -448,8 +448,10 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
                          : bwd_smem_bytes(d, nmax);
     int best = 1 << 30;
     for (int pk = 0; pk < 2; ++pk) {
-        // the LayerNorm, staged and generic kernels have one variant
-        if ((d.path != PATH_VECTOR || d.op == OP_LN_BWD) && pk == 1) continue;
+        // the LayerNorm and generic kernels have one variant; a staged plan
+        // has the scalar one only where staged_scalar_variant says so
+        if ((d.path == PATH_GENERIC || d.op == OP_LN_BWD) && pk == 1) continue;
+        if (staged_path(d.path) && pk == 0 && !staged_scalar_variant(kind_of(dt), d.cmin)) continue;
         const void *k = d.op == OP_LN_BWD ? ln_bwd_kernel(d.id, dt, fused) : bwd_kernel(d.id, dt, fused, pk != 0);
         if (!k) return cudaErrorInvalidDeviceFunction;
         if (staged_path(d.path)) {  // more than 48 KB of dynamic shared memory needs an opt-in
@@ -908,7 +910,11 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     bool packed = plan.packed != 0;
     if (force_packed == 0) packed = false;
     if (force_packed == 1 && plan.path == PATH_VECTOR) packed = true;
-    if (plan.path == PATH_STAGED) packed = true;  // the staged kernel has the packed variant only
+    if (plan.path == PATH_STAGED) {
+        // packed unless the scalar variant is asked for and compiled
+        packed = force_packed != 0;
+        if (!packed && !staged_scalar_variant(kind_of(dt), d->cmin)) return RMSNORM_ERR_UNSUPPORTED;
+    }
     plan.packed = packed ? 1 : 0;
 
     float *ws = static_cast<float *>(workspace);

@@ -86,6 +86,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     __shared__ RT red[2][TEAMS][W * CS];              // row partials, double-buffered
     __shared__ __align__(8) uint64_t rbar[2][1];      // cluster rows: arrival of the peers' partials
     extern __shared__ float4 comb_smem[];      // (TEAMS - 1) * NACC * N floats
+    pdl_wait();  // the kernel before it has completed (the forward's rstd, say)
 
     const int team = threadIdx.x / TPR;
     const int t = threadIdx.x % TPR;
@@ -337,8 +338,8 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     }
 
     // The finalizer may start launching now; it waits for this grid to
-    // finish (griddepcontrol.wait) before it reads the workspace.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // finish (pdl_wait) before it reads the workspace.
+    pdl_trigger();
 
     if (!want_acc) return;  // no parameter partials (non-affine)
 
@@ -433,10 +434,10 @@ __global__ void __launch_bounds__(TPR *TEAMS) layernorm_bwd_vector(const BwdPara
 // ends. Each warp then counts itself done on the stage's counter and the
 // last one to arrive refills the stage; no thread waits for the others. The
 // arithmetic, and so every output bit, is that of HOLD = true.
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool LN, bool HOLD>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool LN, bool HOLD, bool PACKED = true>
 __device__ __forceinline__ void staged_body(const BwdParams &p) {
     static_assert(CS == 1 || !HOLD, "cluster rows use the re-read schedule (no CTA barrier orders their refills)");
-    using Pk = Pair<true>;
+    using Pk = Pair<PACKED>;
     using RT = typename std::conditional<LN, float2, float>::type;  // what a row reduces
     constexpr int NACC = LN ? 2 : 1;     // partial rows per CTA
     constexpr int E = Elem<T>::E;
@@ -449,6 +450,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     __shared__ __align__(8) uint64_t rbar[2];  // cluster rows: arrival of the peers' partials
     __shared__ unsigned done[HOLD ? 1 : S];  // re-read: warps through the stage's row
     extern __shared__ float4 stage_smem[];  // ns * NB * Cb chunks of 16 bytes (+ Cb for gamma)
+    pdl_wait();  // before any read of the rows (the bulk copies included)
     // The LayerNorm re-read schedule keeps gamma in shared memory after the
     // stages rather than in registers (its two accumulators fill them).
     constexpr bool WSM = LN && !HOLD;
@@ -751,8 +753,8 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     if constexpr (CS > 1) cluster_sync();
 
     // The finalizer may start launching now; it waits for this grid to
-    // finish (griddepcontrol.wait) before it reads the workspace.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // finish (pdl_wait) before it reads the workspace.
+    pdl_trigger();
     if (!want_acc) return;
     // the unit's partial row(s): dW, or LayerNorm's dgamma | dbeta (a
     // cluster CTA writes the columns of its slice)
@@ -777,9 +779,9 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     }
 }
 
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool HOLD>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool HOLD, bool PACKED = true>
 __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) {
-    staged_body<T, TW, TPR, V, S, CS, FUSED, false, HOLD>(p);
+    staged_body<T, TW, TPR, V, S, CS, FUSED, false, HOLD, PACKED>(p);
 }
 
 template <typename T, int TPR, int V, int S, int CS, bool FUSED, bool HOLD>
@@ -799,6 +801,7 @@ __global__ void __launch_bounds__(TPR, 1) layernorm_bwd_staged(const BwdParams p
 template <typename T, typename TW, bool FUSED>
 __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
     __shared__ float red[32];
+    pdl_wait();
     constexpr int NP = Elem<T>::NP;
     const int N = p.N;
     const TW *w = reinterpret_cast<const TW *>(p.w);
@@ -883,6 +886,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
         for (int j = sp.tail0 + threadIdx.x; j < N; j += blockDim.x) dx_elem(j);
         first = false;
     }
+    pdl_trigger();  // this CTA's rows done (the finalizer waits for the whole grid)
 }
 
 // Generic LayerNorm backward, the same scheme: per row the pair (sum g,
@@ -899,6 +903,7 @@ template <typename T, bool FUSED, bool CACHE>
 __global__ void __launch_bounds__(256, 5) layernorm_bwd_generic(const BwdParams p) {
     __shared__ float2 red[32];
     extern __shared__ uint4 gen_smem[];
+    pdl_wait();
     constexpr int E = Elem<T>::E;
     constexpr int NP = Elem<T>::NP;
     const int N = p.N;
@@ -997,6 +1002,7 @@ __global__ void __launch_bounds__(256, 5) layernorm_bwd_generic(const BwdParams 
         if (cache) __syncthreads();
         first = false;
     }
+    pdl_trigger();
 }
 
 // Dynamic shared memory of a generic backward launch: the two row-cache
@@ -1009,7 +1015,7 @@ static int generic_bwd_smem(const BwdParams &p) {
 // Finalizer. When launched as a programmatic dependent of the main kernel
 // it starts early and waits here until the main grid has completed and its
 // workspace writes are visible; otherwise the wait returns at once.
-__device__ __forceinline__ void wait_for_main_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void wait_for_main_grid() { pdl_wait(); }
 
 // Vector finalizer (N % 4 == 0): a CTA owns 32 columns as 8 float4 lanes and
 // splits the P partial rows into 32 groups; group q sums rows
@@ -1033,6 +1039,7 @@ __global__ void __launch_bounds__(LANES *RG) rmsnorm_dw_finalize4(const float *w
     constexpr int COLS = 4 * LANES;       // columns per CTA
     __shared__ float part[RG][COLS + 1];
     wait_for_main_grid();
+    pdl_trigger();
     const int lane = threadIdx.x % LANES;  // float4 column within the CTA's columns
     const int rg = threadIdx.x / LANES;    // row group
     const int col = blockIdx.x * COLS + lane * 4;
@@ -1075,6 +1082,7 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int 
     constexpr int RG = 8;
     __shared__ float part[RG][32];
     wait_for_main_grid();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int rg = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
@@ -1101,29 +1109,9 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int 
 
 template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED>
 static int bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    if constexpr (CS == 1) {
-        if (fused)
-            rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, 1, PACKED, true><<<grid, TPR * TEAMS, smem, s>>>(p);
-        else
-            rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, 1, PACKED, false><<<grid, TPR * TEAMS, smem, s>>>(p);
-        return (int)cudaGetLastError();
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(TPR * TEAMS);
-        cfg.dynamicSmemBytes = (size_t)smem;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CS;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return fused
-                   ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, PACKED, true>, p)
-                   : (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, PACKED, false>, p);
-    }
+    LaunchCfg lc((unsigned)grid, TPR * TEAMS, (size_t)smem, s, CS > 1 ? CS : 0);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, PACKED, true>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, PACKED, false>, p);
 }
 
 // A weight type other than the activations' is compiled for the default
@@ -1136,26 +1124,26 @@ constexpr bool bwd_instantiated() {
 // Staged kernel: launched as a cluster of CS CTAs (of one where a CTA
 // holds the whole row; its bulk copies name a shared::cluster destination)
 // with the stages' dynamic shared memory.
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool HOLD>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool HOLD, bool PACKED = true>
 static int bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    const void *k = fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD>
-                          : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD>;
+    const void *k = fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD, PACKED>
+                          : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD, PACKED>;
     const int e = allow_staged_smem(k);
     if (e != 0) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(TPR);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD>, p)
-                 : (int)cudaLaunchKernelEx(&cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD>, p);
+    // a cluster of CS CTAs (of one where a CTA holds the whole row: its bulk
+    // copies name a shared::cluster destination)
+    LaunchCfg lc((unsigned)grid, TPR, (size_t)smem, s, CS);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD, PACKED>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD, PACKED>, p);
+}
+
+// Kernel kind of an (activation, weight) type pair, as the host numbers it:
+// 0 fp32, 1 bf16, 2 fp16, 3 bf16 with an fp32 weight, 4 fp16 with one.
+template <typename T, typename TW>
+constexpr int kernel_kind() {
+    return std::is_same<T, float>::value ? 0
+           : std::is_same<T, TW>::value   ? (std::is_same<T, __nv_bfloat16>::value ? 1 : 2)
+                                          : (std::is_same<T, __nv_bfloat16>::value ? 3 : 4);
 }
 
 template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
@@ -1163,15 +1151,18 @@ static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int gri
     if constexpr (OP != OP_BWD || !bwd_instantiated<T, TW, PATH, CMIN>()) {
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
-        if (fused)
-            rmsnorm_bwd_generic<T, TW, true><<<grid, 256, 0, s>>>(p);
-        else
-            rmsnorm_bwd_generic<T, TW, false><<<grid, 256, 0, s>>>(p);
-        return (int)cudaGetLastError();
+        LaunchCfg lc((unsigned)grid, 256, 0, s);
+        return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_generic<T, TW, true>, p)
+                     : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_generic<T, TW, false>, p);
     } else if constexpr (PATH == PATH_VECTOR) {
         return packed ? bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, true>(fused, p, grid, smem, s)
                       : bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, false>(fused, p, grid, smem, s);
     } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
+        if constexpr (staged_scalar_variant(kernel_kind<T, TW>(), CMIN)) {
+            if (!packed) return bwd_launch_staged<T, TW, TPR, V, D, CS, PATH == PATH_STAGED, false>(fused, p, grid, smem, s);
+        } else if (!packed) {
+            return (int)cudaErrorInvalidValue;
+        }
         return bwd_launch_staged<T, TW, TPR, V, D, CS, PATH == PATH_STAGED>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
@@ -1191,6 +1182,14 @@ static const void *bwd_ptr_entry(bool fused, bool packed) {
         return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, true>
                      : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, false>;
     } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
+        // the scalar variant where it is compiled (nullptr where it is not)
+        if constexpr (staged_scalar_variant(kernel_kind<T, TW>(), CMIN)) {
+            if (!packed)
+                return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, true, PATH == PATH_STAGED, false>
+                             : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, false, PATH == PATH_STAGED, false>;
+        } else if (!packed) {
+            return nullptr;
+        }
         return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, true, PATH == PATH_STAGED>
                      : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, false, PATH == PATH_STAGED>;
     } else {
@@ -1234,21 +1233,13 @@ static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *
     constexpr int kLanes = 8, kGroups = 32;  // vector finalizer: 4 * kLanes columns a CTA
     // float4 columns need every group of 4 on one side of the split
     const bool vec = N % 4 == 0 && split % 4 == 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(vec ? (unsigned)((N + 4 * kLanes - 1) / (4 * kLanes)) : (unsigned)((N + 31) / 32));
-    cfg.blockDim = dim3(vec ? kLanes * kGroups : 256);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = serial ? 0 : 1;
+    LaunchCfg lc(vec ? (unsigned)((N + 4 * kLanes - 1) / (4 * kLanes)) : (unsigned)((N + 31) / 32),
+                 vec ? kLanes * kGroups : 256, 0, static_cast<cudaStream_t>(stream), 0, !serial);
     T *out = static_cast<T *>(dw);
     T *out1 = static_cast<T *>(dw1);
-    cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize4<T, kLanes, kGroups>, ws, parts, N, out, out1,
-                                             split, peel)
-                        : cudaLaunchKernelEx(&cfg, rmsnorm_dw_finalize<T>, ws, parts, N, out, out1, split, peel);
+    cudaError_t e = vec ? cudaLaunchKernelEx(&lc.cfg, rmsnorm_dw_finalize4<T, kLanes, kGroups>, ws, parts, N, out,
+                                             out1, split, peel)
+                        : cudaLaunchKernelEx(&lc.cfg, rmsnorm_dw_finalize<T>, ws, parts, N, out, out1, split, peel);
     return (int)e;
 }
 
@@ -1256,28 +1247,9 @@ static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *
 
 template <typename T, int TPR, int V, int TEAMS, int D, int CS>
 static int ln_bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    if constexpr (CS == 1) {
-        if (fused)
-            layernorm_bwd_vector<T, TPR, V, TEAMS, D, 1, true><<<grid, TPR * TEAMS, smem, s>>>(p);
-        else
-            layernorm_bwd_vector<T, TPR, V, TEAMS, D, 1, false><<<grid, TPR * TEAMS, smem, s>>>(p);
-        return (int)cudaGetLastError();
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(TPR * TEAMS);
-        cfg.dynamicSmemBytes = (size_t)smem;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CS;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return fused ? (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true>, p)
-                     : (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false>, p);
-    }
+    LaunchCfg lc((unsigned)grid, TPR * TEAMS, (size_t)smem, s, CS > 1 ? CS : 0);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false>, p);
 }
 
 template <typename T, int TPR, int V, int S, int CS, bool HOLD>
@@ -1286,20 +1258,9 @@ static int ln_bwd_launch_staged(bool fused, const BwdParams &p, int grid, int sm
                           : (const void *)layernorm_bwd_staged<T, TPR, V, S, CS, false, HOLD>;
     const int e = allow_staged_smem(k);
     if (e != 0) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(TPR);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return fused ? (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, CS, true, HOLD>, p)
-                 : (int)cudaLaunchKernelEx(&cfg, layernorm_bwd_staged<T, TPR, V, S, CS, false, HOLD>, p);
+    LaunchCfg lc((unsigned)grid, TPR, (size_t)smem, s, CS);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_staged<T, TPR, V, S, CS, true, HOLD>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_staged<T, TPR, V, S, CS, false, HOLD>, p);
 }
 
 template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
@@ -1308,13 +1269,12 @@ static int ln_bwd_launch_entry(bool fused, const BwdParams &p, int grid, int sme
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
         const int gs = generic_bwd_smem<T>(p);
+        LaunchCfg lc((unsigned)grid, 256, (size_t)gs, s);
         if (fused)
-            gs ? layernorm_bwd_generic<T, true, true><<<grid, 256, gs, s>>>(p)
-               : layernorm_bwd_generic<T, true, false><<<grid, 256, 0, s>>>(p);
-        else
-            gs ? layernorm_bwd_generic<T, false, true><<<grid, 256, gs, s>>>(p)
-               : layernorm_bwd_generic<T, false, false><<<grid, 256, 0, s>>>(p);
-        return (int)cudaGetLastError();
+            return gs ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, true, true>, p)
+                      : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, true, false>, p);
+        return gs ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, false, true>, p)
+                  : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, false, false>, p);
     } else if constexpr (PATH == PATH_VECTOR) {
         return ln_bwd_launch_vec<T, TPR, V, TEAMS, D, CS>(fused, p, grid, smem, s);
     } else if constexpr (staged_plan(PATH, TEAMS, CS)) {

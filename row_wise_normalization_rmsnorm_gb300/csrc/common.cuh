@@ -29,6 +29,59 @@ template <> struct Elem<__half> {
     static constexpr int NP = 4;
 };
 
+// ------------------------------------------------- launch and ordering --
+// Every kernel is launched on the caller's stream as a programmatic
+// dependent of the kernel before it (cudaLaunchAttributeProgrammatic-
+// StreamSerialization). When that kernel is one of ours and has signalled
+// its dependents (pdl_trigger), this one's CTAs are launched while it
+// drains; each of our kernels calls pdl_wait before it touches global
+// memory, which returns once the kernel before it has completed and its
+// writes are visible (at once when there is none, or when it was not
+// launched this way). Every CTA waits, so a kernel completes only after the
+// one before it: the ordering stays transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Programmatic dependent launches on (1) or off (0, every kernel waits for
+// the one before it as a plain stream launch does), for A/B measurements.
+#ifndef RMSNORM_PDL
+#define RMSNORM_PDL 1
+#endif
+
+// Launch configuration: grid, block, dynamic shared memory, stream, the
+// cluster size (0: no cluster attribute; 1: clusters of one CTA, for the
+// kernels whose bulk copies name a shared::cluster destination) and the
+// programmatic dependency (on unless `pdl` is false). Used in place (its
+// attribute array is referenced by the configuration), never copied.
+struct LaunchCfg {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    LaunchCfg(unsigned grid, unsigned block, size_t smem, cudaStream_t s, unsigned cs = 0, bool pdl = true) {
+        cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(block);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        unsigned n = 0;
+        if (cs > 0) {
+            attr[n].id = cudaLaunchAttributeClusterDimension;
+            attr[n].val.clusterDim.x = cs;
+            attr[n].val.clusterDim.y = 1;
+            attr[n].val.clusterDim.z = 1;
+            ++n;
+        }
+        if (pdl && RMSNORM_PDL) {
+            attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
+        cfg.attrs = attr;
+        cfg.numAttrs = n;
+    }
+    LaunchCfg(const LaunchCfg &) = delete;
+    LaunchCfg &operator=(const LaunchCfg &) = delete;
+};
+
 // ----------------------------------------------------------- 16-byte I/O --
 // Row data is read once: ld.global.cs (streaming, evict-first). The weight
 // is shared by every row: the read-only path. Writes are plain stores.

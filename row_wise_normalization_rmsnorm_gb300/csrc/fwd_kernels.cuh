@@ -28,31 +28,64 @@
 
 namespace rmsn {
 
+// Register budget of the vector forward: its CTAs hold a row (or a team's
+// rows) in registers only between the loads and the stores, so the number
+// of rows in flight per SM, and with it the bandwidth of a short call, is
+// the number of resident CTAs. Left to itself the compiler gives the
+// four-chunk plans 69-72 registers a thread: three 256-thread CTAs an SM
+// (one of 512 threads). The bound below asks for the registers of
+// RMSNORM_FWD_OCC 256-thread CTAs an SM: at 5, 48 registers (a few bytes
+// of spill in the four-chunk plans) and two 512-thread CTAs an SM.
+// Measured on bf16 rows, sustained calls: 4096x7168 27.3 -> 23.0 us,
+// 16384x8192 93.5 -> 82.6 us, 4096x16384 71.0 -> 47.9 us (4 a little
+// slower at 4096x7168, 24.5 us; the same elsewhere).
+#ifndef RMSNORM_FWD_OCC
+#define RMSNORM_FWD_OCC 5
+#endif
+template <int THREADS>
+constexpr int fwd_min_blocks() {
+    return THREADS >= 1024 || RMSNORM_FWD_OCC * 256 / THREADS < 1 ? 1 : RMSNORM_FWD_OCC * 256 / THREADS;
+}
+
 // The row's chunks into registers; with FUSED, h = R(x + residual) is
 // formed in place and stored to residual_out. Chunks past the row are zero.
-// Rows are C chunks apart; rows at a common offset (p.peel) wrap chunk 0.
+// Rows are C chunks apart. Rows at a common offset (p.peel) wrap chunk 0:
+// its thread (t = 0 of the slice holding chunk 0, always chunk slot v = 0)
+// loads the second aligned block beside its other loads and merges the two
+// once every load is in flight, so no warp waits on a load before issuing
+// the rest.
 template <typename T, int TPR, int V, bool FUSED>
 __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, int C, int cbase, int t, int cend,
                                              bool valid, uint4 (&xv)[V]) {
     using Pk = Pair<true>;
     constexpr int NP = Elem<T>::NP;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    const bool wrap0 = p.peel != 0 && cbase + t == 0;
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x) + base;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
-        xv[v] = c < cend ? ld_row_chunk<T>(reinterpret_cast<const uint4 *>(p.x) + base, c, C, p.peel)
-                         : make_uint4(0, 0, 0, 0);
+        xv[v] = c < cend ? ld_stream(x4 + c) : zero;
     }
-    if constexpr (FUSED) {
+    const uint4 xt = wrap0 ? ld_stream(x4 + C) : zero;
+    if constexpr (!FUSED) {
+        if (wrap0) xv[0] = wrap_chunk<T>(xv[0], xt, p.peel);
+    } else {
         // h = R(x + residual). For bf16 inputs the fp32 sum is exact unless
         // the exponents differ by more than 15, and then both it and the
         // exact sum round to the larger operand: one rounding to bf16 gives
         // the correctly rounded sum. For fp32 the add is the rounding.
         uint4 rv[V];
+        const uint4 *r4 = reinterpret_cast<const uint4 *>(p.residual) + base;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = cbase + v * TPR + t;
-            rv[v] = c < cend ? ld_row_chunk<T>(reinterpret_cast<const uint4 *>(p.residual) + base, c, C, p.peel)
-                          : make_uint4(0, 0, 0, 0);
+            rv[v] = c < cend ? ld_stream(r4 + c) : zero;
+        }
+        const uint4 rt = wrap0 ? ld_stream(r4 + C) : zero;
+        if (wrap0) {
+            xv[0] = wrap_chunk<T>(xv[0], xt, p.peel);
+            rv[0] = wrap_chunk<T>(rv[0], rt, p.peel);
         }
 #pragma unroll
         for (int v = 0; v < V; ++v) {
@@ -76,7 +109,8 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
 // E4M3(y * s), one byte per element, with s the given per-tensor scale or
 // 448 / max|y| of the row (a second, max-combining row reduction).
 template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED, int Q = QOUT_NONE>
-__global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR * TEAMS) > 0 ? 1280 / (TPR * TEAMS) : 1))
+__global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? fwd_min_blocks<TPR * TEAMS>()
+                                                               : (1280 / (TPR * TEAMS) > 0 ? 1280 / (TPR * TEAMS) : 1))
     rmsnorm_fwd_vector(const FwdParams p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
     using Pk = Pair<true>;
@@ -84,6 +118,10 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
     constexpr int W = TPR > 32 ? TPR / 32 : 1;
     __shared__ float red[TEAMS][W * CS];
     __shared__ float redm[Q == QOUT_NONE ? 1 : TEAMS][W * CS];  // the max reduction's slots
+    // the kernel before it has completed; the next may launch once every
+    // CTA of this one has started (no CTA of this grid is then waiting)
+    pdl_wait();
+    pdl_trigger();
 
     const int team = threadIdx.x / TPR;
     const int t = threadIdx.x % TPR;
@@ -130,6 +168,14 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
     const bool has_w = p.w != nullptr;  // no weight: non-affine, factor 1
     if constexpr (Q == QOUT_NONE) {
         if (!valid) return;
+        // the wrapped chunk's weights (the weight shares the rows' offset)
+        uint4 wwrap = make_uint4(0, 0, 0, 0);
+        if constexpr (std::is_same<T, TW>::value) {
+            if (has_w && p.peel != 0 && cbase + t == 0) {
+                const uint4 *w4 = reinterpret_cast<const uint4 *>(p.w);
+                wwrap = wrap_chunk<T>(ld_keep(w4), ld_keep(w4 + C), p.peel);
+            }
+        }
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = cbase + v * TPR + t;
@@ -138,7 +184,10 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
                 unpack<T>(xv[v], a);
                 if (has_w) {
                     float2 wv[NP];
-                    load_w_chunk_row<T, TW>(p.w, c, C, p.peel, wv);
+                    if (std::is_same<T, TW>::value && p.peel != 0 && c == 0)
+                        unpack<T>(wwrap, wv);
+                    else
+                        load_w_chunk<T, TW>(p.w, c, wv);
 #pragma unroll
                     for (int k = 0; k < NP; ++k) a[k] = Pk::mul(Pk::mul(a[k], r2), Pk::add(o2, wv[k]));
                 } else {
@@ -211,6 +260,8 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? 1 : (1280 / (TPR 
 template <typename T, typename TW, bool FUSED, int Q = QOUT_NONE>
 __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     __shared__ float red[32];
+    pdl_wait();
+    pdl_trigger();
     constexpr int NP = Elem<T>::NP;
     const int64_t row = blockIdx.x;
     const int N = p.N;
@@ -327,6 +378,8 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     constexpr int NP = Elem<T>::NP;
     constexpr int W = TPR > 32 ? TPR / 32 : 1;
     __shared__ float red[TEAMS][W * CS], red2[TEAMS][W * CS];
+    pdl_wait();
+    pdl_trigger();
 
     const int team = threadIdx.x / TPR;
     const int t = threadIdx.x % TPR;
@@ -426,6 +479,8 @@ template <typename T, bool FUSED>
 __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) {
     __shared__ float red[32];
     extern __shared__ uint4 gen_smem[];
+    pdl_wait();
+    pdl_trigger();
     constexpr int E = Elem<T>::E;
     constexpr int NP = Elem<T>::NP;
     const int64_t row = blockIdx.x;
@@ -546,6 +601,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     __shared__ __align__(8) uint64_t rbar[2];  // cluster rows: arrival of the peers' sums
     __shared__ unsigned done[S];               // warps through the stage's row
     extern __shared__ float4 fstage_smem[];    // ns * NB * Cb chunks of 16 bytes
+    pdl_wait();  // before any read of the rows (the bulk copies included)
 
     const int N = p.N;
     const int C = N / E;
@@ -810,6 +866,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
         }
     }
     if (failed && p.status) *p.status = kStatusWaitTimeout;
+    pdl_trigger();  // every row done: the next kernel may launch
     // no CTA leaves while a peer may still store into its shared memory
     if constexpr (CS > 1) cluster_sync();
 }
@@ -831,48 +888,18 @@ static int launch_fwd_staged_kernel(const void *k, int cs, int threads, const Fw
                                     void *stream) {
     const int e = allow_staged_smem(k);
     if (e != 0) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3((unsigned)threads);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    LaunchCfg lc((unsigned)grid, (unsigned)threads, (size_t)smem, static_cast<cudaStream_t>(stream), (unsigned)cs);
     void *args[] = {const_cast<FwdParams *>(&p)};
-    return (int)cudaLaunchKernelExC(&cfg, k, args);
+    return (int)cudaLaunchKernelExC(&lc.cfg, k, args);
 }
 
 // ------------------------------------------------------------- dispatch --
 
 template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, int Q>
 static int launch_vec(bool fused, const FwdParams &p, int grid, void *stream) {
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if constexpr (CS == 1) {
-        if (fused)
-            rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, 1, true, Q><<<grid, TPR * TEAMS, 0, s>>>(p);
-        else
-            rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, 1, false, Q><<<grid, TPR * TEAMS, 0, s>>>(p);
-        return (int)cudaGetLastError();
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(TPR * TEAMS);
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CS;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return fused ? (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true, Q>, p)
-                     : (int)cudaLaunchKernelEx(&cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false, Q>, p);
-    }
+    LaunchCfg lc((unsigned)grid, TPR * TEAMS, 0, static_cast<cudaStream_t>(stream), CS > 1 ? CS : 0);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true, Q>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false, Q>, p);
 }
 
 template <typename T, typename TW, int TPR, int V, int TEAMS, int CS>
@@ -890,12 +917,9 @@ static int gen_cache_bytes(const FwdParams &p) {
 
 template <typename T, typename TW, int Q>
 static int launch_gen(bool fused, const FwdParams &p, int grid, void *stream) {
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (fused)
-        rmsnorm_fwd_generic<T, TW, true, Q><<<grid, 256, 0, s>>>(p);
-    else
-        rmsnorm_fwd_generic<T, TW, false, Q><<<grid, 256, 0, s>>>(p);
-    return (int)cudaGetLastError();
+    LaunchCfg lc((unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream));
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_fwd_generic<T, TW, true, Q>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_fwd_generic<T, TW, false, Q>, p);
 }
 
 template <typename T, typename TW>
@@ -1035,31 +1059,13 @@ static int ln_launch_entry(bool fused, const FwdParams &p, int grid, void *strea
     if constexpr (OP != OP_FWD || !(PATH == PATH_GENERIC || CMIN > 0)) {
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
-        if (fused)
-            layernorm_fwd_generic<T, true><<<grid, 256, gen_cache_bytes<T>(p), s>>>(p);
-        else
-            layernorm_fwd_generic<T, false><<<grid, 256, gen_cache_bytes<T>(p), s>>>(p);
-        return (int)cudaGetLastError();
-    } else if constexpr (CS == 1) {
-        if (fused)
-            layernorm_fwd_vector<T, TPR, V, TEAMS, 1, true><<<grid, TPR * TEAMS, 0, s>>>(p);
-        else
-            layernorm_fwd_vector<T, TPR, V, TEAMS, 1, false><<<grid, TPR * TEAMS, 0, s>>>(p);
-        return (int)cudaGetLastError();
+        LaunchCfg lc((unsigned)grid, 256, (size_t)gen_cache_bytes<T>(p), s);
+        return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_generic<T, true>, p)
+                     : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_generic<T, false>, p);
     } else {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(TPR * TEAMS);
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CS;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return fused ? (int)cudaLaunchKernelEx(&cfg, layernorm_fwd_vector<T, TPR, V, TEAMS, CS, true>, p)
-                     : (int)cudaLaunchKernelEx(&cfg, layernorm_fwd_vector<T, TPR, V, TEAMS, CS, false>, p);
+        LaunchCfg lc((unsigned)grid, TPR * TEAMS, 0, s, CS > 1 ? CS : 0);
+        return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_vector<T, TPR, V, TEAMS, CS, true>, p)
+                     : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_vector<T, TPR, V, TEAMS, CS, false>, p);
     }
 }
 

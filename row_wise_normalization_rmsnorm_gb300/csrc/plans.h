@@ -33,6 +33,12 @@ constexpr bool staged_path(int path) { return path == PATH_STAGED || path == PAT
 constexpr bool staged_plan(int path, int teams, int cs) {
     return teams == 1 && ((path == PATH_STAGED && cs == 1) || (path == PATH_RESTAGED && (cs == 1 || cs == 2 || cs == 4 || cs == 8)));
 }
+// The staged backward is compiled with packed f32x2 arithmetic and, for the
+// default plans of fp32 and bf16 (weight in the activations' type: kernel
+// kinds 0 and 1), also with per-lane fp32 arithmetic in the same pairing,
+// for A/B measurements of the packed math; the two agree bit for bit.
+constexpr bool staged_scalar_variant(int kind, int cmin) { return (kind == 0 || kind == 1) && cmin > 0; }
+
 // Storage types a default plan applies to (bit 0: fp32, bit 1: bf16,
 // bit 2: fp16; DT_16 = both 2-byte types).
 enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };

@@ -50,6 +50,28 @@ def test_packed_matches_scalar_bitwise(rn, dt, M, N, fused):
     assert cuda_bits_equal(dx1, dx0) and cuda_bits_equal(dw1, dw0)
 
 
+@pytest.mark.parametrize("dt,M,N", [("bf16", 600, 8192), ("bf16", 400, 16384), ("f32", 500, 6144), ("f32", 300, 2048),
+                                    ("bf16", 200, 32768), ("bf16", 300, 4096)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_staged_packed_matches_scalar_bitwise(rn, dt, M, N, fused):
+    """The staged backward's packed f32x2 arithmetic and its scalar variant
+    (same pairing, same CTA count) give the same bits, on the held and
+    re-read schedules and on cluster rows; fp16 refuses the scalar one."""
+    _, t = dev_inputs(M, N, dt, 93, residual=fused, dres=fused)
+    _, rstd = rn.rmsnorm_fwd(t["x"], t["w"])
+    kw = dict(dresidual_out=t.get("dres"), fused=fused)
+    dx1, dw1, p1 = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], rstd, force_packed=1, **kw)
+    dx0, dw0, p0 = rn.rmsnorm_bwd_ex(t["dy"], t["x"], t["w"], rstd, force_packed=0, **kw)
+    torch.cuda.synchronize()
+    assert p1["path_name"] == p0["path_name"] == "staged" and p1["plan_id"] == p0["plan_id"]
+    assert p1["packed"] == 1 and p0["packed"] == 0 and p1["ctas"] == p0["ctas"]
+    assert cuda_bits_equal(dx1, dx0) and cuda_bits_equal(dw1, dw0)
+    _, h = dev_inputs(64, 8192, "f16", 94)
+    _, r16 = rn.rmsnorm_fwd(h["x"], h["w"])
+    with pytest.raises(rn.RMSNormError):
+        rn.rmsnorm_bwd_ex(h["dy"], h["x"], h["w"], r16, force_packed=0)
+
+
 def test_graph_replay_matches_direct(rn):
     _, t = dev_inputs(1000, 4096, "bf16", 91)
     ws = torch.empty(rn.rmsnorm_bwd_workspace_bytes(1000, 4096, torch.bfloat16), dtype=torch.uint8, device="cuda")
