@@ -57,6 +57,10 @@ def parse():
                     help="time the staged backward with packed f32x2 and with scalar fp32 arithmetic at the "
                          "wide-row shapes (bf16 16384x8192, fp32 16384x6144); one JSON line per variant")
     ap.add_argument("--ab-iters", type=int, default=50)
+    ap.add_argument("--ab-reps", type=int, default=4)
+    ap.add_argument("--profile-run", action="store_true",
+                    help="warm-up and timed steps only (no host-enqueue, workspace-NULL, per-op split, e2e, "
+                         "oracle or clock legs): a short program for ncu captures of the bench's kernels")
     return ap.parse_args()
 
 
@@ -515,7 +519,7 @@ def run_packed_ab(args):
         ws = torch.empty(rn.rmsnorm_bwd_workspace_bytes(M, N, td), dtype=torch.uint8, device=dev)
         times = {0: [], 1: []}
         plans = {}
-        for rep in range(4):
+        for rep in range(args.ab_reps):
             for pk in (1, 0):
                 for _ in range(3):
                     _, _, plans[pk] = rn.rmsnorm_bwd_ex(dy, x, w, rstd, dx=dx, dw=dw, workspace=ws, force_packed=pk)
@@ -613,7 +617,7 @@ def main():
     if world > 1:
         dist.barrier()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local, enabled=not args.no_clocks) as clk:
+    with ClockSampler(local, enabled=not (args.no_clocks or args.profile_run)) as clk:
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -625,6 +629,13 @@ def main():
     if world > 1:
         dist.barrier()
     total_ms = max_over_ranks(start.elapsed_time(end), dist if world > 1 else None, dev)
+    if args.profile_run:
+        if rank == 0:
+            print(json.dumps({"profile_run": WORKLOAD_DESC, "steps": K, "ms_per_step": total_ms / K,
+                              "gpu_launches": 3 * K}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
     for i in range(nsplit):
         step(ev[i])
     torch.cuda.synchronize()
