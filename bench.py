@@ -324,10 +324,13 @@ def run_sweep(args):
     Inputs are N(0,1) draws made on the device (timing only; parity uses the
     seeded host recipe).
 
-    sustained: K calls back to back between one pair of events, cycling
-      over R sets of the call's arrays whose inputs together exceed three
-      times the L2 size, so every call reads its inputs from HBM while the
-      launches overlap as in a training step; us = elapsed / K.
+    sustained: calls back to back, cycling over R sets of the call's arrays
+      whose inputs together exceed three times the L2 size, so every call
+      reads its inputs from HBM while the launches overlap as in a training
+      step. The calls are captured once into a CUDA graph (programmatic
+      dependencies included) and the graph replayed between one pair of
+      events, so host-side call overhead cannot starve the GPU on short
+      calls; us = elapsed / calls.
     isolated: before every call a buffer twice the L2 size is read (a sum),
       outside the event bracket, then one event pair brackets the call; the
       bracket itself costs what the empty-kernel line reports (launch and
@@ -365,14 +368,26 @@ def run_sweep(args):
         for i in range(2 * R):
             fn(i)
         torch.cuda.synchronize()
-        K = max(iters, 4 * R)
+        K = 4 * R   # calls in the graph: every set four times
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for i in range(K):
+                    fn(i)
+        torch.cuda.current_stream().wait_stream(side)
+        reps = max(1, -(-iters // K))
+        graph.replay()
+        torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        for i in range(K):
-            fn(i)
+        for _ in range(reps):
+            graph.replay()
         b.record()
         torch.cuda.synchronize()
-        return a.elapsed_time(b) * 1e3 / K
+        del graph
+        return a.elapsed_time(b) * 1e3 / (K * reps)
 
     # the bracket's own cost: an empty kernel, and a forward of one 8-element row
     one = torch.zeros(1, device=dev)
@@ -593,7 +608,7 @@ def main():
     K, W = args.steps, args.warmup
     # per-op split, measured outside the timed region: an event between two
     # kernels also ends the programmatic dependency between them
-    nsplit = min(K, 200)
+    nsplit = K
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nsplit)]
     # torch creates an event on its first record(); materialise them up front
     for e in ev:

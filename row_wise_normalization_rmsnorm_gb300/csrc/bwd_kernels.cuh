@@ -1049,13 +1049,26 @@ __global__ void __launch_bounds__(LANES *RG) rmsnorm_dw_finalize4(const float *w
     if (col < N) {
         const float4 *src = reinterpret_cast<const float4 *>(ws + col);
         const int64_t stride = N / 4;
-#pragma unroll 4
-        for (int q = p0; q < p1; ++q) {
-            const float4 v = src[(int64_t)q * stride];
+        auto add = [&](const float4 &v) {
             s.x = __fadd_rn(s.x, v.x);
             s.y = __fadd_rn(s.y, v.y);
             s.z = __fadd_rn(s.z, v.z);
             s.w = __fadd_rn(s.w, v.w);
+        };
+        // up to kBatch rows a group (P <= 32 * kBatch): every load in flight
+        // at once, one round trip to L2, then the adds in row order
+        constexpr int kBatch = 16;
+        if (p1 - p0 <= kBatch) {
+            float4 v[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                if (p0 + i < p1) v[i] = src[(int64_t)(p0 + i) * stride];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                if (p0 + i < p1) add(v[i]);
+        } else {
+#pragma unroll 4
+            for (int q = p0; q < p1; ++q) add(src[(int64_t)q * stride]);
         }
     }
     part[rg][lane * 4 + 0] = s.x;
