@@ -308,8 +308,10 @@ def sweep_points():
     pts.append(("misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
     pts.append(("misaligned f32 4096x2048", "f32", 4096, 2048, False, True))
     pts.append(("ln misaligned bf16 4096x7168", "bf16", 4096, 7168, False, True))
-    # a row length that is no multiple of 16 bytes: the generic kernels
+    # a row length that is no multiple of 16 bytes, and rows whose x and dy
+    # sit at different addresses mod 16: the generic kernels
     pts.append(("oddn bf16 4096x7169", "bf16", 4096, 7169, False, False))
+    pts.append(("skew bf16 4096x7168", "bf16", 4096, 7168, False, True))
     pts.append(("wide f32 16384x6144", "f32", 16384, 6144, False, False))
     # rows wider than one CTA's stages: a cluster of CTAs shares each row
     for M, N in ((16384, 20480), (8192, 32768), (2048, 65536)):
@@ -403,11 +405,13 @@ def run_sweep(args):
         s = 4 if dt == "f32" else 2
         off = 1 if mis else 0
 
-        def mk(n, dtype=td):
-            buf = torch.randn(n + off, generator=g, device=dev, dtype=torch.float32).to(dtype)
-            return buf[off:off + n]
+        def mk(n, dtype=td, o=None):
+            o = off if o is None else o
+            buf = torch.randn(n + o, generator=g, device=dev, dtype=torch.float32).to(dtype)
+            return buf[o:o + n]
 
         affine = not label.startswith("nonaffine")
+        skew = label.startswith("skew")
         ln = label.startswith("ln ")
         fp8 = label.startswith("fp8")
         wtd = torch.float32 if label.startswith("w32") else td
@@ -425,7 +429,9 @@ def run_sweep(args):
         R = max(2, -(-3 * l2 // in_bytes))
 
         def make_set():
-            st = {"x": mk(M * N).view(M, N), "dy": mk(M * N).view(M, N), "y": mk(M * N).view(M, N),
+            # skew: dy (and dx) one element further from a 16-byte boundary than x
+            st = {"x": mk(M * N).view(M, N), "dy": mk(M * N, o=2 if skew else None).view(M, N),
+                  "y": mk(M * N).view(M, N),
                   "dx": mk(M * N).view(M, N), "rstd": torch.empty(M, dtype=torch.float32, device=dev),
                   "mean": torch.empty(M, dtype=torch.float32, device=dev)}
             if fused:

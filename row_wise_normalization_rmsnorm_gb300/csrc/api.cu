@@ -86,11 +86,45 @@ static const PlanDesc *generic_plan(int op) {
     return nullptr;
 }
 
+// The streamed generic backward's shared memory: `depth` stages of the x
+// and dy (and dres) row covers.
+static int64_t stream_smem_at(int64_t N, int es, bool fused, int depth) {
+    return (int64_t)depth * (fused ? 3 : 2) * stream_slot_bytes(N, es);
+}
+
 static int cta_threads(const PlanDesc &d) { return d.path == PATH_GENERIC ? 256 : d.tpr * d.teams; }
 
 // Largest dynamic shared memory a plan may ask for: the 227 KB a CTA may
 // opt into on sm_103a, less room for the kernels' static arrays.
 constexpr int kMaxDynamicSmem = 226 * 1024;
+
+// Stages a streamed generic backward takes: the plan's depth, or fewer
+// (at least two) where the covers would not fit; 0: none fits.
+static int stream_depth(const PlanDesc &d, int64_t N, int es, bool fused) {
+    for (int k = d.depth; k >= 2; --k)
+        if (stream_smem_at(N, es, fused, k) <= kMaxDynamicSmem) return k;
+    return 0;
+}
+
+// Whether the streamed generic backward takes rows of N elements.
+static bool stream_fits(const PlanDesc &d, int64_t N, int es) {
+    return N <= (int64_t)d.tpr * d.v && stream_depth(d, N, es, true) >= 2;
+}
+
+// The plan for rows no vectorised plan takes: for the backward, the
+// streamed plan whose range holds N (where its stages fit), else the
+// one-CTA-a-row kernel.
+static const PlanDesc *fallback_plan(int op, int64_t N, int es) {
+    if (op == OP_BWD) {
+        for (int i = 0; i < kNumPlans; ++i) {
+            const PlanDesc &d = kPlans[i];
+            if (d.op == op && d.path == PATH_STREAM && d.cmin > 0 && N >= d.cmin && N <= d.cmax &&
+                stream_fits(d, N, es))
+                return &d;
+        }
+    }
+    return generic_plan(op);
+}
 // Longest row (bytes) the generic LayerNorm forward keeps in shared memory
 // between its three passes: eight 256-thread CTAs an SM still fit. (The
 // RMSNorm forward, two passes, measured slower with the cache.)
@@ -146,6 +180,8 @@ static int64_t staged_smem_bytes(const PlanDesc &d, int64_t C, int peel, bool fu
 }
 
 static int nominal_ctas_per_sm(const PlanDesc &d) {
+    // the streamed kernels' register budget (their launch bounds)
+    if (d.path == PATH_STREAM) return d.tpr >= 512 ? 1 : 512 / d.tpr;
     const int t = cta_threads(d);
     int c = 2048 / t;
     return c < 1 ? 1 : c;
@@ -187,6 +223,8 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, int pe
         if (d->path == PATH_VECTOR && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
         // staged plans: aligned rows that fit
         if (staged_path(d->path) && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
+        // the streamed generic kernel: rows of any layout that it holds
+        if (d->path == PATH_STREAM && !stream_fits(*d, N, s)) return RMSNORM_ERR_UNSUPPORTED;
         // with an fp32 weight only the default plans (and the generic one) are compiled
         if (mixed_kind(kind_of(dt)) && row_path(d->path) && d->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
     } else {
@@ -196,19 +234,20 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, int pe
             const PlanDesc *sd = default_vector_plan(OP_FWD_STAGED, dt, C);
             if (sd) d = sd;
         }
-        if (!d) d = generic_plan(op);
+        if (!d) d = fallback_plan(op, N, s);
     }
     if (!d) return RMSNORM_ERR_UNSUPPORTED;
 
     std::memset(out, 0, sizeof(*out));
-    out->path = staged_path(d->path) ? PATH_STAGED : d->path;  // the ABI names one staged path
-    out->peel = (d->path != PATH_GENERIC && peel > 0) ? peel : 0;
+    // the ABI names one staged path and one generic path
+    out->path = staged_path(d->path) ? PATH_STAGED : (generic_path(d->path) ? PATH_GENERIC : d->path);
+    out->peel = (!generic_path(d->path) && peel > 0) ? peel : 0;
     out->plan_id = d->id;
     out->threads_per_row = d->path == PATH_GENERIC ? 256 : d->tpr;
-    out->chunks_per_thread = d->v;
+    out->chunks_per_thread = generic_path(d->path) ? 0 : d->v;  // generic kernels hold no chunks
     out->rows_per_cta = d->path == PATH_GENERIC ? 1 : d->teams;
     out->cta_threads = cta_threads(*d);
-    out->packed = d->path == PATH_GENERIC ? 0 : 1;
+    out->packed = generic_path(d->path) ? 0 : 1;
     out->cluster_size = d->cs;
     const int64_t units = (M + out->rows_per_cta - 1) / out->rows_per_cta;  // CTAs (or clusters) with rows
     const bool staged_fwd = d->op == OP_FWD_STAGED;
@@ -231,7 +270,10 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, int pe
         if (sm > kMaxDynamicSmem) return RMSNORM_ERR_UNSUPPORTED;
         out->smem_bytes = (int32_t)sm;
     }
-    if (!staged_path(d->path) && out->smem_bytes > 44 * 1024) return RMSNORM_ERR_UNSUPPORTED;
+    if (d->path == PATH_STREAM)  // the plain variant's stages; the fused one is set by the backward
+        out->smem_bytes = (int32_t)stream_smem_at(N, s, false, stream_depth(*d, N, s, false));
+    else if (!staged_path(d->path) && out->smem_bytes > 44 * 1024)
+        return RMSNORM_ERR_UNSUPPORTED;
     const int64_t bytes = staged_fwd ? 0 : P * partial_rows(op) * N * 4;  // the forward has no partial rows
     out->workspace_bytes = (bytes + 255) / 256 * 256;
     return RMSNORM_SUCCESS;
@@ -440,21 +482,24 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
     const int E = 16 / elem_size(dt);
     // The dynamic shared memory of the team combine depends on N; occupancy
     // is taken for the largest N the plan serves (the conservative value).
-    const int64_t nmax = d.path != PATH_GENERIC ? plan_capacity(d) * E : N;
+    const int64_t nmax = !generic_path(d.path) ? plan_capacity(d) * E : N;
     // (a staged plan's rows may need less than its capacity: the occupancy
     // query is capped at the largest shared memory a CTA may take)
     const int smem = staged_path(d.path)
                          ? (int)std::min<int64_t>(staged_smem_bytes(d, plan_capacity(d), 1, fused), kMaxDynamicSmem)
+                     : d.path == PATH_STREAM
+                         ? (int)std::min<int64_t>(stream_smem_at((int64_t)d.tpr * d.v, elem_size(dt), fused, d.depth),
+                                                  kMaxDynamicSmem)
                          : bwd_smem_bytes(d, nmax);
     int best = 1 << 30;
     for (int pk = 0; pk < 2; ++pk) {
         // the LayerNorm and generic kernels have one variant; a staged plan
         // has the scalar one only where staged_scalar_variant says so
-        if ((d.path == PATH_GENERIC || d.op == OP_LN_BWD) && pk == 1) continue;
+        if ((generic_path(d.path) || d.op == OP_LN_BWD) && pk == 1) continue;
         if (staged_path(d.path) && pk == 0 && !staged_scalar_variant(kind_of(dt), d.cmin)) continue;
         const void *k = d.op == OP_LN_BWD ? ln_bwd_kernel(d.id, dt, fused) : bwd_kernel(d.id, dt, fused, pk != 0);
         if (!k) return cudaErrorInvalidDeviceFunction;
-        if (staged_path(d.path)) {  // more than 48 KB of dynamic shared memory needs an opt-in
+        if (staged_path(d.path) || d.path == PATH_STREAM) {  // more than 48 KB of dynamic shared memory needs an opt-in
             cudaError_t e = (cudaError_t)allow_staged_smem(k);
             if (e != cudaSuccess) return e;
         }
@@ -626,6 +671,16 @@ int self_check_impl() {
         }
         if (!generic_plan(op)) ++bad;
     }
+    // streamed backward defaults: ranges of N tiling [1, max] in table order
+    {
+        int64_t expect = 1;
+        for (int i = 0; i < kNumPlans; ++i) {
+            const PlanDesc &d = kPlans[i];
+            if (d.path != PATH_STREAM || d.cmin == 0) continue;
+            if (d.cmin != expect || d.cmax < d.cmin) ++bad;
+            expect = d.cmax + 1;
+        }
+    }
     // staged forward defaults: contiguous ranges (they need not start at 1),
     // each selecting its entry and held by it
     for (int dt = 0; dt < 3; ++dt) {
@@ -658,6 +713,12 @@ int self_check_impl() {
                 d.tpr > kMaxCtaThreads || d.v < 1)
                 ++bad;
         }
+        // the streamed generic kernel: a backward of whole warps with 2..8
+        // stages that holds the longest row of its range
+        if (d.path == PATH_STREAM && (d.op != OP_BWD || d.tpr % 32 != 0 || d.tpr < 64 || d.tpr > kMaxCtaThreads ||
+                                      d.v < 1 || d.depth < 2 || d.depth > 8 || d.teams != 1 ||
+                                      d.cs != 1 || (int64_t)d.tpr * d.v < d.cmax))
+            ++bad;
         if (d.dtm < 1 || d.dtm > DT_ANY) ++bad;
         if (d.id < 0 || d.id >= kMaxPlanId) ++bad;
     }
@@ -866,6 +927,10 @@ static rmsnorm_status_t plan_bwd_call(int op, const void *dy, const void *dres, 
     if (st != RMSNORM_SUCCESS) return st;
     // the stages this call's rows take (the fused variant holds three rows a stage)
     if (c->plan.path == PATH_STAGED) c->plan.smem_bytes = (int32_t)staged_smem_bytes(*c->d, C, c->plan.peel, fused);
+    if (c->d->path == PATH_STREAM) {
+        const int es = elem_size(dt);
+        c->plan.smem_bytes = (int32_t)stream_smem_at(N, es, fused, stream_depth(*c->d, N, es, fused));
+    }
     return RMSNORM_SUCCESS;
 }
 
@@ -956,7 +1021,9 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     p.N = (int)N;
     p.offset = offset;
     p.peel = pl;
-    p.stages = staged_path(d->path) ? staged_depth(*d, N * es / 16, pl, fused) : 0;
+    p.stages = staged_path(d->path)       ? staged_depth(*d, N * es / 16, pl, fused)
+               : d->path == PATH_STREAM ? stream_depth(*d, N, es, fused)
+                                        : 0;
     int le = launch_bwd_dt(dt, plan.plan_id, fused, packed, p, plan.ctas, plan.smem_bytes, stream);
     if (le == 0 && event_after_main) le = (int)cudaEventRecord(static_cast<cudaEvent_t>(event_after_main), stream);
     if (le == 0 && affine)

@@ -889,6 +889,156 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const BwdParams p) {
     pdl_trigger();  // this CTA's rows done (the finalizer waits for the whole grid)
 }
 
+// Streamed generic main kernel: persistent CTAs, rows of any alignment and
+// of at most TPR * K elements. Row k of a CTA streams into stage k mod ns
+// by bulk copies of the 16-byte covers (cover16) of its x and dy (and dres)
+// rows, each array's row at its own offset within its first block, so the
+// arrays need not share an address mod 16 and N need not fill whole
+// blocks. The row's rstd travels with it (a 4-byte asynchronous copy into
+// the stage, counted as the stage barrier's second arrival), so no global
+// load sits on a row's critical path. Thread t owns columns t + i TPR
+// (i < K) of every row: its share of the dW partial row stays in registers
+// for the whole kernel and is written to the workspace once. Each thread
+// reads its elements of the stage into registers before the row
+// reduction's barrier; right after the barrier thread 0 refills the stage
+// with row k + ns, as the staged kernels do. dx is stored element by
+// element: a row's first and last 16-byte blocks may hold a neighbouring
+// row, which another CTA writes. The arithmetic is the staged kernels' in
+// per-lane fp32: g = dy (offset + w), c = rstd (sum g x) / N,
+// dx = (xhat (-c) + g) rstd (+ dres), dW += dy xhat. Every wait is bounded:
+// one that gives up records the status word, waits (again bounded) for the
+// stages' last copies and lets the kernel end.
+template <typename T, typename TW, int TPR, int K, int SMAX, bool FUSED>
+__global__ void __launch_bounds__(TPR, TPR >= 512 ? 1 : 512 / TPR) rmsnorm_bwd_stream(const BwdParams p) {
+    static_assert(TPR % 32 == 0 && TPR >= 64 && TPR <= 1024, "whole warps");
+    constexpr int W = TPR / 32;
+    constexpr int NB = FUSED ? 3 : 2;  // arrays a stage holds: x, dy (, dres)
+    __shared__ float red[2][W];
+    __shared__ __align__(8) uint64_t full[SMAX];
+    __shared__ float rs_ring[SMAX];         // the stage's row rstd
+    extern __shared__ float4 stage_smem[];  // ns * NB slots of stream_slot_bytes(N, sizeof(T))
+    pdl_wait();  // before any read of the rows (the bulk copies included)
+    const int N = p.N;
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int ns = p.stages;  // 2 .. SMAX, chosen by the host to fit
+    const int64_t G = gridDim.x;
+    const int64_t unit = blockIdx.x;
+    const int64_t iters = unit < p.M ? (p.M - unit + G - 1) / G : 0;
+    const bool has_dres = FUSED && p.dres != nullptr;
+    const bool has_w = p.w != nullptr;
+    const uint32_t rb = (uint32_t)N * (uint32_t)sizeof(T);  // bytes of a row
+    const uint32_t slot = (uint32_t)stream_slot_bytes(N, (int)sizeof(T));
+    char *const stages = reinterpret_cast<char *>(stage_smem);
+    const char *gx = static_cast<const char *>(p.x);
+    const char *gd = static_cast<const char *>(p.dy);
+    const char *gr = static_cast<const char *>(p.dres);
+    // thread 0: the covers of row k's arrays, and its rstd, into stage s
+    auto issue = [&](int64_t k, int s) {
+        const int64_t row = unit + k * G;
+        const int64_t off = row * (int64_t)rb;
+        const Cover cx = cover16(gx + off, rb);
+        const Cover cd = cover16(gd + off, rb);
+        const Cover cr = has_dres ? cover16(gr + off, rb) : Cover{nullptr, 0u, 0u};
+        char *dst = stages + (size_t)s * NB * slot;
+        mbar_arrive_expect_tx(&full[s], cx.bytes + cd.bytes + cr.bytes);
+        bulk_g2s(dst, cx.src, cx.bytes, &full[s]);
+        bulk_g2s(dst + slot, cd.src, cd.bytes, &full[s]);
+        if (has_dres) bulk_g2s(dst + 2 * slot, cr.src, cr.bytes, &full[s]);
+        cp_async4(&rs_ring[s], p.rstd + row);
+        cp_async_arrive_noinc(&full[s]);
+    };
+    // (offset + w) of this thread's columns, and its dW partials
+    const TW *w = static_cast<const TW *>(p.w);
+    float wf[K], acc[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        const int j = t + i * TPR;
+        wf[i] = (has_w && j < N) ? __fadd_rn(p.offset, load_w(w, j)) : 1.f;
+        acc[i] = 0.f;
+    }
+    if (t == 0) {
+        // two arrivals a phase: the copies' announcement and the rstd copy's
+        for (int s = 0; s < ns; ++s) mbar_init(&full[s], 2);
+        mbar_init_fence();
+        for (int s = 0; s < ns && s < iters; ++s) issue(s, s);
+    }
+    __syncthreads();
+
+    bool failed = false;
+    int s = 0;        // stage of row k (k mod ns)
+    uint32_t ph = 0;  // parity of k / ns
+    for (int64_t k = 0; k < iters; ++k) {
+        const int64_t row = unit + k * G;
+        if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
+        const float r = rs_ring[s];  // read before the barrier that frees the stage
+        // element 0 of the row's arrays in the stage
+        const int64_t off = row * (int64_t)rb;
+        const char *sb = stages + (size_t)s * NB * slot;
+        const T *xs = reinterpret_cast<const T *>(sb + addr_mod16(gx + off));
+        const T *ds = reinterpret_cast<const T *>(sb + slot + addr_mod16(gd + off));
+        const T *rs = reinterpret_cast<const T *>(sb + 2 * slot + (has_dres ? addr_mod16(gr + off) : 0u));
+        float xv[K], dv[K], rv[FUSED ? K : 1];
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const int j = t + i * TPR;
+            const bool in = j < N;
+            xv[i] = in ? load_elem(xs, j) : 0.f;
+            dv[i] = in ? load_elem(ds, j) : 0.f;
+            if constexpr (FUSED) rv[i] = (in && has_dres) ? load_elem(rs, j) : 0.f;
+            dot = __fmaf_rn(__fmul_rn(dv[i], wf[i]), xv[i], dot);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, o));
+        float *slots = red[k & 1];
+        if (lane == 0) slots[t >> 5] = dot;
+        __syncthreads();
+        // every thread has its elements of stage s: refill it with row k + ns
+        if (t == 0 && k + ns < iters) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(k + ns, s);
+        }
+        if (++s == ns) {
+            s = 0;
+            ph ^= 1u;
+        }
+        const float cm = -__fdiv_rn(__fmul_rn(sum_slots<W>(slots, lane), r), (float)N);
+        T *dx = static_cast<T *>(p.dx) + row * (int64_t)N;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const int j = t + i * TPR;
+            if (j < N) {
+                const float xh = __fmul_rn(xv[i], r);
+                float d = __fmul_rn(__fmaf_rn(xh, cm, __fmul_rn(dv[i], wf[i])), r);
+                if constexpr (FUSED) {
+                    if (has_dres) d = __fadd_rn(d, rv[i]);
+                }
+                store_elem(dx, j, d);
+                acc[i] = __fmaf_rn(dv[i], xh, acc[i]);
+            }
+        }
+    }
+    if (failed) {
+        // the last copy into each stage has landed (or its wait gives up
+        // again) before the CTA ends
+        for (int s2 = 0; s2 < ns && s2 < iters; ++s2) {
+            const int64_t kl = s2 + (iters - 1 - s2) / ns * ns;
+            mbar_wait(&full[s2], (uint32_t)((kl / ns) & 1), kWaitLimit);
+        }
+        if (p.status) *p.status = kStatusWaitTimeout;
+    }
+    if (t == 0) cp_async_wait_all();
+    pdl_trigger();  // the finalizer waits for the whole grid before it reads
+    if (!has_w) return;
+    float *wsrow = p.ws + unit * (int64_t)N;
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        const int j = t + i * TPR;
+        if (j < N) wsrow[j] = acc[i];
+    }
+}
+
 // Generic LayerNorm backward, the same scheme: per row the pair (sum g,
 // sum g (x - mean)), then dx; the partial row ws[cta, 0..2N) holds dgamma
 // and dbeta, updated one column a thread. Each row is read three times
@@ -1131,7 +1281,21 @@ static int bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cu
 // plans (and the generic one) only; alternatives are for tuning.
 template <typename T, typename TW, int PATH, int CMIN>
 constexpr bool bwd_instantiated() {
-    return std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0;
+    return std::is_same<T, TW>::value || generic_path(PATH) || CMIN > 0;
+}
+
+// Streamed generic kernel: launched as a cluster of one CTA (its bulk
+// copies name a shared::cluster destination) with the stages' dynamic
+// shared memory.
+template <typename T, typename TW, int TPR, int K, int SMAX>
+static int bwd_launch_stream(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
+    const void *k = fused ? (const void *)rmsnorm_bwd_stream<T, TW, TPR, K, SMAX, true>
+                          : (const void *)rmsnorm_bwd_stream<T, TW, TPR, K, SMAX, false>;
+    const int e = allow_staged_smem(k);
+    if (e != 0) return e;
+    LaunchCfg lc((unsigned)grid, TPR, (size_t)smem, s, 1);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_stream<T, TW, TPR, K, SMAX, true>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_stream<T, TW, TPR, K, SMAX, false>, p);
 }
 
 // Staged kernel: launched as a cluster of CS CTAs (of one where a CTA
@@ -1167,6 +1331,8 @@ static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int gri
         LaunchCfg lc((unsigned)grid, 256, 0, s);
         return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_generic<T, TW, true>, p)
                      : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_generic<T, TW, false>, p);
+    } else if constexpr (PATH == PATH_STREAM) {
+        return bwd_launch_stream<T, TW, TPR, V, D>(fused, p, grid, smem, s);
     } else if constexpr (PATH == PATH_VECTOR) {
         return packed ? bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, true>(fused, p, grid, smem, s)
                       : bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, false>(fused, p, grid, smem, s);
@@ -1188,6 +1354,9 @@ static const void *bwd_ptr_entry(bool fused, bool packed) {
         return nullptr;
     } else if constexpr (PATH == PATH_GENERIC) {
         return fused ? (const void *)rmsnorm_bwd_generic<T, TW, true> : (const void *)rmsnorm_bwd_generic<T, TW, false>;
+    } else if constexpr (PATH == PATH_STREAM) {
+        return fused ? (const void *)rmsnorm_bwd_stream<T, TW, TPR, V, D, true>
+                     : (const void *)rmsnorm_bwd_stream<T, TW, TPR, V, D, false>;
     } else if constexpr (PATH == PATH_VECTOR) {
         if (packed)
             return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, true>

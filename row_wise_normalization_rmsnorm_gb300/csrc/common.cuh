@@ -578,6 +578,34 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Asynchronous copy of one 4-byte word from global into this CTA's shared
+// memory (both 4-byte aligned). cp_async_arrive_noinc makes `bar` receive
+// one arrival once every asynchronous copy this thread has issued so far
+// has landed; the arrival is one of those counted at mbar_init.
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The 16-byte cover of `bytes` bytes at address a: the whole 16-byte
+// blocks that hold them, starting `off` = a mod 16 bytes before a, a
+// multiple of 16 bytes long (what a bulk copy of a row at any alignment
+// moves). A 16-byte block never crosses a page, so a block that holds any
+// byte of an allocation can be read without a fault; the bytes of the
+// cover outside [a, a + bytes) are copied and never used.
+struct Cover {
+    const char *src;
+    uint32_t off, bytes;
+};
+__device__ __forceinline__ Cover cover16(const void *a, uint32_t bytes) {
+    const uintptr_t u = reinterpret_cast<uintptr_t>(a);
+    const uint32_t off = (uint32_t)u & 15u;
+    return Cover{reinterpret_cast<const char *>(u - off), off, (off + bytes + 15u) & ~15u};
+}
+
 // Store v at the address of `local_slot` in cluster CTA `cta` and count 4
 // bytes on that CTA's barrier at the address of `local_bar`.
 __device__ __forceinline__ void st_async_cluster(float *local_slot, uint64_t *local_bar, uint32_t cta, float v) {

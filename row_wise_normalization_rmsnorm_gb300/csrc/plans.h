@@ -26,7 +26,11 @@ enum PlanOp { OP_FWD = 0, OP_BWD = 1, OP_LN_BWD = 2, OP_FWD_STAGED = 3 };
 // copies a row's chunks into registers for both passes, the second reads
 // them from the stage in each pass (fewer registers, the stage stays busy
 // for the whole row). The C ABI reports both as the staged path.
-enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2, PATH_RESTAGED = 3 };
+// PATH_STREAM is a generic (any N, any alignment) backward that streams each
+// row's 16-byte covers into shared memory; the C ABI reports it as the
+// generic path.
+enum PlanPath { PATH_VECTOR = 0, PATH_STAGED = 1, PATH_GENERIC = 2, PATH_RESTAGED = 3, PATH_STREAM = 4 };
+constexpr bool generic_path(int path) { return path == PATH_GENERIC || path == PATH_STREAM; }
 constexpr bool staged_path(int path) { return path == PATH_STAGED || path == PATH_RESTAGED; }
 // The staged kernels run one row team a CTA; a row may be shared by a
 // cluster of CTAs only on the re-read schedule.
@@ -54,7 +58,12 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
 // cluster: CTAs of a thread-block cluster that share one row; each holds
 // threads_per_row * chunks_per_thread chunks of it in registers and the row
 // sums meet in distributed shared memory (1: no cluster).
-// Generic plans hold no chunks (they use a 256-thread CTA per row).
+// Generic plans are chosen by the row layout, not by C: PATH_GENERIC uses
+// a 256-thread CTA per row; a PATH_STREAM plan (backward) persistent CTAs
+// that each stream `depth` rows ahead, for rows of cmin .. cmax elements
+// (there chunks_per_thread counts the elements a thread owns, and
+// threads_per_row * chunks_per_thread >= cmax); past the last PATH_STREAM
+// range, PATH_GENERIC.
 #define RMSNORM_PLAN_TABLE(X) \
     /* forward, row in registers */ \
     X( 0, OP_FWD, PATH_VECTOR ,    8, 1, 32, 0, 1, DT_ANY,     1,     8) \
@@ -141,6 +150,13 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(131, OP_BWD, PATH_RESTAGED, 512, 4, 1, 3, 2, DT_ANY,     0,     0) \
     /* backward main kernel, any N and alignment */ \
     X(36, OP_BWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0) \
+    /* ... streamed (rows in [cmin, cmax] elements; the smaller CTAs of \
+       shorter rows keep more rows in flight an SM) */ \
+    X(58, OP_BWD, PATH_STREAM ,   64,  4, 1, 6, 1, DT_ANY,     1,   256) \
+    X(57, OP_BWD, PATH_STREAM ,   64, 16, 1, 4, 1, DT_ANY,   257,  1024) \
+    X(56, OP_BWD, PATH_STREAM ,  128, 16, 1, 4, 1, DT_ANY,  1025,  2048) \
+    X(43, OP_BWD, PATH_STREAM ,  256, 16, 1, 3, 1, DT_ANY,  2049,  4096) \
+    X(37, OP_BWD, PATH_STREAM ,  512, 16, 1, 8, 1, DT_ANY,  4097,  8192) \
     /* LayerNorm backward main kernel, persistent, row in registers (two \
        chunks a thread where the row allows) or staged; from 1025 chunks of \
        a 2-byte type on the re-read schedule with gamma in shared memory */ \
@@ -253,6 +269,10 @@ struct BwdParams {
 // a slot of this many bytes, placed at x's address mod 16 so that the
 // row's 16-byte chunks stay aligned.
 constexpr int64_t generic_bwd_cache_slot(int64_t N, int es) { return (N * es + 31) / 16 * 16; }
+
+// The streamed generic backward's stage slot for one array's row: its
+// 16-byte cover at the worst offset (15 bytes past a boundary).
+constexpr int64_t stream_slot_bytes(int64_t N, int es) { return (N * es + 30) / 16 * 16; }
 
 // Codes written to the status word: a bounded wait (a cluster row's peer
 // partial, or a staged row's bulk copy) gave up.

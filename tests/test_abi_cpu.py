@@ -208,6 +208,31 @@ def test_misaligned_pointers_take_generic(rn):
     assert rn.plan_query(rn.OP_BWD, 4096, 2048, 0, aligned=False)["path_name"] == "generic"
 
 
+def test_generic_backward_plan_by_row_length(rn):
+    """Rows no vectorised kernel takes (odd N, or arrays at different
+    addresses mod 16) run the streamed generic backward whose range holds N,
+    with its stages (two slots a stage, each a 16-byte cover of a row at its
+    worst offset) in shared memory; longer rows the one-CTA-a-row kernel."""
+    expect = ((1, 58), (256, 58), (257, 57), (1024, 57), (1025, 56), (2048, 56), (2049, 43), (4096, 43),
+              (4097, 37), (7169, 37), (8192, 37), (8193, 36), (65536, 36))
+    for N, pid in expect:
+        for dt, es in ((1, 2), (0, 4)):
+            p = rn.plan_query(rn.OP_BWD, 4096, N, dt, aligned=False, num_sms=152)
+            assert p["plan_id"] == pid and p["path_name"] == "generic", (N, dt, p)
+            if pid != 36:
+                slot = (N * es + 30) // 16 * 16
+                assert p["smem_bytes"] % (2 * slot) == 0 and 2 <= p["smem_bytes"] // (2 * slot) <= 8, (N, dt, p)
+                assert p["smem_bytes"] <= 226 * 1024 and p["chunks_per_thread"] == 0
+    # one CTA an SM for the widest rows: one partial row an SM
+    p = rn.plan_query(rn.OP_BWD, 4096, 7169, 1, aligned=False, num_sms=152)
+    assert p["ctas"] == 152 and p["ws_rows"] == 152 and p["workspace_bytes"] == (152 * 7169 * 4 + 255) // 256 * 256
+    # aligned rows keep the vectorised plans; the streamed plan may be forced on any layout
+    assert rn.plan_query(rn.OP_BWD, 4096, 7168, 1)["path_name"] in ("vector", "staged")
+    assert rn.plan_query(rn.OP_BWD, 4096, 7168, 1, force_plan=37)["plan_id"] == 37
+    with pytest.raises(rn.RMSNormError):  # a row longer than the plan holds
+        rn.plan_query(rn.OP_BWD, 4096, 8193, 1, aligned=False, force_plan=37)
+
+
 def test_plan_independent_of_m(rn):
     for N in (128, 2048, 8192):
         ids = {rn.plan_query(op, M, N, 1)["plan_id"] for op in (0,) for M in (1, 7, 4096, 524288)}

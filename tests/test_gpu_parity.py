@@ -28,6 +28,12 @@ def rn():
 
 
 GENERIC_FWD, GENERIC_BWD = 16, 36   # plan ids of the generic kernels
+# the streamed generic backward by row length: (plan id, longest row)
+STREAM_PLANS = ((58, 256), (57, 1024), (56, 2048), (43, 4096), (37, 8192))
+
+
+def stream_plan_for(N):
+    return next((pid for pid, nmax in STREAM_PLANS if N <= nmax), None)
 
 
 def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_path=None, wdt=None,
@@ -220,6 +226,84 @@ def test_generic_peeled_and_scalar_rows(rn, dt, M, N, offs, fused):
     _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, fused=fused, offset_elems=offs, expect_path="generic", force_generic=True)
 
 
+# Rows no vectorised kernel takes (odd N, or arrays at different addresses
+# mod 16): the streamed generic backward, which copies each row's 16-byte
+# covers into shared memory at any offset. (dt, weight type, M, N, offsets)
+STREAM_CASES = [
+    ("bf16", None, 1000, 7169, {"x": 1, "dy": 2, "dx": 3, "h": 1, "dres": 5}),
+    ("bf16", None, 700, 1500, {"x": 3, "dy": 2, "dx": 1, "h": 3, "dres": 7}),
+    ("f16", "f32", 300, 3001, {"x": 1, "dy": 4, "dx": 5, "h": 1, "dres": 2}),
+    ("f32", None, 2000, 250, {"x": 1, "dy": 2, "dx": 3, "h": 1, "dres": 1}),
+    ("bf16", None, 3000, 257, {"x": 5, "dy": 2, "h": 5, "dres": 3}),
+    ("bf16", None, 300, 7168, {"x": 1, "dy": 2, "dx": 0, "h": 1, "dres": 0}),
+    ("f32", None, 300, 8191, {"x": 1, "dy": 3, "dx": 2, "h": 1, "dres": 1}),
+    ("f32", None, 153, 8192, {"x": 1, "dy": 2, "h": 1, "dres": 3}),
+    ("f16", None, 257, 1000, {"x": 3, "dy": 1, "h": 3, "dres": 6}),
+    ("bf16", "f32", 513, 4100, {"x": 1, "dy": 5, "h": 1, "dres": 2}),
+    ("f16", "f32", 129, 8192, {"x": 2, "dy": 1, "dx": 7, "h": 2, "dres": 4}),
+    ("bf16", None, 64, 5, {"x": 3, "dy": 1, "h": 3, "dres": 1}),
+    ("bf16", None, 2000, 1, {"x": 1, "h": 1}),
+    ("bf16", None, 1, 8191, {"x": 1, "dy": 6, "h": 1, "dres": 7}),
+]
+
+
+@pytest.mark.parametrize("dt,wdt,M,N,offs", STREAM_CASES)
+@pytest.mark.parametrize("fused", [False, True])
+def test_streamed_generic_backward(rn, dt, wdt, M, N, offs, fused):
+    """Element-wise against the oracle, on ragged M (fewer rows than SMs,
+    one row, several rows a CTA), odd N down to 1, and every array at its own
+    offset."""
+    d = inputs.make_inputs(M, N, dt, 390 + N % 13, residual=fused, dres=fused, wdtype=wdt or dt)
+    if fused:
+        offs = dict(offs, residual=offs.get("x", 0), residual_out=offs.get("x", 0))
+    _, bp = _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, fused=fused, offset_elems=offs, expect_path="generic", wdt=wdt)
+    assert bp["plan_id"] == stream_plan_for(N), bp
+    assert bp["ws_rows"] <= M and bp["ctas"] == bp["ws_rows"], bp
+    if bp["plan_id"] == 37:  # one CTA an SM
+        assert bp["ws_rows"] == min(M, torch.cuda.get_device_properties(0).multi_processor_count), bp
+
+
+@pytest.mark.parametrize("dt,N,offs", [("bf16", 7169, (1, 2)), ("f32", 6000, (1, 3)), ("bf16", 4096, (3, 0)),
+                                       ("bf16", 1999, (0, 0)), ("f16", 777, (2, 1)), ("f32", 100, (1, 0))])
+def test_streamed_dw_equals_generic_at_same_ctas(rn, dt, N, offs):
+    """The streamed kernel and the one-CTA-a-row kernel forced to the same
+    CTA count: each CTA adds the same rows in the same order (one fp32
+    fused multiply-add of dy xhat a row) into its partial row, and the same
+    finalizer sums those in a fixed order, so dW agrees bit for bit."""
+    M = 1000
+    d = inputs.make_inputs(M, N, dt, 395)
+    x = to_dev(d["x"], dt, offset=offs[0])
+    dy = to_dev(d["dy"], dt, offset=offs[1])
+    w = to_dev(d["w"], dt)
+    _, rstd = rn.rmsnorm_fwd(x, w)
+    _, dw_a, pa = rn.rmsnorm_bwd_ex(dy, x, w, rstd)
+    _, dw_b, pb = rn.rmsnorm_bwd_ex(dy, x, w, rstd, force_plan=GENERIC_BWD, force_ctas=pa["ctas"])
+    torch.cuda.synchronize()
+    assert pa["plan_id"] == stream_plan_for(N) and pb["plan_id"] == GENERIC_BWD and pb["ctas"] == pa["ctas"]
+    assert cuda_bits_equal(dw_a, dw_b)
+    assert rn.lib().rmsnorm_device_status(1) == 0
+
+
+def test_streamed_backward_full_size_odd_row(rn):
+    """bf16 4096 x 7169 with x and dy at different offsets (the odd-N point
+    of the sweep): sampled rows of dx against the oracle, dW over every row."""
+    M, N, dt = 4096, 7169, "bf16"
+    d = inputs.make_inputs(M, N, dt, inputs.SWEEP_SEED)
+    x, dy = to_dev(d["x"], dt, offset=1), to_dev(d["dy"], dt, offset=2)
+    w = to_dev(d["w"], dt)
+    r32 = _rstd32_all_rows(d["x"], d["w"], dt, 1e-6)
+    dx, dw, p = rn.rmsnorm_bwd_ex(dy, x, w, torch.from_numpy(r32).cuda(), eps=1e-6)
+    torch.cuda.synchronize()
+    assert p["plan_id"] == stream_plan_for(N)
+    assert rn.lib().rmsnorm_device_status(1) == 0
+    rows = sampled_rows(M, seed=7)
+    rows_t = torch.from_numpy(rows).cuda()
+    b = oracle.bwd(d["dy"][rows], d["x"][rows], d["w"], dtype=dt, eps=1e-6, offset=0.0, rstd=r32[rows])
+    check_dx(to_host(dx[rows_t], dt), b, dt)
+    full = oracle.bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0, rstd=r32, want_dx=False, nthreads=8)
+    check_dw(to_host(dw, dt), full, dt)
+
+
 def test_generic_fused_residual_alone_misaligned(rn):
     """A residual at another address mod 16 than x turns the forward's peel
     off (element accesses); the result is the same arithmetic."""
@@ -234,12 +318,20 @@ def test_generic_fused_residual_alone_misaligned(rn):
 @pytest.mark.parametrize("fused", [False, True])
 def test_generic_backward_rows_around_40kb(rn, dt, M, N, fused):
     """Rows whose x and dy together come just under and just over 40 KB
-    (where the LayerNorm generic backward stops caching them): the RMSNorm
-    generic backward re-reads global memory at every length, takes no
-    dynamic shared memory, and gives the oracle's result."""
+    (where the LayerNorm generic backward stops caching them), on the
+    generic backward the call selects (the streamed kernel up to 8192
+    elements, with its stages in shared memory) and on the one-CTA-a-row
+    kernel, which re-reads global memory at every length and takes no
+    dynamic shared memory."""
     d = inputs.make_inputs(M, N, dt, 330 + N % 7, residual=fused, dres=fused)
     _, bplan = _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, fused=fused, offset_elems=1, expect_path="generic")
-    assert bplan["smem_bytes"] == 0, (N, bplan)
+    if N <= 8192:
+        assert bplan["plan_id"] == stream_plan_for(N) and bplan["smem_bytes"] > 0, (N, bplan)
+    else:
+        assert bplan["plan_id"] == GENERIC_BWD and bplan["smem_bytes"] == 0, (N, bplan)
+    _, bplan = _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, fused=fused, offset_elems=1, expect_path="generic",
+                              force_generic=True)
+    assert bplan["plan_id"] == GENERIC_BWD and bplan["smem_bytes"] == 0, (N, bplan)
 
 
 @pytest.mark.parametrize("eps", [0.0, 1e-2, 10.0])

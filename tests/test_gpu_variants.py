@@ -260,7 +260,7 @@ def test_forced_forward_plans_match_oracle(rn, plan):
     check_rstd(r.cpu().numpy(), f["rstd64"])
 
 
-@pytest.mark.parametrize("plan", [27, 34, 35, 36, 44, 45, 48, 49, 88, 89, 90, 96, 97, 98, 118, 119, 121, 123, 124, 127, 128, 131])
+@pytest.mark.parametrize("plan", [27, 34, 35, 36, 37, 44, 45, 48, 49, 88, 89, 90, 96, 97, 98, 118, 119, 121, 123, 124, 127, 128, 131])
 def test_forced_backward_plans_match_oracle(rn, plan):
     M, N, dt = 777, 8192, "bf16"
     d, t = dev_inputs(M, N, dt, 102)
