@@ -43,9 +43,13 @@
  *     are read as whole aligned blocks (never past the 16 bytes that hold
  *     one of the row's elements), joined into one chunk, and written back
  *     element by element; no element outside the arrays is ever written.
- *     Anything else takes the generic kernels. With an fp32 weight only the default plans are compiled
- *     (forcing an alternative plan id returns UNSUPPORTED) and only aligned
- *     rows are vectorised.
+ *     Anything else takes the generic kernels. The generic backward for
+ *     rows of up to 8192 elements likewise reads each row of x, dy (and
+ *     dresidual_out) as the whole 16-byte blocks that hold its elements,
+ *     wherever each array starts, and writes dx element by element. With
+ *     an fp32 weight only the default plans are compiled (forcing an
+ *     alternative plan id returns UNSUPPORTED) and only aligned rows are
+ *     vectorised.
  *   - Every call is asynchronous on `stream` (NULL = legacy default
  *     stream). The library never synchronises and never copies between
  *     host and device.
@@ -181,8 +185,9 @@ typedef enum {
  *     when M == 0).
  * residual / residual_out: both NULL (plain) or both set (fused add, as in
  * rmsnorm_add_fwd). w may be NULL (non-affine). dt is fp32, bf16 or fp16
- * with the weight in the same type (RMSNORM_WEIGHT_F32 is UNSUPPORTED
- * here). y needs no alignment beyond 1 byte; 16-byte alignment of x, w, y
+ * with the weight in the same type, or RMSNORM_BF16_W32 / RMSNORM_F16_W32
+ * (an fp32 weight beside 16-bit activations: the key's wtype apart from its
+ * itype). y needs no alignment beyond 1 byte; 16-byte alignment of x, w, y
  * (and the residual buffers) with N * sizeof(elem) % 16 == 0 selects the
  * vectorised kernels. With M == 0 nothing but amax is written. All
  * pointers are device pointers; argument errors as for rmsnorm_fwd.
@@ -309,14 +314,17 @@ typedef enum {
     RMSNORM_PATH_STAGED = 1,   /* row staged in shared memory by bulk copies */
                                /* (held in registers or re-read, by plan)    */
     RMSNORM_PATH_GENERIC = 2   /* any N and alignment: element head and tail */
-                               /* around 16-byte chunks                      */
+                               /* around 16-byte chunks, or (backward, rows  */
+                               /* up to 8192 elements) rows streamed into    */
+                               /* shared memory as whole 16-byte blocks      */
 } rmsnorm_path_t;
 
 typedef struct {
     int32_t path;               /* rmsnorm_path_t                               */
     int32_t plan_id;            /* index into the library's plan table          */
     int32_t threads_per_row;
-    int32_t chunks_per_thread;  /* 16-byte chunks a thread holds per row        */
+    int32_t chunks_per_thread;  /* 16-byte chunks a thread holds per row (0:
+                                   the generic kernels)                         */
     int32_t rows_per_cta;       /* rows a CTA works on concurrently             */
     int32_t cta_threads;
     int32_t packed;             /* 1: packed f32x2 arithmetic                   */

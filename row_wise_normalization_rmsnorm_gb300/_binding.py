@@ -238,8 +238,6 @@ def rmsnorm_fwd_fp8(x, w, *, scaling="row", scale=None, residual=None, eps: floa
     _check(x, "x")
     if w is not None:
         _check_w(w, "w", x, N)
-        if w.dtype != x.dtype:
-            raise ValueError("the E4M3 forward takes the weight in the activations' type")
     mode = FP8_SCALING[scaling]
     if mode == 0:
         if scale is None:
@@ -268,7 +266,7 @@ def rmsnorm_fwd_fp8(x, w, *, scaling="row", scale=None, residual=None, eps: floa
     p = Plan()
     st = lib().rmsnorm_fwd_fp8_ex(x.data_ptr(), _ptr(residual), _ptr(w), y.data_ptr(), _ptr(residual_out),
                                   rstd.data_ptr(), mode, _ptr(scale), scale_inv.data_ptr(), _ptr(amax_t), M, N,
-                                  _dtype_code(x), eps, offset, _stream_handle(stream, x.device), force_plan,
+                                  _dtype_code_w(x, w), eps, offset, _stream_handle(stream, x.device), force_plan,
                                   ctypes.byref(p))
     _raise(st, "rmsnorm_fwd_fp8")
     return {"y": y, "residual_out": residual_out, "rstd": rstd, "scale_inv": scale_inv, "amax": amax_t,

@@ -86,10 +86,15 @@ static const PlanDesc *generic_plan(int op) {
     return nullptr;
 }
 
-// The streamed generic backward's shared memory: `depth` stages of the x
-// and dy (and dres) row covers.
-static int64_t stream_smem_at(int64_t N, int es, bool fused, int depth) {
-    return (int64_t)depth * (fused ? 3 : 2) * stream_slot_bytes(N, es);
+// Rows a streamed kernel's stage holds: x and dy (and dres) for the
+// backward, x (and residual) for the forward.
+static int stream_arrays(const PlanDesc &d, bool fused) {
+    return d.op == OP_BWD ? (fused ? 3 : 2) : (fused ? 2 : 1);
+}
+
+// A streamed generic kernel's shared memory: `depth` stages of row covers.
+static int64_t stream_smem_at(const PlanDesc &d, int64_t N, int es, bool fused, int depth) {
+    return (int64_t)depth * stream_arrays(d, fused) * stream_slot_bytes(N, es);
 }
 
 static int cta_threads(const PlanDesc &d) { return d.path == PATH_GENERIC ? 256 : d.tpr * d.teams; }
@@ -98,27 +103,29 @@ static int cta_threads(const PlanDesc &d) { return d.path == PATH_GENERIC ? 256 
 // opt into on sm_103a, less room for the kernels' static arrays.
 constexpr int kMaxDynamicSmem = 226 * 1024;
 
-// Stages a streamed generic backward takes: the plan's depth, or fewer
-// (at least two) where the covers would not fit; 0: none fits.
+// Stages a streamed generic kernel takes: the plan's depth, or fewer (at
+// least two) where the covers would not fit; 0: none fits.
 static int stream_depth(const PlanDesc &d, int64_t N, int es, bool fused) {
     for (int k = d.depth; k >= 2; --k)
-        if (stream_smem_at(N, es, fused, k) <= kMaxDynamicSmem) return k;
+        if (stream_smem_at(d, N, es, fused, k) <= kMaxDynamicSmem) return k;
     return 0;
 }
 
-// Whether the streamed generic backward takes rows of N elements.
+// Whether a streamed generic plan takes rows of N elements.
 static bool stream_fits(const PlanDesc &d, int64_t N, int es) {
     return N <= (int64_t)d.tpr * d.v && stream_depth(d, N, es, true) >= 2;
 }
 
-// The plan for rows no vectorised plan takes: for the backward, the
-// streamed plan whose range holds N (where its stages fit), else the
-// one-CTA-a-row kernel.
-static const PlanDesc *fallback_plan(int op, int64_t N, int es) {
-    if (op == OP_BWD) {
+// The plan for rows no vectorised plan takes: the streamed plan whose
+// range holds N (where its stages fit; for the forward only where the
+// caller takes it: the RMSNorm forward with output in the activations'
+// type), else the one-CTA-a-row kernel.
+static const PlanDesc *fallback_plan(int op, int64_t N, int es, bool stream_ok) {
+    const int sop = op == RMSNORM_OP_FWD ? OP_FWD_STAGED : op;
+    if (stream_ok && (op == RMSNORM_OP_BWD || op == RMSNORM_OP_FWD)) {
         for (int i = 0; i < kNumPlans; ++i) {
             const PlanDesc &d = kPlans[i];
-            if (d.op == op && d.path == PATH_STREAM && d.cmin > 0 && N >= d.cmin && N <= d.cmax &&
+            if (d.op == sop && d.path == PATH_STREAM && d.cmin > 0 && N >= d.cmin && N <= d.cmax &&
                 stream_fits(d, N, es))
                 return &d;
         }
@@ -204,7 +211,8 @@ static int64_t plan_capacity(const PlanDesc &d) { return (int64_t)d.tpr * d.v * 
 // resident CTAs (or, for cluster plans, resident clusters) on the device;
 // ctas_per_sm is reported only.
 static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, int peel, int64_t max_parts,
-                                    int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out) {
+                                    int ctas_per_sm, int force_plan, int force_ctas, rmsnorm_plan_t *out,
+                                    bool stream_ok = true) {
     if (!out) return RMSNORM_ERR_INVALID_ARG;
     if (op != RMSNORM_OP_FWD && op != RMSNORM_OP_BWD && op != RMSNORM_OP_LN_BWD) return RMSNORM_ERR_INVALID_ARG;
     if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
@@ -223,8 +231,9 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, int pe
         if (d->path == PATH_VECTOR && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
         // staged plans: aligned rows that fit
         if (staged_path(d->path) && (!vec_ok || C > plan_capacity(*d))) return RMSNORM_ERR_UNSUPPORTED;
-        // the streamed generic kernel: rows of any layout that it holds
-        if (d->path == PATH_STREAM && !stream_fits(*d, N, s)) return RMSNORM_ERR_UNSUPPORTED;
+        // a streamed generic kernel: rows of any layout that it holds, for a
+        // caller that takes it
+        if (d->path == PATH_STREAM && (!stream_ok || !stream_fits(*d, N, s))) return RMSNORM_ERR_UNSUPPORTED;
         // with an fp32 weight only the default plans (and the generic one) are compiled
         if (mixed_kind(kind_of(dt)) && row_path(d->path) && d->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
     } else {
@@ -234,7 +243,7 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, int pe
             const PlanDesc *sd = default_vector_plan(OP_FWD_STAGED, dt, C);
             if (sd) d = sd;
         }
-        if (!d) d = fallback_plan(op, N, s);
+        if (!d) d = fallback_plan(op, N, s, stream_ok);
     }
     if (!d) return RMSNORM_ERR_UNSUPPORTED;
 
@@ -270,8 +279,8 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, int pe
         if (sm > kMaxDynamicSmem) return RMSNORM_ERR_UNSUPPORTED;
         out->smem_bytes = (int32_t)sm;
     }
-    if (d->path == PATH_STREAM)  // the plain variant's stages; the fused one is set by the backward
-        out->smem_bytes = (int32_t)stream_smem_at(N, s, false, stream_depth(*d, N, s, false));
+    if (d->path == PATH_STREAM)  // the plain variant's stages; the fused one is set by the call
+        out->smem_bytes = (int32_t)stream_smem_at(*d, N, s, false, stream_depth(*d, N, s, false));
     else if (!staged_path(d->path) && out->smem_bytes > 44 * 1024)
         return RMSNORM_ERR_UNSUPPORTED;
     const int64_t bytes = staged_fwd ? 0 : P * partial_rows(op) * N * 4;  // the forward has no partial rows
@@ -399,10 +408,29 @@ static const void *fwd_staged_kernel(int plan_id, int dt, bool fused, bool ln) {
 }
 
 static const void *fwd8_staged_kernel(int plan_id, int dt, bool fused, int mode) {
-    switch (base_dtype(dt)) {
-    case RMSNORM_BF16: return fwd8_staged_kernel_ptr_bf16(plan_id, fused, mode);
-    case RMSNORM_F16: return fwd8_staged_kernel_ptr_f16(plan_id, fused, mode);
+    switch (kind_of(dt)) {
+    case 1: return fwd8_staged_kernel_ptr_bf16(plan_id, fused, mode);
+    case 2: return fwd8_staged_kernel_ptr_f16(plan_id, fused, mode);
+    case 3: return fwd8_staged_kernel_ptr_bf16w32(plan_id, fused, mode);
+    case 4: return fwd8_staged_kernel_ptr_f16w32(plan_id, fused, mode);
     default: return fwd8_staged_kernel_ptr_f32(plan_id, fused, mode);
+    }
+}
+
+// The E4M3 forward of the call's type pair (stages > 0: a staged plan).
+static int launch_fwd8_dt(int dt, int plan_id, bool fused, int mode, const FwdParams &p, int grid, int stages,
+                          int smem, void *stream) {
+    switch (kind_of(dt)) {
+    case 1: return stages > 0 ? launch_fwd8_staged_bf16(plan_id, fused, mode, p, grid, smem, stream)
+                              : launch_fwd8_bf16(plan_id, fused, mode, p, grid, stream);
+    case 2: return stages > 0 ? launch_fwd8_staged_f16(plan_id, fused, mode, p, grid, smem, stream)
+                              : launch_fwd8_f16(plan_id, fused, mode, p, grid, stream);
+    case 3: return stages > 0 ? launch_fwd8_staged_bf16w32(plan_id, fused, mode, p, grid, smem, stream)
+                              : launch_fwd8_bf16w32(plan_id, fused, mode, p, grid, stream);
+    case 4: return stages > 0 ? launch_fwd8_staged_f16w32(plan_id, fused, mode, p, grid, smem, stream)
+                              : launch_fwd8_f16w32(plan_id, fused, mode, p, grid, stream);
+    default: return stages > 0 ? launch_fwd8_staged_f32(plan_id, fused, mode, p, grid, smem, stream)
+                               : launch_fwd8_f32(plan_id, fused, mode, p, grid, stream);
     }
 }
 
@@ -488,7 +516,7 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
     const int smem = staged_path(d.path)
                          ? (int)std::min<int64_t>(staged_smem_bytes(d, plan_capacity(d), 1, fused), kMaxDynamicSmem)
                      : d.path == PATH_STREAM
-                         ? (int)std::min<int64_t>(stream_smem_at((int64_t)d.tpr * d.v, elem_size(dt), fused, d.depth),
+                         ? (int)std::min<int64_t>(stream_smem_at(d, (int64_t)d.tpr * d.v, elem_size(dt), fused, d.depth),
                                                   kMaxDynamicSmem)
                          : bwd_smem_bytes(d, nmax);
     int best = 1 << 30;
@@ -594,7 +622,9 @@ static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d,
     if (!k) return cudaErrorInvalidDeviceFunction;
     cudaError_t e = (cudaError_t)allow_staged_smem(k);
     if (e != cudaSuccess) return e;
-    const int smem = (int)std::min<int64_t>(staged_smem_bytes(d, plan_capacity(d), 1, fused), kMaxDynamicSmem);
+    const int64_t sm = d.path == PATH_STREAM ? stream_smem_at(d, (int64_t)d.tpr * d.v, elem_size(dt), fused, d.depth)
+                                             : staged_smem_bytes(d, plan_capacity(d), 1, fused);
+    const int smem = (int)std::min<int64_t>(sm, kMaxDynamicSmem);
     int n = 0;
     if (d.cs > 1) {
         cudaLaunchConfig_t cfg = {};
@@ -631,9 +661,13 @@ static rmsnorm_status_t prepare_staged_fwd(int64_t M, int64_t N, int dt, int pee
     *status = nullptr;
     const PlanDesc *d = find_plan(plan->plan_id);
     if (!d || d->op != OP_FWD_STAGED) return RMSNORM_SUCCESS;
-    const int64_t C = N * elem_size(dt) / 16;
+    const bool stream = d->path == PATH_STREAM;
+    // the streamed generic forward serves the RMSNorm forward in the activations' type
+    if (stream && (ln || qmode != QOUT_NONE)) return RMSNORM_ERR_UNSUPPORTED;
+    const int es = elem_size(dt);
+    const int64_t C = N * es / 16;
     const int pk = peel > 0 ? peel : 0;
-    const int depth = staged_depth(*d, C, pk, fused);
+    const int depth = stream ? stream_depth(*d, N, es, fused) : staged_depth(*d, C, pk, fused);
     if (depth == 0) return RMSNORM_ERR_UNSUPPORTED;
     int dev = 0, sms = 0;
     cudaError_t e = device_sms(&dev, &sms);
@@ -641,9 +675,9 @@ static rmsnorm_status_t prepare_staged_fwd(int64_t M, int64_t N, int dt, int pee
     int parts = 1;
     e = staged_fwd_parts(dev, sms, dt, *d, fused, ln, qmode, &parts);
     if (e != cudaSuccess) return cuda_fail(e);
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, parts, 0, force_plan, 0, plan);
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, parts, 0, force_plan, 0, plan, stream);
     if (st != RMSNORM_SUCCESS) return st;
-    plan->smem_bytes = (int32_t)staged_smem_bytes(*d, C, pk, fused);
+    plan->smem_bytes = (int32_t)(stream ? stream_smem_at(*d, N, es, fused, depth) : staged_smem_bytes(*d, C, pk, fused));
     e = status_word(dev, status);
     if (e != cudaSuccess) return cuda_fail(e);
     *stages = depth;
@@ -671,12 +705,12 @@ int self_check_impl() {
         }
         if (!generic_plan(op)) ++bad;
     }
-    // streamed backward defaults: ranges of N tiling [1, max] in table order
-    {
+    // streamed defaults, backward and forward: ranges of N tiling [1, max] in table order
+    for (int op : {(int)OP_BWD, (int)OP_FWD_STAGED}) {
         int64_t expect = 1;
         for (int i = 0; i < kNumPlans; ++i) {
             const PlanDesc &d = kPlans[i];
-            if (d.path != PATH_STREAM || d.cmin == 0) continue;
+            if (d.op != op || d.path != PATH_STREAM || d.cmin == 0) continue;
             if (d.cmin != expect || d.cmax < d.cmin) ++bad;
             expect = d.cmax + 1;
         }
@@ -687,7 +721,7 @@ int self_check_impl() {
         int64_t expect = -1;
         for (int i = 0; i < kNumPlans; ++i) {
             const PlanDesc &d = kPlans[i];
-            if (d.op != OP_FWD_STAGED || d.cmin == 0 || !(d.dtm & dtype_bit(dt))) continue;
+            if (d.op != OP_FWD_STAGED || d.path == PATH_STREAM || d.cmin == 0 || !(d.dtm & dtype_bit(dt))) continue;
             if ((expect >= 0 && d.cmin != expect) || d.cmax < d.cmin || plan_capacity(d) < d.cmax) ++bad;
             expect = d.cmax + 1;
             if (default_vector_plan(OP_FWD_STAGED, dt, d.cmin) != &d ||
@@ -698,7 +732,7 @@ int self_check_impl() {
     for (int i = 0; i < kNumPlans; ++i) {
         const PlanDesc &d = kPlans[i];
         if (find_plan(d.id) != &d) ++bad;  // ids unique
-        if (d.op == OP_FWD_STAGED && d.path != PATH_RESTAGED) ++bad;
+        if (d.op == OP_FWD_STAGED && d.path != PATH_RESTAGED && d.path != PATH_STREAM) ++bad;
         if (d.path == PATH_VECTOR) {
             const bool pow2 = d.tpr > 0 && (d.tpr & (d.tpr - 1)) == 0;
             if (!pow2 || d.tpr * d.teams > kMaxCtaThreads || d.tpr * d.teams < 32 || d.v < 1) ++bad;
@@ -713,9 +747,9 @@ int self_check_impl() {
                 d.tpr > kMaxCtaThreads || d.v < 1)
                 ++bad;
         }
-        // the streamed generic kernel: a backward of whole warps with 2..8
-        // stages that holds the longest row of its range
-        if (d.path == PATH_STREAM && (d.op != OP_BWD || d.tpr % 32 != 0 || d.tpr < 64 || d.tpr > kMaxCtaThreads ||
+        // a streamed generic kernel: a backward or a forward of whole warps
+        // with 2..8 stages that holds the longest row of its range
+        if (d.path == PATH_STREAM && ((d.op != OP_BWD && d.op != OP_FWD_STAGED) || d.tpr % 32 != 0 || d.tpr < 64 || d.tpr > kMaxCtaThreads ||
                                       d.v < 1 || d.depth < 2 || d.depth > 8 || d.teams != 1 ||
                                       d.cs != 1 || (int64_t)d.tpr * d.v < d.cmax))
             ++bad;
@@ -798,8 +832,6 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
     const bool quant = q.qmode != QOUT_NONE;
     if (quant) {
-        // E4M3 output: the weight in the activations' type only
-        if (mixed_kind(kind_of(dt))) return RMSNORM_ERR_UNSUPPORTED;
         if (q.qmode == QOUT_FP8_TENSOR && (!q.scale || !aligned_to(q.scale, 4))) return RMSNORM_ERR_INVALID_ARG;
         if (q.qmode == QOUT_FP8_ROW && (q.scale || (M > 0 && !q.scale_inv))) return RMSNORM_ERR_INVALID_ARG;
         if ((q.scale_inv && !aligned_to(q.scale_inv, 4)) || (q.amax && !aligned_to(q.amax, 4)))
@@ -832,7 +864,7 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     }
 
     rmsnorm_plan_t plan;
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, 1, 0, force_plan, 0, &plan);
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, 1, 0, force_plan, 0, &plan, !quant);
     if (st != RMSNORM_SUCCESS) return st;
     // the E4M3 kernels are compiled for the default plans and the generic one
     if (quant && force_plan >= 0 && plan.path != PATH_GENERIC && find_plan(plan.plan_id)->cmin == 0)
@@ -870,21 +902,7 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (quant) {
         cudaError_t e = clear_amax();
         if (e != cudaSuccess) return cuda_fail(e);
-        const int sm = plan.smem_bytes;
-        switch (base_dtype(dt)) {
-        case RMSNORM_BF16:
-            le = stages > 0 ? launch_fwd8_staged_bf16(plan.plan_id, fused, q.qmode, p, plan.ctas, sm, stream)
-                            : launch_fwd8_bf16(plan.plan_id, fused, q.qmode, p, plan.ctas, stream);
-            break;
-        case RMSNORM_F16:
-            le = stages > 0 ? launch_fwd8_staged_f16(plan.plan_id, fused, q.qmode, p, plan.ctas, sm, stream)
-                            : launch_fwd8_f16(plan.plan_id, fused, q.qmode, p, plan.ctas, stream);
-            break;
-        default:
-            le = stages > 0 ? launch_fwd8_staged_f32(plan.plan_id, fused, q.qmode, p, plan.ctas, sm, stream)
-                            : launch_fwd8_f32(plan.plan_id, fused, q.qmode, p, plan.ctas, stream);
-            break;
-        }
+        le = launch_fwd8_dt(dt, plan.plan_id, fused, q.qmode, p, plan.ctas, stages, plan.smem_bytes, stream);
     } else if (stages > 0) {
         le = launch_fwd_staged_dt(dt, false, plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream);
     } else {
@@ -929,7 +947,7 @@ static rmsnorm_status_t plan_bwd_call(int op, const void *dy, const void *dres, 
     if (c->plan.path == PATH_STAGED) c->plan.smem_bytes = (int32_t)staged_smem_bytes(*c->d, C, c->plan.peel, fused);
     if (c->d->path == PATH_STREAM) {
         const int es = elem_size(dt);
-        c->plan.smem_bytes = (int32_t)stream_smem_at(N, es, fused, stream_depth(*c->d, N, es, fused));
+        c->plan.smem_bytes = (int32_t)stream_smem_at(*c->d, N, es, fused, stream_depth(*c->d, N, es, fused));
     }
     return RMSNORM_SUCCESS;
 }
@@ -1105,7 +1123,7 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
     if (peel >= 0 && beta && row_layout(dt, N, {x, beta}, nullptr) != peel) peel = -1;
 
     rmsnorm_plan_t plan;
-    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, 1, 0, force_plan, 0, &plan);
+    rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, 1, 0, force_plan, 0, &plan, false);
     if (st != RMSNORM_SUCCESS) return st;
     // the LayerNorm forward is compiled for the default plans and the generic one
     if (plan.path == PATH_VECTOR && find_plan(plan.plan_id)->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;

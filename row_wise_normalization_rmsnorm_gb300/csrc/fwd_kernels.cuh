@@ -881,6 +881,127 @@ __global__ void __launch_bounds__(TPR, 1) layernorm_fwd_staged(const FwdParams p
     staged_fwd_body<T, T, TPR, V, S, CS, FUSED, true>(p);
 }
 
+// Streamed generic forward: persistent CTAs, rows of any alignment and of
+// at most TPR * K elements, the forward counterpart of the streamed generic
+// backward. Row k of a CTA streams into stage k mod ns by bulk copies of
+// the 16-byte covers (cover16) of its x (and residual) rows, each at its
+// own offset within its first block. Thread t owns columns t + i TPR
+// (i < K) of every row, with (offset + w) for them held in registers; it
+// reads its elements of the stage before the row reduction's barrier, after
+// which thread 0 refills the stage with row k + ns. h = x (fused: the sum
+// x + residual rounded to the storage type, which is also stored),
+// rstd = 1 / sqrt(sum h^2 / N + eps), y = (h rstd) (offset + w), each
+// stored element by element (a row's edge blocks may hold a neighbouring
+// row, which another CTA writes). Every wait is bounded: one that gives up
+// records the status word, waits (again bounded) for the stages' last
+// copies and lets the kernel end.
+template <typename T, typename TW, int TPR, int K, int SMAX, bool FUSED>
+__global__ void __launch_bounds__(TPR, TPR >= 512 ? 1 : 512 / TPR) rmsnorm_fwd_stream(const FwdParams p) {
+    static_assert(TPR % 32 == 0 && TPR >= 64 && TPR <= 1024, "whole warps");
+    constexpr int W = TPR / 32;
+    constexpr int NB = FUSED ? 2 : 1;  // arrays a stage holds: x (, residual)
+    __shared__ float red[2][W];
+    __shared__ __align__(8) uint64_t full[SMAX];
+    extern __shared__ float4 sstage_smem[];  // ns * NB slots of stream_slot_bytes(N, sizeof(T))
+    pdl_wait();  // before any read of the rows (the bulk copies included)
+    const int N = p.N;
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int ns = p.stages;  // 2 .. SMAX, chosen by the host to fit
+    const int64_t G = gridDim.x;
+    const int64_t unit = blockIdx.x;
+    const int64_t iters = unit < p.M ? (p.M - unit + G - 1) / G : 0;
+    const uint32_t rb = (uint32_t)N * (uint32_t)sizeof(T);  // bytes of a row
+    const uint32_t slot = (uint32_t)stream_slot_bytes(N, (int)sizeof(T));
+    char *const stages = reinterpret_cast<char *>(sstage_smem);
+    const char *gx = static_cast<const char *>(p.x);
+    const char *gr = static_cast<const char *>(p.residual);
+    // thread 0: the covers of row k's arrays into stage s
+    auto issue = [&](int64_t k, int s) {
+        const int64_t off = (unit + k * G) * (int64_t)rb;
+        const Cover cx = cover16(gx + off, rb);
+        const Cover cr = FUSED ? cover16(gr + off, rb) : Cover{nullptr, 0u, 0u};
+        char *dst = stages + (size_t)s * NB * slot;
+        mbar_arrive_expect_tx(&full[s], cx.bytes + cr.bytes);
+        bulk_g2s(dst, cx.src, cx.bytes, &full[s]);
+        if constexpr (FUSED) bulk_g2s(dst + slot, cr.src, cr.bytes, &full[s]);
+    };
+    const TW *w = static_cast<const TW *>(p.w);
+    const bool has_w = w != nullptr;
+    float wf[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        const int j = t + i * TPR;
+        wf[i] = (has_w && j < N) ? __fadd_rn(p.offset, load_w(w, j)) : 1.f;
+    }
+    if (t == 0) {
+        for (int s = 0; s < ns; ++s) mbar_init(&full[s], 1);
+        mbar_init_fence();
+        for (int s = 0; s < ns && s < iters; ++s) issue(s, s);
+    }
+    __syncthreads();
+
+    bool failed = false;
+    int s = 0;        // stage of row k (k mod ns)
+    uint32_t ph = 0;  // parity of k / ns
+    for (int64_t k = 0; k < iters; ++k) {
+        const int64_t row = unit + k * G;
+        if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
+        const int64_t off = row * (int64_t)rb;
+        const char *sb = stages + (size_t)s * NB * slot;
+        const T *xs = reinterpret_cast<const T *>(sb + addr_mod16(gx + off));
+        const T *rs = reinterpret_cast<const T *>(sb + slot + (FUSED ? addr_mod16(gr + off) : 0u));
+        T *hout = static_cast<T *>(p.residual_out) + row * (int64_t)N;
+        float hv[K];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const int j = t + i * TPR;
+            hv[i] = 0.f;
+            if (j < N) {
+                hv[i] = load_elem(xs, j);
+                if constexpr (FUSED) {
+                    hv[i] = round_to(__fadd_rn(hv[i], load_elem(rs, j)), xs);
+                    store_elem(hout, j, hv[i]);
+                }
+            }
+            ss = __fmaf_rn(hv[i], hv[i], ss);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+        float *slots = red[k & 1];
+        if (lane == 0) slots[t >> 5] = ss;
+        __syncthreads();
+        // every thread has its elements of stage s: refill it with row k + ns
+        if (t == 0 && k + ns < iters) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(k + ns, s);
+        }
+        if (++s == ns) {
+            s = 0;
+            ph ^= 1u;
+        }
+        const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(sum_slots<W>(slots, lane), (float)N), p.eps));
+        if (t == 0) p.rstd[row] = rstd;
+        T *y = static_cast<T *>(p.y) + row * (int64_t)N;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const int j = t + i * TPR;
+            if (j < N) store_elem(y, j, __fmul_rn(__fmul_rn(hv[i], rstd), wf[i]));
+        }
+    }
+    if (failed) {
+        // the last copy into each stage has landed (or its wait gives up
+        // again) before the CTA ends
+        for (int s2 = 0; s2 < ns && s2 < iters; ++s2) {
+            const int64_t kl = s2 + (iters - 1 - s2) / ns * ns;
+            mbar_wait(&full[s2], (uint32_t)((kl / ns) & 1), kWaitLimit);
+        }
+        if (p.status) *p.status = kStatusWaitTimeout;
+    }
+    pdl_trigger();  // every row done: the next kernel may launch
+}
+
 // Launch of a staged forward kernel: a cluster of CS CTAs (of one where a
 // CTA holds the whole row; its bulk copies name a shared::cluster
 // destination) with the stages' dynamic shared memory.
@@ -983,8 +1104,16 @@ static const void *ptr_t(int plan_id, bool fused) {
 template <typename T, typename TW, bool LN, int Q, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS,
           int CMIN>
 static const void *staged_fwd_ptr_entry(bool fused) {
-    if constexpr (OP != OP_FWD_STAGED || PATH != PATH_RESTAGED || !staged_plan(PATH, TEAMS, CS) ||
-                  !instantiated<T, TW, PATH, CMIN, Q>() || (LN && Q != QOUT_NONE)) {
+    if constexpr (OP == OP_FWD_STAGED && PATH == PATH_STREAM) {
+        // the streamed generic forward: RMSNorm, output in the activations' type
+        if constexpr (LN || Q != QOUT_NONE) {
+            return nullptr;
+        } else {
+            return fused ? (const void *)rmsnorm_fwd_stream<T, TW, TPR, V, D, true>
+                         : (const void *)rmsnorm_fwd_stream<T, TW, TPR, V, D, false>;
+        }
+    } else if constexpr (OP != OP_FWD_STAGED || PATH != PATH_RESTAGED || !staged_plan(PATH, TEAMS, CS) ||
+                         !instantiated<T, TW, PATH, CMIN, Q>() || (LN && Q != QOUT_NONE)) {
         return nullptr;
     } else if constexpr (LN) {
         return fused ? (const void *)layernorm_fwd_staged<T, TPR, V, D, CS, true>
@@ -1029,25 +1158,26 @@ static int staged_fwd_launch_t(int plan_id, bool fused, const FwdParams &p, int 
     }
 }
 
-// E4M3 output of the staged forward: the mode picks the instantiation.
-template <typename T>
+// E4M3 output of the staged forward: the mode picks the instantiation
+// (TW: the weight's type, the activations' or fp32).
+template <typename T, typename TW = T>
 static int staged_launch_q(int plan_id, bool fused, int mode, const FwdParams &p, int grid, int smem, void *stream) {
-    if (mode == QOUT_FP8_TENSOR) return staged_fwd_launch_t<T, T, false, QOUT_FP8_TENSOR>(plan_id, fused, p, grid, smem, stream);
-    if (mode == QOUT_FP8_ROW) return staged_fwd_launch_t<T, T, false, QOUT_FP8_ROW>(plan_id, fused, p, grid, smem, stream);
+    if (mode == QOUT_FP8_TENSOR) return staged_fwd_launch_t<T, TW, false, QOUT_FP8_TENSOR>(plan_id, fused, p, grid, smem, stream);
+    if (mode == QOUT_FP8_ROW) return staged_fwd_launch_t<T, TW, false, QOUT_FP8_ROW>(plan_id, fused, p, grid, smem, stream);
     return (int)cudaErrorInvalidValue;
 }
-template <typename T>
+template <typename T, typename TW = T>
 static const void *staged_ptr_q(int plan_id, bool fused, int mode) {
-    if (mode == QOUT_FP8_TENSOR) return staged_fwd_ptr_t<T, T, false, QOUT_FP8_TENSOR>(plan_id, fused);
-    if (mode == QOUT_FP8_ROW) return staged_fwd_ptr_t<T, T, false, QOUT_FP8_ROW>(plan_id, fused);
+    if (mode == QOUT_FP8_TENSOR) return staged_fwd_ptr_t<T, TW, false, QOUT_FP8_TENSOR>(plan_id, fused);
+    if (mode == QOUT_FP8_ROW) return staged_fwd_ptr_t<T, TW, false, QOUT_FP8_ROW>(plan_id, fused);
     return nullptr;
 }
 
 // E4M3 output: the mode picks the instantiation.
-template <typename T>
+template <typename T, typename TW = T>
 static int launch_q(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream) {
-    if (mode == QOUT_FP8_TENSOR) return launch_t<T, T, QOUT_FP8_TENSOR>(plan_id, fused, p, grid, stream);
-    if (mode == QOUT_FP8_ROW) return launch_t<T, T, QOUT_FP8_ROW>(plan_id, fused, p, grid, stream);
+    if (mode == QOUT_FP8_TENSOR) return launch_t<T, TW, QOUT_FP8_TENSOR>(plan_id, fused, p, grid, stream);
+    if (mode == QOUT_FP8_ROW) return launch_t<T, TW, QOUT_FP8_ROW>(plan_id, fused, p, grid, stream);
     return (int)cudaErrorInvalidValue;
 }
 

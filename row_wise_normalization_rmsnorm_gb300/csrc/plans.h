@@ -94,6 +94,14 @@ enum PlanDtypes { DT_F32 = 1, DT_BF16 = 2, DT_F16 = 4, DT_16 = 6, DT_ANY = 7 };
     X(145, OP_FWD_STAGED, PATH_RESTAGED, 512, 3, 1, 2, 4, DT_ANY, 4097,  6144) \
     X(143, OP_FWD_STAGED, PATH_RESTAGED, 512, 4, 1, 2, 4, DT_ANY, 6145,  8192) \
     X(138, OP_FWD_STAGED, PATH_RESTAGED, 512, 4, 1, 4, 1, DT_ANY,    0,     0) \
+    /* forward rows no vectorised plan takes (any alignment): streamed \
+       generic plans, rows in [cmin, cmax] elements */ \
+    X(104, OP_FWD_STAGED, PATH_STREAM,   64,  4, 1, 6, 1, DT_ANY,     1,   256) \
+    X(105, OP_FWD_STAGED, PATH_STREAM,   64, 16, 1, 4, 1, DT_ANY,   257,  1024) \
+    X(106, OP_FWD_STAGED, PATH_STREAM,  128, 16, 1, 4, 1, DT_ANY,  1025,  2048) \
+    X(107, OP_FWD_STAGED, PATH_STREAM,  256, 16, 1, 4, 1, DT_ANY,  2049,  4096) \
+    X(108, OP_FWD_STAGED, PATH_STREAM,  512, 16, 1, 4, 1, DT_ANY,  4097,  8192) \
+    X(109, OP_FWD_STAGED, PATH_STREAM, 1024, 16, 1, 4, 1, DT_ANY,  8193, 16384) \
     /* forward, any N and alignment */ \
     X(16, OP_FWD, PATH_GENERIC,  256, 0,  1, 0, 1, DT_ANY,     0,     0) \
     /* backward main kernel, persistent: rows in registers (vector) or \
@@ -299,17 +307,21 @@ RMSN_DECLARE_LAUNCHERS(f16w32)
 #undef RMSN_DECLARE_LAUNCHERS
 
 // Forward with E4M3 output (mode QOUT_FP8_TENSOR or QOUT_FP8_ROW), for
-// fp32, bf16 and fp16 activations with the weight in the same type.
-int launch_fwd8_f32(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
-int launch_fwd8_bf16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
-int launch_fwd8_f16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream);
-// ... and on the staged forward plans (OP_FWD_STAGED defaults)
-int launch_fwd8_staged_f32(int plan_id, bool fused, int mode, const FwdParams &p, int grid, int smem, void *stream);
-int launch_fwd8_staged_bf16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, int smem, void *stream);
-int launch_fwd8_staged_f16(int plan_id, bool fused, int mode, const FwdParams &p, int grid, int smem, void *stream);
-const void *fwd8_staged_kernel_ptr_f32(int plan_id, bool fused, int mode);
-const void *fwd8_staged_kernel_ptr_bf16(int plan_id, bool fused, int mode);
-const void *fwd8_staged_kernel_ptr_f16(int plan_id, bool fused, int mode);
+// fp32, bf16 and fp16 activations with the weight in the same type, and
+// for bf16 and fp16 activations with an fp32 weight ("w32"); on the
+// register plans and the generic one, and on the staged forward plans
+// (OP_FWD_STAGED defaults).
+#define RMSN_DECLARE_FWD8(suf)                                                                            \
+    int launch_fwd8_##suf(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream); \
+    int launch_fwd8_staged_##suf(int plan_id, bool fused, int mode, const FwdParams &p, int grid, int smem, \
+                                 void *stream);                                                           \
+    const void *fwd8_staged_kernel_ptr_##suf(int plan_id, bool fused, int mode);
+RMSN_DECLARE_FWD8(f32)
+RMSN_DECLARE_FWD8(bf16)
+RMSN_DECLARE_FWD8(f16)
+RMSN_DECLARE_FWD8(bf16w32)
+RMSN_DECLARE_FWD8(f16w32)
+#undef RMSN_DECLARE_FWD8
 
 // Opt a staged kernel into its largest dynamic shared memory on the current
 // device (once per kernel and device); returns a cudaError_t.

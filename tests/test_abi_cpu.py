@@ -233,6 +233,27 @@ def test_generic_backward_plan_by_row_length(rn):
         rn.plan_query(rn.OP_BWD, 4096, 8193, 1, aligned=False, force_plan=37)
 
 
+def test_generic_forward_plan_by_row_length(rn):
+    """The forward's counterpart: streamed plans (one slot a stage, x's
+    cover) up to 16384 elements, the one-CTA-a-row kernel beyond and where
+    two stages of the fused variant (x and residual) would not fit: fp32
+    rows of 16384 elements."""
+    expect = ((1, 104), (256, 104), (257, 105), (1024, 105), (1025, 106), (2048, 106), (2049, 107),
+              (4096, 107), (4097, 108), (8192, 108), (8193, 109), (16384, 109), (16385, 16), (65536, 16))
+    for N, pid in expect:
+        for dt, es in ((1, 2), (0, 4)):
+            if es == 4 and N == 16384:
+                pid = 16
+            p = rn.plan_query(rn.OP_FWD, 4096, N, dt, aligned=False, num_sms=152)
+            assert p["plan_id"] == pid and p["path_name"] == "generic", (N, dt, p)
+            if pid != 16:
+                slot = (N * es + 30) // 16 * 16
+                assert p["smem_bytes"] % slot == 0 and 2 <= p["smem_bytes"] // slot <= 6, (N, dt, p)
+                assert p["workspace_bytes"] == 0 and p["ctas"] == p["ws_rows"], (N, dt, p)
+            else:
+                assert p["ctas"] == 4096
+
+
 def test_plan_independent_of_m(rn):
     for N in (128, 2048, 8192):
         ids = {rn.plan_query(op, M, N, 1)["plan_id"] for op in (0,) for M in (1, 7, 4096, 524288)}
@@ -287,14 +308,14 @@ def test_invalid_arguments_without_gpu(rn):
     assert L.rmsnorm_bwd(x, x, x, r, x, None, None, 0, 4, 8, 1, 1e-6, 0.0, None) == 1
     assert L.rmsnorm_bwd(x, x, x, r, x, x, ctypes.c_void_p(264), 1 << 20, 4, 8, 1, 1e-6, 0.0, None) == 3
     # E4M3 forward: unknown scaling, per-tensor without a scale, per-row
-    # with a given scale or without scale_inv, an fp32 weight (unsupported)
+    # with a given scale or without scale_inv, an fp32 weight not 4-byte aligned
     f8 = L.rmsnorm_fwd_fp8
     assert f8(x, None, x, x, None, r, 2, None, r, None, 4, 8, 1, 1e-6, 0.0, None) == 1
     assert f8(x, None, x, x, None, r, 0, None, r, None, 4, 8, 1, 1e-6, 0.0, None) == 1
     assert f8(x, None, x, x, None, r, 1, r, r, None, 4, 8, 1, 1e-6, 0.0, None) == 1
     assert f8(x, None, x, x, None, r, 1, None, None, None, 4, 8, 1, 1e-6, 0.0, None) == 1
     assert f8(x, None, x, x, None, r, 0, ctypes.c_void_p(514), None, None, 4, 8, 1, 1e-6, 0.0, None) == 1
-    assert f8(x, None, x, x, None, r, 1, None, r, None, 4, 8, 0x101, 1e-6, 0.0, None) == 2
+    assert f8(x, None, ctypes.c_void_p(258), x, None, r, 1, None, r, None, 4, 8, 0x101, 1e-6, 0.0, None) == 1
     assert f8(x, x, x, x, None, r, 1, None, r, None, 4, 8, 1, 1e-6, 0.0, None) == 1   # residual without out
     # M == 0 forward is a no-op that needs no device
     assert L.rmsnorm_fwd(x, x, x, r, 0, 8, 1, 1e-6, 0.0, None) == 0

@@ -28,10 +28,11 @@ def rn():
 
 
 def _run(rn, d, dt, scaling, scale=None, eps=1e-6, offset=0.0, fused=False, offset_elems=0, expect_path=None,
-         amax=True):
+         amax=True, wdt=None):
+    """wdt: the weight's storage type (default the activations')."""
     M, N = d["x"].shape
     x = to_dev(d["x"], dt, offset=offset_elems)
-    w = to_dev(d["w"], dt, offset=offset_elems) if d["w"] is not None else None
+    w = to_dev(d["w"], wdt or dt, offset=offset_elems) if d["w"] is not None else None
     res = to_dev(d["residual"], dt, offset=offset_elems) if fused else None
     sc = torch.tensor([scale], dtype=torch.float32, device="cuda") if scale is not None else None
     buf = torch.full((M * N + offset_elems + 16,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN codes
@@ -39,7 +40,7 @@ def _run(rn, d, dt, scaling, scale=None, eps=1e-6, offset=0.0, fused=False, offs
     out = rn.rmsnorm_fwd_fp8(x, w, scaling=scaling, scale=sc, residual=res, eps=eps, offset=offset, y=y,
                              amax=amax)
     f = oracle.fwd_fp8(d["x"], d["w"], dtype=dt, eps=eps, offset=offset, scaling=scaling, scale=scale,
-                       residual=d.get("residual") if fused else None)
+                       residual=d.get("residual") if fused else None, wdtype=wdt)
     torch.cuda.synchronize()
     assert torch.all(buf[offset_elems + M * N:] == 0xFF), "store past the end of y"
     ties = check_fp8(y.cpu().numpy(), f)
@@ -74,6 +75,20 @@ def test_fp8_shapes(rn, dt, M, N, scaling):
     es = 4 if dt == "f32" else 2
     path = "vector" if (N * es) % 16 == 0 else "generic"
     _run(rn, d, dt, scaling, scale=37.5 if scaling == "tensor" else None, expect_path=path)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N", [(333, 64), (257, 1024), (129, 8192), (65, 16384), (33, 32768), (40, 3),
+                                 (101, 8193)])
+@pytest.mark.parametrize("scaling", ["row", "tensor"])
+@pytest.mark.parametrize("fused", [False, True])
+def test_fp8_fp32_weight(rn, dt, M, N, scaling, fused):
+    """An fp32 weight beside 16-bit activations (the key's wtype apart from
+    its itype), on register, staged cluster and generic rows."""
+    d = inputs.make_inputs(M, N, dt, 170 + N % 13, outlier_frac=0.01, wdtype="f32", residual=fused)
+    path = "vector" if (N * 2) % 16 == 0 else "generic"
+    out, _ = _run(rn, d, dt, scaling, scale=21.0 if scaling == "tensor" else None, fused=fused, expect_path=path,
+                  wdt="f32")
 
 
 @pytest.mark.parametrize("dt,N", [("bf16", 32768), ("bf16", 65536), ("f32", 16384), ("f32", 32768)])

@@ -32,8 +32,11 @@ GENERIC_FWD, GENERIC_BWD = 16, 36   # plan ids of the generic kernels
 STREAM_PLANS = ((58, 256), (57, 1024), (56, 2048), (43, 4096), (37, 8192))
 
 
-def stream_plan_for(N):
-    return next((pid for pid, nmax in STREAM_PLANS if N <= nmax), None)
+STREAM_FWD_PLANS = ((104, 256), (105, 1024), (106, 2048), (107, 4096), (108, 8192), (109, 16384))
+
+
+def stream_plan_for(N, fwd=False):
+    return next((pid for pid, nmax in (STREAM_FWD_PLANS if fwd else STREAM_PLANS) if N <= nmax), None)
 
 
 def _fwd_bwd_check(rn, d, dt, eps, offset, fused=False, offset_elems=0, expect_path=None, wdt=None,
@@ -249,14 +252,15 @@ STREAM_CASES = [
 
 @pytest.mark.parametrize("dt,wdt,M,N,offs", STREAM_CASES)
 @pytest.mark.parametrize("fused", [False, True])
-def test_streamed_generic_backward(rn, dt, wdt, M, N, offs, fused):
-    """Element-wise against the oracle, on ragged M (fewer rows than SMs,
-    one row, several rows a CTA), odd N down to 1, and every array at its own
-    offset."""
+def test_streamed_generic_kernels(rn, dt, wdt, M, N, offs, fused):
+    """The streamed generic forward and backward, element-wise against the
+    oracle, on ragged M (fewer rows than SMs, one row, several rows a CTA),
+    odd N down to 1, and every array at its own offset."""
     d = inputs.make_inputs(M, N, dt, 390 + N % 13, residual=fused, dres=fused, wdtype=wdt or dt)
     if fused:
         offs = dict(offs, residual=offs.get("x", 0), residual_out=offs.get("x", 0))
-    _, bp = _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, fused=fused, offset_elems=offs, expect_path="generic", wdt=wdt)
+    fp, bp = _fwd_bwd_check(rn, d, dt, 1e-6, 0.0, fused=fused, offset_elems=offs, expect_path="generic", wdt=wdt)
+    assert fp["plan_id"] == stream_plan_for(N, fwd=True), fp
     assert bp["plan_id"] == stream_plan_for(N), bp
     assert bp["ws_rows"] <= M and bp["ctas"] == bp["ws_rows"], bp
     if bp["plan_id"] == 37:  # one CTA an SM
@@ -284,13 +288,17 @@ def test_streamed_dw_equals_generic_at_same_ctas(rn, dt, N, offs):
     assert rn.lib().rmsnorm_device_status(1) == 0
 
 
-def test_streamed_backward_full_size_odd_row(rn):
+def test_streamed_kernels_full_size_odd_row(rn):
     """bf16 4096 x 7169 with x and dy at different offsets (the odd-N point
-    of the sweep): sampled rows of dx against the oracle, dW over every row."""
+    of the sweep): sampled rows of y, rstd and dx against the oracle, dW over
+    every row."""
     M, N, dt = 4096, 7169, "bf16"
     d = inputs.make_inputs(M, N, dt, inputs.SWEEP_SEED)
     x, dy = to_dev(d["x"], dt, offset=1), to_dev(d["dy"], dt, offset=2)
     w = to_dev(d["w"], dt)
+    y = empty_dev((M, N), dt, offset=3)
+    _, _, rstd, fp = rn.rmsnorm_fwd_ex(x, w, y=y, eps=1e-6)
+    assert fp["plan_id"] == stream_plan_for(N, fwd=True)
     r32 = _rstd32_all_rows(d["x"], d["w"], dt, 1e-6)
     dx, dw, p = rn.rmsnorm_bwd_ex(dy, x, w, torch.from_numpy(r32).cuda(), eps=1e-6)
     torch.cuda.synchronize()
@@ -298,6 +306,9 @@ def test_streamed_backward_full_size_odd_row(rn):
     assert rn.lib().rmsnorm_device_status(1) == 0
     rows = sampled_rows(M, seed=7)
     rows_t = torch.from_numpy(rows).cuda()
+    f = oracle.fwd(d["x"][rows], d["w"], dtype=dt, eps=1e-6, offset=0.0)
+    check_y(to_host(y[rows_t], dt), f, dt)
+    check_rstd(rstd.cpu().numpy()[rows], f["rstd64"])
     b = oracle.bwd(d["dy"][rows], d["x"][rows], d["w"], dtype=dt, eps=1e-6, offset=0.0, rstd=r32[rows])
     check_dx(to_host(dx[rows_t], dt), b, dt)
     full = oracle.bwd(d["dy"], d["x"], d["w"], dtype=dt, eps=1e-6, offset=0.0, rstd=r32, want_dx=False, nthreads=8)
