@@ -214,8 +214,10 @@ rmsnorm_status_t rmsnorm_fwd_fp8(const void *x, const void *residual, const void
  * variance is the biased one, computed from the row held in registers in
  * two passes (sum, then squared deviations from the mean).
  * gamma == NULL: factor 1 (offset unused); beta == NULL: no bias.
- * gamma, beta, dgamma, dbeta have the activations' storage type
- * (RMSNORM_WEIGHT_F32 is UNSUPPORTED). mean and rstd [M] are fp32.
+ * gamma, beta, dgamma, dbeta have the activations' storage type, or fp32
+ * beside bf16 / fp16 activations (RMSNORM_BF16_W32, RMSNORM_F16_W32; then
+ * only rows on 16-byte boundaries are vectorised and a forced alternative
+ * plan returns UNSUPPORTED, as for RMSNorm). mean and rstd [M] are fp32.
  * residual / residual_out: both NULL, or both set for the fused add
  * (h = R(x + residual), stored to residual_out, as in rmsnorm_add_fwd).
  * Pointers, alignment, errors and aliasing as for the RMSNorm calls.

@@ -144,6 +144,26 @@ def _dtype_code_w(x: torch.Tensor, w) -> int:
     raise ValueError(f"w must be {x.dtype} or torch.float32, is {w.dtype}")
 
 
+def _param_dtype(x: torch.Tensor, *params) -> torch.dtype:
+    """The storage type shared by LayerNorm's gamma / beta (and their
+    gradients) among the given tensors (None entries skipped): x's type, or
+    fp32 beside 16-bit activations; x's type when none is given."""
+    for t in params:
+        if t is not None and t.device != x.device:
+            raise ValueError("gamma, beta and their gradients must be on the input's device")
+    types = {t.dtype for t in params if t is not None}
+    if len(types) > 1:
+        raise ValueError(f"gamma, beta and their gradients must share one type, have {sorted(map(str, types))}")
+    dt = types.pop() if types else x.dtype
+    if dt != x.dtype and not (dt == torch.float32 and x.dtype in (torch.bfloat16, torch.float16)):
+        raise ValueError(f"gamma / beta must be {x.dtype} or (beside 16-bit x) torch.float32, are {dt}")
+    return dt
+
+
+def _param_code(x: torch.Tensor, dt: torch.dtype) -> int:
+    return _dtype_code(x) | (RMSNORM_WEIGHT_F32 if dt != x.dtype else 0)
+
+
 def _check_w(w, name: str, x: torch.Tensor, N: int):
     _check(w, name, numel=N)
     if w.device != x.device:
@@ -381,9 +401,10 @@ def layernorm_fwd(x, gamma, beta, *, residual=None, eps: float = 1e-5, offset: f
     Returns a dict with y, residual_out (fused only), mean, rstd, plan."""
     M, N = _rows(x)
     _check(x, "x")
+    pdt = _param_dtype(x, gamma, beta)
     for t, n in ((gamma, "gamma"), (beta, "beta")):
         if t is not None:
-            _check(t, n, like=x, numel=N)
+            _check(t, n, numel=N)
     y = torch.empty_like(x) if y is None else y
     _check(y, "y", like=x, numel=x.numel())
     if residual is not None:
@@ -396,8 +417,8 @@ def layernorm_fwd(x, gamma, beta, *, residual=None, eps: float = 1e-5, offset: f
     _check(rstd, "rstd", numel=M)
     p = Plan()
     st = lib().layernorm_fwd_ex(x.data_ptr(), _ptr(residual), _ptr(gamma), _ptr(beta), y.data_ptr(),
-                                _ptr(residual_out), mean.data_ptr(), rstd.data_ptr(), M, N, _dtype_code(x), eps,
-                                offset, _stream_handle(stream, x.device), force_plan, ctypes.byref(p))
+                                _ptr(residual_out), mean.data_ptr(), rstd.data_ptr(), M, N, _param_code(x, pdt),
+                                eps, offset, _stream_handle(stream, x.device), force_plan, ctypes.byref(p))
     _raise(st, "layernorm_fwd")
     return {"y": y, "residual_out": residual_out, "mean": mean, "rstd": rstd, "plan": p.as_dict()}
 
@@ -417,23 +438,25 @@ def layernorm_bwd(dy, x, gamma, mean, rstd, *, dresidual_out=None, want_dgamma=T
         _check(dresidual_out, "dresidual_out", like=x, numel=x.numel())
     dx = torch.empty_like(x) if dx is None else dx
     _check(dx, "dx", like=x, numel=x.numel())
+    # gamma, dgamma and dbeta share one type: x's, or fp32 beside 16-bit x
+    pdt = _param_dtype(x, gamma, dgamma if want_dgamma else None, dbeta if want_dbeta else None)
     if gamma is not None:
-        _check(gamma, "gamma", like=x, numel=N)
+        _check(gamma, "gamma", numel=N)
     if gamma is not None and want_dgamma:
-        dgamma = torch.empty(N, dtype=x.dtype, device=x.device) if dgamma is None else dgamma
-        _check(dgamma, "dgamma", like=x, numel=N)
+        dgamma = torch.empty(N, dtype=pdt, device=x.device) if dgamma is None else dgamma
+        _check(dgamma, "dgamma", numel=N)
     else:
         dgamma = None
     if want_dbeta:
-        dbeta = torch.empty(N, dtype=x.dtype, device=x.device) if dbeta is None else dbeta
-        _check(dbeta, "dbeta", like=x, numel=N)
+        dbeta = torch.empty(N, dtype=pdt, device=x.device) if dbeta is None else dbeta
+        _check(dbeta, "dbeta", numel=N)
     else:
         dbeta = None
     wp, wb = _ws(workspace)
     p = Plan()
     st = lib().layernorm_bwd_ex(dy.data_ptr(), _ptr(dresidual_out), x.data_ptr(), _ptr(gamma), mean.data_ptr(),
                                 rstd.data_ptr(), dx.data_ptr(), _ptr(dgamma), _ptr(dbeta), wp, wb, M, N,
-                                _dtype_code(x), eps, offset, _stream_handle(stream, x.device), force_plan,
+                                _param_code(x, pdt), eps, offset, _stream_handle(stream, x.device), force_plan,
                                 force_ctas, ctypes.byref(p))
     _raise(st, "layernorm_bwd")
     return {"dx": dx, "dgamma": dgamma, "dbeta": dbeta, "plan": p.as_dict()}

@@ -25,7 +25,7 @@ LIB = os.path.join(HERE, "librmsnorm_gb300.so")
 HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
 
 SOURCES = ["api.cu", "fwd_bf16.cu", "fwd_f32.cu", "fwd_f16.cu", "fwd_bf16w32.cu", "fwd_f16w32.cu",
-           "fwd8_bf16.cu", "fwd8_f16.cu", "fwd8_f32.cu", "fwd8_bf16w32.cu", "fwd8_f16w32.cu", "ln_bf16.cu", "ln_f16.cu", "ln_f32.cu",
+           "fwd8_bf16.cu", "fwd8_f16.cu", "fwd8_f32.cu", "fwd8_bf16w32.cu", "fwd8_f16w32.cu", "ln_bf16.cu", "ln_f16.cu", "ln_f32.cu", "ln_bf16w32.cu", "ln_f16w32.cu",
            "bwd_bf16.cu", "bwd_f32.cu", "bwd_f16.cu", "bwd_bf16w32.cu", "bwd_f16w32.cu",
            "noalloc.cu"]
 HEADERS = ["common.cuh", "plans.h", "fwd_kernels.cuh", "bwd_kernels.cuh"]

@@ -383,18 +383,22 @@ static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed) {
 }
 
 static const void *ln_bwd_kernel(int plan_id, int dt, bool fused) {
-    switch (base_dtype(dt)) {
-    case RMSNORM_BF16: return ln_bwd_kernel_ptr_bf16(plan_id, fused);
-    case RMSNORM_F16: return ln_bwd_kernel_ptr_f16(plan_id, fused);
+    switch (kind_of(dt)) {
+    case 1: return ln_bwd_kernel_ptr_bf16(plan_id, fused);
+    case 2: return ln_bwd_kernel_ptr_f16(plan_id, fused);
+    case 3: return ln_bwd_kernel_ptr_bf16w32(plan_id, fused);
+    case 4: return ln_bwd_kernel_ptr_f16w32(plan_id, fused);
     default: return ln_bwd_kernel_ptr_f32(plan_id, fused);
     }
 }
 
 static const void *fwd_staged_kernel(int plan_id, int dt, bool fused, bool ln) {
     if (ln) {
-        switch (base_dtype(dt)) {
-        case RMSNORM_BF16: return ln_fwd_staged_kernel_ptr_bf16(plan_id, fused);
-        case RMSNORM_F16: return ln_fwd_staged_kernel_ptr_f16(plan_id, fused);
+        switch (kind_of(dt)) {
+        case 1: return ln_fwd_staged_kernel_ptr_bf16(plan_id, fused);
+        case 2: return ln_fwd_staged_kernel_ptr_f16(plan_id, fused);
+        case 3: return ln_fwd_staged_kernel_ptr_bf16w32(plan_id, fused);
+        case 4: return ln_fwd_staged_kernel_ptr_f16w32(plan_id, fused);
         default: return ln_fwd_staged_kernel_ptr_f32(plan_id, fused);
         }
     }
@@ -437,9 +441,11 @@ static int launch_fwd8_dt(int dt, int plan_id, bool fused, int mode, const FwdPa
 static int launch_fwd_staged_dt(int dt, bool ln, int plan_id, bool fused, const FwdParams &p, int grid, int smem,
                                 void *stream) {
     if (ln) {
-        switch (base_dtype(dt)) {
-        case RMSNORM_BF16: return launch_ln_fwd_staged_bf16(plan_id, fused, p, grid, smem, stream);
-        case RMSNORM_F16: return launch_ln_fwd_staged_f16(plan_id, fused, p, grid, smem, stream);
+        switch (kind_of(dt)) {
+        case 1: return launch_ln_fwd_staged_bf16(plan_id, fused, p, grid, smem, stream);
+        case 2: return launch_ln_fwd_staged_f16(plan_id, fused, p, grid, smem, stream);
+        case 3: return launch_ln_fwd_staged_bf16w32(plan_id, fused, p, grid, smem, stream);
+        case 4: return launch_ln_fwd_staged_f16w32(plan_id, fused, p, grid, smem, stream);
         default: return launch_ln_fwd_staged_f32(plan_id, fused, p, grid, smem, stream);
         }
     }
@@ -1105,7 +1111,6 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
                                     rmsnorm_plan_t *used) {
     if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
     if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
-    if (mixed_kind(kind_of(dt))) return RMSNORM_ERR_UNSUPPORTED;  // gamma, beta in the activations' type
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
     if (M == 0) return RMSNORM_SUCCESS;
@@ -1113,8 +1118,9 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
     if (fused && (!residual || !residual_out)) return RMSNORM_ERR_INVALID_ARG;
     if (!x || !y || !mean || !rstd) return RMSNORM_ERR_INVALID_ARG;
     const uintptr_t s = (uintptr_t)elem_size(dt);
-    if (!aligned_to(x, s) || !aligned_to(y, s) || (gamma && !aligned_to(gamma, s)) || (beta && !aligned_to(beta, s)) ||
-        !aligned_to(mean, 4) || !aligned_to(rstd, 4))
+    const uintptr_t wsz = (uintptr_t)weight_size(dt);  // gamma and beta: the activations' type or fp32
+    if (!aligned_to(x, s) || !aligned_to(y, s) || (gamma && !aligned_to(gamma, wsz)) ||
+        (beta && !aligned_to(beta, wsz)) || !aligned_to(mean, 4) || !aligned_to(rstd, 4))
         return RMSNORM_ERR_INVALID_ARG;
     if (fused && (!aligned_to(residual, s) || !aligned_to(residual_out, s))) return RMSNORM_ERR_INVALID_ARG;
     // gamma and beta must share the rows' offset (beta as a second "row")
@@ -1156,9 +1162,11 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
     if (stages > 0) {
         le = launch_fwd_staged_dt(dt, true, plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream);
     } else {
-        switch (base_dtype(dt)) {
-        case RMSNORM_BF16: le = launch_ln_fwd_bf16(plan.plan_id, fused, p, plan.ctas, stream); break;
-        case RMSNORM_F16: le = launch_ln_fwd_f16(plan.plan_id, fused, p, plan.ctas, stream); break;
+        switch (kind_of(dt)) {
+        case 1: le = launch_ln_fwd_bf16(plan.plan_id, fused, p, plan.ctas, stream); break;
+        case 2: le = launch_ln_fwd_f16(plan.plan_id, fused, p, plan.ctas, stream); break;
+        case 3: le = launch_ln_fwd_bf16w32(plan.plan_id, fused, p, plan.ctas, stream); break;
+        case 4: le = launch_ln_fwd_f16w32(plan.plan_id, fused, p, plan.ctas, stream); break;
         default: le = launch_ln_fwd_f32(plan.plan_id, fused, p, plan.ctas, stream); break;
         }
     }
@@ -1174,19 +1182,19 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
                                     rmsnorm_plan_t *used) {
     if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
     if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
-    if (mixed_kind(kind_of(dt))) return RMSNORM_ERR_UNSUPPORTED;
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
     const uintptr_t s = (uintptr_t)elem_size(dt);
+    const uintptr_t wsz = (uintptr_t)weight_size(dt);  // gamma, dgamma, dbeta: the activations' type or fp32
     // dgamma needs gamma; without gamma the weight factor is 1 and there is no dgamma
     if (dgamma && !gamma) return RMSNORM_ERR_INVALID_ARG;
-    if ((gamma && !aligned_to(gamma, s)) || (dgamma && !aligned_to(dgamma, s)) || (dbeta && !aligned_to(dbeta, s)))
+    if ((gamma && !aligned_to(gamma, wsz)) || (dgamma && !aligned_to(dgamma, wsz)) || (dbeta && !aligned_to(dbeta, wsz)))
         return RMSNORM_ERR_INVALID_ARG;
     const bool want = dgamma != nullptr || dbeta != nullptr;
     if (M == 0) {  // the parameter gradients are the empty sums
         cudaError_t e = cudaSuccess;
-        if (dgamma) e = cudaMemsetAsync(dgamma, 0, (size_t)N * s, stream);
-        if (e == cudaSuccess && dbeta) e = cudaMemsetAsync(dbeta, 0, (size_t)N * s, stream);
+        if (dgamma) e = cudaMemsetAsync(dgamma, 0, (size_t)N * wsz, stream);
+        if (e == cudaSuccess && dbeta) e = cudaMemsetAsync(dbeta, 0, (size_t)N * wsz, stream);
         return e == cudaSuccess ? RMSNORM_SUCCESS : cuda_fail(e);
     }
     if (!dy || !x || !mean || !rstd || !dx) return RMSNORM_ERR_INVALID_ARG;
@@ -1248,9 +1256,11 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
     p.cache_row = generic_bwd_cache(pd->path, N, (int)s, ws != nullptr, call.cps);
     if (p.cache_row) plan.smem_bytes = (int32_t)(2 * generic_bwd_cache_slot(N, (int)s));
     int le;
-    switch (base_dtype(dt)) {
-    case RMSNORM_BF16: le = launch_ln_bwd_bf16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
-    case RMSNORM_F16: le = launch_ln_bwd_f16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+    switch (kind_of(dt)) {
+    case 1: le = launch_ln_bwd_bf16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+    case 2: le = launch_ln_bwd_f16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+    case 3: le = launch_ln_bwd_bf16w32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+    case 4: le = launch_ln_bwd_f16w32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
     default: le = launch_ln_bwd_f32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
     }
     // one finalizer over the [units, 2N] partial rows: dgamma | dbeta (a
@@ -1386,7 +1396,6 @@ rmsnorm_status_t layernorm_bwd_ex(const void *dy, const void *dresidual_out, con
 }
 
 size_t layernorm_bwd_workspace_bytes(int64_t M, int64_t N, rmsnorm_dtype_t dt) {
-    if (mixed_kind(kind_of(dt))) return 0;
     return bwd_workspace_bytes(RMSNORM_OP_LN_BWD, M, N, dt);
 }
 

@@ -409,9 +409,9 @@ __global__ void __launch_bounds__(TPR *TEAMS) rmsnorm_bwd_vector(const BwdParams
     bwd_vector_body<T, TW, TPR, V, TEAMS, D, CS, PACKED, FUSED, false>(p);
 }
 
-template <typename T, int TPR, int V, int TEAMS, int D, int CS, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool FUSED>
 __global__ void __launch_bounds__(TPR *TEAMS) layernorm_bwd_vector(const BwdParams p) {
-    bwd_vector_body<T, T, TPR, V, TEAMS, D, CS, true, FUSED, true>(p);
+    bwd_vector_body<T, TW, TPR, V, TEAMS, D, CS, true, FUSED, true>(p);
 }
 
 // Staged persistent main kernel (bulk-copy pipeline). Each row's x and dy
@@ -452,8 +452,11 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     extern __shared__ float4 stage_smem[];  // ns * NB * Cb chunks of 16 bytes (+ Cb for gamma)
     pdl_wait();  // before any read of the rows (the bulk copies included)
     // The LayerNorm re-read schedule keeps gamma in shared memory after the
-    // stages rather than in registers (its two accumulators fill them).
-    constexpr bool WSM = LN && !HOLD;
+    // stages rather than in registers (its two accumulators fill them); an
+    // fp32 gamma beside 16-bit activations is read from global memory (L1)
+    // where it is used instead.
+    constexpr bool WSM = LN && !HOLD && std::is_same<T, TW>::value;
+    constexpr bool GG = LN && !HOLD && !std::is_same<T, TW>::value;
 
     const int N = p.N;
     const int C = N / E;
@@ -551,12 +554,12 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     // which keeps the thread within its registers
     constexpr bool RAW = V >= 3 && E == 8 && std::is_same<T, TW>::value && !WSM;
     uint4 wraw[RAW ? V : 1];
-    float2 wp[RAW || WSM ? 1 : V][NP], acc[V][NP];
+    float2 wp[RAW || WSM || GG ? 1 : V][NP], acc[V][NP];
     float2 accb[LN ? V : 1][NP];  // LayerNorm: sum dy (dbeta)
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int cl = v * TPR + t;  // chunk of this CTA's slice; cbase + cl in the row
-        if constexpr (WSM) {
+        if constexpr (WSM || GG) {
         } else if constexpr (RAW) {
             wraw[v] = (has_w && cl < Cs) ? ld_w_raw<T>(p.w, cbase + cl, C, peel) : make_uint4(0, 0, 0, 0);
         } else {
@@ -577,7 +580,17 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         }
     }
     auto wfac = [&](int v, float2 (&f)[NP]) {
-        if constexpr (WSM || RAW) {
+        if constexpr (GG) {
+            const int cl = v * TPR + t;
+            if (has_w && cl < Cs) {
+                load_w_chunk_row<T, TW>(p.w, cbase + cl, C, peel, f);
+            } else {
+#pragma unroll
+                for (int q = 0; q < NP; ++q) f[q] = make_float2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < NP; ++q) f[q] = has_w ? Pk::add(o2, f[q]) : make_float2(1.f, 1.f);
+        } else if constexpr (WSM || RAW) {
             const int cl = v * TPR + t;
             if constexpr (WSM)
                 unpack<T>(has_w && cl < Cs ? lds128(wsm + cl) : make_uint4(0, 0, 0, 0), f);
@@ -784,9 +797,9 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) 
     staged_body<T, TW, TPR, V, S, CS, FUSED, false, HOLD, PACKED>(p);
 }
 
-template <typename T, int TPR, int V, int S, int CS, bool FUSED, bool HOLD>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool HOLD>
 __global__ void __launch_bounds__(TPR, 1) layernorm_bwd_staged(const BwdParams p) {
-    staged_body<T, T, TPR, V, S, CS, FUSED, true, HOLD>(p);
+    staged_body<T, TW, TPR, V, S, CS, FUSED, true, HOLD>(p);
 }
 
 // Generic main kernel: one 256-thread CTA per row at a time, any N and
@@ -1049,7 +1062,7 @@ __global__ void __launch_bounds__(TPR, TPR >= 512 ? 1 : 512 / TPR) rmsnorm_bwd_s
 // memory (L1/L2) and the update comes before the barrier, since dx may
 // overwrite dy. Both variants are held to the registers of five CTAs an
 // SM, the residency the grid is sized for.
-template <typename T, bool FUSED, bool CACHE>
+template <typename T, typename TW, bool FUSED, bool CACHE>
 __global__ void __launch_bounds__(256, 5) layernorm_bwd_generic(const BwdParams p) {
     __shared__ float2 red[32];
     extern __shared__ uint4 gen_smem[];
@@ -1057,7 +1070,7 @@ __global__ void __launch_bounds__(256, 5) layernorm_bwd_generic(const BwdParams 
     constexpr int E = Elem<T>::E;
     constexpr int NP = Elem<T>::NP;
     const int N = p.N;
-    const T *w = reinterpret_cast<const T *>(p.w);
+    const TW *w = reinterpret_cast<const TW *>(p.w);
     float *wsrow = p.ws ? p.ws + (int64_t)blockIdx.x * 2 * N : nullptr;
     const bool has_dres = FUSED && p.dres != nullptr;
     const uint32_t a16 = addr_mod16(p.x);
@@ -1099,7 +1112,7 @@ __global__ void __launch_bounds__(256, 5) layernorm_bwd_generic(const BwdParams 
                 float2 dv[NP], xv[NP], wv[NP];
                 load_chunk_at(dy, j0, vdy, dv);
                 load_chunk_at(x, j0, true, xv);
-                if (w) w_chunk_at<T, T>(w, j0, wv);
+                if (w) w_chunk_at<T, TW>(w, j0, wv);
                 if (cache) {
                     store_chunk_at(xs, j0, true, xv);
                     store_chunk_at(ds, j0, true, dv);
@@ -1140,7 +1153,7 @@ __global__ void __launch_bounds__(256, 5) layernorm_bwd_generic(const BwdParams 
                 float2 dv[NP], xv[NP], wv[NP], rv[NP];
                 load_chunk_at(dyr, j0, vdyr, dv);
                 load_chunk_at(xr, j0, true, xv);
-                if (w) w_chunk_at<T, T>(w, j0, wv);
+                if (w) w_chunk_at<T, TW>(w, j0, wv);
                 if (has_dres) load_chunk_at(dr, j0, vdr, rv);
 #pragma unroll
                 for (int q = 0; q < NP; ++q)
@@ -1427,68 +1440,72 @@ static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *
 
 // ------------------------------------------------- LayerNorm dispatch --
 
-template <typename T, int TPR, int V, int TEAMS, int D, int CS>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS>
 static int ln_bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     LaunchCfg lc((unsigned)grid, TPR * TEAMS, (size_t)smem, s, CS > 1 ? CS : 0);
-    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true>, p)
-                 : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false>, p);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false>, p);
 }
 
-template <typename T, int TPR, int V, int S, int CS, bool HOLD>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool HOLD>
 static int ln_bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    const void *k = fused ? (const void *)layernorm_bwd_staged<T, TPR, V, S, CS, true, HOLD>
-                          : (const void *)layernorm_bwd_staged<T, TPR, V, S, CS, false, HOLD>;
+    const void *k = fused ? (const void *)layernorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD>
+                          : (const void *)layernorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD>;
     const int e = allow_staged_smem(k);
     if (e != 0) return e;
     LaunchCfg lc((unsigned)grid, TPR, (size_t)smem, s, CS);
-    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_staged<T, TPR, V, S, CS, true, HOLD>, p)
-                 : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_staged<T, TPR, V, S, CS, false, HOLD>, p);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD>, p);
 }
 
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
+// An fp32 gamma beside 16-bit activations is compiled for the default
+// plans and the generic one only.
+template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
 static int ln_bwd_launch_entry(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    if constexpr (OP != OP_LN_BWD) {
+    if constexpr (OP != OP_LN_BWD || !(std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0)) {
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
         const int gs = generic_bwd_smem<T>(p);
         LaunchCfg lc((unsigned)grid, 256, (size_t)gs, s);
         if (fused)
-            return gs ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, true, true>, p)
-                      : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, true, false>, p);
-        return gs ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, false, true>, p)
-                  : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, false, false>, p);
+            return gs ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, TW, true, true>, p)
+                      : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, TW, true, false>, p);
+        return gs ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, TW, false, true>, p)
+                  : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, TW, false, false>, p);
     } else if constexpr (PATH == PATH_VECTOR) {
-        return ln_bwd_launch_vec<T, TPR, V, TEAMS, D, CS>(fused, p, grid, smem, s);
+        return ln_bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS>(fused, p, grid, smem, s);
     } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
-        return ln_bwd_launch_staged<T, TPR, V, D, CS, PATH == PATH_STAGED>(fused, p, grid, smem, s);
+        return ln_bwd_launch_staged<T, TW, TPR, V, D, CS, PATH == PATH_STAGED>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
 }
 
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS>
+template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
 static const void *ln_bwd_ptr_entry(bool fused) {
-    if constexpr (OP != OP_LN_BWD) {
+    if constexpr (OP != OP_LN_BWD || !(std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0)) {
         return nullptr;
     } else if constexpr (PATH == PATH_GENERIC) {
-        return fused ? (const void *)layernorm_bwd_generic<T, true, false> : (const void *)layernorm_bwd_generic<T, false, false>;
+        return fused ? (const void *)layernorm_bwd_generic<T, TW, true, false>
+                     : (const void *)layernorm_bwd_generic<T, TW, false, false>;
     } else if constexpr (PATH == PATH_VECTOR) {
-        return fused ? (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, true>
-                     : (const void *)layernorm_bwd_vector<T, TPR, V, TEAMS, D, CS, false>;
+        return fused ? (const void *)layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true>
+                     : (const void *)layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false>;
     } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
-        return fused ? (const void *)layernorm_bwd_staged<T, TPR, V, D, CS, true, PATH == PATH_STAGED>
-                     : (const void *)layernorm_bwd_staged<T, TPR, V, D, CS, false, PATH == PATH_STAGED>;
+        return fused ? (const void *)layernorm_bwd_staged<T, TW, TPR, V, D, CS, true, PATH == PATH_STAGED>
+                     : (const void *)layernorm_bwd_staged<T, TW, TPR, V, D, CS, false, PATH == PATH_STAGED>;
     } else {
         return nullptr;
     }
 }
 
-template <typename T>
+// (TW: gamma's type, the activations' or fp32)
+template <typename T, typename TW = T>
 static int ln_bwd_launch_t(int plan_id, bool fused, const BwdParams &p, int grid, int smem, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (plan_id) {
 #define RMSN_LN_BWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return ln_bwd_launch_entry<T, op, path, tpr, v, teams, depth, cs>(fused, p, grid, smem, s);
+    case id: return ln_bwd_launch_entry<T, TW, op, path, tpr, v, teams, depth, cs, cmin>(fused, p, grid, smem, s);
         RMSNORM_PLAN_TABLE(RMSN_LN_BWD_CASE)
 #undef RMSN_LN_BWD_CASE
     default:
@@ -1496,11 +1513,11 @@ static int ln_bwd_launch_t(int plan_id, bool fused, const BwdParams &p, int grid
     }
 }
 
-template <typename T>
+template <typename T, typename TW = T>
 static const void *ln_bwd_ptr_t(int plan_id, bool fused) {
     switch (plan_id) {
 #define RMSN_LN_BWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return ln_bwd_ptr_entry<T, op, path, tpr, v, teams, depth, cs>(fused);
+    case id: return ln_bwd_ptr_entry<T, TW, op, path, tpr, v, teams, depth, cs, cmin>(fused);
         RMSNORM_PLAN_TABLE(RMSN_LN_BWD_PTR)
 #undef RMSN_LN_BWD_PTR
     default:

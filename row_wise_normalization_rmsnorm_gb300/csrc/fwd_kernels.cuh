@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
 // sum of squared deviations from it (a two-pass variance, which loses
 // nothing to cancellation when the mean is large), then
 // y = (h - mean) rstd (offset + gamma) + beta, rounded once.
-template <typename T, int TPR, int V, int TEAMS, int CS, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED>
 __global__ void __launch_bounds__(TPR *TEAMS)
     layernorm_fwd_vector(const FwdParams p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             float2 a[NP], gv[NP], bv[NP];
             unpack<T>(xv[v], a);
             if (p.w) {
-                unpack<T>(ld_w_raw<T>(p.w, c, C, p.peel), gv);
+                load_w_chunk_row<T, TW>(p.w, c, C, p.peel, gv);
 #pragma unroll
                 for (int k = 0; k < NP; ++k) gv[k] = Pk::add(o2, gv[k]);
             } else {
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                 for (int k = 0; k < NP; ++k) gv[k] = make_float2(1.f, 1.f);
             }
             if (p.beta) {
-                unpack<T>(ld_w_raw<T>(p.beta, c, C, p.peel), bv);
+                load_w_chunk_row<T, TW>(p.beta, c, C, p.peel, bv);
             } else {
 #pragma unroll
                 for (int k = 0; k < NP; ++k) bv[k] = make_float2(0.f, 0.f);
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
 
 // Generic LayerNorm forward: one 256-thread CTA per row, three passes over
 // the row (the later ones served by L1/L2), split like the RMSNorm one.
-template <typename T, bool FUSED>
+template <typename T, typename TW, bool FUSED>
 __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) {
     __shared__ float red[32];
     extern __shared__ uint4 gen_smem[];
@@ -488,8 +488,8 @@ __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) 
     const T *x = reinterpret_cast<const T *>(p.x) + row * N;
     const T *res = reinterpret_cast<const T *>(p.residual) + row * N;
     T *hout = reinterpret_cast<T *>(p.residual_out) + row * N;
-    const T *g = reinterpret_cast<const T *>(p.w);
-    const T *b = reinterpret_cast<const T *>(p.beta);
+    const TW *g = reinterpret_cast<const TW *>(p.w);
+    const TW *b = reinterpret_cast<const TW *>(p.beta);
     T *y = reinterpret_cast<T *>(p.y) + row * N;
     const uint32_t a16 = addr_mod16(p.x);
     const bool vy = addr_mod16(p.y) == a16;
@@ -560,12 +560,12 @@ __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) 
     };
     row_visit<E>(
         sp, N,
-        [&](int j) { store_elem(y, j, y_of(h_at(j), g ? load_elem(g, j) : 0.f, b ? load_elem(b, j) : 0.f)); },
+        [&](int j) { store_elem(y, j, y_of(h_at(j), g ? load_w(g, j) : 0.f, b ? load_w(b, j) : 0.f)); },
         [&](int j0) {
             float2 h[NP], gv[NP], bv[NP];
             h_chunk(j0, h);
-            if (g) w_chunk_at<T, T>(g, j0, gv);
-            if (b) w_chunk_at<T, T>(b, j0, bv);
+            if (g) w_chunk_at<T, TW>(g, j0, gv);
+            if (b) w_chunk_at<T, TW>(b, j0, bv);
 #pragma unroll
             for (int q = 0; q < NP; ++q)
                 h[q] = make_float2(y_of(h[q].x, g ? gv[q].x : 0.f, b ? bv[q].x : 0.f),
@@ -769,7 +769,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
             if constexpr (LN) {
                 float2 gv[NP], bv[NP];
                 if (p.w) {
-                    unpack<T>(ld_w_raw<T>(p.w, c, C, peel), gv);
+                    load_w_chunk_row<T, TW>(p.w, c, C, peel, gv);
 #pragma unroll
                     for (int j = 0; j < NP; ++j) gv[j] = Pk::add(o2, gv[j]);
                 } else {
@@ -777,7 +777,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                     for (int j = 0; j < NP; ++j) gv[j] = make_float2(1.f, 1.f);
                 }
                 if (p.beta) {
-                    unpack<T>(ld_w_raw<T>(p.beta, c, C, peel), bv);
+                    load_w_chunk_row<T, TW>(p.beta, c, C, peel, bv);
                 } else {
 #pragma unroll
                     for (int j = 0; j < NP; ++j) bv[j] = make_float2(0.f, 0.f);
@@ -876,9 +876,9 @@ __global__ void __launch_bounds__(TPR, 1) rmsnorm_fwd_staged(const FwdParams p) 
     staged_fwd_body<T, TW, TPR, V, S, CS, FUSED, false, Q>(p);
 }
 
-template <typename T, int TPR, int V, int S, int CS, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED>
 __global__ void __launch_bounds__(TPR, 1) layernorm_fwd_staged(const FwdParams p) {
-    staged_fwd_body<T, T, TPR, V, S, CS, FUSED, true>(p);
+    staged_fwd_body<T, TW, TPR, V, S, CS, FUSED, true>(p);
 }
 
 // Streamed generic forward: persistent CTAs, rows of any alignment and of
@@ -1116,8 +1116,8 @@ static const void *staged_fwd_ptr_entry(bool fused) {
                          !instantiated<T, TW, PATH, CMIN, Q>() || (LN && Q != QOUT_NONE)) {
         return nullptr;
     } else if constexpr (LN) {
-        return fused ? (const void *)layernorm_fwd_staged<T, TPR, V, D, CS, true>
-                     : (const void *)layernorm_fwd_staged<T, TPR, V, D, CS, false>;
+        return fused ? (const void *)layernorm_fwd_staged<T, TW, TPR, V, D, CS, true>
+                     : (const void *)layernorm_fwd_staged<T, TW, TPR, V, D, CS, false>;
     } else {
         return fused ? (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, true, Q>
                      : (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, false, Q>;
@@ -1183,27 +1183,28 @@ static int launch_q(int plan_id, bool fused, int mode, const FwdParams &p, int g
 
 // LayerNorm forward: the forward plans' geometry, default plans and the
 // generic one.
-template <typename T, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
+template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
 static int ln_launch_entry(bool fused, const FwdParams &p, int grid, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if constexpr (OP != OP_FWD || !(PATH == PATH_GENERIC || CMIN > 0)) {
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
         LaunchCfg lc((unsigned)grid, 256, (size_t)gen_cache_bytes<T>(p), s);
-        return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_generic<T, true>, p)
-                     : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_generic<T, false>, p);
+        return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_generic<T, TW, true>, p)
+                     : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_generic<T, TW, false>, p);
     } else {
         LaunchCfg lc((unsigned)grid, TPR * TEAMS, 0, s, CS > 1 ? CS : 0);
-        return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_vector<T, TPR, V, TEAMS, CS, true>, p)
-                     : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_vector<T, TPR, V, TEAMS, CS, false>, p);
+        return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true>, p)
+                     : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false>, p);
     }
 }
 
-template <typename T>
+// (TW: gamma's and beta's type, the activations' or fp32)
+template <typename T, typename TW = T>
 static int ln_launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
     switch (plan_id) {
 #define RMSN_LN_FWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return ln_launch_entry<T, op, path, tpr, v, teams, cs, cmin>(fused, p, grid, stream);
+    case id: return ln_launch_entry<T, TW, op, path, tpr, v, teams, cs, cmin>(fused, p, grid, stream);
         RMSNORM_PLAN_TABLE(RMSN_LN_FWD_CASE)
 #undef RMSN_LN_FWD_CASE
     default:

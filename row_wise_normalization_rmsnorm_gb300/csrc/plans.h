@@ -339,8 +339,9 @@ int launch_dw_finalize_bf16(const float *ws, int parts, int ncols, void *out0, v
 int launch_dw_finalize_f16(const float *ws, int parts, int ncols, void *out0, void *out1, int split, int peel,
                            void *stream, bool serial);
 
-// LayerNorm forward and backward main kernels (weight in the activations'
-// type; the default plans and the generic one).
+// LayerNorm forward and backward main kernels (gamma and beta in the
+// activations' type, or fp32 beside 16-bit activations: "w32"; the default
+// plans and the generic one).
 #define RMSN_DECLARE_LN(suf)                                                                               \
     int launch_ln_fwd_##suf(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);         \
     int launch_ln_bwd_##suf(int plan_id, bool fused, const BwdParams &p, int grid, int smem, void *stream); \
@@ -350,6 +351,8 @@ int launch_dw_finalize_f16(const float *ws, int parts, int ncols, void *out0, vo
 RMSN_DECLARE_LN(f32)
 RMSN_DECLARE_LN(bf16)
 RMSN_DECLARE_LN(f16)
+RMSN_DECLARE_LN(bf16w32)
+RMSN_DECLARE_LN(f16w32)
 #undef RMSN_DECLARE_LN
 
 }  // namespace rmsn

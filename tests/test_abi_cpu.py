@@ -189,10 +189,12 @@ def test_layernorm_invalid_arguments_without_gpu(rn):
     L = rn.lib()
     x = ctypes.c_void_p(256)
     r = ctypes.c_void_p(512)
-    # forward: residual without residual_out, missing mean, fp32 weight flag
+    # forward: residual without residual_out, missing mean, an fp32 gamma or
+    # beta not 4-byte aligned
     assert L.layernorm_fwd(x, x, x, None, x, None, r, r, 4, 8, 1, 1e-5, 0.0, None) == 1
     assert L.layernorm_fwd(x, None, x, None, x, None, None, r, 4, 8, 1, 1e-5, 0.0, None) == 1
-    assert L.layernorm_fwd(x, None, x, None, x, None, r, r, 4, 8, 0x101, 1e-5, 0.0, None) == 2
+    assert L.layernorm_fwd(x, None, ctypes.c_void_p(258), None, x, None, r, r, 4, 8, 0x101, 1e-5, 0.0, None) == 1
+    assert L.layernorm_fwd(x, None, x, ctypes.c_void_p(258), x, None, r, r, 4, 8, 0x101, 1e-5, 0.0, None) == 1
     assert L.layernorm_fwd(x, None, x, None, x, None, r, r, 0, 8, 1, 1e-5, 0.0, None) == 0
     # backward: dgamma without gamma, odd bf16 address, negative eps
     assert L.layernorm_bwd(x, None, x, None, r, r, x, x, None, None, 0, 4, 8, 1, 1e-5, 0.0, None) == 1

@@ -31,10 +31,12 @@ def _factor(d, dt, offset):
 
 
 def _ln_check(rn, d, dt, eps=1e-5, offset=0.0, fused=False, offset_elems=0, expect_path=None, gamma=True,
-              beta=True, want_dgamma=True, want_dbeta=True):
+              beta=True, want_dgamma=True, want_dbeta=True, wdt=None):
     """offset_elems: one element offset for every array, or a dict of
     offsets by array name (x, gamma, beta, y, residual, residual_out, dy,
-    dx, dgamma, dbeta, dres; missing names: 0)."""
+    dx, dgamma, dbeta, dres; missing names: 0). wdt: the storage type of
+    gamma, beta and their gradients (default the activations')."""
+    wdt = wdt or dt
     M, N = d["x"].shape
     offs = offset_elems if isinstance(offset_elems, dict) else None
 
@@ -43,19 +45,19 @@ def _ln_check(rn, d, dt, eps=1e-5, offset=0.0, fused=False, offset_elems=0, expe
     dg_np = d["w"] if gamma else None
     b_np = d.get("beta") if beta else None
     x = to_dev(d["x"], dt, offset=o("x"))
-    g = to_dev(dg_np, dt, offset=o("gamma")) if gamma else None
-    b = to_dev(b_np, dt, offset=o("beta")) if beta else None
+    g = to_dev(dg_np, wdt, offset=o("gamma")) if gamma else None
+    b = to_dev(b_np, wdt, offset=o("beta")) if beta else None
     y = empty_dev((M, N), dt, offset=o("y"))
     res = to_dev(d["residual"], dt, offset=o("residual")) if fused else None
     hout = empty_dev((M, N), dt, offset=o("residual_out")) if fused else None
     out = rn.layernorm_fwd(x, g, b, residual=res, residual_out=hout, y=y, eps=eps, offset=offset)
     f = oracle.ln_fwd(d["x"], dg_np, b_np, dtype=dt, eps=eps, offset=offset,
-                      residual=d.get("residual") if fused else None)
+                      residual=d.get("residual") if fused else None, wdtype=wdt)
     torch.cuda.synchronize()
     h_np = f["h"] if fused else d["x"]
     h64 = oracle.to_f64(h_np, dt)
-    factor = (offset + oracle.to_f64(dg_np, dt)) if gamma else np.ones(N)
-    bias = oracle.to_f64(b_np, dt) if beta else np.zeros(N)
+    factor = (offset + oracle.to_f64(dg_np, wdt)) if gamma else np.ones(N)
+    bias = oracle.to_f64(b_np, wdt) if beta else np.zeros(N)
     check_ln_y(to_host(y, dt), f, dt, h64, factor, bias)
     check_ln_stats(out["mean"].cpu().numpy(), out["rstd"].cpu().numpy(), f, h64)
     if fused:
@@ -67,20 +69,20 @@ def _ln_check(rn, d, dt, eps=1e-5, offset=0.0, fused=False, offset_elems=0, expe
     hdev = to_dev(h_np, dt, offset=o("x"))
     dy = to_dev(d["dy"], dt, offset=o("dy"))
     dx = empty_dev((M, N), dt, offset=o("dx"))
-    dgam = empty_dev((N,), dt, offset=o("dgamma")) if (gamma and want_dgamma) else None
-    dbet = empty_dev((N,), dt, offset=o("dbeta")) if want_dbeta else None
+    dgam = empty_dev((N,), wdt, offset=o("dgamma")) if (gamma and want_dgamma) else None
+    dbet = empty_dev((N,), wdt, offset=o("dbeta")) if want_dbeta else None
     dres_np = d.get("dres") if fused else None
     dres = to_dev(dres_np, dt, offset=o("dres")) if dres_np is not None else None
     bo = rn.layernorm_bwd(dy, hdev, g, m32, r32, dresidual_out=dres, eps=eps, offset=offset, dx=dx, dgamma=dgam,
                           dbeta=dbet, want_dgamma=want_dgamma, want_dbeta=want_dbeta)
     r = oracle.ln_bwd(d["dy"], h_np, dg_np, dtype=dt, eps=eps, offset=offset, mean=f["mean32"],
-                      rstd=f["rstd32"], dres=dres_np)
+                      rstd=f["rstd32"], dres=dres_np, wdtype=wdt)
     torch.cuda.synchronize()
     needed = check_dx(to_host(dx, dt), r, dt)
     if dgam is not None:
-        check_param_grad(to_host(dgam, dt), r["dg64"], r["dg_abs"], dt)
+        check_param_grad(to_host(dgam, wdt), r["dg64"], r["dg_abs"], wdt)
     if dbet is not None:
-        check_param_grad(to_host(dbet, dt), r["db64"], r["db_abs"], dt)
+        check_param_grad(to_host(dbet, wdt), r["db64"], r["db_abs"], wdt)
     if expect_path is not None:
         # "vector": the fast paths (the backward may stage rows in shared memory)
         fast = ("vector", "staged") if expect_path == "vector" else (expect_path,)
@@ -97,6 +99,27 @@ def test_ln_shapes(rn, dt, M, N):
     d = inputs.make_inputs(M, N, dt, 170 + N % 19, beta=True, x_shift=0.5)
     es = 4 if dt == "f32" else 2
     _ln_check(rn, d, dt, expect_path="vector" if (N * es) % 16 == 0 else "generic")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N", [(333, 64), (257, 1024), (300, 4096), (129, 8192), (65, 16384), (33, 32768),
+                                 (101, 8193), (40, 3), (200, 12288), (77, 2048)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_ln_fp32_params(rn, dt, M, N, fused):
+    """gamma, beta, dgamma and dbeta in fp32 beside 16-bit activations, on
+    register, staged (held and re-read schedules), cluster and generic rows."""
+    d = inputs.make_inputs(M, N, dt, 175 + N % 23, beta=True, x_shift=0.5, wdtype="f32", residual=fused,
+                           dres=fused)
+    _ln_check(rn, d, dt, fused=fused, expect_path="vector" if (N * 2) % 16 == 0 else "generic", wdt="f32")
+
+
+def test_ln_fp32_params_partial_outputs_and_alignment(rn):
+    """No gamma (dbeta alone), dgamma without dbeta, and a misaligned x,
+    which takes the generic kernels with fp32 parameters."""
+    d = inputs.make_inputs(300, 4096, "bf16", 176, beta=True, wdtype="f32")
+    _ln_check(rn, d, "bf16", gamma=False, wdt="f32")
+    _ln_check(rn, d, "bf16", want_dbeta=False, wdt="f32")
+    _ln_check(rn, d, "bf16", offset_elems={"x": 1, "y": 1, "dy": 1, "dx": 1}, expect_path="generic", wdt="f32")
 
 
 @pytest.mark.parametrize("dt,N", [("bf16", 32768), ("bf16", 65536), ("f32", 16384), ("f32", 32768)])
