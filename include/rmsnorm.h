@@ -89,7 +89,15 @@ typedef enum {
      * same as fp32. */
     RMSNORM_WEIGHT_F32 = 0x100,
     RMSNORM_BF16_W32 = 0x101, /* bf16 activations, fp32 w and dw */
-    RMSNORM_F16_W32 = 0x102   /* fp16 activations, fp32 w and dw */
+    RMSNORM_F16_W32 = 0x102,  /* fp16 activations, fp32 w and dw */
+    /* Forward only (rmsnorm_fwd, rmsnorm_add_fwd, rmsnorm_fwd_ex): OR'ed
+     * into RMSNORM_F32, y is stored in bf16 or fp16 (the key's otype apart
+     * from its itype), rounded once from the fp32 result; residual_out
+     * stays fp32. Vectorised where x, y (and the residual buffers) are
+     * 16-byte aligned and N % 4 == 0, generic otherwise. Other entry
+     * points return INVALID_ARG for these flags. */
+    RMSNORM_OUT_BF16 = 0x200,
+    RMSNORM_OUT_F16 = 0x400
 } rmsnorm_dtype_t;
 
 typedef enum {

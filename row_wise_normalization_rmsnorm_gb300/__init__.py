@@ -24,6 +24,8 @@ from ._binding import (  # noqa: F401
     RMSNORM_BF16,
     RMSNORM_F16,
     RMSNORM_F32,
+    RMSNORM_OUT_BF16,
+    RMSNORM_OUT_F16,
     RMSNORM_WEIGHT_F32,
     TORCH_DTYPE,
     LIB_PATH,

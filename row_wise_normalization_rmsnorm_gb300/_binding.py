@@ -17,6 +17,8 @@ LIB_PATH = os.path.join(_HERE, "librmsnorm_gb300.so")
 
 RMSNORM_F32, RMSNORM_BF16, RMSNORM_F16 = 0, 1, 2
 RMSNORM_WEIGHT_F32 = 0x100  # OR'ed into a 16-bit type: w and dw are fp32
+RMSNORM_OUT_BF16 = 0x200    # forward of fp32 activations: y in bf16
+RMSNORM_OUT_F16 = 0x400     # ... or in fp16
 STATUS = {0: "SUCCESS", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_WORKSPACE", 4: "ERR_CUDA"}
 PATH_NAMES = {0: "vector", 1: "staged", 2: "generic"}
 OP_FWD, OP_BWD, OP_LN_BWD = 0, 1, 2
@@ -164,6 +166,22 @@ def _param_code(x: torch.Tensor, dt: torch.dtype) -> int:
     return _dtype_code(x) | (RMSNORM_WEIGHT_F32 if dt != x.dtype else 0)
 
 
+def _out_flag(x: torch.Tensor, y: torch.Tensor) -> int:
+    """The forward's output-type flag: 0 when y has x's type; fp32 x may
+    write y in bf16 (RMSNORM_OUT_BF16) or fp16 (RMSNORM_OUT_F16)."""
+    if y.dtype == x.dtype:
+        return 0
+    if x.dtype == torch.float32 and y.dtype in (torch.bfloat16, torch.float16):
+        return RMSNORM_OUT_BF16 if y.dtype == torch.bfloat16 else RMSNORM_OUT_F16
+    raise ValueError(f"y must be {x.dtype} (or, for float32 x, bfloat16 / float16), is {y.dtype}")
+
+
+def _new_y(x: torch.Tensor, y, out_dtype):
+    if y is not None:
+        return y
+    return torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+
+
 def _check_w(w, name: str, x: torch.Tensor, N: int):
     _check(w, name, numel=N)
     if w.device != x.device:
@@ -202,40 +220,42 @@ def _ws(workspace):
     return workspace.data_ptr(), workspace.numel() * workspace.element_size()
 
 
-def rmsnorm_fwd(x, w, *, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=None, stream=None):
+def rmsnorm_fwd(x, w, *, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=None, out_dtype=None, stream=None):
     """y, rstd = RMSNorm(x) over the last dimension (llama mode); w None is
-    non-affine RMSNorm (y = x * rstd)."""
+    non-affine RMSNorm (y = x * rstd). For float32 x, y may be bfloat16 or
+    float16 (``out_dtype``, or a given ``y`` of that type)."""
     M, N = _rows(x)
     _check(x, "x")
     if w is not None:
         _check_w(w, "w", x, N)
-    y = torch.empty_like(x) if y is None else y
+    y = _new_y(x, y, out_dtype)
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
-    _check(y, "y", like=x, numel=x.numel())
+    _check(y, "y", numel=x.numel())
     _check(rstd, "rstd", numel=M)
-    st = lib().rmsnorm_fwd(x.data_ptr(), _ptr(w), y.data_ptr(), rstd.data_ptr(), M, N, _dtype_code_w(x, w),
-                           eps, offset, _stream_handle(stream, x.device))
+    st = lib().rmsnorm_fwd(x.data_ptr(), _ptr(w), y.data_ptr(), rstd.data_ptr(), M, N,
+                           _dtype_code_w(x, w) | _out_flag(x, y), eps, offset, _stream_handle(stream, x.device))
     _raise(st, "rmsnorm_fwd")
     return y, rstd
 
 
 def rmsnorm_add_fwd(x, residual, w, *, eps: float = 1e-6, offset: float = 0.0, y=None, residual_out=None,
-                    rstd=None, stream=None):
-    """h = x + residual (rounded), y = RMSNorm(h); returns y, h, rstd."""
+                    rstd=None, out_dtype=None, stream=None):
+    """h = x + residual (rounded), y = RMSNorm(h); returns y, h, rstd. For
+    float32 x, y may be bfloat16 or float16 (h stays float32)."""
     M, N = _rows(x)
     _check(x, "x")
     _check(residual, "residual", like=x, numel=x.numel())
     if w is not None:
         _check_w(w, "w", x, N)
-    y = torch.empty_like(x) if y is None else y
+    y = _new_y(x, y, out_dtype)
     residual_out = torch.empty_like(x) if residual_out is None else residual_out
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
-    _check(y, "y", like=x, numel=x.numel())
+    _check(y, "y", numel=x.numel())
     _check(residual_out, "residual_out", like=x, numel=x.numel())
     _check(rstd, "rstd", numel=M)
     st = lib().rmsnorm_add_fwd(x.data_ptr(), residual.data_ptr(), _ptr(w), y.data_ptr(),
-                               residual_out.data_ptr(), rstd.data_ptr(), M, N, _dtype_code_w(x, w), eps, offset,
-                               _stream_handle(stream, x.device))
+                               residual_out.data_ptr(), rstd.data_ptr(), M, N, _dtype_code_w(x, w) | _out_flag(x, y),
+                               eps, offset, _stream_handle(stream, x.device))
     _raise(st, "rmsnorm_add_fwd")
     return y, residual_out, rstd
 
@@ -359,17 +379,17 @@ def plan_query(op: int, M: int, N: int, dtype: int, *, aligned: bool = True, num
 
 
 def rmsnorm_fwd_ex(x, w, *, residual=None, eps=1e-6, offset=0.0, y=None, residual_out=None, rstd=None,
-                   force_plan=-1, stream=None):
+                   force_plan=-1, out_dtype=None, stream=None):
     """Forward with a forced plan; returns (y, residual_out or None, rstd, plan dict)."""
     M, N = _rows(x)
-    y = torch.empty_like(x) if y is None else y
+    y = _new_y(x, y, out_dtype)
     if residual is not None and residual_out is None:
         residual_out = torch.empty_like(x)
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
     p = Plan()
     st = lib().rmsnorm_fwd_ex(_ptr(x), _ptr(residual), _ptr(w), _ptr(y), _ptr(residual_out), _ptr(rstd), M, N,
-                              _dtype_code_w(x, w), eps, offset, _stream_handle(stream, x.device), force_plan,
-                              ctypes.byref(p))
+                              _dtype_code_w(x, w) | _out_flag(x, y), eps, offset, _stream_handle(stream, x.device),
+                              force_plan, ctypes.byref(p))
     _raise(st, "rmsnorm_fwd_ex")
     return y, residual_out, rstd, p.as_dict()
 

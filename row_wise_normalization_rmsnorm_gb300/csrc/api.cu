@@ -613,9 +613,12 @@ static std::map<uint64_t, int> g_sfwd_parts;
 
 static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d, bool fused, bool ln, int qmode,
                                     int *parts_out) {
-    if (d.id < 0 || d.id >= kMaxPlanId || qmode < 0 || qmode > 2) return cudaErrorInvalidValue;
-    const uint64_t key = ((((((uint64_t)dev * kNumKinds + kind_of(dt)) * 2 + (fused ? 1 : 0)) * 2 + (ln ? 1 : 0)) * 3 +
-                          (uint64_t)qmode) * kMaxPlanId) + (uint64_t)d.id;
+    if (d.id < 0 || d.id >= kMaxPlanId || qmode < 0 || qmode > QOUT_F16) return cudaErrorInvalidValue;
+    const uint64_t key = ((((((uint64_t)dev * kNumKinds + kind_of(dt)) * 2 + (fused ? 1 : 0)) * 2 + (ln ? 1 : 0)) *
+                               (QOUT_F16 + 1) +
+                           (uint64_t)qmode) *
+                          kMaxPlanId) +
+                         (uint64_t)d.id;
     {
         std::lock_guard<std::mutex> lk(g_occ_mutex);
         auto it = g_sfwd_parts.find(key);
@@ -829,15 +832,28 @@ struct QuantOut {
 };
 
 static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void *w, void *y,
-                                 void *residual_out, float *rstd, int64_t M, int64_t N, int dt, float eps,
+                                 void *residual_out, float *rstd, int64_t M, int64_t N, int dt_arg, float eps,
                                  float offset, cudaStream_t stream, int force_plan, rmsnorm_plan_t *used,
-                                 const QuantOut &q = QuantOut{QOUT_NONE, nullptr, nullptr, nullptr}) {
+                                 const QuantOut &q_arg = QuantOut{QOUT_NONE, nullptr, nullptr, nullptr}) {
     if (!table_ok()) return RMSNORM_ERR_UNSUPPORTED;
+    // fp32 activations with y in bf16 or fp16 (RMSNORM_OUT_BF16 / _F16): the
+    // kernels' narrow output modes, on the E4M3 forward's launch path
+    int dt = dt_arg;
+    QuantOut q = q_arg;
+    const int om = dt & (RMSNORM_OUT_BF16 | RMSNORM_OUT_F16);
+    if (om != 0) {
+        dt &= ~(RMSNORM_OUT_BF16 | RMSNORM_OUT_F16);
+        if (om == (RMSNORM_OUT_BF16 | RMSNORM_OUT_F16) || base_dtype(dt) != RMSNORM_F32)
+            return RMSNORM_ERR_INVALID_ARG;
+        if (q.qmode != QOUT_NONE) return RMSNORM_ERR_UNSUPPORTED;  // E4M3 is an output type of its own
+        q = QuantOut{om == RMSNORM_OUT_BF16 ? QOUT_BF16 : QOUT_F16, nullptr, nullptr, nullptr};
+    }
     if (!valid_dtype(dt)) return RMSNORM_ERR_INVALID_ARG;
     if (N < 1 || N > RMSNORM_MAX_N || M < 0 || M > 0x7fffffffLL) return RMSNORM_ERR_INVALID_ARG;
     if (!finite_scalar(eps) || !finite_scalar(offset) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
+    // quant: y in another type than x (E4M3, or the narrow outputs)
     const bool quant = q.qmode != QOUT_NONE;
-    if (quant) {
+    if (fp8_out(q.qmode)) {
         if (q.qmode == QOUT_FP8_TENSOR && (!q.scale || !aligned_to(q.scale, 4))) return RMSNORM_ERR_INVALID_ARG;
         if (q.qmode == QOUT_FP8_ROW && (q.scale || (M > 0 && !q.scale_inv))) return RMSNORM_ERR_INVALID_ARG;
         if ((q.scale_inv && !aligned_to(q.scale_inv, 4)) || (q.amax && !aligned_to(q.amax, 4)))
@@ -857,14 +873,14 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     if (!x || !y || !rstd) return RMSNORM_ERR_INVALID_ARG;  // w NULL: non-affine
     const uintptr_t s = (uintptr_t)elem_size(dt);
     const uintptr_t ws_ = (uintptr_t)weight_size(dt);
-    const uintptr_t ys = quant ? 1 : s;
+    const uintptr_t ys = fp8_out(q.qmode) ? 1 : (narrow_out(q.qmode) ? 2 : s);
     if (!aligned_to(x, s) || (w && !aligned_to(w, ws_)) || !aligned_to(y, ys) || !aligned_to(rstd, 4))
         return RMSNORM_ERR_INVALID_ARG;
     if (fused && (!aligned_to(residual, s) || !aligned_to(residual_out, s))) return RMSNORM_ERR_INVALID_ARG;
 
     int peel = fused ? row_layout(dt, N, {x, y, residual, residual_out}, w) : row_layout(dt, N, {x, y}, w);
     if (quant) {
-        // E4M3 output (one byte an element): 16-byte aligned rows only
+        // E4M3 or narrow output: 16-byte aligned rows only
         const int in = fused ? row_layout(dt, N, {x, residual, residual_out}, w) : row_layout(dt, N, {x}, w);
         peel = (in == 0 && aligned_to(y, 16)) ? 0 : -1;
     }
@@ -872,7 +888,7 @@ static rmsnorm_status_t fwd_impl(const void *x, const void *residual, const void
     rmsnorm_plan_t plan;
     rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, 1, 0, force_plan, 0, &plan, !quant);
     if (st != RMSNORM_SUCCESS) return st;
-    // the E4M3 kernels are compiled for the default plans and the generic one
+    // the E4M3 and narrow-output kernels are compiled for the default plans and the generic one
     if (quant && force_plan >= 0 && plan.path != PATH_GENERIC && find_plan(plan.plan_id)->cmin == 0)
         return RMSNORM_ERR_UNSUPPORTED;
     if (plan.path == PATH_GENERIC && force_plan < 0) note_generic(NOTE_FWD, N, dt);

@@ -47,6 +47,15 @@ constexpr int fwd_min_blocks() {
     return THREADS >= 1024 || RMSNORM_FWD_OCC * 256 / THREADS < 1 ? 1 : RMSNORM_FWD_OCC * 256 / THREADS;
 }
 
+// A chunk of fp32 y (four values) stored in the narrower output type of Q
+// (bf16 or fp16, rounded to nearest even): 8 bytes at chunk index i of y.
+template <int Q>
+__device__ __forceinline__ void st_narrow_chunk(void *y, int64_t i, const float2 (&a)[2]) {
+    const uint2 u = Q == QOUT_BF16 ? make_uint2(f2_to_bf16x2(a[0]), f2_to_bf16x2(a[1]))
+                                   : make_uint2(f2_to_f16x2(a[0]), f2_to_f16x2(a[1]));
+    reinterpret_cast<uint2 *>(y)[i] = u;
+}
+
 // The row's chunks into registers; with FUSED, h = R(x + residual) is
 // formed in place and stored to residual_out. Chunks past the row are zero.
 // Rows are C chunks apart. Rows at a common offset (p.peel) wrap chunk 0:
@@ -107,17 +116,19 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
 //
 // Q selects the output: QOUT_NONE stores y in T; the E4M3 modes store
 // E4M3(y * s), one byte per element, with s the given per-tensor scale or
-// 448 / max|y| of the row (a second, max-combining row reduction).
+// 448 / max|y| of the row (a second, max-combining row reduction); the
+// narrow modes (fp32 activations) store y in bf16 or fp16, 8 bytes a chunk.
 template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED, int Q = QOUT_NONE>
-__global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? fwd_min_blocks<TPR * TEAMS>()
-                                                               : (1280 / (TPR * TEAMS) > 0 ? 1280 / (TPR * TEAMS) : 1))
+__global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR * TEAMS>()
+                                                          : (1280 / (TPR * TEAMS) > 0 ? 1280 / (TPR * TEAMS) : 1))
     rmsnorm_fwd_vector(const FwdParams p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
+    static_assert(!narrow_out(Q) || std::is_same<T, float>::value, "a narrower output for fp32 activations");
     using Pk = Pair<true>;
     constexpr int NP = Elem<T>::NP;
     constexpr int W = TPR > 32 ? TPR / 32 : 1;
     __shared__ float red[TEAMS][W * CS];
-    __shared__ float redm[Q == QOUT_NONE ? 1 : TEAMS][W * CS];  // the max reduction's slots
+    __shared__ float redm[fp8_out(Q) ? TEAMS : 1][W * CS];  // the max reduction's slots
     // the kernel before it has completed; the next may launch once every
     // CTA of this one has started (no CTA of this grid is then waiting)
     pdl_wait();
@@ -166,7 +177,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? fwd_min_blocks<TP
     const float2 r2 = make_float2(rstd, rstd);
     const float2 o2 = make_float2(p.offset, p.offset);
     const bool has_w = p.w != nullptr;  // no weight: non-affine, factor 1
-    if constexpr (Q == QOUT_NONE) {
+    if constexpr (!fp8_out(Q)) {
         if (!valid) return;
         // the wrapped chunk's weights (the weight shares the rows' offset)
         uint4 wwrap = make_uint4(0, 0, 0, 0);
@@ -194,7 +205,10 @@ __global__ void __launch_bounds__(TPR *TEAMS, Q == QOUT_NONE ? fwd_min_blocks<TP
 #pragma unroll
                     for (int k = 0; k < NP; ++k) a[k] = Pk::mul(a[k], r2);
                 }
-                st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, p.peel, pack<T>(a));
+                if constexpr (narrow_out(Q))
+                    st_narrow_chunk<Q>(p.y, base + c, a);  // (rows on 16-byte boundaries: no peel)
+                else
+                    st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, p.peel, pack<T>(a));
             }
         }
     } else {
@@ -278,7 +292,7 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     const bool vy = addr_mod16(p.y) == a16;
     const bool vr = FUSED && addr_mod16(p.residual) == a16;
     const bool vh = FUSED && addr_mod16(p.residual_out) == a16;
-    const RowSplit sp = row_split(x, N, Q == QOUT_NONE);
+    const RowSplit sp = row_split(x, N, Q == QOUT_NONE);  // (other outputs: element by element)
 
     float ss = 0.f;
     auto h_elem = [&](int j) {
@@ -324,7 +338,11 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
         const float hr = __fmul_rn(h, rstd);
         return w ? __fmul_rn(hr, __fadd_rn(p.offset, load_w(w, j))) : hr;
     };
-    if constexpr (Q == QOUT_NONE) {
+    if constexpr (narrow_out(Q)) {
+        using TO = typename std::conditional<Q == QOUT_BF16, __nv_bfloat16, __half>::type;
+        TO *yo = reinterpret_cast<TO *>(p.y) + row * N;
+        for (int j = threadIdx.x; j < N; j += blockDim.x) store_elem(yo, j, y_at(j));
+    } else if constexpr (Q == QOUT_NONE) {
         for (int j = threadIdx.x; j < sp.head; j += blockDim.x) store_elem(y, j, y_at(j));
         for (int c = threadIdx.x; c < sp.nb; c += blockDim.x) {
             const int64_t j0 = sp.head + (int64_t)c * Elem<T>::E;
@@ -794,14 +812,17 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                 for (int j = 0; j < NP; ++j) a[j] = Pk::mul(a[j], r2);
             }
         };
-        if constexpr (Q == QOUT_NONE) {
+        if constexpr (!fp8_out(Q)) {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 const int cl = v * TPR + t;
                 if (cl < Cs) {
                     float2 a[NP];
                     ychunk(v, a);
-                    st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + rowbase, cbase + cl, C, peel, pack<T>(a));
+                    if constexpr (narrow_out(Q))
+                        st_narrow_chunk<Q>(p.y, rowbase + cbase + cl, a);  // (no peel)
+                    else
+                        st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + rowbase, cbase + cl, C, peel, pack<T>(a));
                 }
             }
         } else {
@@ -1164,20 +1185,33 @@ template <typename T, typename TW = T>
 static int staged_launch_q(int plan_id, bool fused, int mode, const FwdParams &p, int grid, int smem, void *stream) {
     if (mode == QOUT_FP8_TENSOR) return staged_fwd_launch_t<T, TW, false, QOUT_FP8_TENSOR>(plan_id, fused, p, grid, smem, stream);
     if (mode == QOUT_FP8_ROW) return staged_fwd_launch_t<T, TW, false, QOUT_FP8_ROW>(plan_id, fused, p, grid, smem, stream);
+    if constexpr (std::is_same<T, float>::value) {
+        if (mode == QOUT_BF16) return staged_fwd_launch_t<T, TW, false, QOUT_BF16>(plan_id, fused, p, grid, smem, stream);
+        if (mode == QOUT_F16) return staged_fwd_launch_t<T, TW, false, QOUT_F16>(plan_id, fused, p, grid, smem, stream);
+    }
     return (int)cudaErrorInvalidValue;
 }
 template <typename T, typename TW = T>
 static const void *staged_ptr_q(int plan_id, bool fused, int mode) {
     if (mode == QOUT_FP8_TENSOR) return staged_fwd_ptr_t<T, TW, false, QOUT_FP8_TENSOR>(plan_id, fused);
     if (mode == QOUT_FP8_ROW) return staged_fwd_ptr_t<T, TW, false, QOUT_FP8_ROW>(plan_id, fused);
+    if constexpr (std::is_same<T, float>::value) {
+        if (mode == QOUT_BF16) return staged_fwd_ptr_t<T, TW, false, QOUT_BF16>(plan_id, fused);
+        if (mode == QOUT_F16) return staged_fwd_ptr_t<T, TW, false, QOUT_F16>(plan_id, fused);
+    }
     return nullptr;
 }
 
-// E4M3 output: the mode picks the instantiation.
+// E4M3 (and, for fp32 activations, bf16 or fp16) output: the mode picks
+// the instantiation.
 template <typename T, typename TW = T>
 static int launch_q(int plan_id, bool fused, int mode, const FwdParams &p, int grid, void *stream) {
     if (mode == QOUT_FP8_TENSOR) return launch_t<T, TW, QOUT_FP8_TENSOR>(plan_id, fused, p, grid, stream);
     if (mode == QOUT_FP8_ROW) return launch_t<T, TW, QOUT_FP8_ROW>(plan_id, fused, p, grid, stream);
+    if constexpr (std::is_same<T, float>::value) {
+        if (mode == QOUT_BF16) return launch_t<T, TW, QOUT_BF16>(plan_id, fused, p, grid, stream);
+        if (mode == QOUT_F16) return launch_t<T, TW, QOUT_F16>(plan_id, fused, p, grid, stream);
+    }
     return (int)cudaErrorInvalidValue;
 }
 

@@ -250,8 +250,11 @@ struct FwdParams {
 };
 
 // Output of the forward: the activations' type, or E4M3 with a per-tensor
-// scale, or E4M3 with a per-row scale from the row's own max |y|.
-enum { QOUT_NONE = 0, QOUT_FP8_TENSOR = 1, QOUT_FP8_ROW = 2 };
+// scale, or E4M3 with a per-row scale from the row's own max |y|, or (fp32
+// activations) bf16 or fp16: y rounded once from fp32 to the narrower type.
+enum { QOUT_NONE = 0, QOUT_FP8_TENSOR = 1, QOUT_FP8_ROW = 2, QOUT_BF16 = 3, QOUT_F16 = 4 };
+constexpr bool narrow_out(int q) { return q == QOUT_BF16 || q == QOUT_F16; }
+constexpr bool fp8_out(int q) { return q == QOUT_FP8_TENSOR || q == QOUT_FP8_ROW; }
 
 struct BwdParams {
     const void *dy;

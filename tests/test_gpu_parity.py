@@ -569,3 +569,52 @@ def test_fp32_weight_refuses_alternative_plans(rn):
     y, _, _, plan = rn.rmsnorm_fwd_ex(x, w, force_plan=default)
     torch.cuda.synchronize()
     assert plan["plan_id"] == default
+
+
+# ------------------------------------------- fp32 in, bf16 / fp16 out --
+
+@pytest.mark.parametrize("odt", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N", [(333, 64), (257, 1024), (300, 4096), (129, 8192), (65, 16384), (33, 32768),
+                                 (101, 4097), (40, 3)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_fp32_in_narrow_out(rn, odt, M, N, fused):
+    """fp32 activations and weight, y stored in bf16 or fp16 (rounded once
+    from the fp32 result: within 1 ulp of the exact value rounded to the
+    output type); rstd and the fp32 residual_out as for an fp32 forward.
+    Register rows, staged cluster rows (N > 8192) and generic rows."""
+    d = inputs.make_inputs(M, N, "f32", 420 + N % 13, residual=fused)
+    x, w = to_dev(d["x"], "f32"), to_dev(d["w"], "f32")
+    tdt = torch.bfloat16 if odt == "bf16" else torch.float16
+    if fused:
+        y, h, rstd, plan = rn.rmsnorm_fwd_ex(x, w, residual=to_dev(d["residual"], "f32"), out_dtype=tdt)
+    else:
+        y, _, rstd, plan = rn.rmsnorm_fwd_ex(x, w, out_dtype=tdt)
+    f = oracle.fwd(d["x"], d["w"], dtype="f32", eps=1e-6, offset=0.0, residual=d.get("residual") if fused else None)
+    torch.cuda.synchronize()
+    assert y.dtype == tdt
+    ref = {"y": oracle.bf16_round(f["y64"]) if odt == "bf16" else oracle.f16_round(f["y64"])}
+    check_y(to_host(y, odt), ref, odt)
+    check_rstd(rstd.cpu().numpy(), f["rstd64"])
+    if fused:
+        assert np.array_equal(to_host(h, "f32"), f["h"])
+    expect = ("vector", "staged") if N % 4 == 0 else ("generic",)
+    assert plan["path_name"] in expect, plan
+
+
+def test_fp32_in_narrow_out_misaligned_and_refusals(rn):
+    """y one element past an aligned allocation takes the generic kernel;
+    the output flags are refused on 16-bit activations and by the backward."""
+    d = inputs.make_inputs(200, 2048, "f32", 430)
+    x, w = to_dev(d["x"], "f32"), to_dev(d["w"], "f32")
+    y = empty_dev((200, 2048), "bf16", offset=1)
+    _, _, rstd, plan = rn.rmsnorm_fwd_ex(x, w, y=y)
+    f = oracle.fwd(d["x"], d["w"], dtype="f32", eps=1e-6, offset=0.0)
+    torch.cuda.synchronize()
+    assert plan["path_name"] == "generic"
+    check_y(to_host(y, "bf16"), {"y": oracle.bf16_round(f["y64"])}, "bf16")
+    L = rn.lib()
+    xb = to_dev(d["x"], "bf16")
+    assert L.rmsnorm_fwd(xb.data_ptr(), None, xb.data_ptr(), rstd.data_ptr(), 200, 2048,
+                         rn.RMSNORM_BF16 | rn.RMSNORM_OUT_F16, 1e-6, 0.0, None) == 1
+    assert L.rmsnorm_bwd(x.data_ptr(), x.data_ptr(), w.data_ptr(), rstd.data_ptr(), x.data_ptr(), w.data_ptr(),
+                         None, 0, 200, 2048, rn.RMSNORM_F32 | rn.RMSNORM_OUT_BF16, 1e-6, 0.0, None) == 1
