@@ -52,13 +52,15 @@ __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, in
     const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x) + base;
     const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dy) + base;
     const uint4 *r4 = reinterpret_cast<const uint4 *>(p.dres) + base;
+    const bool e0 = p.peel != 0 && cbase + t == 0;  // slot 0 is the row's wrapped chunk
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
         const bool in = c < C;
-        x[v] = in ? ld_row_chunk<T>(x4, c, C, p.peel) : make_uint4(0, 0, 0, 0);
-        d[v] = in ? ld_row_chunk<T>(d4, c, C, p.peel) : make_uint4(0, 0, 0, 0);
-        r[v] = (has_dres && in) ? ld_row_chunk<T>(r4, c, C, p.peel) : make_uint4(0, 0, 0, 0);
+        const bool edge = v == 0 && e0;
+        x[v] = in ? ld_row_chunk<T>(x4, c, C, p.peel, edge) : make_uint4(0, 0, 0, 0);
+        d[v] = in ? ld_row_chunk<T>(d4, c, C, p.peel, edge) : make_uint4(0, 0, 0, 0);
+        r[v] = (has_dres && in) ? ld_row_chunk<T>(r4, c, C, p.peel, edge) : make_uint4(0, 0, 0, 0);
     }
     rs = p.rstd[rr];
     if constexpr (LN) mu = p.mean[rr];
@@ -97,6 +99,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     uint32_t rank = 0;
     if constexpr (CS > 1) rank = cluster_ctarank();
     const int cbase = (int)rank * TPR * V;  // first chunk of this CTA's slice
+    const bool e0 = p.peel != 0 && cbase + t == 0;  // slot 0 is the row's wrapped chunk
 
     // (offset + w) for this thread's columns: loaded once per CTA. Without
     // a weight (non-affine) the factor is 1 and there is no dW.
@@ -119,7 +122,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
         if constexpr (RAWW) {
-            wraw[v] = (has_w && c < C) ? ld_w_raw<T>(p.w, c, C, p.peel) : make_uint4(0, 0, 0, 0);
+            wraw[v] = (has_w && c < C) ? ld_w_raw<T>(p.w, c, C, p.peel, p.peel != 0 && c == 0) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int k = 0; k < NP; ++k) {
                 acc[v][k] = make_float2(0.f, 0.f);
@@ -129,7 +132,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
         }
         float2 wv[NP];
         if (has_w && c < C) {
-            load_w_chunk_row<T, TW>(p.w, c, C, p.peel, wv);
+            load_w_chunk_row<T, TW>(p.w, c, C, p.peel, p.peel != 0 && c == 0, wv);
         } else {
 #pragma unroll
             for (int k = 0; k < NP; ++k) wv[k] = make_float2(0.f, 0.f);
@@ -289,7 +292,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
 #pragma unroll
                 for (int q = 0; q < NP; ++q) out[q] = Pk::add(out[q], rf[q]);
             }
-            if (valid && c < C) st_row_chunk<T>(dx4 + base, c, C, p.peel, pack<T>(out));
+            if (valid && c < C) st_row_chunk<T>(dx4 + base, c, C, p.peel, v == 0 && e0, pack<T>(out));
         }
     };
 
@@ -477,10 +480,11 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     const int peel = p.peel;
     const bool wrap = peel != 0 && cbase == 0;
     const int Cb = Cst + (peel != 0 ? 1 : 0);  // slots of a stage's row buffer
-    // chunk cl of this CTA's slice from a staged row buffer
-    auto staged = [&](const uint4 *buf, int cl) {
-        return wrap && cl == 0 ? wrap_chunk<T>(lds128(buf), lds128(buf + Cst), peel) : lds128(buf + cl);
-    };
+    // chunk cl = v TPR + t of this CTA's slice from a staged row buffer;
+    // only slot v = 0 of thread 0 can be the wrapped chunk (e0), which that
+    // thread wraps in place once a row (wrap_staged) before reading it
+    const bool e0 = wrap && tid == 0;
+    auto staged = [&](const uint4 *buf, int /*v*/, int cl) { return lds128(buf + cl); };
     const int64_t unit = CS > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
     const int64_t G = CS > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
     const int64_t iters = unit < p.M ? (p.M - unit + G - 1) / G : 0;
@@ -515,7 +519,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     uint4 *wsm = stages + (size_t)ns * NB * Cb;
     if constexpr (WSM) {
         if (p.w != nullptr)
-            for (int c = tid; c < Cs; c += TPR) wsm[c] = ld_w_raw<T>(p.w, cbase + c, C, peel);
+            for (int c = tid; c < Cs; c += TPR) wsm[c] = ld_w_raw<T>(p.w, cbase + c, C, peel, wrap && c == 0);
     }
     constexpr uint32_t kSlotBytes = CS * W * sizeof(RT);  // one row's partials from the whole cluster
     if (tid == 0) {
@@ -561,11 +565,11 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         const int cl = v * TPR + t;  // chunk of this CTA's slice; cbase + cl in the row
         if constexpr (WSM || GG) {
         } else if constexpr (RAW) {
-            wraw[v] = (has_w && cl < Cs) ? ld_w_raw<T>(p.w, cbase + cl, C, peel) : make_uint4(0, 0, 0, 0);
+            wraw[v] = (has_w && cl < Cs) ? ld_w_raw<T>(p.w, cbase + cl, C, peel, v == 0 && e0) : make_uint4(0, 0, 0, 0);
         } else {
             float2 wv[NP];
             if (has_w && cl < Cs) {
-                load_w_chunk_row<T, TW>(p.w, cbase + cl, C, peel, wv);
+                load_w_chunk_row<T, TW>(p.w, cbase + cl, C, peel, v == 0 && e0, wv);
             } else {
 #pragma unroll
                 for (int q = 0; q < NP; ++q) wv[q] = make_float2(0.f, 0.f);
@@ -583,7 +587,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         if constexpr (GG) {
             const int cl = v * TPR + t;
             if (has_w && cl < Cs) {
-                load_w_chunk_row<T, TW>(p.w, cbase + cl, C, peel, f);
+                load_w_chunk_row<T, TW>(p.w, cbase + cl, C, peel, v == 0 && e0, f);
             } else {
 #pragma unroll
                 for (int q = 0; q < NP; ++q) f[q] = make_float2(0.f, 0.f);
@@ -621,6 +625,12 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
         const int sk = s;  // this row's stage
         const uint4 *src = stages + (size_t)s * NB * Cb;
+        if (e0) {
+            uint4 *w0 = stages + (size_t)s * NB * Cb;
+            wrap_staged<T>(w0, Cst, peel);
+            wrap_staged<T>(w0 + Cb, Cst, peel);
+            if (has_dres) wrap_staged<T>(w0 + 2 * Cb, Cst, peel);
+        }
         // HOLD: the row's chunks, read once and kept for both passes
         uint4 xv[HOLD ? V : 1], dv[HOLD ? V : 1], rv[FUSED && HOLD ? V : 1];
         if constexpr (HOLD) {
@@ -628,15 +638,15 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
             for (int v = 0; v < V; ++v) {
                 const int cl = v * TPR + t;
                 const bool in = cl < Cs;
-                xv[v] = in ? staged(src, cl) : make_uint4(0, 0, 0, 0);
-                dv[v] = in ? staged(src + Cb, cl) : make_uint4(0, 0, 0, 0);
-                if constexpr (FUSED) rv[v] = (in && has_dres) ? staged(src + 2 * Cb, cl) : make_uint4(0, 0, 0, 0);
+                xv[v] = in ? staged(src, v, cl) : make_uint4(0, 0, 0, 0);
+                dv[v] = in ? staged(src + Cb, v, cl) : make_uint4(0, 0, 0, 0);
+                if constexpr (FUSED) rv[v] = (in && has_dres) ? staged(src + 2 * Cb, v, cl) : make_uint4(0, 0, 0, 0);
             }
         }
         // chunk v of the stage's x (b = 0), dy (1) or dres (2) row
         auto chunk = [&](int b, int v) {
             const int cl = v * TPR + t;
-            return cl < Cs ? staged(src + b * Cb, cl) : make_uint4(0, 0, 0, 0);
+            return cl < Cs ? staged(src + b * Cb, v, cl) : make_uint4(0, 0, 0, 0);
         };
 
         const float2 r2 = make_float2(r, r);
@@ -743,7 +753,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
                     for (int q = 0; q < NP; ++q) out[q] = Pk::add(out[q], rf[q]);
                 }
             }
-            if (cl < Cs) st_row_chunk<T>(dx4 + base, cbase + cl, C, peel, pack<T>(out));
+            if (cl < Cs) st_row_chunk<T>(dx4 + base, cbase + cl, C, peel, v == 0 && e0, pack<T>(out));
         }
         if constexpr (!HOLD) {
             // re-read: the warp is through stage sk; the last warp to say so

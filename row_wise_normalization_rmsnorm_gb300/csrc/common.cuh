@@ -245,24 +245,42 @@ __device__ __forceinline__ void store_part(uint4 *p, uint4 v, bool first, int pe
     }
 }
 
-// Chunk c of the row starting at `row` (C chunks a row): a streaming load,
-// or for a wrapped chunk two loads merged.
+// The helpers below take `edge`: the chunk is the row's wrapped chunk 0
+// (peel != 0 and c == 0). Kernels pass it as `v == 0 && e0`, v the
+// compile-time slot of the chunk among a thread's and e0 whether the
+// thread's slot 0 is chunk 0 of a peeled row, so that the test folds away
+// for every other slot and aligned rows pay one predicate a row, not one
+// branch a chunk.
+
+// The wrapped chunk's two loads and its element stores are kept out of
+// line: only the one thread holding a peeled row's chunk 0 calls them, and
+// inlined the compiler would predicate them into every thread's chunk 0.
 template <typename T>
-__device__ __forceinline__ uint4 ld_row_chunk(const uint4 *row, int c, int C, int peel) {
-    if (peel != 0 && c == 0) return wrap_chunk<T>(ld_stream(row), ld_stream(row + C), peel);
+__device__ __noinline__ uint4 ld_wrapped(const uint4 *row, int C, int peel) {
+    return wrap_chunk<T>(ld_stream(row), ld_stream(row + C), peel);
+}
+template <typename T>
+__device__ __noinline__ void st_wrapped(uint4 *row, int C, int peel, uint4 v) {
+    store_part<T>(row, v, true, peel);
+    store_part<T>(row + C, v, false, peel);
+}
+
+// Chunk c of the row starting at `row` (C chunks a row): a streaming load,
+// or for the wrapped chunk two loads merged.
+template <typename T>
+__device__ __forceinline__ uint4 ld_row_chunk(const uint4 *row, int c, int C, int peel, bool edge) {
+    if (edge) return ld_wrapped<T>(row, C, peel);
     return ld_stream(row + c);
 }
 
-// Store chunk c of the row starting at `row`: whole, or a wrapped chunk's
+// Store chunk c of the row starting at `row`: whole, or the wrapped chunk's
 // two parts element by element.
 template <typename T>
-__device__ __forceinline__ void st_row_chunk(uint4 *row, int c, int C, int peel, const uint4 &v) {
-    if (peel != 0 && c == 0) {
-        store_part<T>(row, v, true, peel);
-        store_part<T>(row + C, v, false, peel);
-    } else {
+__device__ __forceinline__ void st_row_chunk(uint4 *row, int c, int C, int peel, bool edge, const uint4 &v) {
+    if (edge)
+        st_wrapped<T>(row, C, peel, v);
+    else
         row[c] = v;
-    }
 }
 
 // load_w_chunk for chunk c of a row of C chunks (the weight vector shares
@@ -270,19 +288,20 @@ __device__ __forceinline__ void st_row_chunk(uint4 *row, int c, int C, int peel,
 // offset take the weight in the activations' type; the fp32-weight kernels
 // always see peel == 0.
 template <typename T, typename TW>
-__device__ __forceinline__ void load_w_chunk_row(const void *w, int c, int C, int peel, float2 (&wv)[Elem<T>::NP]) {
+__device__ __forceinline__ void load_w_chunk_row(const void *w, int c, int C, int peel, bool edge,
+                                                 float2 (&wv)[Elem<T>::NP]) {
     if constexpr (std::is_same<T, TW>::value) {
         const uint4 *w4 = reinterpret_cast<const uint4 *>(w);
-        unpack<T>(peel != 0 && c == 0 ? wrap_chunk<T>(ld_keep(w4), ld_keep(w4 + C), peel) : ld_keep(w4 + c), wv);
+        unpack<T>(edge ? wrap_chunk<T>(ld_keep(w4), ld_keep(w4 + C), peel) : ld_keep(w4 + c), wv);
     } else {
         load_w_chunk<T, TW>(w, c, wv);
     }
 }
 // The raw 16 bytes of the weight's chunk c (weight in the activations' type).
 template <typename T>
-__device__ __forceinline__ uint4 ld_w_raw(const void *w, int c, int C, int peel) {
+__device__ __forceinline__ uint4 ld_w_raw(const void *w, int c, int C, int peel, bool edge) {
     const uint4 *w4 = reinterpret_cast<const uint4 *>(w);
-    return peel != 0 && c == 0 ? wrap_chunk<T>(ld_keep(w4), ld_keep(w4 + C), peel) : ld_keep(w4 + c);
+    return edge ? wrap_chunk<T>(ld_keep(w4), ld_keep(w4 + C), peel) : ld_keep(w4 + c);
 }
 
 // --------------------------------------------------- peeled generic rows --
@@ -564,6 +583,26 @@ __device__ __forceinline__ uint4 lds128(const void *p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(smem_u32(p)));
     return v;
+}
+
+// 16-byte store into this CTA's shared memory (shared-window address).
+__device__ __forceinline__ void sts128(void *p, const uint4 &v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// A staged row's chunk 0 wrapped in place (rows at a common offset): the
+// row buffer holds aligned chunks 0 .. Cst of its slice, and slot 0 becomes
+// the wrapped chunk from slots 0 and Cst. Called by the thread that alone
+// reads slot 0 (thread 0 of the CTA holding chunk 0), after the stage's
+// copies landed and before it reads the slot. The proxy fence orders the
+// write before the bulk copy that later refills the stage, whichever
+// thread issues it.
+template <typename T>
+__device__ __noinline__ void wrap_staged(uint4 *buf, int Cst, int peel) {
+    sts128(buf, wrap_chunk<T>(lds128(buf), lds128(buf + Cst), peel));
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Bulk copy (the TMA engine's 1-D form) of `bytes` from global memory into

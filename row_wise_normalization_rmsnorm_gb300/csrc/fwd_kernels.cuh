@@ -105,7 +105,8 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
             for (int k = 0; k < NP; ++k) a[k] = Pk::add(a[k], b[k]);
             xv[v] = pack<T>(a);
             const int c = cbase + v * TPR + t;
-            if (valid && c < cend) st_row_chunk<T>(reinterpret_cast<uint4 *>(p.residual_out) + base, c, C, p.peel, xv[v]);
+            if (valid && c < cend)
+                st_row_chunk<T>(reinterpret_cast<uint4 *>(p.residual_out) + base, c, C, p.peel, v == 0 && wrap0, xv[v]);
         }
     }
 }
@@ -179,14 +180,9 @@ __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR *
     const bool has_w = p.w != nullptr;  // no weight: non-affine, factor 1
     if constexpr (!fp8_out(Q)) {
         if (!valid) return;
-        // the wrapped chunk's weights (the weight shares the rows' offset)
-        uint4 wwrap = make_uint4(0, 0, 0, 0);
-        if constexpr (std::is_same<T, TW>::value) {
-            if (has_w && p.peel != 0 && cbase + t == 0) {
-                const uint4 *w4 = reinterpret_cast<const uint4 *>(p.w);
-                wwrap = wrap_chunk<T>(ld_keep(w4), ld_keep(w4 + C), p.peel);
-            }
-        }
+        // slot 0 of this thread is the row's wrapped chunk (the weight
+        // shares the rows' offset)
+        const bool e0 = p.peel != 0 && cbase + t == 0;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = cbase + v * TPR + t;
@@ -195,10 +191,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR *
                 unpack<T>(xv[v], a);
                 if (has_w) {
                     float2 wv[NP];
-                    if (std::is_same<T, TW>::value && p.peel != 0 && c == 0)
-                        unpack<T>(wwrap, wv);
-                    else
-                        load_w_chunk<T, TW>(p.w, c, wv);
+                    load_w_chunk_row<T, TW>(p.w, c, C, p.peel, v == 0 && e0, wv);
 #pragma unroll
                     for (int k = 0; k < NP; ++k) a[k] = Pk::mul(Pk::mul(a[k], r2), Pk::add(o2, wv[k]));
                 } else {
@@ -208,7 +201,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR *
                 if constexpr (narrow_out(Q))
                     st_narrow_chunk<Q>(p.y, base + c, a);  // (rows on 16-byte boundaries: no peel)
                 else
-                    st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, p.peel, pack<T>(a));
+                    st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, p.peel, v == 0 && e0, pack<T>(a));
             }
         }
     } else {
@@ -464,6 +457,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     }
     const float2 r2 = make_float2(rstd, rstd);
     const float2 o2 = make_float2(p.offset, p.offset);
+    const bool e0 = p.peel != 0 && cbase + t == 0;  // slot 0 is the row's wrapped chunk
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
@@ -471,7 +465,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             float2 a[NP], gv[NP], bv[NP];
             unpack<T>(xv[v], a);
             if (p.w) {
-                load_w_chunk_row<T, TW>(p.w, c, C, p.peel, gv);
+                load_w_chunk_row<T, TW>(p.w, c, C, p.peel, v == 0 && e0, gv);
 #pragma unroll
                 for (int k = 0; k < NP; ++k) gv[k] = Pk::add(o2, gv[k]);
             } else {
@@ -479,14 +473,14 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                 for (int k = 0; k < NP; ++k) gv[k] = make_float2(1.f, 1.f);
             }
             if (p.beta) {
-                load_w_chunk_row<T, TW>(p.beta, c, C, p.peel, bv);
+                load_w_chunk_row<T, TW>(p.beta, c, C, p.peel, v == 0 && e0, bv);
             } else {
 #pragma unroll
                 for (int k = 0; k < NP; ++k) bv[k] = make_float2(0.f, 0.f);
             }
 #pragma unroll
             for (int k = 0; k < NP; ++k) a[k] = Pk::fma(Pk::mul(Pk::add(a[k], nmu2), r2), gv[k], bv[k]);
-            st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, p.peel, pack<T>(a));
+            st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, p.peel, v == 0 && e0, pack<T>(a));
         }
     }
 }
@@ -635,9 +629,10 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     const int peel = p.peel;
     const bool wrap = peel != 0 && cbase == 0;
     const int Cb = Cst + (peel != 0 ? 1 : 0);
-    auto staged = [&](const uint4 *buf, int cl) {
-        return wrap && cl == 0 ? wrap_chunk<T>(lds128(buf), lds128(buf + Cst), peel) : lds128(buf + cl);
-    };
+    // (only slot v = 0 of thread 0 can be the wrapped chunk: e0, which
+    // that thread wraps in place once a row before reading it)
+    const bool e0 = wrap && threadIdx.x == 0;
+    auto staged = [&](const uint4 *buf, int /*v*/, int cl) { return lds128(buf + cl); };
     const int64_t unit = CS > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
     const int64_t G = CS > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
     const int64_t iters = unit < p.M ? (p.M - unit + G - 1) / G : 0;
@@ -723,21 +718,27 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
         if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
         const int sk = s;
         const uint4 *src = stages + (size_t)s * NB * Cb;
+        if (e0) {
+            uint4 *w0 = stages + (size_t)s * NB * Cb;
+            wrap_staged<T>(w0, Cst, peel);
+            if constexpr (FUSED) wrap_staged<T>(w0 + Cb, Cst, peel);
+        }
         const int64_t base = row * C + cbase;
         const int64_t rowbase = row * C;
         // h of chunk v of the slice (fused: R(x + r), stored once in pass 1)
         auto hchunk = [&](int v, float2 (&h)[NP], bool store) {
             const int cl = v * TPR + t;
             if (cl < Cs) {
-                unpack<T>(staged(src, cl), h);
+                unpack<T>(staged(src, v, cl), h);
                 if constexpr (FUSED) {
                     float2 rr[NP];
-                    unpack<T>(staged(src + Cb, cl), rr);
+                    unpack<T>(staged(src + Cb, v, cl), rr);
 #pragma unroll
                     for (int j = 0; j < NP; ++j) h[j] = Pk::add(h[j], rr[j]);
                     const uint4 hp = pack<T>(h);
                     if (store)
-                        st_row_chunk<T>(reinterpret_cast<uint4 *>(p.residual_out) + rowbase, cbase + cl, C, peel, hp);
+                        st_row_chunk<T>(reinterpret_cast<uint4 *>(p.residual_out) + rowbase, cbase + cl, C, peel,
+                                        v == 0 && e0, hp);
                     unpack<T>(hp, h);
                 }
             } else {
@@ -787,7 +788,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
             if constexpr (LN) {
                 float2 gv[NP], bv[NP];
                 if (p.w) {
-                    load_w_chunk_row<T, TW>(p.w, c, C, peel, gv);
+                    load_w_chunk_row<T, TW>(p.w, c, C, peel, v == 0 && e0, gv);
 #pragma unroll
                     for (int j = 0; j < NP; ++j) gv[j] = Pk::add(o2, gv[j]);
                 } else {
@@ -795,7 +796,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                     for (int j = 0; j < NP; ++j) gv[j] = make_float2(1.f, 1.f);
                 }
                 if (p.beta) {
-                    load_w_chunk_row<T, TW>(p.beta, c, C, peel, bv);
+                    load_w_chunk_row<T, TW>(p.beta, c, C, peel, v == 0 && e0, bv);
                 } else {
 #pragma unroll
                     for (int j = 0; j < NP; ++j) bv[j] = make_float2(0.f, 0.f);
@@ -804,7 +805,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                 for (int j = 0; j < NP; ++j) a[j] = Pk::fma(Pk::mul(Pk::add(a[j], nmu2), r2), gv[j], bv[j]);
             } else if (p.w) {
                 float2 wv[NP];
-                load_w_chunk_row<T, TW>(p.w, c, C, peel, wv);
+                load_w_chunk_row<T, TW>(p.w, c, C, peel, v == 0 && e0, wv);
 #pragma unroll
                 for (int j = 0; j < NP; ++j) a[j] = Pk::mul(Pk::mul(a[j], r2), Pk::add(o2, wv[j]));
             } else {
@@ -822,7 +823,8 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                     if constexpr (narrow_out(Q))
                         st_narrow_chunk<Q>(p.y, rowbase + cbase + cl, a);  // (no peel)
                     else
-                        st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + rowbase, cbase + cl, C, peel, pack<T>(a));
+                        st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + rowbase, cbase + cl, C, peel, v == 0 && e0,
+                                        pack<T>(a));
                 }
             }
         } else {
