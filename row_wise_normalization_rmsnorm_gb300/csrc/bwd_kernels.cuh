@@ -481,10 +481,17 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     const bool wrap = peel != 0 && cbase == 0;
     const int Cb = Cst + (peel != 0 ? 1 : 0);  // slots of a stage's row buffer
     // chunk cl = v TPR + t of this CTA's slice from a staged row buffer;
-    // only slot v = 0 of thread 0 can be the wrapped chunk (e0), which that
-    // thread wraps in place once a row (wrap_staged) before reading it
+    // only slot v = 0 of thread 0 can be the wrapped chunk (e0). The held
+    // schedule reads a stage once: that thread merges the two parts as it
+    // loads. The re-read schedule reads it twice: that thread wraps the
+    // stage's chunk 0 in place once a row (wrap_staged) before reading it.
     const bool e0 = wrap && tid == 0;
-    auto staged = [&](const uint4 *buf, int /*v*/, int cl) { return lds128(buf + cl); };
+    auto staged = [&](const uint4 *buf, int v, int cl) {
+        if constexpr (HOLD)
+            return v == 0 && e0 ? wrap_chunk<T>(lds128(buf), lds128(buf + Cst), peel) : lds128(buf + cl);
+        else
+            return lds128(buf + cl);
+    };
     const int64_t unit = CS > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
     const int64_t G = CS > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
     const int64_t iters = unit < p.M ? (p.M - unit + G - 1) / G : 0;
@@ -625,12 +632,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
         if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
         const int sk = s;  // this row's stage
         const uint4 *src = stages + (size_t)s * NB * Cb;
-        if (e0) {
-            uint4 *w0 = stages + (size_t)s * NB * Cb;
-            wrap_staged<T>(w0, Cst, peel);
-            wrap_staged<T>(w0 + Cb, Cst, peel);
-            if (has_dres) wrap_staged<T>(w0 + 2 * Cb, Cst, peel);
-        }
+        if (!HOLD && e0) wrap_staged<T>(stages + (size_t)s * NB * Cb, Cb, has_dres ? 3 : 2, Cst, peel);
         // HOLD: the row's chunks, read once and kept for both passes
         uint4 xv[HOLD ? V : 1], dv[HOLD ? V : 1], rv[FUSED && HOLD ? V : 1];
         if constexpr (HOLD) {

@@ -592,16 +592,20 @@ __device__ __forceinline__ void sts128(void *p, const uint4 &v) {
                  : "memory");
 }
 
-// A staged row's chunk 0 wrapped in place (rows at a common offset): the
-// row buffer holds aligned chunks 0 .. Cst of its slice, and slot 0 becomes
-// the wrapped chunk from slots 0 and Cst. Called by the thread that alone
-// reads slot 0 (thread 0 of the CTA holding chunk 0), after the stage's
-// copies landed and before it reads the slot. The proxy fence orders the
-// write before the bulk copy that later refills the stage, whichever
-// thread issues it.
+// A stage's rows' chunk 0 wrapped in place (rows at a common offset, for
+// the kernels that read a stage more than once): each of the `nb` row
+// buffers (`stride` slots apart) holds aligned chunks 0 .. Cst of its
+// slice, and its slot 0 becomes the wrapped chunk from slots 0 and Cst.
+// Called once a row by the thread that alone reads slot 0 (thread 0 of the
+// CTA holding chunk 0), after the stage's copies landed and before it reads
+// the slot. The proxy fence orders the writes before the bulk copy that
+// later refills the stage, whichever thread issues it.
 template <typename T>
-__device__ __noinline__ void wrap_staged(uint4 *buf, int Cst, int peel) {
-    sts128(buf, wrap_chunk<T>(lds128(buf), lds128(buf + Cst), peel));
+__device__ __noinline__ void wrap_staged(uint4 *buf, int stride, int nb, int Cst, int peel) {
+    for (int b = 0; b < nb; ++b) {
+        uint4 *r = buf + b * stride;
+        sts128(r, wrap_chunk<T>(lds128(r), lds128(r + Cst), peel));
+    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 

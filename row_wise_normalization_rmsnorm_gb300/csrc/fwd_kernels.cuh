@@ -718,11 +718,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
         if (!mbar_wait(&full[s], ph, kWaitLimit)) failed = true;
         const int sk = s;
         const uint4 *src = stages + (size_t)s * NB * Cb;
-        if (e0) {
-            uint4 *w0 = stages + (size_t)s * NB * Cb;
-            wrap_staged<T>(w0, Cst, peel);
-            if constexpr (FUSED) wrap_staged<T>(w0 + Cb, Cst, peel);
-        }
+        if (e0) wrap_staged<T>(stages + (size_t)s * NB * Cb, Cb, NB, Cst, peel);
         const int64_t base = row * C + cbase;
         const int64_t rowbase = row * C;
         // h of chunk v of the slice (fused: R(x + r), stored once in pass 1)
