@@ -49,7 +49,10 @@
  *     wherever each array starts, and writes dx element by element. With
  *     an fp32 weight only the default plans are compiled (forcing an
  *     alternative plan id returns UNSUPPORTED) and only aligned rows are
- *     vectorised.
+ *     vectorised. Rows at a common offset run kernels of their own
+ *     (compiled for the default plans only, so that aligned rows pay
+ *     nothing for the wrapped chunk): forcing an alternative plan id on
+ *     them returns UNSUPPORTED as well.
  *   - Every call is asynchronous on `stream` (NULL = legacy default
  *     stream). The library never synchronises and never copies between
  *     host and device.

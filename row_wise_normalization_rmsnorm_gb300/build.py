@@ -27,7 +27,8 @@ HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
 SOURCES = ["api.cu", "fwd_bf16.cu", "fwd_f32.cu", "fwd_f16.cu", "fwd_bf16w32.cu", "fwd_f16w32.cu",
            "fwd8_bf16.cu", "fwd8_f16.cu", "fwd8_f32.cu", "fwd8_bf16w32.cu", "fwd8_f16w32.cu", "ln_bf16.cu", "ln_f16.cu", "ln_f32.cu", "ln_bf16w32.cu", "ln_f16w32.cu",
            "bwd_bf16.cu", "bwd_f32.cu", "bwd_f16.cu", "bwd_bf16w32.cu", "bwd_f16w32.cu",
-           "noalloc.cu"]
+           "fwd_peel_f32.cu", "fwd_peel_bf16.cu", "fwd_peel_f16.cu", "bwd_peel_f32.cu", "bwd_peel_bf16.cu",
+           "bwd_peel_f16.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "plans.h", "fwd_kernels.cuh", "bwd_kernels.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

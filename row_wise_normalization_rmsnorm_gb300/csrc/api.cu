@@ -236,6 +236,8 @@ static rmsnorm_status_t select_plan(int op, int64_t M, int64_t N, int dt, int pe
         if (d->path == PATH_STREAM && (!stream_ok || !stream_fits(*d, N, s))) return RMSNORM_ERR_UNSUPPORTED;
         // with an fp32 weight only the default plans (and the generic one) are compiled
         if (mixed_kind(kind_of(dt)) && row_path(d->path) && d->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
+        // so are the kernels for rows at a common offset
+        if (peel > 0 && row_path(d->path) && d->cmin == 0) return RMSNORM_ERR_UNSUPPORTED;
     } else {
         d = vec_ok ? default_vector_plan(op, dt, C) : nullptr;
         // a staged forward plan that covers the row is preferred
@@ -372,7 +374,18 @@ static cudaError_t device_sms(int *dev_out, int *sms_out) {
     return cudaSuccess;
 }
 
-static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed) {
+// The kernels of a call's type pair. `peel`: the instantiation for rows at a
+// common offset, which exists for the default vectorised plans of the types
+// whose weight is the activations' type (NULL elsewhere).
+static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed, bool peel = false) {
+    if (peel) {
+        switch (kind_of(dt)) {
+        case 0: return bwd_main_kernel_ptr_peel_f32(plan_id, fused, packed);
+        case 1: return bwd_main_kernel_ptr_peel_bf16(plan_id, fused, packed);
+        case 2: return bwd_main_kernel_ptr_peel_f16(plan_id, fused, packed);
+        default: return nullptr;
+        }
+    }
     switch (kind_of(dt)) {
     case 1: return bwd_main_kernel_ptr_bf16(plan_id, fused, packed);
     case 2: return bwd_main_kernel_ptr_f16(plan_id, fused, packed);
@@ -382,7 +395,15 @@ static const void *bwd_kernel(int plan_id, int dt, bool fused, bool packed) {
     }
 }
 
-static const void *ln_bwd_kernel(int plan_id, int dt, bool fused) {
+static const void *ln_bwd_kernel(int plan_id, int dt, bool fused, bool peel = false) {
+    if (peel) {
+        switch (kind_of(dt)) {
+        case 0: return ln_bwd_kernel_ptr_peel_f32(plan_id, fused);
+        case 1: return ln_bwd_kernel_ptr_peel_bf16(plan_id, fused);
+        case 2: return ln_bwd_kernel_ptr_peel_f16(plan_id, fused);
+        default: return nullptr;
+        }
+    }
     switch (kind_of(dt)) {
     case 1: return ln_bwd_kernel_ptr_bf16(plan_id, fused);
     case 2: return ln_bwd_kernel_ptr_f16(plan_id, fused);
@@ -392,7 +413,19 @@ static const void *ln_bwd_kernel(int plan_id, int dt, bool fused) {
     }
 }
 
-static const void *fwd_staged_kernel(int plan_id, int dt, bool fused, bool ln) {
+static const void *fwd_staged_kernel(int plan_id, int dt, bool fused, bool ln, bool peel = false) {
+    if (peel) {
+        switch (kind_of(dt)) {
+        case 0:
+            return ln ? ln_fwd_staged_kernel_ptr_peel_f32(plan_id, fused) : fwd_staged_kernel_ptr_peel_f32(plan_id, fused);
+        case 1:
+            return ln ? ln_fwd_staged_kernel_ptr_peel_bf16(plan_id, fused)
+                      : fwd_staged_kernel_ptr_peel_bf16(plan_id, fused);
+        case 2:
+            return ln ? ln_fwd_staged_kernel_ptr_peel_f16(plan_id, fused) : fwd_staged_kernel_ptr_peel_f16(plan_id, fused);
+        default: return nullptr;
+        }
+    }
     if (ln) {
         switch (kind_of(dt)) {
         case 1: return ln_fwd_staged_kernel_ptr_bf16(plan_id, fused);
@@ -438,8 +471,21 @@ static int launch_fwd8_dt(int dt, int plan_id, bool fused, int mode, const FwdPa
     }
 }
 
+// Launches by type pair; rows at a common offset (p.peel > 0) take the
+// PEEL instantiations.
 static int launch_fwd_staged_dt(int dt, bool ln, int plan_id, bool fused, const FwdParams &p, int grid, int smem,
                                 void *stream) {
+    if (p.peel > 0) {
+        switch (kind_of(dt)) {
+        case 0: return ln ? launch_ln_fwd_staged_peel_f32(plan_id, fused, p, grid, smem, stream)
+                          : launch_fwd_staged_peel_f32(plan_id, fused, p, grid, smem, stream);
+        case 1: return ln ? launch_ln_fwd_staged_peel_bf16(plan_id, fused, p, grid, smem, stream)
+                          : launch_fwd_staged_peel_bf16(plan_id, fused, p, grid, smem, stream);
+        case 2: return ln ? launch_ln_fwd_staged_peel_f16(plan_id, fused, p, grid, smem, stream)
+                          : launch_fwd_staged_peel_f16(plan_id, fused, p, grid, smem, stream);
+        default: return (int)cudaErrorInvalidValue;
+        }
+    }
     if (ln) {
         switch (kind_of(dt)) {
         case 1: return launch_ln_fwd_staged_bf16(plan_id, fused, p, grid, smem, stream);
@@ -459,6 +505,14 @@ static int launch_fwd_staged_dt(int dt, bool ln, int plan_id, bool fused, const 
 }
 
 static int launch_fwd_dt(int dt, int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
+    if (p.peel > 0) {
+        switch (kind_of(dt)) {
+        case 0: return launch_fwd_peel_f32(plan_id, fused, p, grid, stream);
+        case 1: return launch_fwd_peel_bf16(plan_id, fused, p, grid, stream);
+        case 2: return launch_fwd_peel_f16(plan_id, fused, p, grid, stream);
+        default: return (int)cudaErrorInvalidValue;
+        }
+    }
     switch (kind_of(dt)) {
     case 1: return launch_fwd_bf16(plan_id, fused, p, grid, stream);
     case 2: return launch_fwd_f16(plan_id, fused, p, grid, stream);
@@ -470,6 +524,14 @@ static int launch_fwd_dt(int dt, int plan_id, bool fused, const FwdParams &p, in
 
 static int launch_bwd_dt(int dt, int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem,
                          void *stream) {
+    if (p.peel > 0) {
+        switch (kind_of(dt)) {
+        case 0: return launch_bwd_main_peel_f32(plan_id, fused, packed, p, grid, smem, stream);
+        case 1: return launch_bwd_main_peel_bf16(plan_id, fused, packed, p, grid, smem, stream);
+        case 2: return launch_bwd_main_peel_f16(plan_id, fused, packed, p, grid, smem, stream);
+        default: return (int)cudaErrorInvalidValue;
+        }
+    }
     switch (kind_of(dt)) {
     case 1: return launch_bwd_main_bf16(plan_id, fused, packed, p, grid, smem, stream);
     case 2: return launch_bwd_main_f16(plan_id, fused, packed, p, grid, smem, stream);
@@ -491,8 +553,10 @@ static int launch_finalize_dt(int dt, const float *ws, int parts, int ncols, voi
 
 // Largest number of backward dW partial rows worth launching for a plan:
 // resident CTAs on the device (resident clusters for a cluster plan), the
-// minimum over its packed and scalar variants for the given fusion mode, so
-// those two variants use the same count (and dW the same summation order).
+// minimum over its packed and scalar variants, and its instantiations for
+// aligned rows and rows at a common offset, for the given fusion mode, so
+// that all of them use the same count (and dW the same summation order,
+// and the workspace the same size whatever the rows' offset).
 // Cached per device, kernel kind, plan and mode.
 static std::mutex g_occ_mutex;
 static int g_parts_cache[kMaxDevices][kNumKinds][2][kMaxPlanId];
@@ -526,12 +590,18 @@ static cudaError_t bwd_max_parts(int dev, int sms, int dt, const PlanDesc &d, in
                                                   kMaxDynamicSmem)
                          : bwd_smem_bytes(d, nmax);
     int best = 1 << 30;
-    for (int pk = 0; pk < 2; ++pk) {
+    // rows at a common offset: default vectorised plans, weight in the activations' type
+    const bool has_peel = row_path(d.path) && d.cmin > 0 && !mixed_kind(kind_of(dt));
+    for (int var = 0; var < 4; ++var) {
+        const int pk = var & 1;
+        const bool pe = var >= 2;
+        if (pe && !has_peel) continue;
         // the LayerNorm and generic kernels have one variant; a staged plan
         // has the scalar one only where staged_scalar_variant says so
         if ((generic_path(d.path) || d.op == OP_LN_BWD) && pk == 1) continue;
         if (staged_path(d.path) && pk == 0 && !staged_scalar_variant(kind_of(dt), d.cmin)) continue;
-        const void *k = d.op == OP_LN_BWD ? ln_bwd_kernel(d.id, dt, fused) : bwd_kernel(d.id, dt, fused, pk != 0);
+        const void *k =
+            d.op == OP_LN_BWD ? ln_bwd_kernel(d.id, dt, fused, pe) : bwd_kernel(d.id, dt, fused, pk != 0, pe);
         if (!k) return cudaErrorInvalidDeviceFunction;
         if (staged_path(d.path) || d.path == PATH_STREAM) {  // more than 48 KB of dynamic shared memory needs an opt-in
             cudaError_t e = (cudaError_t)allow_staged_smem(k);
@@ -608,17 +678,22 @@ static bool finite_scalar(float v) { return std::isfinite(v); }
 
 // Resident units (CTAs, or clusters) of a staged forward plan on the
 // device, taken at the plan's largest rows (the conservative value) and
-// cached per device, type, fusion mode and RMSNorm/LayerNorm.
+// cached per device, type, fusion mode, RMSNorm/LayerNorm, output mode and
+// row layout (`peel`: the instantiation for rows at a common offset, whose
+// row buffers are one slot longer). The forward keeps no partial rows, so
+// the two layouts may differ in their unit count.
 static std::map<uint64_t, int> g_sfwd_parts;
 
 static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d, bool fused, bool ln, int qmode,
-                                    int *parts_out) {
+                                    bool peel, int *parts_out) {
     if (d.id < 0 || d.id >= kMaxPlanId || qmode < 0 || qmode > QOUT_F16) return cudaErrorInvalidValue;
-    const uint64_t key = ((((((uint64_t)dev * kNumKinds + kind_of(dt)) * 2 + (fused ? 1 : 0)) * 2 + (ln ? 1 : 0)) *
-                               (QOUT_F16 + 1) +
-                           (uint64_t)qmode) *
-                          kMaxPlanId) +
-                         (uint64_t)d.id;
+    if (peel && (qmode != QOUT_NONE || d.path == PATH_STREAM)) return cudaErrorInvalidValue;
+    const uint64_t key =
+        (((((((uint64_t)dev * kNumKinds + kind_of(dt)) * 2 + (fused ? 1 : 0)) * 2 + (ln ? 1 : 0)) * 2 + (peel ? 1 : 0)) *
+              (QOUT_F16 + 1) +
+          (uint64_t)qmode) *
+         kMaxPlanId) +
+        (uint64_t)d.id;
     {
         std::lock_guard<std::mutex> lk(g_occ_mutex);
         auto it = g_sfwd_parts.find(key);
@@ -627,12 +702,13 @@ static cudaError_t staged_fwd_parts(int dev, int sms, int dt, const PlanDesc &d,
             return cudaSuccess;
         }
     }
-    const void *k = qmode != QOUT_NONE ? fwd8_staged_kernel(d.id, dt, fused, qmode) : fwd_staged_kernel(d.id, dt, fused, ln);
+    const void *k = qmode != QOUT_NONE ? fwd8_staged_kernel(d.id, dt, fused, qmode)
+                                       : fwd_staged_kernel(d.id, dt, fused, ln, peel);
     if (!k) return cudaErrorInvalidDeviceFunction;
     cudaError_t e = (cudaError_t)allow_staged_smem(k);
     if (e != cudaSuccess) return e;
     const int64_t sm = d.path == PATH_STREAM ? stream_smem_at(d, (int64_t)d.tpr * d.v, elem_size(dt), fused, d.depth)
-                                             : staged_smem_bytes(d, plan_capacity(d), 1, fused);
+                                             : staged_smem_bytes(d, plan_capacity(d), peel ? 1 : 0, fused);
     const int smem = (int)std::min<int64_t>(sm, kMaxDynamicSmem);
     int n = 0;
     if (d.cs > 1) {
@@ -682,7 +758,7 @@ static rmsnorm_status_t prepare_staged_fwd(int64_t M, int64_t N, int dt, int pee
     cudaError_t e = device_sms(&dev, &sms);
     if (e != cudaSuccess) return cuda_fail(e);
     int parts = 1;
-    e = staged_fwd_parts(dev, sms, dt, *d, fused, ln, qmode, &parts);
+    e = staged_fwd_parts(dev, sms, dt, *d, fused, ln, qmode, pk > 0, &parts);
     if (e != cudaSuccess) return cuda_fail(e);
     rmsnorm_status_t st = select_plan(RMSNORM_OP_FWD, M, N, dt, peel, parts, 0, force_plan, 0, plan, stream);
     if (st != RMSNORM_SUCCESS) return st;
@@ -1177,6 +1253,13 @@ static rmsnorm_status_t ln_fwd_impl(const void *x, const void *residual, const v
     int le;
     if (stages > 0) {
         le = launch_fwd_staged_dt(dt, true, plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream);
+    } else if (p.peel > 0) {
+        switch (kind_of(dt)) {
+        case 0: le = launch_ln_fwd_peel_f32(plan.plan_id, fused, p, plan.ctas, stream); break;
+        case 1: le = launch_ln_fwd_peel_bf16(plan.plan_id, fused, p, plan.ctas, stream); break;
+        case 2: le = launch_ln_fwd_peel_f16(plan.plan_id, fused, p, plan.ctas, stream); break;
+        default: le = (int)cudaErrorInvalidValue; break;
+        }
     } else {
         switch (kind_of(dt)) {
         case 1: le = launch_ln_fwd_bf16(plan.plan_id, fused, p, plan.ctas, stream); break;
@@ -1272,12 +1355,21 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
     p.cache_row = generic_bwd_cache(pd->path, N, (int)s, ws != nullptr, call.cps);
     if (p.cache_row) plan.smem_bytes = (int32_t)(2 * generic_bwd_cache_slot(N, (int)s));
     int le;
-    switch (kind_of(dt)) {
-    case 1: le = launch_ln_bwd_bf16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
-    case 2: le = launch_ln_bwd_f16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
-    case 3: le = launch_ln_bwd_bf16w32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
-    case 4: le = launch_ln_bwd_f16w32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
-    default: le = launch_ln_bwd_f32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+    if (pl > 0) {
+        switch (kind_of(dt)) {
+        case 0: le = launch_ln_bwd_peel_f32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+        case 1: le = launch_ln_bwd_peel_bf16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+        case 2: le = launch_ln_bwd_peel_f16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+        default: le = (int)cudaErrorInvalidValue; break;
+        }
+    } else {
+        switch (kind_of(dt)) {
+        case 1: le = launch_ln_bwd_bf16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+        case 2: le = launch_ln_bwd_f16(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+        case 3: le = launch_ln_bwd_bf16w32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+        case 4: le = launch_ln_bwd_f16w32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+        default: le = launch_ln_bwd_f32(plan.plan_id, fused, p, plan.ctas, plan.smem_bytes, stream); break;
+        }
     }
     // one finalizer over the [units, 2N] partial rows: dgamma | dbeta (a
     // NULL output's half is not written)

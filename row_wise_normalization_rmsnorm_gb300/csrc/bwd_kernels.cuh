@@ -43,7 +43,7 @@ namespace rmsn {
 // past M are clamped to the last row (their results are masked later), so
 // every thread of the CTA keeps taking part in the reductions. Rows at a
 // common offset (p.peel) read their chunk 0 wrapped (ld_row_chunk).
-template <typename T, int TPR, int V, bool LN>
+template <typename T, int TPR, int V, bool LN, bool PEEL>
 __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, int C, int cbase, int t,
                                              bool has_dres, uint4 (&x)[V], uint4 (&d)[V], uint4 (&r)[V],
                                              float &rs, float &mu) {
@@ -52,15 +52,16 @@ __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, in
     const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x) + base;
     const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dy) + base;
     const uint4 *r4 = reinterpret_cast<const uint4 *>(p.dres) + base;
-    const bool e0 = p.peel != 0 && cbase + t == 0;  // slot 0 is the row's wrapped chunk
+    const int peel = peel_of<PEEL>(p);
+    const bool e0 = peel != 0 && cbase + t == 0;  // slot 0 is the row's wrapped chunk
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
         const bool in = c < C;
         const bool edge = v == 0 && e0;
-        x[v] = in ? ld_row_chunk<T>(x4, c, C, p.peel, edge) : make_uint4(0, 0, 0, 0);
-        d[v] = in ? ld_row_chunk<T>(d4, c, C, p.peel, edge) : make_uint4(0, 0, 0, 0);
-        r[v] = (has_dres && in) ? ld_row_chunk<T>(r4, c, C, p.peel, edge) : make_uint4(0, 0, 0, 0);
+        x[v] = in ? ld_row_chunk<T>(x4, c, C, peel, edge) : make_uint4(0, 0, 0, 0);
+        d[v] = in ? ld_row_chunk<T>(d4, c, C, peel, edge) : make_uint4(0, 0, 0, 0);
+        r[v] = (has_dres && in) ? ld_row_chunk<T>(r4, c, C, peel, edge) : make_uint4(0, 0, 0, 0);
     }
     rs = p.rstd[rr];
     if constexpr (LN) mu = p.mean[rr];
@@ -74,7 +75,8 @@ __device__ __forceinline__ void bwd_load_row(const BwdParams &p, int64_t row, in
 // CS > 1: the CTAs of a cluster share each row (CTA rank r holds chunks
 // [r TPR V, (r+1) TPR V)); the row sum meets in distributed shared memory
 // and the cluster, not the CTA, owns one dW partial row.
-template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool FUSED, bool LN>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool FUSED, bool LN,
+          bool PEEL>
 __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
     using Pk = Pair<PACKED>;
@@ -99,7 +101,8 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     uint32_t rank = 0;
     if constexpr (CS > 1) rank = cluster_ctarank();
     const int cbase = (int)rank * TPR * V;  // first chunk of this CTA's slice
-    const bool e0 = p.peel != 0 && cbase + t == 0;  // slot 0 is the row's wrapped chunk
+    const int peel = peel_of<PEEL>(p);
+    const bool e0 = peel != 0 && cbase + t == 0;  // slot 0 is the row's wrapped chunk
 
     // (offset + w) for this thread's columns: loaded once per CTA. Without
     // a weight (non-affine) the factor is 1 and there is no dW.
@@ -122,7 +125,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
         if constexpr (RAWW) {
-            wraw[v] = (has_w && c < C) ? ld_w_raw<T>(p.w, c, C, p.peel, p.peel != 0 && c == 0) : make_uint4(0, 0, 0, 0);
+            wraw[v] = (has_w && c < C) ? ld_w_raw<T>(p.w, c, C, peel, peel != 0 && c == 0) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int k = 0; k < NP; ++k) {
                 acc[v][k] = make_float2(0.f, 0.f);
@@ -132,7 +135,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
         }
         float2 wv[NP];
         if (has_w && c < C) {
-            load_w_chunk_row<T, TW>(p.w, c, C, p.peel, p.peel != 0 && c == 0, wv);
+            load_w_chunk_row<T, TW>(p.w, c, C, peel, peel != 0 && c == 0, wv);
         } else {
 #pragma unroll
             for (int k = 0; k < NP; ++k) wv[k] = make_float2(0.f, 0.f);
@@ -292,7 +295,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
 #pragma unroll
                 for (int q = 0; q < NP; ++q) out[q] = Pk::add(out[q], rf[q]);
             }
-            if (valid && c < C) st_row_chunk<T>(dx4 + base, c, C, p.peel, v == 0 && e0, pack<T>(out));
+            if (valid && c < C) st_row_chunk<T>(dx4 + base, c, C, peel, v == 0 && e0, pack<T>(out));
         }
     };
 
@@ -311,7 +314,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
 #pragma unroll
     for (int s = 0; s < D; ++s)
         if (s < iters)
-            bwd_load_row<T, TPR, V, LN>(p, first + s * G, C, cbase, t, has_dres, xb[s], db[s],
+            bwd_load_row<T, TPR, V, LN, PEEL>(p, first + s * G, C, cbase, t, has_dres, xb[s], db[s],
                                         rb[FUSED ? s : 0], rs[s], mus[s]);
     // every CTA of the cluster runs, with its barriers initialised, before
     // any peer stores into its shared memory
@@ -325,7 +328,7 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
                 // slot (s + D) % B held row k - 1, already done: refill it with row k + D
                 const int sn = (s + D) % B;
                 if (k + D < iters)
-                    bwd_load_row<T, TPR, V, LN>(p, first + (k + D) * G, C, cbase, t, has_dres, xb[sn], db[sn],
+                    bwd_load_row<T, TPR, V, LN, PEEL>(p, first + (k + D) * G, C, cbase, t, has_dres, xb[sn], db[sn],
                                                 rb[FUSED ? sn : 0], rs[sn], mus[sn]);
                 process(xb[s], db[s], rb[FUSED ? s : 0], rs[s], mus[s], k);
                 if (failed) break;
@@ -407,14 +410,15 @@ __device__ __forceinline__ void bwd_vector_body(const BwdParams &p) {
     }
 }
 
-template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool FUSED,
+          bool PEEL = false>
 __global__ void __launch_bounds__(TPR *TEAMS) rmsnorm_bwd_vector(const BwdParams p) {
-    bwd_vector_body<T, TW, TPR, V, TEAMS, D, CS, PACKED, FUSED, false>(p);
+    bwd_vector_body<T, TW, TPR, V, TEAMS, D, CS, PACKED, FUSED, false, PEEL>(p);
 }
 
-template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool FUSED, bool PEEL = false>
 __global__ void __launch_bounds__(TPR *TEAMS) layernorm_bwd_vector(const BwdParams p) {
-    bwd_vector_body<T, TW, TPR, V, TEAMS, D, CS, true, FUSED, true>(p);
+    bwd_vector_body<T, TW, TPR, V, TEAMS, D, CS, true, FUSED, true, PEEL>(p);
 }
 
 // Staged persistent main kernel (bulk-copy pipeline). Each row's x and dy
@@ -437,7 +441,8 @@ __global__ void __launch_bounds__(TPR *TEAMS) layernorm_bwd_vector(const BwdPara
 // ends. Each warp then counts itself done on the stage's counter and the
 // last one to arrive refills the stage; no thread waits for the others. The
 // arithmetic, and so every output bit, is that of HOLD = true.
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool LN, bool HOLD, bool PACKED = true>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool LN, bool HOLD, bool PACKED,
+          bool PEEL>
 __device__ __forceinline__ void staged_body(const BwdParams &p) {
     static_assert(CS == 1 || !HOLD, "cluster rows use the re-read schedule (no CTA barrier orders their refills)");
     using Pk = Pair<PACKED>;
@@ -477,7 +482,7 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     // rows at a common offset: the CTA holding chunk 0 also stages aligned
     // chunk C (after its slice) to wrap chunk 0; a stage's row buffers are
     // one slot longer
-    const int peel = p.peel;
+    const int peel = peel_of<PEEL>(p);
     const bool wrap = peel != 0 && cbase == 0;
     const int Cb = Cst + (peel != 0 ? 1 : 0);  // slots of a stage's row buffer
     // chunk cl = v TPR + t of this CTA's slice from a staged row buffer;
@@ -804,14 +809,15 @@ __device__ __forceinline__ void staged_body(const BwdParams &p) {
     }
 }
 
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool HOLD, bool PACKED = true>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool HOLD, bool PACKED = true,
+          bool PEEL = false>
 __global__ void __launch_bounds__(TPR, 1) rmsnorm_bwd_staged(const BwdParams p) {
-    staged_body<T, TW, TPR, V, S, CS, FUSED, false, HOLD, PACKED>(p);
+    staged_body<T, TW, TPR, V, S, CS, FUSED, false, HOLD, PACKED, PEEL>(p);
 }
 
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool HOLD>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool HOLD, bool PEEL = false>
 __global__ void __launch_bounds__(TPR, 1) layernorm_bwd_staged(const BwdParams p) {
-    staged_body<T, TW, TPR, V, S, CS, FUSED, true, HOLD>(p);
+    staged_body<T, TW, TPR, V, S, CS, FUSED, true, HOLD, true, PEEL>(p);
 }
 
 // Generic main kernel: one 256-thread CTA per row at a time, any N and
@@ -1295,18 +1301,24 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_finalize(const float *ws, int 
 // ------------------------------------------------------------- dispatch --
 
 
-template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PACKED, bool PEEL>
 static int bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     LaunchCfg lc((unsigned)grid, TPR * TEAMS, (size_t)smem, s, CS > 1 ? CS : 0);
-    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, PACKED, true>, p)
-                 : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, PACKED, false>, p);
+    return fused
+               ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, PACKED, true, PEEL>, p)
+               : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, PACKED, false, PEEL>, p);
 }
 
 // A weight type other than the activations' is compiled for the default
-// plans (and the generic one) only; alternatives are for tuning.
-template <typename T, typename TW, int PATH, int CMIN>
+// plans (and the generic one) only; alternatives are for tuning. The PEEL
+// instantiations (rows at a common offset, weight in the activations'
+// type) exist for the default vectorised plans only.
+template <typename T, typename TW, int PATH, int CMIN, bool PEEL = false>
 constexpr bool bwd_instantiated() {
-    return std::is_same<T, TW>::value || generic_path(PATH) || CMIN > 0;
+    if constexpr (PEEL)
+        return std::is_same<T, TW>::value && CMIN > 0 && !generic_path(PATH);
+    else
+        return std::is_same<T, TW>::value || generic_path(PATH) || CMIN > 0;
 }
 
 // Streamed generic kernel: launched as a cluster of one CTA (its bulk
@@ -1326,17 +1338,18 @@ static int bwd_launch_stream(bool fused, const BwdParams &p, int grid, int smem,
 // Staged kernel: launched as a cluster of CS CTAs (of one where a CTA
 // holds the whole row; its bulk copies name a shared::cluster destination)
 // with the stages' dynamic shared memory.
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool HOLD, bool PACKED = true>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool HOLD, bool PACKED, bool PEEL>
 static int bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    const void *k = fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD, PACKED>
-                          : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD, PACKED>;
+    const void *k = fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD, PACKED, PEEL>
+                          : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD, PACKED, PEEL>;
     const int e = allow_staged_smem(k);
     if (e != 0) return e;
     // a cluster of CS CTAs (of one where a CTA holds the whole row: its bulk
     // copies name a shared::cluster destination)
     LaunchCfg lc((unsigned)grid, TPR, (size_t)smem, s, CS);
-    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD, PACKED>, p)
-                 : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD, PACKED>, p);
+    return fused
+               ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD, PACKED, PEEL>, p)
+               : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD, PACKED, PEEL>, p);
 }
 
 // Kernel kind of an (activation, weight) type pair, as the host numbers it:
@@ -1348,9 +1361,9 @@ constexpr int kernel_kind() {
                                           : (std::is_same<T, __nv_bfloat16>::value ? 3 : 4);
 }
 
-template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
+template <typename T, typename TW, bool PEEL, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
 static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    if constexpr (OP != OP_BWD || !bwd_instantiated<T, TW, PATH, CMIN>()) {
+    if constexpr (OP != OP_BWD || !bwd_instantiated<T, TW, PATH, CMIN, PEEL>()) {
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
         LaunchCfg lc((unsigned)grid, 256, 0, s);
@@ -1359,23 +1372,25 @@ static int bwd_launch_entry(bool fused, bool packed, const BwdParams &p, int gri
     } else if constexpr (PATH == PATH_STREAM) {
         return bwd_launch_stream<T, TW, TPR, V, D>(fused, p, grid, smem, s);
     } else if constexpr (PATH == PATH_VECTOR) {
-        return packed ? bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, true>(fused, p, grid, smem, s)
-                      : bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, false>(fused, p, grid, smem, s);
+        return packed ? bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, true, PEEL>(fused, p, grid, smem, s)
+                      : bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, false, PEEL>(fused, p, grid, smem, s);
     } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
         if constexpr (staged_scalar_variant(kernel_kind<T, TW>(), CMIN)) {
-            if (!packed) return bwd_launch_staged<T, TW, TPR, V, D, CS, PATH == PATH_STAGED, false>(fused, p, grid, smem, s);
+            if (!packed)
+                return bwd_launch_staged<T, TW, TPR, V, D, CS, PATH == PATH_STAGED, false, PEEL>(fused, p, grid, smem,
+                                                                                                 s);
         } else if (!packed) {
             return (int)cudaErrorInvalidValue;
         }
-        return bwd_launch_staged<T, TW, TPR, V, D, CS, PATH == PATH_STAGED>(fused, p, grid, smem, s);
+        return bwd_launch_staged<T, TW, TPR, V, D, CS, PATH == PATH_STAGED, true, PEEL>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
 }
 
-template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
+template <typename T, typename TW, bool PEEL, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
 static const void *bwd_ptr_entry(bool fused, bool packed) {
-    if constexpr (OP != OP_BWD || !bwd_instantiated<T, TW, PATH, CMIN>()) {
+    if constexpr (OP != OP_BWD || !bwd_instantiated<T, TW, PATH, CMIN, PEEL>()) {
         return nullptr;
     } else if constexpr (PATH == PATH_GENERIC) {
         return fused ? (const void *)rmsnorm_bwd_generic<T, TW, true> : (const void *)rmsnorm_bwd_generic<T, TW, false>;
@@ -1384,34 +1399,35 @@ static const void *bwd_ptr_entry(bool fused, bool packed) {
                      : (const void *)rmsnorm_bwd_stream<T, TW, TPR, V, D, false>;
     } else if constexpr (PATH == PATH_VECTOR) {
         if (packed)
-            return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, true>
-                         : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, false>;
-        return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, true>
-                     : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, false>;
+            return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, true, PEEL>
+                         : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, false, PEEL>;
+        return fused ? (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, true, PEEL>
+                     : (const void *)rmsnorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, false, PEEL>;
     } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
+        constexpr bool HOLD = PATH == PATH_STAGED;
         // the scalar variant where it is compiled (nullptr where it is not)
         if constexpr (staged_scalar_variant(kernel_kind<T, TW>(), CMIN)) {
             if (!packed)
-                return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, true, PATH == PATH_STAGED, false>
-                             : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, false, PATH == PATH_STAGED, false>;
+                return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, true, HOLD, false, PEEL>
+                             : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, false, HOLD, false, PEEL>;
         } else if (!packed) {
             return nullptr;
         }
-        return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, true, PATH == PATH_STAGED>
-                     : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, false, PATH == PATH_STAGED>;
+        return fused ? (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, true, HOLD, true, PEEL>
+                     : (const void *)rmsnorm_bwd_staged<T, TW, TPR, V, D, CS, false, HOLD, true, PEEL>;
     } else {
         return nullptr;
     }
 }
 
-template <typename T, typename TW>
+template <typename T, typename TW, bool PEEL = false>
 static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem,
                         void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (plan_id) {
 #define RMSN_BWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
     case id:                                                                    \
-        return bwd_launch_entry<T, TW, op, path, tpr, v, teams, depth, cs, cmin>(fused, packed, p, grid, smem, s);
+        return bwd_launch_entry<T, TW, PEEL, op, path, tpr, v, teams, depth, cs, cmin>(fused, packed, p, grid, smem, s);
         RMSNORM_PLAN_TABLE(RMSN_BWD_CASE)
 #undef RMSN_BWD_CASE
     default:
@@ -1419,11 +1435,11 @@ static int bwd_launch_t(int plan_id, bool fused, bool packed, const BwdParams &p
     }
 }
 
-template <typename T, typename TW>
+template <typename T, typename TW, bool PEEL = false>
 static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
     switch (plan_id) {
 #define RMSN_BWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return bwd_ptr_entry<T, TW, op, path, tpr, v, teams, depth, cs, cmin>(fused, packed);
+    case id: return bwd_ptr_entry<T, TW, PEEL, op, path, tpr, v, teams, depth, cs, cmin>(fused, packed);
         RMSNORM_PLAN_TABLE(RMSN_BWD_PTR)
 #undef RMSN_BWD_PTR
     default:
@@ -1452,29 +1468,38 @@ static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *
 
 // ------------------------------------------------- LayerNorm dispatch --
 
-template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int D, int CS, bool PEEL>
 static int ln_bwd_launch_vec(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
     LaunchCfg lc((unsigned)grid, TPR * TEAMS, (size_t)smem, s, CS > 1 ? CS : 0);
-    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true>, p)
-                 : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false>, p);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, PEEL>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, PEEL>, p);
 }
 
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool HOLD>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool HOLD, bool PEEL>
 static int ln_bwd_launch_staged(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    const void *k = fused ? (const void *)layernorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD>
-                          : (const void *)layernorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD>;
+    const void *k = fused ? (const void *)layernorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD, PEEL>
+                          : (const void *)layernorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD, PEEL>;
     const int e = allow_staged_smem(k);
     if (e != 0) return e;
     LaunchCfg lc((unsigned)grid, TPR, (size_t)smem, s, CS);
-    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD>, p)
-                 : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD>, p);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_staged<T, TW, TPR, V, S, CS, true, HOLD, PEEL>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_staged<T, TW, TPR, V, S, CS, false, HOLD, PEEL>, p);
 }
 
 // An fp32 gamma beside 16-bit activations is compiled for the default
-// plans and the generic one only.
-template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
+// plans and the generic one only; the PEEL instantiations for the default
+// vectorised plans with gamma in the activations' type.
+template <typename T, typename TW, int PATH, int CMIN, bool PEEL>
+constexpr bool ln_bwd_instantiated() {
+    if constexpr (PEEL)
+        return std::is_same<T, TW>::value && CMIN > 0 && !generic_path(PATH);
+    else
+        return std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0;
+}
+
+template <typename T, typename TW, bool PEEL, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
 static int ln_bwd_launch_entry(bool fused, const BwdParams &p, int grid, int smem, cudaStream_t s) {
-    if constexpr (OP != OP_LN_BWD || !(std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0)) {
+    if constexpr (OP != OP_LN_BWD || !ln_bwd_instantiated<T, TW, PATH, CMIN, PEEL>()) {
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
         const int gs = generic_bwd_smem<T>(p);
@@ -1485,39 +1510,40 @@ static int ln_bwd_launch_entry(bool fused, const BwdParams &p, int grid, int sme
         return gs ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, TW, false, true>, p)
                   : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_bwd_generic<T, TW, false, false>, p);
     } else if constexpr (PATH == PATH_VECTOR) {
-        return ln_bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS>(fused, p, grid, smem, s);
+        return ln_bwd_launch_vec<T, TW, TPR, V, TEAMS, D, CS, PEEL>(fused, p, grid, smem, s);
     } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
-        return ln_bwd_launch_staged<T, TW, TPR, V, D, CS, PATH == PATH_STAGED>(fused, p, grid, smem, s);
+        return ln_bwd_launch_staged<T, TW, TPR, V, D, CS, PATH == PATH_STAGED, PEEL>(fused, p, grid, smem, s);
     } else {
         return (int)cudaErrorInvalidValue;
     }
 }
 
-template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
+template <typename T, typename TW, bool PEEL, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS, int CMIN>
 static const void *ln_bwd_ptr_entry(bool fused) {
-    if constexpr (OP != OP_LN_BWD || !(std::is_same<T, TW>::value || PATH == PATH_GENERIC || CMIN > 0)) {
+    if constexpr (OP != OP_LN_BWD || !ln_bwd_instantiated<T, TW, PATH, CMIN, PEEL>()) {
         return nullptr;
     } else if constexpr (PATH == PATH_GENERIC) {
         return fused ? (const void *)layernorm_bwd_generic<T, TW, true, false>
                      : (const void *)layernorm_bwd_generic<T, TW, false, false>;
     } else if constexpr (PATH == PATH_VECTOR) {
-        return fused ? (const void *)layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true>
-                     : (const void *)layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false>;
+        return fused ? (const void *)layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, true, PEEL>
+                     : (const void *)layernorm_bwd_vector<T, TW, TPR, V, TEAMS, D, CS, false, PEEL>;
     } else if constexpr (staged_plan(PATH, TEAMS, CS)) {
-        return fused ? (const void *)layernorm_bwd_staged<T, TW, TPR, V, D, CS, true, PATH == PATH_STAGED>
-                     : (const void *)layernorm_bwd_staged<T, TW, TPR, V, D, CS, false, PATH == PATH_STAGED>;
+        return fused ? (const void *)layernorm_bwd_staged<T, TW, TPR, V, D, CS, true, PATH == PATH_STAGED, PEEL>
+                     : (const void *)layernorm_bwd_staged<T, TW, TPR, V, D, CS, false, PATH == PATH_STAGED, PEEL>;
     } else {
         return nullptr;
     }
 }
 
 // (TW: gamma's type, the activations' or fp32)
-template <typename T, typename TW = T>
+template <typename T, typename TW = T, bool PEEL = false>
 static int ln_bwd_launch_t(int plan_id, bool fused, const BwdParams &p, int grid, int smem, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (plan_id) {
 #define RMSN_LN_BWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return ln_bwd_launch_entry<T, TW, op, path, tpr, v, teams, depth, cs, cmin>(fused, p, grid, smem, s);
+    case id:                                                                       \
+        return ln_bwd_launch_entry<T, TW, PEEL, op, path, tpr, v, teams, depth, cs, cmin>(fused, p, grid, smem, s);
         RMSNORM_PLAN_TABLE(RMSN_LN_BWD_CASE)
 #undef RMSN_LN_BWD_CASE
     default:
@@ -1525,11 +1551,11 @@ static int ln_bwd_launch_t(int plan_id, bool fused, const BwdParams &p, int grid
     }
 }
 
-template <typename T, typename TW = T>
+template <typename T, typename TW = T, bool PEEL = false>
 static const void *ln_bwd_ptr_t(int plan_id, bool fused) {
     switch (plan_id) {
 #define RMSN_LN_BWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return ln_bwd_ptr_entry<T, TW, op, path, tpr, v, teams, depth, cs, cmin>(fused);
+    case id: return ln_bwd_ptr_entry<T, TW, PEEL, op, path, tpr, v, teams, depth, cs, cmin>(fused);
         RMSNORM_PLAN_TABLE(RMSN_LN_BWD_PTR)
 #undef RMSN_LN_BWD_PTR
     default:

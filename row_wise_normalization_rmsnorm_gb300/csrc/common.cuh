@@ -245,12 +245,21 @@ __device__ __forceinline__ void store_part(uint4 *p, uint4 v, bool first, int pe
     }
 }
 
+// The rows' common offset as a vectorised kernel sees it. Each such kernel
+// is compiled twice: PEEL = false serves aligned rows, and there the offset
+// is the constant 0, so every wrapped-chunk test, load, merge and store
+// below folds away and the kernel is the plain aligned one (registers and
+// instructions included); PEEL = true reads it from the parameters.
+template <bool PEEL, typename Params>
+__device__ __forceinline__ int peel_of(const Params &p) {
+    return PEEL ? p.peel : 0;
+}
+
 // The helpers below take `edge`: the chunk is the row's wrapped chunk 0
 // (peel != 0 and c == 0). Kernels pass it as `v == 0 && e0`, v the
 // compile-time slot of the chunk among a thread's and e0 whether the
 // thread's slot 0 is chunk 0 of a peeled row, so that the test folds away
-// for every other slot and aligned rows pay one predicate a row, not one
-// branch a chunk.
+// for every other slot.
 
 // The wrapped chunk's two loads and its element stores are kept out of
 // line: only the one thread holding a peeled row's chunk 0 calls them, and

@@ -63,13 +63,14 @@ __device__ __forceinline__ void st_narrow_chunk(void *y, int64_t i, const float2
 // loads the second aligned block beside its other loads and merges the two
 // once every load is in flight, so no warp waits on a load before issuing
 // the rest.
-template <typename T, int TPR, int V, bool FUSED>
+template <typename T, int TPR, int V, bool FUSED, bool PEEL>
 __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, int C, int cbase, int t, int cend,
                                              bool valid, uint4 (&xv)[V]) {
     using Pk = Pair<true>;
     constexpr int NP = Elem<T>::NP;
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    const bool wrap0 = p.peel != 0 && cbase + t == 0;
+    const int peel = peel_of<PEEL>(p);
+    const bool wrap0 = peel != 0 && cbase + t == 0;
     const uint4 *x4 = reinterpret_cast<const uint4 *>(p.x) + base;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -78,7 +79,7 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
     }
     const uint4 xt = wrap0 ? ld_stream(x4 + C) : zero;
     if constexpr (!FUSED) {
-        if (wrap0) xv[0] = wrap_chunk<T>(xv[0], xt, p.peel);
+        if (wrap0) xv[0] = wrap_chunk<T>(xv[0], xt, peel);
     } else {
         // h = R(x + residual). For bf16 inputs the fp32 sum is exact unless
         // the exponents differ by more than 15, and then both it and the
@@ -93,8 +94,8 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
         }
         const uint4 rt = wrap0 ? ld_stream(r4 + C) : zero;
         if (wrap0) {
-            xv[0] = wrap_chunk<T>(xv[0], xt, p.peel);
-            rv[0] = wrap_chunk<T>(rv[0], rt, p.peel);
+            xv[0] = wrap_chunk<T>(xv[0], xt, peel);
+            rv[0] = wrap_chunk<T>(rv[0], rt, peel);
         }
 #pragma unroll
         for (int v = 0; v < V; ++v) {
@@ -106,7 +107,7 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
             xv[v] = pack<T>(a);
             const int c = cbase + v * TPR + t;
             if (valid && c < cend)
-                st_row_chunk<T>(reinterpret_cast<uint4 *>(p.residual_out) + base, c, C, p.peel, v == 0 && wrap0, xv[v]);
+                st_row_chunk<T>(reinterpret_cast<uint4 *>(p.residual_out) + base, c, C, peel, v == 0 && wrap0, xv[v]);
         }
     }
 }
@@ -119,7 +120,7 @@ __device__ __forceinline__ void fwd_load_row(const FwdParams &p, int64_t base, i
 // E4M3(y * s), one byte per element, with s the given per-tensor scale or
 // 448 / max|y| of the row (a second, max-combining row reduction); the
 // narrow modes (fp32 activations) store y in bf16 or fp16, 8 bytes a chunk.
-template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED, int Q = QOUT_NONE>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED, int Q = QOUT_NONE, bool PEEL = false>
 __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR * TEAMS>()
                                                           : (1280 / (TPR * TEAMS) > 0 ? 1280 / (TPR * TEAMS) : 1))
     rmsnorm_fwd_vector(const FwdParams p) {
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR *
     const int cend = cbase + cslice < C ? cbase + cslice : C;
 
     uint4 xv[V];
-    fwd_load_row<T, TPR, V, FUSED>(p, base, C, cbase, t, cend, valid, xv);
+    fwd_load_row<T, TPR, V, FUSED, PEEL>(p, base, C, cbase, t, cend, valid, xv);
 
     float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
@@ -182,7 +183,8 @@ __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR *
         if (!valid) return;
         // slot 0 of this thread is the row's wrapped chunk (the weight
         // shares the rows' offset)
-        const bool e0 = p.peel != 0 && cbase + t == 0;
+        const int peel = peel_of<PEEL>(p);
+        const bool e0 = peel != 0 && cbase + t == 0;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = cbase + v * TPR + t;
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR *
                 unpack<T>(xv[v], a);
                 if (has_w) {
                     float2 wv[NP];
-                    load_w_chunk_row<T, TW>(p.w, c, C, p.peel, v == 0 && e0, wv);
+                    load_w_chunk_row<T, TW>(p.w, c, C, peel, v == 0 && e0, wv);
 #pragma unroll
                     for (int k = 0; k < NP; ++k) a[k] = Pk::mul(Pk::mul(a[k], r2), Pk::add(o2, wv[k]));
                 } else {
@@ -201,7 +203,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR *
                 if constexpr (narrow_out(Q))
                     st_narrow_chunk<Q>(p.y, base + c, a);  // (rows on 16-byte boundaries: no peel)
                 else
-                    st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, p.peel, v == 0 && e0, pack<T>(a));
+                    st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, peel, v == 0 && e0, pack<T>(a));
             }
         }
     } else {
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
 // sum of squared deviations from it (a two-pass variance, which loses
 // nothing to cancellation when the mean is large), then
 // y = (h - mean) rstd (offset + gamma) + beta, rounded once.
-template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED, bool PEEL = false>
 __global__ void __launch_bounds__(TPR *TEAMS)
     layernorm_fwd_vector(const FwdParams p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
@@ -411,7 +413,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     const int cend = cbase + cslice < C ? cbase + cslice : C;
 
     uint4 xv[V];
-    fwd_load_row<T, TPR, V, FUSED>(p, base, C, cbase, t, cend, valid, xv);
+    fwd_load_row<T, TPR, V, FUSED, PEEL>(p, base, C, cbase, t, cend, valid, xv);
 
     float2 sm = make_float2(0.f, 0.f);
 #pragma unroll
@@ -457,7 +459,8 @@ __global__ void __launch_bounds__(TPR *TEAMS)
     }
     const float2 r2 = make_float2(rstd, rstd);
     const float2 o2 = make_float2(p.offset, p.offset);
-    const bool e0 = p.peel != 0 && cbase + t == 0;  // slot 0 is the row's wrapped chunk
+    const int peel = peel_of<PEEL>(p);
+    const bool e0 = peel != 0 && cbase + t == 0;  // slot 0 is the row's wrapped chunk
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = cbase + v * TPR + t;
@@ -465,7 +468,7 @@ __global__ void __launch_bounds__(TPR *TEAMS)
             float2 a[NP], gv[NP], bv[NP];
             unpack<T>(xv[v], a);
             if (p.w) {
-                load_w_chunk_row<T, TW>(p.w, c, C, p.peel, v == 0 && e0, gv);
+                load_w_chunk_row<T, TW>(p.w, c, C, peel, v == 0 && e0, gv);
 #pragma unroll
                 for (int k = 0; k < NP; ++k) gv[k] = Pk::add(o2, gv[k]);
             } else {
@@ -473,14 +476,14 @@ __global__ void __launch_bounds__(TPR *TEAMS)
                 for (int k = 0; k < NP; ++k) gv[k] = make_float2(1.f, 1.f);
             }
             if (p.beta) {
-                load_w_chunk_row<T, TW>(p.beta, c, C, p.peel, v == 0 && e0, bv);
+                load_w_chunk_row<T, TW>(p.beta, c, C, peel, v == 0 && e0, bv);
             } else {
 #pragma unroll
                 for (int k = 0; k < NP; ++k) bv[k] = make_float2(0.f, 0.f);
             }
 #pragma unroll
             for (int k = 0; k < NP; ++k) a[k] = Pk::fma(Pk::mul(Pk::add(a[k], nmu2), r2), gv[k], bv[k]);
-            st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, p.peel, v == 0 && e0, pack<T>(a));
+            st_row_chunk<T>(reinterpret_cast<uint4 *>(p.y) + base, c, C, peel, v == 0 && e0, pack<T>(a));
         }
     }
 }
@@ -599,7 +602,7 @@ __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) 
 // reduction tree are the register forward's, so y and rstd are the same
 // bits. Every wait is bounded; one that gives up writes the status word and
 // the kernel carries on.
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool LN, int Q = QOUT_NONE>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool LN, int Q, bool PEEL>
 __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     static_assert(Q == QOUT_NONE || !LN, "E4M3 output: RMSNorm only");
     using Pk = Pair<true>;
@@ -626,7 +629,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     const int Cs = C - cbase <= 0 ? 0 : (C - cbase < Cst ? C - cbase : Cst);
     // rows at a common offset: the CTA holding chunk 0 also stages aligned
     // chunk C (after its slice) to wrap chunk 0; row buffers are one slot longer
-    const int peel = p.peel;
+    const int peel = peel_of<PEEL>(p);
     const bool wrap = peel != 0 && cbase == 0;
     const int Cb = Cst + (peel != 0 ? 1 : 0);
     // (only slot v = 0 of thread 0 can be the wrapped chunk: e0, which
@@ -890,14 +893,14 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     if constexpr (CS > 1) cluster_sync();
 }
 
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, int Q = QOUT_NONE>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, int Q = QOUT_NONE, bool PEEL = false>
 __global__ void __launch_bounds__(TPR, 1) rmsnorm_fwd_staged(const FwdParams p) {
-    staged_fwd_body<T, TW, TPR, V, S, CS, FUSED, false, Q>(p);
+    staged_fwd_body<T, TW, TPR, V, S, CS, FUSED, false, Q, PEEL>(p);
 }
 
-template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED>
+template <typename T, typename TW, int TPR, int V, int S, int CS, bool FUSED, bool PEEL = false>
 __global__ void __launch_bounds__(TPR, 1) layernorm_fwd_staged(const FwdParams p) {
-    staged_fwd_body<T, TW, TPR, V, S, CS, FUSED, true>(p);
+    staged_fwd_body<T, TW, TPR, V, S, CS, FUSED, true, QOUT_NONE, PEEL>(p);
 }
 
 // Streamed generic forward: persistent CTAs, rows of any alignment and of
@@ -1035,17 +1038,17 @@ static int launch_fwd_staged_kernel(const void *k, int cs, int threads, const Fw
 
 // ------------------------------------------------------------- dispatch --
 
-template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, int Q>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, int Q, bool PEEL>
 static int launch_vec(bool fused, const FwdParams &p, int grid, void *stream) {
     LaunchCfg lc((unsigned)grid, TPR * TEAMS, 0, static_cast<cudaStream_t>(stream), CS > 1 ? CS : 0);
-    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true, Q>, p)
-                 : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false, Q>, p);
+    return fused ? (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true, Q, PEEL>, p)
+                 : (int)cudaLaunchKernelEx(&lc.cfg, rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false, Q, PEEL>, p);
 }
 
-template <typename T, typename TW, int TPR, int V, int TEAMS, int CS>
+template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool PEEL>
 static const void *ptr_vec(bool fused) {
-    return fused ? (const void *)rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true>
-                 : (const void *)rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false>;
+    return fused ? (const void *)rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true, QOUT_NONE, PEEL>
+                 : (const void *)rmsnorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false, QOUT_NONE, PEEL>;
 }
 
 // The generic LayerNorm forward's row cache: N elements and 16 bytes of
@@ -1069,35 +1072,39 @@ static const void *ptr_gen(bool fused) {
 
 // A weight type other than the activations', and the E4M3 outputs, are
 // compiled for the default plans (and the generic one) only; alternatives
-// are for tuning.
-template <typename T, typename TW, int PATH, int CMIN, int Q>
+// are for tuning. The PEEL instantiations (rows at a common offset, which
+// take neither) exist for the default vectorised plans only.
+template <typename T, typename TW, int PATH, int CMIN, int Q, bool PEEL = false>
 constexpr bool instantiated() {
-    return (std::is_same<T, TW>::value && Q == QOUT_NONE) || PATH == PATH_GENERIC || CMIN > 0;
+    if constexpr (PEEL)
+        return std::is_same<T, TW>::value && Q == QOUT_NONE && CMIN > 0 && !generic_path(PATH);
+    else
+        return (std::is_same<T, TW>::value && Q == QOUT_NONE) || PATH == PATH_GENERIC || CMIN > 0;
 }
 
 // One switch case per table entry; `if constexpr` keeps kernels of other
 // ops, paths, weight types and outputs from being instantiated here.
-template <typename T, typename TW, int Q, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
+template <typename T, typename TW, int Q, bool PEEL, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
 static int launch_entry(bool fused, const FwdParams &p, int grid, void *stream) {
-    if constexpr (OP != OP_FWD || !instantiated<T, TW, PATH, CMIN, Q>()) return (int)cudaErrorInvalidValue;
+    if constexpr (OP != OP_FWD || !instantiated<T, TW, PATH, CMIN, Q, PEEL>()) return (int)cudaErrorInvalidValue;
     else if constexpr (PATH == PATH_GENERIC) return launch_gen<T, TW, Q>(fused, p, grid, stream);
-    else if constexpr (PATH == PATH_VECTOR) return launch_vec<T, TW, TPR, V, TEAMS, CS, Q>(fused, p, grid, stream);
+    else if constexpr (PATH == PATH_VECTOR) return launch_vec<T, TW, TPR, V, TEAMS, CS, Q, PEEL>(fused, p, grid, stream);
     else return (int)cudaErrorInvalidValue;
 }
 
-template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
+template <typename T, typename TW, bool PEEL, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
 static const void *ptr_entry(bool fused) {
-    if constexpr (OP != OP_FWD || !instantiated<T, TW, PATH, CMIN, QOUT_NONE>()) return nullptr;
+    if constexpr (OP != OP_FWD || !instantiated<T, TW, PATH, CMIN, QOUT_NONE, PEEL>()) return nullptr;
     else if constexpr (PATH == PATH_GENERIC) return ptr_gen<T, TW>(fused);
-    else if constexpr (PATH == PATH_VECTOR) return ptr_vec<T, TW, TPR, V, TEAMS, CS>(fused);
+    else if constexpr (PATH == PATH_VECTOR) return ptr_vec<T, TW, TPR, V, TEAMS, CS, PEEL>(fused);
     else return nullptr;
 }
 
-template <typename T, typename TW, int Q = QOUT_NONE>
+template <typename T, typename TW, int Q = QOUT_NONE, bool PEEL = false>
 static int launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
     switch (plan_id) {
 #define RMSN_FWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return launch_entry<T, TW, Q, op, path, tpr, v, teams, cs, cmin>(fused, p, grid, stream);
+    case id: return launch_entry<T, TW, Q, PEEL, op, path, tpr, v, teams, cs, cmin>(fused, p, grid, stream);
         RMSNORM_PLAN_TABLE(RMSN_FWD_CASE)
 #undef RMSN_FWD_CASE
     default:
@@ -1105,11 +1112,11 @@ static int launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void 
     }
 }
 
-template <typename T, typename TW>
+template <typename T, typename TW, bool PEEL = false>
 static const void *ptr_t(int plan_id, bool fused) {
     switch (plan_id) {
 #define RMSN_FWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return ptr_entry<T, TW, op, path, tpr, v, teams, cs, cmin>(fused);
+    case id: return ptr_entry<T, TW, PEEL, op, path, tpr, v, teams, cs, cmin>(fused);
         RMSNORM_PLAN_TABLE(RMSN_FWD_PTR)
 #undef RMSN_FWD_PTR
     default:
@@ -1120,42 +1127,42 @@ static const void *ptr_t(int plan_id, bool fused) {
 // Staged forward plans (OP_FWD_STAGED): one entry per table row; kernels of
 // other ops are not instantiated, and a weight type other than the
 // activations' only for the default plans.
-template <typename T, typename TW, bool LN, int Q, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS,
-          int CMIN>
+template <typename T, typename TW, bool LN, int Q, bool PEEL, int OP, int PATH, int TPR, int V, int TEAMS, int D,
+          int CS, int CMIN>
 static const void *staged_fwd_ptr_entry(bool fused) {
     if constexpr (OP == OP_FWD_STAGED && PATH == PATH_STREAM) {
         // the streamed generic forward: RMSNorm, output in the activations' type
-        if constexpr (LN || Q != QOUT_NONE) {
+        if constexpr (LN || Q != QOUT_NONE || PEEL) {
             return nullptr;
         } else {
             return fused ? (const void *)rmsnorm_fwd_stream<T, TW, TPR, V, D, true>
                          : (const void *)rmsnorm_fwd_stream<T, TW, TPR, V, D, false>;
         }
     } else if constexpr (OP != OP_FWD_STAGED || PATH != PATH_RESTAGED || !staged_plan(PATH, TEAMS, CS) ||
-                         !instantiated<T, TW, PATH, CMIN, Q>() || (LN && Q != QOUT_NONE)) {
+                         !instantiated<T, TW, PATH, CMIN, Q, PEEL>() || (LN && Q != QOUT_NONE)) {
         return nullptr;
     } else if constexpr (LN) {
-        return fused ? (const void *)layernorm_fwd_staged<T, TW, TPR, V, D, CS, true>
-                     : (const void *)layernorm_fwd_staged<T, TW, TPR, V, D, CS, false>;
+        return fused ? (const void *)layernorm_fwd_staged<T, TW, TPR, V, D, CS, true, PEEL>
+                     : (const void *)layernorm_fwd_staged<T, TW, TPR, V, D, CS, false, PEEL>;
     } else {
-        return fused ? (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, true, Q>
-                     : (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, false, Q>;
+        return fused ? (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, true, Q, PEEL>
+                     : (const void *)rmsnorm_fwd_staged<T, TW, TPR, V, D, CS, false, Q, PEEL>;
     }
 }
 
-template <typename T, typename TW, bool LN, int Q, int OP, int PATH, int TPR, int V, int TEAMS, int D, int CS,
-          int CMIN>
+template <typename T, typename TW, bool LN, int Q, bool PEEL, int OP, int PATH, int TPR, int V, int TEAMS, int D,
+          int CS, int CMIN>
 static int staged_fwd_launch_entry(bool fused, const FwdParams &p, int grid, int smem, void *stream) {
-    const void *k = staged_fwd_ptr_entry<T, TW, LN, Q, OP, PATH, TPR, V, TEAMS, D, CS, CMIN>(fused);
+    const void *k = staged_fwd_ptr_entry<T, TW, LN, Q, PEEL, OP, PATH, TPR, V, TEAMS, D, CS, CMIN>(fused);
     if (!k) return (int)cudaErrorInvalidValue;
     return launch_fwd_staged_kernel(k, CS, TPR, p, grid, smem, stream);
 }
 
-template <typename T, typename TW, bool LN, int Q = QOUT_NONE>
+template <typename T, typename TW, bool LN, int Q = QOUT_NONE, bool PEEL = false>
 static const void *staged_fwd_ptr_t(int plan_id, bool fused) {
     switch (plan_id) {
 #define RMSN_SFWD_PTR(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return staged_fwd_ptr_entry<T, TW, LN, Q, op, path, tpr, v, teams, depth, cs, cmin>(fused);
+    case id: return staged_fwd_ptr_entry<T, TW, LN, Q, PEEL, op, path, tpr, v, teams, depth, cs, cmin>(fused);
         RMSNORM_PLAN_TABLE(RMSN_SFWD_PTR)
 #undef RMSN_SFWD_PTR
     default:
@@ -1163,13 +1170,13 @@ static const void *staged_fwd_ptr_t(int plan_id, bool fused) {
     }
 }
 
-template <typename T, typename TW, bool LN, int Q = QOUT_NONE>
+template <typename T, typename TW, bool LN, int Q = QOUT_NONE, bool PEEL = false>
 static int staged_fwd_launch_t(int plan_id, bool fused, const FwdParams &p, int grid, int smem, void *stream) {
     switch (plan_id) {
 #define RMSN_SFWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
     case id:                                                                    \
-        return staged_fwd_launch_entry<T, TW, LN, Q, op, path, tpr, v, teams, depth, cs, cmin>(fused, p, grid, smem, \
-                                                                                            stream);
+        return staged_fwd_launch_entry<T, TW, LN, Q, PEEL, op, path, tpr, v, teams, depth, cs, cmin>(fused, p, grid, \
+                                                                                                  smem, stream);
         RMSNORM_PLAN_TABLE(RMSN_SFWD_CASE)
 #undef RMSN_SFWD_CASE
     default:
@@ -1215,10 +1222,11 @@ static int launch_q(int plan_id, bool fused, int mode, const FwdParams &p, int g
 
 // LayerNorm forward: the forward plans' geometry, default plans and the
 // generic one.
-template <typename T, typename TW, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
+template <typename T, typename TW, bool PEEL, int OP, int PATH, int TPR, int V, int TEAMS, int CS, int CMIN>
 static int ln_launch_entry(bool fused, const FwdParams &p, int grid, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if constexpr (OP != OP_FWD || !(PATH == PATH_GENERIC || CMIN > 0)) {
+    if constexpr (OP != OP_FWD || !(PATH == PATH_GENERIC || CMIN > 0) ||
+                  (PEEL && !instantiated<T, TW, PATH, CMIN, QOUT_NONE, true>())) {
         return (int)cudaErrorInvalidValue;
     } else if constexpr (PATH == PATH_GENERIC) {
         LaunchCfg lc((unsigned)grid, 256, (size_t)gen_cache_bytes<T>(p), s);
@@ -1226,17 +1234,17 @@ static int ln_launch_entry(bool fused, const FwdParams &p, int grid, void *strea
                      : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_generic<T, TW, false>, p);
     } else {
         LaunchCfg lc((unsigned)grid, TPR * TEAMS, 0, s, CS > 1 ? CS : 0);
-        return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true>, p)
-                     : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false>, p);
+        return fused ? (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, true, PEEL>, p)
+                     : (int)cudaLaunchKernelEx(&lc.cfg, layernorm_fwd_vector<T, TW, TPR, V, TEAMS, CS, false, PEEL>, p);
     }
 }
 
 // (TW: gamma's and beta's type, the activations' or fp32)
-template <typename T, typename TW = T>
+template <typename T, typename TW = T, bool PEEL = false>
 static int ln_launch_t(int plan_id, bool fused, const FwdParams &p, int grid, void *stream) {
     switch (plan_id) {
 #define RMSN_LN_FWD_CASE(id, op, path, tpr, v, teams, depth, cs, dtm, cmin, cmax) \
-    case id: return ln_launch_entry<T, TW, op, path, tpr, v, teams, cs, cmin>(fused, p, grid, stream);
+    case id: return ln_launch_entry<T, TW, PEEL, op, path, tpr, v, teams, cs, cmin>(fused, p, grid, stream);
         RMSNORM_PLAN_TABLE(RMSN_LN_FWD_CASE)
 #undef RMSN_LN_FWD_CASE
     default:

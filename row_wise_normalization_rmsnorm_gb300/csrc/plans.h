@@ -309,6 +309,29 @@ RMSN_DECLARE_LAUNCHERS(bf16w32)
 RMSN_DECLARE_LAUNCHERS(f16w32)
 #undef RMSN_DECLARE_LAUNCHERS
 
+// Rows at a common offset (FwdParams / BwdParams peel > 0): the default
+// vectorised plans of RMSNorm and LayerNorm, forward and backward, compiled
+// with the row's wrapped chunk 0 (PEEL), for the types whose weight (gamma,
+// beta) is in the activations' type. The launchers above serve aligned rows.
+#define RMSN_DECLARE_PEEL(suf)                                                                                  \
+    int launch_fwd_peel_##suf(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);            \
+    int launch_fwd_staged_peel_##suf(int plan_id, bool fused, const FwdParams &p, int grid, int smem,           \
+                                     void *stream);                                                             \
+    const void *fwd_staged_kernel_ptr_peel_##suf(int plan_id, bool fused);                                     \
+    int launch_ln_fwd_peel_##suf(int plan_id, bool fused, const FwdParams &p, int grid, void *stream);         \
+    int launch_ln_fwd_staged_peel_##suf(int plan_id, bool fused, const FwdParams &p, int grid, int smem,        \
+                                        void *stream);                                                          \
+    const void *ln_fwd_staged_kernel_ptr_peel_##suf(int plan_id, bool fused);                                  \
+    int launch_bwd_main_peel_##suf(int plan_id, bool fused, bool packed, const BwdParams &p, int grid, int smem, \
+                                   void *stream);                                                               \
+    const void *bwd_main_kernel_ptr_peel_##suf(int plan_id, bool fused, bool packed);                           \
+    int launch_ln_bwd_peel_##suf(int plan_id, bool fused, const BwdParams &p, int grid, int smem, void *stream); \
+    const void *ln_bwd_kernel_ptr_peel_##suf(int plan_id, bool fused);
+RMSN_DECLARE_PEEL(f32)
+RMSN_DECLARE_PEEL(bf16)
+RMSN_DECLARE_PEEL(f16)
+#undef RMSN_DECLARE_PEEL
+
 // Forward with E4M3 output (mode QOUT_FP8_TENSOR or QOUT_FP8_ROW), for
 // fp32, bf16 and fp16 activations with the weight in the same type, and
 // for bf16 and fp16 activations with an fp32 weight ("w32"); on the

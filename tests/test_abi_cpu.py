@@ -360,6 +360,39 @@ def test_generic_note_is_optional_and_printed_once(rn, capfd):
     L.rmsnorm_set_generic_note(0)
 
 
+def test_common_offset_rows_refuse_forced_alternative_plans(rn):
+    """The kernels for rows at a common offset are compiled for the plans of
+    the default ranges only: forcing a plan the defaults select on such rows
+    is accepted, alternative (tuning) plans are refused, and the generic plan
+    still serves them."""
+    defaults = {rn.plan_query(op, 64, n, t)["plan_id"] for op in (rn.OP_FWD, rn.OP_BWD, rn.OP_LN_BWD)
+                for n in range(8, 65537, 8) for t in (0, 1, 2)}
+    refused = accepted = 0
+    for op in (rn.OP_FWD, rn.OP_BWD, rn.OP_LN_BWD):
+        for i in range(rn.lib().rmsnorm_plan_count()):
+            pid = rn.lib().rmsnorm_plan_id_at(i)
+            try:
+                a = rn.plan_query(op, 64, 2048, rn.RMSNORM_BF16, force_plan=pid)
+            except rn.RMSNormError:
+                continue
+            if a["path_name"] == "generic":
+                continue
+            if pid in defaults:
+                assert rn.plan_query(op, 64, 2048, rn.RMSNORM_BF16, aligned=2, force_plan=pid)["peel"] == 1
+                accepted += 1
+            else:
+                try:
+                    p = rn.plan_query(op, 64, 2048, rn.RMSNORM_BF16, aligned=2, force_plan=pid)
+                except rn.RMSNormError:
+                    refused += 1
+                    continue
+                # a plan of the default ranges that another one shadows (the
+                # register cluster forward beside the staged one)
+                assert p["peel"] == 1 and p["cluster_size"] > 1, p
+    assert refused > 0 and accepted > 0
+    assert rn.plan_query(rn.OP_BWD, 64, 2048, rn.RMSNORM_BF16, aligned=2, force_plan=36)["path_name"] == "generic"
+
+
 @pytest.mark.parametrize("dt,N,k", [(1, 7168, 1), (1, 8192, 7), (0, 2048, 3), (2, 128, 5), (1, 32768, 2)])
 def test_common_offset_plans_match_aligned_plans(rn, dt, N, k):
     """Rows at one common offset (every array k elements past a 16-byte
