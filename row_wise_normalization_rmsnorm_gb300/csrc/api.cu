@@ -543,11 +543,11 @@ static int launch_bwd_dt(int dt, int plan_id, bool fused, bool packed, const Bwd
 
 // dW is written in the weight's storage type.
 static int launch_finalize_dt(int dt, const float *ws, int parts, int ncols, void *out0, void *out1, int split,
-                              int peel, void *stream, bool serial) {
+                              int peel, void *stream, bool serial, int sms) {
     switch (kind_of(dt)) {
-    case 1: return launch_dw_finalize_bf16(ws, parts, ncols, out0, out1, split, peel, stream, serial);
-    case 2: return launch_dw_finalize_f16(ws, parts, ncols, out0, out1, split, peel, stream, serial);
-    default: return launch_dw_finalize_f32(ws, parts, ncols, out0, out1, split, peel, stream, serial);
+    case 1: return launch_dw_finalize_bf16(ws, parts, ncols, out0, out1, split, peel, stream, serial, sms);
+    case 2: return launch_dw_finalize_f16(ws, parts, ncols, out0, out1, split, peel, stream, serial, sms);
+    default: return launch_dw_finalize_f32(ws, parts, ncols, out0, out1, split, peel, stream, serial, sms);
     }
 }
 
@@ -1144,7 +1144,7 @@ static rmsnorm_status_t bwd_impl(const void *dy, const void *dres, const void *x
     if (le == 0 && event_after_main) le = (int)cudaEventRecord(static_cast<cudaEvent_t>(event_after_main), stream);
     if (le == 0 && affine)
         le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)N, dw, nullptr, (int)N, pl, stream,
-                                event_after_main != nullptr);
+                                event_after_main != nullptr, call.sms);
     if (owned) {
         cudaError_t fe = cudaFreeAsync(ws, stream);
         if (le == 0 && fe != cudaSuccess) le = (int)fe;
@@ -1374,7 +1374,8 @@ static rmsnorm_status_t ln_bwd_impl(const void *dy, const void *dres, const void
     // one finalizer over the [units, 2N] partial rows: dgamma | dbeta (a
     // NULL output's half is not written)
     if (le == 0 && want)
-        le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)(2 * N), dgamma, dbeta, (int)N, pl, stream, false);
+        le = launch_finalize_dt(dt, ws, plan.ws_rows, (int)(2 * N), dgamma, dbeta, (int)N, pl, stream, false,
+                                call.sms);
     if (owned) {
         cudaError_t fe = cudaFreeAsync(ws, stream);
         if (le == 0 && fe != cudaSuccess) le = (int)fe;

@@ -10,7 +10,7 @@ const void *bwd_main_kernel_ptr_bf16(int plan_id, bool fused, bool packed) {
     return bwd_ptr_t<__nv_bfloat16, __nv_bfloat16>(plan_id, fused, packed);
 }
 int launch_dw_finalize_bf16(const float *ws, int parts, int ncols, void *out0, void *out1, int split, int peel,
-                           void *stream, bool serial) {
-    return finalize_launch_t<__nv_bfloat16>(ws, parts, ncols, out0, out1, split, peel, stream, serial);
+                           void *stream, bool serial, int sms) {
+    return finalize_launch_t<__nv_bfloat16>(ws, parts, ncols, out0, out1, split, peel, stream, serial, sms);
 }
 }  // namespace rmsn

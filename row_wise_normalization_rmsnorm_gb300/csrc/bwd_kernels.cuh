@@ -1214,7 +1214,13 @@ __device__ __forceinline__ void store_param(T *out0, T *out1, int split, int pee
     if (out) store_elem(out, oc, v);
 }
 
-template <typename T, int LANES = 8, int RG = 32>
+// KB > 0: a group of at most KB partial rows issues all its loads before
+// its adds (one round trip to L2 instead of one a row), at the price of KB
+// float4 registers a thread (84 registers at KB = 16: three CTAs an SM);
+// KB = 0: one row at a time (32 registers: eight CTAs an SM). The host takes
+// the batched kernel where its grid fits one wave of it. Both add the rows
+// in the same order, so they give the same bits.
+template <typename T, int LANES = 8, int RG = 32, int KB = 16>
 __global__ void __launch_bounds__(LANES *RG) rmsnorm_dw_finalize4(const float *ws, int parts, int N, T *dw, T *dw1,
                                                                   int split, int peel) {
     constexpr int COLS = 4 * LANES;       // columns per CTA
@@ -1236,16 +1242,15 @@ __global__ void __launch_bounds__(LANES *RG) rmsnorm_dw_finalize4(const float *w
             s.z = __fadd_rn(s.z, v.z);
             s.w = __fadd_rn(s.w, v.w);
         };
-        // up to kBatch rows a group (P <= 32 * kBatch): every load in flight
-        // at once, one round trip to L2, then the adds in row order
-        constexpr int kBatch = 16;
-        if (p1 - p0 <= kBatch) {
-            float4 v[kBatch];
+        // up to KB rows a group (P <= RG * KB): every load in flight at
+        // once, one round trip to L2, then the adds in row order
+        if (KB > 0 && p1 - p0 <= KB) {
+            float4 v[KB > 0 ? KB : 1];
 #pragma unroll
-            for (int i = 0; i < kBatch; ++i)
+            for (int i = 0; i < KB; ++i)
                 if (p0 + i < p1) v[i] = src[(int64_t)(p0 + i) * stride];
 #pragma unroll
-            for (int i = 0; i < kBatch; ++i)
+            for (int i = 0; i < KB; ++i)
                 if (p0 + i < p1) add(v[i]);
         } else {
 #pragma unroll 4
@@ -1449,20 +1454,27 @@ static const void *bwd_ptr_t(int plan_id, bool fused, bool packed) {
 
 // The finalizer is launched as a programmatic dependent of the main kernel
 // (its launch overlaps the main kernel's tail) unless `serial` asks for a
-// plain launch (when the caller records an event between the two).
+// plain launch (when the caller records an event between the two). `sms`:
+// the device's SM count, which picks the batched vector finalizer where its
+// grid fits one wave (three of its CTAs an SM).
 template <typename T>
 static int finalize_launch_t(const float *ws, int parts, int N, void *dw, void *dw1, int split, int peel,
-                             void *stream, bool serial) {
+                             void *stream, bool serial, int sms) {
     constexpr int kLanes = 8, kGroups = 32;  // vector finalizer: 4 * kLanes columns a CTA
+    constexpr int kBatchPerSm = 3;           // resident CTAs an SM of the batched finalizer
     // float4 columns need every group of 4 on one side of the split
     const bool vec = N % 4 == 0 && split % 4 == 0;
+    const int vgrid = (N + 4 * kLanes - 1) / (4 * kLanes);
+    const bool batch = vgrid <= kBatchPerSm * sms;
     LaunchCfg lc(vec ? (unsigned)((N + 4 * kLanes - 1) / (4 * kLanes)) : (unsigned)((N + 31) / 32),
                  vec ? kLanes * kGroups : 256, 0, static_cast<cudaStream_t>(stream), 0, !serial);
     T *out = static_cast<T *>(dw);
     T *out1 = static_cast<T *>(dw1);
-    cudaError_t e = vec ? cudaLaunchKernelEx(&lc.cfg, rmsnorm_dw_finalize4<T, kLanes, kGroups>, ws, parts, N, out,
-                                             out1, split, peel)
-                        : cudaLaunchKernelEx(&lc.cfg, rmsnorm_dw_finalize<T>, ws, parts, N, out, out1, split, peel);
+    cudaError_t e = !vec    ? cudaLaunchKernelEx(&lc.cfg, rmsnorm_dw_finalize<T>, ws, parts, N, out, out1, split, peel)
+                    : batch ? cudaLaunchKernelEx(&lc.cfg, rmsnorm_dw_finalize4<T, kLanes, kGroups, 16>, ws, parts, N,
+                                                 out, out1, split, peel)
+                            : cudaLaunchKernelEx(&lc.cfg, rmsnorm_dw_finalize4<T, kLanes, kGroups, 0>, ws, parts, N,
+                                                 out, out1, split, peel);
     return (int)e;
 }
 

@@ -358,12 +358,13 @@ int allow_staged_smem(const void *kernel);
 // out1[c - split] (out1 may be NULL: those columns are not written).
 // Within each half (of split columns) the workspace column c holds
 // parameter column (c - peel) mod split (peel > 0: rows at a common offset).
+// sms: the device's SM count (it picks the finalizer's variant).
 int launch_dw_finalize_f32(const float *ws, int parts, int ncols, void *out0, void *out1, int split, int peel,
-                           void *stream, bool serial);
+                           void *stream, bool serial, int sms);
 int launch_dw_finalize_bf16(const float *ws, int parts, int ncols, void *out0, void *out1, int split, int peel,
-                            void *stream, bool serial);
+                            void *stream, bool serial, int sms);
 int launch_dw_finalize_f16(const float *ws, int parts, int ncols, void *out0, void *out1, int split, int peel,
-                           void *stream, bool serial);
+                           void *stream, bool serial, int sms);
 
 // LayerNorm forward and backward main kernels (gamma and beta in the
 // activations' type, or fp32 beside 16-bit activations: "w32"; the default
