@@ -703,15 +703,21 @@ __device__ __forceinline__ float cluster_allreduce(float v, float *red, int t, u
 }
 
 // ------------------------------------------------- two sums at once --
-// The same reductions on a pair of sums (the LayerNorm backward's sum of g
-// and sum of g (x - mean)); each component is combined exactly as the
-// single-value versions combine theirs.
+// The same reductions on a pair of values (the LayerNorm backward's sum of
+// g and sum of g (x - mean); the E4M3 forward's sum of squares and row
+// max), each component combined with its own op (PairOp) exactly as the
+// single-value versions combine theirs, so each component has their bits.
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y)); }
 __device__ __forceinline__ float2 shfl_xor2(float2 v, int o) {
     return make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
 }
+template <class OA = OpAdd, class OB = OpAdd>
+struct PairOp {
+    static __device__ __forceinline__ float2 f(float2 a, float2 b) { return make_float2(OA::f(a.x, b.x), OB::f(a.y, b.y)); }
+};
+using SumMax = PairOp<OpAdd, OpMax>;  // (sum of squares, max |value|)
 
-template <int S>
+template <int S, class PO = PairOp<>>
 __device__ __forceinline__ float2 sum_slots2(const float2 *red, int lane) {
     static_assert((S & (S - 1)) == 0, "slot count must be a power of two");
     float2 s;
@@ -720,38 +726,61 @@ __device__ __forceinline__ float2 sum_slots2(const float2 *red, int lane) {
     } else {
         s = red[lane];
 #pragma unroll
-        for (int j = 1; j < S / 32; ++j) s = add2(s, red[lane + 32 * j]);
+        for (int j = 1; j < S / 32; ++j) s = PO::f(s, red[lane + 32 * j]);
     }
     constexpr int WIDTH = S < 32 ? S : 32;
 #pragma unroll
-    for (int o = WIDTH / 2; o > 0; o >>= 1) s = add2(s, shfl_xor2(s, o));
+    for (int o = WIDTH / 2; o > 0; o >>= 1) s = PO::f(s, shfl_xor2(s, o));
     return s;
 }
 
-template <int TPR>
+template <int TPR, class PO = PairOp<>>
 __device__ __forceinline__ float2 team_allreduce2(float2 v, float2 *red, int t) {
     constexpr int WIDTH = TPR < 32 ? TPR : 32;
 #pragma unroll
-    for (int o = WIDTH / 2; o > 0; o >>= 1) v = add2(v, shfl_xor2(v, o));
+    for (int o = WIDTH / 2; o > 0; o >>= 1) v = PO::f(v, shfl_xor2(v, o));
     if constexpr (TPR > 32) {
         constexpr int W = TPR / 32;
         if ((t & 31) == 0) red[t >> 5] = v;
         __syncthreads();
-        v = sum_slots2<W>(red, t & 31);
+        v = sum_slots2<W, PO>(red, t & 31);
     }
     return v;
 }
 
+template <class PO = PairOp<>>
 __device__ __forceinline__ float2 cta_allreduce2(float2 v, float2 *red) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = add2(v, shfl_xor2(v, o));
+    for (int o = 16; o > 0; o >>= 1) v = PO::f(v, shfl_xor2(v, o));
     const int W = blockDim.x >> 5;
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
     float2 s = red[0];
-    for (int i = 1; i < W; ++i) s = add2(s, red[i]);
+    for (int i = 1; i < W; ++i) s = PO::f(s, red[i]);
     __syncthreads();  // red is reused by the next call
     return s;
+}
+
+// cluster_allreduce on a pair (8-byte distributed shared-memory stores).
+__device__ __forceinline__ void st_cluster2(float2 *local, uint32_t cta, float2 v) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(cta));
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(r), "f"(v.x), "f"(v.y) : "memory");
+}
+template <int TPR, int CS, class PO = PairOp<>>
+__device__ __forceinline__ float2 cluster_allreduce2(float2 v, float2 *red, int t, uint32_t rank) {
+    static_assert(TPR >= 32, "cluster rows need whole warps");
+    constexpr int W = TPR / 32;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = PO::f(v, shfl_xor2(v, o));
+    if ((t & 31) == 0) {
+#pragma unroll
+        for (int c = 0; c < CS; ++c) st_cluster2(&red[rank * W + (t >> 5)], (uint32_t)c, v);
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    return sum_slots2<CS * W, PO>(red, t & 31);
 }
 
 // st_async_cluster for a pair: 8 bytes counted on the receiver's barrier.

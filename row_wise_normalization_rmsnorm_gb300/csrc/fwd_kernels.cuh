@@ -207,7 +207,11 @@ __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR *
             }
         }
     } else {
-        // y in fp32, kept in registers until the scale is known
+        // y' = (h (offset + w)) rstd in fp32, kept in registers until the
+        // scale is known. Rounding a product with rstd > 0 is monotone, so
+        // the row's max |y'| is exactly rstd max_j |h_j (offset + w_j)|: the
+        // form every E4M3 kernel takes it in (here after the products, in
+        // the staged and generic kernels in their first pass)
         float2 yv[V][NP];
         float m = 0.f;
 #pragma unroll
@@ -223,18 +227,21 @@ __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR *
             }
 #pragma unroll
             for (int k = 0; k < NP; ++k) {
-                yv[v][k] = has_w ? Pk::mul(Pk::mul(yv[v][k], r2), Pk::add(o2, wv[k])) : Pk::mul(yv[v][k], r2);
-                m = fmaxf(m, fmaxf(fabsf(yv[v][k].x), fabsf(yv[v][k].y)));
+                const float2 hg = has_w ? Pk::mul(yv[v][k], Pk::add(o2, wv[k])) : yv[v][k];
+                m = fmaxf(m, fmaxf(fabsf(hg.x), fabsf(hg.y)));
+                yv[v][k] = Pk::mul(hg, r2);
             }
         }
-        float amax = 0.f;
+        float mrow = 0.f;
         if (Q == QOUT_FP8_ROW || p.qamax != nullptr) {  // uniform over the grid
             if constexpr (CS > 1) {
-                amax = cluster_allreduce<TPR, CS, OpMax>(m, &redm[0][0], t, rank);
+                mrow = cluster_allreduce<TPR, CS, OpMax>(m, &redm[0][0], t, rank);
             } else {
-                amax = team_allreduce<TPR, OpMax>(m, &redm[team][0], t);
+                mrow = team_allreduce<TPR, OpMax>(m, &redm[team][0], t);
             }
         }
+        // (fmaxf drops a NaN product: a zero row with eps = 0 reports 0)
+        const float amax = fmaxf(0.f, __fmul_rn(rstd, mrow));
         if (!valid) return;
         float sc;
         if constexpr (Q == QOUT_FP8_ROW) {
@@ -269,6 +276,7 @@ __global__ void __launch_bounds__(TPR *TEAMS, !fp8_out(Q) ? fwd_min_blocks<TPR *
 template <typename T, typename TW, bool FUSED, int Q = QOUT_NONE>
 __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     __shared__ float red[32];
+    __shared__ float2 red2[fp8_out(Q) ? 32 : 1];  // E4M3: (sum of squares, max) slots
     pdl_wait();
     pdl_trigger();
     constexpr int NP = Elem<T>::NP;
@@ -290,6 +298,11 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     const RowSplit sp = row_split(x, N, Q == QOUT_NONE);  // (other outputs: element by element)
 
     float ss = 0.f;
+    // E4M3: max |h (offset + w)|, whose product with rstd is the row's max |y|
+    float m = 0.f;
+    auto hg_max = [&](float h, int j) {
+        if constexpr (fp8_out(Q)) m = fmaxf(m, fabsf(w ? __fmul_rn(h, __fadd_rn(p.offset, load_w(w, j))) : h));
+    };
     auto h_elem = [&](int j) {
         float h = load_elem(x, j);
         if constexpr (FUSED) {
@@ -301,6 +314,7 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
     for (int j = threadIdx.x; j < sp.head; j += blockDim.x) {
         const float h = h_elem(j);
         ss = __fmaf_rn(h, h, ss);
+        hg_max(h, j);
     }
     for (int c = threadIdx.x; c < sp.nb; c += blockDim.x) {
         const int64_t j0 = sp.head + (int64_t)c * Elem<T>::E;
@@ -319,19 +333,41 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
             ss = __fmaf_rn(h[q].x, h[q].x, ss);
             ss = __fmaf_rn(h[q].y, h[q].y, ss);
         }
+        if constexpr (fp8_out(Q)) {
+            float2 g[NP];
+            if (w) w_chunk_at<T, TW>(w, (int)j0, g);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const float gx = w ? __fmul_rn(h[q].x, __fadd_rn(p.offset, g[q].x)) : h[q].x;
+                const float gy = w ? __fmul_rn(h[q].y, __fadd_rn(p.offset, g[q].y)) : h[q].y;
+                m = fmaxf(m, fmaxf(fabsf(gx), fabsf(gy)));
+            }
+        }
     }
     for (int j = sp.tail0 + threadIdx.x; j < N; j += blockDim.x) {
         const float h = h_elem(j);
         ss = __fmaf_rn(h, h, ss);
+        hg_max(h, j);
     }
-    const float s = cta_allreduce(ss, red);
+    float s, mrow = 0.f;
+    if constexpr (fp8_out(Q)) {
+        const float2 r = cta_allreduce2<SumMax>(make_float2(ss, m), red2);
+        s = r.x;
+        mrow = r.y;
+    } else {
+        s = cta_allreduce(ss, red);
+    }
     const float rstd = rsqrtf(__fadd_rn(__fdiv_rn(s, (float)N), p.eps));
     if (threadIdx.x == 0) p.rstd[row] = rstd;
     // The same thread wrote hout[j] above, so it reads its own value.
     auto y_at = [&](int j) {
         const float h = FUSED ? load_elem(static_cast<const T *>(hout), j) : load_elem(x, j);
-        const float hr = __fmul_rn(h, rstd);
-        return w ? __fmul_rn(hr, __fadd_rn(p.offset, load_w(w, j))) : hr;
+        if constexpr (fp8_out(Q)) {  // E4M3: y' = (h (offset + w)) rstd, whose max is rstd max |h (offset + w)|
+            return __fmul_rn(w ? __fmul_rn(h, __fadd_rn(p.offset, load_w(w, j))) : h, rstd);
+        } else {
+            const float hr = __fmul_rn(h, rstd);
+            return w ? __fmul_rn(hr, __fadd_rn(p.offset, load_w(w, j))) : hr;
+        }
     };
     if constexpr (narrow_out(Q)) {
         using TO = typename std::conditional<Q == QOUT_BF16, __nv_bfloat16, __half>::type;
@@ -358,12 +394,8 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
         }
         for (int j = sp.tail0 + threadIdx.x; j < N; j += blockDim.x) store_elem(y, j, y_at(j));
     } else {
-        float amax = 0.f;
-        if (Q == QOUT_FP8_ROW || p.qamax != nullptr) {
-            float m = 0.f;
-            for (int j = threadIdx.x; j < N; j += blockDim.x) m = fmaxf(m, fabsf(y_at(j)));
-            amax = cta_allreduce<OpMax>(m, red);
-        }
+        // (fmaxf drops a NaN product: a zero row with eps = 0 reports 0)
+        const float amax = fmaxf(0.f, __fmul_rn(rstd, mrow));
         float sc;
         if constexpr (Q == QOUT_FP8_ROW) {
             sc = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
@@ -614,6 +646,10 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     __shared__ float red[2][CS * W];
     __shared__ __align__(8) uint64_t full[S];
     __shared__ __align__(8) uint64_t rbar[2];  // cluster rows: arrival of the peers' sums
+    // E4M3: one reduction a row of (sum of squares, max), its own slots and barriers
+    constexpr bool PAIR = fp8_out(Q);
+    __shared__ float2 red2[PAIR ? 2 : 1][PAIR ? CS * W : 1];
+    __shared__ __align__(8) uint64_t rbar2[PAIR ? 2 : 1];
     __shared__ unsigned done[S];               // warps through the stage's row
     extern __shared__ float4 fstage_smem[];    // ns * NB * Cb chunks of 16 bytes
     pdl_wait();  // before any read of the rows (the bulk copies included)
@@ -663,6 +699,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
         if constexpr (FUSED) copy(dst + Cb, r4);
     };
     constexpr uint32_t kSlotBytes = CS * W * sizeof(float);
+    constexpr uint32_t kSlotBytes2 = CS * W * sizeof(float2);
     if (t == 0) {
 #pragma unroll
         for (int s = 0; s < S; ++s) {
@@ -674,6 +711,12 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
             mbar_init(&rbar[1], 1);
             mbar_arrive_expect_tx(&rbar[0], kSlotBytes);
             mbar_arrive_expect_tx(&rbar[1], kSlotBytes);
+            if constexpr (PAIR) {
+                mbar_init(&rbar2[0], 1);
+                mbar_init(&rbar2[1], 1);
+                mbar_arrive_expect_tx(&rbar2[0], kSlotBytes2);
+                mbar_arrive_expect_tx(&rbar2[1], kSlotBytes2);
+            }
         }
         mbar_init_fence();
         for (int s = 0; s < ns && s < iters; ++s) issue(s, s);
@@ -712,6 +755,31 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
         return sum;
     };
     auto rowsum = [&](float v) { return rowred(OpAdd{}, v); };
+    // the E4M3 row's (sum of squares, max) in one reduction, with the same
+    // buffer and barrier rules on its own slots (q2: its reduction count)
+    uint32_t q2 = 0;
+    auto rowred2 = [&](float2 v) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = SumMax::f(v, shfl_xor2(v, o));
+        const int b = (int)(q2 & 1);
+        float2 r;
+        if constexpr (CS > 1) {
+            if (lane == 0) {
+#pragma unroll
+                for (int c = 0; c < CS; ++c)
+                    st_async_cluster2(&red2[b][rank * W + (t >> 5)], &rbar2[b], (uint32_t)c, v);
+            }
+            if (!mbar_wait(&rbar2[b], (q2 >> 1) & 1u, kWaitLimit)) failed = true;
+            r = sum_slots2<CS * W, SumMax>(&red2[b][0], lane);
+            if (t == 0) mbar_arrive_expect_tx(&rbar2[b], kSlotBytes2);
+        } else {
+            if (lane == 0) red2[b][t >> 5] = v;
+            __syncthreads();
+            r = sum_slots2<W, SumMax>(&red2[b][0], lane);
+        }
+        ++q2;
+        return r;
+    };
 
     const float2 o2 = make_float2(p.offset, p.offset);
     int s = 0;
@@ -746,15 +814,34 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
             }
         };
         float2 acc = make_float2(0.f, 0.f);
+        float mh = 0.f;  // E4M3: max |h (offset + w)| of this thread's elements
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             float2 h[NP];
             hchunk(v, h, true);
 #pragma unroll
             for (int j = 0; j < NP; ++j) acc = LN ? Pk::add(acc, h[j]) : Pk::fma(h[j], h[j], acc);
+            if constexpr (PAIR) {
+                const int cl = v * TPR + t;
+                float2 g[NP];
+                if (p.w && cl < Cs) {
+                    load_w_chunk_row<T, TW>(p.w, cbase + cl, C, peel, v == 0 && e0, g);
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) g[j] = Pk::mul(h[j], Pk::add(o2, g[j]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < NP; ++j) g[j] = h[j];  // factor 1 (zero past the slice)
+                }
+#pragma unroll
+                for (int j = 0; j < NP; ++j) mh = fmaxf(mh, fmaxf(fabsf(g[j].x), fabsf(g[j].y)));
+            }
         }
-        float rstd, mu = 0.f;
-        if constexpr (LN) {
+        float rstd, mu = 0.f, mrow = 0.f;
+        if constexpr (PAIR) {
+            const float2 r = rowred2(make_float2(__fadd_rn(acc.x, acc.y), mh));
+            rstd = rsqrtf(__fadd_rn(__fdiv_rn(r.x, (float)N), p.eps));
+            mrow = r.y;
+        } else if constexpr (LN) {
             mu = __fdiv_rn(rowsum(__fadd_rn(acc.x, acc.y)), (float)N);
             const float2 nmu2 = make_float2(-mu, -mu);
             float2 sq = make_float2(0.f, 0.f);
@@ -806,7 +893,9 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                 float2 wv[NP];
                 load_w_chunk_row<T, TW>(p.w, c, C, peel, v == 0 && e0, wv);
 #pragma unroll
-                for (int j = 0; j < NP; ++j) a[j] = Pk::mul(Pk::mul(a[j], r2), Pk::add(o2, wv[j]));
+                for (int j = 0; j < NP; ++j)  // (E4M3: y' = (h (offset + w)) rstd, as the first pass's max)
+                    a[j] = PAIR ? Pk::mul(Pk::mul(a[j], Pk::add(o2, wv[j])), r2)
+                                : Pk::mul(Pk::mul(a[j], r2), Pk::add(o2, wv[j]));
             } else {
 #pragma unroll
                 for (int j = 0; j < NP; ++j) a[j] = Pk::mul(a[j], r2);
@@ -827,22 +916,9 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
                 }
             }
         } else {
-            // E4M3: the row's max |y| (per-row scale, or the reported amax)
-            // from one pass over the stage, then the codes from another
-            float amax = 0.f;
-            if (Q == QOUT_FP8_ROW || p.qamax != nullptr) {  // uniform over the grid
-                float m = 0.f;
-#pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    if (v * TPR + t < Cs) {
-                        float2 a[NP];
-                        ychunk(v, a);
-#pragma unroll
-                        for (int j = 0; j < NP; ++j) m = fmaxf(m, fmaxf(fabsf(a[j].x), fabsf(a[j].y)));
-                    }
-                }
-                amax = rowred(OpMax{}, m);
-            }
+            // E4M3: the row's max |y| = rstd max |h (offset + w)| from the
+            // first pass's reduction, then the codes from one more pass
+            const float amax = fmaxf(0.f, __fmul_rn(rstd, mrow));
             float sc;
             if constexpr (Q == QOUT_FP8_ROW) {
                 sc = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
