@@ -170,3 +170,29 @@ def test_fp8_codes_match_plain_forward_dequantised(rn):
     y = y16.float().cpu().numpy().astype(np.float64)
     amax = np.abs(y).max(axis=1, keepdims=True)
     assert np.all(np.abs(deq - y) <= 2.0 ** -4 * np.abs(y) + 2.0 ** -9 * amax / 448.0 + 2.0 ** -8 * np.abs(y))
+
+
+@pytest.mark.parametrize("N,offs,path", [(4096, 0, "vector"), (32768, 0, "staged"), (4100, 1, "generic")])
+@pytest.mark.parametrize("offset", [0.0, 1.0])
+def test_fp8_row_scale_is_the_max_of_y_to_the_bit(rn, N, offs, path, offset):
+    """Every E4M3 kernel forms y' = (h (offset + w)) rstd in fp32 and takes
+    the row's max |y'| as rstd max_j |h_j (offset + w_j)|, which is the same
+    number because rounding a product with rstd > 0 is monotone. So the
+    reported 1/s is max_j |y'_j| / 448 with y' recomputed here in fp32 from
+    the kernel's own rstd (numpy's float32 products round as the GPU's do),
+    bit for bit: on the register path, the staged cluster path (whose max
+    rides on the first pass's reduction) and the generic path."""
+    M = 48
+    d = inputs.make_inputs(M, N, "bf16", 177 + N % 13)
+    x = to_dev(d["x"], "bf16", offset=offs)
+    w = to_dev(d["w"], "bf16", offset=offs)
+    out = rn.rmsnorm_fwd_fp8(x, w, scaling="row", offset=offset)
+    torch.cuda.synchronize()
+    assert out["plan"]["path_name"] == path, out["plan"]
+    h = x.float().cpu().numpy()
+    g = np.float32(offset) + w.float().cpu().numpy()
+    rstd = out["rstd"].cpu().numpy()
+    y = (h * g[None, :]).astype(np.float32) * rstd[:, None]
+    amax = np.abs(y).max(axis=1)
+    want = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    assert y.dtype == np.float32 and np.array_equal(out["scale_inv"].cpu().numpy(), want)
