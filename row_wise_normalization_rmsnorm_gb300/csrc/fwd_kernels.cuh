@@ -415,8 +415,9 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const FwdParams p) {
 // sum of squared deviations from it (a two-pass variance, which loses
 // nothing to cancellation when the mean is large), then
 // y = (h - mean) rstd (offset + gamma) + beta, rounded once.
+// (held to the register forward's budget, as the RMSNorm one)
 template <typename T, typename TW, int TPR, int V, int TEAMS, int CS, bool FUSED, bool PEEL = false>
-__global__ void __launch_bounds__(TPR *TEAMS)
+__global__ void __launch_bounds__(TPR *TEAMS, fwd_min_blocks<TPR * TEAMS>())
     layernorm_fwd_vector(const FwdParams p) {
     static_assert(CS == 1 || TEAMS == 1, "a cluster row uses one team per CTA");
     using Pk = Pair<true>;
