@@ -629,8 +629,9 @@ __global__ void __launch_bounds__(256) layernorm_fwd_generic(const FwdParams p) 
 // residual) slice streams by cp.async.bulk into one of the stages, counted
 // in bytes on the stage's mbarrier. Pass 1 forms h (fused: R(x + r), stored
 // to residual_out) and the row sum of squares (LayerNorm: the sum, then in
-// a pass of its own the squared deviations); pass 2 reads the stage again
-// and writes y. The last warp through a stage refills it, as in the
+// a pass of its own the squared deviations; E4M3: beside the sum of squares
+// the max of |h (offset + w)|, the pair meeting in one reduction); pass 2
+// reads the stage again and writes y. The last warp through a stage refills it, as in the
 // backward's re-read schedule. A thread's chunks, their order and the
 // reduction tree are the register forward's, so y and rstd are the same
 // bits. Every wait is bounded; one that gives up writes the status word and
@@ -732,7 +733,7 @@ __device__ __forceinline__ void staged_fwd_body(const FwdParams &p) {
     // after reading; a buffer is written again (q + 2) only after every warp
     // sent its q + 1 sum, which it does after reading the buffer for q.
     uint32_t q = 0;
-    // combines with Op (OpAdd: a row sum; OpMax: the E4M3 row max)
+    // combines with Op (OpAdd: a row sum)
     auto rowred = [&](auto op, float v) {
         using Op = decltype(op);
 #pragma unroll
